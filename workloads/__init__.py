@@ -1,0 +1,396 @@
+"""Seeded synthetic workloads for the Kamera relocate + patch + scatter operator.
+
+This module only draws inputs: canonical K/V stores, patch factors, chunk
+lengths, phase shifts, page permutations and canary-filled pools.  It holds
+none of the operator's arithmetic, and both sides use it: the CUDA path (the
+tensors go to the GPU through the C-ABI binding) and the fp64 oracle (the same
+tensors, copied to host memory).
+
+The shapes follow the workloads named for the method ("Kamera: Unified
+Position-Invariant Multimodal KV Cache for Training-Free Reuse"): Qwen2.5-VL-7B
+shaped GQA caches with image-sized chunks, a DeepSeek-V2-Lite shaped MLA cache,
+sliding-window survival and an MHA reorder + recall batch.  The pages' own
+benchmarks (MM-NIAH, MileBench, two-page doc-QA) measure accuracy with trained
+weights; these synthetic inputs stand in for them as shapes only.
+
+Recipe (the pages give none; readings):
+  * K/V ~ N(0, 1) drawn in fp32, rounded to bf16; config "qwen_recall" scales
+    each (layer, head, dim) channel by exp(U(ln 0.1, ln 10)), K and V independently.
+  * patch factors U, V_m ~ N(0, 0.05^2) (std 0.05), bf16.
+  * pools are paged (P tokens per page); a chunk's tokens fill pages in order and
+    the pages are a random permutation of the pool's pages; unused slots hold a
+    canary bit pattern.
+  * tensors are drawn with torch.Generator seeded from (SEED, workload, tensor);
+    lengths, deltas and page permutations with numpy PCG64 SeedSequence([SEED, ...]).
+"""
+from __future__ import annotations
+
+import math
+import zlib
+from dataclasses import dataclass, field
+from typing import List, Optional, Sequence
+
+import numpy as np
+import torch
+
+SEED = 20260623
+CANARY_BITS = 0x5A5A  # bf16 pattern left in slots that no chunk targets
+
+ROTATE_HALF = 0
+INTERLEAVED = 1
+
+
+# ---------------------------------------------------------------- specs ----
+@dataclass(frozen=True)
+class GqaSpec:
+    """GQA/MHA relocate + patch (kind 'gqa') or rotate-only slide (kind 'slide')."""
+    name: str
+    kind: str                      # "gqa" | "slide"
+    L: int
+    H: int
+    d: int
+    base: float
+    lens: Sequence[int]
+    deltas: Sequence[int]
+    m: int
+    page: int
+    pairing: int = ROTATE_HALF
+    rot_dim: Optional[int] = None  # default: whole head (d)
+    rot_offset: int = 0
+    channel_scale: bool = False
+    pool_pages: Optional[int] = None
+    window: int = 0                # slide: tokens held in the window (pool)
+    evicted: int = 0               # slide: oldest tokens evicted
+
+
+@dataclass(frozen=True)
+class MlaSpec:
+    name: str
+    L: int
+    kv_lora: int
+    rope: int
+    base: float
+    lens: Sequence[int]
+    deltas: Sequence[int]
+    m: int
+    page: int
+    pairing: int = INTERLEAVED
+    pool_pages: Optional[int] = None
+
+    kind: str = "mla"
+
+
+def _np_rng(*tags) -> np.random.Generator:
+    key = [SEED] + [zlib.crc32(str(t).encode()) for t in tags]
+    return np.random.Generator(np.random.PCG64(np.random.SeedSequence(key)))
+
+
+def _torch_seed(*tags) -> int:
+    return int(_np_rng("torch", *tags).integers(0, 2**62))
+
+
+# ------------------------------------------------------------ the configs --
+def tiny_gqa() -> GqaSpec:
+    """1 layer, 2 KV heads, d=64, one 128-token chunk, delta=+37, rank 4, base 1e4, P=16."""
+    return GqaSpec("tiny_gqa", "gqa", L=1, H=2, d=64, base=1e4, lens=(128,), deltas=(37,),
+                   m=4, page=16, pool_pages=16)
+
+
+def qwen_recall() -> GqaSpec:
+    """Qwen2.5-VL-7B shaped recall batch: 28 L, 4 KV heads, d=128, base 1e6,
+    8 chunks of 1296 tokens, delta ~ U{-32768..32768}, rank 32, P=16."""
+    r = _np_rng("qwen_recall", "delta")
+    deltas = tuple(int(x) for x in r.integers(-32768, 32769, size=8))
+    return GqaSpec("qwen_recall", "gqa", L=28, H=4, d=128, base=1e6, lens=(1296,) * 8,
+                   deltas=deltas, m=32, page=16, channel_scale=True)
+
+
+def dsv2_mla() -> MlaSpec:
+    """DeepSeek-V2-Lite shaped MLA: 27 L, c_KV 512 + k_rope 64, base 1e4 on k_rope,
+    16 chunks of 4096 tokens, delta ~ U{-16384..16384}, rank 16 on both channels, P=64."""
+    r = _np_rng("dsv2_mla", "delta")
+    deltas = tuple(int(x) for x in r.integers(-16384, 16385, size=16))
+    return MlaSpec("dsv2_mla", L=27, kv_lora=512, rope=64, base=1e4, lens=(4096,) * 16,
+                   deltas=deltas, m=16, page=64)
+
+
+def qwen_slide() -> GqaSpec:
+    """Sliding-window survival: 131072-token window of a Qwen2.5-VL-7B shaped cache;
+    the oldest 32768 are evicted and the 98304 survivors (75 x 1296 + 1104) turn by -32768."""
+    survivors = 131072 - 32768
+    lens = [1296] * (survivors // 1296)
+    if survivors % 1296:
+        lens.append(survivors % 1296)
+    return GqaSpec("qwen_slide", "slide", L=28, H=4, d=128, base=1e6, lens=tuple(lens),
+                   deltas=(-32768,) * len(lens), m=0, page=16, window=131072, evicted=32768)
+
+
+def mha_reorder_recall() -> GqaSpec:
+    """MHA reorder + recall: 32 L, 32 heads, d=128, base 1e4, 64 chunks of U{256..2048}
+    tokens permuted (delta = new start - old start) plus 8 recall chunks placed after them
+    (canonical at position 0, delta = target start), rank 64 on K and V, P=16."""
+    r = _np_rng("mha_reorder_recall", "lens")
+    lens = [int(x) for x in r.integers(256, 2049, size=64)]
+    rec = [int(x) for x in r.integers(256, 2049, size=8)]
+    starts = np.concatenate([[0], np.cumsum(lens)[:-1]])
+    perm = _np_rng("mha_reorder_recall", "perm").permutation(64)
+    new_starts = np.empty(64, dtype=np.int64)
+    pos = 0
+    for c in perm:                       # chunk c now sits at position pos
+        new_starts[c] = pos
+        pos += lens[c]
+    deltas = [int(new_starts[c] - starts[c]) for c in range(64)]
+    for t in rec:                        # recalled chunks follow the reordered set
+        deltas.append(int(pos))
+        pos += t
+    return GqaSpec("mha_reorder_recall", "gqa", L=32, H=32, d=128, base=1e4,
+                   lens=tuple(lens + rec), deltas=tuple(deltas), m=64, page=16)
+
+
+def tiny_gqa_x(n: int = 4096) -> GqaSpec:
+    """The tiny GQA chunk replicated n times in one call (n chunks of 128 tokens)."""
+    r = _np_rng("tiny_gqa_x", n)
+    deltas = tuple(int(x) for x in r.integers(-32768, 32769, size=n))
+    return GqaSpec(f"tiny_gqa_x{n}", "gqa", L=1, H=2, d=64, base=1e4, lens=(128,) * n,
+                   deltas=deltas, m=4, page=16, pool_pages=2 * 8 * n)
+
+
+CONFIGS = {
+    "tiny_gqa": tiny_gqa,
+    "qwen_recall": qwen_recall,
+    "dsv2_mla": dsv2_mla,
+    "qwen_slide": qwen_slide,
+    "mha_reorder_recall": mha_reorder_recall,
+}
+
+
+def scaled(spec, L: Optional[int] = None, lens: Optional[Sequence[int]] = None,
+           H: Optional[int] = None, m: Optional[int] = None, name: Optional[str] = None):
+    """A smaller copy of a spec (fewer layers / tokens / heads) with the same structure."""
+    kw = dict(spec.__dict__)
+    if L is not None:
+        kw["L"] = L
+    if H is not None:
+        kw["H"] = H
+    if m is not None:
+        kw["m"] = m
+    if lens is not None:
+        n = len(lens)
+        kw["lens"] = tuple(lens)
+        kw["deltas"] = tuple(spec.deltas[i % len(spec.deltas)] for i in range(n))
+        kw["pool_pages"] = None
+        if spec.kind == "slide":
+            kw["evicted"] = sum(lens) // 3
+            kw["window"] = sum(lens) + kw["evicted"]
+    kw["name"] = name or (spec.name + "_small")
+    return type(spec)(**kw)
+
+
+# ------------------------------------------------------------- workloads --
+@dataclass
+class ChunkData:
+    src_offset: int
+    length: int
+    delta: int
+    rank: int
+    slots: torch.Tensor                       # int64 [length]
+    patches: List[torch.Tensor] = field(default_factory=list)   # 4 bf16 tensors or empty
+
+
+@dataclass
+class Workload:
+    spec: object
+    kind: str
+    chunks: List[ChunkData]
+    store_k: Optional[torch.Tensor] = None    # gqa: [L, N, H, d]; mla: store [L, N, W]
+    store_v: Optional[torch.Tensor] = None
+    pool_k: Optional[torch.Tensor] = None     # gqa/slide: [L, S, H, d]; mla: pool [L, S, W]
+    pool_v: Optional[torch.Tensor] = None
+    rot_dim: int = 0
+    rot_offset: int = 0
+    pairing: int = ROTATE_HALF
+    base: float = 1e4
+    kv_lora: int = 0
+
+    @property
+    def tokens(self) -> int:
+        return sum(c.length for c in self.chunks)
+
+    @property
+    def max_len(self) -> int:
+        return max((c.length for c in self.chunks), default=0)
+
+    @property
+    def num_slots(self) -> int:
+        return self.pool_k.shape[1]
+
+
+def _randn_bf16(shape, std, gen, device, scale=None) -> torch.Tensor:
+    """bf16 tensor of N(0, std^2) draws, generated one leading slice at a time."""
+    out = torch.empty(shape, dtype=torch.bfloat16, device=device)
+    for i in range(shape[0]):
+        x = torch.randn(shape[1:], generator=gen, device=device, dtype=torch.float32)
+        if scale is not None:
+            x.mul_(scale[i])
+        if std != 1.0:
+            x.mul_(std)
+        out[i].copy_(x)
+    return out
+
+
+def _canary(shape, device) -> torch.Tensor:
+    t = torch.empty(shape, dtype=torch.int16, device=device)
+    t.fill_(CANARY_BITS if CANARY_BITS < 0x8000 else CANARY_BITS - 0x10000)
+    return t.view(torch.bfloat16)
+
+
+def _page_slots(name: str, lens: Sequence[int], page: int, pool_pages: Optional[int],
+                first_page_gap: int = 0):
+    """Slots for chunks laid end to end over randomly permuted pages.
+
+    Chunk tokens occupy consecutive positions of one logical sequence; position p
+    lives in slot perm[p // page] * page + p % page.  Returns (per-chunk slots,
+    number of pool pages).
+    """
+    total = sum(lens) + first_page_gap
+    need = -(-total // page)
+    if pool_pages is None:
+        pool_pages = need + max(1, need // 8)
+    if pool_pages < need:
+        raise ValueError("pool too small")
+    perm = _np_rng(name, "pages").permutation(pool_pages)[:need].astype(np.int64)
+    out = []
+    pos = first_page_gap
+    for t in lens:
+        p = np.arange(pos, pos + t, dtype=np.int64)
+        out.append(perm[p // page] * page + p % page)
+        pos += t
+    return out, pool_pages
+
+
+def make(spec, device="cpu", with_patches: bool = True) -> Workload:
+    """Materialise a spec on ``device`` (seeded; the same spec gives the same draws
+    on the same device type)."""
+    device = torch.device(device)
+    if isinstance(spec, MlaSpec):
+        return _make_mla(spec, device)
+    if spec.kind == "slide":
+        return _make_slide(spec, device)
+    return _make_gqa(spec, device, with_patches)
+
+
+def _gen(device, *tags) -> torch.Generator:
+    g = torch.Generator(device=device)
+    g.manual_seed(_torch_seed(*tags))
+    return g
+
+
+def _make_gqa(spec: GqaSpec, device, with_patches: bool) -> Workload:
+    L, H, d, m = spec.L, spec.H, spec.d, spec.m
+    N = sum(spec.lens)
+    scale_k = scale_v = None
+    if spec.channel_scale:
+        gs = _gen(device, spec.name, "scale")
+        lo, hi = math.log(0.1), math.log(10.0)
+        scale_k = torch.exp(torch.rand((L, 1, H, d), generator=gs, device=device) * (hi - lo) + lo)
+        scale_v = torch.exp(torch.rand((L, 1, H, d), generator=gs, device=device) * (hi - lo) + lo)
+        scale_k = scale_k[:, 0]
+        scale_v = scale_v[:, 0]
+    store_k = _randn_bf16((L, N, H, d), 1.0, _gen(device, spec.name, "store_k"), device, scale_k)
+    store_v = _randn_bf16((L, N, H, d), 1.0, _gen(device, spec.name, "store_v"), device, scale_v)
+    slots, pages = _page_slots(spec.name, spec.lens, spec.page, spec.pool_pages)
+    S = pages * spec.page
+    pool_k = _canary((L, S, H, d), device)
+    pool_v = _canary((L, S, H, d), device)
+    chunks = []
+    gp = _gen(device, spec.name, "patch")
+    off = 0
+    for c, t in enumerate(spec.lens):
+        patches = []
+        if m > 0 and with_patches:
+            patches = [
+                _randn_bf16((L, H, t, m), 0.05, gp, device),
+                _randn_bf16((L, H, d, m), 0.05, gp, device),
+                _randn_bf16((L, H, t, m), 0.05, gp, device),
+                _randn_bf16((L, H, d, m), 0.05, gp, device),
+            ]
+        chunks.append(ChunkData(off, t, int(spec.deltas[c]), m if with_patches else 0,
+                                torch.from_numpy(slots[c]).to(device), patches))
+        off += t
+    return Workload(spec, "gqa", chunks, store_k, store_v, pool_k, pool_v,
+                    rot_dim=spec.rot_dim or d, rot_offset=spec.rot_offset,
+                    pairing=spec.pairing, base=spec.base)
+
+
+def _make_slide(spec: GqaSpec, device) -> Workload:
+    L, H, d = spec.L, spec.H, spec.d
+    window = spec.window or (sum(spec.lens) + spec.evicted)
+    if window != spec.evicted + sum(spec.lens):
+        raise ValueError("window must equal evicted + survivors")
+    # the whole window sits in the pool; the survivors are its last tokens
+    win_slots, pages = _page_slots(spec.name, [window], spec.page,
+                                   spec.pool_pages or -(-window // spec.page))
+    S = pages * spec.page
+    pool_k = _randn_bf16((L, S, H, d), 1.0, _gen(device, spec.name, "pool_k"), device)
+    ws = win_slots[0]
+    chunks = []
+    pos = spec.evicted
+    for c, t in enumerate(spec.lens):
+        chunks.append(ChunkData(0, t, int(spec.deltas[c]), 0,
+                                torch.from_numpy(ws[pos:pos + t].copy()).to(device), []))
+        pos += t
+    return Workload(spec, "slide", chunks, pool_k=pool_k, rot_dim=spec.rot_dim or d,
+                    rot_offset=spec.rot_offset, pairing=spec.pairing, base=spec.base)
+
+
+def _make_mla(spec: MlaSpec, device) -> Workload:
+    L, W, m = spec.L, spec.kv_lora + spec.rope, spec.m
+    N = sum(spec.lens)
+    store = _randn_bf16((L, N, W), 1.0, _gen(device, spec.name, "store"), device)
+    slots, pages = _page_slots(spec.name, spec.lens, spec.page, spec.pool_pages)
+    S = pages * spec.page
+    pool = _canary((L, S, W), device)
+    gp = _gen(device, spec.name, "patch")
+    chunks = []
+    off = 0
+    for c, t in enumerate(spec.lens):
+        patches = []
+        if m > 0:
+            patches = [
+                _randn_bf16((L, t, m), 0.05, gp, device),
+                _randn_bf16((L, spec.kv_lora, m), 0.05, gp, device),
+                _randn_bf16((L, t, m), 0.05, gp, device),
+                _randn_bf16((L, spec.rope, m), 0.05, gp, device),
+            ]
+        chunks.append(ChunkData(off, t, int(spec.deltas[c]), m,
+                                torch.from_numpy(slots[c]).to(device), patches))
+        off += t
+    return Workload(spec, "mla", chunks, store_k=store, pool_k=pool, rot_dim=spec.rope,
+                    rot_offset=spec.kv_lora, pairing=spec.pairing, base=spec.base,
+                    kv_lora=spec.kv_lora)
+
+
+# ------------------------------------------------------------- accounting --
+def algorithmic_bytes(spec) -> int:
+    """Bytes the operator must move at minimum: canonical rows read, patch factors
+    read (U: len x m and V_m: width x m per factor), rows written, int64 slot map."""
+    B = 2
+    T = sum(spec.lens)
+    if isinstance(spec, MlaSpec):
+        W = spec.kv_lora + spec.rope
+        kv = T * spec.L * W * B
+        patch = 0
+        if spec.m:
+            patch = sum((t + spec.kv_lora) * spec.m + (t + spec.rope) * spec.m
+                        for t in spec.lens) * spec.L * B
+        return 2 * kv + patch + T * 8
+    if spec.kind == "slide":
+        kv = T * spec.L * spec.H * spec.d * B
+        return 2 * kv + T * 8
+    kv = 2 * T * spec.L * spec.H * spec.d * B                      # K and V
+    patch = sum((t + spec.d) * spec.m for t in spec.lens) * spec.L * spec.H * 2 * B if spec.m else 0
+    return 2 * kv + patch + T * 8
+
+
+def tokens(spec) -> int:
+    return sum(spec.lens)
