@@ -1,0 +1,296 @@
+/*
+ * kamera.h -- C ABI of the GB300 (sm_103a) Kamera reuse operator.
+ *
+ * The operator is the reuse equation of "Kamera: Unified Position-Invariant
+ * Multimodal KV Cache for Training-Free Reuse" (gist.science technical summary,
+ * section 2, "Methodology: The Kamera Operator"):
+ *
+ *     KV^(B|A) = R(delta) . KV(B|empty) + U_m V_m^T
+ *
+ * A chunk B was prefilled once with no antecedent and stored position-free
+ * (the canonical store, section 2 "Canonical KV").  To reuse it at a new
+ * position its keys are turned by the exact RoPE phase shift R(delta) ("an
+ * exact algebraic operation, not a forward pass"), the rank-m conditioning
+ * patch U_m V_m^T (section 2 "Rank-m Conditioning Patch") is added to keys and
+ * values, and the rows are written into a paged KV pool at the slots the
+ * caller chose.  Section 2 "Unified Architecture Support" fixes the
+ * per-family rule, one entry point each:
+ *
+ *   kamera_relocate_patch      GQA and MHA: the whole key (the rotary range of
+ *                              each head) is re-rotated; K and V are patched.
+ *   kamera_mla_relocate_patch  MLA: only the 64-dim decoupled k_rope is
+ *                              re-rotated; c_KV is reused byte for byte; both
+ *                              channels are patched.
+ *   kamera_slide_inplace       Sliding-window survival (technical summary
+ *                              section 3.2): survivors relocate by rotation
+ *                              only, no patch, in place in the pool.
+ *
+ * Reorder (section 3.1, one orbit patch for every ordering) and recall
+ * (section 3.3, rehydration of an evicted chunk) are batches of chunk
+ * descriptors for kamera_relocate_patch: each chunk carries its own delta,
+ * rank, factors and target slots.
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ *  - Element type: bf16 (IEEE binary32 truncated to its top 16 bits) for all
+ *    K/V rows and patch factors.  Arithmetic is fp32; every output element is
+ *    rounded once to bf16, round-to-nearest-even.  A key row with delta == 0
+ *    and rank == 0, a value row with rank == 0 and the MLA c_KV block with
+ *    rank == 0 are copied bit for bit.
+ *  - RoPE: pair i (i < rot_dim/2) of the rotary range turns by
+ *    phi_i = delta * theta_i, theta_i = base^(-2i/rot_dim) (or the override
+ *    table):  x_a' = x_a cos phi - x_b sin phi,  x_b' = x_b cos phi + x_a sin phi.
+ *    ROTATE_HALF pairs (o+i, o+i+rot_dim/2); INTERLEAVED pairs (o+2i, o+2i+1),
+ *    o = rot_offset.  delta > 0 moves a chunk later: RoPE(x, p + delta) =
+ *    R(delta) RoPE(x, p).  The phase is formed and reduced modulo 2 pi in fp64.
+ *  - The patch is added after the rotation, in the target frame, as the
+ *    equation is printed.  A caller holding a canonical-frame patch passes
+ *    R(delta) applied to the columns of V_m instead (R(delta)(K + U V^T) =
+ *    R(delta) K + U (R(delta) V)^T).
+ *  - Memory: every pointer in the structs below, and every pointer inside the
+ *    chunk descriptors, is caller-owned device memory (except the RoPE
+ *    override table, which is host memory read during the call).  The library
+ *    allocates nothing, keeps no state between calls, never synchronises, and
+ *    is safe to call from several host threads.  Work is enqueued on `stream`
+ *    (a cudaStream_t of the current device; NULL = legacy default stream).
+ *  - Synchronous status: the return value (KAMERA_OK or a KAMERA_ERR_* code).
+ *    On any error nothing is enqueued.  n_chunks == 0 or max_len == 0 is a
+ *    successful no-op.
+ *  - Asynchronous status: violations only visible on the device (a slot
+ *    outside the pool, a source range outside the store, a malformed
+ *    descriptor, a chunk longer than max_len or of higher rank than max_rank)
+ *    OR a KAMERA_DEVERR_* bit into *d_err (device int32, may be NULL to
+ *    ignore) and skip the offending row or chunk; nothing outside the
+ *    targeted slots is ever written.  The caller clears *d_err.
+ *  - Preconditions (undefined results when violated; kamera_validate_chunks
+ *    checks them on a host copy): slots are distinct within one call; the
+ *    store and the pool do not overlap.
+ */
+#ifndef KAMERA_H
+#define KAMERA_H
+
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
+
+#define KAMERA_ABI_VERSION 1
+
+/* Limits of this build. */
+#define KAMERA_MAX_RANK 128          /* largest patch rank m */
+#define KAMERA_MAX_ROT_DIM 256       /* largest rotary width (128 frequencies) */
+#define KAMERA_MAX_ROW_ELEMS 4096    /* largest head_dim (GQA) / row width (MLA) */
+#define KAMERA_MAX_ABS_DELTA 2147483647LL /* |delta| bound (positions are int32) */
+
+/* Synchronous status codes. */
+enum {
+    KAMERA_OK = 0,
+    KAMERA_ERR_INVALID_ARGUMENT = 1, /* NULL pointer, negative count or size, bad stride */
+    KAMERA_ERR_MISALIGNED = 2,       /* a base pointer or stride is not 16-byte aligned */
+    KAMERA_ERR_UNSUPPORTED = 3,      /* a shape or RoPE layout this build does not handle */
+    KAMERA_ERR_CUDA = 4              /* a CUDA launch or attribute call failed */
+};
+
+/* Bits OR-ed into *d_err by the device. */
+enum {
+    KAMERA_DEVERR_SLOT = 1,        /* a slot outside [0, num_slots): that row skipped */
+    KAMERA_DEVERR_SOURCE = 2,      /* src_offset < 0 or src_offset + len > store rows: chunk skipped */
+    KAMERA_DEVERR_DESCRIPTOR = 4,  /* len < 0, rank < 0, |delta| too large, a NULL or
+                                      misaligned factor or slot map: chunk skipped */
+    KAMERA_DEVERR_LEN = 8,         /* len > max_len: chunk skipped */
+    KAMERA_DEVERR_RANK = 16,       /* rank > max_rank: chunk skipped */
+    KAMERA_DEVERR_TIMEOUT = 32     /* an internal pipeline wait gave up: results incomplete */
+};
+
+/* RoPE pairings. */
+enum {
+    KAMERA_ROPE_ROTATE_HALF = 0,   /* (o+i, o+i+r/2): Llama/Qwen/NeoX style */
+    KAMERA_ROPE_INTERLEAVED = 1    /* (o+2i, o+2i+1): original / GPT-J style */
+};
+
+/*
+ * One chunk of work (64 bytes; an array of these lives in device memory).
+ *   src_offset        first canonical row of the chunk in the store (ignored by
+ *                     kamera_slide_inplace)
+ *   len               tokens in the chunk, 0 <= len <= max_len of the call
+ *   rank              patch rank m, 0 <= m <= max_rank of the call (0 = no
+ *                     patch; kamera_slide_inplace requires 0)
+ *   delta             RoPE phase shift in positions (target - canonical)
+ *   patch_ptrs        four bf16 factor arrays, all NULL iff rank == 0, each
+ *                     16-byte aligned:
+ *                       GQA/MHA: Uk [L][H][len][m], Vk [L][H][head_dim][m],
+ *                                Uv [L][H][len][m], Vv [L][H][head_dim][m]
+ *                       MLA:     Uc [L][len][m], Vc [L][kv_lora_rank][m],
+ *                                Ur [L][len][m], Vr [L][rope_dim][m]
+ *                     (row-major, m contiguous; a joint 576-wide MLA factor is
+ *                     the same call with Uc == Ur)
+ *   dst_slot_mapping  len int64 pool slots, token j -> slot (16-byte aligned)
+ */
+typedef struct KameraChunk {
+    int64_t src_offset;
+    int32_t len;
+    int32_t rank;
+    int64_t delta;
+    const void* patch_ptrs[4];
+    const int64_t* dst_slot_mapping;
+} KameraChunk;
+
+/*
+ * RoPE layout inside each head (GQA/MHA) or of the k_rope block (MLA).
+ *   base               theta_i = base^(-2i/rot_dim) (ignored with an override)
+ *   rot_dim            rotated components (even; 0 = no rotation); a multiple
+ *                      of 16 for ROTATE_HALF and of 8 for INTERLEAVED
+ *   rot_offset         first rotated component (multiple of 8); for MLA it is
+ *                      relative to the start of k_rope and rot_offset + rot_dim
+ *                      <= rope_dim
+ *   pairing            KAMERA_ROPE_ROTATE_HALF or KAMERA_ROPE_INTERLEAVED
+ *   reserved           0
+ *   inv_freq_override  NULL, or a host array of rot_dim/2 fp64 frequencies
+ *                      (e.g. a model's scaled table), read during the call
+ */
+typedef struct KameraRope {
+    double base;
+    int32_t rot_dim;
+    int32_t rot_offset;
+    int32_t pairing;
+    int32_t reserved;
+    const double* inv_freq_override;
+} KameraRope;
+
+/*
+ * Paged GQA/MHA pool.  Element (l, s, h, i) of K lives at
+ * k[l*layer_stride + s*slot_stride + h*head_dim + i] (strides in elements,
+ * multiples of 8; slot_stride >= num_kv_heads*head_dim; layer_stride >=
+ * num_slots*slot_stride).  Slot s = page*P + offset for page size P: the
+ * library sees slots only.  head_dim is a multiple of 8.
+ */
+typedef struct KameraGqaPool {
+    int32_t num_layers;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t reserved;
+    void* k;
+    void* v;
+    int64_t num_slots;
+    int64_t layer_stride;
+    int64_t slot_stride;
+} KameraGqaPool;
+
+/* Canonical GQA/MHA store (same L, H, head_dim as the pool): element
+ * (l, row, h, i) of K at k[l*layer_stride + row*row_stride + h*head_dim + i]. */
+typedef struct KameraGqaStore {
+    const void* k;
+    const void* v;
+    int64_t num_rows;
+    int64_t layer_stride;
+    int64_t row_stride;
+} KameraGqaStore;
+
+/* Pool for the in-place slide: the K half of a GQA pool (V is never touched).
+ * MLA k_rope survival uses num_kv_heads = 1, head_dim = kv_lora + rope and a
+ * rotary range at rot_offset = kv_lora. */
+typedef struct KameraSlidePool {
+    int32_t num_layers;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t reserved;
+    void* k;
+    int64_t num_slots;
+    int64_t layer_stride;
+    int64_t slot_stride;
+} KameraSlidePool;
+
+/*
+ * Paged MLA pool: one row per (layer, slot) = c_KV (kv_lora_rank elements)
+ * followed by k_rope (rope_dim elements); element (l, s, i) at
+ * kv[l*layer_stride + s*slot_stride + i].  kv_lora_rank and rope_dim are
+ * multiples of 16.
+ */
+typedef struct KameraMlaPool {
+    int32_t num_layers;
+    int32_t kv_lora_rank;
+    int32_t rope_dim;
+    int32_t reserved;
+    void* kv;
+    int64_t num_slots;
+    int64_t layer_stride;
+    int64_t slot_stride;
+} KameraMlaPool;
+
+/* Canonical MLA store: element (l, row, i) at kv[l*layer_stride + row*row_stride + i]. */
+typedef struct KameraMlaStore {
+    const void* kv;
+    int64_t num_rows;
+    int64_t layer_stride;
+    int64_t row_stride;
+} KameraMlaStore;
+
+/*
+ * GQA/MHA relocate + patch + paged scatter (reuse equation; recall and
+ * reorder batches).  For every chunk c, layer l, head h, token j < len:
+ *   K[l][slot_j][h] = bf16( R(delta_c) Kstore[l][src_c+j][h] + Uk[l][h][j] Vk[l][h]^T )
+ *   V[l][slot_j][h] = bf16(            Vstore[l][src_c+j][h] + Uv[l][h][j] Vv[l][h]^T )
+ *   pool, store, rope   host structs (read during the call)
+ *   d_chunks            device array of n_chunks descriptors
+ *   max_len, max_rank   upper bounds of len and rank over the chunks (size the
+ *                       launch; larger chunks are skipped with a d_err bit)
+ *   d_err               device int32 or NULL
+ * Returns KAMERA_OK or a KAMERA_ERR_* code (nothing enqueued on error).
+ */
+int kamera_relocate_patch(const KameraGqaPool* pool, const KameraGqaStore* store,
+                          const KameraRope* rope, const KameraChunk* d_chunks, int32_t n_chunks,
+                          int32_t max_len, int32_t max_rank, int32_t* d_err,
+                          struct CUstream_st* stream);
+
+/*
+ * Sliding-window survival in place (technical summary section 3.2): for every
+ * chunk c, layer l, head h, token j < len:
+ *   K[l][slot_j][h] = bf16( R(delta_c) K[l][slot_j][h] )
+ * src_offset is ignored and rank must be 0 (else KAMERA_DEVERR_DESCRIPTOR).
+ * V is never read or written.
+ */
+int kamera_slide_inplace(const KameraSlidePool* pool, const KameraRope* rope,
+                         const KameraChunk* d_chunks, int32_t n_chunks, int32_t max_len,
+                         int32_t* d_err, struct CUstream_st* stream);
+
+/*
+ * MLA relocate + patch + paged scatter (section 2, MLA rule): for every chunk
+ * c, layer l, token j < len, with row = c_KV | k_rope:
+ *   c_KV'   = bf16( c_KV + Uc[l][j] Vc[l]^T )                (bit copy when rank == 0)
+ *   k_rope' = bf16( R(delta_c) k_rope + Ur[l][j] Vr[l]^T )
+ * rope->rot_offset/rot_dim are relative to k_rope (usually 0 / rope_dim).
+ */
+int kamera_mla_relocate_patch(const KameraMlaPool* pool, const KameraMlaStore* store,
+                              const KameraRope* rope, const KameraChunk* d_chunks,
+                              int32_t n_chunks, int32_t max_len, int32_t max_rank,
+                              int32_t* d_err, struct CUstream_st* stream);
+
+/*
+ * Host-side check of a HOST copy of a descriptor array (dst_slot_mapping
+ * pointers must point to host memory here; patch pointers are only tested
+ * for NULL-ness and 16-byte alignment).  Checks every device-side condition
+ * plus the preconditions: slots distinct across the whole array and in
+ * [0, num_slots); source ranges inside [0, num_store_rows) (skipped when
+ * num_store_rows < 0, as for the slide); len <= max_len; rank <= max_rank.
+ * Returns KAMERA_OK, or KAMERA_ERR_INVALID_ARGUMENT with *bad_chunk (if
+ * non-NULL) set to the first offending chunk index and *bad_bits to the
+ * KAMERA_DEVERR_* bits it would raise (KAMERA_DEVERR_SLOT also for a duplicate).
+ */
+int kamera_validate_chunks(const KameraChunk* h_chunks, int32_t n_chunks, int64_t num_store_rows,
+                           int64_t num_slots, int32_t max_len, int32_t max_rank,
+                           int32_t* bad_chunk, int32_t* bad_bits);
+
+/* Static description of a status code (never NULL). */
+const char* kamera_status_string(int status);
+
+/* KAMERA_ABI_VERSION of the loaded library. */
+int kamera_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KAMERA_H */

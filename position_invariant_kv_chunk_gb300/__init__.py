@@ -1,0 +1,322 @@
+"""GB300 (sm_103a) Kamera reuse operator: thin Python binding of the C ABI.
+
+The operator ("Kamera: Unified Position-Invariant Multimodal KV Cache for
+Training-Free Reuse", gist.science technical summary, section 2) relocates a
+position-free canonical chunk to a new position and restores its cross-chunk
+conditioning:  KV^(B|A) = R(delta) KV(B|empty) + U_m V_m^T, written into a
+paged KV pool.  Every step runs in the CUDA kernels of ``libkamera.so``
+(``include/kamera.h``); this module only marshals torch tensors into the C
+structs and calls the entry points of the same names.  There is no CPU path:
+without the compiled library (or without a GPU) every call raises.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import build as _build
+
+__all__ = [
+    "KameraError", "Rope", "ChunkSpec", "load_library", "pack_chunks",
+    "kamera_relocate_patch", "kamera_slide_inplace", "kamera_mla_relocate_patch",
+    "kamera_validate_chunks", "kamera_status_string", "kamera_abi_version",
+    "ROTATE_HALF", "INTERLEAVED", "DEVERR",
+]
+
+ROTATE_HALF = 0
+INTERLEAVED = 1
+MAX_RANK = 128
+
+DEVERR = {
+    1: "slot out of range",
+    2: "source rows out of range",
+    4: "malformed descriptor",
+    8: "len > max_len",
+    16: "rank > max_rank",
+    32: "pipeline wait timed out",
+}
+
+
+class KameraError(RuntimeError):
+    def __init__(self, status: int, where: str):
+        super().__init__(f"{where}: {kamera_status_string(status)} (status {status})")
+        self.status = status
+
+
+# ----------------------------------------------------------------- C structs
+class _Chunk(C.Structure):
+    _fields_ = [("src_offset", C.c_int64), ("len", C.c_int32), ("rank", C.c_int32),
+                ("delta", C.c_int64), ("patch_ptrs", C.c_void_p * 4),
+                ("dst_slot_mapping", C.c_void_p)]
+
+
+class _Rope(C.Structure):
+    _fields_ = [("base", C.c_double), ("rot_dim", C.c_int32), ("rot_offset", C.c_int32),
+                ("pairing", C.c_int32), ("reserved", C.c_int32),
+                ("inv_freq_override", C.POINTER(C.c_double))]
+
+
+class _GqaPool(C.Structure):
+    _fields_ = [("num_layers", C.c_int32), ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("reserved", C.c_int32), ("k", C.c_void_p), ("v", C.c_void_p),
+                ("num_slots", C.c_int64), ("layer_stride", C.c_int64), ("slot_stride", C.c_int64)]
+
+
+class _GqaStore(C.Structure):
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("num_rows", C.c_int64),
+                ("layer_stride", C.c_int64), ("row_stride", C.c_int64)]
+
+
+class _SlidePool(C.Structure):
+    _fields_ = [("num_layers", C.c_int32), ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32),
+                ("reserved", C.c_int32), ("k", C.c_void_p), ("num_slots", C.c_int64),
+                ("layer_stride", C.c_int64), ("slot_stride", C.c_int64)]
+
+
+class _MlaPool(C.Structure):
+    _fields_ = [("num_layers", C.c_int32), ("kv_lora_rank", C.c_int32), ("rope_dim", C.c_int32),
+                ("reserved", C.c_int32), ("kv", C.c_void_p), ("num_slots", C.c_int64),
+                ("layer_stride", C.c_int64), ("slot_stride", C.c_int64)]
+
+
+class _MlaStore(C.Structure):
+    _fields_ = [("kv", C.c_void_p), ("num_rows", C.c_int64), ("layer_stride", C.c_int64),
+                ("row_stride", C.c_int64)]
+
+
+assert C.sizeof(_Chunk) == 64
+
+_LIB: Optional[C.CDLL] = None
+
+
+def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C.CDLL:
+    """Load ``libkamera.so`` (building it in-tree with nvcc if absent or stale)."""
+    global _LIB
+    if _LIB is not None and path is None:
+        return _LIB
+    if path is None:
+        path = _build.LIB_PATH
+        if build_if_missing:
+            _build.build()
+    if not os.path.exists(path):
+        raise RuntimeError(f"Kamera CUDA library not found at {path}; run build()")
+    lib = C.CDLL(path)
+    P = C.POINTER
+    lib.kamera_relocate_patch.restype = C.c_int
+    lib.kamera_relocate_patch.argtypes = [P(_GqaPool), P(_GqaStore), P(_Rope), C.c_void_p, C.c_int32,
+                                          C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
+    lib.kamera_slide_inplace.restype = C.c_int
+    lib.kamera_slide_inplace.argtypes = [P(_SlidePool), P(_Rope), C.c_void_p, C.c_int32, C.c_int32,
+                                         C.c_void_p, C.c_void_p]
+    lib.kamera_mla_relocate_patch.restype = C.c_int
+    lib.kamera_mla_relocate_patch.argtypes = [P(_MlaPool), P(_MlaStore), P(_Rope), C.c_void_p, C.c_int32,
+                                              C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
+    lib.kamera_validate_chunks.restype = C.c_int
+    lib.kamera_validate_chunks.argtypes = [P(_Chunk), C.c_int32, C.c_int64, C.c_int64, C.c_int32,
+                                           C.c_int32, P(C.c_int32), P(C.c_int32)]
+    lib.kamera_status_string.restype = C.c_char_p
+    lib.kamera_status_string.argtypes = [C.c_int]
+    lib.kamera_abi_version.restype = C.c_int
+    lib.kamera_abi_version.argtypes = []
+    if path == _build.LIB_PATH:
+        _LIB = lib
+    return lib
+
+
+def kamera_status_string(status: int) -> str:
+    return load_library().kamera_status_string(int(status)).decode()
+
+
+def kamera_abi_version() -> int:
+    return int(load_library().kamera_abi_version())
+
+
+# ------------------------------------------------------------------ helpers
+@dataclass
+class Rope:
+    """RoPE layout (see ``KameraRope``): theta_i = base^(-2i/rot_dim) unless
+    ``inv_freq`` is given."""
+    base: float
+    rot_dim: int
+    rot_offset: int = 0
+    pairing: int = ROTATE_HALF
+    inv_freq: Optional[Sequence[float]] = None
+
+    def _c(self):
+        keep = None
+        ptr = None
+        if self.inv_freq is not None:
+            keep = np.ascontiguousarray(self.inv_freq, dtype=np.float64)
+            ptr = keep.ctypes.data_as(C.POINTER(C.c_double))
+        return _Rope(float(self.base), int(self.rot_dim), int(self.rot_offset), int(self.pairing), 0,
+                     ptr), keep
+
+
+@dataclass
+class ChunkSpec:
+    """One chunk descriptor before packing.  ``patches`` holds the four bf16
+    factor tensors (GQA: Uk, Vk, Uv, Vv; MLA: Uc, Vc, Ur, Vr) or is empty."""
+    src_offset: int
+    length: int
+    delta: int
+    rank: int
+    slots: torch.Tensor
+    patches: Sequence[torch.Tensor] = ()
+
+
+def _addr(t: Optional[torch.Tensor]) -> int:
+    return 0 if t is None else int(t.data_ptr())
+
+
+def pack_chunks(chunks: Sequence, device=None) -> torch.Tensor:
+    """Marshal chunk descriptors into the 64-byte ``KameraChunk`` layout.
+
+    Accepts ``ChunkSpec``-like objects (attributes src_offset, length, delta,
+    rank, slots, patches).  Returns a uint8 tensor on ``device`` (default: the
+    slot tensors' device) holding ``len(chunks)`` packed descriptors; the
+    referenced tensors must stay alive while the call runs.
+    """
+    n = len(chunks)
+    arr = (_Chunk * max(n, 1))()
+    for i, c in enumerate(chunks):
+        ptrs = [0, 0, 0, 0]
+        if c.rank > 0:
+            for k in range(4):
+                ptrs[k] = _addr(c.patches[k])
+        arr[i] = _Chunk(int(c.src_offset), int(c.length), int(c.rank), int(c.delta),
+                        (C.c_void_p * 4)(*ptrs), _addr(c.slots) if c.length > 0 else 0)
+    raw = bytes(arr)[: 64 * n]
+    if device is None:
+        device = chunks[0].slots.device if n else "cpu"
+    host = torch.frombuffer(bytearray(raw), dtype=torch.uint8) if n else torch.empty(0, dtype=torch.uint8)
+    return host.to(device)
+
+
+def _stream_handle(stream) -> int:
+    if stream is None:
+        return int(torch.cuda.current_stream().cuda_stream)
+    if isinstance(stream, torch.cuda.Stream):
+        return int(stream.cuda_stream)
+    return int(stream)
+
+
+def _check(rc: int, where: str):
+    if rc != 0:
+        raise KameraError(rc, where)
+
+
+def _bf16(t: torch.Tensor, name: str):
+    if t.dtype != torch.bfloat16:
+        raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
+
+
+# -------------------------------------------------------------- entry points
+def kamera_relocate_patch(pool_k: torch.Tensor, pool_v: torch.Tensor, store_k: torch.Tensor,
+                          store_v: torch.Tensor, rope: Rope, chunks: torch.Tensor, n_chunks: int,
+                          max_len: int, max_rank: int, err: Optional[torch.Tensor] = None,
+                          stream=None) -> None:
+    """GQA/MHA relocate + patch + paged scatter.
+
+    pool_*: bf16 ``[L, S, H, d]`` (layer/slot strides free, head/dim packed);
+    store_*: bf16 ``[L, N, H, d]``; chunks: packed descriptors (``pack_chunks``)
+    on the device; err: optional device int32 error word.
+    """
+    for t, nm in ((pool_k, "pool_k"), (pool_v, "pool_v"), (store_k, "store_k"), (store_v, "store_v")):
+        _bf16(t, nm)
+        if t.dim() != 4 or t.stride(3) != 1 or t.stride(2) != t.shape[3]:
+            raise ValueError(f"{nm} must be [L, rows, H, d] with packed heads")
+    L, S, H, d = pool_k.shape
+    pool = _GqaPool(L, H, d, 0, _addr(pool_k), _addr(pool_v), S, pool_k.stride(0), pool_k.stride(1))
+    if pool_v.stride() != pool_k.stride() or pool_v.shape != pool_k.shape:
+        raise ValueError("pool_k and pool_v must share shape and strides")
+    if store_v.stride() != store_k.stride() or store_v.shape != store_k.shape:
+        raise ValueError("store_k and store_v must share shape and strides")
+    if store_k.shape[0] != L or store_k.shape[2] != H or store_k.shape[3] != d:
+        raise ValueError("store and pool disagree on L, H or d")
+    store = _GqaStore(_addr(store_k), _addr(store_v), store_k.shape[1], store_k.stride(0), store_k.stride(1))
+    r, keep = rope._c()
+    rc = load_library().kamera_relocate_patch(C.byref(pool), C.byref(store), C.byref(r), _addr(chunks),
+                                              int(n_chunks), int(max_len), int(max_rank), _addr(err),
+                                              _stream_handle(stream))
+    del keep
+    _check(rc, "kamera_relocate_patch")
+
+
+def kamera_slide_inplace(pool_k: torch.Tensor, rope: Rope, chunks: torch.Tensor, n_chunks: int,
+                         max_len: int, err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Sliding-window survival: rotate the key rows at the chunks' slots in place.
+
+    pool_k: bf16 ``[L, S, H, d]`` (for MLA k_rope: ``[L, S, 1, kv_lora + rope]``
+    with ``rope.rot_offset = kv_lora``)."""
+    _bf16(pool_k, "pool_k")
+    if pool_k.dim() != 4 or pool_k.stride(3) != 1 or pool_k.stride(2) != pool_k.shape[3]:
+        raise ValueError("pool_k must be [L, S, H, d] with packed heads")
+    L, S, H, d = pool_k.shape
+    pool = _SlidePool(L, H, d, 0, _addr(pool_k), S, pool_k.stride(0), pool_k.stride(1))
+    r, keep = rope._c()
+    rc = load_library().kamera_slide_inplace(C.byref(pool), C.byref(r), _addr(chunks), int(n_chunks),
+                                             int(max_len), _addr(err), _stream_handle(stream))
+    del keep
+    _check(rc, "kamera_slide_inplace")
+
+
+def kamera_mla_relocate_patch(pool: torch.Tensor, store: torch.Tensor, kv_lora: int, rope: Rope,
+                              chunks: torch.Tensor, n_chunks: int, max_len: int, max_rank: int,
+                              err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """MLA relocate + patch + paged scatter.  pool: bf16 ``[L, S, kv_lora + rope]``;
+    store: bf16 ``[L, N, kv_lora + rope]``; rope offsets relative to k_rope."""
+    _bf16(pool, "pool")
+    _bf16(store, "store")
+    for t, nm in ((pool, "pool"), (store, "store")):
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError(f"{nm} must be [L, rows, width] with packed rows")
+    L, S, W = pool.shape
+    if store.shape[0] != L or store.shape[2] != W:
+        raise ValueError("store and pool disagree on L or row width")
+    p = _MlaPool(L, int(kv_lora), W - int(kv_lora), 0, _addr(pool), S, pool.stride(0), pool.stride(1))
+    s = _MlaStore(_addr(store), store.shape[1], store.stride(0), store.stride(1))
+    r, keep = rope._c()
+    rc = load_library().kamera_mla_relocate_patch(C.byref(p), C.byref(s), C.byref(r), _addr(chunks),
+                                                  int(n_chunks), int(max_len), int(max_rank), _addr(err),
+                                                  _stream_handle(stream))
+    del keep
+    _check(rc, "kamera_mla_relocate_patch")
+
+
+def _aligned_i64(a) -> np.ndarray:
+    """Copy into a 16-byte aligned int64 array (the ABI wants aligned slot maps)."""
+    a = np.asarray(a, dtype=np.int64).reshape(-1)
+    buf = np.empty(a.size + 2, dtype=np.int64)
+    off = (-buf.ctypes.data % 16) // 8
+    out = buf[off:off + a.size]
+    out[:] = a
+    return out
+
+
+def kamera_validate_chunks(chunks: Sequence, num_store_rows: int, num_slots: int, max_len: int,
+                           max_rank: int):
+    """Host-side check of descriptors (slot tensors read on the host).
+
+    Returns ``(status, bad_chunk, bad_bits)``; status 0 means valid."""
+    n = len(chunks)
+    arr = (_Chunk * max(n, 1))()
+    keep = []
+    for i, c in enumerate(chunks):
+        s = _aligned_i64(c.slots.detach().cpu().numpy() if isinstance(c.slots, torch.Tensor) else c.slots)
+        keep.append(s)
+        ptrs = [0, 0, 0, 0]
+        if c.rank > 0:
+            ptrs = [_addr(p) if isinstance(p, torch.Tensor) else int(p) for p in c.patches]
+        arr[i] = _Chunk(int(c.src_offset), int(c.length), int(c.rank), int(c.delta),
+                        (C.c_void_p * 4)(*ptrs), s.ctypes.data if c.length > 0 else 0)
+    bad = C.c_int32(-1)
+    bits = C.c_int32(0)
+    rc = load_library().kamera_validate_chunks(arr, n, int(num_store_rows), int(num_slots), int(max_len),
+                                               int(max_rank), C.byref(bad), C.byref(bits))
+    del keep
+    return int(rc), int(bad.value), int(bits.value)

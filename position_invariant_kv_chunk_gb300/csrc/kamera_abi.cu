@@ -1,0 +1,337 @@
+// kamera_abi.cu -- host side of the Kamera C ABI (include/kamera.h):
+// argument validation, RoPE frequency tables, kernel selection and launch.
+//
+// Nothing here allocates device memory or synchronises; every error is
+// reported before anything is enqueued.
+#include <algorithm>
+#include <cmath>
+#include <cstdint>
+#include <cstring>
+#include <utility>
+#include <vector>
+
+#include "kamera.h"
+#include "kamera_common.cuh"
+#include "kamera_internal.h"
+
+using namespace kamera;
+
+namespace {
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// Byte range [lo, hi) spanned by a strided [L][rows][width] bf16 array.
+std::pair<uintptr_t, uintptr_t> span(const void* base, int64_t L, int64_t ls, int64_t rows, int64_t rs,
+                                     int64_t width)
+{
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(base);
+    if (L <= 0 || rows <= 0)
+        return {lo, lo};
+    const int64_t last = (L - 1) * ls + (rows - 1) * rs + width;
+    return {lo, lo + static_cast<uintptr_t>(last) * 2u};
+}
+
+bool overlap(std::pair<uintptr_t, uintptr_t> a, std::pair<uintptr_t, uintptr_t> b)
+{
+    return a.first < b.second && b.first < a.second;
+}
+
+// RoPE: theta_i = base^(-2i/rot_dim) (standard rotary frequencies) or the
+// caller's table.  `width` is the extent the rotary range must fit in.
+int fill_rope(const KameraRope* r, int width, RopeParams* out)
+{
+    if (!r || r->reserved != 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (r->rot_dim < 0 || (r->rot_dim & 1) || r->rot_offset < 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (r->rot_dim > KAMERA_MAX_ROT_DIM)
+        return KAMERA_ERR_UNSUPPORTED;
+    if ((int64_t)r->rot_offset + r->rot_dim > width)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (r->pairing != KAMERA_ROPE_ROTATE_HALF && r->pairing != KAMERA_ROPE_INTERLEAVED)
+        return KAMERA_ERR_UNSUPPORTED;
+    if (r->rot_dim > 0) {
+        if (r->pairing == KAMERA_ROPE_ROTATE_HALF && (r->rot_dim % 16))
+            return KAMERA_ERR_UNSUPPORTED;
+        if (r->pairing == KAMERA_ROPE_INTERLEAVED && (r->rot_dim % 8))
+            return KAMERA_ERR_UNSUPPORTED;
+        if (r->rot_offset % 8)
+            return KAMERA_ERR_UNSUPPORTED;
+    }
+    std::memset(out, 0, sizeof(*out));
+    out->rot_dim = r->rot_dim;
+    out->rot_offset = r->rot_offset;
+    out->pairing = r->pairing;
+    out->n_freq = r->rot_dim / 2;
+    for (int i = 0; i < out->n_freq; ++i) {
+        double t;
+        if (r->inv_freq_override) {
+            t = r->inv_freq_override[i];
+        } else {
+            if (!(r->base > 0.0) || !std::isfinite(r->base))
+                return KAMERA_ERR_INVALID_ARGUMENT;
+            t = std::pow(r->base, -2.0 * (double)i / (double)r->rot_dim);
+        }
+        if (!std::isfinite(t))
+            return KAMERA_ERR_INVALID_ARGUMENT;
+        out->inv_freq[i] = t;
+    }
+    return KAMERA_OK;
+}
+
+int check_call(const KameraChunk* d_chunks, int32_t n_chunks, int32_t max_len, int32_t max_rank,
+               bool* noop)
+{
+    *noop = false;
+    if (n_chunks < 0 || max_len < 0 || max_rank < 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (max_rank > KAMERA_MAX_RANK)
+        return KAMERA_ERR_UNSUPPORTED;
+    if (n_chunks == 0 || max_len == 0) {
+        *noop = true;
+        return KAMERA_OK;
+    }
+    if (!d_chunks)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (reinterpret_cast<uintptr_t>(d_chunks) & 7u)
+        return KAMERA_ERR_MISALIGNED;
+    return KAMERA_OK;
+}
+
+int check_strided(const void* base, int64_t L, int64_t ls, int64_t rows, int64_t rs, int64_t width,
+                  bool need_rows)
+{
+    if (!base)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(base) || (ls & 7) || (rs & 7))
+        return KAMERA_ERR_MISALIGNED;
+    if (rows < 0 || (need_rows && rows < 1) || rs < width || ls < 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (L > 1 && ls < rows * rs)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    return KAMERA_OK;
+}
+
+int launch(const RowsParams& p, int family, cudaStream_t stream)
+{
+    const size_t smem = simt_smem_bytes(p, family, 64);
+    if (smem > 227u * 1024u)
+        return KAMERA_ERR_UNSUPPORTED;
+    const int64_t tiles = (p.max_len + 63) / 64;
+    if ((int64_t)p.n_chunks * tiles > 0x7FFFFFFFll || p.L > 65535)
+        return KAMERA_ERR_UNSUPPORTED;
+    return launch_simt(p, family, stream) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+int kamera_abi_version(void) { return KAMERA_ABI_VERSION; }
+
+const char* kamera_status_string(int status)
+{
+    switch (status) {
+    case KAMERA_OK: return "ok";
+    case KAMERA_ERR_INVALID_ARGUMENT: return "invalid argument";
+    case KAMERA_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
+    case KAMERA_ERR_UNSUPPORTED: return "shape or RoPE layout not supported by this build";
+    case KAMERA_ERR_CUDA: return "CUDA launch failed";
+    default: return "unknown status";
+    }
+}
+
+int kamera_relocate_patch(const KameraGqaPool* pool, const KameraGqaStore* store, const KameraRope* rope,
+                          const KameraChunk* d_chunks, int32_t n_chunks, int32_t max_len, int32_t max_rank,
+                          int32_t* d_err, struct CUstream_st* stream)
+{
+    if (!pool || !store || !rope)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (pool->num_layers < 1 || pool->num_kv_heads < 1 || pool->head_dim < 8 || pool->reserved != 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if ((pool->head_dim % 8) || pool->head_dim > KAMERA_MAX_ROW_ELEMS)
+        return KAMERA_ERR_UNSUPPORTED;
+    const int64_t L = pool->num_layers, W = (int64_t)pool->num_kv_heads * pool->head_dim;
+    int rc;
+    if ((rc = check_strided(pool->k, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W, true)))
+        return rc;
+    if ((rc = check_strided(pool->v, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W, true)))
+        return rc;
+    if ((rc = check_strided(store->k, L, store->layer_stride, store->num_rows, store->row_stride, W, false)))
+        return rc;
+    if ((rc = check_strided(store->v, L, store->layer_stride, store->num_rows, store->row_stride, W, false)))
+        return rc;
+    const auto pk = span(pool->k, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W);
+    const auto pv = span(pool->v, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W);
+    const auto sk = span(store->k, L, store->layer_stride, store->num_rows, store->row_stride, W);
+    const auto sv = span(store->v, L, store->layer_stride, store->num_rows, store->row_stride, W);
+    if (overlap(pk, pv) || overlap(pk, sk) || overlap(pk, sv) || overlap(pv, sk) || overlap(pv, sv))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    bool noop;
+    if ((rc = check_call(d_chunks, n_chunks, max_len, max_rank, &noop)) || noop)
+        return rc;
+    RowsParams p;
+    std::memset(&p, 0, sizeof(p));
+    if ((rc = fill_rope(rope, pool->head_dim, &p.rope)))
+        return rc;
+    p.dst_k = static_cast<__nv_bfloat16*>(pool->k);
+    p.dst_v = static_cast<__nv_bfloat16*>(pool->v);
+    p.num_slots = pool->num_slots;
+    p.dst_ls = pool->layer_stride;
+    p.dst_ss = pool->slot_stride;
+    p.src_k = static_cast<const __nv_bfloat16*>(store->k);
+    p.src_v = static_cast<const __nv_bfloat16*>(store->v);
+    p.num_rows = store->num_rows;
+    p.src_ls = store->layer_stride;
+    p.src_rs = store->row_stride;
+    p.L = pool->num_layers;
+    p.H = pool->num_kv_heads;
+    p.d = pool->head_dim;
+    p.kv_lora = 0;
+    p.chunks = d_chunks;
+    p.n_chunks = n_chunks;
+    p.max_len = max_len;
+    p.max_rank = max_rank;
+    p.err = d_err;
+    return launch(p, FAMILY_GQA, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kamera_slide_inplace(const KameraSlidePool* pool, const KameraRope* rope, const KameraChunk* d_chunks,
+                         int32_t n_chunks, int32_t max_len, int32_t* d_err, struct CUstream_st* stream)
+{
+    if (!pool || !rope)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (pool->num_layers < 1 || pool->num_kv_heads < 1 || pool->head_dim < 8 || pool->reserved != 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if ((pool->head_dim % 8) || pool->head_dim > KAMERA_MAX_ROW_ELEMS)
+        return KAMERA_ERR_UNSUPPORTED;
+    const int64_t L = pool->num_layers, W = (int64_t)pool->num_kv_heads * pool->head_dim;
+    int rc;
+    if ((rc = check_strided(pool->k, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W, true)))
+        return rc;
+    bool noop;
+    if ((rc = check_call(d_chunks, n_chunks, max_len, 0, &noop)) || noop)
+        return rc;
+    RowsParams p;
+    std::memset(&p, 0, sizeof(p));
+    if ((rc = fill_rope(rope, pool->head_dim, &p.rope)))
+        return rc;
+    p.dst_k = static_cast<__nv_bfloat16*>(pool->k);
+    p.num_slots = pool->num_slots;
+    p.dst_ls = pool->layer_stride;
+    p.dst_ss = pool->slot_stride;
+    p.L = pool->num_layers;
+    p.H = pool->num_kv_heads;
+    p.d = pool->head_dim;
+    p.chunks = d_chunks;
+    p.n_chunks = n_chunks;
+    p.max_len = max_len;
+    p.max_rank = 0;
+    p.err = d_err;
+    return launch(p, FAMILY_SLIDE, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kamera_mla_relocate_patch(const KameraMlaPool* pool, const KameraMlaStore* store, const KameraRope* rope,
+                              const KameraChunk* d_chunks, int32_t n_chunks, int32_t max_len, int32_t max_rank,
+                              int32_t* d_err, struct CUstream_st* stream)
+{
+    if (!pool || !store || !rope)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (pool->num_layers < 1 || pool->kv_lora_rank < 0 || pool->rope_dim < 0 || pool->reserved != 0 ||
+        pool->kv_lora_rank + pool->rope_dim < 16)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if ((pool->kv_lora_rank % 16) || (pool->rope_dim % 16) ||
+        pool->kv_lora_rank + pool->rope_dim > KAMERA_MAX_ROW_ELEMS || pool->rope_dim > KAMERA_MAX_ROT_DIM)
+        return KAMERA_ERR_UNSUPPORTED;
+    const int64_t L = pool->num_layers, W = (int64_t)pool->kv_lora_rank + pool->rope_dim;
+    int rc;
+    if ((rc = check_strided(pool->kv, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W, true)))
+        return rc;
+    if ((rc = check_strided(store->kv, L, store->layer_stride, store->num_rows, store->row_stride, W, false)))
+        return rc;
+    if (overlap(span(pool->kv, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W),
+                span(store->kv, L, store->layer_stride, store->num_rows, store->row_stride, W)))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    bool noop;
+    if ((rc = check_call(d_chunks, n_chunks, max_len, max_rank, &noop)) || noop)
+        return rc;
+    RowsParams p;
+    std::memset(&p, 0, sizeof(p));
+    if ((rc = fill_rope(rope, pool->rope_dim, &p.rope)))
+        return rc;
+    p.dst_k = static_cast<__nv_bfloat16*>(pool->kv);
+    p.num_slots = pool->num_slots;
+    p.dst_ls = pool->layer_stride;
+    p.dst_ss = pool->slot_stride;
+    p.src_k = static_cast<const __nv_bfloat16*>(store->kv);
+    p.num_rows = store->num_rows;
+    p.src_ls = store->layer_stride;
+    p.src_rs = store->row_stride;
+    p.L = pool->num_layers;
+    p.H = 1;
+    p.d = (int32_t)W;
+    p.kv_lora = pool->kv_lora_rank;
+    p.chunks = d_chunks;
+    p.n_chunks = n_chunks;
+    p.max_len = max_len;
+    p.max_rank = max_rank;
+    p.err = d_err;
+    return launch(p, FAMILY_MLA, reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kamera_validate_chunks(const KameraChunk* h_chunks, int32_t n_chunks, int64_t num_store_rows, int64_t num_slots,
+                           int32_t max_len, int32_t max_rank, int32_t* bad_chunk, int32_t* bad_bits)
+{
+    if (bad_chunk)
+        *bad_chunk = -1;
+    if (bad_bits)
+        *bad_bits = 0;
+    if (n_chunks < 0 || (n_chunks > 0 && !h_chunks))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    auto fail = [&](int32_t c, int32_t bits) {
+        if (bad_chunk)
+            *bad_chunk = c;
+        if (bad_bits)
+            *bad_bits = bits;
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    };
+    std::vector<std::pair<int64_t, int32_t>> all;
+    for (int32_t c = 0; c < n_chunks; ++c) {
+        const KameraChunk& ch = h_chunks[c];
+        int32_t bits = 0;
+        if (ch.len < 0 || ch.rank < 0 || ch.delta > KAMERA_MAX_ABS_DELTA || ch.delta < -KAMERA_MAX_ABS_DELTA)
+            bits |= KAMERA_DEVERR_DESCRIPTOR;
+        if (ch.len > 0 && (!ch.dst_slot_mapping || !aligned16(ch.dst_slot_mapping)))
+            bits |= KAMERA_DEVERR_DESCRIPTOR;
+        for (int i = 0; i < 4; ++i) {
+            const bool null = ch.patch_ptrs[i] == nullptr;
+            if ((ch.rank > 0 && (null || !aligned16(ch.patch_ptrs[i]))) || (ch.rank == 0 && !null))
+                bits |= KAMERA_DEVERR_DESCRIPTOR;
+        }
+        if (num_store_rows >= 0 && (ch.src_offset < 0 || ch.src_offset + (int64_t)ch.len > num_store_rows))
+            bits |= KAMERA_DEVERR_SOURCE;
+        if (ch.len > max_len)
+            bits |= KAMERA_DEVERR_LEN;
+        if (ch.rank > max_rank)
+            bits |= KAMERA_DEVERR_RANK;
+        if (!bits && ch.len > 0) {
+            for (int32_t j = 0; j < ch.len; ++j) {
+                const int64_t s = ch.dst_slot_mapping[j];
+                if (s < 0 || s >= num_slots) {
+                    bits |= KAMERA_DEVERR_SLOT;
+                    break;
+                }
+                all.emplace_back(s, c);
+            }
+        }
+        if (bits)
+            return fail(c, bits);
+    }
+    std::sort(all.begin(), all.end());
+    for (size_t i = 1; i < all.size(); ++i)
+        if (all[i].first == all[i - 1].first)
+            return fail(std::max(all[i].second, all[i - 1].second), KAMERA_DEVERR_SLOT);
+    return KAMERA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,145 @@
+// kamera_common.cuh -- device helpers shared by the Kamera kernels (sm_103a).
+//
+// The operator (Kamera, gist.science technical summary section 2, reuse
+// equation) is  KV^(B|A) = R(delta) KV(B|empty) + U_m V_m^T.  This header holds
+// the pieces every kernel needs: the launch parameter blocks, bf16 packing,
+// the fp64-formed RoPE phase, descriptor checks and device error reporting.
+#pragma once
+
+#include <cstdint>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+
+#include "kamera.h"
+
+namespace kamera {
+
+// ------------------------------------------------------------ parameters --
+struct RopeParams {
+    int32_t rot_dim;       // rotated components (0 = none)
+    int32_t rot_offset;    // first rotated component inside the row segment
+    int32_t pairing;       // KAMERA_ROPE_*
+    int32_t n_freq;        // rot_dim / 2
+    double inv_freq[KAMERA_MAX_ROT_DIM / 2];
+};
+
+// A family-neutral description of one call: token rows are read from `src`
+// (the canonical store; the pool itself for the in-place slide) and written to
+// `dst` at the chunk's slots.  Each kernel cuts a row into segments (GQA: one
+// head of K or V; MLA: 128-wide c_KV blocks, then k_rope; slide: one head).
+struct RowsParams {
+    // destination (pool), element (l, s, e) at dst[l*dst_ls + s*dst_ss + e]
+    __nv_bfloat16* dst_k;
+    __nv_bfloat16* dst_v;           // GQA values (NULL for MLA / slide)
+    int64_t num_slots;
+    int64_t dst_ls, dst_ss;
+    // source (store), element (l, r, e) at src[l*src_ls + r*src_rs + e]
+    const __nv_bfloat16* src_k;
+    const __nv_bfloat16* src_v;
+    int64_t num_rows;               // rows in the store (ignored in place)
+    int64_t src_ls, src_rs;
+    int32_t L;
+    int32_t H;                      // GQA heads (1 for MLA)
+    int32_t d;                      // GQA head_dim; MLA row width
+    int32_t kv_lora;                // MLA c_KV width (0 for GQA)
+    const KameraChunk* chunks;
+    int32_t n_chunks;
+    int32_t max_len;
+    int32_t max_rank;
+    int32_t tiles_per_chunk;
+    int32_t* err;
+    RopeParams rope;
+};
+
+// ------------------------------------------------------------------ bf16 --
+__device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
+__device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
+
+// Two fp32 -> packed bf16x2, each rounded to nearest even (lo in the low half).
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi)
+{
+    uint32_t r;
+    asm("cvt.rn.bf16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+__device__ __forceinline__ void unpack8(const uint4& v, float* f)
+{
+    f[0] = bf16lo(v.x); f[1] = bf16hi(v.x);
+    f[2] = bf16lo(v.y); f[3] = bf16hi(v.y);
+    f[4] = bf16lo(v.z); f[5] = bf16hi(v.z);
+    f[6] = bf16lo(v.w); f[7] = bf16hi(v.w);
+}
+
+__device__ __forceinline__ uint4 pack8(const float* f)
+{
+    uint4 v;
+    v.x = pack_bf16x2(f[0], f[1]);
+    v.y = pack_bf16x2(f[2], f[3]);
+    v.z = pack_bf16x2(f[4], f[5]);
+    v.w = pack_bf16x2(f[6], f[7]);
+    return v;
+}
+
+// ----------------------------------------------------------------- phase --
+// cos/sin of phi = delta * theta.  The product is formed in fp64 (exact to
+// ~1 ulp of phi) and reduced to [-pi, pi] with a two-term Cody-Waite split of
+// 2*pi (Cody & Waite, "Software Manual for the Elementary Functions", 1980):
+// hi = fp64(2*pi), lo = 2*pi - hi.  With |k| < 2^31 the two fused steps leave
+// an error of a few fp64 ulps of pi, so the only fp32 rounding is that of the
+// reduced angle (<= 2^-24 * pi) and of sincosf itself.
+__device__ __forceinline__ void phase_cos_sin(int64_t delta, double theta, float& c, float& s)
+{
+    const double kTwoPiHi = 6.283185307179586232;     // 0x401921FB54442D18
+    const double kTwoPiLo = 2.4492935982947064e-16;   // 2*pi - kTwoPiHi
+    const double kInvTwoPi = 0.15915494309189535;
+    const double phi = (double)delta * theta;
+    const double k = rint(phi * kInvTwoPi);
+    double red = fma(-k, kTwoPiHi, phi);
+    red = fma(-k, kTwoPiLo, red);
+    sincosf((float)red, &s, &c);
+}
+
+// ---------------------------------------------------------------- errors --
+__device__ __forceinline__ void raise_err(int32_t* err, int32_t bits)
+{
+    if (err)
+        atomicOr(err, bits);
+}
+
+// Checks one descriptor against the call; returns 0 when the chunk may run,
+// else the KAMERA_DEVERR_* bits (the chunk is then skipped whole).
+// in_place: the slide (src_offset ignored, rank must be 0).
+__device__ __forceinline__ int32_t check_chunk(const KameraChunk& ch, const RowsParams& p, bool in_place)
+{
+    int32_t bits = 0;
+    if (ch.len < 0 || ch.rank < 0 || ch.delta > KAMERA_MAX_ABS_DELTA || ch.delta < -KAMERA_MAX_ABS_DELTA)
+        bits |= KAMERA_DEVERR_DESCRIPTOR;
+    if (ch.len > 0 && (ch.dst_slot_mapping == nullptr || (reinterpret_cast<uintptr_t>(ch.dst_slot_mapping) & 15)))
+        bits |= KAMERA_DEVERR_DESCRIPTOR;
+    if (in_place) {
+        if (ch.rank != 0)
+            bits |= KAMERA_DEVERR_DESCRIPTOR;
+    } else {
+        if (ch.src_offset < 0 || ch.len < 0 || ch.src_offset + (int64_t)ch.len > p.num_rows)
+            bits |= KAMERA_DEVERR_SOURCE;
+        if (ch.rank > 0) {
+            for (int i = 0; i < 4; ++i) {
+                const uintptr_t a = reinterpret_cast<uintptr_t>(ch.patch_ptrs[i]);
+                if (a == 0 || (a & 15))
+                    bits |= KAMERA_DEVERR_DESCRIPTOR;
+            }
+        } else if (ch.rank == 0) {
+            for (int i = 0; i < 4; ++i)
+                if (ch.patch_ptrs[i] != nullptr)
+                    bits |= KAMERA_DEVERR_DESCRIPTOR;
+        }
+    }
+    if (ch.len > p.max_len)
+        bits |= KAMERA_DEVERR_LEN;
+    if (ch.rank > p.max_rank)
+        bits |= KAMERA_DEVERR_RANK;
+    return bits;
+}
+
+}  // namespace kamera

@@ -1,0 +1,18 @@
+// kamera_internal.h -- declarations shared by the Kamera translation units
+// (host launchers; not part of the public C ABI).
+#pragma once
+
+#include <cstddef>
+#include <cuda_runtime.h>
+
+namespace kamera {
+
+enum Family { FAMILY_GQA = 0, FAMILY_MLA = 1, FAMILY_SLIDE = 2 };
+
+struct RowsParams;
+
+// CUDA-core streaming path (any rank within the shared-memory budget).
+cudaError_t launch_simt(const RowsParams& p, int family, cudaStream_t stream);
+size_t simt_smem_bytes(const RowsParams& p, int family, int tile_tokens);
+
+}  // namespace kamera

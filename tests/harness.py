@@ -1,0 +1,190 @@
+"""Shared test plumbing: run a workload through the C ABI on the GPU, run the
+same seeded inputs through the fp64 oracle on the host, and compare.
+
+Tolerances (stated for the operator: within 1 bf16 ulp per element of the
+fp64 result rounded to bf16; relative Frobenius error <= 4e-3 per (layer,
+head) block; bit-exact for copies and indexing):
+
+* every element: |ord(gpu) - ord(oracle)| <= 1 in the ordered bf16 encoding
+  (adjacent representable values, across binade boundaries and +-0);
+* elements beyond 1 ulp are accepted only as cancellation: the true value is
+  small against the terms that made it, so fp32 rounding of those terms moves
+  it by more than a bf16 ulp of the result.  They must satisfy
+  |gpu - oracle| <= 2^-8 * scale, scale = |x cos| + |y sin| + sum |u_r v_r|
+  (the oracle's per-element magnitude), and be rare (<= 1e-4 of the elements
+  compared, plus 2);
+* per (layer, head) block: ||gpu - oracle||_F <= 4e-3 ||oracle||_F.
+"""
+from __future__ import annotations
+
+from dataclasses import dataclass
+
+import numpy as np
+import torch
+
+import oracle as O
+import position_invariant_kv_chunk_gb300 as K
+import workloads as W
+
+
+def u16(t: torch.Tensor) -> np.ndarray:
+    """bf16 tensor -> uint16 numpy array of its bit patterns (host copy)."""
+    return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
+
+
+def ordered(bits: np.ndarray) -> np.ndarray:
+    b = bits.astype(np.int32)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+
+
+def to_f64(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
+
+
+@dataclass
+class Stats:
+    n: int
+    over_1ulp: int
+    cancellation: int
+    max_ulp: int
+    worst_frob: float
+
+    def ok(self) -> bool:
+        return True
+
+
+def compare(gpu: np.ndarray, ref: np.ndarray, scale: np.ndarray, block_axes=None, what="") -> Stats:
+    """Element-wise comparison under the tolerances above; raises AssertionError."""
+    assert gpu.shape == ref.shape, (gpu.shape, ref.shape)
+    d = np.abs(ordered(gpu) - ordered(ref))
+    over = d > 1
+    n_over = int(over.sum())
+    if n_over:
+        g = to_f64(gpu[over])
+        r = to_f64(ref[over])
+        lim = 2.0 ** -8 * scale[over]
+        bad = np.abs(g - r) > lim
+        assert not bad.any(), f"{what}: {int(bad.sum())} elements beyond 1 ulp and the cancellation bound; " \
+                              f"first gpu={g[bad][:4]} oracle={r[bad][:4]} scale={scale[over][bad][:4]}"
+        assert n_over <= 1e-4 * gpu.size + 2, f"{what}: {n_over} of {gpu.size} elements beyond 1 ulp"
+    worst = 0.0
+    if block_axes is not None:
+        g = to_f64(gpu)
+        r = to_f64(ref)
+        num = np.sqrt(((g - r) ** 2).sum(axis=block_axes))
+        den = np.sqrt((r ** 2).sum(axis=block_axes))
+        rel = np.where(den > 0, num / np.where(den > 0, den, 1), num)
+        worst = float(rel.max()) if rel.size else 0.0
+        assert worst <= 4e-3, f"{what}: relative Frobenius error {worst:.3g} > 4e-3"
+    return Stats(gpu.size, n_over, n_over, int(d.max()) if d.size else 0, worst)
+
+
+# ------------------------------------------------------------- execution
+def rope_of(wl: W.Workload) -> K.Rope:
+    if wl.kind == "mla":
+        return K.Rope(wl.base, wl.rot_dim, 0, wl.pairing)
+    return K.Rope(wl.base, wl.rot_dim, wl.rot_offset, wl.pairing)
+
+
+def max_rank(wl: W.Workload) -> int:
+    return max((c.rank for c in wl.chunks), default=0)
+
+
+def run_gpu(wl: W.Workload, chunks_dev=None, err=None, max_len=None, mrank=None, stream=None):
+    """One call of the workload's entry point through the C ABI."""
+    if chunks_dev is None:
+        chunks_dev = K.pack_chunks(wl.chunks, device=wl.pool_k.device)
+    n = len(wl.chunks)
+    ml = wl.max_len if max_len is None else max_len
+    mr = max_rank(wl) if mrank is None else mrank
+    if wl.kind == "gqa":
+        K.kamera_relocate_patch(wl.pool_k, wl.pool_v, wl.store_k, wl.store_v, rope_of(wl), chunks_dev, n,
+                                ml, mr, err, stream)
+    elif wl.kind == "mla":
+        K.kamera_mla_relocate_patch(wl.pool_k, wl.store_k, wl.kv_lora, rope_of(wl), chunks_dev, n, ml, mr,
+                                    err, stream)
+    else:
+        K.kamera_slide_inplace(wl.pool_k, rope_of(wl), chunks_dev, n, ml, err, stream)
+    return chunks_dev
+
+
+def oracle_chunks(wl: W.Workload):
+    out = []
+    for c in wl.chunks:
+        out.append(O.Chunk(c.src_offset, c.length, c.delta, c.rank,
+                           c.slots.detach().cpu().numpy().astype(np.int64),
+                           [u16(p) for p in c.patches] if c.rank else []))
+    return out
+
+
+@dataclass
+class HostCopy:
+    store_k: np.ndarray = None
+    store_v: np.ndarray = None
+    pool_k: np.ndarray = None
+    pool_v: np.ndarray = None
+    chunks: list = None
+
+
+def snapshot(wl: W.Workload) -> HostCopy:
+    """Host copies of every input, taken before the GPU call."""
+    h = HostCopy()
+    h.store_k = u16(wl.store_k) if wl.store_k is not None else None
+    h.store_v = u16(wl.store_v) if wl.store_v is not None else None
+    h.pool_k = u16(wl.pool_k)
+    h.pool_v = u16(wl.pool_v) if wl.pool_v is not None else None
+    h.chunks = oracle_chunks(wl)
+    return h
+
+
+def run_oracle(wl: W.Workload, h: HostCopy, orc: O.Oracle = None):
+    """Oracle result on host copies: returns (pool_k, pool_v, scale_k, scale_v)."""
+    orc = orc or O.default()
+    pk = h.pool_k.copy()
+    pv = h.pool_v.copy() if h.pool_v is not None else None
+    if wl.kind == "gqa":
+        th = orc.inv_freq(wl.base, wl.rot_dim)
+        sk, sv = orc.gqa(h.store_k, h.store_v, pk, pv, h.chunks, th, wl.rot_dim, wl.rot_offset, wl.pairing,
+                         want_scale=True)
+        return pk, pv, sk, sv
+    if wl.kind == "mla":
+        th = orc.inv_freq(wl.base, wl.rot_dim)
+        sk = orc.mla(h.store_k, pk, h.chunks, wl.kv_lora, th, wl.pairing, want_scale=True)
+        return pk, None, sk, None
+    th = orc.inv_freq(wl.base, wl.rot_dim)
+    sk = orc.slide(pk, h.chunks, th, wl.rot_dim, wl.rot_offset, wl.pairing, want_scale=True)
+    return pk, None, sk, None
+
+
+def touched_slots(wl: W.Workload) -> np.ndarray:
+    if not wl.chunks:
+        return np.zeros(0, dtype=np.int64)
+    return np.concatenate([c.slots.detach().cpu().numpy() for c in wl.chunks]).astype(np.int64)
+
+
+def check_parity(wl: W.Workload, h: HostCopy, what: str):
+    """Full comparison of the GPU pool against the oracle (small workloads)."""
+    torch.cuda.synchronize()
+    ok, ov, sk, sv = run_oracle(wl, h)
+    gk = u16(wl.pool_k)
+    touched = np.zeros(gk.shape[1], dtype=bool)
+    touched[touched_slots(wl)] = True
+    # untouched slots keep their bytes exactly (canary)
+    assert np.array_equal(gk[:, ~touched], h.pool_k[:, ~touched]), f"{what}: untouched K slots changed"
+    stats = []
+    if wl.kind == "mla":
+        kv = wl.kv_lora
+        g = gk[:, touched]
+        r = ok[:, touched]
+        s = sk[:, touched]
+        stats.append(compare(g[..., :kv], r[..., :kv], s[..., :kv], block_axes=(1, 2), what=what + " c_KV"))
+        stats.append(compare(g[..., kv:], r[..., kv:], s[..., kv:], block_axes=(1, 2), what=what + " k_rope"))
+        if all(c.rank == 0 for c in wl.chunks):
+            assert np.array_equal(g[..., :kv], r[..., :kv]), f"{what}: c_KV not a bit copy"
+        return stats
+    stats.append(compare(gk[:, touched], ok[:, touched], sk[:, touched], block_axes=(1, 3), what=what + " K"))
+    if wl.kind == "gqa":
+        gv = u16(wl.pool_v)
+        assert np.array_equal(gv[:, ~touched], h.pool_v[:, ~touched]), f"{what}: untouched V slots changed"
+        stats.append(compare(gv[:, touched], ov[:, touched], sv[:, touched], block_axes=(1, 3), what=what + " V"))
+    return stats

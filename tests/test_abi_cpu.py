@@ -1,0 +1,134 @@
+"""The C-ABI library without a GPU: it builds, loads, exports every symbol the
+header declares, its struct layouts match the Python marshalling, and its
+host-side checks (descriptor validator, argument validation) behave.  No call
+here launches a kernel."""
+import ctypes as C
+import os
+import re
+import subprocess
+
+import numpy as np
+import pytest
+import torch
+
+import position_invariant_kv_chunk_gb300 as K
+from position_invariant_kv_chunk_gb300 import build as B
+
+HEADER = os.path.join(B.INCLUDE, "kamera.h")
+
+
+def declared_functions():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(kamera_\w+)\s*\(", src, re.M)))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("kamera_relocate_patch", "kamera_slide_inplace", "kamera_mla_relocate_patch",
+              "kamera_validate_chunks", "kamera_status_string", "kamera_abi_version"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol():
+    lib = C.CDLL(B.build())
+    for n in declared_functions():
+        assert hasattr(lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", B.LIB_PATH], capture_output=True, text=True).stdout
+    for n in declared_functions():
+        assert re.search(rf"\bT {n}$", out, re.M), n
+
+
+def test_struct_layouts_match_header(tmp_path):
+    """Compile a probe against the header with gcc and compare sizes/offsets
+    with the ctypes structures the binding marshals."""
+    structs = {
+        "KameraChunk": K._Chunk, "KameraRope": K._Rope, "KameraGqaPool": K._GqaPool,
+        "KameraGqaStore": K._GqaStore, "KameraSlidePool": K._SlidePool, "KameraMlaPool": K._MlaPool,
+        "KameraMlaStore": K._MlaStore,
+    }
+    lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kamera.h"', 'int main(void){']
+    for cname, py in structs.items():
+        lines.append(f'printf("{cname} size %zu\\n", sizeof({cname}));')
+        for f, _ in py._fields_:
+            lines.append(f'printf("{cname} {f} %zu\\n", offsetof({cname}, {f}));')
+    lines.append("return 0;}")
+    src = tmp_path / "probe.c"
+    src.write_text("\n".join(lines))
+    exe = tmp_path / "probe"
+    subprocess.run(["gcc", "-std=c11", "-I", B.INCLUDE, str(src), "-o", str(exe)], check=True)
+    out = subprocess.run([str(exe)], capture_output=True, text=True, check=True).stdout.split("\n")
+    got = {}
+    for ln in out:
+        if ln:
+            s, f, v = ln.split()
+            got[(s, f)] = int(v)
+    for cname, py in structs.items():
+        assert got[(cname, "size")] == C.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, (cname, f)
+
+
+def test_status_strings_and_version():
+    assert K.kamera_abi_version() == 1
+    for code in range(5):
+        assert K.kamera_status_string(code)
+    assert K.kamera_status_string(99) == "unknown status"
+
+
+def _chunk(src, ln, slots, rank=0, delta=0, patches=()):
+    return K.ChunkSpec(src, ln, delta, rank, np.asarray(slots, dtype=np.int64), patches)
+
+
+def test_validator_accepts_disjoint_chunks():
+    ch = [_chunk(0, 4, [3, 9, 1, 2]), _chunk(4, 3, [0, 4, 5])]
+    assert K.kamera_validate_chunks(ch, 7, 10, 4, 0) == (0, -1, 0)
+
+
+@pytest.mark.parametrize("mutate,bits,bad", [
+    (lambda ch: ch[1].__setattr__("slots", np.array([0, 4, 10])), 1, 1),        # slot == num_slots
+    (lambda ch: ch[1].__setattr__("slots", np.array([0, 4, 9])), 1, 1),         # duplicate slot 9
+    (lambda ch: ch[0].__setattr__("src_offset", -1), 2, 0),                     # source before the store
+    (lambda ch: ch[1].__setattr__("src_offset", 5), 2, 1),                      # source past the store
+    (lambda ch: ch[0].__setattr__("length", 5) or ch[0].__setattr__("slots", np.arange(20, 25)), 8, 0),
+    (lambda ch: ch[1].__setattr__("rank", 3) or ch[1].__setattr__("patches", (16, 32, 48, 64)), 16, 1),
+    (lambda ch: ch[1].__setattr__("rank", 2) or ch[1].__setattr__("patches", (16, 0, 48, 64)), 4, 1),
+    (lambda ch: ch[1].__setattr__("rank", 2) or ch[1].__setattr__("patches", (16, 8, 48, 64)), 4, 1),
+    (lambda ch: ch[0].__setattr__("delta", 2 ** 40), 4, 0),
+])
+def test_validator_rejects(mutate, bits, bad):
+    ch = [_chunk(0, 4, [3, 9, 1, 2]), _chunk(4, 3, [0, 4, 5])]
+    mutate(ch)
+    rc, b, got = K.kamera_validate_chunks(ch, 7, 10, 4, 2)
+    assert rc == 1 and b == bad and got == bits, (rc, b, got)
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-only argument checks; run where no GPU exists")
+def test_argument_errors_before_any_launch():
+    """Each call is malformed, so the library returns before touching CUDA."""
+    L, S, H, d = 1, 16, 2, 64
+    pk = torch.zeros(L, S, H, d, dtype=torch.bfloat16)
+    pv = torch.zeros_like(pk)
+    sk = torch.zeros(L, 8, H, d, dtype=torch.bfloat16)
+    sv = torch.zeros_like(sk)
+    ch = torch.zeros(64, dtype=torch.uint8)
+    rope = K.Rope(1e4, 64)
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_relocate_patch(pk, pv, sk, sv, K.Rope(1e4, 24), ch, 1, 8, 0, stream=0)
+    assert e.value.status == 3
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_relocate_patch(pk, pv, sk, sv, rope, ch, 1, 8, 200, stream=0)
+    assert e.value.status == 3
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_relocate_patch(pk, pv, sk, sv, rope, ch, 1, -8, 0, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_relocate_patch(pk, pv, torch.as_strided(pk, sk.shape, sk.stride()), sv, rope, ch, 1, 8, 0,
+                                stream=0)
+    assert e.value.status == 1
+    # n_chunks == 0 is a successful no-op that never reaches CUDA
+    K.kamera_relocate_patch(pk, pv, sk, sv, rope, ch, 0, 8, 0, stream=0)
+    mla = torch.zeros(1, 16, 24, dtype=torch.bfloat16)
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_mla_relocate_patch(mla, torch.zeros(1, 8, 24, dtype=torch.bfloat16), 12,
+                                    K.Rope(1e4, 12, 0, K.INTERLEAVED), ch, 1, 8, 0, stream=0)
+    assert e.value.status == 3

@@ -1,0 +1,235 @@
+"""GPU parity: every entry point through the C ABI against the fp64 oracle,
+element by element, at sizes that span several token tiles, ragged tails and
+page boundaries, plus the degenerate cases of the method."""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import position_invariant_kv_chunk_gb300 as K
+import workloads as W
+from tests import harness as Hn
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+def _cases():
+    return {
+        "tiny_gqa": W.tiny_gqa(),
+        "qwen_recall_small": W.scaled(W.qwen_recall(), L=3, lens=(1296, 200, 65, 1)),
+        "dsv2_mla_small": W.scaled(W.dsv2_mla(), L=2, lens=(300, 129, 64, 7)),
+        "qwen_slide_small": W.scaled(W.qwen_slide(), L=2, lens=(1296, 77, 128)),
+        "mha_reorder_recall_small": W.scaled(W.mha_reorder_recall(), L=2, H=4, lens=(513, 256, 1000, 2048, 300)),
+        "tiny_gqa_x64": W.tiny_gqa_x(64),
+    }
+
+
+@pytest.mark.parametrize("name", list(_cases()))
+def test_parity(name):
+    spec = _cases()[name]
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    Hn.check_parity(wl, h, name)
+    assert int(err.item()) == 0
+
+
+@pytest.mark.parametrize("pairing,rot_dim,rot_offset", [(K.INTERLEAVED, 128, 0), (K.ROTATE_HALF, 64, 32),
+                                                        (K.INTERLEAVED, 32, 96), (K.ROTATE_HALF, 16, 0)])
+def test_gqa_rope_layouts(pairing, rot_dim, rot_offset):
+    spec = W.scaled(W.qwen_recall(), L=2, lens=(150, 64), m=16)
+    spec = W.GqaSpec(**{**spec.__dict__, "pairing": pairing, "rot_dim": rot_dim, "rot_offset": rot_offset})
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    Hn.run_gpu(wl)
+    Hn.check_parity(wl, h, f"rope {pairing}/{rot_dim}/{rot_offset}")
+
+
+@pytest.mark.parametrize("m", [1, 3, 8, 16, 17, 48, 64, 96, 128])
+def test_gqa_ranks(m):
+    spec = W.scaled(W.qwen_recall(), L=1, H=2, lens=(130, 5), m=m)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    Hn.run_gpu(wl)
+    Hn.check_parity(wl, h, f"rank {m}")
+
+
+@pytest.mark.parametrize("d", [64, 128, 256])
+def test_gqa_head_dims(d):
+    spec = W.GqaSpec("hd", "gqa", L=2, H=2, d=d, base=1e4, lens=(140, 33), deltas=(999, -5), m=16, page=16)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    Hn.run_gpu(wl)
+    Hn.check_parity(wl, h, f"head_dim {d}")
+
+
+def test_zero_delta_zero_rank_is_bit_exact_permutation():
+    spec = W.scaled(W.qwen_recall(), L=2, lens=(300, 41), m=0)
+    spec = W.GqaSpec(**{**spec.__dict__, "deltas": (0, 0)})
+    wl = W.make(spec, DEV)
+    wl.store_k.view(torch.int16)[0, :5] = -32768          # -0.0 survives a copy
+    h = Hn.snapshot(wl)
+    Hn.run_gpu(wl)
+    torch.cuda.synchronize()
+    gk, gv = Hn.u16(wl.pool_k), Hn.u16(wl.pool_v)
+    for c in h.chunks:
+        src = slice(c.src_offset, c.src_offset + c.length)
+        assert np.array_equal(gk[:, c.slots], h.store_k[:, src])
+        assert np.array_equal(gv[:, c.slots], h.store_v[:, src])
+
+
+def test_rank0_values_are_bit_copies():
+    spec = W.scaled(W.qwen_recall(), L=2, lens=(200,), m=0)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    Hn.run_gpu(wl)
+    torch.cuda.synchronize()
+    gv = Hn.u16(wl.pool_v)
+    c = h.chunks[0]
+    assert np.array_equal(gv[:, c.slots], h.store_v[:, c.src_offset:c.src_offset + c.length])
+    Hn.check_parity(wl, h, "rank0")
+
+
+def test_mla_rank0_c_kv_bit_exact():
+    spec = W.scaled(W.dsv2_mla(), L=2, lens=(257, 64), m=0)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    Hn.run_gpu(wl)
+    Hn.check_parity(wl, h, "mla rank0")   # includes the bit-exact c_KV check
+
+
+def test_slide_mla_rope_subrange():
+    """Slide on an MLA pool: only k_rope (offset 512, 64 wide, interleaved) turns."""
+    spec = W.GqaSpec("mla_slide", "slide", L=2, H=1, d=576, base=1e4, lens=(200, 64), deltas=(-4096, 17),
+                     m=0, page=64, pairing=K.INTERLEAVED, rot_dim=64, rot_offset=512, evicted=100, window=364)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    Hn.run_gpu(wl)
+    Hn.check_parity(wl, h, "mla slide")
+    gk = Hn.u16(wl.pool_k)
+    sl = Hn.touched_slots(wl)
+    assert np.array_equal(gk[:, sl, :, :512], h.pool_k[:, sl, :, :512])
+
+
+def test_slide_zero_delta_is_noop():
+    spec = W.scaled(W.qwen_slide(), L=1, lens=(100,))
+    spec = W.GqaSpec(**{**spec.__dict__, "deltas": (0,)})
+    wl = W.make(spec, DEV)
+    before = Hn.u16(wl.pool_k)
+    Hn.run_gpu(wl)
+    torch.cuda.synchronize()
+    assert np.array_equal(Hn.u16(wl.pool_k), before)
+
+
+def test_empty_and_zero_length():
+    spec = W.scaled(W.qwen_recall(), L=1, lens=(40,), m=4)
+    wl = W.make(spec, DEV)
+    before_k = Hn.u16(wl.pool_k)
+    # no chunks: a no-op
+    K.kamera_relocate_patch(wl.pool_k, wl.pool_v, wl.store_k, wl.store_v, Hn.rope_of(wl),
+                            torch.empty(0, dtype=torch.uint8, device=DEV), 0, 40, 4)
+    # a zero-length chunk: nothing written, no error
+    z = W.ChunkData(0, 0, 5, 0, torch.empty(0, dtype=torch.int64, device=DEV), [])
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    K.kamera_relocate_patch(wl.pool_k, wl.pool_v, wl.store_k, wl.store_v, Hn.rope_of(wl),
+                            K.pack_chunks([z], device=DEV), 1, 40, 4, err)
+    torch.cuda.synchronize()
+    assert np.array_equal(Hn.u16(wl.pool_k), before_k)
+    assert int(err.item()) == 0
+
+
+def _bad_case(mutate, expect_bits, skip_whole_chunk=True):
+    spec = W.scaled(W.qwen_recall(), L=2, lens=(70, 50), m=8)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    bad = wl.chunks[1]
+    mutate(wl, bad)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err, max_len=70, mrank=8)
+    torch.cuda.synchronize()
+    assert int(err.item()) & expect_bits == expect_bits
+    # the good chunk is still right
+    good = W.Workload(wl.spec, wl.kind, [wl.chunks[0]], wl.store_k, wl.store_v, wl.pool_k, wl.pool_v,
+                      wl.rot_dim, wl.rot_offset, wl.pairing, wl.base)
+    hg = Hn.HostCopy(h.store_k, h.store_v, h.pool_k, h.pool_v, [h.chunks[0]])
+    ok, ov, sk, sv = Hn.run_oracle(good, hg)
+    gk = Hn.u16(wl.pool_k)
+    s0 = h.chunks[0].slots
+    Hn.compare(gk[:, s0], ok[:, s0], sk[:, s0], what="good chunk")
+    return wl, h, gk
+
+
+def test_device_error_slot_out_of_range():
+    def mut(wl, c):
+        c.slots = c.slots.clone()
+        c.slots[7] = wl.num_slots + 3
+    wl, h, gk = _bad_case(mut, 1)
+    # only that row was skipped: the others of the chunk were written
+    sl = wl.chunks[1].slots.cpu().numpy()
+    written = [s for i, s in enumerate(sl) if i != 7]
+    assert not np.array_equal(gk[:, written], h.pool_k[:, written])
+
+
+def test_device_error_source_range():
+    def mut(wl, c):
+        c.src_offset = wl.store_k.shape[1] - 10
+    wl, h, gk = _bad_case(mut, 2)
+    sl = wl.chunks[1].slots.cpu().numpy()
+    assert np.array_equal(gk[:, sl], h.pool_k[:, sl])   # whole chunk skipped
+
+
+def test_device_error_len_and_rank():
+    def mut(wl, c):
+        c.rank = 8
+    spec = W.scaled(W.qwen_recall(), L=1, lens=(70, 90), m=8)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err, max_len=80, mrank=8)        # chunk 1 is longer than max_len
+    torch.cuda.synchronize()
+    assert int(err.item()) == 8
+    gk = Hn.u16(wl.pool_k)
+    sl = wl.chunks[1].slots.cpu().numpy()
+    assert np.array_equal(gk[:, sl], h.pool_k[:, sl])
+    err.zero_()
+    Hn.run_gpu(wl, err=err, max_len=90, mrank=4)        # rank 8 > max_rank 4
+    torch.cuda.synchronize()
+    assert int(err.item()) == 16
+
+
+def test_device_error_null_factor():
+    def mut(wl, c):
+        c.patches = [c.patches[0], None, c.patches[2], c.patches[3]]
+    wl, h, gk = _bad_case(mut, 4)
+
+
+def test_host_errors():
+    """Argument errors are reported synchronously and enqueue nothing."""
+    spec = W.scaled(W.qwen_recall(), L=1, lens=(16,), m=4)
+    wl = W.make(spec, DEV)
+    before = Hn.u16(wl.pool_k)
+    ch = K.pack_chunks(wl.chunks, device=DEV)
+    r = Hn.rope_of(wl)
+    args = (wl.pool_k, wl.pool_v, wl.store_k, wl.store_v)
+    cases = [
+        ((*args, K.Rope(1e6, 12), ch, 1, 16, 4), 3),          # rot_dim not a multiple of 16
+        ((*args, K.Rope(1e6, 128, 8), ch, 1, 16, 4), 1),      # rotary range past head_dim
+        ((*args, r, ch, 1, 16, 999), 3),                      # max_rank beyond the build limit
+        ((*args, r, ch, -1, 16, 4), 1),                       # negative chunk count
+        ((*args, K.Rope(-1.0, 128), ch, 1, 16, 4), 1),        # base must be positive
+    ]
+    L, S, H, d = wl.pool_k.shape
+    mis_k = torch.as_strided(wl.pool_k.view(-1)[1:], (L, S - 1, H, d), (S * H * d, H * d, d, 1))
+    mis_v = torch.as_strided(wl.pool_v.view(-1)[1:], (L, S - 1, H, d), (S * H * d, H * d, d, 1))
+    cases.append(((mis_k, mis_v, wl.store_k, wl.store_v, r, ch, 1, 16, 4), 2))     # misaligned base
+    over = torch.as_strided(wl.pool_k, wl.store_k.shape, wl.store_k.stride())
+    cases.append(((wl.pool_k, wl.pool_v, over, wl.store_v, r, ch, 1, 16, 4), 1))  # store overlaps pool
+    for a, status in cases:
+        with pytest.raises(K.KameraError) as e:
+            K.kamera_relocate_patch(*a)
+        assert e.value.status == status, (status, e.value)
+    torch.cuda.synchronize()
+    assert np.array_equal(Hn.u16(wl.pool_k), before)
