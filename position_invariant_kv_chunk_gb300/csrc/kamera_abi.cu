@@ -6,6 +6,7 @@
 #include <algorithm>
 #include <cmath>
 #include <cstdint>
+#include <cstdlib>
 #include <cstring>
 #include <utility>
 #include <vector>
@@ -112,8 +113,22 @@ int check_strided(const void* base, int64_t L, int64_t ls, int64_t rows, int64_t
     return KAMERA_OK;
 }
 
+// Kernel choice: the tensor-core path whenever the call carries patches and
+// its shape fits (head_dim 64/128, whole-head rotary; MLA c_KV in 128-blocks
+// and a 64/128 k_rope), the CUDA-core path otherwise.  KAMERA_PATH=simt or
+// =umma in the environment pins one of them (testing both on one input).
 int launch(const RowsParams& p, int family, cudaStream_t stream)
 {
+    const char* force = std::getenv("KAMERA_PATH");
+    const bool want_simt = force && std::strcmp(force, "simt") == 0;
+    const bool want_umma = force && std::strcmp(force, "umma") == 0;
+    if (!want_simt && family != FAMILY_SLIDE && umma_supported(p, family)) {
+        if (umma_smem_bytes(p) > 227u * 1024u)
+            return KAMERA_ERR_UNSUPPORTED;
+        return launch_umma(p, family, stream) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
+    }
+    if (want_umma)
+        return KAMERA_ERR_UNSUPPORTED;
     const size_t smem = simt_smem_bytes(p, family, 64);
     if (smem > 227u * 1024u)
         return KAMERA_ERR_UNSUPPORTED;

@@ -15,4 +15,9 @@ struct RowsParams;
 cudaError_t launch_simt(const RowsParams& p, int family, cudaStream_t stream);
 size_t simt_smem_bytes(const RowsParams& p, int family, int tile_tokens);
 
+// Tensor-core path (tcgen05 MMA for the rank-m patch; relocation with rank > 0).
+bool umma_supported(const RowsParams& p, int family);
+size_t umma_smem_bytes(const RowsParams& p);
+cudaError_t launch_umma(const RowsParams& p, int family, cudaStream_t stream);
+
 }  // namespace kamera

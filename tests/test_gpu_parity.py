@@ -15,6 +15,14 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
+@pytest.fixture(params=["auto", "simt"])
+def path(request, monkeypatch):
+    """Run the case on the default kernel choice (tensor-core path for patched
+    GQA/MHA/MLA calls) and pinned to the CUDA-core path."""
+    monkeypatch.setenv("KAMERA_PATH", request.param)
+    return request.param
+
+
 def _cases():
     return {
         "tiny_gqa": W.tiny_gqa(),
@@ -27,7 +35,7 @@ def _cases():
 
 
 @pytest.mark.parametrize("name", list(_cases()))
-def test_parity(name):
+def test_parity(name, path):
     spec = _cases()[name]
     wl = W.make(spec, DEV)
     h = Hn.snapshot(wl)
@@ -38,8 +46,9 @@ def test_parity(name):
 
 
 @pytest.mark.parametrize("pairing,rot_dim,rot_offset", [(K.INTERLEAVED, 128, 0), (K.ROTATE_HALF, 64, 32),
-                                                        (K.INTERLEAVED, 32, 96), (K.ROTATE_HALF, 16, 0)])
-def test_gqa_rope_layouts(pairing, rot_dim, rot_offset):
+                                                        (K.INTERLEAVED, 32, 96), (K.ROTATE_HALF, 16, 0),
+                                                        (K.ROTATE_HALF, 0, 0)])
+def test_gqa_rope_layouts(pairing, rot_dim, rot_offset, path):
     spec = W.scaled(W.qwen_recall(), L=2, lens=(150, 64), m=16)
     spec = W.GqaSpec(**{**spec.__dict__, "pairing": pairing, "rot_dim": rot_dim, "rot_offset": rot_offset})
     wl = W.make(spec, DEV)
@@ -49,7 +58,7 @@ def test_gqa_rope_layouts(pairing, rot_dim, rot_offset):
 
 
 @pytest.mark.parametrize("m", [1, 3, 8, 16, 17, 48, 64, 96, 128])
-def test_gqa_ranks(m):
+def test_gqa_ranks(m, path):
     spec = W.scaled(W.qwen_recall(), L=1, H=2, lens=(130, 5), m=m)
     wl = W.make(spec, DEV)
     h = Hn.snapshot(wl)
@@ -58,7 +67,7 @@ def test_gqa_ranks(m):
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
-def test_gqa_head_dims(d):
+def test_gqa_head_dims(d, path):
     spec = W.GqaSpec("hd", "gqa", L=2, H=2, d=d, base=1e4, lens=(140, 33), deltas=(999, -5), m=16, page=16)
     wl = W.make(spec, DEV)
     h = Hn.snapshot(wl)
@@ -66,7 +75,7 @@ def test_gqa_head_dims(d):
     Hn.check_parity(wl, h, f"head_dim {d}")
 
 
-def test_zero_delta_zero_rank_is_bit_exact_permutation():
+def test_zero_delta_zero_rank_is_bit_exact_permutation(path):
     spec = W.scaled(W.qwen_recall(), L=2, lens=(300, 41), m=0)
     spec = W.GqaSpec(**{**spec.__dict__, "deltas": (0, 0)})
     wl = W.make(spec, DEV)
@@ -93,7 +102,7 @@ def test_rank0_values_are_bit_copies():
     Hn.check_parity(wl, h, "rank0")
 
 
-def test_mla_rank0_c_kv_bit_exact():
+def test_mla_rank0_c_kv_bit_exact(path):
     spec = W.scaled(W.dsv2_mla(), L=2, lens=(257, 64), m=0)
     wl = W.make(spec, DEV)
     h = Hn.snapshot(wl)
@@ -162,7 +171,7 @@ def _bad_case(mutate, expect_bits, skip_whole_chunk=True):
     return wl, h, gk
 
 
-def test_device_error_slot_out_of_range():
+def test_device_error_slot_out_of_range(path):
     def mut(wl, c):
         c.slots = c.slots.clone()
         c.slots[7] = wl.num_slots + 3
@@ -173,7 +182,7 @@ def test_device_error_slot_out_of_range():
     assert not np.array_equal(gk[:, written], h.pool_k[:, written])
 
 
-def test_device_error_source_range():
+def test_device_error_source_range(path):
     def mut(wl, c):
         c.src_offset = wl.store_k.shape[1] - 10
     wl, h, gk = _bad_case(mut, 2)
@@ -181,7 +190,7 @@ def test_device_error_source_range():
     assert np.array_equal(gk[:, sl], h.pool_k[:, sl])   # whole chunk skipped
 
 
-def test_device_error_len_and_rank():
+def test_device_error_len_and_rank(path):
     def mut(wl, c):
         c.rank = 8
     spec = W.scaled(W.qwen_recall(), L=1, lens=(70, 90), m=8)
@@ -200,7 +209,7 @@ def test_device_error_len_and_rank():
     assert int(err.item()) == 16
 
 
-def test_device_error_null_factor():
+def test_device_error_null_factor(path):
     def mut(wl, c):
         c.patches = [c.patches[0], None, c.patches[2], c.patches[3]]
     wl, h, gk = _bad_case(mut, 4)
@@ -233,3 +242,34 @@ def test_host_errors():
         assert e.value.status == status, (status, e.value)
     torch.cuda.synchronize()
     assert np.array_equal(Hn.u16(wl.pool_k), before)
+
+
+def test_mixed_ranks_in_one_call(path):
+    """Chunks of rank 32, 0 and 16 in one call (the tensor-core path skips the
+    MMA for rank-0 chunks and pads rank 16 inside its operand tiles)."""
+    spec = W.scaled(W.qwen_recall(), L=2, lens=(300, 200, 129, 64, 260), m=32)
+    wl = W.make(spec, DEV)
+    for i in (1, 3):
+        wl.chunks[i].rank = 0
+        wl.chunks[i].patches = []
+    c = wl.chunks[2]
+    c.rank = 16
+    c.patches = [p[..., :16].contiguous() for p in c.patches]
+    h = Hn.snapshot(wl)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    Hn.check_parity(wl, h, "mixed ranks")
+    assert int(err.item()) == 0
+
+
+def test_many_tiles_per_cta_boundaries(path):
+    """More tiles than CTAs with uneven chunk lengths: contiguous tile ranges of
+    the persistent grid start and end inside chunks and segments."""
+    lens = tuple(int(x) for x in np.random.default_rng(5).integers(1, 700, size=23))
+    spec = W.scaled(W.mha_reorder_recall(), L=3, H=3, lens=lens, m=24)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    Hn.check_parity(wl, h, "many tiles")
+    assert int(err.item()) == 0
