@@ -3,32 +3,37 @@
 // Reuse equation (gist.science technical summary, section 2):
 //     KV^(B|A) = R(delta) KV(B|empty) + U_m V_m^T
 // The rank-m patch U_m V_m^T of one (chunk, layer, row segment) over a tile of
-// 128 tokens is a 128 x w x m contraction (w = head_dim for GQA/MHA, 128 or
-// 64 for the MLA c_KV blocks / k_rope).  It runs on the 5th-generation tensor
-// cores: one tcgen05.mma (M=128, N=w, K=16 per instruction, bf16 in, fp32 out)
-// per 16 ranks, accumulator in TMEM.  Everything else streams:
+// 128 tokens is a 128 x w x m contraction (w = head_dim for GQA/MHA, 128 for
+// an MLA c_KV block, 64 or 128 for k_rope).  It runs on the 5th-generation
+// tensor cores: one tcgen05.mma (M=128, N=w, K=16, bf16 in, fp32 out) per 16
+// ranks, accumulator in TMEM.  Everything else streams through shared memory:
 //
-//   warp 0  producer   canonical rows -> shared memory with bulk async copies
-//                      (one per row, completion counted on an mbarrier); the
-//                      U tile and V_m (per job) with 16-byte async copies into
-//                      the 128-byte-swizzled K-major operand layout; the
-//                      per-chunk cos/sin table (fp64-reduced phase).
-//   warp 1  MMA        TMEM allocation; one elected lane issues the MMAs and
-//                      commits them to mbarriers.
-//   warps 2-5 epilogue thread = token row = TMEM lane: tcgen05.ld the patch,
-//                      read the canonical row from shared memory, rotate the
-//                      RoPE pairs in fp32, add, round once to bf16, write the
-//                      row back in place and scatter it to its pool slot with
-//                      one bulk async store.
+//   warp 0    producer: canonical rows of the tile with tiled TMA loads from a
+//             tensor map of the store (128B-swizzled boxes of 64 columns x 128
+//             rows; 16-row boxes for the ragged tail) and the per-chunk
+//             cos/sin table (phase formed and reduced in fp64).
+//   warp 1    operands + MMA: 16-byte async copies build the U tile and V_m in
+//             the 128B-swizzled K-major layout ahead of use; the copying lanes
+//             fence their writes into the async proxy; one lane issues the
+//             MMAs and commits them to mbarriers.  Also owns TMEM.
+//   warps 2-9 epilogue: two warps per TMEM sub-partition, each owning half of
+//             the columns (whole RoPE pairs) of the same 32 token rows; thread
+//             = token row = TMEM lane.  tcgen05.ld the patch, read the canonical
+//             row (swizzled, conflict-free), rotate the RoPE pairs in fp32, add,
+//             round once to bf16 and write back in place; then each warp stores
+//             its columns of its 32 rows to their pool slots with coalesced
+//             16-byte stores.
 //
-// Stages: S shared-memory stages (tile data), 2 V_m buffers (job data), 2
-// TMEM accumulators.  The grid is persistent (one CTA per SM); the tiles of a
-// call, ordered (layer, segment, chunk, tile), are split into equal
-// contiguous ranges, so consecutive tiles of a CTA share V_m.  Every wait is
+// The grid is persistent (one CTA per SM).  The tiles of a call, ordered
+// (layer, segment, chunk, tile), are split into equal contiguous ranges, so
+// consecutive tiles of a CTA share V_m and the cos/sin table.  Every wait is
 // bounded in time: on expiry the CTA records KAMERA_DEVERR_TIMEOUT, drains its
 // own copies and MMAs, frees TMEM and returns.
 #include <cstdint>
+#include <cstring>
+#include <cuda.h>
 #include <cuda_bf16.h>
+#include <cudaTypedefs.h>
 
 #include "kamera_common.cuh"
 #include "kamera_internal.h"
@@ -38,23 +43,36 @@ namespace kamera {
 
 namespace {
 
-constexpr int kTileM = 128;                   // tokens per tile = UMMA M = TMEM lanes
-constexpr int kWMax = 128;                    // widest segment = UMMA N
-constexpr int kRowPitch = kWMax * 2 + 16;     // padded row: conflict-free row-per-thread access
-constexpr int kAtomBytes = kTileM * 128;      // one 64-rank K atom of the U tile
-constexpr int kThreads = 192;
-constexpr int kTableBytes = kWMax / 2 * 8;    // float2 per frequency
-constexpr uint32_t kTmemCols = 2 * kWMax;     // two accumulators
+constexpr int kTileM = 128;                     // tokens per tile = UMMA M = TMEM lanes
+constexpr int kWMax = 128;                      // widest segment = UMMA N
+constexpr int kHalfBytes = kTileM * 128;        // one 64-column swizzled box of 128 rows
+constexpr int kRowsBytes = 2 * kHalfBytes;      // canonical rows of a tile (w <= 128)
+constexpr int kStageBytes = kRowsBytes + 1024;  // rows + cos/sin table (64 float2), 1024-aligned
+constexpr int kAtomBytes = kTileM * 128;        // one 64-rank K atom of a 128-row operand
+constexpr int kThreads = 320;                  // producer, MMA, 8 epilogue warps
+constexpr int kEpiWarps = 8;
+constexpr uint32_t kTmemCols = 2 * kWMax;       // two accumulators
 constexpr uint64_t kTimeoutNs = 1000000000ull;
+constexpr int kTailRows = 16;                   // box height of the tail tensor maps
 
 struct UmmaParams {
+    CUtensorMap map_full[2];   // per array (K|V, or the MLA row): 64 x 128 boxes
+    CUtensorMap map_tail[2];   // 64 x 16 boxes
     RowsParams r;
     int32_t family;
-    int32_t Z;            // row segments
-    int32_t KA;           // 64-rank K atoms per operand tile (1 or 2)
-    int32_t S;            // shared-memory stages
-    uint32_t stage_bytes;
-    uint32_t vm_bytes;    // one V_m buffer
+    int32_t Z;                 // row segments
+};
+
+template <int KA>
+struct Geometry {
+    static constexpr int LA = KA == 1 ? 2 : 1;  // operand lookahead (tiles)
+    static constexpr int D = LA + 1;            // U operand buffers
+    static constexpr int S = KA == 1 ? 4 : 2;   // row stages
+    static constexpr int kUBytes = KA * kAtomBytes;
+    static constexpr int kVBytes = KA * kWMax * 128;
+    static constexpr int kUOff = S * kStageBytes;
+    static constexpr int kVOff = kUOff + D * kUBytes;
+    static constexpr int kSharedOff = kVOff + 2 * kVBytes;
 };
 
 struct Seg {
@@ -133,7 +151,7 @@ struct Cursor {
 };
 
 struct Shared {
-    uint64_t full[4], empty[4], tfull[2], tempty[2], vmempty[2], mmadone;
+    uint64_t full[4], empty[4], tfull[2], tempty[2], uempty[3], vmempty[2], mmadone;
     uint32_t tmem_base;
     int32_t abort_flag;
     int32_t start_lz, start_rem, start_c, start_t, count;
@@ -161,6 +179,13 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
     }
 }
 
+// The whole warp waits; a timeout seen by any lane is seen by all (the abort
+// flag reaches every polling lane), so the result is warp-uniform.
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag, int32_t* err)
+{
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, err)) != 0;
+}
+
 // time-bounded wait that ignores the abort flag (used while draining)
 __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity)
 {
@@ -170,31 +195,59 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity)
             return;
 }
 
-// Copies `rows` rows of an [*, m] bf16 factor (row stride m) into the
-// 128B-swizzled K-major operand layout at `dst` (atom stride atom_bytes),
-// zero-filling ranks m..mpad-1.  Lanes of one warp share the work.
+// Byte offset of the 16-byte piece (row r, piece kc) in a 128B-swizzled
+// K-major operand with atoms of `atom_bytes` (64 ranks per atom).
+__device__ __forceinline__ uint32_t operand_offset(int r, int kc, uint32_t atom_bytes)
+{
+    return (kc >> 3) * atom_bytes + r * 128 + ((((kc & 7) ^ (r & 7))) << 4);
+}
+
+// Copies `rows` rows of a [*, m] bf16 factor (row stride m) into the
+// 128B-swizzled K-major operand layout at `dst`, zero-filling ranks
+// m..mpad-1, in async copies of G bytes (G divides the 2m-byte row, so every
+// piece stays inside one 16-byte chunk of the swizzled layout).  The 32 lanes
+// of the calling warp share the work.
+template <int G>
+__device__ __forceinline__ void load_operand_g(uint32_t dst, const __nv_bfloat16* src, int rows, int m, int mpad,
+                                               uint32_t atom_bytes, int lane)
+{
+    constexpr int E = G / 2;   // elements per piece
+    const int pr = m / E, pp = (mpad - m) / E;
+    for (int p = lane; p < rows * pr; p += 32) {
+        const int r = p / pr, k = (p - r * pr) * E;
+        const uint32_t d = dst + operand_offset(r, k >> 3, atom_bytes) + (k & 7) * 2;
+        if constexpr (G == 16)
+            ptx::cp_async16(d, src + (size_t)r * m + k);
+        else
+            ptx::cp_async_small<G>(d, src + (size_t)r * m + k);
+    }
+    for (int p = lane; p < rows * pp; p += 32) {
+        const int r = p / pp, k = m + (p - r * pp) * E;
+        const uint32_t d = dst + operand_offset(r, k >> 3, atom_bytes) + (k & 7) * 2;
+        if constexpr (G == 16)
+            ptx::st_shared_zero16(d);
+        else if constexpr (G == 8)
+            asm volatile("st.shared.v2.u32 [%0], {%1, %1};" ::"r"(d), "r"(0) : "memory");
+        else
+            asm volatile("st.shared.u32 [%0], %1;" ::"r"(d), "r"(0) : "memory");
+    }
+}
+
 __device__ __forceinline__ void load_operand(uint32_t dst, const __nv_bfloat16* src, int rows, int m, int mpad,
                                              uint32_t atom_bytes, int lane)
 {
     if ((m & 7) == 0) {
-        const int pr = m >> 3;               // 16-byte pieces per row
-        for (int p = lane; p < rows * pr; p += 32) {
-            const int r = p / pr, kc = p - r * pr;
-            const uint32_t d = dst + (kc >> 3) * atom_bytes + r * 128 + ((((kc & 7) ^ (r & 7))) << 4);
-            ptx::cp_async16(d, src + (size_t)r * m + kc * 8);
-        }
-        const int pp = (mpad - m) >> 3;
-        for (int p = lane; p < rows * pp; p += 32) {
-            const int r = p / pp, kc = (m >> 3) + (p - r * pp);
-            ptx::st_shared_zero16(dst + (kc >> 3) * atom_bytes + r * 128 + ((((kc & 7) ^ (r & 7))) << 4));
-        }
-    } else {
+        load_operand_g<16>(dst, src, rows, m, mpad, atom_bytes, lane);
+    } else if ((m & 3) == 0) {
+        load_operand_g<8>(dst, src, rows, m, mpad, atom_bytes, lane);
+    } else if ((m & 1) == 0) {
+        load_operand_g<4>(dst, src, rows, m, mpad, atom_bytes, lane);
+    } else {   // odd rank: rows are only 2-byte aligned
         const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
         for (int p = lane; p < rows * mpad; p += 32) {
             const int r = p / mpad, k = p - r * mpad;
             const uint16_t v = k < m ? s16[(size_t)r * m + k] : (uint16_t)0;
-            const int kc = k >> 3;
-            ptx::st_shared_u16(dst + (kc >> 3) * atom_bytes + r * 128 + ((((kc & 7) ^ (r & 7))) << 4) + (k & 7) * 2, v);
+            ptx::st_shared_u16(dst + operand_offset(r, k >> 3, atom_bytes) + (k & 7) * 2, v);
         }
     }
 }
@@ -202,21 +255,18 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const __nv_bfloat16* 
 __device__ __forceinline__ float f_lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float f_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
 
-__device__ __forceinline__ void lds128(uint32_t a, uint32_t (&v)[4])
+// Address of the 16-byte piece holding columns [8q, 8q+8) of row tt in the
+// canonical-row area (two 64-column swizzled boxes).
+__device__ __forceinline__ uint32_t row_piece(uint32_t rows, int tt, int q)
 {
-    asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v[0]), "=r"(v[1]), "=r"(v[2]), "=r"(v[3]) : "r"(a));
-}
-__device__ __forceinline__ void sts128(uint32_t a, uint32_t x, uint32_t y, uint32_t z, uint32_t w)
-{
-    asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(a), "r"(x), "r"(y), "r"(z), "r"(w) : "memory");
+    return rows + (q >> 3) * kHalfBytes + tt * 128 + ((((q & 7) ^ (tt & 7))) << 4);
 }
 
-// 16 consecutive bf16 of a shared row -> fp32
-__device__ __forceinline__ void load16(uint32_t a, float* f)
+__device__ __forceinline__ void load16(uint32_t rows, int tt, int c, float* f)
 {
     uint32_t v[4], u[4];
-    lds128(a, v);
-    lds128(a + 16, u);
+    ptx::lds128(row_piece(rows, tt, c >> 3), v);
+    ptx::lds128(row_piece(rows, tt, (c >> 3) + 1), u);
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
         f[2 * i] = f_lo(v[i]);
@@ -226,24 +276,25 @@ __device__ __forceinline__ void load16(uint32_t a, float* f)
     }
 }
 
-__device__ __forceinline__ void store16(uint32_t a, const float* f)
+__device__ __forceinline__ void store16(uint32_t rows, int tt, int c, const float* f)
 {
-    sts128(a, pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]), pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-    sts128(a + 16, pack_bf16x2(f[8], f[9]), pack_bf16x2(f[10], f[11]), pack_bf16x2(f[12], f[13]),
-           pack_bf16x2(f[14], f[15]));
+    ptx::sts128(row_piece(rows, tt, c >> 3), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
+                pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
+    ptx::sts128(row_piece(rows, tt, (c >> 3) + 1), pack_bf16x2(f[8], f[9]), pack_bf16x2(f[10], f[11]),
+                pack_bf16x2(f[12], f[13]), pack_bf16x2(f[14], f[15]));
 }
 
 }  // namespace
 
+template <int KA>
 __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const __grid_constant__ UmmaParams p)
 {
+    using G = Geometry<KA>;
     extern __shared__ uint8_t smem_raw[];
-    // 1024-byte aligned base for the swizzled operand tiles
     const uint32_t raw = ptx::smem_addr(smem_raw);
-    const uint32_t base = (raw + 1023u) & ~1023u;
+    const uint32_t base = (raw + 1023u) & ~1023u;   // swizzle atoms need 1024-byte alignment
     uint8_t* gbase = smem_raw + (base - raw);
-    const uint32_t vm_base = base + p.S * p.stage_bytes;
-    Shared& sh = *reinterpret_cast<Shared*>(gbase + p.S * p.stage_bytes + 2 * p.vm_bytes);
+    Shared& sh = *reinterpret_cast<Shared*>(gbase + G::kSharedOff);
     volatile int32_t* abort_flag = &sh.abort_flag;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -251,20 +302,28 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
 
     // ---------------------------------------------------------- prologue
     if (tid == 0) {
-        for (int i = 0; i < p.S; ++i) {
-            ptx::mbar_init(ptx::smem_addr(&sh.full[i]), 2);
-            ptx::mbar_init(ptx::smem_addr(&sh.empty[i]), 4);
+        for (int i = 0; i < G::S; ++i) {
+            ptx::mbar_init(ptx::smem_addr(&sh.full[i]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sh.empty[i]), kEpiWarps);
             sh.stage_tag[i] = -1;
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(ptx::smem_addr(&sh.tfull[i]), 1);
-            ptx::mbar_init(ptx::smem_addr(&sh.tempty[i]), 4);
+            ptx::mbar_init(ptx::smem_addr(&sh.tempty[i]), kEpiWarps);
             ptx::mbar_init(ptx::smem_addr(&sh.vmempty[i]), 1);
         }
+        for (int i = 0; i < G::D; ++i)
+            ptx::mbar_init(ptx::smem_addr(&sh.uempty[i]), 1);
         ptx::mbar_init(ptx::smem_addr(&sh.mmadone), 1);
         sh.abort_flag = 0;
         ptx::fence_barrier_init();
         ptx::fence_proxy_async();
+    }
+    if (tid == 32) {
+        for (int i = 0; i < 2; ++i) {
+            ptx::prefetch_tmap(&p.map_full[i]);
+            ptx::prefetch_tmap(&p.map_tail[i]);
+        }
     }
     // tiles per chunk: each thread sums a contiguous block of chunks
     const int n = r.n_chunks;
@@ -335,43 +394,23 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
     if (count > 0)
         cur.load(p);
 
-    const int KA = p.KA;
+    const uint32_t ubase = base + G::kUOff, vbase = base + G::kVOff;
+
     if (warp == 0 && count > 0) {
         // ------------------------------------------------------ producer
-        int pending = -1, issued = 0, vjobs = -1;
-        int prev_lz = -1, prev_c = -1;
+        int issued = 0;
         for (int i = 0; i < count; ++i, cur.next(p)) {
-            const int s = i % p.S, rnd = i / p.S;
-            if (!wait_bar(ptx::smem_addr(&sh.empty[s]), (rnd & 1) ^ 1, abort_flag, r.err))
+            const int s = i % G::S, rnd = i / G::S;
+            if (!warp_wait(ptx::smem_addr(&sh.empty[s]), (rnd & 1) ^ 1, abort_flag, r.err))
                 break;
             const int l = cur.lz / p.Z, z = cur.lz - l * p.Z;
             const Seg sg = segment(p, z);
             const KameraChunk& ch = cur.ch;
             const int tok0 = cur.t * kTileM;
             const int ntok = min(kTileM, ch.len - tok0);
-            const int m = ch.rank, mpad = (m + 15) & ~15;
-            const uint32_t st = base + s * p.stage_bytes;
-            const bool new_job = cur.lz != prev_lz || cur.c != prev_c;
-            prev_lz = cur.lz;
-            prev_c = cur.c;
-            if (m > 0) {
-                const int64_t lh = (int64_t)l * sg.FH + sg.fh;
-                if (new_job) {
-                    ++vjobs;
-                    const int b = vjobs & 1;
-                    if (!wait_bar(ptx::smem_addr(&sh.vmempty[b]), ((vjobs >> 1) & 1) ^ 1, abort_flag, r.err))
-                        break;
-                    const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(ch.patch_ptrs[sg.v_idx]);
-                    load_operand(vm_base + b * p.vm_bytes, V + (lh * sg.vm_rows + sg.vm_row0) * m, sg.w, m, mpad,
-                                 (uint32_t)sg.w * 128u, lane);
-                }
-                const __nv_bfloat16* U = static_cast<const __nv_bfloat16*>(ch.patch_ptrs[sg.u_idx]);
-                load_operand(st, U + (lh * ch.len + tok0) * m, ntok, m, mpad, kAtomBytes, lane);
-            }
-            ptx::cp_async_commit();
             const bool rot = sg.rot && ch.delta != 0;
             if (rot && sh.stage_tag[s] != cur.c) {
-                float2* cs = reinterpret_cast<float2*>(gbase + s * p.stage_bytes + KA * kAtomBytes + kTileM * kRowPitch);
+                float2* cs = reinterpret_cast<float2*>(gbase + s * kStageBytes + kRowsBytes);
                 for (int f = lane; f < r.rope.n_freq; f += 32) {
                     float c_, s_;
                     phase_cos_sin(ch.delta, r.rope.inv_freq[f], c_, s_);
@@ -382,94 +421,146 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
                     sh.stage_tag[s] = cur.c;
             }
             __syncwarp();
-            const uint32_t full = ptx::smem_addr(&sh.full[s]);
-            const uint32_t row_bytes = (uint32_t)sg.w * 2u;
-            if (lane == 0)
-                ptx::mbar_arrive_expect_tx(full, row_bytes * (uint32_t)ntok);
-            __syncwarp();
-            const __nv_bfloat16* src = (sg.array == 0 ? r.src_k : r.src_v) + (int64_t)l * r.src_ls +
-                                       (ch.src_offset + tok0) * r.src_rs + sg.e0;
-            const uint32_t rows_s = st + KA * kAtomBytes;
-            for (int tt = lane; tt < ntok; tt += 32)
-                ptx::bulk_g2s(rows_s + tt * kRowPitch, src + (int64_t)tt * r.src_rs, row_bytes, full);
-            ++issued;
-            if (pending >= 0) {   // operand copies of the previous tile are complete: publish them
-                ptx::cp_async_wait<1>();
-                ptx::fence_proxy_async();
-                __syncwarp();
-                if (lane == 0)
-                    ptx::mbar_arrive(ptx::smem_addr(&sh.full[pending]));
+            if (lane == 0) {
+                const uint32_t full = ptx::smem_addr(&sh.full[s]);
+                const uint32_t rows = base + s * kStageBytes;
+                const int nx = sg.w >> 6;   // 64-column boxes
+                const int y = (int)(ch.src_offset + tok0);
+                if (ntok == kTileM) {
+                    ptx::mbar_arrive_expect_tx(full, (uint32_t)(nx * kHalfBytes));
+                    for (int x = 0; x < nx; ++x)
+                        ptx::tma_load_3d(rows + x * kHalfBytes, &p.map_full[sg.array], sg.e0 + 64 * x, y, l, full);
+                } else {
+                    const int nb = (ntok + kTailRows - 1) / kTailRows;
+                    ptx::mbar_arrive_expect_tx(full, (uint32_t)(nx * nb * kTailRows * 128));
+                    for (int x = 0; x < nx; ++x)
+                        for (int b = 0; b < nb; ++b)
+                            ptx::tma_load_3d(rows + x * kHalfBytes + b * kTailRows * 128, &p.map_tail[sg.array],
+                                             sg.e0 + 64 * x, y + b * kTailRows, l, full);
+                }
             }
-            pending = s;
+            __syncwarp();
+            ++issued;
+        }
+        // no TMA load may still be writing shared memory when the CTA exits
+        if (lane == 0)
+            for (int j = max(0, issued - G::S); j < issued; ++j)
+                drain_bar(ptx::smem_addr(&sh.full[j % G::S]), (j / G::S) & 1);
+        __syncwarp();
+    } else if (warp == 1 && count > 0) {
+        // ------------------------------------------- operands + MMA
+        Cursor ld = cur;   // load cursor, LA tiles ahead of the MMA cursor
+        int ld_i = 0, ld_u = 0, ld_v = -1, ld_plz = -1, ld_pc = -1;
+        bool stop = false;
+        // operand copies of the load cursor's next tile (always one commit group)
+        auto issue = [&]() {
+            if (ld_i < count && !stop) {
+                const int l = ld.lz / p.Z, z = ld.lz - l * p.Z;
+                const Seg sg = segment(p, z);
+                const KameraChunk& ch = ld.ch;
+                const int m = ch.rank, mpad = (m + 15) & ~15;
+                const bool new_job = ld.lz != ld_plz || ld.c != ld_pc;
+                ld_plz = ld.lz;
+                ld_pc = ld.c;
+                if (m > 0) {
+                    const int64_t lh = (int64_t)l * sg.FH + sg.fh;
+                    if (new_job) {
+                        ++ld_v;
+                        if (!warp_wait(ptx::smem_addr(&sh.vmempty[ld_v & 1]), ((ld_v >> 1) & 1) ^ 1, abort_flag,
+                                       r.err))
+                            stop = true;
+                        else
+                            load_operand(vbase + (ld_v & 1) * G::kVBytes,
+                                         static_cast<const __nv_bfloat16*>(ch.patch_ptrs[sg.v_idx]) +
+                                             (lh * sg.vm_rows + sg.vm_row0) * m,
+                                         sg.w, m, mpad, (uint32_t)sg.w * 128u, lane);
+                    }
+                    const int u = ld_u % G::D;
+                    if (!stop && !warp_wait(ptx::smem_addr(&sh.uempty[u]), ((ld_u / G::D) & 1) ^ 1, abort_flag, r.err))
+                        stop = true;
+                    if (!stop) {
+                        const int tok0 = ld.t * kTileM;
+                        load_operand(ubase + u * G::kUBytes,
+                                     static_cast<const __nv_bfloat16*>(ch.patch_ptrs[sg.u_idx]) +
+                                         (lh * ch.len + tok0) * m,
+                                     min(kTileM, ch.len - tok0), m, mpad, kAtomBytes, lane);
+                    }
+                    ++ld_u;
+                }
+                ++ld_i;
+                ld.next(p);
+            }
+            ptx::cp_async_commit();
+        };
+        for (int j = 0; j < G::LA; ++j)
+            issue();
+        int k = 0, vjob = -1, plz = -1, pc = -1, issued_mma = 0;
+        for (int i = 0; i < count && !stop; ++i) {
+            ptx::cp_async_wait<G::LA - 1>();   // this tile's operand copies have landed ...
+            ptx::fence_proxy_async();          // ... and are visible to the tensor cores
+            __syncwarp();
+            const int l = cur.lz / p.Z, z = cur.lz - l * p.Z;
+            const Seg sg = segment(p, z);
+            const int m = cur.ch.rank;
+            const bool new_job = cur.lz != plz || cur.c != pc;
+            plz = cur.lz;
+            pc = cur.c;
+            const int lz_now = cur.lz, c_now = cur.c;
+            cur.next(p);
+            const bool last_of_job = (i == count - 1) || cur.lz != lz_now || cur.c != c_now;
+            if (m > 0) {
+                if (new_job)
+                    ++vjob;
+                if (lane == 0) {
+                    const int acc = k & 1;
+                    if (!wait_bar(ptx::smem_addr(&sh.tempty[acc]), ((k >> 1) & 1) ^ 1, abort_flag, r.err)) {
+                        stop = true;
+                    } else {
+                        ptx::tc_fence_after();
+                        const uint32_t a0 = ubase + (k % G::D) * G::kUBytes;
+                        const uint32_t b0 = vbase + (vjob & 1) * G::kVBytes;
+                        const uint32_t idesc = ptx::idesc_bf16_f32(kTileM, sg.w);
+                        const uint32_t d = tmem + acc * kWMax;
+                        const int steps = (m + 15) >> 4;
+                        for (int q = 0; q < steps; ++q) {
+                            const uint32_t koff = (q & 3) * 32;
+                            const uint64_t ad = ptx::desc_k_sw128(a0 + (q >> 2) * kAtomBytes + koff);
+                            const uint64_t bd = ptx::desc_k_sw128(b0 + (q >> 2) * (uint32_t)sg.w * 128u + koff);
+                            ptx::umma_bf16(d, ad, bd, idesc, q > 0 ? 1u : 0u);
+                        }
+                        ptx::umma_commit(ptx::smem_addr(&sh.tfull[acc]));
+                        ptx::umma_commit(ptx::smem_addr(&sh.uempty[k % G::D]));
+                        if (last_of_job)
+                            ptx::umma_commit(ptx::smem_addr(&sh.vmempty[vjob & 1]));
+                        ++issued_mma;
+                    }
+                }
+                ++k;
+                stop = __shfl_sync(0xffffffffu, stop ? 1 : 0, 0) != 0;
+            }
+            issue();
         }
         ptx::cp_async_wait<0>();
-        ptx::fence_proxy_async();
-        __syncwarp();
-        if (pending >= 0 && lane == 0)
-            ptx::mbar_arrive(ptx::smem_addr(&sh.full[pending]));
-        // no bulk load may still be writing shared memory when the CTA exits
-        for (int j = max(0, issued - p.S); j < issued; ++j)
-            drain_bar(ptx::smem_addr(&sh.full[j % p.S]), (j / p.S) & 1);
-    } else if (warp == 1 && count > 0) {
-        // ----------------------------------------------------------- MMA
-        if (lane == 0) {
-            int k = 0, vjobs = -1, issued_mma = 0;
-            int prev_lz = -1, prev_c = -1;
-            for (int i = 0; i < count; ++i) {
-                const int s = i % p.S, rnd = i / p.S;
-                const int l = cur.lz / p.Z, z = cur.lz - l * p.Z;
-                const Seg sg = segment(p, z);
-                const int m = cur.ch.rank;
-                const bool new_job = cur.lz != prev_lz || cur.c != prev_c;
-                prev_lz = cur.lz;
-                prev_c = cur.c;
-                const int lz_now = cur.lz, c_now = cur.c;
-                cur.next(p);
-                const bool last_of_job = (i == count - 1) || cur.lz != lz_now || cur.c != c_now;
-                (void)l;
-                if (m == 0)
-                    continue;
-                if (new_job)
-                    ++vjobs;
-                const int acc = k & 1;
-                if (!wait_bar(ptx::smem_addr(&sh.tempty[acc]), ((k >> 1) & 1) ^ 1, abort_flag, r.err))
-                    break;
-                if (!wait_bar(ptx::smem_addr(&sh.full[s]), rnd & 1, abort_flag, r.err))
-                    break;
-                ptx::tc_fence_after();
-                const uint32_t a0 = base + s * p.stage_bytes;
-                const uint32_t b0 = vm_base + (vjobs & 1) * p.vm_bytes;
-                const uint32_t idesc = ptx::idesc_bf16_f32(kTileM, sg.w);
-                const uint32_t d = tmem + acc * kWMax;
-                const int steps = (m + 15) >> 4;
-                for (int q = 0; q < steps; ++q) {
-                    const uint32_t koff = (q & 3) * 32;
-                    const uint64_t ad = ptx::desc_k_sw128(a0 + (q >> 2) * kAtomBytes + koff);
-                    const uint64_t bd = ptx::desc_k_sw128(b0 + (q >> 2) * (uint32_t)sg.w * 128u + koff);
-                    ptx::umma_bf16(d, ad, bd, idesc, q > 0 ? 1u : 0u);
-                }
-                ptx::umma_commit(ptx::smem_addr(&sh.tfull[acc]));
-                if (last_of_job)
-                    ptx::umma_commit(ptx::smem_addr(&sh.vmempty[vjobs & 1]));
-                ++k;
-                ++issued_mma;
-            }
-            if (issued_mma) {   // every MMA done before TMEM is freed
-                ptx::umma_commit(ptx::smem_addr(&sh.mmadone));
-                drain_bar(ptx::smem_addr(&sh.mmadone), 0);
-            }
+        if (lane == 0 && issued_mma) {   // every MMA done before TMEM is freed
+            ptx::umma_commit(ptx::smem_addr(&sh.mmadone));
+            drain_bar(ptx::smem_addr(&sh.mmadone), 0);
         }
         __syncwarp();
     } else if (warp >= 2 && count > 0) {
         // ------------------------------------------------------ epilogue
-        const int q = warp & 3;                 // TMEM sub-partition of this warp
-        const int tt = q * 32 + lane;           // token row of the tile = TMEM lane
+        const int q = warp & 3;         // TMEM sub-partition of this warp
+        const int hh = (warp - 2) >> 2; // which half of the columns this warp owns
+        const int tt = q * 32 + lane;   // token row of the tile = TMEM lane
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         int k = 0;
-        for (int i = 0; i < count; ++i, cur.next(p)) {
-            const int s = i % p.S, rnd = i / p.S;
-            if (!wait_bar(ptx::smem_addr(&sh.full[s]), rnd & 1, abort_flag, r.err))
-                break;
+        int64_t slot_next = -1;
+        {
+            const int ntok = min(kTileM, cur.ch.len - cur.t * kTileM);
+            if (tt < ntok)
+                slot_next = cur.ch.dst_slot_mapping[cur.t * kTileM + tt];
+        }
+        for (int i = 0; i < count; ++i) {
+            const int s = i % G::S, rnd = i / G::S;
             const int l = cur.lz / p.Z, z = cur.lz - l * p.Z;
             const Seg sg = segment(p, z);
             const KameraChunk& ch = cur.ch;
@@ -477,36 +568,34 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
             const int ntok = min(kTileM, ch.len - tok0);
             const int m = ch.rank;
             const bool rot = sg.rot && ch.delta != 0;
+            int64_t slot = tt < ntok ? slot_next : -1;
+            if (slot >= r.num_slots || (tt < ntok && slot < 0)) {
+                raise_err(r.err, KAMERA_DEVERR_SLOT);
+                slot = -1;
+            }
+            const bool valid = slot >= 0;
+            if (!warp_wait(ptx::smem_addr(&sh.full[s]), rnd & 1, abort_flag, r.err))
+                break;
             const int acc = k & 1;
             if (m > 0) {
-                if (!wait_bar(ptx::smem_addr(&sh.tfull[acc]), (k >> 1) & 1, abort_flag, r.err))
+                if (!warp_wait(ptx::smem_addr(&sh.tfull[acc]), (k >> 1) & 1, abort_flag, r.err))
                     break;
                 ptx::tc_fence_after();
             }
-            bool valid = tt < ntok;
-            int64_t slot = 0;
-            if (valid) {
-                slot = ch.dst_slot_mapping[tok0 + tt];
-                if (slot < 0 || slot >= r.num_slots) {
-                    raise_err(r.err, KAMERA_DEVERR_SLOT);
-                    valid = false;
-                }
-            }
-            const uint32_t row = base + s * p.stage_bytes + KA * kAtomBytes + tt * kRowPitch;
-            const float2* cs =
-                reinterpret_cast<const float2*>(gbase + s * p.stage_bytes + KA * kAtomBytes + kTileM * kRowPitch);
+            const uint32_t rows = base + s * kStageBytes;
+            const float2* cs = reinterpret_cast<const float2*>(gbase + s * kStageBytes + kRowsBytes);
             const uint32_t tacc = tmem + lane_addr + acc * kWMax;
             if (m > 0 || rot) {
                 if (rot && r.rope.pairing == KAMERA_ROPE_ROTATE_HALF) {
                     const int half = sg.w >> 1;
-                    for (int cb = 0; cb < half; cb += 16) {
+                    for (int cb = hh * (half >> 1); cb < (hh + 1) * (half >> 1); cb += 16) {
                         uint32_t pa[16], pb[16];
                         if (m > 0)
                             ptx::tmem_ld16x2(tacc + cb, tacc + cb + half, pa, pb);
                         if (valid) {
                             float xa[16], xb[16];
-                            load16(row + cb * 2, xa);
-                            load16(row + (cb + half) * 2, xb);
+                            load16(rows, tt, cb, xa);
+                            load16(rows, tt, cb + half, xb);
 #pragma unroll
                             for (int e = 0; e < 16; ++e) {
                                 const float2 t = cs[cb + e];
@@ -519,19 +608,19 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
                                 xa[e] = oa;
                                 xb[e] = ob;
                             }
-                            store16(row + cb * 2, xa);
-                            store16(row + (cb + half) * 2, xb);
+                            store16(rows, tt, cb, xa);
+                            store16(rows, tt, cb + half, xb);
                         }
                     }
                 } else {
-                    for (int cb = 0; cb < sg.w; cb += 32) {
+                    for (int cb = hh * (sg.w >> 1); cb < (hh + 1) * (sg.w >> 1); cb += 32) {
                         uint32_t pa[16], pb[16];
                         if (m > 0)
                             ptx::tmem_ld16x2(tacc + cb, tacc + cb + 16, pa, pb);
                         if (valid) {
                             float xa[16], xb[16];
-                            load16(row + cb * 2, xa);
-                            load16(row + (cb + 16) * 2, xb);
+                            load16(rows, tt, cb, xa);
+                            load16(rows, tt, cb + 16, xb);
                             if (rot) {   // interleaved pairs (2i, 2i+1), frequency cb/2 + i
 #pragma unroll
                                 for (int e = 0; e < 8; ++e) {
@@ -552,8 +641,8 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
                                     xb[e] += __uint_as_float(pb[e]);
                                 }
                             }
-                            store16(row + cb * 2, xa);
-                            store16(row + (cb + 16) * 2, xb);
+                            store16(rows, tt, cb, xa);
+                            store16(rows, tt, cb + 16, xb);
                         }
                     }
                 }
@@ -565,18 +654,41 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
                     ptx::mbar_arrive(ptx::smem_addr(&sh.tempty[acc]));
                 ++k;
             }
-            if (valid) {
-                ptx::fence_proxy_async();
-                __nv_bfloat16* dst = (sg.array == 0 ? r.dst_k : r.dst_v) + (int64_t)l * r.dst_ls + slot * r.dst_ss + sg.e0;
-                ptx::bulk_s2g(dst, row, (uint32_t)sg.w * 2u);
-                ptx::bulk_commit();
+            __syncwarp();
+            // this warp's columns of its 32 rows -> pool slots, coalesced 16-byte pieces
+            {
+                const int ppr = sg.w >> 4;   // pieces per row owned by this warp (8 or 4)
+                const int rpi = 32 / ppr;    // rows per warp instruction
+                const int j = lane % ppr;
+                int piece;
+                if (rot && r.rope.pairing == KAMERA_ROPE_ROTATE_HALF) {
+                    const int quarter = ppr >> 1;   // first half-row pieces, then their partners
+                    piece = j < quarter ? hh * quarter + j : ppr + hh * quarter + (j - quarter);
+                } else {
+                    piece = hh * ppr + j;
+                }
+                __nv_bfloat16* dbase =
+                    (sg.array == 0 ? r.dst_k : r.dst_v) + (int64_t)l * r.dst_ls + sg.e0 + piece * 8;
+                for (int i2 = 0; i2 < 32; i2 += rpi) {
+                    const int src_lane = i2 + lane / ppr;
+                    const int64_t sl = __shfl_sync(0xffffffffu, slot, src_lane);
+                    if (sl >= 0) {
+                        uint32_t v[4];
+                        ptx::lds128(row_piece(rows, q * 32 + src_lane, piece), v);
+                        ptx::stg128(dbase + sl * r.dst_ss, v);
+                    }
+                }
             }
-            ptx::bulk_wait_read_all();
+            ptx::fence_proxy_async();   // our shared-memory accesses precede the next TMA write here
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive(ptx::smem_addr(&sh.empty[s]));
+            cur.next(p);
+            if (i + 1 < count) {   // prefetch the next tile's slot
+                const int ntok2 = min(kTileM, cur.ch.len - cur.t * kTileM);
+                slot_next = tt < ntok2 ? cur.ch.dst_slot_mapping[cur.t * kTileM + tt] : -1;
+            }
         }
-        ptx::bulk_wait_all();
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -588,7 +700,7 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
 
 bool umma_supported(const RowsParams& p, int family)
 {
-    if (p.max_rank < 1 || p.max_rank > 128)
+    if (p.max_rank < 1 || p.max_rank > 128 || p.num_rows < 1)
         return false;
     if (family == FAMILY_GQA) {
         if (p.d != 64 && p.d != 128)
@@ -604,35 +716,88 @@ bool umma_supported(const RowsParams& p, int family)
     return false;
 }
 
+template <int KA>
+static size_t smem_bytes_for()
+{
+    return 1024 + (size_t)Geometry<KA>::kSharedOff + sizeof(Shared);
+}
+
 size_t umma_smem_bytes(const RowsParams& p)
 {
-    const int KA = (p.max_rank + 63) / 64;
-    const int S = KA == 1 ? 3 : 2;
-    const uint32_t stage = ((uint32_t)(KA * kAtomBytes + kTileM * kRowPitch + kTableBytes) + 1023u) & ~1023u;
-    const uint32_t vm = (uint32_t)KA * kWMax * 128u;
-    return 1024 + (size_t)S * stage + 2 * (size_t)vm + sizeof(Shared);
+    return p.max_rank > 64 ? smem_bytes_for<2>() : smem_bytes_for<1>();
 }
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn()
+{
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    if (!fn) {
+        void* f = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+    }
+    return fn;
+}
+
+// 3-D map over a strided [L][rows][width] bf16 array: boxes of 64 columns x
+// box_rows rows x 1 layer, 128-byte swizzle, out-of-range rows read as zero.
+bool make_map(CUtensorMap* m, const void* base, int64_t L, int64_t rows, int64_t width, int64_t row_stride,
+              int64_t layer_stride, int box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn)
+        return false;
+    cuuint64_t dims[3] = {(cuuint64_t)width, (cuuint64_t)rows, (cuuint64_t)L};
+    const int64_t ls = L > 1 ? layer_stride : rows * row_stride;
+    cuuint64_t strides[2] = {(cuuint64_t)row_stride * 2u, (cuuint64_t)ls * 2u};
+    cuuint32_t box[3] = {64u, (cuuint32_t)box_rows, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+}  // namespace
 
 cudaError_t launch_umma(const RowsParams& rp, int family, cudaStream_t stream)
 {
     UmmaParams p;
+    std::memset(&p, 0, sizeof(p));
     p.r = rp;
     p.family = family;
     p.Z = family == FAMILY_GQA ? 2 * rp.H : rp.kv_lora / kWMax + 1;
-    p.KA = (rp.max_rank + 63) / 64;
-    p.S = p.KA == 1 ? 3 : 2;
-    p.stage_bytes = ((uint32_t)(p.KA * kAtomBytes + kTileM * kRowPitch + kTableBytes) + 1023u) & ~1023u;
-    p.vm_bytes = (uint32_t)p.KA * kWMax * 128u;
-    const size_t smem = umma_smem_bytes(rp);
+    const int64_t width = family == FAMILY_GQA ? (int64_t)rp.H * rp.d : rp.d;
+    const void* arrays[2] = {rp.src_k, family == FAMILY_GQA ? rp.src_v : rp.src_k};
+    for (int a = 0; a < 2; ++a) {
+        if (!make_map(&p.map_full[a], arrays[a], rp.L, rp.num_rows, width, rp.src_rs, rp.src_ls, kTileM) ||
+            !make_map(&p.map_tail[a], arrays[a], rp.L, rp.num_rows, width, rp.src_rs, rp.src_ls, kTailRows))
+            return cudaErrorInvalidValue;
+    }
     int dev = 0, sms = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e == cudaSuccess)
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-    if (e == cudaSuccess)
-        e = cudaFuncSetAttribute(relocate_patch_umma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess)
         return e;
-    relocate_patch_umma_kernel<<<sms, kThreads, smem, stream>>>(p);
+    if (rp.max_rank > 64) {
+        const size_t smem = smem_bytes_for<2>();
+        e = cudaFuncSetAttribute(relocate_patch_umma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        relocate_patch_umma_kernel<2><<<sms, kThreads, smem, stream>>>(p);
+    } else {
+        const size_t smem = smem_bytes_for<1>();
+        e = cudaFuncSetAttribute(relocate_patch_umma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 (int)smem);
+        if (e != cudaSuccess)
+            return e;
+        relocate_patch_umma_kernel<1><<<sms, kThreads, smem, stream>>>(p);
+    }
     return cudaGetLastError();
 }
 
