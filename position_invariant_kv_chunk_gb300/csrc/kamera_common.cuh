@@ -100,6 +100,13 @@ __device__ __forceinline__ void phase_cos_sin(int64_t delta, double theta, float
     sincosf((float)red, &s, &c);
 }
 
+// patch_ptrs[i] without dynamic indexing (keeps a descriptor in registers)
+__device__ __forceinline__ const __nv_bfloat16* patch_ptr(const KameraChunk& ch, int i)
+{
+    const void* v = i == 0 ? ch.patch_ptrs[0] : i == 1 ? ch.patch_ptrs[1] : i == 2 ? ch.patch_ptrs[2] : ch.patch_ptrs[3];
+    return static_cast<const __nv_bfloat16*>(v);
+}
+
 // ---------------------------------------------------------------- errors --
 __device__ __forceinline__ void raise_err(int32_t* err, int32_t bits)
 {
@@ -124,12 +131,14 @@ __device__ __forceinline__ int32_t check_chunk(const KameraChunk& ch, const Rows
         if (ch.src_offset < 0 || ch.len < 0 || ch.src_offset + (int64_t)ch.len > p.num_rows)
             bits |= KAMERA_DEVERR_SOURCE;
         if (ch.rank > 0) {
+#pragma unroll
             for (int i = 0; i < 4; ++i) {
                 const uintptr_t a = reinterpret_cast<uintptr_t>(ch.patch_ptrs[i]);
                 if (a == 0 || (a & 15))
                     bits |= KAMERA_DEVERR_DESCRIPTOR;
             }
         } else if (ch.rank == 0) {
+#pragma unroll
             for (int i = 0; i < 4; ++i)
                 if (ch.patch_ptrs[i] != nullptr)
                     bits |= KAMERA_DEVERR_DESCRIPTOR;

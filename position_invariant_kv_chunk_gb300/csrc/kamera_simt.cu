@@ -154,8 +154,8 @@ __global__ void __launch_bounds__(256) rows_simt_kernel(const __grid_constant__ 
             cs[i] = make_float2(c, s);
         }
     if (m > 0) {
-        const __nv_bfloat16* U = static_cast<const __nv_bfloat16*>(ch.patch_ptrs[sg.u_idx]);
-        const __nv_bfloat16* V = static_cast<const __nv_bfloat16*>(ch.patch_ptrs[sg.v_idx]);
+        const __nv_bfloat16* U = patch_ptr(ch, sg.u_idx);
+        const __nv_bfloat16* V = patch_ptr(ch, sg.v_idx);
         const int64_t lh = (int64_t)l * sg.FH + sg.fh;
         const __nv_bfloat16* vrow = V + (lh * sg.vm_rows + sg.vm_row0) * m;
         for (int i = threadIdx.x; i < sg.w * m; i += blockDim.x) {

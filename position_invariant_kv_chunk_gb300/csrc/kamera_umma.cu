@@ -49,8 +49,9 @@ constexpr int kHalfBytes = kTileM * 128;        // one 64-column swizzled box of
 constexpr int kRowsBytes = 2 * kHalfBytes;      // canonical rows of a tile (w <= 128)
 constexpr int kStageBytes = kRowsBytes + 1024;  // rows + cos/sin table (64 float2), 1024-aligned
 constexpr int kAtomBytes = kTileM * 128;        // one 64-rank K atom of a 128-row operand
-constexpr int kThreads = 320;                  // producer, MMA, 8 epilogue warps
-constexpr int kEpiWarps = 8;
+constexpr int kEpiPerSub = 2;                   // epilogue warps per TMEM sub-partition
+constexpr int kEpiWarps = 4 * kEpiPerSub;
+constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, epilogue warps
 constexpr uint32_t kTmemCols = 2 * kWMax;       // two accumulators
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr int kTailRows = 16;                   // box height of the tail tensor maps
@@ -213,8 +214,11 @@ __device__ __forceinline__ void load_operand_g(uint32_t dst, const __nv_bfloat16
 {
     constexpr int E = G / 2;   // elements per piece
     const int pr = m / E, pp = (mpad - m) / E;
+    const bool pow2 = (pr & (pr - 1)) == 0;
+    const int sh = 31 - __clz(pr);
     for (int p = lane; p < rows * pr; p += 32) {
-        const int r = p / pr, k = (p - r * pr) * E;
+        const int r = pow2 ? p >> sh : p / pr;
+        const int k = (p - r * pr) * E;
         const uint32_t d = dst + operand_offset(r, k >> 3, atom_bytes) + (k & 7) * 2;
         if constexpr (G == 16)
             ptx::cp_async16(d, src + (size_t)r * m + k);
@@ -252,36 +256,106 @@ __device__ __forceinline__ void load_operand(uint32_t dst, const __nv_bfloat16* 
     }
 }
 
-__device__ __forceinline__ float f_lo(uint32_t w) { return __uint_as_float(w << 16); }
-__device__ __forceinline__ float f_hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }
-
-// Address of the 16-byte piece holding columns [8q, 8q+8) of row tt in the
-// canonical-row area (two 64-column swizzled boxes).
-__device__ __forceinline__ uint32_t row_piece(uint32_t rows, int tt, int q)
+// Shared address of the 16-byte piece q of row tt in a stage's canonical rows
+// (two 64-column boxes, 128-byte swizzle: piece q of row tt sits at chunk q ^ (tt & 7)).
+__device__ __forceinline__ uint32_t piece_addr(uint32_t rows, int tt, int q)
 {
     return rows + (q >> 3) * kHalfBytes + tt * 128 + ((((q & 7) ^ (tt & 7))) << 4);
 }
 
-__device__ __forceinline__ void load16(uint32_t rows, int tt, int c, float* f)
+// One thread's share of a tile row: two spans of N columns starting at a0 and
+// b0 (RoPE partners for rotate-half, else adjacent), read from TMEM (patch)
+// and from the row in shared memory, combined, rounded and written back.
+// mode: 0 no rotation, 1 rotate-half pairs (a0+i, b0+i), 2 interleaved pairs.
+// Arithmetic runs on packed fp32 pairs; per element it is the same sequence
+// of roundings as x*c + round(y*(-s)) [+ patch].  Work goes in rounds of 8
+// columns per span; in each round the shared loads (row pieces and the
+// cos/sin table) are issued before the TMEM load, so their latencies overlap.
+//   table, rotate-half: cos[64] | sin[64] | -sin[64]      (fp32, by frequency)
+//   table, interleaved: (cos, cos)[64] | (-sin, sin)[64]  (fp32 pairs)
+template <int N>
+__device__ __forceinline__ void epilogue_spans(uint32_t rows, int tt, int a0, int b0, int mode, bool patch,
+                                               uint32_t tacc, uint32_t tab, bool valid)
 {
-    uint32_t v[4], u[4];
-    ptx::lds128(row_piece(rows, tt, c >> 3), v);
-    ptx::lds128(row_piece(rows, tt, (c >> 3) + 1), u);
 #pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        f[2 * i] = f_lo(v[i]);
-        f[2 * i + 1] = f_hi(v[i]);
-        f[8 + 2 * i] = f_lo(u[i]);
-        f[8 + 2 * i + 1] = f_hi(u[i]);
+    for (int r0 = 0; r0 < N; r0 += 8) {
+        uint32_t va[4], vb[4], t0[4], t1[4], t2[4], t3[4], t4[4], t5[4];
+        if (valid) {
+            ptx::lds128(piece_addr(rows, tt, (a0 + r0) >> 3), va);
+            ptx::lds128(piece_addr(rows, tt, (b0 + r0) >> 3), vb);
+            if (mode == 1) {   // 8 frequencies f0..f0+7: cos, sin, -sin
+                const uint32_t f0 = (uint32_t)(a0 + r0) * 4u;
+                ptx::lds128(tab + f0, t0);
+                ptx::lds128(tab + f0 + 16, t1);
+                ptx::lds128(tab + 256 + f0, t2);
+                ptx::lds128(tab + 256 + f0 + 16, t3);
+                ptx::lds128(tab + 512 + f0, t4);
+                ptx::lds128(tab + 512 + f0 + 16, t5);
+            } else if (mode == 2) {   // 4 frequencies per span: (c, c) and (-s, s) pairs
+                const uint32_t fa = (uint32_t)((a0 + r0) >> 1) * 8u, fb = (uint32_t)((b0 + r0) >> 1) * 8u;
+                ptx::lds128(tab + fa, t0);
+                ptx::lds128(tab + fa + 16, t1);
+                ptx::lds128(tab + 512 + fa, t2);
+                ptx::lds128(tab + 512 + fa + 16, t3);
+                ptx::lds128(tab + fb, t4);
+                ptx::lds128(tab + fb + 16, t5);
+            }
+        }
+        uint32_t pa[8], pb[8];
+        if (patch)   // warp-collective: every lane loads, valid row or not
+            ptx::tmem_ld8x2(tacc + a0 + r0, tacc + b0 + r0, pa, pb);
+        if (!valid)
+            continue;
+        uint64_t xa[4], xb[4];
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            xa[i] = ptx::f2_from_bf16x2(va[i]);
+            xb[i] = ptx::f2_from_bf16x2(vb[i]);
+        }
+        if (mode == 1) {
+            const uint64_t c[4] = {ptx::f2_make(t0[0], t0[1]), ptx::f2_make(t0[2], t0[3]), ptx::f2_make(t1[0], t1[1]),
+                                   ptx::f2_make(t1[2], t1[3])};
+            const uint64_t sn[4] = {ptx::f2_make(t2[0], t2[1]), ptx::f2_make(t2[2], t2[3]),
+                                    ptx::f2_make(t3[0], t3[1]), ptx::f2_make(t3[2], t3[3])};
+            const uint64_t ns[4] = {ptx::f2_make(t4[0], t4[1]), ptx::f2_make(t4[2], t4[3]),
+                                    ptx::f2_make(t5[0], t5[1]), ptx::f2_make(t5[2], t5[3])};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                const uint64_t oa = ptx::f2_fma(xa[i], c[i], ptx::f2_mul(xb[i], ns[i]));
+                const uint64_t ob = ptx::f2_fma(xb[i], c[i], ptx::f2_mul(xa[i], sn[i]));
+                xa[i] = oa;
+                xb[i] = ob;
+            }
+        } else if (mode == 2) {
+            const uint64_t cca[4] = {ptx::f2_make(t0[0], t0[1]), ptx::f2_make(t0[2], t0[3]),
+                                     ptx::f2_make(t1[0], t1[1]), ptx::f2_make(t1[2], t1[3])};
+            const uint64_t ssa[4] = {ptx::f2_make(t2[0], t2[1]), ptx::f2_make(t2[2], t2[3]),
+                                     ptx::f2_make(t3[0], t3[1]), ptx::f2_make(t3[2], t3[3])};
+            uint32_t u0[4], u1[4];   // the b span's (-s, s) pairs
+            ptx::lds128(tab + 512 + (uint32_t)((b0 + r0) >> 1) * 8u, u0);
+            ptx::lds128(tab + 512 + (uint32_t)((b0 + r0) >> 1) * 8u + 16, u1);
+            const uint64_t ccb[4] = {ptx::f2_make(t4[0], t4[1]), ptx::f2_make(t4[2], t4[3]),
+                                     ptx::f2_make(t5[0], t5[1]), ptx::f2_make(t5[2], t5[3])};
+            const uint64_t ssb[4] = {ptx::f2_make(u0[0], u0[1]), ptx::f2_make(u0[2], u0[3]),
+                                     ptx::f2_make(u1[0], u1[1]), ptx::f2_make(u1[2], u1[3])};
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                xa[i] = ptx::f2_fma(xa[i], cca[i], ptx::f2_mul(ptx::f2_swap(xa[i]), ssa[i]));
+                xb[i] = ptx::f2_fma(xb[i], ccb[i], ptx::f2_mul(ptx::f2_swap(xb[i]), ssb[i]));
+            }
+        }
+        if (patch) {
+#pragma unroll
+            for (int i = 0; i < 4; ++i) {
+                xa[i] = ptx::f2_add(xa[i], ptx::f2_make(pa[2 * i], pa[2 * i + 1]));
+                xb[i] = ptx::f2_add(xb[i], ptx::f2_make(pb[2 * i], pb[2 * i + 1]));
+            }
+        }
+        ptx::sts128(piece_addr(rows, tt, (a0 + r0) >> 3), ptx::f2_to_bf16x2(xa[0]), ptx::f2_to_bf16x2(xa[1]),
+                    ptx::f2_to_bf16x2(xa[2]), ptx::f2_to_bf16x2(xa[3]));
+        ptx::sts128(piece_addr(rows, tt, (b0 + r0) >> 3), ptx::f2_to_bf16x2(xb[0]), ptx::f2_to_bf16x2(xb[1]),
+                    ptx::f2_to_bf16x2(xb[2]), ptx::f2_to_bf16x2(xb[3]));
     }
-}
-
-__device__ __forceinline__ void store16(uint32_t rows, int tt, int c, const float* f)
-{
-    ptx::sts128(row_piece(rows, tt, c >> 3), pack_bf16x2(f[0], f[1]), pack_bf16x2(f[2], f[3]),
-                pack_bf16x2(f[4], f[5]), pack_bf16x2(f[6], f[7]));
-    ptx::sts128(row_piece(rows, tt, (c >> 3) + 1), pack_bf16x2(f[8], f[9]), pack_bf16x2(f[10], f[11]),
-                pack_bf16x2(f[12], f[13]), pack_bf16x2(f[14], f[15]));
 }
 
 }  // namespace
@@ -409,12 +483,22 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
             const int tok0 = cur.t * kTileM;
             const int ntok = min(kTileM, ch.len - tok0);
             const bool rot = sg.rot && ch.delta != 0;
-            if (rot && sh.stage_tag[s] != cur.c) {
-                float2* cs = reinterpret_cast<float2*>(gbase + s * kStageBytes + kRowsBytes);
+            if (rot && sh.stage_tag[s] != cur.c) {   // cos/sin table in the epilogue's operand order
+                float* tab = reinterpret_cast<float*>(gbase + s * kStageBytes + kRowsBytes);
+                const bool half_pairs = r.rope.pairing == KAMERA_ROPE_ROTATE_HALF;
                 for (int f = lane; f < r.rope.n_freq; f += 32) {
                     float c_, s_;
                     phase_cos_sin(ch.delta, r.rope.inv_freq[f], c_, s_);
-                    cs[f] = make_float2(c_, s_);
+                    if (half_pairs) {
+                        tab[f] = c_;
+                        tab[64 + f] = s_;
+                        tab[128 + f] = -s_;
+                    } else {
+                        tab[2 * f] = c_;
+                        tab[2 * f + 1] = c_;
+                        tab[128 + 2 * f] = -s_;
+                        tab[128 + 2 * f + 1] = s_;
+                    }
                 }
                 __syncwarp();
                 if (lane == 0)
@@ -471,7 +555,7 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
                             stop = true;
                         else
                             load_operand(vbase + (ld_v & 1) * G::kVBytes,
-                                         static_cast<const __nv_bfloat16*>(ch.patch_ptrs[sg.v_idx]) +
+                                         patch_ptr(ch, sg.v_idx) +
                                              (lh * sg.vm_rows + sg.vm_row0) * m,
                                          sg.w, m, mpad, (uint32_t)sg.w * 128u, lane);
                     }
@@ -481,7 +565,7 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
                     if (!stop) {
                         const int tok0 = ld.t * kTileM;
                         load_operand(ubase + u * G::kUBytes,
-                                     static_cast<const __nv_bfloat16*>(ch.patch_ptrs[sg.u_idx]) +
+                                     patch_ptr(ch, sg.u_idx) +
                                          (lh * ch.len + tok0) * m,
                                      min(kTileM, ch.len - tok0), m, mpad, kAtomBytes, lane);
                     }
@@ -549,17 +633,32 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
     } else if (warp >= 2 && count > 0) {
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;         // TMEM sub-partition of this warp
-        const int hh = (warp - 2) >> 2; // which half of the columns this warp owns
+        const int hh = (warp - 2) >> 2; // which share of the columns this warp owns (0..kEpiPerSub-1)
         const int tt = q * 32 + lane;   // token row of the tile = TMEM lane
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         int k = 0;
-        int64_t slot_next = -1;
+        int64_t slot_cur = -1;
         {
             const int ntok = min(kTileM, cur.ch.len - cur.t * kTileM);
             if (tt < ntok)
-                slot_next = cur.ch.dst_slot_mapping[cur.t * kTileM + tt];
+                slot_cur = cur.ch.dst_slot_mapping[cur.t * kTileM + tt];
         }
         for (int i = 0; i < count; ++i) {
+            // the next tile's slot is loaded a whole tile ahead of its use
+            int64_t slot_nxt = -1;
+            if (i + 1 < count) {
+                if (cur.t + 1 < cur.ntile) {   // same chunk: the common case
+                    const int ntok2 = min(kTileM, cur.ch.len - (cur.t + 1) * kTileM);
+                    if (tt < ntok2)
+                        slot_nxt = cur.ch.dst_slot_mapping[(cur.t + 1) * kTileM + tt];
+                } else {
+                    Cursor nxt = cur;
+                    nxt.next(p);
+                    const int ntok2 = min(kTileM, nxt.ch.len - nxt.t * kTileM);
+                    if (tt < ntok2)
+                        slot_nxt = nxt.ch.dst_slot_mapping[nxt.t * kTileM + tt];
+                }
+            }
             const int s = i % G::S, rnd = i / G::S;
             const int l = cur.lz / p.Z, z = cur.lz - l * p.Z;
             const Seg sg = segment(p, z);
@@ -568,12 +667,6 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
             const int ntok = min(kTileM, ch.len - tok0);
             const int m = ch.rank;
             const bool rot = sg.rot && ch.delta != 0;
-            int64_t slot = tt < ntok ? slot_next : -1;
-            if (slot >= r.num_slots || (tt < ntok && slot < 0)) {
-                raise_err(r.err, KAMERA_DEVERR_SLOT);
-                slot = -1;
-            }
-            const bool valid = slot >= 0;
             if (!warp_wait(ptx::smem_addr(&sh.full[s]), rnd & 1, abort_flag, r.err))
                 break;
             const int acc = k & 1;
@@ -582,70 +675,26 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
                     break;
                 ptx::tc_fence_after();
             }
-            const uint32_t rows = base + s * kStageBytes;
-            const float2* cs = reinterpret_cast<const float2*>(gbase + s * kStageBytes + kRowsBytes);
+            int64_t slot = tt < ntok ? slot_cur : -1;
+            if (slot >= r.num_slots || (tt < ntok && slot < 0)) {
+                raise_err(r.err, KAMERA_DEVERR_SLOT);
+                slot = -1;
+            }
+            const bool valid = slot >= 0;
             const uint32_t tacc = tmem + lane_addr + acc * kWMax;
+            const uint32_t rows_s = base + s * kStageBytes;
+            const uint32_t cs_s = rows_s + kRowsBytes;
+            const int mode = rot ? (r.rope.pairing == KAMERA_ROPE_ROTATE_HALF ? 1 : 2) : 0;
+            // this warp's two spans of w/(2*kEpiPerSub) columns: whole RoPE pairs for
+            // rotate-half, else a contiguous 1/kEpiPerSub of the row
+            const int span = sg.w / (2 * kEpiPerSub);
+            const int a0 = mode == 1 ? hh * span : hh * 2 * span;
+            const int b0 = mode == 1 ? a0 + (sg.w >> 1) : a0 + span;
             if (m > 0 || rot) {
-                if (rot && r.rope.pairing == KAMERA_ROPE_ROTATE_HALF) {
-                    const int half = sg.w >> 1;
-                    for (int cb = hh * (half >> 1); cb < (hh + 1) * (half >> 1); cb += 16) {
-                        uint32_t pa[16], pb[16];
-                        if (m > 0)
-                            ptx::tmem_ld16x2(tacc + cb, tacc + cb + half, pa, pb);
-                        if (valid) {
-                            float xa[16], xb[16];
-                            load16(rows, tt, cb, xa);
-                            load16(rows, tt, cb + half, xb);
-#pragma unroll
-                            for (int e = 0; e < 16; ++e) {
-                                const float2 t = cs[cb + e];
-                                float oa = fmaf(xa[e], t.x, -(xb[e] * t.y));
-                                float ob = fmaf(xb[e], t.x, xa[e] * t.y);
-                                if (m > 0) {
-                                    oa += __uint_as_float(pa[e]);
-                                    ob += __uint_as_float(pb[e]);
-                                }
-                                xa[e] = oa;
-                                xb[e] = ob;
-                            }
-                            store16(rows, tt, cb, xa);
-                            store16(rows, tt, cb + half, xb);
-                        }
-                    }
-                } else {
-                    for (int cb = hh * (sg.w >> 1); cb < (hh + 1) * (sg.w >> 1); cb += 32) {
-                        uint32_t pa[16], pb[16];
-                        if (m > 0)
-                            ptx::tmem_ld16x2(tacc + cb, tacc + cb + 16, pa, pb);
-                        if (valid) {
-                            float xa[16], xb[16];
-                            load16(rows, tt, cb, xa);
-                            load16(rows, tt, cb + 16, xb);
-                            if (rot) {   // interleaved pairs (2i, 2i+1), frequency cb/2 + i
-#pragma unroll
-                                for (int e = 0; e < 8; ++e) {
-                                    const float2 t = cs[cb / 2 + e];
-                                    const float a = xa[2 * e], b = xa[2 * e + 1];
-                                    xa[2 * e] = fmaf(a, t.x, -(b * t.y));
-                                    xa[2 * e + 1] = fmaf(b, t.x, a * t.y);
-                                    const float2 u = cs[cb / 2 + 8 + e];
-                                    const float c2 = xb[2 * e], d2 = xb[2 * e + 1];
-                                    xb[2 * e] = fmaf(c2, u.x, -(d2 * u.y));
-                                    xb[2 * e + 1] = fmaf(d2, u.x, c2 * u.y);
-                                }
-                            }
-                            if (m > 0) {
-#pragma unroll
-                                for (int e = 0; e < 16; ++e) {
-                                    xa[e] += __uint_as_float(pa[e]);
-                                    xb[e] += __uint_as_float(pb[e]);
-                                }
-                            }
-                            store16(rows, tt, cb, xa);
-                            store16(rows, tt, cb + 16, xb);
-                        }
-                    }
-                }
+                if (sg.w == 128)
+                    epilogue_spans<kWMax / (2 * kEpiPerSub)>(rows_s, tt, a0, b0, mode, m > 0, tacc, cs_s, valid);
+                else
+                    epilogue_spans<kWMax / (4 * kEpiPerSub)>(rows_s, tt, a0, b0, mode, m > 0, tacc, cs_s, valid);
             }
             if (m > 0) {   // accumulator free for the next MMA
                 ptx::tc_fence_before();
@@ -655,28 +704,32 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
                 ++k;
             }
             __syncwarp();
-            // this warp's columns of its 32 rows -> pool slots, coalesced 16-byte pieces
+            // this warp's columns of its 32 rows -> pool slots, coalesced 16-byte pieces;
+            // all slots, then all shared loads, then all global stores
             {
-                const int ppr = sg.w >> 4;   // pieces per row owned by this warp (8 or 4)
-                const int rpi = 32 / ppr;    // rows per warp instruction
-                const int j = lane % ppr;
-                int piece;
-                if (rot && r.rope.pairing == KAMERA_ROPE_ROTATE_HALF) {
-                    const int quarter = ppr >> 1;   // first half-row pieces, then their partners
-                    piece = j < quarter ? hh * quarter + j : ppr + hh * quarter + (j - quarter);
-                } else {
-                    piece = hh * ppr + j;
-                }
+                const int ppr = sg.w / (8 * kEpiPerSub);   // pieces per row owned by this warp
+                const int sh_ = 31 - __clz(ppr);
+                const int j = lane & (ppr - 1);
+                const int piece = j < (ppr >> 1) ? (a0 >> 3) + j : (b0 >> 3) + j - (ppr >> 1);
                 __nv_bfloat16* dbase =
                     (sg.array == 0 ? r.dst_k : r.dst_v) + (int64_t)l * r.dst_ls + sg.e0 + piece * 8;
-                for (int i2 = 0; i2 < 32; i2 += rpi) {
-                    const int src_lane = i2 + lane / ppr;
-                    const int64_t sl = __shfl_sync(0xffffffffu, slot, src_lane);
-                    if (sl >= 0) {
-                        uint32_t v[4];
-                        ptx::lds128(row_piece(rows, q * 32 + src_lane, piece), v);
-                        ptx::stg128(dbase + sl * r.dst_ss, v);
-                    }
+                const int n_it = ppr;        // 32 rows / (32 / ppr rows per instruction)
+                for (int b4 = 0; b4 < n_it; b4 += 4) {   // batches of 4 rows-per-instruction groups
+                    int64_t sl[4];
+                    uint32_t v[4][4];
+#pragma unroll
+                    for (int it = 0; it < 4; ++it)
+                        sl[it] = b4 + it < n_it ? __shfl_sync(0xffffffffu, slot, ((b4 + it) << (5 - sh_)) + (lane >> sh_))
+                                                : -1;
+#pragma unroll
+                    for (int it = 0; it < 4; ++it)
+                        if (sl[it] >= 0)
+                            ptx::lds128(piece_addr(rows_s, q * 32 + ((b4 + it) << (5 - sh_)) + (lane >> sh_), piece),
+                                        v[it]);
+#pragma unroll
+                    for (int it = 0; it < 4; ++it)
+                        if (sl[it] >= 0)
+                            ptx::stg128(dbase + sl[it] * r.dst_ss, v[it]);
                 }
             }
             ptx::fence_proxy_async();   // our shared-memory accesses precede the next TMA write here
@@ -684,10 +737,7 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
             if (lane == 0)
                 ptx::mbar_arrive(ptx::smem_addr(&sh.empty[s]));
             cur.next(p);
-            if (i + 1 < count) {   // prefetch the next tile's slot
-                const int ntok2 = min(kTileM, cur.ch.len - cur.t * kTileM);
-                slot_next = tt < ntok2 ? cur.ch.dst_slot_mapping[cur.t * kTileM + tt] : -1;
-            }
+            slot_cur = slot_nxt;
         }
     }
     ptx::tc_fence_before();
