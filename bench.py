@@ -55,6 +55,20 @@ def measured_peaks():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def max_over_ranks(value: float, dist=None, device="cpu") -> float:
+    """The largest `value` over all ranks (the slowest rank sets the job time)."""
+    if dist is None:
+        return float(value)
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def job_throughput(bytes_per_rank: int, world: int, seconds_per_step: float) -> float:
+    """Whole-job GB/s: every rank processes its own copy of the workload (weak scaling)."""
+    return bytes_per_rank * world / seconds_per_step / 1e9
+
+
 def dist_env():
     return int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")), \
         int(os.environ.get("LOCAL_RANK", "0"))
@@ -362,14 +376,10 @@ def ours_arm(args):
         launch_ms = time_launches(call, args.steps, flush)
     else:
         launch_ms = step_ms
-    t_max = total_ms
-    if pg:
-        tt = torch.tensor([total_ms], device=dev)
-        pg.all_reduce(tt, op=pg.ReduceOp.MAX)
-        t_max = float(tt.item())
+    t_max = max_over_ranks(total_ms, pg, dev)
     ms_per_step = t_max / args.steps
     bytes_step = W.algorithmic_bytes(spec)
-    value = bytes_step * world / (ms_per_step * 1e-3) / 1e9
+    value = job_throughput(bytes_step, world, ms_per_step * 1e-3)
     launch_avg = float(np.mean(launch_ms))
     achieved = bytes_step / (launch_avg * 1e-3) / 1e9
     dev_err = int(err.item())

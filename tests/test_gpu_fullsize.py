@@ -1,0 +1,160 @@
+"""Parity at the benchmark's full sizes, in the launch configuration bench.py
+times (same entry point, max_len and max_rank as the benchmark call).
+
+The fp64 oracle cannot compute whole workloads of 1-100 GB in a test, so it
+computes a seeded sample of output rows one by one (``oracle.row`` on the
+sampled canonical rows and patch factors, copied to the host before the
+call), and properties that hold at any size are checked on the whole pool:
+every slot no chunk targets keeps its canary bits, and no device error bit
+is raised.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle as O
+import position_invariant_kv_chunk_gb300 as K
+import workloads as W
+from tests import harness as Hn
+
+pytestmark = pytest.mark.gpu
+DEV = "cuda"
+N_SAMPLES = 96     # sampled (chunk, layer) groups
+TOK_PER = 3        # sampled tokens per group
+
+
+def _targeted_mask(wl):
+    mask = torch.zeros(wl.num_slots, dtype=torch.bool, device=DEV)
+    for c in wl.chunks:
+        mask[c.slots] = True
+    return mask
+
+
+def _samples(wl, seed):
+    rng = np.random.default_rng(seed)
+    out = []
+    for _ in range(N_SAMPLES):
+        ci = int(rng.integers(len(wl.chunks)))
+        c = wl.chunks[ci]
+        l = int(rng.integers(wl.spec.L))
+        toks = sorted(set(int(t) for t in rng.integers(0, c.length, TOK_PER)))
+        out.append((ci, l, toks))
+    return out
+
+
+def _u16(t):
+    return Hn.u16(t)
+
+
+def _check_rows(got, want, scale, what):
+    Hn.compare(np.stack(got), np.stack(want), np.stack(scale), what=what)
+
+
+@pytest.mark.parametrize("name", ["qwen_recall", "mha_reorder_recall", "tiny_gqa_x4096"])
+def test_gqa_fullsize_sampled(name):
+    spec = W.tiny_gqa_x(4096) if name == "tiny_gqa_x4096" else W.CONFIGS[name]()
+    wl = W.make(spec, DEV)
+    orc = O.default()
+    th = orc.inv_freq(wl.base, wl.rot_dim)
+    samples = _samples(wl, 11)
+    snap = []
+    for ci, l, toks in samples:   # host copies of every input the sampled rows need
+        c = wl.chunks[ci]
+        rows = torch.tensor([c.src_offset + j for j in toks], device=DEV)
+        item = {"k": _u16(wl.store_k[l, rows]), "v": _u16(wl.store_v[l, rows]),
+                "slots": c.slots[toks].cpu().numpy()}
+        if c.rank:
+            item["uk"] = _u16(c.patches[0][l][:, toks])
+            item["vk"] = _u16(c.patches[1][l])
+            item["uv"] = _u16(c.patches[2][l][:, toks])
+            item["vv"] = _u16(c.patches[3][l])
+        snap.append(item)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    H = wl.spec.H
+    gk, wk, sk, gv, wv, sv = [], [], [], [], [], []
+    for (ci, l, toks), item in zip(samples, snap):
+        c = wl.chunks[ci]
+        pk = _u16(wl.pool_k[l, torch.as_tensor(item["slots"], device=DEV)])
+        pv = _u16(wl.pool_v[l, torch.as_tensor(item["slots"], device=DEV)])
+        for a in range(len(toks)):
+            for h in range(H):
+                kw = dict(u=item["uk"][h, a], vm=item["vk"][h]) if c.rank else {}
+                vw = dict(u=item["uv"][h, a], vm=item["vv"][h]) if c.rank else {}
+                b, _, s = orc.row(item["k"][a, h], True, c.delta, th, wl.rot_dim, wl.rot_offset, wl.pairing, **kw)
+                gk.append(pk[a, h]); wk.append(b); sk.append(s)
+                b, _, s = orc.row(item["v"][a, h], False, 0, th, wl.rot_dim, wl.rot_offset, wl.pairing, **vw)
+                gv.append(pv[a, h]); wv.append(b); sv.append(s)
+    _check_rows(gk, wk, sk, f"{name} K (sampled)")
+    _check_rows(gv, wv, sv, f"{name} V (sampled)")
+    untouched = ~_targeted_mask(wl)
+    canary = torch.tensor(W.CANARY_BITS - 0x10000 if W.CANARY_BITS >= 0x8000 else W.CANARY_BITS,
+                          dtype=torch.int16, device=DEV)
+    for pool in (wl.pool_k, wl.pool_v):
+        assert bool((pool.view(torch.int16)[:, untouched] == canary).all()), f"{name}: untouched slots changed"
+
+
+def test_mla_fullsize_sampled():
+    wl = W.make(W.dsv2_mla(), DEV)
+    orc = O.default()
+    th = orc.inv_freq(wl.base, wl.rot_dim)
+    kv = wl.kv_lora
+    samples = _samples(wl, 12)
+    snap = []
+    for ci, l, toks in samples:
+        c = wl.chunks[ci]
+        rows = torch.tensor([c.src_offset + j for j in toks], device=DEV)
+        snap.append({"x": _u16(wl.store_k[l, rows]), "slots": c.slots[toks].cpu().numpy(),
+                     "uc": _u16(c.patches[0][l][toks]), "vc": _u16(c.patches[1][l]),
+                     "ur": _u16(c.patches[2][l][toks]), "vr": _u16(c.patches[3][l])})
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    gc, wc, sc, gr, wr, sr = [], [], [], [], [], []
+    for (ci, l, toks), item in zip(samples, snap):
+        c = wl.chunks[ci]
+        pool = _u16(wl.pool_k[l, torch.as_tensor(item["slots"], device=DEV)])
+        for a in range(len(toks)):
+            b, _, s = orc.row(item["x"][a, :kv], False, 0, th, wl.rot_dim, 0, wl.pairing, u=item["uc"][a], vm=item["vc"])
+            gc.append(pool[a, :kv]); wc.append(b); sc.append(s)
+            b, _, s = orc.row(item["x"][a, kv:], True, c.delta, th, wl.rot_dim, 0, wl.pairing, u=item["ur"][a],
+                              vm=item["vr"])
+            gr.append(pool[a, kv:]); wr.append(b); sr.append(s)
+    _check_rows(gc, wc, sc, "dsv2_mla c_KV (sampled)")
+    _check_rows(gr, wr, sr, "dsv2_mla k_rope (sampled)")
+    untouched = ~_targeted_mask(wl)
+    canary = torch.tensor(W.CANARY_BITS, dtype=torch.int16, device=DEV)
+    assert bool((wl.pool_k.view(torch.int16)[:, untouched] == canary).all())
+
+
+def test_slide_fullsize_sampled():
+    wl = W.make(W.qwen_slide(), DEV)
+    orc = O.default()
+    th = orc.inv_freq(wl.base, wl.rot_dim)
+    samples = _samples(wl, 13)
+    before = []
+    for ci, l, toks in samples:
+        c = wl.chunks[ci]
+        before.append(_u16(wl.pool_k[l, c.slots[toks]]))
+    targeted = _targeted_mask(wl)
+    # a sample of evicted (untouched) slots, copied before the call
+    ev = torch.nonzero(~targeted).flatten()
+    ev = ev[torch.randperm(ev.numel(), generator=torch.Generator().manual_seed(3))[:4096].to(DEV)]
+    ev_before = _u16(wl.pool_k[:, ev])
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    got, want, scale = [], [], []
+    for (ci, l, toks), x in zip(samples, before):
+        c = wl.chunks[ci]
+        after = _u16(wl.pool_k[l, c.slots[toks]])
+        for a in range(len(toks)):
+            for h in range(wl.spec.H):
+                b, _, s = orc.row(x[a, h], True, c.delta, th, wl.rot_dim, wl.rot_offset, wl.pairing)
+                got.append(after[a, h]); want.append(b); scale.append(s)
+    _check_rows(got, want, scale, "qwen_slide (sampled)")
+    assert np.array_equal(_u16(wl.pool_k[:, ev]), ev_before), "evicted slots changed"
