@@ -343,6 +343,8 @@ def ours_arm(args):
     peak, peak_src = measured_peaks()
 
     spec = W.CONFIGS[args.config]()
+    if args.layers:
+        spec = W.scaled(spec, L=args.layers, name=spec.name)
     wl = W.make(spec, dev)
     err = torch.zeros(1, dtype=torch.int32, device=dev)
     chunks_dev = K.pack_chunks(wl.chunks, device=dev)
@@ -436,6 +438,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-headline-in-sweep", action="store_true")
     ap.add_argument("--ref-seconds", type=float, default=8.0, help="oracle seconds per sample")
+    ap.add_argument("--layers", type=int, default=0,
+                    help="run the workload with this many layers (a smaller case for profiler captures)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
