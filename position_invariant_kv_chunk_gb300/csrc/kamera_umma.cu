@@ -266,53 +266,60 @@ __device__ __forceinline__ uint32_t piece_addr(uint32_t rows, int tt, int q)
 // One thread's share of a tile row: two spans of N columns starting at a0 and
 // b0 (RoPE partners for rotate-half, else adjacent), read from TMEM (patch)
 // and from the row in shared memory, combined, rounded and written back.
-// mode: 0 no rotation, 1 rotate-half pairs (a0+i, b0+i), 2 interleaved pairs.
-// Arithmetic runs on packed fp32 pairs; per element it is the same sequence
-// of roundings as x*c + round(y*(-s)) [+ patch].  Work goes in rounds of 8
-// columns per span; in each round the shared loads (row pieces and the
-// cos/sin table) are issued before the TMEM load, so their latencies overlap.
+// MODE: 0 no rotation, 1 rotate-half pairs (a0+i, b0+i), 2 interleaved pairs;
+// PATCH: a rank-m patch sits in TMEM.  Work goes in rounds of 8 columns per
+// span.  The TMEM load of round j+1 is issued before round j's arithmetic, so
+// its latency hides behind that work; round j's shared loads (row pieces and
+// the cos/sin table) are issued together at the top of the round.  Arithmetic
+// runs on packed fp32 pairs; per element it is the same sequence of roundings
+// as x*c + round(y*(-s)) [+ patch].
 //   table, rotate-half: cos[64] | sin[64] | -sin[64]      (fp32, by frequency)
 //   table, interleaved: (cos, cos)[64] | (-sin, sin)[64]  (fp32 pairs)
-template <int N>
-__device__ __forceinline__ void epilogue_spans(uint32_t rows, int tt, int a0, int b0, int mode, bool patch,
-                                               uint32_t tacc, uint32_t tab, bool valid)
+template <int N, int MODE, bool PATCH>
+__device__ __forceinline__ void epilogue_spans(uint32_t rows, int tt, int a0, int b0, uint32_t tacc, uint32_t tab,
+                                               bool valid)
 {
+    constexpr int R = N / 8;
+    uint32_t pa[2][8], pb[2][8];   // TMEM patch of this round and of the next
+    if constexpr (PATCH)           // warp-collective: every lane loads, valid row or not
+        ptx::tmem_ld8x2_issue(tacc + a0, tacc + b0, pa[0], pb[0]);
 #pragma unroll
-    for (int r0 = 0; r0 < N; r0 += 8) {
-        uint32_t va[4], vb[4], t0[4], t1[4], t2[4], t3[4], t4[4], t5[4];
-        if (valid) {
-            ptx::lds128(piece_addr(rows, tt, (a0 + r0) >> 3), va);
-            ptx::lds128(piece_addr(rows, tt, (b0 + r0) >> 3), vb);
-            if (mode == 1) {   // 8 frequencies f0..f0+7: cos, sin, -sin
-                const uint32_t f0 = (uint32_t)(a0 + r0) * 4u;
-                ptx::lds128(tab + f0, t0);
-                ptx::lds128(tab + f0 + 16, t1);
-                ptx::lds128(tab + 256 + f0, t2);
-                ptx::lds128(tab + 256 + f0 + 16, t3);
-                ptx::lds128(tab + 512 + f0, t4);
-                ptx::lds128(tab + 512 + f0 + 16, t5);
-            } else if (mode == 2) {   // 4 frequencies per span: (c, c) and (-s, s) pairs
-                const uint32_t fa = (uint32_t)((a0 + r0) >> 1) * 8u, fb = (uint32_t)((b0 + r0) >> 1) * 8u;
-                ptx::lds128(tab + fa, t0);
-                ptx::lds128(tab + fa + 16, t1);
-                ptx::lds128(tab + 512 + fa, t2);
-                ptx::lds128(tab + 512 + fa + 16, t3);
-                ptx::lds128(tab + fb, t4);
-                ptx::lds128(tab + fb + 16, t5);
-            }
+    for (int j = 0; j < R; ++j) {
+        const int r0 = 8 * j, cur = j & 1;
+        if constexpr (PATCH) {
+            ptx::tmem_wait8x2(pa[cur], pb[cur]);
+            if (j + 1 < R)
+                ptx::tmem_ld8x2_issue(tacc + a0 + r0 + 8, tacc + b0 + r0 + 8, pa[cur ^ 1], pb[cur ^ 1]);
         }
-        uint32_t pa[8], pb[8];
-        if (patch)   // warp-collective: every lane loads, valid row or not
-            ptx::tmem_ld8x2(tacc + a0 + r0, tacc + b0 + r0, pa, pb);
         if (!valid)
             continue;
+        uint32_t va[4], vb[4], t0[4], t1[4], t2[4], t3[4], t4[4], t5[4];
+        ptx::lds128(piece_addr(rows, tt, (a0 + r0) >> 3), va);
+        ptx::lds128(piece_addr(rows, tt, (b0 + r0) >> 3), vb);
+        if constexpr (MODE == 1) {   // 8 frequencies f0..f0+7: cos, sin, -sin
+            const uint32_t f0 = (uint32_t)(a0 + r0) * 4u;
+            ptx::lds128(tab + f0, t0);
+            ptx::lds128(tab + f0 + 16, t1);
+            ptx::lds128(tab + 256 + f0, t2);
+            ptx::lds128(tab + 256 + f0 + 16, t3);
+            ptx::lds128(tab + 512 + f0, t4);
+            ptx::lds128(tab + 512 + f0 + 16, t5);
+        } else if constexpr (MODE == 2) {   // 4 frequencies per span: (c, c) and (-s, s) pairs
+            const uint32_t fa = (uint32_t)((a0 + r0) >> 1) * 8u, fb = (uint32_t)((b0 + r0) >> 1) * 8u;
+            ptx::lds128(tab + fa, t0);
+            ptx::lds128(tab + fa + 16, t1);
+            ptx::lds128(tab + 512 + fa, t2);
+            ptx::lds128(tab + 512 + fa + 16, t3);
+            ptx::lds128(tab + fb, t4);
+            ptx::lds128(tab + fb + 16, t5);
+        }
         uint64_t xa[4], xb[4];
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
             xa[i] = ptx::f2_from_bf16x2(va[i]);
             xb[i] = ptx::f2_from_bf16x2(vb[i]);
         }
-        if (mode == 1) {
+        if constexpr (MODE == 1) {
             const uint64_t c[4] = {ptx::f2_make(t0[0], t0[1]), ptx::f2_make(t0[2], t0[3]), ptx::f2_make(t1[0], t1[1]),
                                    ptx::f2_make(t1[2], t1[3])};
             const uint64_t sn[4] = {ptx::f2_make(t2[0], t2[1]), ptx::f2_make(t2[2], t2[3]),
@@ -326,7 +333,7 @@ __device__ __forceinline__ void epilogue_spans(uint32_t rows, int tt, int a0, in
                 xa[i] = oa;
                 xb[i] = ob;
             }
-        } else if (mode == 2) {
+        } else if constexpr (MODE == 2) {
             const uint64_t cca[4] = {ptx::f2_make(t0[0], t0[1]), ptx::f2_make(t0[2], t0[3]),
                                      ptx::f2_make(t1[0], t1[1]), ptx::f2_make(t1[2], t1[3])};
             const uint64_t ssa[4] = {ptx::f2_make(t2[0], t2[1]), ptx::f2_make(t2[2], t2[3]),
@@ -344,17 +351,33 @@ __device__ __forceinline__ void epilogue_spans(uint32_t rows, int tt, int a0, in
                 xb[i] = ptx::f2_fma(xb[i], ccb[i], ptx::f2_mul(ptx::f2_swap(xb[i]), ssb[i]));
             }
         }
-        if (patch) {
+        if constexpr (PATCH) {
 #pragma unroll
             for (int i = 0; i < 4; ++i) {
-                xa[i] = ptx::f2_add(xa[i], ptx::f2_make(pa[2 * i], pa[2 * i + 1]));
-                xb[i] = ptx::f2_add(xb[i], ptx::f2_make(pb[2 * i], pb[2 * i + 1]));
+                xa[i] = ptx::f2_add(xa[i], ptx::f2_make(pa[cur][2 * i], pa[cur][2 * i + 1]));
+                xb[i] = ptx::f2_add(xb[i], ptx::f2_make(pb[cur][2 * i], pb[cur][2 * i + 1]));
             }
         }
         ptx::sts128(piece_addr(rows, tt, (a0 + r0) >> 3), ptx::f2_to_bf16x2(xa[0]), ptx::f2_to_bf16x2(xa[1]),
                     ptx::f2_to_bf16x2(xa[2]), ptx::f2_to_bf16x2(xa[3]));
         ptx::sts128(piece_addr(rows, tt, (b0 + r0) >> 3), ptx::f2_to_bf16x2(xb[0]), ptx::f2_to_bf16x2(xb[1]),
                     ptx::f2_to_bf16x2(xb[2]), ptx::f2_to_bf16x2(xb[3]));
+    }
+}
+
+// The epilogue specialised for the tile's segment width, rotation mode and
+// patch: one dispatch per tile, branch-free rounds inside.
+template <int N>
+__device__ __forceinline__ void epilogue_dispatch(int mode, bool patch, uint32_t rows, int tt, int a0, int b0,
+                                                  uint32_t tacc, uint32_t tab, bool valid)
+{
+    switch (mode * 2 + (patch ? 1 : 0)) {
+    case 1: epilogue_spans<N, 0, true>(rows, tt, a0, b0, tacc, tab, valid); break;
+    case 2: epilogue_spans<N, 1, false>(rows, tt, a0, b0, tacc, tab, valid); break;
+    case 3: epilogue_spans<N, 1, true>(rows, tt, a0, b0, tacc, tab, valid); break;
+    case 4: epilogue_spans<N, 2, false>(rows, tt, a0, b0, tacc, tab, valid); break;
+    case 5: epilogue_spans<N, 2, true>(rows, tt, a0, b0, tacc, tab, valid); break;
+    default: break;   // no rotation and no patch: the row is stored as loaded
     }
 }
 
@@ -690,12 +713,10 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
             const int span = sg.w / (2 * kEpiPerSub);
             const int a0 = mode == 1 ? hh * span : hh * 2 * span;
             const int b0 = mode == 1 ? a0 + (sg.w >> 1) : a0 + span;
-            if (m > 0 || rot) {
-                if (sg.w == 128)
-                    epilogue_spans<kWMax / (2 * kEpiPerSub)>(rows_s, tt, a0, b0, mode, m > 0, tacc, cs_s, valid);
-                else
-                    epilogue_spans<kWMax / (4 * kEpiPerSub)>(rows_s, tt, a0, b0, mode, m > 0, tacc, cs_s, valid);
-            }
+            if (sg.w == 128)
+                epilogue_dispatch<kWMax / (2 * kEpiPerSub)>(mode, m > 0, rows_s, tt, a0, b0, tacc, cs_s, valid);
+            else
+                epilogue_dispatch<kWMax / (4 * kEpiPerSub)>(mode, m > 0, rows_s, tt, a0, b0, tacc, cs_s, valid);
             if (m > 0) {   // accumulator free for the next MMA
                 ptx::tc_fence_before();
                 __syncwarp();
