@@ -87,6 +87,22 @@ __device__ __forceinline__ void cp_async_small(uint32_t dst, const void* src)
 {
     asm volatile("cp.async.ca.shared.global [%0], [%1], %2;" ::"r"(dst), "l"(src), "n"(BYTES) : "memory");
 }
+// arrive on the mbarrier once all of this thread's earlier cp.async copies
+// have landed (the arrival is counted in the barrier's expected count)
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint32_t bar)
+{
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(bar) : "memory");
+}
+__device__ __forceinline__ void st_shared_s64(uint32_t a, int64_t v)
+{
+    asm volatile("st.shared.s64 [%0], %1;" ::"r"(a), "l"(v) : "memory");
+}
+__device__ __forceinline__ int64_t ld_shared_s64(uint32_t a)
+{
+    int64_t v;
+    asm volatile("ld.shared.s64 %0, [%1];" : "=l"(v) : "r"(a) : "memory");
+    return v;
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int N>
 __device__ __forceinline__ void cp_async_wait()

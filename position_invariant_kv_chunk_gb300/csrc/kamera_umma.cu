@@ -47,11 +47,16 @@ constexpr int kTileM = 128;                     // tokens per tile = UMMA M = TM
 constexpr int kWMax = 128;                      // widest segment = UMMA N
 constexpr int kHalfBytes = kTileM * 128;        // one 64-column swizzled box of 128 rows
 constexpr int kRowsBytes = 2 * kHalfBytes;      // canonical rows of a tile (w <= 128)
-constexpr int kStageBytes = kRowsBytes + 1024;  // rows + cos/sin table (64 float2), 1024-aligned
+constexpr int kTabOff = kRowsBytes;             // cos/sin table of the tile's chunk (1 KB)
+constexpr int kSlotOff = kRowsBytes + 1024;      // the tile's 128 destination slots (int64)
+constexpr int kStageBytes = kRowsBytes + 2048;  // rows + table + slots, 1024-aligned
 constexpr int kAtomBytes = kTileM * 128;        // one 64-rank K atom of a 128-row operand
-constexpr int kEpiPerSub = 2;                   // epilogue warps per TMEM sub-partition
+constexpr int kEpiPerSub = 3;                   // epilogue warps per TMEM sub-partition
 constexpr int kEpiWarps = 4 * kEpiPerSub;
 constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, epilogue warps
+// Warp w runs on SM sub-partition w % 4, whose register file holds 16384
+// registers: the busiest sub-partition bounds the registers per thread.
+constexpr int kRegCap = 16384 / (32 * ((kThreads / 32 + 3) / 4));
 constexpr uint32_t kTmemCols = 2 * kWMax;       // two accumulators
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr int kTailRows = 16;                   // box height of the tail tensor maps
@@ -151,12 +156,18 @@ struct Cursor {
     }
 };
 
+// What the epilogue needs to know of the tile in a stage (written by the producer).
+struct TileInfo {
+    int32_t l, z, m, ntok, rot;
+};
+
 struct Shared {
     uint64_t full[4], empty[4], tfull[2], tempty[2], uempty[3], vmempty[2], mmadone;
     uint32_t tmem_base;
     int32_t abort_flag;
     int32_t start_lz, start_rem, start_c, start_t, count;
     int32_t stage_tag[4];
+    TileInfo tinfo[4];
     int64_t part[kThreads];
 };
 
@@ -263,120 +274,134 @@ __device__ __forceinline__ uint32_t piece_addr(uint32_t rows, int tt, int q)
     return rows + (q >> 3) * kHalfBytes + tt * 128 + ((((q & 7) ^ (tt & 7))) << 4);
 }
 
-// One thread's share of a tile row: two spans of N columns starting at a0 and
-// b0 (RoPE partners for rotate-half, else adjacent), read from TMEM (patch)
-// and from the row in shared memory, combined, rounded and written back.
-// MODE: 0 no rotation, 1 rotate-half pairs (a0+i, b0+i), 2 interleaved pairs;
-// PATCH: a rank-m patch sits in TMEM.  Work goes in rounds of 8 columns per
-// span.  The TMEM load of round j+1 is issued before round j's arithmetic, so
-// its latency hides behind that work; round j's shared loads (row pieces and
-// the cos/sin table) are issued together at the top of the round.  Arithmetic
-// runs on packed fp32 pairs; per element it is the same sequence of roundings
-// as x*c + round(y*(-s)) [+ patch].
+// One round of a thread's share of a tile row: 8 columns at a (span A) and
+// the 8 at b (span B; RoPE partners for rotate-half), read from the row in
+// shared memory, combined with the patch (fp32, from TMEM), rounded once to
+// bf16 and written back in place.  MODE: 0 no rotation, 1 rotate-half pairs
+// (a+i, b+i), 2 interleaved pairs inside each span; PATCH: a rank-m patch is
+// present.  Arithmetic runs on packed fp32 pairs; per element it is the same
+// sequence of roundings as x*c + round(y*(-s)) [+ patch].
 //   table, rotate-half: cos[64] | sin[64] | -sin[64]      (fp32, by frequency)
 //   table, interleaved: (cos, cos)[64] | (-sin, sin)[64]  (fp32 pairs)
-template <int N, int MODE, bool PATCH>
-__device__ __forceinline__ void epilogue_spans(uint32_t rows, int tt, int a0, int b0, uint32_t tacc, uint32_t tab,
-                                               bool valid)
+template <int MODE, bool PATCH>
+__device__ __forceinline__ void epilogue_round(uint32_t rows, int tt, int a, int b, uint32_t tab,
+                                               const uint32_t (&pa)[8], const uint32_t (&pb)[8])
 {
-    constexpr int R = N / 8;
-    uint32_t pa[2][8], pb[2][8];   // TMEM patch of this round and of the next
-    if constexpr (PATCH)           // warp-collective: every lane loads, valid row or not
-        ptx::tmem_ld8x2_issue(tacc + a0, tacc + b0, pa[0], pb[0]);
+    uint32_t va[4], vb[4], t0[4], t1[4], t2[4], t3[4], t4[4], t5[4];
+    ptx::lds128(piece_addr(rows, tt, a >> 3), va);
+    ptx::lds128(piece_addr(rows, tt, b >> 3), vb);
+    if constexpr (MODE == 1) {   // 8 frequencies a..a+7: cos, sin, -sin
+        const uint32_t f0 = (uint32_t)a * 4u;
+        ptx::lds128(tab + f0, t0);
+        ptx::lds128(tab + f0 + 16, t1);
+        ptx::lds128(tab + 256 + f0, t2);
+        ptx::lds128(tab + 256 + f0 + 16, t3);
+        ptx::lds128(tab + 512 + f0, t4);
+        ptx::lds128(tab + 512 + f0 + 16, t5);
+    } else if constexpr (MODE == 2) {   // 4 frequencies per span: (c, c) and (-s, s) pairs
+        const uint32_t fa = (uint32_t)(a >> 1) * 8u, fb = (uint32_t)(b >> 1) * 8u;
+        ptx::lds128(tab + fa, t0);
+        ptx::lds128(tab + fa + 16, t1);
+        ptx::lds128(tab + 512 + fa, t2);
+        ptx::lds128(tab + 512 + fa + 16, t3);
+        ptx::lds128(tab + fb, t4);
+        ptx::lds128(tab + fb + 16, t5);
+    }
+    uint64_t xa[4], xb[4];
 #pragma unroll
-    for (int j = 0; j < R; ++j) {
-        const int r0 = 8 * j, cur = j & 1;
-        if constexpr (PATCH) {
-            ptx::tmem_wait8x2(pa[cur], pb[cur]);
-            if (j + 1 < R)
-                ptx::tmem_ld8x2_issue(tacc + a0 + r0 + 8, tacc + b0 + r0 + 8, pa[cur ^ 1], pb[cur ^ 1]);
-        }
-        if (!valid)
-            continue;
-        uint32_t va[4], vb[4], t0[4], t1[4], t2[4], t3[4], t4[4], t5[4];
-        ptx::lds128(piece_addr(rows, tt, (a0 + r0) >> 3), va);
-        ptx::lds128(piece_addr(rows, tt, (b0 + r0) >> 3), vb);
-        if constexpr (MODE == 1) {   // 8 frequencies f0..f0+7: cos, sin, -sin
-            const uint32_t f0 = (uint32_t)(a0 + r0) * 4u;
-            ptx::lds128(tab + f0, t0);
-            ptx::lds128(tab + f0 + 16, t1);
-            ptx::lds128(tab + 256 + f0, t2);
-            ptx::lds128(tab + 256 + f0 + 16, t3);
-            ptx::lds128(tab + 512 + f0, t4);
-            ptx::lds128(tab + 512 + f0 + 16, t5);
-        } else if constexpr (MODE == 2) {   // 4 frequencies per span: (c, c) and (-s, s) pairs
-            const uint32_t fa = (uint32_t)((a0 + r0) >> 1) * 8u, fb = (uint32_t)((b0 + r0) >> 1) * 8u;
-            ptx::lds128(tab + fa, t0);
-            ptx::lds128(tab + fa + 16, t1);
-            ptx::lds128(tab + 512 + fa, t2);
-            ptx::lds128(tab + 512 + fa + 16, t3);
-            ptx::lds128(tab + fb, t4);
-            ptx::lds128(tab + fb + 16, t5);
-        }
-        uint64_t xa[4], xb[4];
+    for (int i = 0; i < 4; ++i) {
+        xa[i] = ptx::f2_from_bf16x2(va[i]);
+        xb[i] = ptx::f2_from_bf16x2(vb[i]);
+    }
+    if constexpr (MODE == 1) {
+        const uint64_t c[4] = {ptx::f2_make(t0[0], t0[1]), ptx::f2_make(t0[2], t0[3]), ptx::f2_make(t1[0], t1[1]),
+                               ptx::f2_make(t1[2], t1[3])};
+        const uint64_t sn[4] = {ptx::f2_make(t2[0], t2[1]), ptx::f2_make(t2[2], t2[3]), ptx::f2_make(t3[0], t3[1]),
+                                ptx::f2_make(t3[2], t3[3])};
+        const uint64_t ns[4] = {ptx::f2_make(t4[0], t4[1]), ptx::f2_make(t4[2], t4[3]), ptx::f2_make(t5[0], t5[1]),
+                                ptx::f2_make(t5[2], t5[3])};
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
-            xa[i] = ptx::f2_from_bf16x2(va[i]);
-            xb[i] = ptx::f2_from_bf16x2(vb[i]);
+            const uint64_t oa = ptx::f2_fma(xa[i], c[i], ptx::f2_mul(xb[i], ns[i]));
+            const uint64_t ob = ptx::f2_fma(xb[i], c[i], ptx::f2_mul(xa[i], sn[i]));
+            xa[i] = oa;
+            xb[i] = ob;
         }
-        if constexpr (MODE == 1) {
-            const uint64_t c[4] = {ptx::f2_make(t0[0], t0[1]), ptx::f2_make(t0[2], t0[3]), ptx::f2_make(t1[0], t1[1]),
-                                   ptx::f2_make(t1[2], t1[3])};
-            const uint64_t sn[4] = {ptx::f2_make(t2[0], t2[1]), ptx::f2_make(t2[2], t2[3]),
-                                    ptx::f2_make(t3[0], t3[1]), ptx::f2_make(t3[2], t3[3])};
-            const uint64_t ns[4] = {ptx::f2_make(t4[0], t4[1]), ptx::f2_make(t4[2], t4[3]),
-                                    ptx::f2_make(t5[0], t5[1]), ptx::f2_make(t5[2], t5[3])};
+    } else if constexpr (MODE == 2) {
+        const uint64_t cca[4] = {ptx::f2_make(t0[0], t0[1]), ptx::f2_make(t0[2], t0[3]), ptx::f2_make(t1[0], t1[1]),
+                                 ptx::f2_make(t1[2], t1[3])};
+        const uint64_t ssa[4] = {ptx::f2_make(t2[0], t2[1]), ptx::f2_make(t2[2], t2[3]), ptx::f2_make(t3[0], t3[1]),
+                                 ptx::f2_make(t3[2], t3[3])};
+        uint32_t u0[4], u1[4];   // the b span's (-s, s) pairs
+        ptx::lds128(tab + 512 + (uint32_t)(b >> 1) * 8u, u0);
+        ptx::lds128(tab + 512 + (uint32_t)(b >> 1) * 8u + 16, u1);
+        const uint64_t ccb[4] = {ptx::f2_make(t4[0], t4[1]), ptx::f2_make(t4[2], t4[3]), ptx::f2_make(t5[0], t5[1]),
+                                 ptx::f2_make(t5[2], t5[3])};
+        const uint64_t ssb[4] = {ptx::f2_make(u0[0], u0[1]), ptx::f2_make(u0[2], u0[3]), ptx::f2_make(u1[0], u1[1]),
+                                 ptx::f2_make(u1[2], u1[3])};
 #pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                const uint64_t oa = ptx::f2_fma(xa[i], c[i], ptx::f2_mul(xb[i], ns[i]));
-                const uint64_t ob = ptx::f2_fma(xb[i], c[i], ptx::f2_mul(xa[i], sn[i]));
-                xa[i] = oa;
-                xb[i] = ob;
-            }
-        } else if constexpr (MODE == 2) {
-            const uint64_t cca[4] = {ptx::f2_make(t0[0], t0[1]), ptx::f2_make(t0[2], t0[3]),
-                                     ptx::f2_make(t1[0], t1[1]), ptx::f2_make(t1[2], t1[3])};
-            const uint64_t ssa[4] = {ptx::f2_make(t2[0], t2[1]), ptx::f2_make(t2[2], t2[3]),
-                                     ptx::f2_make(t3[0], t3[1]), ptx::f2_make(t3[2], t3[3])};
-            uint32_t u0[4], u1[4];   // the b span's (-s, s) pairs
-            ptx::lds128(tab + 512 + (uint32_t)((b0 + r0) >> 1) * 8u, u0);
-            ptx::lds128(tab + 512 + (uint32_t)((b0 + r0) >> 1) * 8u + 16, u1);
-            const uint64_t ccb[4] = {ptx::f2_make(t4[0], t4[1]), ptx::f2_make(t4[2], t4[3]),
-                                     ptx::f2_make(t5[0], t5[1]), ptx::f2_make(t5[2], t5[3])};
-            const uint64_t ssb[4] = {ptx::f2_make(u0[0], u0[1]), ptx::f2_make(u0[2], u0[3]),
-                                     ptx::f2_make(u1[0], u1[1]), ptx::f2_make(u1[2], u1[3])};
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                xa[i] = ptx::f2_fma(xa[i], cca[i], ptx::f2_mul(ptx::f2_swap(xa[i]), ssa[i]));
-                xb[i] = ptx::f2_fma(xb[i], ccb[i], ptx::f2_mul(ptx::f2_swap(xb[i]), ssb[i]));
-            }
+        for (int i = 0; i < 4; ++i) {
+            xa[i] = ptx::f2_fma(xa[i], cca[i], ptx::f2_mul(ptx::f2_swap(xa[i]), ssa[i]));
+            xb[i] = ptx::f2_fma(xb[i], ccb[i], ptx::f2_mul(ptx::f2_swap(xb[i]), ssb[i]));
         }
+    }
+    if constexpr (PATCH) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            xa[i] = ptx::f2_add(xa[i], ptx::f2_make(pa[2 * i], pa[2 * i + 1]));
+            xb[i] = ptx::f2_add(xb[i], ptx::f2_make(pb[2 * i], pb[2 * i + 1]));
+        }
+    }
+    ptx::sts128(piece_addr(rows, tt, a >> 3), ptx::f2_to_bf16x2(xa[0]), ptx::f2_to_bf16x2(xa[1]),
+                ptx::f2_to_bf16x2(xa[2]), ptx::f2_to_bf16x2(xa[3]));
+    ptx::sts128(piece_addr(rows, tt, b >> 3), ptx::f2_to_bf16x2(xb[0]), ptx::f2_to_bf16x2(xb[1]),
+                ptx::f2_to_bf16x2(xb[2]), ptx::f2_to_bf16x2(xb[3]));
+}
+
+// A thread's share of a tile row: R rounds over the spans at a0 and b0.  The
+// TMEM load of round j+1 is issued before round j's arithmetic, so its
+// latency hides behind that work; the rounds go two per loop trip, one per
+// TMEM buffer.
+template <int MODE, bool PATCH>
+__device__ __forceinline__ void epilogue_spans(uint32_t rows, int tt, int a0, int b0, int R, uint32_t tacc,
+                                               uint32_t tab, bool valid)
+{
+    uint32_t p0a[8], p0b[8], p1a[8], p1b[8];
+    if constexpr (PATCH)   // warp-collective: every lane loads, valid row or not
+        ptx::tmem_ld8x2_issue(tacc + a0, tacc + b0, p0a, p0b);
+#pragma unroll 1
+    for (int j = 0; j < R; j += 2) {
+        const int r0 = 8 * j;
         if constexpr (PATCH) {
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-                xa[i] = ptx::f2_add(xa[i], ptx::f2_make(pa[cur][2 * i], pa[cur][2 * i + 1]));
-                xb[i] = ptx::f2_add(xb[i], ptx::f2_make(pb[cur][2 * i], pb[cur][2 * i + 1]));
-            }
+            ptx::tmem_wait8x2(p0a, p0b);
+            if (j + 1 < R)
+                ptx::tmem_ld8x2_issue(tacc + a0 + r0 + 8, tacc + b0 + r0 + 8, p1a, p1b);
         }
-        ptx::sts128(piece_addr(rows, tt, (a0 + r0) >> 3), ptx::f2_to_bf16x2(xa[0]), ptx::f2_to_bf16x2(xa[1]),
-                    ptx::f2_to_bf16x2(xa[2]), ptx::f2_to_bf16x2(xa[3]));
-        ptx::sts128(piece_addr(rows, tt, (b0 + r0) >> 3), ptx::f2_to_bf16x2(xb[0]), ptx::f2_to_bf16x2(xb[1]),
-                    ptx::f2_to_bf16x2(xb[2]), ptx::f2_to_bf16x2(xb[3]));
+        if (valid)
+            epilogue_round<MODE, PATCH>(rows, tt, a0 + r0, b0 + r0, tab, p0a, p0b);
+        if (j + 1 < R) {
+            if constexpr (PATCH) {
+                ptx::tmem_wait8x2(p1a, p1b);
+                if (j + 2 < R)
+                    ptx::tmem_ld8x2_issue(tacc + a0 + r0 + 16, tacc + b0 + r0 + 16, p0a, p0b);
+            }
+            if (valid)
+                epilogue_round<MODE, PATCH>(rows, tt, a0 + r0 + 8, b0 + r0 + 8, tab, p1a, p1b);
+        }
     }
 }
 
-// The epilogue specialised for the tile's segment width, rotation mode and
-// patch: one dispatch per tile, branch-free rounds inside.
-template <int N>
-__device__ __forceinline__ void epilogue_dispatch(int mode, bool patch, uint32_t rows, int tt, int a0, int b0,
+// The epilogue specialised for the tile's rotation mode and patch: one
+// dispatch per tile, branch-free rounds inside.
+__device__ __forceinline__ void epilogue_dispatch(int mode, bool patch, uint32_t rows, int tt, int a0, int b0, int R,
                                                   uint32_t tacc, uint32_t tab, bool valid)
 {
     switch (mode * 2 + (patch ? 1 : 0)) {
-    case 1: epilogue_spans<N, 0, true>(rows, tt, a0, b0, tacc, tab, valid); break;
-    case 2: epilogue_spans<N, 1, false>(rows, tt, a0, b0, tacc, tab, valid); break;
-    case 3: epilogue_spans<N, 1, true>(rows, tt, a0, b0, tacc, tab, valid); break;
-    case 4: epilogue_spans<N, 2, false>(rows, tt, a0, b0, tacc, tab, valid); break;
-    case 5: epilogue_spans<N, 2, true>(rows, tt, a0, b0, tacc, tab, valid); break;
+    case 1: epilogue_spans<0, true>(rows, tt, a0, b0, R, tacc, tab, valid); break;
+    case 2: epilogue_spans<1, false>(rows, tt, a0, b0, R, tacc, tab, valid); break;
+    case 3: epilogue_spans<1, true>(rows, tt, a0, b0, R, tacc, tab, valid); break;
+    case 4: epilogue_spans<2, false>(rows, tt, a0, b0, R, tacc, tab, valid); break;
+    case 5: epilogue_spans<2, true>(rows, tt, a0, b0, R, tacc, tab, valid); break;
     default: break;   // no rotation and no patch: the row is stored as loaded
     }
 }
@@ -384,7 +409,7 @@ __device__ __forceinline__ void epilogue_dispatch(int mode, bool patch, uint32_t
 }  // namespace
 
 template <int KA>
-__global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const __grid_constant__ UmmaParams p)
+__global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_constant__ UmmaParams p)
 {
     using G = Geometry<KA>;
     extern __shared__ uint8_t smem_raw[];
@@ -400,7 +425,7 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
     // ---------------------------------------------------------- prologue
     if (tid == 0) {
         for (int i = 0; i < G::S; ++i) {
-            ptx::mbar_init(ptx::smem_addr(&sh.full[i]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sh.full[i]), 1 + 32);   // TMA issue + the slot copies of 32 lanes
             ptx::mbar_init(ptx::smem_addr(&sh.empty[i]), kEpiWarps);
             sh.stage_tag[i] = -1;
         }
@@ -507,7 +532,7 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
             const int ntok = min(kTileM, ch.len - tok0);
             const bool rot = sg.rot && ch.delta != 0;
             if (rot && sh.stage_tag[s] != cur.c) {   // cos/sin table in the epilogue's operand order
-                float* tab = reinterpret_cast<float*>(gbase + s * kStageBytes + kRowsBytes);
+                float* tab = reinterpret_cast<float*>(gbase + s * kStageBytes + kTabOff);
                 const bool half_pairs = r.rope.pairing == KAMERA_ROPE_ROTATE_HALF;
                 for (int f = lane; f < r.rope.n_freq; f += 32) {
                     float c_, s_;
@@ -526,6 +551,20 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
                 __syncwarp();
                 if (lane == 0)
                     sh.stage_tag[s] = cur.c;
+            }
+            {   // the tile's destination slots (-1 past its last row) and its description
+                const uint32_t slots = base + s * kStageBytes + kSlotOff;
+                const int64_t* map = ch.dst_slot_mapping + tok0;
+#pragma unroll
+                for (int j = lane; j < kTileM; j += 32) {
+                    if (j < ntok)
+                        ptx::cp_async_small<8>(slots + 8 * j, map + j);
+                    else
+                        ptx::st_shared_s64(slots + 8 * j, -1);
+                }
+                ptx::cp_async_mbar_arrive_noinc(ptx::smem_addr(&sh.full[s]));
+                if (lane == 0)
+                    sh.tinfo[s] = TileInfo{l, z, ch.rank, ntok, rot ? 1 : 0};
             }
             __syncwarp();
             if (lane == 0) {
@@ -660,63 +699,37 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
         const int tt = q * 32 + lane;   // token row of the tile = TMEM lane
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         int k = 0;
-        int64_t slot_cur = -1;
-        {
-            const int ntok = min(kTileM, cur.ch.len - cur.t * kTileM);
-            if (tt < ntok)
-                slot_cur = cur.ch.dst_slot_mapping[cur.t * kTileM + tt];
-        }
         for (int i = 0; i < count; ++i) {
-            // the next tile's slot is loaded a whole tile ahead of its use
-            int64_t slot_nxt = -1;
-            if (i + 1 < count) {
-                if (cur.t + 1 < cur.ntile) {   // same chunk: the common case
-                    const int ntok2 = min(kTileM, cur.ch.len - (cur.t + 1) * kTileM);
-                    if (tt < ntok2)
-                        slot_nxt = cur.ch.dst_slot_mapping[(cur.t + 1) * kTileM + tt];
-                } else {
-                    Cursor nxt = cur;
-                    nxt.next(p);
-                    const int ntok2 = min(kTileM, nxt.ch.len - nxt.t * kTileM);
-                    if (tt < ntok2)
-                        slot_nxt = nxt.ch.dst_slot_mapping[nxt.t * kTileM + tt];
-                }
-            }
             const int s = i % G::S, rnd = i / G::S;
-            const int l = cur.lz / p.Z, z = cur.lz - l * p.Z;
-            const Seg sg = segment(p, z);
-            const KameraChunk& ch = cur.ch;
-            const int tok0 = cur.t * kTileM;
-            const int ntok = min(kTileM, ch.len - tok0);
-            const int m = ch.rank;
-            const bool rot = sg.rot && ch.delta != 0;
             if (!warp_wait(ptx::smem_addr(&sh.full[s]), rnd & 1, abort_flag, r.err))
                 break;
+            const TileInfo ti = sh.tinfo[s];   // the producer's description of the tile in this stage
+            const int l = ti.l, m = ti.m, ntok = ti.ntok;
+            const bool rot = ti.rot != 0;
+            const Seg sg = segment(p, ti.z);
             const int acc = k & 1;
             if (m > 0) {
                 if (!warp_wait(ptx::smem_addr(&sh.tfull[acc]), (k >> 1) & 1, abort_flag, r.err))
                     break;
                 ptx::tc_fence_after();
             }
-            int64_t slot = tt < ntok ? slot_cur : -1;
+            const uint32_t rows_s = base + s * kStageBytes;
+            const uint32_t cs_s = rows_s + kTabOff;
+            int64_t slot = ptx::ld_shared_s64(rows_s + kSlotOff + 8 * tt);
             if (slot >= r.num_slots || (tt < ntok && slot < 0)) {
                 raise_err(r.err, KAMERA_DEVERR_SLOT);
                 slot = -1;
             }
             const bool valid = slot >= 0;
             const uint32_t tacc = tmem + lane_addr + acc * kWMax;
-            const uint32_t rows_s = base + s * kStageBytes;
-            const uint32_t cs_s = rows_s + kRowsBytes;
             const int mode = rot ? (r.rope.pairing == KAMERA_ROPE_ROTATE_HALF ? 1 : 2) : 0;
-            // this warp's two spans of w/(2*kEpiPerSub) columns: whole RoPE pairs for
-            // rotate-half, else a contiguous 1/kEpiPerSub of the row
-            const int span = sg.w / (2 * kEpiPerSub);
-            const int a0 = mode == 1 ? hh * span : hh * 2 * span;
-            const int b0 = mode == 1 ? a0 + (sg.w >> 1) : a0 + span;
-            if (sg.w == 128)
-                epilogue_dispatch<kWMax / (2 * kEpiPerSub)>(mode, m > 0, rows_s, tt, a0, b0, tacc, cs_s, valid);
-            else
-                epilogue_dispatch<kWMax / (4 * kEpiPerSub)>(mode, m > 0, rows_s, tt, a0, b0, tacc, cs_s, valid);
+            // The row splits into P = w/16 pair-pieces: 8 columns j*8.. and their
+            // partners w/2 further on (whole RoPE pairs for rotate-half).  This
+            // warp owns pair-pieces [j0, j1): spans at a0 and b0, R rounds.
+            const int P = sg.w >> 4;
+            const int j0 = hh * P / kEpiPerSub, R = (hh + 1) * P / kEpiPerSub - j0;
+            const int a0 = 8 * j0, b0 = (sg.w >> 1) + 8 * j0;
+            epilogue_dispatch(mode, m > 0, rows_s, tt, a0, b0, R, tacc, cs_s, valid);
             if (m > 0) {   // accumulator free for the next MMA
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -727,38 +740,38 @@ __global__ void __launch_bounds__(kThreads, 1) relocate_patch_umma_kernel(const 
             __syncwarp();
             // this warp's columns of its 32 rows -> pool slots, coalesced 16-byte pieces;
             // all slots, then all shared loads, then all global stores
+            // 32 rows x ppr pieces; item = instruction * 32 + lane walks them row by
+            // row, the pieces of a span being adjacent in the pool row
             {
-                const int ppr = sg.w / (8 * kEpiPerSub);   // pieces per row owned by this warp
-                const int sh_ = 31 - __clz(ppr);
-                const int j = lane & (ppr - 1);
-                const int piece = j < (ppr >> 1) ? (a0 >> 3) + j : (b0 >> 3) + j - (ppr >> 1);
-                __nv_bfloat16* dbase =
-                    (sg.array == 0 ? r.dst_k : r.dst_v) + (int64_t)l * r.dst_ls + sg.e0 + piece * 8;
-                const int n_it = ppr;        // 32 rows / (32 / ppr rows per instruction)
-                for (int b4 = 0; b4 < n_it; b4 += 4) {   // batches of 4 rows-per-instruction groups
-                    int64_t sl[4];
-                    uint32_t v[4][4];
+                const int ppr = 2 * R;
+                const uint32_t inv = (65536u + (uint32_t)ppr - 1u) / (uint32_t)ppr;   // item / ppr, exact below 512
+                __nv_bfloat16* dbase = (sg.array == 0 ? r.dst_k : r.dst_v) + (int64_t)l * r.dst_ls + sg.e0;
+                for (int b4 = 0; b4 < ppr; b4 += 2) {   // batches of 2 instructions (ppr is even)
+                    int64_t sl[2];
+                    int row[2], piece[2];
+                    uint32_t v[2][4];
 #pragma unroll
-                    for (int it = 0; it < 4; ++it)
-                        sl[it] = b4 + it < n_it ? __shfl_sync(0xffffffffu, slot, ((b4 + it) << (5 - sh_)) + (lane >> sh_))
-                                                : -1;
+                    for (int it = 0; it < 2; ++it) {
+                        const int item = (b4 + it) * 32 + lane;
+                        row[it] = (int)(((uint32_t)item * inv) >> 16);
+                        const int pi = item - row[it] * ppr;
+                        piece[it] = pi < R ? j0 + pi : P + j0 + (pi - R);
+                        sl[it] = __shfl_sync(0xffffffffu, slot, row[it]);
+                    }
 #pragma unroll
-                    for (int it = 0; it < 4; ++it)
+                    for (int it = 0; it < 2; ++it)
                         if (sl[it] >= 0)
-                            ptx::lds128(piece_addr(rows_s, q * 32 + ((b4 + it) << (5 - sh_)) + (lane >> sh_), piece),
-                                        v[it]);
+                            ptx::lds128(piece_addr(rows_s, q * 32 + row[it], piece[it]), v[it]);
 #pragma unroll
-                    for (int it = 0; it < 4; ++it)
+                    for (int it = 0; it < 2; ++it)
                         if (sl[it] >= 0)
-                            ptx::stg128(dbase + sl[it] * r.dst_ss, v[it]);
+                            ptx::stg128(dbase + sl[it] * r.dst_ss + piece[it] * 8, v[it]);
                 }
             }
             ptx::fence_proxy_async();   // our shared-memory accesses precede the next TMA write here
             __syncwarp();
             if (lane == 0)
                 ptx::mbar_arrive(ptx::smem_addr(&sh.empty[s]));
-            cur.next(p);
-            slot_cur = slot_nxt;
         }
     }
     ptx::tc_fence_before();
