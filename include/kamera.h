@@ -77,7 +77,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
-#define KAMERA_ABI_VERSION 1
+#define KAMERA_ABI_VERSION 2
 
 /* Limits of this build. */
 #define KAMERA_MAX_RANK 128          /* largest patch rank m */
@@ -235,15 +235,24 @@ typedef struct KameraMlaStore {
  *   V[l][slot_j][h] = bf16(            Vstore[l][src_c+j][h] + Uv[l][h][j] Vv[l][h]^T )
  *   pool, store, rope   host structs (read during the call)
  *   d_chunks            device array of n_chunks descriptors
+ *   h_chunks            NULL, or a host copy of the same n_chunks descriptors,
+ *                       read during the call.  It lets the library describe
+ *                       each chunk's U factors to the tensor-memory-access
+ *                       engine, which then moves the U tiles of chunks of rank
+ *                       16, 32, 64 or 128 (the first 112 chunks of a call)
+ *                       without the copy work of a warp.  Results are the same
+ *                       with or without it.  Its pointers and sizes are the ones
+ *                       the copies use, so it must hold exactly d_chunks'
+ *                       contents; any other contents are undefined behaviour.
  *   max_len, max_rank   upper bounds of len and rank over the chunks (size the
  *                       launch; larger chunks are skipped with a d_err bit)
  *   d_err               device int32 or NULL
  * Returns KAMERA_OK or a KAMERA_ERR_* code (nothing enqueued on error).
  */
 int kamera_relocate_patch(const KameraGqaPool* pool, const KameraGqaStore* store,
-                          const KameraRope* rope, const KameraChunk* d_chunks, int32_t n_chunks,
-                          int32_t max_len, int32_t max_rank, int32_t* d_err,
-                          struct CUstream_st* stream);
+                          const KameraRope* rope, const KameraChunk* d_chunks,
+                          const KameraChunk* h_chunks, int32_t n_chunks, int32_t max_len,
+                          int32_t max_rank, int32_t* d_err, struct CUstream_st* stream);
 
 /*
  * Sliding-window survival in place (technical summary section 3.2): for every
@@ -262,11 +271,13 @@ int kamera_slide_inplace(const KameraSlidePool* pool, const KameraRope* rope,
  *   c_KV'   = bf16( c_KV + Uc[l][j] Vc[l]^T )                (bit copy when rank == 0)
  *   k_rope' = bf16( R(delta_c) k_rope + Ur[l][j] Vr[l]^T )
  * rope->rot_offset/rot_dim are relative to k_rope (usually 0 / rope_dim).
+ * Arguments as for kamera_relocate_patch (h_chunks: NULL or a host copy of
+ * d_chunks, whose Uc and Ur tiles it lets the copy engine move).
  */
 int kamera_mla_relocate_patch(const KameraMlaPool* pool, const KameraMlaStore* store,
                               const KameraRope* rope, const KameraChunk* d_chunks,
-                              int32_t n_chunks, int32_t max_len, int32_t max_rank,
-                              int32_t* d_err, struct CUstream_st* stream);
+                              const KameraChunk* h_chunks, int32_t n_chunks, int32_t max_len,
+                              int32_t max_rank, int32_t* d_err, struct CUstream_st* stream);
 
 /*
  * Host-side check of a HOST copy of a descriptor array (dst_slot_mapping

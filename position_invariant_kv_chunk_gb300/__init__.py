@@ -108,14 +108,14 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C
     lib = C.CDLL(path)
     P = C.POINTER
     lib.kamera_relocate_patch.restype = C.c_int
-    lib.kamera_relocate_patch.argtypes = [P(_GqaPool), P(_GqaStore), P(_Rope), C.c_void_p, C.c_int32,
-                                          C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
+    lib.kamera_relocate_patch.argtypes = [P(_GqaPool), P(_GqaStore), P(_Rope), C.c_void_p, C.c_void_p,
+                                          C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
     lib.kamera_slide_inplace.restype = C.c_int
     lib.kamera_slide_inplace.argtypes = [P(_SlidePool), P(_Rope), C.c_void_p, C.c_int32, C.c_int32,
                                          C.c_void_p, C.c_void_p]
     lib.kamera_mla_relocate_patch.restype = C.c_int
-    lib.kamera_mla_relocate_patch.argtypes = [P(_MlaPool), P(_MlaStore), P(_Rope), C.c_void_p, C.c_int32,
-                                              C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
+    lib.kamera_mla_relocate_patch.argtypes = [P(_MlaPool), P(_MlaStore), P(_Rope), C.c_void_p, C.c_void_p,
+                                              C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
     lib.kamera_validate_chunks.restype = C.c_int
     lib.kamera_validate_chunks.argtypes = [P(_Chunk), C.c_int32, C.c_int64, C.c_int64, C.c_int32,
                                            C.c_int32, P(C.c_int32), P(C.c_int32)]
@@ -123,6 +123,9 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C
     lib.kamera_status_string.argtypes = [C.c_int]
     lib.kamera_abi_version.restype = C.c_int
     lib.kamera_abi_version.argtypes = []
+    if lib.kamera_abi_version() != ABI_VERSION:
+        raise RuntimeError(f"{path} implements Kamera ABI {lib.kamera_abi_version()}, these bindings "
+                           f"expect {ABI_VERSION}; rebuild it with build()")
     if path == _build.LIB_PATH:
         _LIB = lib
     return lib
@@ -130,6 +133,9 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C
 
 def kamera_status_string(status: int) -> str:
     return load_library().kamera_status_string(int(status)).decode()
+
+
+ABI_VERSION = 2   # the KAMERA_ABI_VERSION these bindings marshal for
 
 
 def kamera_abi_version() -> int:
@@ -179,7 +185,9 @@ def pack_chunks(chunks: Sequence, device=None) -> torch.Tensor:
     Accepts ``ChunkSpec``-like objects (attributes src_offset, length, delta,
     rank, slots, patches).  Returns a uint8 tensor on ``device`` (default: the
     slot tensors' device) holding ``len(chunks)`` packed descriptors; the
-    referenced tensors must stay alive while the call runs.
+    referenced tensors must stay alive while the call runs.  The host bytes
+    ride along as the attribute ``kamera_host`` (passed to the relocate entry
+    points as their ``h_chunks`` copy).
     """
     n = len(chunks)
     arr = (_Chunk * max(n, 1))()
@@ -194,7 +202,23 @@ def pack_chunks(chunks: Sequence, device=None) -> torch.Tensor:
     if device is None:
         device = chunks[0].slots.device if n else "cpu"
     host = torch.frombuffer(bytearray(raw), dtype=torch.uint8) if n else torch.empty(0, dtype=torch.uint8)
-    return host.to(device)
+    out = host.to(device)
+    out.kamera_host = host if out.device.type != "cpu" else out
+    return out
+
+
+def _host_copy(chunks: torch.Tensor, host_chunks) -> int:
+    """Address of the host descriptor copy: ``host_chunks`` if given (False: none),
+    else the copy ``pack_chunks`` attached."""
+    if host_chunks is False:
+        return 0
+    if host_chunks is None:
+        host_chunks = getattr(chunks, "kamera_host", None)
+    if host_chunks is None:
+        return 0
+    if host_chunks.device.type != "cpu" or host_chunks.numel() != chunks.numel():
+        raise ValueError("host_chunks must be a CPU copy of the packed descriptors")
+    return _addr(host_chunks)
 
 
 def _stream_handle(stream) -> int:
@@ -219,12 +243,14 @@ def _bf16(t: torch.Tensor, name: str):
 def kamera_relocate_patch(pool_k: torch.Tensor, pool_v: torch.Tensor, store_k: torch.Tensor,
                           store_v: torch.Tensor, rope: Rope, chunks: torch.Tensor, n_chunks: int,
                           max_len: int, max_rank: int, err: Optional[torch.Tensor] = None,
-                          stream=None) -> None:
+                          stream=None, host_chunks=None) -> None:
     """GQA/MHA relocate + patch + paged scatter.
 
     pool_*: bf16 ``[L, S, H, d]`` (layer/slot strides free, head/dim packed);
     store_*: bf16 ``[L, N, H, d]``; chunks: packed descriptors (``pack_chunks``)
-    on the device; err: optional device int32 error word.
+    on the device; err: optional device int32 error word; host_chunks: the
+    host copy of ``chunks`` (default: the one ``pack_chunks`` attached; False:
+    none, every U tile then moves by per-thread copies).
     """
     for t, nm in ((pool_k, "pool_k"), (pool_v, "pool_v"), (store_k, "store_k"), (store_v, "store_v")):
         _bf16(t, nm)
@@ -241,8 +267,8 @@ def kamera_relocate_patch(pool_k: torch.Tensor, pool_v: torch.Tensor, store_k: t
     store = _GqaStore(_addr(store_k), _addr(store_v), store_k.shape[1], store_k.stride(0), store_k.stride(1))
     r, keep = rope._c()
     rc = load_library().kamera_relocate_patch(C.byref(pool), C.byref(store), C.byref(r), _addr(chunks),
-                                              int(n_chunks), int(max_len), int(max_rank), _addr(err),
-                                              _stream_handle(stream))
+                                              _host_copy(chunks, host_chunks), int(n_chunks), int(max_len),
+                                              int(max_rank), _addr(err), _stream_handle(stream))
     del keep
     _check(rc, "kamera_relocate_patch")
 
@@ -267,9 +293,10 @@ def kamera_slide_inplace(pool_k: torch.Tensor, rope: Rope, chunks: torch.Tensor,
 
 def kamera_mla_relocate_patch(pool: torch.Tensor, store: torch.Tensor, kv_lora: int, rope: Rope,
                               chunks: torch.Tensor, n_chunks: int, max_len: int, max_rank: int,
-                              err: Optional[torch.Tensor] = None, stream=None) -> None:
+                              err: Optional[torch.Tensor] = None, stream=None, host_chunks=None) -> None:
     """MLA relocate + patch + paged scatter.  pool: bf16 ``[L, S, kv_lora + rope]``;
-    store: bf16 ``[L, N, kv_lora + rope]``; rope offsets relative to k_rope."""
+    store: bf16 ``[L, N, kv_lora + rope]``; rope offsets relative to k_rope;
+    host_chunks as for ``kamera_relocate_patch``."""
     _bf16(pool, "pool")
     _bf16(store, "store")
     for t, nm in ((pool, "pool"), (store, "store")):
@@ -282,8 +309,8 @@ def kamera_mla_relocate_patch(pool: torch.Tensor, store: torch.Tensor, kv_lora: 
     s = _MlaStore(_addr(store), store.shape[1], store.stride(0), store.stride(1))
     r, keep = rope._c()
     rc = load_library().kamera_mla_relocate_patch(C.byref(p), C.byref(s), C.byref(r), _addr(chunks),
-                                                  int(n_chunks), int(max_len), int(max_rank), _addr(err),
-                                                  _stream_handle(stream))
+                                                  _host_copy(chunks, host_chunks), int(n_chunks), int(max_len),
+                                                  int(max_rank), _addr(err), _stream_handle(stream))
     del keep
     _check(rc, "kamera_mla_relocate_patch")
 

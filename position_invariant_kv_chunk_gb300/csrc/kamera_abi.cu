@@ -117,7 +117,7 @@ int check_strided(const void* base, int64_t L, int64_t ls, int64_t rows, int64_t
 // its shape fits (head_dim 64/128, whole-head rotary; MLA c_KV in 128-blocks
 // and a 64/128 k_rope), the CUDA-core path otherwise.  KAMERA_PATH=simt or
 // =umma in the environment pins one of them (testing both on one input).
-int launch(const RowsParams& p, int family, cudaStream_t stream)
+int launch(const RowsParams& p, int family, const KameraChunk* h_chunks, cudaStream_t stream)
 {
     const char* force = std::getenv("KAMERA_PATH");
     const bool want_simt = force && std::strcmp(force, "simt") == 0;
@@ -125,7 +125,7 @@ int launch(const RowsParams& p, int family, cudaStream_t stream)
     if (!want_simt && family != FAMILY_SLIDE && umma_supported(p, family)) {
         if (umma_smem_bytes(p) > 227u * 1024u)
             return KAMERA_ERR_UNSUPPORTED;
-        return launch_umma(p, family, stream) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
+        return launch_umma(p, family, h_chunks, stream) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
     }
     if (want_umma)
         return KAMERA_ERR_UNSUPPORTED;
@@ -157,8 +157,8 @@ const char* kamera_status_string(int status)
 }
 
 int kamera_relocate_patch(const KameraGqaPool* pool, const KameraGqaStore* store, const KameraRope* rope,
-                          const KameraChunk* d_chunks, int32_t n_chunks, int32_t max_len, int32_t max_rank,
-                          int32_t* d_err, struct CUstream_st* stream)
+                          const KameraChunk* d_chunks, const KameraChunk* h_chunks, int32_t n_chunks,
+                          int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream)
 {
     if (!pool || !store || !rope)
         return KAMERA_ERR_INVALID_ARGUMENT;
@@ -208,7 +208,7 @@ int kamera_relocate_patch(const KameraGqaPool* pool, const KameraGqaStore* store
     p.max_len = max_len;
     p.max_rank = max_rank;
     p.err = d_err;
-    return launch(p, FAMILY_GQA, reinterpret_cast<cudaStream_t>(stream));
+    return launch(p, FAMILY_GQA, h_chunks, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kamera_slide_inplace(const KameraSlidePool* pool, const KameraRope* rope, const KameraChunk* d_chunks,
@@ -243,12 +243,12 @@ int kamera_slide_inplace(const KameraSlidePool* pool, const KameraRope* rope, co
     p.max_len = max_len;
     p.max_rank = 0;
     p.err = d_err;
-    return launch(p, FAMILY_SLIDE, reinterpret_cast<cudaStream_t>(stream));
+    return launch(p, FAMILY_SLIDE, nullptr, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kamera_mla_relocate_patch(const KameraMlaPool* pool, const KameraMlaStore* store, const KameraRope* rope,
-                              const KameraChunk* d_chunks, int32_t n_chunks, int32_t max_len, int32_t max_rank,
-                              int32_t* d_err, struct CUstream_st* stream)
+                              const KameraChunk* d_chunks, const KameraChunk* h_chunks, int32_t n_chunks,
+                              int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream)
 {
     if (!pool || !store || !rope)
         return KAMERA_ERR_INVALID_ARGUMENT;
@@ -291,7 +291,7 @@ int kamera_mla_relocate_patch(const KameraMlaPool* pool, const KameraMlaStore* s
     p.max_len = max_len;
     p.max_rank = max_rank;
     p.err = d_err;
-    return launch(p, FAMILY_MLA, reinterpret_cast<cudaStream_t>(stream));
+    return launch(p, FAMILY_MLA, h_chunks, reinterpret_cast<cudaStream_t>(stream));
 }
 
 int kamera_validate_chunks(const KameraChunk* h_chunks, int32_t n_chunks, int64_t num_store_rows, int64_t num_slots,

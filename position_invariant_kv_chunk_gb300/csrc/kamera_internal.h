@@ -5,6 +5,8 @@
 #include <cstddef>
 #include <cuda_runtime.h>
 
+#include "kamera.h"
+
 namespace kamera {
 
 enum Family { FAMILY_GQA = 0, FAMILY_MLA = 1, FAMILY_SLIDE = 2 };
@@ -18,6 +20,7 @@ size_t simt_smem_bytes(const RowsParams& p, int family, int tile_tokens);
 // Tensor-core path (tcgen05 MMA for the rank-m patch; relocation with rank > 0).
 bool umma_supported(const RowsParams& p, int family);
 size_t umma_smem_bytes(const RowsParams& p);
-cudaError_t launch_umma(const RowsParams& p, int family, cudaStream_t stream);
+// h_chunks: NULL or a host copy of the descriptors (U tiles then move by TMA).
+cudaError_t launch_umma(const RowsParams& p, int family, const KameraChunk* h_chunks, cudaStream_t stream);
 
 }  // namespace kamera

@@ -242,6 +242,20 @@ __device__ __forceinline__ uint64_t desc_k_sw128(uint32_t saddr)
            | ((uint64_t)2 << 61);              // swizzle: 128 B
 }
 
+// The same for an operand whose rows are 64 bytes (32 ranks, 64-byte swizzle,
+// 8-row groups 512 bytes apart) or 32 bytes (16 ranks, 32-byte swizzle, 256
+// bytes apart): the layouts a tiled TMA load with that swizzle writes.
+__device__ __forceinline__ uint64_t desc_k_sw64(uint32_t saddr)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(512 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)4 << 61);
+}
+__device__ __forceinline__ uint64_t desc_k_sw32(uint32_t saddr)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)1 << 16) | ((uint64_t)(256 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)6 << 61);
+}
+
 // Instruction descriptor: bf16 x bf16 -> fp32, both operands K-major, M x N.
 __host__ __device__ constexpr uint32_t idesc_bf16_f32(int M, int N)
 {

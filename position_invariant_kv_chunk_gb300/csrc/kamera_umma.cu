@@ -60,6 +60,8 @@ constexpr int kRegCap = 16384 / (32 * ((kThreads / 32 + 3) / 4));
 constexpr uint32_t kTmemCols = 2 * kWMax;       // two accumulators
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr int kTailRows = 16;                   // box height of the tail tensor maps
+constexpr int kMapChunksFew = 8;                // U map tables: calls of <= 8 chunks ...
+constexpr int kMapChunksMany = 112;             // ... and larger ones (the parameter block stays < 32 KB)
 
 struct UmmaParams {
     CUtensorMap map_full[2];   // per array (K|V, or the MLA row): 64 x 128 boxes
@@ -68,6 +70,23 @@ struct UmmaParams {
     int32_t family;
     int32_t Z;                 // row segments
 };
+
+// Per-call U tensor maps (from a host copy of the descriptors): chunk c < MC
+// with u_rank[c] == its rank > 0 has maps 2c (K or c_KV factor) and 2c+1
+// (V or k_rope factor) over its [L*FH][len][m] U array; boxes of
+// min(m, 64) ranks x 128 rows, swizzled to match the MMA operand layout.
+template <int MC>
+struct UmmaLaunch {
+    UmmaParams core;
+    CUtensorMap map_u[2 * MC];
+    int32_t u_rank[MC];
+};
+
+template <int MC>
+__device__ __forceinline__ bool u_mapped(const UmmaLaunch<MC>& P, int c, int rank)
+{
+    return rank > 0 && c < MC && P.u_rank[c] == rank;
+}
 
 template <int KA>
 struct Geometry {
@@ -162,7 +181,7 @@ struct TileInfo {
 };
 
 struct Shared {
-    uint64_t full[4], empty[4], tfull[2], tempty[2], uempty[3], vmempty[2], mmadone;
+    uint64_t full[4], empty[4], tfull[2], tempty[2], uempty[3], ufull[3], vmempty[2], mmadone;
     uint32_t tmem_base;
     int32_t abort_flag;
     int32_t start_lz, start_rem, start_c, start_t, count;
@@ -408,9 +427,10 @@ __device__ __forceinline__ void epilogue_dispatch(int mode, bool patch, uint32_t
 
 }  // namespace
 
-template <int KA>
-__global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_constant__ UmmaParams p)
+template <int KA, int MC>
+__global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_constant__ UmmaLaunch<MC> P)
 {
+    const UmmaParams& p = P.core;
     using G = Geometry<KA>;
     extern __shared__ uint8_t smem_raw[];
     const uint32_t raw = ptx::smem_addr(smem_raw);
@@ -434,8 +454,10 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             ptx::mbar_init(ptx::smem_addr(&sh.tempty[i]), kEpiWarps);
             ptx::mbar_init(ptx::smem_addr(&sh.vmempty[i]), 1);
         }
-        for (int i = 0; i < G::D; ++i)
+        for (int i = 0; i < G::D; ++i) {
             ptx::mbar_init(ptx::smem_addr(&sh.uempty[i]), 1);
+            ptx::mbar_init(ptx::smem_addr(&sh.ufull[i]), 1);
+        }
         ptx::mbar_init(ptx::smem_addr(&sh.mmadone), 1);
         sh.abort_flag = 0;
         ptx::fence_barrier_init();
@@ -520,7 +542,8 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
 
     if (warp == 0 && count > 0) {
         // ------------------------------------------------------ producer
-        int issued = 0;
+        int issued = 0, pu = 0;
+        uint32_t upar = 0, uload = 0;   // per U buffer: phase parity of its TMA loads; last use was a TMA load
         for (int i = 0; i < count; ++i, cur.next(p)) {
             const int s = i % G::S, rnd = i / G::S;
             if (!warp_wait(ptx::smem_addr(&sh.empty[s]), (rnd & 1) ^ 1, abort_flag, r.err))
@@ -551,6 +574,27 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                 __syncwarp();
                 if (lane == 0)
                     sh.stage_tag[s] = cur.c;
+            }
+            if (ch.rank > 0) {   // U tile of a mapped chunk: one or two swizzled boxes into the U ring
+                const int u = pu % G::D;
+                if (u_mapped(P, cur.c, ch.rank)) {
+                    if (!warp_wait(ptx::smem_addr(&sh.uempty[u]), ((pu / G::D) & 1) ^ 1, abort_flag, r.err))
+                        break;
+                    if (lane == 0) {
+                        const int nbox = ch.rank > 64 ? 2 : 1;
+                        const uint32_t ufull = ptx::smem_addr(&sh.ufull[u]);
+                        ptx::mbar_arrive_expect_tx(ufull, (uint32_t)(nbox * min(ch.rank, 64) * 2 * kTileM));
+                        const CUtensorMap* map = &P.map_u[2 * cur.c + (sg.u_idx >> 1)];
+                        for (int x = 0; x < nbox; ++x)
+                            ptx::tma_load_3d(ubase + u * G::kUBytes + x * kAtomBytes, map, 64 * x, tok0,
+                                             l * sg.FH + sg.fh, ufull);
+                    }
+                    upar ^= 1u << u;
+                    uload |= 1u << u;
+                } else {
+                    uload &= ~(1u << u);
+                }
+                ++pu;
             }
             {   // the tile's destination slots (-1 past its last row) and its description
                 const uint32_t slots = base + s * kStageBytes + kSlotOff;
@@ -588,10 +632,15 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             __syncwarp();
             ++issued;
         }
-        // no TMA load may still be writing shared memory when the CTA exits
-        if (lane == 0)
+        // no TMA load or copy may still be writing shared memory when the CTA exits
+        ptx::cp_async_wait<0>();
+        if (lane == 0) {
             for (int j = max(0, issued - G::S); j < issued; ++j)
                 drain_bar(ptx::smem_addr(&sh.full[j % G::S]), (j / G::S) & 1);
+            for (int u = 0; u < G::D; ++u)
+                if ((uload >> u) & 1u)
+                    drain_bar(ptx::smem_addr(&sh.ufull[u]), ((upar >> u) & 1u) ^ 1u);
+        }
         __syncwarp();
     } else if (warp == 1 && count > 0) {
         // ------------------------------------------- operands + MMA
@@ -622,9 +671,11 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                                          sg.w, m, mpad, (uint32_t)sg.w * 128u, lane);
                     }
                     const int u = ld_u % G::D;
-                    if (!stop && !warp_wait(ptx::smem_addr(&sh.uempty[u]), ((ld_u / G::D) & 1) ^ 1, abort_flag, r.err))
+                    const bool by_tma = u_mapped(P, ld.c, m);   // the producer loads this U tile
+                    if (!by_tma && !stop &&
+                        !warp_wait(ptx::smem_addr(&sh.uempty[u]), ((ld_u / G::D) & 1) ^ 1, abort_flag, r.err))
                         stop = true;
-                    if (!stop) {
+                    if (!by_tma && !stop) {
                         const int tok0 = ld.t * kTileM;
                         load_operand(ubase + u * G::kUBytes,
                                      patch_ptr(ch, sg.u_idx) +
@@ -641,6 +692,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
         for (int j = 0; j < G::LA; ++j)
             issue();
         int k = 0, vjob = -1, plz = -1, pc = -1, issued_mma = 0;
+        uint32_t upar = 0;   // per U buffer: phase parity of the producer's TMA loads
         for (int i = 0; i < count && !stop; ++i) {
             ptx::cp_async_wait<G::LA - 1>();   // this tile's operand copies have landed ...
             ptx::fence_proxy_async();          // ... and are visible to the tensor cores
@@ -657,20 +709,29 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             if (m > 0) {
                 if (new_job)
                     ++vjob;
+                const bool by_tma = u_mapped(P, c_now, m);
                 if (lane == 0) {
-                    const int acc = k & 1;
-                    if (!wait_bar(ptx::smem_addr(&sh.tempty[acc]), ((k >> 1) & 1) ^ 1, abort_flag, r.err)) {
+                    const int acc = k & 1, u = k % G::D;
+                    bool ok = true;
+                    if (by_tma) {
+                        ok = wait_bar(ptx::smem_addr(&sh.ufull[u]), (upar >> u) & 1u, abort_flag, r.err);
+                        upar ^= 1u << u;
+                    }
+                    if (!ok || !wait_bar(ptx::smem_addr(&sh.tempty[acc]), ((k >> 1) & 1) ^ 1, abort_flag, r.err)) {
                         stop = true;
                     } else {
                         ptx::tc_fence_after();
-                        const uint32_t a0 = ubase + (k % G::D) * G::kUBytes;
+                        const uint32_t a0 = ubase + u * G::kUBytes;
                         const uint32_t b0 = vbase + (vjob & 1) * G::kVBytes;
                         const uint32_t idesc = ptx::idesc_bf16_f32(kTileM, sg.w);
                         const uint32_t d = tmem + acc * kWMax;
                         const int steps = (m + 15) >> 4;
                         for (int q = 0; q < steps; ++q) {
                             const uint32_t koff = (q & 3) * 32;
-                            const uint64_t ad = ptx::desc_k_sw128(a0 + (q >> 2) * kAtomBytes + koff);
+                            // A as the TMA load laid it out (rows of 2m bytes, m < 64) or in 64-rank atoms
+                            const uint64_t ad = by_tma && m == 16   ? ptx::desc_k_sw32(a0)
+                                                : by_tma && m == 32 ? ptx::desc_k_sw64(a0 + koff)
+                                                                    : ptx::desc_k_sw128(a0 + (q >> 2) * kAtomBytes + koff);
                             const uint64_t bd = ptx::desc_k_sw128(b0 + (q >> 2) * (uint32_t)sg.w * 128u + koff);
                             ptx::umma_bf16(d, ad, bd, idesc, q > 0 ? 1u : 0u);
                         }
@@ -845,9 +906,59 @@ bool make_map(CUtensorMap* m, const void* base, int64_t L, int64_t rows, int64_t
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// 3-D map over one chunk's U factor, [L*FH][len][m] bf16 (m-contiguous):
+// boxes of min(m, 64) ranks x 128 rows x 1, swizzled like the MMA operand
+// (rows of 32, 64 or 128 bytes); rows past len read as zero.
+bool make_u_map(CUtensorMap* m, const void* base, int64_t planes, int64_t len, int rank)
+{
+    auto fn = encode_fn();
+    if (!fn || !base || (reinterpret_cast<uintptr_t>(base) & 15u) || len < 1)
+        return false;
+    const int inner = rank < 64 ? rank : 64;
+    cuuint64_t dims[3] = {(cuuint64_t)rank, (cuuint64_t)len, (cuuint64_t)planes};
+    cuuint64_t strides[2] = {(cuuint64_t)rank * 2u, (cuuint64_t)(len * rank * 2)};
+    cuuint32_t box[3] = {(cuuint32_t)inner, (cuuint32_t)kTileM, 1u};
+    cuuint32_t estr[3] = {1u, 1u, 1u};
+    const CUtensorMapSwizzle sw = rank == 16   ? CU_TENSOR_MAP_SWIZZLE_32B
+                                  : rank == 32 ? CU_TENSOR_MAP_SWIZZLE_64B
+                                               : CU_TENSOR_MAP_SWIZZLE_128B;
+    return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, sw, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+template <int KA, int MC>
+cudaError_t launch_kernel(const UmmaParams& core, const KameraChunk* h_chunks, int sms, cudaStream_t stream)
+{
+    UmmaLaunch<MC> local;
+    std::memset(&local, 0, sizeof(local));
+    local.core = core;
+    const RowsParams& rp = core.r;
+    if (h_chunks) {
+        const int64_t planes = core.family == FAMILY_GQA ? (int64_t)rp.L * rp.H : rp.L;
+        const int n = rp.n_chunks < MC ? rp.n_chunks : MC;
+        for (int c = 0; c < n; ++c) {
+            const KameraChunk& ch = h_chunks[c];
+            const int m = ch.rank;
+            if ((m != 16 && m != 32 && m != 64 && m != 128) || m > rp.max_rank || ch.len < 1)
+                continue;
+            if (make_u_map(&local.map_u[2 * c], ch.patch_ptrs[0], planes, ch.len, m) &&
+                make_u_map(&local.map_u[2 * c + 1], ch.patch_ptrs[2], planes, ch.len, m))
+                local.u_rank[c] = m;
+        }
+    }
+    const size_t smem = smem_bytes_for<KA>();
+    cudaError_t e = cudaFuncSetAttribute(relocate_patch_umma_kernel<KA, MC>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess)
+        return e;
+    relocate_patch_umma_kernel<KA, MC><<<sms, kThreads, smem, stream>>>(local);
+    return cudaGetLastError();
+}
+
 }  // namespace
 
-cudaError_t launch_umma(const RowsParams& rp, int family, cudaStream_t stream)
+cudaError_t launch_umma(const RowsParams& rp, int family, const KameraChunk* h_chunks, cudaStream_t stream)
 {
     UmmaParams p;
     std::memset(&p, 0, sizeof(p));
@@ -867,22 +978,13 @@ cudaError_t launch_umma(const RowsParams& rp, int family, cudaStream_t stream)
         e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess)
         return e;
-    if (rp.max_rank > 64) {
-        const size_t smem = smem_bytes_for<2>();
-        e = cudaFuncSetAttribute(relocate_patch_umma_kernel<2>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        relocate_patch_umma_kernel<2><<<sms, kThreads, smem, stream>>>(p);
-    } else {
-        const size_t smem = smem_bytes_for<1>();
-        e = cudaFuncSetAttribute(relocate_patch_umma_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 (int)smem);
-        if (e != cudaSuccess)
-            return e;
-        relocate_patch_umma_kernel<1><<<sms, kThreads, smem, stream>>>(p);
-    }
-    return cudaGetLastError();
+    // a small map table for small calls keeps the launch's parameter block short
+    const bool few = rp.n_chunks <= kMapChunksFew;
+    if (rp.max_rank > 64)
+        return few ? launch_kernel<2, kMapChunksFew>(p, h_chunks, sms, stream)
+                   : launch_kernel<2, kMapChunksMany>(p, h_chunks, sms, stream);
+    return few ? launch_kernel<1, kMapChunksFew>(p, h_chunks, sms, stream)
+               : launch_kernel<1, kMapChunksMany>(p, h_chunks, sms, stream);
 }
 
 }  // namespace kamera

@@ -90,6 +90,11 @@ def max_rank(wl: W.Workload) -> int:
     return max((c.rank for c in wl.chunks), default=0)
 
 
+# False: relocate calls withhold the host copy of the descriptors, so every
+# factor tile moves by per-thread copies instead of tensor-map loads
+USE_HOST_COPY = True
+
+
 def run_gpu(wl: W.Workload, chunks_dev=None, err=None, max_len=None, mrank=None, stream=None):
     """One call of the workload's entry point through the C ABI."""
     if chunks_dev is None:
@@ -97,12 +102,13 @@ def run_gpu(wl: W.Workload, chunks_dev=None, err=None, max_len=None, mrank=None,
     n = len(wl.chunks)
     ml = wl.max_len if max_len is None else max_len
     mr = max_rank(wl) if mrank is None else mrank
+    hc = None if USE_HOST_COPY else False
     if wl.kind == "gqa":
         K.kamera_relocate_patch(wl.pool_k, wl.pool_v, wl.store_k, wl.store_v, rope_of(wl), chunks_dev, n,
-                                ml, mr, err, stream)
+                                ml, mr, err, stream, host_chunks=hc)
     elif wl.kind == "mla":
         K.kamera_mla_relocate_patch(wl.pool_k, wl.store_k, wl.kv_lora, rope_of(wl), chunks_dev, n, ml, mr,
-                                    err, stream)
+                                    err, stream, host_chunks=hc)
     else:
         K.kamera_slide_inplace(wl.pool_k, rope_of(wl), chunks_dev, n, ml, err, stream)
     return chunks_dev

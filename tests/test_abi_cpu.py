@@ -69,7 +69,9 @@ def test_struct_layouts_match_header(tmp_path):
 
 
 def test_status_strings_and_version():
-    assert K.kamera_abi_version() == 1
+    hdr = open(os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "include", "kamera.h")).read()
+    declared = int(re.search(r"#define KAMERA_ABI_VERSION (\d+)", hdr).group(1))
+    assert K.kamera_abi_version() == declared == K.ABI_VERSION
     for code in range(5):
         assert K.kamera_status_string(code)
     assert K.kamera_status_string(99) == "unknown status"

@@ -15,11 +15,14 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=["auto", "simt"])
+@pytest.fixture(params=["auto", "copies", "simt"])
 def path(request, monkeypatch):
     """Run the case on the default kernel choice (tensor-core path for patched
-    GQA/MHA/MLA calls) and pinned to the CUDA-core path."""
-    monkeypatch.setenv("KAMERA_PATH", request.param)
+    GQA/MHA/MLA calls; factor tiles by tensor-map loads where the host copy of
+    the descriptors allows), on the same choice without the host copy (every
+    factor tile by per-thread copies), and pinned to the CUDA-core path."""
+    monkeypatch.setenv("KAMERA_PATH", "simt" if request.param == "simt" else "auto")
+    monkeypatch.setattr(Hn, "USE_HOST_COPY", request.param != "copies")
     return request.param
 
 
@@ -57,13 +60,34 @@ def test_gqa_rope_layouts(pairing, rot_dim, rot_offset, path):
     Hn.check_parity(wl, h, f"rope {pairing}/{rot_dim}/{rot_offset}")
 
 
-@pytest.mark.parametrize("m", [1, 3, 8, 16, 17, 48, 64, 96, 128])
+@pytest.mark.parametrize("m", [1, 3, 8, 16, 17, 32, 48, 64, 96, 128])
 def test_gqa_ranks(m, path):
     spec = W.scaled(W.qwen_recall(), L=1, H=2, lens=(130, 5), m=m)
     wl = W.make(spec, DEV)
     h = Hn.snapshot(wl)
     Hn.run_gpu(wl)
     Hn.check_parity(wl, h, f"rank {m}")
+
+
+@pytest.mark.parametrize("m", [16, 32, 64, 128])
+def test_mla_ranks(m, path):
+    """Every rank whose factor tiles a tensor map can carry, on both MLA channels."""
+    spec = W.scaled(W.dsv2_mla(), L=2, lens=(300, 128, 9), m=m)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    Hn.run_gpu(wl)
+    Hn.check_parity(wl, h, f"mla rank {m}")
+
+
+def test_more_chunks_than_map_table(path):
+    """A call with more chunks than the tensor-map table: the chunks past it
+    move their factor tiles by per-thread copies within the same launch."""
+    spec = W.scaled(W.qwen_recall(), L=1, H=2, lens=tuple([37, 130, 64, 1, 200] * 24), m=32)
+    wl = W.make(spec, DEV)
+    assert len(wl.chunks) == 120
+    h = Hn.snapshot(wl)
+    Hn.run_gpu(wl)
+    Hn.check_parity(wl, h, "120 chunks")
 
 
 @pytest.mark.parametrize("d", [64, 128, 256])
