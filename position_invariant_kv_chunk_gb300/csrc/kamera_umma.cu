@@ -25,8 +25,11 @@
 //             16-byte stores.
 //
 // The grid is persistent (one CTA per SM).  The tiles of a call, ordered
-// (layer, segment, chunk, tile), are split into equal contiguous ranges, so
-// consecutive tiles of a CTA share V_m and the cos/sin table.  Every wait is
+// (layer, chunk, segment, tile), are split into equal contiguous ranges:
+// consecutive tiles of a CTA share V_m (a job is one chunk, layer and segment)
+// and the cos/sin table (one chunk), and every range mixes the segments of its
+// chunks (rotated keys and plain values; 128-wide c_KV blocks and the narrower
+// k_rope) in the proportion of the whole call, which keeps the CTAs' work even.  Every wait is
 // bounded in time: on expiry the CTA records KAMERA_DEVERR_TIMEOUT, drains its
 // own copies and MMAs, frees TMEM and returns.
 #include <cstdint>
@@ -53,10 +56,17 @@ constexpr int kStageBytes = kRowsBytes + 2048;  // rows + table + slots, 1024-al
 constexpr int kAtomBytes = kTileM * 128;        // one 64-rank K atom of a 128-row operand
 constexpr int kEpiPerSub = 3;                   // epilogue warps per TMEM sub-partition
 constexpr int kEpiWarps = 4 * kEpiPerSub;
-constexpr int kThreads = 32 * (2 + kEpiWarps);  // producer, MMA, epilogue warps
+constexpr int kEpiWarp0 = 4;                     // warpgroup 0: producer, MMA and two idle warps
+constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 // Warp w runs on SM sub-partition w % 4, whose register file holds 16384
-// registers: the busiest sub-partition bounds the registers per thread.
+// registers: the busiest sub-partition bounds the registers per thread at
+// launch.  Warpgroup 0 then lowers its budget and the epilogue warpgroups
+// take the freed registers (each sub-partition holds one warp of each group).
 constexpr int kRegCap = 16384 / (32 * ((kThreads / 32 + 3) / 4));
+constexpr int kRegsLow = 72;                     // producer / MMA warpgroup
+constexpr int kRegsEpi = 144;                    // epilogue warpgroups
+static_assert(128 * kRegsLow + 32 * kEpiWarps * kRegsEpi <= kThreads * kRegCap, "register split exceeds the launch");
+static_assert(32 * (kRegsLow + kEpiPerSub * kRegsEpi) <= 16384, "register split exceeds a sub-partition");
 constexpr uint32_t kTmemCols = 2 * kWMax;       // two accumulators
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr int kTailRows = 16;                   // box height of the tail tensor maps
@@ -150,7 +160,8 @@ __device__ __forceinline__ int chunk_tiles(const KameraChunk& ch, const RowsPara
     return check_chunk(ch, r, false) ? 0 : (ch.len + kTileM - 1) / kTileM;
 }
 
-// Walks the CTA's tiles in order; every role runs its own copy.
+// Walks the CTA's tiles in (layer, chunk, segment, tile) order; every role
+// runs its own copy.  lz = layer * Z + segment.
 struct Cursor {
     int lz, c, t, ntile;
     KameraChunk ch;
@@ -165,10 +176,14 @@ struct Cursor {
         if (++t < ntile)
             return;
         t = 0;
+        const int l = lz / p.Z;
+        if (++lz < (l + 1) * p.Z)   // the chunk's next segment
+            return;
+        lz = l * p.Z;               // segment 0 of the next chunk with tiles
         do {
             if (++c == p.r.n_chunks) {
                 c = 0;
-                ++lz;
+                lz += p.Z;
             }
             load(p);
         } while (ntile == 0);
@@ -498,26 +513,29 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
         const int64_t T = TC * r.L * p.Z;
         const int64_t b0 = T * blockIdx.x / gridDim.x, b1 = T * (blockIdx.x + 1) / gridDim.x;
         sh.count = (int32_t)(b1 - b0);
-        sh.start_lz = TC ? (int32_t)(b0 / TC) : 0;
-        sh.start_rem = (int32_t)(TC ? b0 % TC : 0);   // tile offset inside the (layer, segment) block
+        const int64_t LB = TC * p.Z;   // tiles of one layer
+        sh.start_lz = LB ? (int32_t)(b0 / LB) * p.Z : 0;   // layer of the first tile (segment added below)
+        sh.start_rem = (int32_t)(LB ? b0 % LB : 0);         // its offset inside the layer
         sh.start_c = 0;
         sh.start_t = 0;
     }
     __syncthreads();
     if (sh.count > 0) {
         const int64_t rem = sh.start_rem;
-        const int64_t lo = sh.part[tid];
-        if (rem >= lo && rem < lo + mine) {   // exactly one thread owns the starting tile
+        const int64_t lo = (int64_t)p.Z * sh.part[tid];   // a chunk holds Z * (its tiles) of a layer
+        if (rem >= lo && rem < lo + (int64_t)p.Z * mine) {   // exactly one thread owns the starting tile
             int64_t acc = lo;
             for (int c = c_lo; c < c_hi; ++c) {
                 const KameraChunk ch = r.chunks[c];
                 const int nt = chunk_tiles(ch, r);
-                if (rem < acc + nt) {
-                    sh.start_t = (int32_t)(rem - acc);
+                if (rem < acc + (int64_t)p.Z * nt) {
+                    const int64_t o = rem - acc;
+                    sh.start_lz += (int32_t)(o / nt);
+                    sh.start_t = (int32_t)(o % nt);
                     sh.start_c = c;
                     break;
                 }
-                acc += nt;
+                acc += (int64_t)p.Z * nt;
             }
         }
     }
@@ -540,6 +558,8 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
 
     const uint32_t ubase = base + G::kUOff, vbase = base + G::kVOff;
 
+    if (warp < kEpiWarp0) {
+    ptx::setmaxnreg_dec<kRegsLow>();
     if (warp == 0 && count > 0) {
         // ------------------------------------------------------ producer
         int issued = 0, pu = 0;
@@ -753,10 +773,13 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             drain_bar(ptx::smem_addr(&sh.mmadone), 0);
         }
         __syncwarp();
-    } else if (warp >= 2 && count > 0) {
+    }
+    } else {
+    ptx::setmaxnreg_inc<kRegsEpi>();
+    if (count > 0) {
         // ------------------------------------------------------ epilogue
         const int q = warp & 3;         // TMEM sub-partition of this warp
-        const int hh = (warp - 2) >> 2; // which share of the columns this warp owns (0..kEpiPerSub-1)
+        const int hh = (warp - kEpiWarp0) >> 2;   // which share of the columns this warp owns (0..kEpiPerSub-1)
         const int tt = q * 32 + lane;   // token row of the tile = TMEM lane
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
         int k = 0;
@@ -834,6 +857,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             if (lane == 0)
                 ptx::mbar_arrive(ptx::smem_addr(&sh.empty[s]));
         }
+    }
     }
     ptx::tc_fence_before();
     __syncthreads();
