@@ -115,8 +115,9 @@ int check_strided(const void* base, int64_t L, int64_t ls, int64_t rows, int64_t
 
 // Kernel choice: the tensor-core path whenever the call carries patches and
 // its shape fits (head_dim 64/128, whole-head rotary; MLA c_KV in 128-blocks
-// and a 64/128 k_rope), the CUDA-core path otherwise.  KAMERA_PATH=simt or
-// =umma in the environment pins one of them (testing both on one input).
+// and a 64/128 k_rope), the slide kernel for the in-place rotation when its
+// rotary units tile a block, the CUDA-core path otherwise.  KAMERA_PATH=simt
+// or =umma in the environment pins one of them (testing both on one input).
 int launch(const RowsParams& p, int family, const KameraChunk* h_chunks, cudaStream_t stream)
 {
     const char* force = std::getenv("KAMERA_PATH");
@@ -129,6 +130,8 @@ int launch(const RowsParams& p, int family, const KameraChunk* h_chunks, cudaStr
     }
     if (want_umma)
         return KAMERA_ERR_UNSUPPORTED;
+    if (!want_simt && family == FAMILY_SLIDE && p.L <= 65535 && slide_supported(p))
+        return launch_slide(p, stream) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
     const size_t smem = simt_smem_bytes(p, family, 64);
     if (smem > 227u * 1024u)
         return KAMERA_ERR_UNSUPPORTED;

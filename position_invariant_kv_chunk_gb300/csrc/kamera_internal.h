@@ -17,6 +17,11 @@ struct RowsParams;
 cudaError_t launch_simt(const RowsParams& p, int family, cudaStream_t stream);
 size_t simt_smem_bytes(const RowsParams& p, int family, int tile_tokens);
 
+// Sliding-window survival (in place, rotation only): one fixed rotary unit
+// per thread; shapes whose units per row divide the block (else the CUDA-core path).
+bool slide_supported(const RowsParams& p);
+cudaError_t launch_slide(const RowsParams& p, cudaStream_t stream);
+
 // Tensor-core path (tcgen05 MMA for the rank-m patch; relocation with rank > 0).
 bool umma_supported(const RowsParams& p, int family);
 size_t umma_smem_bytes(const RowsParams& p);

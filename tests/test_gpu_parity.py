@@ -134,7 +134,7 @@ def test_mla_rank0_c_kv_bit_exact(path):
     Hn.check_parity(wl, h, "mla rank0")   # includes the bit-exact c_KV check
 
 
-def test_slide_mla_rope_subrange():
+def test_slide_mla_rope_subrange(path):
     """Slide on an MLA pool: only k_rope (offset 512, 64 wide, interleaved) turns."""
     spec = W.GqaSpec("mla_slide", "slide", L=2, H=1, d=576, base=1e4, lens=(200, 64), deltas=(-4096, 17),
                      m=0, page=64, pairing=K.INTERLEAVED, rot_dim=64, rot_offset=512, evicted=100, window=364)
@@ -147,7 +147,7 @@ def test_slide_mla_rope_subrange():
     assert np.array_equal(gk[:, sl, :, :512], h.pool_k[:, sl, :, :512])
 
 
-def test_slide_zero_delta_is_noop():
+def test_slide_zero_delta_is_noop(path):
     spec = W.scaled(W.qwen_slide(), L=1, lens=(100,))
     spec = W.GqaSpec(**{**spec.__dict__, "deltas": (0,)})
     wl = W.make(spec, DEV)
@@ -155,6 +155,26 @@ def test_slide_zero_delta_is_noop():
     Hn.run_gpu(wl)
     torch.cuda.synchronize()
     assert np.array_equal(Hn.u16(wl.pool_k), before)
+
+
+@pytest.mark.parametrize("H,d,rot_dim,rot_offset,pairing", [
+    (3, 128, 128, 0, K.ROTATE_HALF),     # 24 units per row: the CUDA-core path
+    (8, 64, 32, 16, K.ROTATE_HALF),      # rotary sub-range inside each head
+    (2, 256, 256, 0, K.ROTATE_HALF),
+    (32, 128, 128, 0, K.ROTATE_HALF),    # 256 units per row: one row per pass
+    (64, 64, 64, 0, K.INTERLEAVED),      # 512 units per row: the CUDA-core path
+    (4, 128, 64, 64, K.INTERLEAVED)])
+def test_slide_shapes(H, d, rot_dim, rot_offset, pairing, path):
+    """In-place rotation over head counts, head dims, rotary sub-ranges and
+    pairings, with ragged chunk tails and page boundaries."""
+    spec = W.GqaSpec("slide_shape", "slide", L=2, H=H, d=d, base=1e4, lens=(300, 129, 1), deltas=(-32768, 5, 999),
+                     m=0, page=16, pairing=pairing, rot_dim=rot_dim, rot_offset=rot_offset, evicted=100, window=530)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    Hn.check_parity(wl, h, f"slide H{H} d{d} r{rot_dim}+{rot_offset}")
+    assert int(err.item()) == 0
 
 
 def test_empty_and_zero_length():
