@@ -251,21 +251,33 @@ def e2e_measure(K, wl, steps, warmup):
             "tokens_per_s": wl.tokens / t, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
 
 
-def traffic_record(kernel: str):
-    """ncu DRAM bytes per launch for `kernel`, if the committed profile summary
-    was taken on the current kernel source (matching source hash)."""
+def kernel_sources(B):
+    """Every file the CUDA library is built from (translation units, headers, the C ABI)."""
+    import glob
+    return sorted(glob.glob(os.path.join(B.CSRC, "*.cu")) + glob.glob(os.path.join(B.CSRC, "*.cuh")) +
+                  glob.glob(os.path.join(B.CSRC, "*.h")) + [os.path.join(B.INCLUDE, "kamera.h")])
+
+
+def source_digest() -> str:
     import hashlib
+    from position_invariant_kv_chunk_gb300 import build as B
+    h = hashlib.sha256()
+    for src in kernel_sources(B):
+        h.update(open(src, "rb").read())
+    return h.hexdigest()[:16]
+
+
+def traffic_record(kernel: str, workload: str):
+    """ncu DRAM bytes (read + write) per launch of `kernel` on `workload`, if the
+    committed record (profiles/dram_traffic.txt: kernel, workload, source hash,
+    bytes, ...) was taken on the current kernel sources (matching hash)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    from position_invariant_kv_chunk_gb300 import build as B
-    h = hashlib.sha256()
-    for src in B.sources():
-        h.update(open(src, "rb").read())
-    digest = h.hexdigest()[:16]
+    digest = source_digest()
     for ln in open(path):
         f = ln.split()
-        if len(f) >= 4 and f[0] == kernel and f[2] == digest:
+        if len(f) >= 4 and f[0] == kernel and f[1] == workload and f[2] == digest:
             return float(f[3])
     return None
 
@@ -392,7 +404,7 @@ def ours_arm(args):
             pg.destroy_process_group()
         return 0
 
-    kernel_name = "relocate_patch" if spec.kind == "gqa" else spec.kind
+    kernel_name = "slide_kernel" if spec.kind == "slide" else "relocate_patch_umma_kernel"
     e2e = e2e_measure(K, wl, max(2, min(args.steps, 10)), 1)
     e2e["value"] *= world
     line = {
@@ -408,7 +420,7 @@ def ours_arm(args):
         "e2e": e2e,
         "gpu_launches": args.steps,
         "roofline": {"bound": "hbm", "achieved": achieved, "peak": peak, "unit": "GB/s",
-                     "frac": achieved / peak, "traffic": traffic_record(kernel_name),
+                     "frac": achieved / peak, "traffic": traffic_record(kernel_name, args.config),
                      "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
                      else "fallback 6.8 TB/s", "launch_ms": launch_avg,
                      "bytes_per_launch": bytes_step},
