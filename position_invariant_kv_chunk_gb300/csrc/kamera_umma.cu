@@ -62,7 +62,7 @@ constexpr int kThreads = 32 * (kEpiWarp0 + kEpiWarps);
 // registers: the busiest sub-partition bounds the registers per thread at
 // launch.  Warpgroup 0 then lowers its budget and the epilogue warpgroups
 // take the freed registers (each sub-partition holds one warp of each group).
-constexpr int kRegCap = 16384 / (32 * ((kThreads / 32 + 3) / 4));
+constexpr int kRegCap = (16384 / (32 * ((kThreads / 32 + 3) / 4))) & ~7;   // allocated in units of 8
 constexpr int kRegsLow = 72;                     // producer / MMA warpgroup
 constexpr int kRegsEpi = 144;                    // epilogue warpgroups
 static_assert(128 * kRegsLow + 32 * kEpiWarps * kRegsEpi <= kThreads * kRegCap, "register split exceeds the launch");
@@ -807,12 +807,14 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             const bool valid = slot >= 0;
             const uint32_t tacc = tmem + lane_addr + acc * kWMax;
             const int mode = rot ? (r.rope.pairing == KAMERA_ROPE_ROTATE_HALF ? 1 : 2) : 0;
-            // The row splits into P = w/16 pair-pieces: 8 columns j*8.. and their
-            // partners w/2 further on (whole RoPE pairs for rotate-half).  This
-            // warp owns pair-pieces [j0, j1): spans at a0 and b0, R rounds.
+            // The row splits into P = w/16 pair-pieces and this warp owns [j0, j0+R):
+            // two spans of 8R columns at a0 and b0, R rounds.  Rotate-half needs each
+            // thread to hold RoPE partners, so a pair-piece is 8 columns j*8.. and the 8
+            // w/2 further on; otherwise the warp's pieces form one contiguous run of the
+            // row, which keeps its pool stores to whole 32-byte sectors.
             const int P = sg.w >> 4;
             const int j0 = hh * P / kEpiPerSub, R = (hh + 1) * P / kEpiPerSub - j0;
-            const int a0 = 8 * j0, b0 = (sg.w >> 1) + 8 * j0;
+            const int a0 = mode == 1 ? 8 * j0 : 16 * j0, b0 = mode == 1 ? (sg.w >> 1) + 8 * j0 : a0 + 8 * R;
             epilogue_dispatch(mode, m > 0, rows_s, tt, a0, b0, R, tacc, cs_s, valid);
             if (m > 0) {   // accumulator free for the next MMA
                 ptx::tc_fence_before();
@@ -839,7 +841,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                         const int item = (b4 + it) * 32 + lane;
                         row[it] = (int)(((uint32_t)item * inv) >> 16);
                         const int pi = item - row[it] * ppr;
-                        piece[it] = pi < R ? j0 + pi : P + j0 + (pi - R);
+                        piece[it] = pi < R ? (a0 >> 3) + pi : (b0 >> 3) + (pi - R);
                         sl[it] = __shfl_sync(0xffffffffu, slot, row[it]);
                     }
 #pragma unroll
