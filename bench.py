@@ -209,46 +209,77 @@ def sweep(K, dev, peak, skip):
     return out
 
 
+def _replica(wl):
+    """A second device copy of the workload's tensors (same shapes, fresh memory)."""
+    import dataclasses
+    cl = lambda t: None if t is None else t.clone()
+    chunks = [dataclasses.replace(c, slots=c.slots.clone(), patches=[p.clone() for p in c.patches])
+              for c in wl.chunks]
+    return dataclasses.replace(wl, chunks=chunks, store_k=cl(wl.store_k), store_v=cl(wl.store_v),
+                               pool_k=cl(wl.pool_k), pool_v=cl(wl.pool_v))
+
+
 def e2e_measure(K, wl, steps, warmup):
     """Same metric through the C ABI with host buffers: every step copies its
     inputs host->device from pinned memory, runs the operator and reads the
-    pool back device->host, all inside the timed region."""
-    dev_in = []
-    for c in wl.chunks:
-        dev_in += list(c.patches) + [c.slots]
-    dev_in += [t for t in (wl.store_k, wl.store_v) if t is not None]
-    host_in = [t.cpu().pin_memory() for t in dev_in]
-    chunks_dev = K.pack_chunks(wl.chunks, device=wl.pool_k.device)
-    chunks_host = chunks_dev.cpu().pin_memory()
-    outs = [t for t in (wl.pool_k, wl.pool_v) if t is not None]
-    host_out = [torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outs]
-    err = torch.zeros(1, dtype=torch.int32, device=wl.pool_k.device)
-    call = make_call(K, wl, chunks_dev, err)
-    h2d = sum(t.numel() * t.element_size() for t in host_in) + chunks_host.numel()
-    d2h = sum(t.numel() * t.element_size() for t in host_out)
+    pool back device->host, all inside the timed region.  Steps alternate
+    between two device buffer sets on two streams, so one step's read-back
+    overlaps the next step's upload (the link carries both directions at
+    once); workloads above 16 GB on the device run one set, serially."""
+    def inputs(w):
+        t = []
+        for c in w.chunks:
+            t += list(c.patches) + [c.slots]
+        t += [x for x in (w.store_k, w.store_v) if x is not None]
+        if w.kind == "slide":   # in place: the pool is the step's input too
+            t.append(w.pool_k)
+        return t
 
-    def step():
-        for d, h in zip(dev_in, host_in):
-            d.copy_(h, non_blocking=True)
-        chunks_dev.copy_(chunks_host, non_blocking=True)
-        call()
-        for h, d in zip(host_out, outs):
-            h.copy_(d, non_blocking=True)
+    def outputs(w):
+        return [x for x in (w.pool_k, w.pool_v) if x is not None]
 
-    for _ in range(warmup):
-        step()
+    dev_bytes = sum(t.numel() * t.element_size() for t in inputs(wl) + outputs(wl))
+    sets = [wl, _replica(wl)] if dev_bytes <= (16 << 30) else [wl]
+    host_in = [t.cpu().pin_memory() for t in inputs(wl)]
+    chunks_dev = [K.pack_chunks(w.chunks, device=wl.pool_k.device) for w in sets]
+    chunks_host = [c.cpu().pin_memory() for c in chunks_dev]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype, pin_memory=True) for t in outputs(w)] for w in sets]
+    errs = [torch.zeros(1, dtype=torch.int32, device=wl.pool_k.device) for _ in sets]
+    calls = [make_call(K, w, c, e) for w, c, e in zip(sets, chunks_dev, errs)]
+    streams = [torch.cuda.Stream() for _ in sets]
+    h2d = sum(t.numel() * t.element_size() for t in host_in) + chunks_host[0].numel()
+    d2h = sum(t.numel() * t.element_size() for t in host_out[0])
+
+    def step(i):
+        k = i % len(sets)
+        with torch.cuda.stream(streams[k]):
+            for d, h in zip(inputs(sets[k]), host_in):
+                d.copy_(h, non_blocking=True)
+            chunks_dev[k].copy_(chunks_host[k], non_blocking=True)
+            calls[k]()
+            for h, d in zip(host_out[k], outputs(sets[k])):
+                h.copy_(d, non_blocking=True)
+
+    main = torch.cuda.current_stream()
+    for i in range(warmup):
+        step(i)
     torch.cuda.synchronize()
-    s = torch.cuda.current_stream()
     a = torch.cuda.Event(enable_timing=True)
     b = torch.cuda.Event(enable_timing=True)
-    a.record(s)
-    for _ in range(steps):
-        step()
-    b.record(s)
+    a.record(main)
+    for st in streams:
+        st.wait_stream(main)
+    for i in range(steps):
+        step(i)
+    for st in streams:
+        main.wait_stream(st)
+    b.record(main)
     torch.cuda.synchronize()
     t = a.elapsed_time(b) / 1e3 / steps
+    del sets
     return {"value": W.algorithmic_bytes(wl.spec) / t / 1e9, "unit": "GB/s", "ms_per_step": t * 1e3,
-            "tokens_per_s": wl.tokens / t, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h)}
+            "tokens_per_s": wl.tokens / t, "h2d_bytes_per_step": int(h2d), "d2h_bytes_per_step": int(d2h),
+            "buffer_sets": len(streams)}
 
 
 def kernel_sources(B):
