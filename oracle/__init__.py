@@ -103,6 +103,12 @@ def _declare(lib: C.CDLL) -> C.CDLL:
         C.c_int, C.c_int, C.c_int, _u16p, C.c_int64, C.c_int64, C.c_int64,
         _f64p, C.c_int, C.c_int, C.c_int,
         C.c_int, _i32p, _i64p, S, _f64p]
+    lib.kamera_oracle_ingest.restype = C.c_int
+    lib.kamera_oracle_ingest.argtypes = [
+        C.c_int, C.c_int, C.c_int, _u16p, _u16p, C.c_int64, C.c_int64, C.c_int64,
+        _u16p, _u16p, C.c_int64, C.c_int64, C.c_int64,
+        _f64p, C.c_int, C.c_int, C.c_int,
+        C.c_int, _i64p, _i32p, _i64p, S, _f64p]
     lib.kamera_oracle_num_threads.restype = C.c_int
     lib.kamera_oracle_num_threads.argtypes = []
     return lib
@@ -307,6 +313,35 @@ class Oracle:
         rc = self.lib.kamera_oracle_slide(
             L, H, d, _ptr(pool_k, _u16p), S, S * H * d, H * d, _ptr(f, _f64p), rot_dim,
             rot_offset, pairing, n, _ptr(ln, _i32p), _ptr(de, _i64p), sp, _ptr(sc, _f64p))
+        if rc != 0:
+            raise ValueError("oracle: index out of range in the chunk list")
+        del keep
+        return sc if want_scale else None
+
+    def ingest(self, pool_k, pool_v, store_k, store_v, chunks: Sequence[Chunk], inv_freq, rot_dim: int,
+               rot_offset: int = 0, pairing: int = ROTATE_HALF, want_scale: bool = False):
+        """Canonical ingest: gather each chunk's rows from its slots, turn the keys by
+        R(delta) (delta = minus the chunk's start position in the live cache) and
+        write them to the store rows src_offset.. (``src_offset`` names the first
+        store row written; ``rank`` is ignored).  ``pool_*``: uint16 ``[L, S, H, d]``,
+        ``store_*``: uint16 ``[L, N, H, d]`` (``*_v`` may be None: MLA rows or keys only).
+        """
+        for t in (pool_k, store_k) + tuple(x for x in (pool_v, store_v) if x is not None):
+            if t.dtype != np.uint16 or not t.flags.c_contiguous:
+                raise TypeError("arrays must be C-contiguous uint16")
+        if (pool_v is None) != (store_v is None):
+            raise ValueError("pool_v and store_v go together")
+        L, S, H, d = pool_k.shape
+        N = store_k.shape[1]
+        f = np.ascontiguousarray(inv_freq, dtype=np.float64)
+        n, src, ln, de, rk, pp, sp, keep = self._chunk_arrays(
+            [Chunk(c.src_offset, c.length, c.delta, 0, c.slots) for c in chunks])
+        sc = np.zeros(store_k.shape) if want_scale else None
+        rc = self.lib.kamera_oracle_ingest(
+            L, H, d, _ptr(pool_k, _u16p), _ptr(pool_v, _u16p), S, S * H * d, H * d,
+            _ptr(store_k, _u16p), _ptr(store_v, _u16p), N, N * H * d, H * d,
+            _ptr(f, _f64p), rot_dim, rot_offset, pairing, n, _ptr(src, _i64p), _ptr(ln, _i32p),
+            _ptr(de, _i64p), sp, _ptr(sc, _f64p))
         if rc != 0:
             raise ValueError("oracle: index out of range in the chunk list")
         del keep

@@ -373,6 +373,54 @@ int kamera_oracle_slide(int L, int H, int d, uint16_t* pool_k, int64_t n_slots,
     return 0;
 }
 
+/* Canonical ingest, the inverse of relocation: a chunk that sits in the live
+ * paged cache at positions s..s+len-1 is read back from its slots and turned
+ * to the position-free canonical frame (its first token at position 0) by
+ * R(-s).  With delta_c = -s_c, for every chunk c, layer l, head h, token j:
+ *   store_k[l][row_c + j][h] = bf16( R(delta_c) pool_k[l][slot_j][h] )
+ *   store_v[l][row_c + j][h] = pool_v[l][slot_j][h]          (when pool_v)
+ * (Canonical KV: gist.science technical summary, section 2; R(delta) as in
+ * kamera_oracle_rotate, so delta = 0 copies the row bit for bit.)  MLA rows
+ * are H = 1 segments of d = kv_lora + rope elements with the rotary range at
+ * rot_offset = kv_lora: c_KV is copied, k_rope turned.  Returns -1 on an
+ * out-of-range slot or store row. */
+int kamera_oracle_ingest(int L, int H, int d,
+                         const uint16_t* pool_k, const uint16_t* pool_v, int64_t n_slots,
+                         int64_t pool_layer_stride, int64_t pool_row_stride,
+                         uint16_t* store_k, uint16_t* store_v, int64_t n_store_rows,
+                         int64_t store_layer_stride, int64_t store_row_stride,
+                         const double* inv_freq, int rot_dim, int rot_offset, int pairing,
+                         int n_chunks, const int64_t* dst_row, const int32_t* len, const int64_t* delta,
+                         const int64_t* const* slots, double* scale_k)
+{
+    for (int c = 0; c < n_chunks; ++c) {
+        if (len[c] < 0 || dst_row[c] < 0 || dst_row[c] + len[c] > n_store_rows)
+            return -1;
+        for (int32_t j = 0; j < len[c]; ++j)
+            if (slots[c][j] < 0 || slots[c][j] >= n_slots)
+                return -1;
+    }
+    for (int c = 0; c < n_chunks; ++c) {
+        const int32_t T = len[c];
+        const int64_t work = (int64_t)L * T;
+#pragma omp parallel for schedule(static)
+        for (int64_t w = 0; w < work; ++w) {
+            const int l = (int)(w / T);
+            const int32_t j = (int32_t)(w % T);
+            const int64_t po = l * pool_layer_stride + slots[c][j] * pool_row_stride;
+            const int64_t so = l * store_layer_stride + (dst_row[c] + j) * store_row_stride;
+            for (int h = 0; h < H; ++h) {
+                kamera_oracle_row(pool_k + po + (int64_t)h * d, d, 1, delta[c], inv_freq, rot_dim, rot_offset,
+                                  pairing, NULL, NULL, 0, store_k + so + (int64_t)h * d, NULL,
+                                  scale_k ? scale_k + so + (int64_t)h * d : NULL);
+                if (pool_v)
+                    memcpy(store_v + so + (int64_t)h * d, pool_v + po + (int64_t)h * d, sizeof(uint16_t) * (size_t)d);
+            }
+        }
+    }
+    return 0;
+}
+
 /* Threads the OpenMP runtime would use (1 when built without OpenMP). */
 #ifdef _OPENMP
 #include <omp.h>

@@ -495,6 +495,55 @@ def pin_slide_problem(orc: O.Oracle):
         assert np.array_equal(pool[:, rest], before[:, rest])
 
 
+def pin_ingest_problem(orc: O.Oracle):
+    """Ingest = gather by slot, turn the keys by R(delta) (complex formulation,
+    exact rounding), copy the values, write store rows src_offset..; other
+    store rows untouched; delta 0 is a bit-exact gather."""
+    rng = np.random.default_rng(18)
+    L, S, H, d, N = 2, 48, 2, 32, 40
+    for pairing, r, o in ((RH, 32, 0), (IL, 16, 16)):
+        pool_k, pool_v = rand_bf16(rng, (L, S, H, d)), rand_bf16(rng, (L, S, H, d))
+        store_k = np.full((L, N, H, d), 0x5A5A, np.uint16)
+        store_v = store_k.copy()
+        slots = rng.permutation(S)[:30].astype(np.int64)
+        chunks = [O.Chunk(3, 18, -5000, 0, slots[:18]), O.Chunk(25, 12, 0, 0, slots[18:])]
+        th = orc.inv_freq(1e4, r)
+        orc.ingest(pool_k, pool_v, store_k, store_v, chunks, th, r, o, pairing)
+        want = complex_rotate(to_f64(pool_k[:, slots[:18]]), -5000, th, r, o, pairing)
+        assert np.array_equal(store_k[:, 3:21], _round(want))
+        assert np.array_equal(store_k[:, 25:37], pool_k[:, slots[18:]])      # delta 0: exact gather
+        assert np.array_equal(store_v[:, 3:21], pool_v[:, slots[:18]])
+        assert np.array_equal(store_v[:, 25:37], pool_v[:, slots[18:]])
+        rest = np.r_[0:3, 21:25, 37:N]
+        assert np.all(store_k[:, rest] == 0x5A5A) and np.all(store_v[:, rest] == 0x5A5A)
+
+
+def pin_ingest_recovers_canonical_keys(orc: O.Oracle):
+    """A chunk prefilled at positions s..s+T-1 (model-style RoPE table, rounded
+    to bf16 in the cache) and ingested with delta = -s equals the same keys made
+    at positions 0..T-1, to within the cache's own bf16 rounding; relocating the
+    ingested chunk back by +s returns the cache rows within that rounding too."""
+    rng = np.random.default_rng(19)
+    for pairing in (RH, IL):
+        d, T, s0, S = 64, 24, 4242, 64
+        th = orc.inv_freq(1e4, d)
+        k_raw = rng.standard_normal((T, d))
+        pos = s0 + np.arange(T)
+        live = np.stack([table_rope(k_raw[j], pos[j], th, pairing) for j in range(T)])
+        canon = np.stack([table_rope(k_raw[j], j, th, pairing) for j in range(T)])
+        pool = np.zeros((1, S, 1, d), np.uint16)
+        slots = rng.permutation(S)[:T].astype(np.int64)
+        pool[0, slots, 0] = _round(live)
+        store = np.zeros((1, T, 1, d), np.uint16)
+        orc.ingest(pool, None, store, None, [O.Chunk(0, T, -s0, 0, slots)], th, d, 0, pairing)
+        got = to_f64(store[0, :, 0])
+        tol = 2.0 ** -7 * np.max(np.abs(canon), axis=1, keepdims=True)   # two bf16 roundings of the row
+        assert np.all(np.abs(got - canon) <= tol)
+        assert np.abs(got - canon).max() > 0                               # the rounding is really there
+        rows = orc.rotate(got, s0, th, d, 0, pairing)
+        assert np.all(np.abs(rows - to_f64(pool[0, slots, 0])) <= tol)
+
+
 def pin_rejects_bad_indices(orc: O.Oracle):
     rng = np.random.default_rng(17)
     sk, sv, pk, pv, chunks = _small_gqa(rng)

@@ -49,6 +49,9 @@ MUTANTS = {
                              "kamera_oracle_row(store + so + kv_lora, rope_dim, 0, delta[c],"),
     "mla_rope_factor_swapped": ("ur = p2[c] + ((int64_t)l * T + j) * m;",
                                 "ur = p0[c] + ((int64_t)l * T + j) * m;"),
+    "ingest_row_offset_dropped": ("const int64_t so = l * store_layer_stride + (dst_row[c] + j) * store_row_stride;",
+                                  "const int64_t so = l * store_layer_stride + (int64_t)j * store_row_stride;"),
+    "ingest_values_not_copied": ("if (pool_v)\n                    memcpy(", "if (0)\n                    memcpy("),
     "slide_offset_ignored": ("kamera_oracle_row(row, d, 1, delta[c], inv_freq, rot_dim, rot_offset, pairing,",
                              "kamera_oracle_row(row, d, 1, delta[c], inv_freq, rot_dim, 0, pairing,"),
 }
