@@ -141,7 +141,7 @@ def flush_l2(buf: torch.Tensor):
 # --------------------------------------------------------------- workload
 def make_call(K, wl, chunks_dev, err):
     """The operator call of one step, through the C ABI binding."""
-    rope = K.Rope(wl.base, wl.rot_dim, 0 if wl.kind == "mla" else wl.rot_offset, wl.pairing)
+    rope = K.Rope(wl.base, wl.rot_dim, 0 if wl.kind in ("mla", "mla_ingest") else wl.rot_offset, wl.pairing)
     n = len(wl.chunks)
     ml, mr = wl.max_len, max((c.rank for c in wl.chunks), default=0)
     if wl.kind == "gqa":
@@ -150,6 +150,12 @@ def make_call(K, wl, chunks_dev, err):
     if wl.kind == "mla":
         return lambda: K.kamera_mla_relocate_patch(wl.pool_k, wl.store_k, wl.kv_lora, rope, chunks_dev, n, ml,
                                                    mr, err)
+    if wl.kind == "ingest":
+        return lambda: K.kamera_ingest_canonical(wl.pool_k, wl.pool_v, wl.store_k, wl.store_v, rope, chunks_dev,
+                                                 n, ml, err)
+    if wl.kind == "mla_ingest":
+        return lambda: K.kamera_mla_ingest_canonical(wl.pool_k, wl.store_k, wl.kv_lora, rope, chunks_dev, n, ml,
+                                                     err)
     return lambda: K.kamera_slide_inplace(wl.pool_k, rope, chunks_dev, n, ml, err)
 
 
@@ -157,9 +163,11 @@ def config_block(spec, name):
     blk = {"workload": name, "layers": spec.L, "chunks": len(spec.lens), "tokens": W.tokens(spec),
            "rank": spec.m, "page_size": spec.page, "algorithmic_bytes": W.algorithmic_bytes(spec)}
     if isinstance(spec, W.MlaSpec):
-        blk.update({"attention": "MLA", "kv_lora": spec.kv_lora, "rope_dim": spec.rope})
+        blk.update({"attention": "MLA" if spec.kind == "mla" else "MLA canonical ingest (pool -> store)",
+                    "kv_lora": spec.kv_lora, "rope_dim": spec.rope})
     else:
-        blk.update({"attention": "GQA/MHA" if spec.kind == "gqa" else "slide (rotate-only, in place)",
+        blk.update({"attention": {"gqa": "GQA/MHA", "slide": "slide (rotate-only, in place)",
+                                  "ingest": "GQA/MHA canonical ingest (pool -> store)"}[spec.kind],
                     "kv_heads": spec.H, "head_dim": spec.d})
     return blk
 
@@ -226,16 +234,23 @@ def e2e_measure(K, wl, steps, warmup):
     between two device buffer sets on two streams, so one step's read-back
     overlaps the next step's upload (the link carries both directions at
     once); workloads above 16 GB on the device run one set, serially."""
+    ingest = wl.kind in ("ingest", "mla_ingest")
+
     def inputs(w):
         t = []
         for c in w.chunks:
             t += list(c.patches) + [c.slots]
+        if ingest:              # the live cache is the input, the canonical store the result
+            t += [x for x in (w.pool_k, w.pool_v) if x is not None]
+            return t
         t += [x for x in (w.store_k, w.store_v) if x is not None]
         if w.kind == "slide":   # in place: the pool is the step's input too
             t.append(w.pool_k)
         return t
 
     def outputs(w):
+        if ingest:
+            return [x for x in (w.store_k, w.store_v) if x is not None]
         return [x for x in (w.pool_k, w.pool_v) if x is not None]
 
     dev_bytes = sum(t.numel() * t.element_size() for t in inputs(wl) + outputs(wl))
@@ -435,7 +450,8 @@ def ours_arm(args):
             pg.destroy_process_group()
         return 0
 
-    kernel_name = "slide_kernel" if spec.kind == "slide" else "relocate_patch_umma_kernel"
+    kernel_name = {"slide": "slide_kernel", "ingest": "ingest_kernel", "mla_ingest": "ingest_kernel"}.get(
+        spec.kind, "relocate_patch_umma_kernel")
     e2e = e2e_measure(K, wl, max(2, min(args.steps, 10)), 1)
     e2e["value"] *= world
     line = {

@@ -77,7 +77,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
-#define KAMERA_ABI_VERSION 2
+#define KAMERA_ABI_VERSION 3
 
 /* Limits of this build. */
 #define KAMERA_MAX_RANK 128          /* largest patch rank m */
@@ -278,6 +278,55 @@ int kamera_mla_relocate_patch(const KameraMlaPool* pool, const KameraMlaStore* s
                               const KameraRope* rope, const KameraChunk* d_chunks,
                               const KameraChunk* h_chunks, int32_t n_chunks, int32_t max_len,
                               int32_t max_rank, int32_t* d_err, struct CUstream_st* stream);
+
+/* Canonical stores written by the ingest calls (layouts as KameraGqaStore and
+ * KameraMlaStore, writable). */
+typedef struct KameraGqaStoreOut {
+    void* k;
+    void* v;
+    int64_t num_rows;
+    int64_t layer_stride;
+    int64_t row_stride;
+} KameraGqaStoreOut;
+
+typedef struct KameraMlaStoreOut {
+    void* kv;
+    int64_t num_rows;
+    int64_t layer_stride;
+    int64_t row_stride;
+} KameraMlaStoreOut;
+
+/*
+ * Canonical ingest, the inverse of relocation (technical summary section 2,
+ * "Canonical KV": a chunk's KV as if it had no antecedent and started at
+ * position 0).  A chunk that sits in the live paged cache at positions
+ * s_c..s_c+len-1 is gathered from its slots and turned to that frame:
+ *   Kstore[l][row_c + j][h] = bf16( R(delta_c) K[l][slot_j][h] ),  delta_c = -s_c
+ *   Vstore[l][row_c + j][h] = V[l][slot_j][h]                       (bit copy)
+ * Descriptor fields: src_offset = row_c, the first store row written; len;
+ * delta; rank must be 0 and patch_ptrs NULL (else KAMERA_DEVERR_DESCRIPTOR);
+ * dst_slot_mapping = the pool slots READ (outside [0, num_slots):
+ * KAMERA_DEVERR_SLOT, that row skipped); row_c + len beyond the store:
+ * KAMERA_DEVERR_SOURCE.  Elements outside the rotary range are copied, and
+ * delta == 0 copies every row bit for bit.  Store rows of different chunks
+ * must not overlap, and pool and store must not overlap.
+ *   pool, store, rope   host structs (read during the call); store is written
+ *   d_chunks, n_chunks  device descriptors; max_len bounds len (larger: KAMERA_DEVERR_LEN)
+ *   d_err               device int32 or NULL
+ * Returns KAMERA_OK or a KAMERA_ERR_* code (nothing enqueued on error).
+ */
+int kamera_ingest_canonical(const KameraGqaPool* pool, const KameraGqaStoreOut* store,
+                            const KameraRope* rope, const KameraChunk* d_chunks, int32_t n_chunks,
+                            int32_t max_len, int32_t* d_err, struct CUstream_st* stream);
+
+/*
+ * MLA canonical ingest: row = c_KV | k_rope; c_KV is copied bit for bit and
+ * k_rope turned by R(delta_c) (rope->rot_offset/rot_dim relative to k_rope, as
+ * for kamera_mla_relocate_patch).  Arguments as for kamera_ingest_canonical.
+ */
+int kamera_mla_ingest_canonical(const KameraMlaPool* pool, const KameraMlaStoreOut* store,
+                                const KameraRope* rope, const KameraChunk* d_chunks, int32_t n_chunks,
+                                int32_t max_len, int32_t* d_err, struct CUstream_st* stream);
 
 /*
  * Host-side check of a HOST copy of a descriptor array (dst_slot_mapping

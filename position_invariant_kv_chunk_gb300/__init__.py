@@ -24,6 +24,7 @@ from . import build as _build
 __all__ = [
     "KameraError", "Rope", "ChunkSpec", "load_library", "pack_chunks",
     "kamera_relocate_patch", "kamera_slide_inplace", "kamera_mla_relocate_patch",
+    "kamera_ingest_canonical", "kamera_mla_ingest_canonical",
     "kamera_validate_chunks", "kamera_status_string", "kamera_abi_version",
     "ROTATE_HALF", "INTERLEAVED", "DEVERR",
 ]
@@ -116,6 +117,12 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C
     lib.kamera_mla_relocate_patch.restype = C.c_int
     lib.kamera_mla_relocate_patch.argtypes = [P(_MlaPool), P(_MlaStore), P(_Rope), C.c_void_p, C.c_void_p,
                                               C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
+    lib.kamera_ingest_canonical.restype = C.c_int
+    lib.kamera_ingest_canonical.argtypes = [P(_GqaPool), P(_GqaStore), P(_Rope), C.c_void_p, C.c_int32,
+                                            C.c_int32, C.c_void_p, C.c_void_p]
+    lib.kamera_mla_ingest_canonical.restype = C.c_int
+    lib.kamera_mla_ingest_canonical.argtypes = [P(_MlaPool), P(_MlaStore), P(_Rope), C.c_void_p, C.c_int32,
+                                                C.c_int32, C.c_void_p, C.c_void_p]
     lib.kamera_validate_chunks.restype = C.c_int
     lib.kamera_validate_chunks.argtypes = [P(_Chunk), C.c_int32, C.c_int64, C.c_int64, C.c_int32,
                                            C.c_int32, P(C.c_int32), P(C.c_int32)]
@@ -135,7 +142,7 @@ def kamera_status_string(status: int) -> str:
     return load_library().kamera_status_string(int(status)).decode()
 
 
-ABI_VERSION = 2   # the KAMERA_ABI_VERSION these bindings marshal for
+ABI_VERSION = 3   # the KAMERA_ABI_VERSION these bindings marshal for
 
 
 def kamera_abi_version() -> int:
@@ -313,6 +320,58 @@ def kamera_mla_relocate_patch(pool: torch.Tensor, store: torch.Tensor, kv_lora: 
                                                   int(max_rank), _addr(err), _stream_handle(stream))
     del keep
     _check(rc, "kamera_mla_relocate_patch")
+
+
+def kamera_ingest_canonical(pool_k: torch.Tensor, pool_v: torch.Tensor, store_k: torch.Tensor,
+                            store_v: torch.Tensor, rope: Rope, chunks: torch.Tensor, n_chunks: int,
+                            max_len: int, err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """Canonical ingest (the inverse of relocation): gather each chunk's rows from the
+    pool at its slots (``slots`` of the descriptor), turn the keys by R(delta)
+    (delta = minus the chunk's start position in the live cache), copy the values,
+    and write store rows ``src_offset``.. .  pool_*: bf16 ``[L, S, H, d]``;
+    store_*: bf16 ``[L, N, H, d]`` (written); rank 0 descriptors."""
+    for t, nm in ((pool_k, "pool_k"), (pool_v, "pool_v"), (store_k, "store_k"), (store_v, "store_v")):
+        _bf16(t, nm)
+        if t.dim() != 4 or t.stride(3) != 1 or t.stride(2) != t.shape[3]:
+            raise ValueError(f"{nm} must be [L, rows, H, d] with packed heads")
+    L, S, H, d = pool_k.shape
+    if pool_v.stride() != pool_k.stride() or pool_v.shape != pool_k.shape:
+        raise ValueError("pool_k and pool_v must share shape and strides")
+    if store_v.stride() != store_k.stride() or store_v.shape != store_k.shape:
+        raise ValueError("store_k and store_v must share shape and strides")
+    if store_k.shape[0] != L or store_k.shape[2] != H or store_k.shape[3] != d:
+        raise ValueError("store and pool disagree on L, H or d")
+    pool = _GqaPool(L, H, d, 0, _addr(pool_k), _addr(pool_v), S, pool_k.stride(0), pool_k.stride(1))
+    store = _GqaStore(_addr(store_k), _addr(store_v), store_k.shape[1], store_k.stride(0), store_k.stride(1))
+    r, keep = rope._c()
+    rc = load_library().kamera_ingest_canonical(C.byref(pool), C.byref(store), C.byref(r), _addr(chunks),
+                                                int(n_chunks), int(max_len), _addr(err), _stream_handle(stream))
+    del keep
+    _check(rc, "kamera_ingest_canonical")
+
+
+def kamera_mla_ingest_canonical(pool: torch.Tensor, store: torch.Tensor, kv_lora: int, rope: Rope,
+                                chunks: torch.Tensor, n_chunks: int, max_len: int,
+                                err: Optional[torch.Tensor] = None, stream=None) -> None:
+    """MLA canonical ingest: c_KV copied, k_rope turned by R(delta).  pool: bf16
+    ``[L, S, kv_lora + rope]``; store: bf16 ``[L, N, kv_lora + rope]`` (written);
+    rope offsets relative to k_rope."""
+    _bf16(pool, "pool")
+    _bf16(store, "store")
+    for t, nm in ((pool, "pool"), (store, "store")):
+        if t.dim() != 3 or t.stride(2) != 1:
+            raise ValueError(f"{nm} must be [L, rows, width] with packed rows")
+    L, S, Wd = pool.shape
+    if store.shape[0] != L or store.shape[2] != Wd:
+        raise ValueError("store and pool disagree on L or row width")
+    p = _MlaPool(L, int(kv_lora), Wd - int(kv_lora), 0, _addr(pool), S, pool.stride(0), pool.stride(1))
+    s = _MlaStore(_addr(store), store.shape[1], store.stride(0), store.stride(1))
+    r, keep = rope._c()
+    rc = load_library().kamera_mla_ingest_canonical(C.byref(p), C.byref(s), C.byref(r), _addr(chunks),
+                                                    int(n_chunks), int(max_len), _addr(err),
+                                                    _stream_handle(stream))
+    del keep
+    _check(rc, "kamera_mla_ingest_canonical")
 
 
 def _aligned_i64(a) -> np.ndarray:

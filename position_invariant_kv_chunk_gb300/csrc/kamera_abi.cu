@@ -297,6 +297,128 @@ int kamera_mla_relocate_patch(const KameraMlaPool* pool, const KameraMlaStore* s
     return launch(p, FAMILY_MLA, h_chunks, reinterpret_cast<cudaStream_t>(stream));
 }
 
+static int ingest_launch(const RowsParams& rp, bool values, const void* pk, const void* pv, void* sk, void* sv,
+                         int64_t src_ls, int64_t src_ss, int64_t num_rows, int64_t dst_ls, int64_t dst_rs,
+                         cudaStream_t stream)
+{
+    IngestParams ip;
+    std::memset(&ip, 0, sizeof(ip));
+    const int np = ingest_passes(rp, values, ip.pass);
+    if (np <= 0)
+        return KAMERA_ERR_UNSUPPORTED;
+    ip.n_pass = np;
+    ip.src[0] = static_cast<const __nv_bfloat16*>(pk);
+    ip.src[1] = static_cast<const __nv_bfloat16*>(pv);
+    ip.dst[0] = static_cast<__nv_bfloat16*>(sk);
+    ip.dst[1] = static_cast<__nv_bfloat16*>(sv);
+    ip.src_ls = src_ls;
+    ip.src_ss = src_ss;
+    ip.dst_ls = dst_ls;
+    ip.dst_rs = dst_rs;
+    ip.num_slots = rp.num_slots;
+    ip.num_rows = num_rows;
+    ip.L = rp.L;
+    ip.H = rp.H;
+    ip.d = rp.d;
+    ip.chunks = rp.chunks;
+    ip.n_chunks = rp.n_chunks;
+    ip.max_len = rp.max_len;
+    ip.err = rp.err;
+    ip.rope = rp.rope;
+    const int64_t tiles = (rp.max_len + 127) / 128;
+    if ((int64_t)rp.n_chunks * tiles > 0x7FFFFFFFll || rp.L > 65535)
+        return KAMERA_ERR_UNSUPPORTED;
+    return launch_ingest(ip, stream) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
+}
+
+int kamera_ingest_canonical(const KameraGqaPool* pool, const KameraGqaStoreOut* store, const KameraRope* rope,
+                            const KameraChunk* d_chunks, int32_t n_chunks, int32_t max_len, int32_t* d_err,
+                            struct CUstream_st* stream)
+{
+    if (!pool || !store || !rope)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (pool->num_layers < 1 || pool->num_kv_heads < 1 || pool->head_dim < 8 || pool->reserved != 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if ((pool->head_dim % 8) || pool->head_dim > KAMERA_MAX_ROW_ELEMS)
+        return KAMERA_ERR_UNSUPPORTED;
+    const int64_t L = pool->num_layers, W = (int64_t)pool->num_kv_heads * pool->head_dim;
+    int rc;
+    if ((rc = check_strided(pool->k, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W, true)))
+        return rc;
+    if ((rc = check_strided(pool->v, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W, true)))
+        return rc;
+    if ((rc = check_strided(store->k, L, store->layer_stride, store->num_rows, store->row_stride, W, false)))
+        return rc;
+    if ((rc = check_strided(store->v, L, store->layer_stride, store->num_rows, store->row_stride, W, false)))
+        return rc;
+    const auto pk = span(pool->k, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W);
+    const auto pv = span(pool->v, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W);
+    const auto sk = span(store->k, L, store->layer_stride, store->num_rows, store->row_stride, W);
+    const auto sv = span(store->v, L, store->layer_stride, store->num_rows, store->row_stride, W);
+    if (overlap(sk, sv) || overlap(pk, sk) || overlap(pk, sv) || overlap(pv, sk) || overlap(pv, sv))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    bool noop;
+    if ((rc = check_call(d_chunks, n_chunks, max_len, 0, &noop)) || noop)
+        return rc;
+    RowsParams p;
+    std::memset(&p, 0, sizeof(p));
+    if ((rc = fill_rope(rope, pool->head_dim, &p.rope)))
+        return rc;
+    p.num_slots = pool->num_slots;
+    p.L = pool->num_layers;
+    p.H = pool->num_kv_heads;
+    p.d = pool->head_dim;
+    p.chunks = d_chunks;
+    p.n_chunks = n_chunks;
+    p.max_len = max_len;
+    p.err = d_err;
+    return ingest_launch(p, true, pool->k, pool->v, store->k, store->v, pool->layer_stride, pool->slot_stride,
+                         store->num_rows, store->layer_stride, store->row_stride,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
+int kamera_mla_ingest_canonical(const KameraMlaPool* pool, const KameraMlaStoreOut* store, const KameraRope* rope,
+                                const KameraChunk* d_chunks, int32_t n_chunks, int32_t max_len, int32_t* d_err,
+                                struct CUstream_st* stream)
+{
+    if (!pool || !store || !rope)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (pool->num_layers < 1 || pool->kv_lora_rank < 0 || pool->rope_dim < 0 || pool->reserved != 0 ||
+        pool->kv_lora_rank + pool->rope_dim < 16)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if ((pool->kv_lora_rank % 16) || (pool->rope_dim % 16) ||
+        pool->kv_lora_rank + pool->rope_dim > KAMERA_MAX_ROW_ELEMS || pool->rope_dim > KAMERA_MAX_ROT_DIM)
+        return KAMERA_ERR_UNSUPPORTED;
+    const int64_t L = pool->num_layers, W = (int64_t)pool->kv_lora_rank + pool->rope_dim;
+    int rc;
+    if ((rc = check_strided(pool->kv, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W, true)))
+        return rc;
+    if ((rc = check_strided(store->kv, L, store->layer_stride, store->num_rows, store->row_stride, W, false)))
+        return rc;
+    if (overlap(span(pool->kv, L, pool->layer_stride, pool->num_slots, pool->slot_stride, W),
+                span(store->kv, L, store->layer_stride, store->num_rows, store->row_stride, W)))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    bool noop;
+    if ((rc = check_call(d_chunks, n_chunks, max_len, 0, &noop)) || noop)
+        return rc;
+    RowsParams p;
+    std::memset(&p, 0, sizeof(p));
+    if ((rc = fill_rope(rope, pool->rope_dim, &p.rope)))
+        return rc;
+    p.rope.rot_offset += pool->kv_lora_rank;   // relative to k_rope in the ABI, to the row here
+    p.num_slots = pool->num_slots;
+    p.L = pool->num_layers;
+    p.H = 1;
+    p.d = (int32_t)W;
+    p.chunks = d_chunks;
+    p.n_chunks = n_chunks;
+    p.max_len = max_len;
+    p.err = d_err;
+    return ingest_launch(p, false, pool->kv, nullptr, store->kv, nullptr, pool->layer_stride, pool->slot_stride,
+                         store->num_rows, store->layer_stride, store->row_stride,
+                         reinterpret_cast<cudaStream_t>(stream));
+}
+
 int kamera_validate_chunks(const KameraChunk* h_chunks, int32_t n_chunks, int64_t num_store_rows, int64_t num_slots,
                            int32_t max_len, int32_t max_rank, int32_t* bad_chunk, int32_t* bad_bits)
 {

@@ -51,6 +51,34 @@ struct RowsParams {
     RopeParams rope;
 };
 
+// Canonical ingest (kamera_ingest.cu): a pass is a set of 16-byte units of a
+// row, repeated per head (head h's unit i starts at element h*d + off + 8*i).
+enum IngestKind { INGEST_COPY = 0, INGEST_ROT_HALF = 1, INGEST_ROT_IL = 2 };
+
+struct IngestPass {
+    int32_t array;      // 0: K (or the MLA row), 1: V
+    int32_t kind;       // IngestKind
+    int32_t off;        // first element of head 0's unit 0
+    int32_t per_head;   // units per head
+    int32_t half;       // rotate-half: distance in elements to the partner vector
+    int32_t f_off;      // rotary units: first frequency of unit 0
+};
+
+struct IngestParams {
+    const __nv_bfloat16* src[2];   // pool arrays (K | V, or the MLA row), read at the slots
+    __nv_bfloat16* dst[2];         // store arrays, written at rows src_offset..
+    int64_t src_ls, src_ss;        // pool layer and slot strides (elements)
+    int64_t dst_ls, dst_rs;        // store layer and row strides
+    int64_t num_slots, num_rows;
+    int32_t L, H, d;               // layers; heads of a row and their stride (elements)
+    int32_t n_pass;
+    IngestPass pass[6];
+    const KameraChunk* chunks;
+    int32_t n_chunks, max_len;
+    int32_t* err;
+    RopeParams rope;
+};
+
 // ------------------------------------------------------------------ bf16 --
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -22,6 +22,13 @@ size_t simt_smem_bytes(const RowsParams& p, int family, int tile_tokens);
 bool slide_supported(const RowsParams& p);
 cudaError_t launch_slide(const RowsParams& p, cudaStream_t stream);
 
+// Canonical ingest: the passes of a row (returns their count, -1 if the rotary
+// layout does not split into 16-byte units) and the launch.
+struct IngestPass;
+struct IngestParams;
+int ingest_passes(const RowsParams& rp, bool values, IngestPass* out);
+cudaError_t launch_ingest(const IngestParams& p, cudaStream_t stream);
+
 // Tensor-core path (tcgen05 MMA for the rank-m patch; relocation with rank > 0).
 bool umma_supported(const RowsParams& p, int family);
 size_t umma_smem_bytes(const RowsParams& p);

@@ -81,7 +81,7 @@ def compare(gpu: np.ndarray, ref: np.ndarray, scale: np.ndarray, block_axes=None
 
 # ------------------------------------------------------------- execution
 def rope_of(wl: W.Workload) -> K.Rope:
-    if wl.kind == "mla":
+    if wl.kind in ("mla", "mla_ingest"):   # the ABI's MLA rotary range is relative to k_rope
         return K.Rope(wl.base, wl.rot_dim, 0, wl.pairing)
     return K.Rope(wl.base, wl.rot_dim, wl.rot_offset, wl.pairing)
 
@@ -109,6 +109,12 @@ def run_gpu(wl: W.Workload, chunks_dev=None, err=None, max_len=None, mrank=None,
     elif wl.kind == "mla":
         K.kamera_mla_relocate_patch(wl.pool_k, wl.store_k, wl.kv_lora, rope_of(wl), chunks_dev, n, ml, mr,
                                     err, stream, host_chunks=hc)
+    elif wl.kind == "ingest":
+        K.kamera_ingest_canonical(wl.pool_k, wl.pool_v, wl.store_k, wl.store_v, rope_of(wl), chunks_dev, n, ml,
+                                  err, stream)
+    elif wl.kind == "mla_ingest":
+        K.kamera_mla_ingest_canonical(wl.pool_k, wl.store_k, wl.kv_lora, rope_of(wl), chunks_dev, n, ml, err,
+                                      stream)
     else:
         K.kamera_slide_inplace(wl.pool_k, rope_of(wl), chunks_dev, n, ml, err, stream)
     return chunks_dev
@@ -157,6 +163,19 @@ def run_oracle(wl: W.Workload, h: HostCopy, orc: O.Oracle = None):
         th = orc.inv_freq(wl.base, wl.rot_dim)
         sk = orc.mla(h.store_k, pk, h.chunks, wl.kv_lora, th, wl.pairing, want_scale=True)
         return pk, None, sk, None
+    if wl.kind in ("ingest", "mla_ingest"):   # returns the store arrays instead of the pool's
+        th = orc.inv_freq(wl.base, wl.rot_dim)
+        st_k = h.store_k.copy()
+        st_v = h.store_v.copy() if h.store_v is not None else None
+        if wl.kind == "ingest":
+            sk = orc.ingest(h.pool_k, h.pool_v, st_k, st_v, h.chunks, th, wl.rot_dim, wl.rot_offset, wl.pairing,
+                            want_scale=True)
+        else:
+            L, S, Wd = h.pool_k.shape
+            sk = orc.ingest(h.pool_k.reshape(L, S, 1, Wd), None, st_k.reshape(L, -1, 1, Wd), None, h.chunks, th,
+                            wl.rot_dim, wl.rot_offset, wl.pairing, want_scale=True)
+            sk = sk.reshape(st_k.shape)
+        return st_k, st_v, sk, None
     th = orc.inv_freq(wl.base, wl.rot_dim)
     sk = orc.slide(pk, h.chunks, th, wl.rot_dim, wl.rot_offset, wl.pairing, want_scale=True)
     return pk, None, sk, None
@@ -168,8 +187,40 @@ def touched_slots(wl: W.Workload) -> np.ndarray:
     return np.concatenate([c.slots.detach().cpu().numpy() for c in wl.chunks]).astype(np.int64)
 
 
+def written_rows(wl: W.Workload) -> np.ndarray:
+    """Store rows an ingest call writes."""
+    return np.concatenate([np.arange(c.src_offset, c.src_offset + c.length) for c in wl.chunks]
+                          or [np.zeros(0, np.int64)]).astype(np.int64)
+
+
+def check_ingest_parity(wl: W.Workload, h: HostCopy, what: str):
+    torch.cuda.synchronize()
+    ok, ov, sk, _ = run_oracle(wl, h)
+    gk = u16(wl.store_k)
+    rows = np.zeros(gk.shape[1], dtype=bool)
+    rows[written_rows(wl)] = True
+    assert np.array_equal(gk[:, ~rows], h.store_k[:, ~rows]), f"{what}: unwritten store rows changed"
+    assert np.array_equal(u16(wl.pool_k), h.pool_k), f"{what}: the pool changed"
+    stats = []
+    if wl.kind == "mla_ingest":
+        kv = wl.kv_lora
+        g, r, s = gk[:, rows], ok[:, rows], sk[:, rows]
+        assert np.array_equal(g[..., :kv], r[..., :kv]), f"{what}: c_KV not a bit copy"
+        stats.append(compare(g[..., kv:], r[..., kv:], s[..., kv:], block_axes=(1, 2), what=what + " k_rope"))
+        return stats
+    stats.append(compare(gk[:, rows], ok[:, rows], sk[:, rows], block_axes=(1, 3), what=what + " K"))
+    gv = u16(wl.store_v)
+    assert np.array_equal(gv, ov), f"{what}: values not a bit copy (or unwritten rows changed)"
+    assert np.array_equal(u16(wl.pool_v), h.pool_v), f"{what}: the value pool changed"
+    if all(c.delta == 0 for c in wl.chunks):
+        assert np.array_equal(gk, ok), f"{what}: delta 0 is not a bit copy"
+    return stats
+
+
 def check_parity(wl: W.Workload, h: HostCopy, what: str):
-    """Full comparison of the GPU pool against the oracle (small workloads)."""
+    """Full comparison of the GPU pool (or, for ingest, the store) against the oracle."""
+    if wl.kind in ("ingest", "mla_ingest"):
+        return check_ingest_parity(wl, h, what)
     torch.cuda.synchronize()
     ok, ov, sk, sv = run_oracle(wl, h)
     gk = u16(wl.pool_k)

@@ -25,6 +25,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("kamera_relocate_patch", "kamera_slide_inplace", "kamera_mla_relocate_patch",
+              "kamera_ingest_canonical", "kamera_mla_ingest_canonical",
               "kamera_validate_chunks", "kamera_status_string", "kamera_abi_version"):
         assert n in names
 
@@ -44,7 +45,7 @@ def test_struct_layouts_match_header(tmp_path):
     structs = {
         "KameraChunk": K._Chunk, "KameraRope": K._Rope, "KameraGqaPool": K._GqaPool,
         "KameraGqaStore": K._GqaStore, "KameraSlidePool": K._SlidePool, "KameraMlaPool": K._MlaPool,
-        "KameraMlaStore": K._MlaStore,
+        "KameraMlaStore": K._MlaStore, "KameraGqaStoreOut": K._GqaStore, "KameraMlaStoreOut": K._MlaStore,
     }
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kamera.h"', 'int main(void){']
     for cname, py in structs.items():
@@ -129,6 +130,17 @@ def test_argument_errors_before_any_launch():
     assert e.value.status == 1
     # n_chunks == 0 is a successful no-op that never reaches CUDA
     K.kamera_relocate_patch(pk, pv, sk, sv, rope, ch, 0, 8, 0, stream=0)
+    # ingest: overlapping pool and store, a rank-bound call, a no-op
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_ingest_canonical(pk, pv, torch.as_strided(pk, sk.shape, sk.stride()), sv, rope, ch, 1, 8, stream=0)
+    assert e.value.status == 1
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_ingest_canonical(pk, pv, sk, sv, K.Rope(1e4, 24), ch, 1, 8, stream=0)
+    assert e.value.status == 3
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_ingest_canonical(pk, pv, sk, sv, rope, ch, 1, -1, stream=0)
+    assert e.value.status == 1
+    K.kamera_ingest_canonical(pk, pv, sk, sv, rope, ch, 0, 8, stream=0)
     mla = torch.zeros(1, 16, 24, dtype=torch.bfloat16)
     with pytest.raises(K.KameraError) as e:
         K.kamera_mla_relocate_patch(mla, torch.zeros(1, 8, 24, dtype=torch.bfloat16), 12,

@@ -34,6 +34,8 @@ def _cases():
         "qwen_slide_small": W.scaled(W.qwen_slide(), L=2, lens=(1296, 77, 128)),
         "mha_reorder_recall_small": W.scaled(W.mha_reorder_recall(), L=2, H=4, lens=(513, 256, 1000, 2048, 300)),
         "tiny_gqa_x64": W.tiny_gqa_x(64),
+        "qwen_ingest_small": W.scaled(W.qwen_ingest(), L=2, lens=(1296, 200, 65, 1)),
+        "dsv2_mla_ingest_small": W.scaled(W.dsv2_mla_ingest(), L=2, lens=(300, 129, 7)),
     }
 
 
@@ -317,3 +319,86 @@ def test_many_tiles_per_cta_boundaries(path):
     Hn.run_gpu(wl, err=err)
     Hn.check_parity(wl, h, "many tiles")
     assert int(err.item()) == 0
+
+
+# ------------------------------------------------------------ canonical ingest
+@pytest.mark.parametrize("H,d,rot_dim,rot_offset,pairing", [
+    (4, 128, 128, 0, K.ROTATE_HALF),
+    (3, 128, 128, 0, K.ROTATE_HALF),     # units per row do not divide the block: strided items
+    (8, 64, 32, 16, K.ROTATE_HALF),      # copied columns on both sides of the rotary range
+    (2, 256, 256, 0, K.ROTATE_HALF),
+    (4, 128, 24, 8, K.INTERLEAVED),      # interleaved range that is not a multiple of 16
+    (32, 128, 128, 0, K.INTERLEAVED),
+    (2, 64, 0, 0, K.ROTATE_HALF)])       # no rotary range: a pure gather
+def test_ingest_shapes(H, d, rot_dim, rot_offset, pairing):
+    spec = W.GqaSpec("ingest_shape", "ingest", L=2, H=H, d=d, base=1e4, lens=(300, 129, 1),
+                     deltas=(-32768, -5, 0), m=0, page=16, pairing=pairing, rot_dim=rot_dim, rot_offset=rot_offset)
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    Hn.check_parity(wl, h, f"ingest H{H} d{d} r{rot_dim}+{rot_offset}")
+    assert int(err.item()) == 0
+
+
+def test_ingest_zero_delta_is_a_bit_exact_gather():
+    spec = W.scaled(W.qwen_ingest(), L=2, lens=(257, 3))
+    spec = W.GqaSpec(**{**spec.__dict__, "deltas": (0, 0)})
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    Hn.run_gpu(wl)
+    torch.cuda.synchronize()
+    for c in wl.chunks:
+        sl = c.slots.cpu().numpy()
+        rows = np.arange(c.src_offset, c.src_offset + c.length)
+        assert np.array_equal(Hn.u16(wl.store_k)[:, rows], h.pool_k[:, sl])
+        assert np.array_equal(Hn.u16(wl.store_v)[:, rows], h.pool_v[:, sl])
+
+
+def test_ingest_then_relocate_round_trip():
+    """Ingest by -s, then relocate (rank 0) by +s into an empty pool at the same
+    slots: the live rows come back within two bf16 roundings."""
+    spec = W.scaled(W.qwen_ingest(), L=2, lens=(300, 77))
+    wl = W.make(spec, DEV)
+    Hn.run_gpu(wl)
+    pool_k2 = torch.zeros_like(wl.pool_k)
+    pool_v2 = torch.zeros_like(wl.pool_v)
+    back = [W.ChunkData(c.src_offset, c.length, -c.delta, 0, c.slots, []) for c in wl.chunks]
+    K.kamera_relocate_patch(pool_k2, pool_v2, wl.store_k, wl.store_v, Hn.rope_of(wl),
+                            K.pack_chunks(back, device=DEV), len(back), wl.max_len, 0)
+    torch.cuda.synchronize()
+    sl = Hn.touched_slots(wl)
+    a = wl.pool_k[:, sl].float()
+    b = pool_k2[:, sl].float()
+    assert torch.equal(pool_v2[:, sl], wl.pool_v[:, sl])
+    assert float((a - b).abs().max()) <= 2.0 ** -6 * float(a.abs().max())
+
+
+@pytest.mark.parametrize("bad", ["slot", "store_row", "rank"])
+def test_ingest_device_errors(bad):
+    spec = W.scaled(W.qwen_ingest(), L=1, lens=(100, 50))
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    c = wl.chunks[1]
+    if bad == "slot":
+        c.slots = c.slots.clone()
+        c.slots[7] = wl.pool_k.shape[1] + 3
+    elif bad == "store_row":
+        c.src_offset = wl.store_k.shape[1] - 10
+    else:
+        c.rank = 1
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    chunks = K.pack_chunks(wl.chunks, device=DEV) if bad != "rank" else None
+    if bad == "rank":   # a rank-1 descriptor with no factors: pack by hand through the ChunkSpec path
+        specs = [K.ChunkSpec(x.src_offset, x.length, x.delta, 0, x.slots) for x in wl.chunks]
+        chunks = K.pack_chunks(specs, device=DEV)
+        raw = chunks.cpu().numpy().copy()
+        raw[64 + 12:64 + 16] = np.frombuffer(np.int32(1).tobytes(), np.uint8)   # rank field of chunk 1
+        chunks = torch.from_numpy(raw).to(DEV)
+    Hn.run_gpu(wl, chunks_dev=chunks, err=err)
+    torch.cuda.synchronize()
+    bits = {"slot": 1, "store_row": 2, "rank": 4}[bad]   # KAMERA_DEVERR_SLOT, _SOURCE, _DESCRIPTOR
+    assert int(err.item()) & bits
+    # chunk 0 was ingested regardless
+    rows0 = np.arange(0, 100)
+    assert not np.array_equal(Hn.u16(wl.store_k)[:, rows0], h.store_k[:, rows0])

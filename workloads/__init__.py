@@ -43,9 +43,11 @@ INTERLEAVED = 1
 # ---------------------------------------------------------------- specs ----
 @dataclass(frozen=True)
 class GqaSpec:
-    """GQA/MHA relocate + patch (kind 'gqa') or rotate-only slide (kind 'slide')."""
+    """GQA/MHA relocate + patch (kind 'gqa'), rotate-only slide (kind 'slide') or
+    canonical ingest (kind 'ingest': the chunks sit in the pool at live positions,
+    delta = minus each chunk's start, and are written to the store)."""
     name: str
-    kind: str                      # "gqa" | "slide"
+    kind: str                      # "gqa" | "slide" | "ingest"
     L: int
     H: int
     d: int
@@ -77,7 +79,7 @@ class MlaSpec:
     pairing: int = INTERLEAVED
     pool_pages: Optional[int] = None
 
-    kind: str = "mla"
+    kind: str = "mla"             # "mla" | "mla_ingest"
 
 
 def _np_rng(*tags) -> np.random.Generator:
@@ -147,6 +149,26 @@ def mha_reorder_recall() -> GqaSpec:
                    lens=tuple(lens + rec), deltas=tuple(deltas), m=64, page=16)
 
 
+def qwen_ingest() -> GqaSpec:
+    """Canonical ingest of a Qwen2.5-VL-7B shaped recall batch's chunks from a live
+    cache: 28 L, 4 KV heads, d=128, base 1e6, 8 chunks of 1296 tokens whose first
+    tokens sit at positions s ~ U{0..32767} (delta = -s), P=16."""
+    r = _np_rng("qwen_ingest", "start")
+    deltas = tuple(-int(x) for x in r.integers(0, 32768, size=8))
+    return GqaSpec("qwen_ingest", "ingest", L=28, H=4, d=128, base=1e6, lens=(1296,) * 8,
+                   deltas=deltas, m=0, page=16)
+
+
+def dsv2_mla_ingest() -> MlaSpec:
+    """Canonical ingest on the DeepSeek-V2-Lite shaped MLA cache: 27 L, c_KV 512
+    (copied) + k_rope 64 (interleaved, base 1e4, turned), 16 chunks of 4096 tokens
+    starting at s ~ U{0..16383} (delta = -s), P=64."""
+    r = _np_rng("dsv2_mla_ingest", "start")
+    deltas = tuple(-int(x) for x in r.integers(0, 16384, size=16))
+    return MlaSpec("dsv2_mla_ingest", L=27, kv_lora=512, rope=64, base=1e4, lens=(4096,) * 16,
+                   deltas=deltas, m=0, page=64, kind="mla_ingest")
+
+
 def tiny_gqa_x(n: int = 4096) -> GqaSpec:
     """The tiny GQA chunk replicated n times in one call (n chunks of 128 tokens)."""
     r = _np_rng("tiny_gqa_x", n)
@@ -161,6 +183,8 @@ CONFIGS = {
     "dsv2_mla": dsv2_mla,
     "qwen_slide": qwen_slide,
     "mha_reorder_recall": mha_reorder_recall,
+    "qwen_ingest": qwen_ingest,
+    "dsv2_mla_ingest": dsv2_mla_ingest,
 }
 
 
@@ -273,9 +297,11 @@ def make(spec, device="cpu", with_patches: bool = True) -> Workload:
     on the same device type)."""
     device = torch.device(device)
     if isinstance(spec, MlaSpec):
-        return _make_mla(spec, device)
+        return _make_mla_ingest(spec, device) if spec.kind == "mla_ingest" else _make_mla(spec, device)
     if spec.kind == "slide":
         return _make_slide(spec, device)
+    if spec.kind == "ingest":
+        return _make_ingest(spec, device)
     return _make_gqa(spec, device, with_patches)
 
 
@@ -370,6 +396,42 @@ def _make_mla(spec: MlaSpec, device) -> Workload:
                     kv_lora=spec.kv_lora)
 
 
+def _make_ingest(spec: GqaSpec, device) -> Workload:
+    """Live paged cache (K, V ~ N(0,1) at the chunks' slots and elsewhere) -> canonical
+    store (canary-filled); chunk c's store rows follow chunk c-1's."""
+    L, H, d = spec.L, spec.H, spec.d
+    N = sum(spec.lens)
+    slots, pages = _page_slots(spec.name, spec.lens, spec.page, spec.pool_pages)
+    S = pages * spec.page
+    pool_k = _randn_bf16((L, S, H, d), 1.0, _gen(device, spec.name, "pool_k"), device)
+    pool_v = _randn_bf16((L, S, H, d), 1.0, _gen(device, spec.name, "pool_v"), device)
+    store_k = _canary((L, N, H, d), device)
+    store_v = _canary((L, N, H, d), device)
+    chunks = []
+    off = 0
+    for c, t in enumerate(spec.lens):
+        chunks.append(ChunkData(off, t, int(spec.deltas[c]), 0, torch.from_numpy(slots[c]).to(device), []))
+        off += t
+    return Workload(spec, "ingest", chunks, store_k, store_v, pool_k, pool_v, rot_dim=spec.rot_dim or d,
+                    rot_offset=spec.rot_offset, pairing=spec.pairing, base=spec.base)
+
+
+def _make_mla_ingest(spec: MlaSpec, device) -> Workload:
+    L, W = spec.L, spec.kv_lora + spec.rope
+    N = sum(spec.lens)
+    slots, pages = _page_slots(spec.name, spec.lens, spec.page, spec.pool_pages)
+    S = pages * spec.page
+    pool = _randn_bf16((L, S, W), 1.0, _gen(device, spec.name, "pool"), device)
+    store = _canary((L, N, W), device)
+    chunks = []
+    off = 0
+    for c, t in enumerate(spec.lens):
+        chunks.append(ChunkData(off, t, int(spec.deltas[c]), 0, torch.from_numpy(slots[c]).to(device), []))
+        off += t
+    return Workload(spec, "mla_ingest", chunks, store_k=store, pool_k=pool, rot_dim=spec.rope,
+                    rot_offset=spec.kv_lora, pairing=spec.pairing, base=spec.base, kv_lora=spec.kv_lora)
+
+
 # ------------------------------------------------------------- accounting --
 def algorithmic_bytes(spec) -> int:
     """Bytes the operator must move at minimum: canonical rows read, patch factors
@@ -386,6 +448,9 @@ def algorithmic_bytes(spec) -> int:
         return 2 * kv + patch + T * 8
     if spec.kind == "slide":
         kv = T * spec.L * spec.H * spec.d * B
+        return 2 * kv + T * 8
+    if spec.kind == "ingest":
+        kv = 2 * T * spec.L * spec.H * spec.d * B                  # K and V
         return 2 * kv + T * 8
     kv = 2 * T * spec.L * spec.H * spec.d * B                      # K and V
     patch = sum((t + spec.d) * spec.m for t in spec.lens) * spec.L * spec.H * 2 * B if spec.m else 0
