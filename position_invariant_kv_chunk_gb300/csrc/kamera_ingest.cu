@@ -14,8 +14,10 @@
 // memory, then streams the rows through a short list of passes built on the
 // host, each a set of 16-byte units repeated per head: a rotate-half pair
 // of vectors whose elements are RoPE partners, an interleaved vector (four
-// adjacent pairs), or a plain vector copy.  When a pass's units per row
-// divide the block, every thread owns one fixed unit (its cos/sin values in
+// adjacent pairs), or a plain vector copy.  Each pass is its own launch of
+// the kernel specialised for its kind, so every launch stays lean enough to
+// keep four rows per thread in flight.  When a pass's units per row divide
+// the block, every thread owns one fixed unit (its cos/sin values in
 // registers) and walks the rows four at a time; otherwise the threads stride
 // over (row, unit) items.
 #include <cstdint>
@@ -30,7 +32,7 @@ namespace {
 
 constexpr int kIngestThreads = 256;
 constexpr int kIngestTile = 128;   // tokens per CTA
-constexpr int kIngestUnroll = 2;   // rows per thread in flight (fixed mapping)
+constexpr int kIngestUnroll = 4;   // rows per thread in flight (fixed mapping)
 
 // A unit's vectors of one row: loaded, then turned (or not) and stored.
 template <int KIND>
@@ -43,10 +45,12 @@ __device__ __forceinline__ void unit_load(const __nv_bfloat16* src, int e, int h
 
 template <int KIND>
 __device__ __forceinline__ void unit_store(__nv_bfloat16* dst, int e, int half, const uint4& va, const uint4& vb,
-                                           const float (&c)[8], const float (&s)[8])
+                                           const float (&c)[8], const float (&s)[8], bool turn)
 {
-    if constexpr (KIND == INGEST_COPY) {
+    if (KIND == INGEST_COPY || !turn) {   // delta 0: the unit's vectors are copied bit for bit
         *reinterpret_cast<uint4*>(dst + e) = va;
+        if constexpr (KIND == INGEST_ROT_HALF)
+            *reinterpret_cast<uint4*>(dst + e + half) = vb;
     } else if constexpr (KIND == INGEST_ROT_HALF) {
         float a[8], b[8], oa[8], ob[8];
         unpack8(va, a);
@@ -72,7 +76,7 @@ __device__ __forceinline__ void unit_store(__nv_bfloat16* dst, int e, int half, 
 
 template <int KIND>
 __device__ __forceinline__ void ingest_pass(const IngestParams& p, const IngestPass& ps, const float2* cs,
-                                            const int64_t* slots, int l, int64_t row0, int ntok)
+                                            const int64_t* slots, int l, int64_t row0, int ntok, bool turn)
 {
     const int nu = p.H * ps.per_head;
     const __nv_bfloat16* src = p.src[ps.array] + (int64_t)l * p.src_ls;
@@ -81,7 +85,7 @@ __device__ __forceinline__ void ingest_pass(const IngestParams& p, const IngestP
     auto unit_setup = [&](int u, int& e, float (&c)[8], float (&s)[8]) {
         const int h = u / ps.per_head, i = u - h * ps.per_head;
         e = h * p.d + ps.off + 8 * i;
-        if constexpr (KIND != INGEST_COPY) {
+        if (KIND != INGEST_COPY && turn) {
 #pragma unroll
             for (int k = 0; k < NF; ++k) {
                 const float2 t = cs[ps.f_off + NF * i + k];
@@ -109,7 +113,7 @@ __device__ __forceinline__ void ingest_pass(const IngestParams& p, const IngestP
 #pragma unroll
             for (int k = 0; k < kIngestUnroll; ++k)      // ... then the arithmetic and the stores
                 if (ok[k])
-                    unit_store<KIND>(dst + (int64_t)(jb + k * rpp) * p.dst_rs, e, ps.half, va[k], vb[k], c, s);
+                    unit_store<KIND>(dst + (int64_t)(jb + k * rpp) * p.dst_rs, e, ps.half, va[k], vb[k], c, s, turn);
         }
     } else {                          // (row, unit) items strided over the block
         for (int item = threadIdx.x; item < ntok * nu; item += kIngestThreads) {
@@ -120,12 +124,13 @@ __device__ __forceinline__ void ingest_pass(const IngestParams& p, const IngestP
             uint4 va, vb;
             unit_setup(u, e, c, s);
             unit_load<KIND>(src + slots[j] * p.src_ss, e, ps.half, va, vb);
-            unit_store<KIND>(dst + (int64_t)j * p.dst_rs, e, ps.half, va, vb, c, s);
+            unit_store<KIND>(dst + (int64_t)j * p.dst_rs, e, ps.half, va, vb, c, s, turn);
         }
     }
 }
 
-__global__ void __launch_bounds__(kIngestThreads, 2) ingest_kernel(const __grid_constant__ IngestParams p,
+template <int KIND>
+__global__ void __launch_bounds__(kIngestThreads, 2) ingest_kernel(const __grid_constant__ IngestParams p, int pass,
                                                                 int tiles_per_chunk, int layers_per_cta)
 {
     __shared__ float2 cs[KAMERA_MAX_ROT_DIM / 2];
@@ -141,7 +146,7 @@ __global__ void __launch_bounds__(kIngestThreads, 2) ingest_kernel(const __grid_
     if (ch.len > p.max_len)
         bad |= KAMERA_DEVERR_LEN;
     if (bad) {
-        if (tile == 0 && blockIdx.y == 0 && threadIdx.x == 0)
+        if (tile == 0 && blockIdx.y == 0 && threadIdx.x == 0 && pass == 0)
             raise_err(p.err, bad);
         return;
     }
@@ -150,7 +155,7 @@ __global__ void __launch_bounds__(kIngestThreads, 2) ingest_kernel(const __grid_
         return;
     const int ntok = min(kIngestTile, ch.len - t0);
     const bool turn = ch.delta != 0;
-    if (turn)
+    if (KIND != INGEST_COPY && turn)
         for (int f = threadIdx.x; f < p.rope.n_freq; f += kIngestThreads) {
             float c, s;
             phase_cos_sin(ch.delta, p.rope.inv_freq[f], c, s);
@@ -159,7 +164,7 @@ __global__ void __launch_bounds__(kIngestThreads, 2) ingest_kernel(const __grid_
     for (int j = threadIdx.x; j < ntok; j += kIngestThreads) {
         int64_t sl = ch.dst_slot_mapping[t0 + j];
         if (sl < 0 || sl >= p.num_slots) {
-            if (blockIdx.y == 0)
+            if (blockIdx.y == 0 && pass == 0)
                 raise_err(p.err, KAMERA_DEVERR_SLOT);
             sl = -1;
         }
@@ -169,22 +174,7 @@ __global__ void __launch_bounds__(kIngestThreads, 2) ingest_kernel(const __grid_
     const int64_t row0 = ch.src_offset + t0;
     const int l_end = min(p.L, (int)(blockIdx.y + 1) * layers_per_cta);
     for (int l = blockIdx.y * layers_per_cta; l < l_end; ++l) {
-        for (int q = 0; q < p.n_pass; ++q) {
-            const IngestPass ps = p.pass[q];
-            const int kind = turn ? ps.kind : INGEST_COPY;
-            if (kind == INGEST_ROT_HALF) {
-                ingest_pass<INGEST_ROT_HALF>(p, ps, cs, slots, l, row0, ntok);
-            } else if (kind == INGEST_ROT_IL) {
-                ingest_pass<INGEST_ROT_IL>(p, ps, cs, slots, l, row0, ntok);
-            } else if (ps.kind == INGEST_ROT_HALF) {   // delta 0: both vectors of each pair copied
-                IngestPass a = ps, b = ps;
-                b.off += ps.half;
-                ingest_pass<INGEST_COPY>(p, a, cs, slots, l, row0, ntok);
-                ingest_pass<INGEST_COPY>(p, b, cs, slots, l, row0, ntok);
-            } else {
-                ingest_pass<INGEST_COPY>(p, ps, cs, slots, l, row0, ntok);
-            }
-        }
+        ingest_pass<KIND>(p, p.pass[pass], cs, slots, l, row0, ntok, turn);
     }
 }
 
@@ -225,8 +215,17 @@ cudaError_t launch_ingest(const IngestParams& p, cudaStream_t stream)
     if (lg > p.L)
         lg = p.L;
     const dim3 grid((unsigned)tile_rows, (unsigned)((p.L + lg - 1) / lg));
-    ingest_kernel<<<grid, kIngestThreads, 0, stream>>>(p, tiles, lg);
-    return cudaGetLastError();
+    for (int q = 0; q < p.n_pass; ++q) {
+        switch (p.pass[q].kind) {
+        case INGEST_ROT_HALF: ingest_kernel<INGEST_ROT_HALF><<<grid, kIngestThreads, 0, stream>>>(p, q, tiles, lg); break;
+        case INGEST_ROT_IL: ingest_kernel<INGEST_ROT_IL><<<grid, kIngestThreads, 0, stream>>>(p, q, tiles, lg); break;
+        default: ingest_kernel<INGEST_COPY><<<grid, kIngestThreads, 0, stream>>>(p, q, tiles, lg); break;
+        }
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess)
+            return e;
+    }
+    return cudaSuccess;
 }
 
 }  // namespace kamera
