@@ -82,8 +82,15 @@ def compare(gpu: np.ndarray, ref: np.ndarray, scale: np.ndarray, block_axes=None
 # ------------------------------------------------------------- execution
 def rope_of(wl: W.Workload) -> K.Rope:
     if wl.kind in ("mla", "mla_ingest"):   # the ABI's MLA rotary range is relative to k_rope
-        return K.Rope(wl.base, wl.rot_dim, 0, wl.pairing)
-    return K.Rope(wl.base, wl.rot_dim, wl.rot_offset, wl.pairing)
+        return K.Rope(wl.base, wl.rot_dim, 0, wl.pairing, inv_freq=wl.inv_freq)
+    return K.Rope(wl.base, wl.rot_dim, wl.rot_offset, wl.pairing, inv_freq=wl.inv_freq)
+
+
+def theta_of(wl: W.Workload, orc: O.Oracle) -> np.ndarray:
+    """The frequency table both sides use: the workload's own, else base^(-2i/r)."""
+    if wl.inv_freq is not None:
+        return np.asarray(wl.inv_freq, dtype=np.float64)
+    return orc.inv_freq(wl.base, wl.rot_dim)
 
 
 def max_rank(wl: W.Workload) -> int:
@@ -155,16 +162,16 @@ def run_oracle(wl: W.Workload, h: HostCopy, orc: O.Oracle = None):
     pk = h.pool_k.copy()
     pv = h.pool_v.copy() if h.pool_v is not None else None
     if wl.kind == "gqa":
-        th = orc.inv_freq(wl.base, wl.rot_dim)
+        th = theta_of(wl, orc)
         sk, sv = orc.gqa(h.store_k, h.store_v, pk, pv, h.chunks, th, wl.rot_dim, wl.rot_offset, wl.pairing,
                          want_scale=True)
         return pk, pv, sk, sv
     if wl.kind == "mla":
-        th = orc.inv_freq(wl.base, wl.rot_dim)
+        th = theta_of(wl, orc)
         sk = orc.mla(h.store_k, pk, h.chunks, wl.kv_lora, th, wl.pairing, want_scale=True)
         return pk, None, sk, None
     if wl.kind in ("ingest", "mla_ingest"):   # returns the store arrays instead of the pool's
-        th = orc.inv_freq(wl.base, wl.rot_dim)
+        th = theta_of(wl, orc)
         st_k = h.store_k.copy()
         st_v = h.store_v.copy() if h.store_v is not None else None
         if wl.kind == "ingest":
@@ -176,7 +183,7 @@ def run_oracle(wl: W.Workload, h: HostCopy, orc: O.Oracle = None):
                             wl.rot_dim, wl.rot_offset, wl.pairing, want_scale=True)
             sk = sk.reshape(st_k.shape)
         return st_k, st_v, sk, None
-    th = orc.inv_freq(wl.base, wl.rot_dim)
+    th = theta_of(wl, orc)
     sk = orc.slide(pk, h.chunks, th, wl.rot_dim, wl.rot_offset, wl.pairing, want_scale=True)
     return pk, None, sk, None
 

@@ -26,6 +26,7 @@ import numpy as np
 import torch
 
 import oracle as O
+import workloads as W
 
 RH, IL = O.ROTATE_HALF, O.INTERLEAVED
 
@@ -261,6 +262,37 @@ def pin_rotation_relocates_keys(orc: O.Oracle):
 
 
 # ------------------------------------------------------------------- patch
+def pin_rotation_model_tables(orc: O.Oracle):
+    """R(delta) with a model's own frequency table.  A context-extension table:
+    keys made at position p with that table equal R(p) of the keys made at 0.
+    Multi-axis RoPE (per-frequency positions: time, height, width sections):
+    keys made at axis positions (t, h, w) and moved by (dt, dh, dw) equal
+    R(dt) with each section's frequencies scaled by its axis's share of dt --
+    the tables 'temporal' (dt, 0, 0) and 'axes' (dt, dt/2, dt/4) of the input
+    generator."""
+    rng = np.random.default_rng(21)
+    for pairing in (RH, IL):
+        for base, d in ((1e6, 128), (1e4, 64), (1e4, 16)):
+            th = base ** (-2.0 * np.arange(d // 2) / d)
+            k0 = rng.standard_normal((3, d))
+            ext = W.model_inv_freq("extended", base, d)
+            assert not np.allclose(ext, th) or d < 64
+            for p in (1, 37, 4096, 32767, -900):
+                assert np.max(np.abs(orc.rotate(k0, p, ext, d, 0, pairing) - table_rope(k0, p, ext, pairing))) < 1e-9
+            axis = np.empty(d // 2, dtype=np.int64)
+            for a, (lo, hi) in enumerate(W.mrope_sections(d // 2)):
+                axis[lo:hi] = a
+            start = np.array([40.0, 3.0, 11.0])   # a frame's (t, h, w) position
+            kt = table_rope(k0, start[axis], th, pairing)
+            for kind, move in (("temporal", lambda dt: (dt, 0, 0)), ("axes", lambda dt: (dt, dt // 2, dt // 4)),
+                               ("standard", lambda dt: (dt, dt, dt))):
+                tab = W.model_inv_freq(kind, base, d)
+                for dt in (4, 1000, -40, 32764):
+                    want = table_rope(k0, (start + np.array(move(dt), dtype=np.float64))[axis], th, pairing)
+                    got = orc.rotate(kt, dt, tab, d, 0, pairing)
+                    assert np.max(np.abs(got - want)) < 1e-8, (kind, dt, pairing, d)
+
+
 def pin_row_patch_is_matmul(orc: O.Oracle):
     """delta = 0 reduces the row operator to x + U V^T (numpy matmul, fp64)."""
     rng = np.random.default_rng(8)

@@ -62,6 +62,23 @@ def test_gqa_rope_layouts(pairing, rot_dim, rot_offset, path):
     Hn.check_parity(wl, h, f"rope {pairing}/{rot_dim}/{rot_offset}")
 
 
+@pytest.mark.parametrize("table", ["extended", "temporal", "axes"])
+@pytest.mark.parametrize("name", ["qwen_recall", "dsv2_mla", "qwen_slide", "qwen_ingest", "dsv2_mla_ingest"])
+def test_model_frequency_tables(name, table, path):
+    """A model's own frequency table passed through the RoPE override: a
+    context-extension rescale, and multi-axis RoPE moved along time only or by
+    per-axis shares of delta.  Every kind of call, against the oracle given
+    the same table."""
+    spec = W.scaled(W.CONFIGS[name](), L=2, lens=(300, 129, 7))
+    wl = W.make(spec, DEV)
+    wl.inv_freq = W.model_inv_freq(table, wl.base, wl.rot_dim)
+    h = Hn.snapshot(wl)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    Hn.check_parity(wl, h, f"{name} {table}")
+    assert int(err.item()) == 0
+
+
 @pytest.mark.parametrize("m", [1, 3, 8, 16, 17, 32, 48, 64, 96, 128])
 def test_gqa_ranks(m, path):
     spec = W.scaled(W.qwen_recall(), L=1, H=2, lens=(130, 5), m=m)

@@ -210,6 +210,53 @@ def scaled(spec, L: Optional[int] = None, lens: Optional[Sequence[int]] = None,
     return type(spec)(**kw)
 
 
+# ----------------------------------------------------- frequency tables --
+def mrope_sections(n_freq: int):
+    """Frequency index ranges of a three-axis (time, height, width) rotary
+    layout: a quarter of the frequencies follow time, the rest split evenly
+    between height and width (16/24/24 of the 64 frequencies of a 128-wide
+    head, the split of Qwen2.5-VL's multimodal RoPE)."""
+    t = n_freq // 4
+    hgt = (n_freq - t) // 2
+    return [(0, t), (t, t + hgt), (t + hgt, n_freq)]
+
+
+def model_inv_freq(kind: str, base: float, rot_dim: int) -> np.ndarray:
+    """A model's own rotary frequency table, passed to the operator as an input.
+
+    'standard'  base^(-2i/r)
+    'extended'  a context-extension rescale of the standard table by s = 8:
+                wavelengths longer than the 4096-token original context are
+                interpolated (theta/s), those shorter than 1/32 of it keep
+                theta, a linear ramp in between
+    'temporal'  multi-axis RoPE moved along time only: the height and width
+                sections' frequencies are 0, so R(delta) turns the time section
+                and leaves the spatial ones as they are
+    'axes'      multi-axis RoPE moved by (delta, delta/2, delta/4) along (time,
+                height, width): each section's frequencies scaled by its axis's
+                share of delta"""
+    n = rot_dim // 2
+    th = base ** (-2.0 * np.arange(n, dtype=np.float64) / rot_dim)
+    if kind == "standard":
+        return th
+    if kind == "extended":
+        s, ctx, lo, hi = 8.0, 4096.0, 1.0, 32.0
+        wavelengths = 2.0 * math.pi / th
+        ramp = np.clip((ctx / wavelengths - lo) / (hi - lo), 0.0, 1.0)   # 0: interpolate, 1: keep
+        return th * (ramp + (1.0 - ramp) / s)
+    sec = mrope_sections(n)
+    if kind == "temporal":
+        share = (1.0, 0.0, 0.0)
+    elif kind == "axes":
+        share = (1.0, 0.5, 0.25)
+    else:
+        raise ValueError(kind)
+    out = th.copy()
+    for (a, b), w in zip(sec, share):
+        out[a:b] *= w
+    return out
+
+
 # ------------------------------------------------------------- workloads --
 @dataclass
 class ChunkData:
@@ -235,6 +282,7 @@ class Workload:
     pairing: int = ROTATE_HALF
     base: float = 1e4
     kv_lora: int = 0
+    inv_freq: Optional[np.ndarray] = None      # a model's own rotary frequency table (default: base^(-2i/r))
 
     @property
     def tokens(self) -> int:
