@@ -77,7 +77,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
-#define KAMERA_ABI_VERSION 3
+#define KAMERA_ABI_VERSION 4
 
 /* Limits of this build. */
 #define KAMERA_MAX_RANK 128          /* largest patch rank m */
@@ -102,7 +102,9 @@ enum {
                                       misaligned factor or slot map: chunk skipped */
     KAMERA_DEVERR_LEN = 8,         /* len > max_len: chunk skipped */
     KAMERA_DEVERR_RANK = 16,       /* rank > max_rank: chunk skipped */
-    KAMERA_DEVERR_TIMEOUT = 32     /* an internal pipeline wait gave up: results incomplete */
+    KAMERA_DEVERR_TIMEOUT = 32,    /* an internal pipeline wait gave up: results incomplete */
+    KAMERA_DEVERR_NOCONV = 64      /* kamera_form_patch: an eigen-solve reached its sweep limit
+                                      (factors written from the last iterate) */
 };
 
 /* RoPE pairings. */
@@ -345,6 +347,48 @@ int kamera_validate_chunks(const KameraChunk* h_chunks, int32_t n_chunks, int64_
 
 /* Static description of a status code (never NULL). */
 const char* kamera_status_string(int status);
+
+/*
+ * One deficit tensor for kamera_form_patch: blocks (o, i), o < n_outer,
+ * i < n_inner, each a rows x cols bf16 matrix (row-major, row_stride apart)
+ * at x + o * outer_stride + i * inner_stride; with n_terms > 1 the block is
+ * the mean of n_terms such matrices, term_stride apart (the orbit patch).
+ * Strides in elements, multiples of 8; x 16-byte aligned.  A [L][len][H][d]
+ * deficit is n_outer = L, n_inner = H, outer_stride = len*H*d,
+ * inner_stride = d, row_stride = H*d.
+ */
+typedef struct KameraDeficit {
+    const void* x;
+    int64_t n_outer, n_inner;
+    int64_t outer_stride, inner_stride, row_stride, term_stride;
+    int32_t n_terms;
+    int32_t rows, cols;
+    int32_t reserved;   /* 0 */
+} KameraDeficit;
+
+/*
+ * Patch formation, the one-time step before reuse (technical summary
+ * section 2, "Rank-m Conditioning Patch": the patch is the top-m part of an
+ * SVD of Delta = KV(B|A) - KV(B|empty); section 3.1: the orbit patch is the
+ * same from the deficit averaged over orderings).  For every block X it
+ * writes the best rank-m approximation U V^T of X (Eckart-Young):
+ *     X = W diag(sigma) Z^T (sigma descending),  V = Z[:, :m],  U = X V = W[:, :m] diag(sigma[:m])
+ * i.e. the singular values sit in U and V has orthonormal columns.  Method:
+ * fp32 Gram matrix X^T X, cyclic Jacobi eigen-solve, U = X V; each column's
+ * sign is the one the solve reaches (singular vectors are unique up to sign,
+ * and within equal singular values only their span is).
+ *   u      bf16 [n_outer*n_inner][rows][m] (written; block index o*n_inner + i:
+ *          the Uk/Uv or Ur layout of KameraChunk for a [L][H] block grid)
+ *   v      bf16 [n_outer*n_inner][cols][m] (written; the Vk/Vv or Vr layout)
+ *   sigma  fp32 [n_outer*n_inner][m] singular values (written), or NULL
+ * Supported: 8 <= cols <= 128 with cols % 8 == 0 (head_dim up to 128, MLA
+ * k_rope), 1 <= m <= cols, rows >= 1, n_outer*n_inner < 2^31.  u, v and sigma
+ * must not overlap each other or the deficit.  Non-finite input gives
+ * non-finite factors.  No block (n_outer, n_inner or rows 0) is a successful
+ * no-op.  d_err (may be NULL): KAMERA_DEVERR_NOCONV.
+ */
+int kamera_form_patch(const KameraDeficit* deficit, int32_t m, void* u, void* v, float* sigma,
+                      int32_t* d_err, struct CUstream_st* stream);
 
 /* KAMERA_ABI_VERSION of the loaded library. */
 int kamera_abi_version(void);

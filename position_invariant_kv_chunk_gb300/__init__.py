@@ -24,7 +24,7 @@ from . import build as _build
 __all__ = [
     "KameraError", "Rope", "ChunkSpec", "load_library", "pack_chunks",
     "kamera_relocate_patch", "kamera_slide_inplace", "kamera_mla_relocate_patch",
-    "kamera_ingest_canonical", "kamera_mla_ingest_canonical",
+    "kamera_ingest_canonical", "kamera_mla_ingest_canonical", "kamera_form_patch",
     "kamera_validate_chunks", "kamera_status_string", "kamera_abi_version",
     "ROTATE_HALF", "INTERLEAVED", "DEVERR",
 ]
@@ -40,6 +40,7 @@ DEVERR = {
     8: "len > max_len",
     16: "rank > max_rank",
     32: "pipeline wait timed out",
+    64: "eigen-solve reached its sweep limit",
 }
 
 
@@ -85,6 +86,13 @@ class _MlaPool(C.Structure):
                 ("layer_stride", C.c_int64), ("slot_stride", C.c_int64)]
 
 
+class _Deficit(C.Structure):
+    _fields_ = [("x", C.c_void_p), ("n_outer", C.c_int64), ("n_inner", C.c_int64),
+                ("outer_stride", C.c_int64), ("inner_stride", C.c_int64), ("row_stride", C.c_int64),
+                ("term_stride", C.c_int64), ("n_terms", C.c_int32), ("rows", C.c_int32), ("cols", C.c_int32),
+                ("reserved", C.c_int32)]
+
+
 class _MlaStore(C.Structure):
     _fields_ = [("kv", C.c_void_p), ("num_rows", C.c_int64), ("layer_stride", C.c_int64),
                 ("row_stride", C.c_int64)]
@@ -123,6 +131,9 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C
     lib.kamera_mla_ingest_canonical.restype = C.c_int
     lib.kamera_mla_ingest_canonical.argtypes = [P(_MlaPool), P(_MlaStore), P(_Rope), C.c_void_p, C.c_int32,
                                                 C.c_int32, C.c_void_p, C.c_void_p]
+    lib.kamera_form_patch.restype = C.c_int
+    lib.kamera_form_patch.argtypes = [P(_Deficit), C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
+                                      C.c_void_p]
     lib.kamera_validate_chunks.restype = C.c_int
     lib.kamera_validate_chunks.argtypes = [P(_Chunk), C.c_int32, C.c_int64, C.c_int64, C.c_int32,
                                            C.c_int32, P(C.c_int32), P(C.c_int32)]
@@ -142,7 +153,7 @@ def kamera_status_string(status: int) -> str:
     return load_library().kamera_status_string(int(status)).decode()
 
 
-ABI_VERSION = 3   # the KAMERA_ABI_VERSION these bindings marshal for
+ABI_VERSION = 4   # the KAMERA_ABI_VERSION these bindings marshal for
 
 
 def kamera_abi_version() -> int:
@@ -406,3 +417,44 @@ def kamera_validate_chunks(chunks: Sequence, num_store_rows: int, num_slots: int
                                                int(max_rank), C.byref(bad), C.byref(bits))
     del keep
     return int(rc), int(bad.value), int(bits.value)
+
+
+def kamera_form_patch(delta: torch.Tensor, m: int, u: Optional[torch.Tensor] = None,
+                      v: Optional[torch.Tensor] = None, sigma: Optional[torch.Tensor] = None,
+                      err: Optional[torch.Tensor] = None, stream=None):
+    """Rank-m patch factors of deficit blocks: U V^T is the best rank-m
+    approximation of each block, V with orthonormal columns, the singular values
+    in U (and in ``sigma`` when given).
+
+    delta: bf16 ``[O, I, rows, cols]`` (any strides with packed columns, e.g. a
+    ``[L, len, H, d]`` deficit permuted to ``[L, H, len, d]``), or
+    ``[T, O, I, rows, cols]`` to factor the mean over T (the orbit patch).
+    u: bf16 ``[O, I, rows, m]``, v: bf16 ``[O, I, cols, m]`` (allocated when
+    None), sigma: optional fp32 ``[O, I, m]``.  Returns ``(u, v)``."""
+    _bf16(delta, "delta")
+    if delta.dim() == 4:
+        delta5, t_stride = delta.unsqueeze(0), 0
+    elif delta.dim() == 5:
+        delta5, t_stride = delta, delta.stride(0)
+    else:
+        raise ValueError("delta must be [O, I, rows, cols] or [T, O, I, rows, cols]")
+    T, O, I, rows, cols = delta5.shape
+    if delta5.stride(4) != 1:
+        raise ValueError("delta's columns must be packed")
+    if u is None:
+        u = torch.empty(O, I, rows, m, dtype=torch.bfloat16, device=delta.device)
+    if v is None:
+        v = torch.empty(O, I, cols, m, dtype=torch.bfloat16, device=delta.device)
+    for t, nm, shape in ((u, "u", (O, I, rows, m)), (v, "v", (O, I, cols, m))):
+        _bf16(t, nm)
+        if tuple(t.shape) != shape or not t.is_contiguous():
+            raise ValueError(f"{nm} must be a contiguous {shape} tensor")
+    if sigma is not None and (sigma.dtype != torch.float32 or tuple(sigma.shape) != (O, I, m)
+                              or not sigma.is_contiguous()):
+        raise ValueError(f"sigma must be a contiguous float32 {(O, I, m)} tensor")
+    df = _Deficit(_addr(delta5), O, I, delta5.stride(1), delta5.stride(2), delta5.stride(3),
+                  t_stride if T > 1 else 0, T, rows, cols, 0)
+    rc = load_library().kamera_form_patch(C.byref(df), int(m), _addr(u), _addr(v), _addr(sigma), _addr(err),
+                                          _stream_handle(stream))
+    _check(rc, "kamera_form_patch")
+    return u, v

@@ -474,4 +474,63 @@ int kamera_validate_chunks(const KameraChunk* h_chunks, int32_t n_chunks, int64_
     return KAMERA_OK;
 }
 
+
+int kamera_form_patch(const KameraDeficit* df, int32_t m, void* u, void* v, float* sigma, int32_t* d_err,
+                      struct CUstream_st* stream)
+{
+    if (!df || df->reserved != 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (df->n_outer < 0 || df->n_inner < 0 || df->n_terms < 1 || df->rows < 0 || df->cols < 1 || m < 1)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (df->n_outer == 0 || df->n_inner == 0 || df->rows == 0)
+        return KAMERA_OK;   // no block: nothing to form
+    if (!df->x || !u || !v)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (df->outer_stride < 0 || df->inner_stride < 0 || df->row_stride < df->cols || df->term_stride < 0 ||
+        (df->n_terms > 1 && df->term_stride == 0))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (!patch_form_supported(df->cols, m))
+        return KAMERA_ERR_UNSUPPORTED;
+    if (!aligned16(df->x) || !aligned16(u) || !aligned16(v) || (sigma && !aligned16(sigma)) ||
+        (df->outer_stride | df->inner_stride | df->row_stride | df->term_stride) % 8)
+        return KAMERA_ERR_MISALIGNED;
+    if (df->n_outer > 0 && df->n_inner > 0x7FFFFFFFll / df->n_outer)
+        return KAMERA_ERR_UNSUPPORTED;
+    const int64_t nb = df->n_outer * df->n_inner;
+    const int64_t last = (df->n_outer - 1) * df->outer_stride + (df->n_inner - 1) * df->inner_stride +
+                         (int64_t)(df->n_terms - 1) * df->term_stride + (int64_t)(df->rows - 1) * df->row_stride +
+                         df->cols;
+    const uintptr_t x0 = reinterpret_cast<uintptr_t>(df->x);
+    const std::pair<uintptr_t, uintptr_t> xs{x0, x0 + (uintptr_t)last * 2u};
+    const uintptr_t u0 = reinterpret_cast<uintptr_t>(u), v0 = reinterpret_cast<uintptr_t>(v);
+    const std::pair<uintptr_t, uintptr_t> us{u0, u0 + (uintptr_t)(nb * df->rows * m) * 2u};
+    const std::pair<uintptr_t, uintptr_t> vs{v0, v0 + (uintptr_t)(nb * df->cols * m) * 2u};
+    if (overlap(xs, us) || overlap(xs, vs) || overlap(us, vs))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (sigma) {
+        const uintptr_t s0 = reinterpret_cast<uintptr_t>(sigma);
+        const std::pair<uintptr_t, uintptr_t> ss{s0, s0 + (uintptr_t)(nb * m) * 4u};
+        if (overlap(ss, xs) || overlap(ss, us) || overlap(ss, vs))
+            return KAMERA_ERR_INVALID_ARGUMENT;
+    }
+    PatchFormParams p;
+    std::memset(&p, 0, sizeof(p));
+    p.x = static_cast<const __nv_bfloat16*>(df->x);
+    p.n_inner = df->n_inner;
+    p.outer_stride = df->outer_stride;
+    p.inner_stride = df->inner_stride;
+    p.row_stride = df->row_stride;
+    p.term_stride = df->term_stride;
+    p.n_terms = df->n_terms;
+    p.rows = df->rows;
+    p.cols = df->cols;
+    p.m = m;
+    p.u = static_cast<__nv_bfloat16*>(u);
+    p.v = static_cast<__nv_bfloat16*>(v);
+    p.sigma = sigma;
+    p.err = d_err;
+    return launch_patch_form(p, nb, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KAMERA_OK
+                                                                                          : KAMERA_ERR_CUDA;
+}
+
 }  // extern "C"

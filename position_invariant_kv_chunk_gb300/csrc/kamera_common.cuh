@@ -79,6 +79,18 @@ struct IngestParams {
     RopeParams rope;
 };
 
+// Patch formation: blocks (o, i) of a deficit, block index o * n_inner + i.
+struct PatchFormParams {
+    const __nv_bfloat16* x;        // deficit, block (o, i) at x + o * outer_stride + i * inner_stride
+    int64_t n_inner, outer_stride, inner_stride, row_stride, term_stride;   // elements
+    int32_t n_terms;               // deficits averaged per block (orbit patch), >= 1
+    int32_t rows, cols, m;
+    __nv_bfloat16* u;              // [blocks][rows][m]
+    __nv_bfloat16* v;              // [blocks][cols][m]
+    float* sigma;                  // [blocks][m] or null
+    int32_t* err;
+};
+
 // ------------------------------------------------------------------ bf16 --
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -25,7 +25,7 @@ def declared_functions():
 def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("kamera_relocate_patch", "kamera_slide_inplace", "kamera_mla_relocate_patch",
-              "kamera_ingest_canonical", "kamera_mla_ingest_canonical",
+              "kamera_ingest_canonical", "kamera_mla_ingest_canonical", "kamera_form_patch",
               "kamera_validate_chunks", "kamera_status_string", "kamera_abi_version"):
         assert n in names
 
@@ -46,6 +46,7 @@ def test_struct_layouts_match_header(tmp_path):
         "KameraChunk": K._Chunk, "KameraRope": K._Rope, "KameraGqaPool": K._GqaPool,
         "KameraGqaStore": K._GqaStore, "KameraSlidePool": K._SlidePool, "KameraMlaPool": K._MlaPool,
         "KameraMlaStore": K._MlaStore, "KameraGqaStoreOut": K._GqaStore, "KameraMlaStoreOut": K._MlaStore,
+        "KameraDeficit": K._Deficit,
     }
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kamera.h"', 'int main(void){']
     for cname, py in structs.items():
@@ -146,3 +147,28 @@ def test_argument_errors_before_any_launch():
         K.kamera_mla_relocate_patch(mla, torch.zeros(1, 8, 24, dtype=torch.bfloat16), 12,
                                     K.Rope(1e4, 12, 0, K.INTERLEAVED), ch, 1, 8, 0, stream=0)
     assert e.value.status == 3
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-only argument checks; run where no GPU exists")
+def test_form_patch_argument_errors():
+    """Malformed patch-formation calls return before touching CUDA."""
+    x = torch.zeros(2, 3, 16, 64, dtype=torch.bfloat16)
+    for m, status in ((0, 1), (65, 3)):
+        with pytest.raises(K.KameraError) as e:
+            K.kamera_form_patch(x, m, stream=0)
+        assert e.value.status == status
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_form_patch(torch.zeros(1, 1, 16, 256, dtype=torch.bfloat16), 8, stream=0)   # wider than 128
+    assert e.value.status == 3
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_form_patch(torch.zeros(1, 1, 16, 60, dtype=torch.bfloat16), 8, stream=0)    # not a multiple of 8
+    assert e.value.status == 3
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_form_patch(torch.zeros(1, 1, 16, 72, dtype=torch.bfloat16)[..., 4:68], 8, stream=0)   # 8-byte offset
+    assert e.value.status == 2
+    u = torch.zeros(2, 3, 16, 8, dtype=torch.bfloat16)
+    with pytest.raises(K.KameraError) as e:   # u aliases the deficit
+        K.kamera_form_patch(torch.as_strided(u, (2, 3, 16, 8), u.stride()), 8, u=u, stream=0)
+    assert e.value.status in (1, 3)
+    # an empty block grid is a successful no-op
+    K.kamera_form_patch(torch.zeros(0, 3, 16, 64, dtype=torch.bfloat16), 8, stream=0)

@@ -257,6 +257,58 @@ def model_inv_freq(kind: str, base: float, rot_dim: int) -> np.ndarray:
     return out
 
 
+# -------------------------------------------------------------- deficits --
+@dataclass(frozen=True)
+class DeficitSpec:
+    """Deficits Delta = KV(B|A) - KV(B|empty) of one chunk's keys and values for
+    patch formation, synthetic: each (kv, layer, head) block is a planted
+    low-rank matrix (``planted`` orthonormal directions on both sides with
+    singular values geometric from s_max to s_min: the deficit's energy sits in
+    about 32 feature directions) plus i.i.d. N(0, noise^2) entries; bf16
+    ``[kv, L, len, H, d]`` (kv = 2: keys and values), rank-m factors asked for."""
+    name: str
+    L: int
+    length: int
+    H: int
+    d: int
+    m: int = 32
+    kv: int = 2
+    planted: int = 32
+    s_max: float = 1.0
+    s_min: float = 0.05
+    noise: float = 1e-4
+    terms: int = 1          # > 1: that many deficits per block, factored as their mean (orbit patch)
+    kind: str = "patch_form"
+
+
+def qwen_patch_form() -> DeficitSpec:
+    """Rank-32 patch formation for one Qwen2.5-VL-7B shaped 1296-token frame chunk:
+    keys and values of 28 layers x 4 KV heads, d = 128 (224 blocks)."""
+    return DeficitSpec("qwen_patch_form", L=28, length=1296, H=4, d=128, m=32)
+
+
+def make_deficit(spec: DeficitSpec, device="cpu") -> torch.Tensor:
+    """Materialise a DeficitSpec (seeded): bf16 [terms, kv, L, len, H, d], or
+    [kv, L, len, H, d] when terms == 1."""
+    rng = _np_rng("deficit", spec.name, spec.L, spec.length, spec.H, spec.d, spec.terms)
+    T, n = spec.terms, spec.kv * spec.L * spec.H
+    k = min(spec.planted, spec.length, spec.d)
+    s = np.geomspace(spec.s_max, spec.s_min, k) if k > 1 else np.array([spec.s_max])
+    out = np.empty((T, spec.kv, spec.L, spec.H, spec.length, spec.d), dtype=np.float32)
+    flat = out.reshape(T, n, spec.length, spec.d)
+    for t in range(T):
+        for b in range(n):
+            a, _ = np.linalg.qr(rng.standard_normal((spec.length, k)))
+            z, _ = np.linalg.qr(rng.standard_normal((spec.d, k)))
+            flat[t, b] = (a * s) @ z.T + spec.noise * rng.standard_normal((spec.length, spec.d))
+    x = torch.from_numpy(out).to(torch.bfloat16).permute(0, 1, 2, 4, 3, 5).contiguous()
+    x = x.to(device)
+    return x[0] if T == 1 else x
+
+
+FORMATION = {"qwen_patch_form": qwen_patch_form}
+
+
 # ------------------------------------------------------------- workloads --
 @dataclass
 class ChunkData:
