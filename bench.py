@@ -214,7 +214,37 @@ def sweep(K, dev, peak, skip):
             torch.cuda.empty_cache()
         except Exception as e:  # report, keep the headline
             out[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
+    for name, f in W.FORMATION.items():
+        if name in skip:
+            continue
+        try:
+            out[name] = formation_entry(K, f(), dev, peak, flush)
+        except Exception as e:  # report, keep the headline
+            out[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
     return out
+
+
+def formation_entry(K, spec, dev, peak, flush):
+    """Patch formation of one chunk's deficits (all (kv, layer, head) blocks in
+    one call), timed per launch with L2 flushes."""
+    x = W.make_deficit(spec, dev)
+    xb = x.reshape(spec.kv * spec.L, spec.length, spec.H, spec.d).permute(0, 2, 1, 3)
+    u = torch.empty(spec.kv * spec.L, spec.H, spec.length, spec.m, dtype=torch.bfloat16, device=dev)
+    v = torch.empty(spec.kv * spec.L, spec.H, spec.d, spec.m, dtype=torch.bfloat16, device=dev)
+    sig = torch.empty(spec.kv * spec.L, spec.H, spec.m, dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        K.kamera_form_patch(xb, spec.m, u=u, v=v, sigma=sig, err=err)
+
+    for _ in range(3):
+        call()
+    t = float(np.median(time_launches(call, 10, flush))) * 1e-3
+    b, fl = W.deficit_bytes(spec), W.deficit_flops(spec)
+    return {"ms": t * 1e3, "blocks": W.deficit_blocks(spec), "blocks_per_s": W.deficit_blocks(spec) / t,
+            "tokens_per_s": spec.length / t, "gbs": b / t / 1e9, "frac_of_hbm_peak": b / t / 1e9 / peak,
+            "bytes": b, "contraction_tflops": fl / t / 1e12, "rank": spec.m,
+            "l2": "flushed between launches", "device_err": int(err.item())}
 
 
 def _replica(wl):
@@ -297,18 +327,27 @@ def e2e_measure(K, wl, steps, warmup):
             "buffer_sets": len(streams)}
 
 
-def kernel_sources(B):
-    """Every file the CUDA library is built from (translation units, headers, the C ABI)."""
+KERNEL_UNITS = {   # the translation unit each timed kernel is compiled from
+    "relocate_patch_umma_kernel": "kamera_umma.cu",
+    "slide_kernel": "kamera_slide.cu",
+    "ingest_kernel": "kamera_ingest.cu",
+    "patch_form_kernel": "kamera_patchform.cu",
+}
+
+
+def kernel_sources(B, kernel: str):
+    """The files a kernel is built from: its translation unit, the library's
+    internal headers and the C ABI header."""
     import glob
-    return sorted(glob.glob(os.path.join(B.CSRC, "*.cu")) + glob.glob(os.path.join(B.CSRC, "*.cuh")) +
+    return sorted([os.path.join(B.CSRC, KERNEL_UNITS[kernel])] + glob.glob(os.path.join(B.CSRC, "*.cuh")) +
                   glob.glob(os.path.join(B.CSRC, "*.h")) + [os.path.join(B.INCLUDE, "kamera.h")])
 
 
-def source_digest() -> str:
+def source_digest(kernel: str) -> str:
     import hashlib
     from position_invariant_kv_chunk_gb300 import build as B
     h = hashlib.sha256()
-    for src in kernel_sources(B):
+    for src in kernel_sources(B, kernel):
         h.update(open(src, "rb").read())
     return h.hexdigest()[:16]
 
@@ -316,11 +355,11 @@ def source_digest() -> str:
 def traffic_record(kernel: str, workload: str):
     """ncu DRAM bytes (read + write) per launch of `kernel` on `workload`, if the
     committed record (profiles/dram_traffic.txt: kernel, workload, source hash,
-    bytes, ...) was taken on the current kernel sources (matching hash)."""
+    bytes, ...) was taken on the kernel's current sources (matching hash)."""
     path = os.path.join(ROOT, "profiles", "dram_traffic.txt")
     if not os.path.exists(path):
         return None
-    digest = source_digest()
+    digest = source_digest(kernel)
     for ln in open(path):
         f = ln.split()
         if len(f) >= 4 and f[0] == kernel and f[1] == workload and f[2] == digest:

@@ -39,11 +39,7 @@ constexpr int kPfMaxSweeps = 30;
 struct PfShared {
     float* g;          // [n][n+1] Gram, then the eigenvector table for the U pass
     float* z;          // [n][n+1] eigenvectors; staging of X rows outside the solve
-    int* pp;           // [n/2] pair of the round
-    int* pq;
-    float* pc;         // cosines, sines, tangents of the round
-    float* ps;
-    float* pt;
+    float4* prm;       // [n/2] pair of the round: (p | q << 16 as bits, c, s, t); t = 0: no turn
     uint32_t* tri;     // (a, b) pair blocks with a <= b, packed a | b << 16
     int* order;        // [n] rank -> eigen index
 };
@@ -53,7 +49,7 @@ __host__ __device__ inline int pf_round16(int bytes) { return (bytes + 15) & ~15
 __host__ __device__ inline int pf_smem_bytes(int n)
 {
     const int n2 = n / 2;
-    return 2 * pf_round16(n * (n + 1) * 4) + pf_round16(n2 * 4) * 5 + pf_round16(n2 * (n2 + 1) / 2 * 4) +
+    return 2 * pf_round16(n * (n + 1) * 4) + pf_round16(n2 * 16) + pf_round16(n2 * (n2 + 1) / 2 * 4) +
            pf_round16(n * 4);
 }
 
@@ -135,6 +131,52 @@ __device__ void gram(const PatchFormParams& p, const __nv_bfloat16* x, const PfS
     __syncthreads();
 }
 
+// One 2x2 block of G for the pair blocks (a, b), a < b: G <- J_a^T G J_b on
+// rows {p_a, q_a} x columns {p_b, q_b}, written to both triangles.
+__device__ __forceinline__ void turn_block(float* g, int ld, const float4& A, const float4& B)
+{
+    const uint32_t ia = __float_as_uint(A.x), ib = __float_as_uint(B.x);
+    const int pa = (int)(ia & 0xFFFF), qa = (int)(ia >> 16), pb = (int)(ib & 0xFFFF), qb = (int)(ib >> 16);
+    const float ca = A.y, sa = A.z, cb = B.y, sb = B.z;
+    const float x00 = g[pa * ld + pb], x01 = g[pa * ld + qb];
+    const float x10 = g[qa * ld + pb], x11 = g[qa * ld + qb];
+    const float y00 = ca * x00 - sa * x10, y01 = ca * x01 - sa * x11;   // rows of pair a
+    const float y10 = sa * x00 + ca * x10, y11 = sa * x01 + ca * x11;
+    const float z00 = cb * y00 - sb * y01, z01 = sb * y00 + cb * y01;   // columns of pair b
+    const float z10 = cb * y10 - sb * y11, z11 = sb * y10 + cb * y11;
+    g[pa * ld + pb] = z00;
+    g[pa * ld + qb] = z01;
+    g[qa * ld + pb] = z10;
+    g[qa * ld + qb] = z11;
+    g[pb * ld + pa] = z00;
+    g[qb * ld + pa] = z01;
+    g[pb * ld + qa] = z10;
+    g[qb * ld + qa] = z11;
+}
+
+// Diagonal block of pair a: g_pp -= t g_pq, g_qq += t g_pq, g_pq = g_qp = 0.
+__device__ __forceinline__ void turn_diag(float* g, int ld, const float4& A)
+{
+    const uint32_t ia = __float_as_uint(A.x);
+    const int p = (int)(ia & 0xFFFF), q = (int)(ia >> 16);
+    const float t = A.w, apq = g[p * ld + q];
+    g[p * ld + p] -= t * apq;
+    g[q * ld + q] += t * apq;
+    g[p * ld + q] = 0.f;
+    g[q * ld + p] = 0.f;
+}
+
+// Z <- Z J on columns p, q of row zr.
+__device__ __forceinline__ void turn_z(float* zr, const float4& A)
+{
+    const uint32_t ia = __float_as_uint(A.x);
+    const int p = (int)(ia & 0xFFFF), q = (int)(ia >> 16);
+    const float c = A.y, sn = A.z;
+    const float zp = zr[p], zq = zr[q];
+    zr[p] = c * zp - sn * zq;
+    zr[q] = sn * zp + c * zq;
+}
+
 // Cyclic Jacobi on s.g (n x n, symmetric); eigenvectors accumulate in s.z.
 // Returns true when a sweep ended without a rotation.
 __device__ bool jacobi(int n, const PfShared& s, float tol_abs)
@@ -151,6 +193,9 @@ __device__ bool jacobi(int n, const PfShared& s, float tol_abs)
             s.tri[base + b - a] = (uint32_t)a | ((uint32_t)b << 16);
     }
     __syncthreads();
+    // eigenvector update: a fixed pair per thread when the pairs divide the block
+    const bool zfixed = kPfThreads % n2 == 0;
+    const int za = threadIdx.x % n2, zi0 = threadIdx.x / n2, zstep = kPfThreads / n2;
     for (int sweep = 0; sweep < kPfMaxSweeps; ++sweep) {
         int swept = 0;
         for (int r = 0; r < n - 1; ++r) {
@@ -171,64 +216,53 @@ __device__ bool jacobi(int n, const PfShared& s, float tol_abs)
                         c = rsqrtf(fmaf(t, t, 1.f));
                         sn = t * c;
                         rot = 1;
+                    } else {
+                        t = 0.f;
                     }
                 }
-                s.pp[k] = p;
-                s.pq[k] = q;
-                s.pc[k] = c;
-                s.ps[k] = sn;
-                s.pt[k] = rot ? t : 0.f;
+                s.prm[k] = make_float4(__uint_as_float((uint32_t)p | ((uint32_t)q << 16)), c, sn, t);
             }
             if (!__syncthreads_or(rot))
                 continue;   // nothing turns this round
             swept = 1;
-            // G <- J^T G J over the pair blocks (a <= b), mirrored
-            for (int e = threadIdx.x; e < ntri; e += kPfThreads) {
-                const uint32_t ab = s.tri[e];
+            // G <- J^T G J over the pair blocks (a <= b), two blocks in flight
+            for (int e = threadIdx.x; e < ntri; e += 2 * kPfThreads) {
+                const int e2 = e + kPfThreads;
+                const uint32_t ab = s.tri[e], ab2 = e2 < ntri ? s.tri[e2] : 0u;
                 const int a = (int)(ab & 0xFFFF), b = (int)(ab >> 16);
-                const float ta = s.pt[a], tb = s.pt[b];
-                const float ca = s.pc[a], sa = s.ps[a];
-                const int pa = s.pp[a], qa = s.pq[a];
+                const int a2 = (int)(ab2 & 0xFFFF), b2 = (int)(ab2 >> 16);
+                const float4 A = s.prm[a], B = s.prm[b];
+                const float4 A2 = s.prm[a2], B2 = s.prm[b2];
                 if (a == b) {
-                    if (ta != 0.f) {
-                        const float apq = s.g[pa * ld + qa];
-                        s.g[pa * ld + pa] -= ta * apq;
-                        s.g[qa * ld + qa] += ta * apq;
-                        s.g[pa * ld + qa] = 0.f;
-                        s.g[qa * ld + pa] = 0.f;
-                    }
-                    continue;
+                    if (A.w != 0.f)
+                        turn_diag(s.g, ld, A);
+                } else if (A.w != 0.f || B.w != 0.f) {
+                    turn_block(s.g, ld, A, B);
                 }
-                if (ta == 0.f && tb == 0.f)
-                    continue;
-                const float cb = s.pc[b], sb = s.ps[b];
-                const int pb = s.pp[b], qb = s.pq[b];
-                const float x00 = s.g[pa * ld + pb], x01 = s.g[pa * ld + qb];
-                const float x10 = s.g[qa * ld + pb], x11 = s.g[qa * ld + qb];
-                const float y00 = ca * x00 - sa * x10, y01 = ca * x01 - sa * x11;   // rows of pair a
-                const float y10 = sa * x00 + ca * x10, y11 = sa * x01 + ca * x11;
-                const float z00 = cb * y00 - sb * y01, z01 = sb * y00 + cb * y01;   // columns of pair b
-                const float z10 = cb * y10 - sb * y11, z11 = sb * y10 + cb * y11;
-                s.g[pa * ld + pb] = z00;
-                s.g[pa * ld + qb] = z01;
-                s.g[qa * ld + pb] = z10;
-                s.g[qa * ld + qb] = z11;
-                s.g[pb * ld + pa] = z00;
-                s.g[qb * ld + pa] = z01;
-                s.g[pb * ld + qa] = z10;
-                s.g[qb * ld + qa] = z11;
+                if (e2 < ntri) {
+                    if (a2 == b2) {
+                        if (A2.w != 0.f)
+                            turn_diag(s.g, ld, A2);
+                    } else if (A2.w != 0.f || B2.w != 0.f) {
+                        turn_block(s.g, ld, A2, B2);
+                    }
+                }
             }
             // Z <- Z J (columns p, q of every row)
-            for (int e = threadIdx.x; e < n * n2; e += kPfThreads) {
-                const int i = e / n2, a = e - i * n2;
-                if (s.pt[a] == 0.f)
-                    continue;
-                const float ca = s.pc[a], sa = s.ps[a];
-                float* zr = s.z + i * ld;
-                const int pa = s.pp[a], qa = s.pq[a];
-                const float zp = zr[pa], zq = zr[qa];
-                zr[pa] = ca * zp - sa * zq;
-                zr[qa] = sa * zp + ca * zq;
+            if (zfixed) {
+                const float4 A = s.prm[za];
+                if (A.w != 0.f) {
+#pragma unroll 4
+                    for (int i = zi0; i < n; i += zstep)
+                        turn_z(s.z + i * ld, A);
+                }
+            } else {
+                for (int e = threadIdx.x; e < n * n2; e += kPfThreads) {
+                    const int i = e / n2, a = e - i * n2;
+                    const float4 A = s.prm[a];
+                    if (A.w != 0.f)
+                        turn_z(s.z + i * ld, A);
+                }
             }
             __syncthreads();
         }
@@ -249,16 +283,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_kernel(const __grid_
         q += pf_round16(n * ld * 4);
         s.z = reinterpret_cast<float*>(q);
         q += pf_round16(n * ld * 4);
-        s.pp = reinterpret_cast<int*>(q);
-        q += pf_round16(n2 * 4);
-        s.pq = reinterpret_cast<int*>(q);
-        q += pf_round16(n2 * 4);
-        s.pc = reinterpret_cast<float*>(q);
-        q += pf_round16(n2 * 4);
-        s.ps = reinterpret_cast<float*>(q);
-        q += pf_round16(n2 * 4);
-        s.pt = reinterpret_cast<float*>(q);
-        q += pf_round16(n2 * 4);
+        s.prm = reinterpret_cast<float4*>(q);
+        q += pf_round16(n2 * 16);
         s.tri = reinterpret_cast<uint32_t*>(q);
         q += pf_round16(n2 * (n2 + 1) / 2 * 4);
         s.order = reinterpret_cast<int*>(q);

@@ -559,3 +559,20 @@ def algorithmic_bytes(spec) -> int:
 
 def tokens(spec) -> int:
     return sum(spec.lens)
+
+
+def deficit_blocks(spec: DeficitSpec) -> int:
+    return spec.kv * spec.L * spec.H
+
+
+def deficit_bytes(spec: DeficitSpec) -> int:
+    """Bytes patch formation must move at minimum: every deficit block read once
+    (each of its terms), U (len x m) and V (d x m) written in bf16, fp32 sigma."""
+    n = deficit_blocks(spec)
+    return n * (spec.terms * spec.length * spec.d * 2 + (spec.length + spec.d) * spec.m * 2 + spec.m * 4)
+
+
+def deficit_flops(spec: DeficitSpec) -> int:
+    """Multiply-adds x 2 of the two contractions every method needs: the Gram
+    matrix X^T X (len d^2) and U = X V (len d m), per block."""
+    return deficit_blocks(spec) * 2 * (spec.length * spec.d * spec.d + spec.length * spec.d * spec.m)
