@@ -102,9 +102,7 @@ enum {
                                       misaligned factor or slot map: chunk skipped */
     KAMERA_DEVERR_LEN = 8,         /* len > max_len: chunk skipped */
     KAMERA_DEVERR_RANK = 16,       /* rank > max_rank: chunk skipped */
-    KAMERA_DEVERR_TIMEOUT = 32,    /* an internal pipeline wait gave up: results incomplete */
-    KAMERA_DEVERR_NOCONV = 64      /* kamera_form_patch: an eigen-solve reached its sweep limit
-                                      (factors written from the last iterate) */
+    KAMERA_DEVERR_TIMEOUT = 32     /* an internal pipeline wait gave up: results incomplete */
 };
 
 /* RoPE pairings. */
@@ -373,10 +371,13 @@ typedef struct KameraDeficit {
  * same from the deficit averaged over orderings).  For every block X it
  * writes the best rank-m approximation U V^T of X (Eckart-Young):
  *     X = W diag(sigma) Z^T (sigma descending),  V = Z[:, :m],  U = X V = W[:, :m] diag(sigma[:m])
- * i.e. the singular values sit in U and V has orthonormal columns.  Method:
- * fp32 Gram matrix X^T X, cyclic Jacobi eigen-solve, U = X V; each column's
- * sign is the one the solve reaches (singular vectors are unique up to sign,
- * and within equal singular values only their span is).
+ * i.e. the singular values sit in U and V has orthonormal columns.  Method,
+ * in fp32: Gram matrix X^T X, Householder tridiagonalisation, bisection for
+ * the m largest eigenvalues, inverse iteration and Gram-Schmidt for their
+ * eigenvectors, U = X V.  Each column's sign is the one the solve reaches
+ * (singular vectors are unique up to sign, and within equal singular values
+ * only their span is); directions whose squared singular value lies below
+ * ~1e-6 of the largest are resolved as a span, not one by one.
  *   u      bf16 [n_outer*n_inner][rows][m] (written; block index o*n_inner + i:
  *          the Uk/Uv or Ur layout of KameraChunk for a [L][H] block grid)
  *   v      bf16 [n_outer*n_inner][cols][m] (written; the Vk/Vv or Vr layout)
@@ -385,7 +386,8 @@ typedef struct KameraDeficit {
  * k_rope), 1 <= m <= cols, rows >= 1, n_outer*n_inner < 2^31.  u, v and sigma
  * must not overlap each other or the deficit.  Non-finite input gives
  * non-finite factors.  No block (n_outer, n_inner or rows 0) is a successful
- * no-op.  d_err (may be NULL): KAMERA_DEVERR_NOCONV.
+ * no-op.  d_err: reserved for device-side errors (none is raised by this
+ * entry point); may be NULL.
  */
 int kamera_form_patch(const KameraDeficit* deficit, int32_t m, void* u, void* v, float* sigma,
                       int32_t* d_err, struct CUstream_st* stream);

@@ -40,7 +40,6 @@ DEVERR = {
     8: "len > max_len",
     16: "rank > max_rank",
     32: "pipeline wait timed out",
-    64: "eigen-solve reached its sweep limit",
 }
 
 

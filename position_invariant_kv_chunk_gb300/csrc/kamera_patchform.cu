@@ -6,51 +6,113 @@
 // same from the deficit averaged over orderings).  For every block
 // X (rows x cols: one (layer, head) of a chunk's keys or values, or the mean
 // of n_terms such blocks):
-//     G = X^T X                          Gram matrix, fp32
-//     G = Z diag(lambda) Z^T             cyclic Jacobi, eigenvalues sorted descending
-//     V = Z[:, :m],  U = X V             (= W Sigma: the singular values sit in U)
+//     G = X^T X / trace                 Gram matrix, fp32, scaled to trace 1
+//     G = Z diag(lambda) Z^T            top m eigenpairs, lambda descending
+//     V = Z[:, :m],  U = X V            (= W Sigma: the singular values sit in U)
 // so that U V^T is the best rank-m approximation of X (Eckart-Young) and the
 // factors have the layouts the relocation kernels read.
 //
-// One CTA owns one block.  G and Z live in shared memory (row stride cols+1,
-// so row- and column-wise accesses of a warp hit distinct banks).  Each Jacobi
-// round takes cols/2 disjoint index pairs of the round-robin (circle) ordering,
-// so every pair (p, q) is met once per sweep; all rotations of a round come
-// from the same G and are applied together: thread-per-2x2-block updates over
-// the upper triangle of pair blocks (mirrored to keep G exactly symmetric),
-// then the eigenvector columns.  A pair whose off-diagonal entry is already
-// below the threshold is skipped, a round with no rotation costs one barrier,
-// and the solve ends after a sweep without rotations (KAMERA_DEVERR_NOCONV
-// if the sweep limit is reached first).
+// One CTA owns one block; everything between the two passes over X stays in
+// shared memory.  The eigen-solve is the textbook route for a few eigenpairs
+// of a small dense symmetric matrix (Golub & Van Loan, sections 8.3-8.4; the
+// LAPACK tridiagonal-bisection-inverse-iteration path):
+//   1. Householder tridiagonalisation T = Q^T G Q, one reflector per column:
+//      p = beta G22 v and the rank-2 update G22 -= v w^T + w v^T spread over
+//      all warps; the reflectors stay in the zeroed part of G.
+//   2. The m largest eigenvalues of T by bisection on Sturm counts (the
+//      inertia of T - x I from its LDL^T pivots): S lanes per eigenvalue test
+//      S points at once, so each round narrows the interval S + 1 times.
+//   3. Their eigenvectors by inverse iteration: (T - lambda I) y = b solved by
+//      Gaussian elimination with partial pivoting (U keeps three diagonals),
+//      three solves from a fixed pseudo-random start, one lane per vector;
+//      then classical Gram-Schmidt applied twice over the m vectors, which
+//      also separates vectors of clustered (or repeated) eigenvalues.
+//   4. Back-transformation Z = Q Y, reflector by reflector over all columns.
+// Shared-memory traffic is O(n^3) words once instead of once per Jacobi sweep.
 #include <cstdint>
 #include <cuda_bf16.h>
 
 #include "kamera_common.cuh"
 #include "kamera_internal.h"
+#include "kamera_ptx.cuh"
 
 namespace kamera {
 
 namespace {
 
 constexpr int kPfThreads = 512;
+constexpr int kPfWarps = kPfThreads / 32;
 constexpr int kPfMaxCols = 128;
-constexpr int kPfMaxSweeps = 30;
+constexpr int kPfSolves = 3;   // inverse-iteration solves per eigenvector
 
 struct PfShared {
-    float* g;          // [n][n+1] Gram, then the eigenvector table for the U pass
-    float* z;          // [n][n+1] eigenvectors; staging of X rows outside the solve
-    float4* prm;       // [n/2] pair of the round: (p | q << 16 as bits, c, s, t); t = 0: no turn
-    uint32_t* tri;     // (a, b) pair blocks with a <= b, packed a | b << 16
-    int* order;        // [n] rank -> eigen index
+    float* g;      // [n][n+1]: Gram, then its tridiagonal reduction (reflectors below the subdiagonal)
+    float* z;      // [n][n+1]: staged rows of X; the elimination work arrays of the solves
+    float* y;      // [n][ys]: eigenvectors (row stride ys = m + 1, odd or 1 apart from a bank multiple)
+    float* d;      // [n] diagonal of T
+    float* e;      // [n] subdiagonal of T
+    float* e2;     // [n] its squares
+    float* beta;   // [n] reflector scales
+    float* vv;     // [n] reflector of the current column
+    float* pv;     // [n] beta G22 v; Gram-Schmidt coefficients
+    float* lam;    // [m] eigenvalues of the scaled Gram, descending
 };
 
 __host__ __device__ inline int pf_round16(int bytes) { return (bytes + 15) & ~15; }
 
-__host__ __device__ inline int pf_smem_bytes(int n)
+__host__ __device__ inline int pf_mpad(int m) { return (m + 3) & ~3; }
+
+// Row stride of the eigenvector table: m + 1, so that a warp walking down a
+// column (Gram-Schmidt, back-transformation) meets 32 different banks
+// whenever m is a multiple of 32 (and at most 2-way conflicts otherwise).
+__host__ __device__ inline int pf_ystride(int m) { return m + 1; }
+
+// Shared-memory layout (bytes from a 1024-aligned base): the eigenvector
+// table first, then G, the staging region, six n-vectors and the eigenvalues.
+// The tensor-core operand tiles start at the first 1024-byte boundary after
+// the eigenvector table and overlap G and what follows: they live only while
+// those are not in use (the Gram pass writes G after its last MMA; the U pass
+// runs after the solve).
+struct PfLayout {
+    int y, g, z, vec, lam, end, tc, tc_end;
+};
+
+__host__ __device__ inline int pf_round1024(int bytes) { return (bytes + 1023) & ~1023; }
+
+__host__ __device__ inline int pf_uatoms(int n) { return (n + 63) / 64; }   // 64-column K atoms of X
+
+__host__ __device__ inline int pf_nb(int m) { return (m + 15) & ~15; }     // MMA N of the U pass
+
+__host__ __device__ inline PfLayout pf_layout(int n, int m)
 {
-    const int n2 = n / 2;
-    return 2 * pf_round16(n * (n + 1) * 4) + pf_round16(n2 * 16) + pf_round16(n2 * (n2 + 1) / 2 * 4) +
-           pf_round16(n * 4);
+    PfLayout L;
+    const int ld = n + 1;
+    L.y = 0;
+    L.g = pf_round16(n * pf_ystride(m) * 4);
+    L.z = L.g + pf_round16(n * ld * 4);
+    L.vec = L.z + pf_round16(n * ld * 4);
+    L.lam = L.vec + 6 * pf_round16(n * 4);
+    L.end = L.lam + pf_round16(m * 4);
+    L.tc = pf_round1024(L.g);
+    const int ua = pf_uatoms(n);
+    const int gram_tile = 2 * 128 * 128;                                 // 128 x 128 tokens, bf16
+    const int u_tiles = ua * 128 * 128 + 2 * ua * pf_nb(m) * 128;        // X tile, V^T hi and lo
+    L.tc_end = L.tc + (gram_tile > u_tiles ? gram_tile : u_tiles);
+    return L;
+}
+
+__host__ __device__ inline int pf_smem_bytes(int n, int m)
+{
+    const PfLayout L = pf_layout(n, m);
+    return (L.end > L.tc_end ? L.end : L.tc_end) + 1024;   // + room to align the base
+}
+
+__device__ __forceinline__ float warp_sum(float v)
+{
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1)
+        v += __shfl_xor_sync(0xffffffffu, v, o);
+    return v;
 }
 
 // Stage rows [r0, r0 + nr) of the block's (mean) deficit as fp32, row-major with
@@ -131,256 +193,694 @@ __device__ void gram(const PatchFormParams& p, const __nv_bfloat16* x, const PfS
     __syncthreads();
 }
 
-// One 2x2 block of G for the pair blocks (a, b), a < b: G <- J_a^T G J_b on
-// rows {p_a, q_a} x columns {p_b, q_b}, written to both triangles.
-__device__ __forceinline__ void turn_block(float* g, int ld, const float4& A, const float4& B)
+// ------------------------------------------------------ tensor-core passes --
+constexpr uint64_t kPfTimeoutNs = 1000000000ull;   // bound on every MMA completion wait
+constexpr uint32_t kPfTmemCols = 128;
+constexpr uint32_t kPfAtom = 128 * 128;            // one 64-element K atom of a 128-row operand
+
+struct PfTc {
+    uint32_t tile;    // shared address of the operand tiles (1024-aligned)
+    uint32_t bar;     // MMA completion barrier
+    uint32_t tmem;    // accumulator columns
+    uint32_t phase;   // completions waited for so far
+};
+
+// Byte offset of the 16-byte piece (row r, K piece kc) of a K-major operand
+// with 128-byte swizzle and atoms of atom_bytes.
+__device__ __forceinline__ uint32_t pf_piece(int r, int kc, uint32_t atom_bytes)
 {
-    const uint32_t ia = __float_as_uint(A.x), ib = __float_as_uint(B.x);
-    const int pa = (int)(ia & 0xFFFF), qa = (int)(ia >> 16), pb = (int)(ib & 0xFFFF), qb = (int)(ib >> 16);
-    const float ca = A.y, sa = A.z, cb = B.y, sb = B.z;
-    const float x00 = g[pa * ld + pb], x01 = g[pa * ld + qb];
-    const float x10 = g[qa * ld + pb], x11 = g[qa * ld + qb];
-    const float y00 = ca * x00 - sa * x10, y01 = ca * x01 - sa * x11;   // rows of pair a
-    const float y10 = sa * x00 + ca * x10, y11 = sa * x01 + ca * x11;
-    const float z00 = cb * y00 - sb * y01, z01 = sb * y00 + cb * y01;   // columns of pair b
-    const float z10 = cb * y10 - sb * y11, z11 = sb * y10 + cb * y11;
-    g[pa * ld + pb] = z00;
-    g[pa * ld + qb] = z01;
-    g[qa * ld + pb] = z10;
-    g[qa * ld + qb] = z11;
-    g[pb * ld + pa] = z00;
-    g[qb * ld + pa] = z01;
-    g[pb * ld + qa] = z10;
-    g[qb * ld + qa] = z11;
+    return (uint32_t)(kc >> 3) * atom_bytes + (uint32_t)r * 128u + ((uint32_t)((kc & 7) ^ (r & 7)) << 4);
 }
 
-// Diagonal block of pair a: g_pp -= t g_pq, g_qq += t g_pq, g_pq = g_qp = 0.
-__device__ __forceinline__ void turn_diag(float* g, int ld, const float4& A)
+// Thread 0 waits for the next MMA completion (bounded); the result reaches
+// every thread through the barrier that follows.
+__device__ __forceinline__ bool pf_wait_mma(PfTc& t, int32_t* err, int* s_abort)
 {
-    const uint32_t ia = __float_as_uint(A.x);
-    const int p = (int)(ia & 0xFFFF), q = (int)(ia >> 16);
-    const float t = A.w, apq = g[p * ld + q];
-    g[p * ld + p] -= t * apq;
-    g[q * ld + q] += t * apq;
-    g[p * ld + q] = 0.f;
-    g[q * ld + p] = 0.f;
-}
-
-// Z <- Z J on columns p, q of row zr.
-__device__ __forceinline__ void turn_z(float* zr, const float4& A)
-{
-    const uint32_t ia = __float_as_uint(A.x);
-    const int p = (int)(ia & 0xFFFF), q = (int)(ia >> 16);
-    const float c = A.y, sn = A.z;
-    const float zp = zr[p], zq = zr[q];
-    zr[p] = c * zp - sn * zq;
-    zr[q] = sn * zp + c * zq;
-}
-
-// Cyclic Jacobi on s.g (n x n, symmetric); eigenvectors accumulate in s.z.
-// Returns true when a sweep ended without a rotation.
-__device__ bool jacobi(int n, const PfShared& s, float tol_abs)
-{
-    const int ld = n + 1, n2 = n / 2, ntri = n2 * (n2 + 1) / 2;
-    const float tol_rel = 2.4e-7f;   // ~2 ulp of fp32
-    for (int e = threadIdx.x; e < n * n; e += kPfThreads) {
-        const int i = e / n, j = e - i * n;
-        s.z[i * ld + j] = i == j ? 1.f : 0.f;
+    if (threadIdx.x == 0) {
+        const uint64_t t0 = ptx::globaltimer();
+        while (!ptx::mbar_try_wait(t.bar, t.phase & 1u)) {
+            if (ptx::globaltimer() - t0 > kPfTimeoutNs) {
+                *s_abort = 1;
+                raise_err(err, KAMERA_DEVERR_TIMEOUT);
+                break;
+            }
+        }
     }
-    for (int a = threadIdx.x; a < n2; a += kPfThreads) {
-        const int base = a * n2 - a * (a - 1) / 2;
-        for (int b = a; b < n2; ++b)
-            s.tri[base + b - a] = (uint32_t)a | ((uint32_t)b << 16);
+    ++t.phase;
+    __syncthreads();
+    ptx::tc_fence_after();
+    return *(volatile int*)s_abort == 0;
+}
+
+// Eight bf16 rows (one 16-byte vector each) -> eight columns: out[c] holds
+// element c of rows 0..7.
+__device__ __forceinline__ void transpose8(const uint4 (&in)[8], uint4 (&out)[8])
+{
+    uint32_t w[8][4];
+#pragma unroll
+    for (int r = 0; r < 8; ++r) {
+        w[r][0] = in[r].x;
+        w[r][1] = in[r].y;
+        w[r][2] = in[r].z;
+        w[r][3] = in[r].w;
+    }
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+        const uint32_t sel = (c & 1) ? 0x7632u : 0x5410u;
+        uint32_t o[4];
+#pragma unroll
+        for (int k = 0; k < 4; ++k)
+            o[k] = __byte_perm(w[2 * k][c >> 1], w[2 * k + 1][c >> 1], sel);
+        out[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+// G = X^T X on the tensor cores: per 128-token tile, X^T is written as a
+// K-major operand (rows = columns of X, zero rows past n) and multiplied by
+// itself; G leaves TMEM into s.g.  Returns false after a timeout.
+__device__ bool gram_tc(const PatchFormParams& p, const __nv_bfloat16* x, const PfShared& s, PfTc& t,
+                        int* s_abort)
+{
+    const int n = p.cols, ld = n + 1, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int e = threadIdx.x; e < 2 * (int)kPfAtom / 16; e += kPfThreads)
+        ptx::sts128(t.tile + 16u * e, 0u, 0u, 0u, 0u);
+    const int nb = n / 8, items = 16 * nb;   // 8 x 8 blocks of a tile: 16 token blocks x n/8 column blocks
+    const int tb = threadIdx.x / nb, cb = threadIdx.x - tb * nb;
+    const uint32_t idesc = ptx::idesc_bf16_f32(128, 128);
+    for (int t0 = 0; t0 < p.rows; t0 += 128) {
+        uint4 in[8];
+        if (threadIdx.x < items) {
+#pragma unroll
+            for (int r = 0; r < 8; ++r) {
+                const int tok = t0 + 8 * tb + r;
+                in[r] = tok < p.rows ? *reinterpret_cast<const uint4*>(x + (int64_t)tok * p.row_stride + 8 * cb)
+                                     : make_uint4(0u, 0u, 0u, 0u);
+            }
+        }
+        if (t0 > 0 && !pf_wait_mma(t, p.err, s_abort))   // the previous tile's MMAs have read the tile
+            return false;
+        if (threadIdx.x < items) {
+            uint4 out[8];
+            transpose8(in, out);
+#pragma unroll
+            for (int c = 0; c < 8; ++c)   // row 8 cb + c, tokens 8 tb .. 8 tb + 7
+                ptx::sts128(t.tile + pf_piece(8 * cb + c, tb, kPfAtom), out[c].x, out[c].y, out[c].z, out[c].w);
+        }
+        ptx::fence_proxy_async();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int q = 0; q < 8; ++q) {
+                const uint64_t d = ptx::desc_k_sw128(t.tile + (q >> 2) * kPfAtom + (q & 3) * 32);
+                ptx::umma_bf16(t.tmem, d, d, idesc, (t0 > 0 || q > 0) ? 1u : 0u);
+            }
+            ptx::umma_commit(t.bar);
+        }
+    }
+    if (!pf_wait_mma(t, p.err, s_abort))
+        return false;
+    {   // TMEM lanes are rows of G; warp w reads lanes 32 (w % 4).., columns 32 (w / 4)..
+        const int i = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
+        const uint32_t ta = t.tmem + ((uint32_t)(32 * (warp & 3)) << 16) + c0;
+        uint32_t a[8], b[8], c[8], d[8];
+        ptx::tmem_ld8x2_issue(ta, ta + 8, a, b);
+        ptx::tmem_ld8x2_issue(ta + 16, ta + 24, c, d);
+        ptx::tmem_wait8x2(a, b);
+        ptx::tmem_wait8x2(c, d);
+        if (i < n) {
+            float* row = s.g + i * ld + c0;
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                if (c0 + k < n) row[k] = __uint_as_float(a[k]);
+                if (c0 + 8 + k < n) row[8 + k] = __uint_as_float(b[k]);
+                if (c0 + 16 + k < n) row[16 + k] = __uint_as_float(c[k]);
+                if (c0 + 24 + k < n) row[24 + k] = __uint_as_float(d[k]);
+            }
+        }
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    return true;
+}
+
+// U = X V on the tensor cores: V^T split into bf16 hi + lo parts (B operands,
+// rows = ranks, zero past m), X tiles of 128 tokens as A; the two products
+// accumulate in TMEM and leave as bf16 rows of U.
+__device__ bool u_tc(const PatchFormParams& p, const __nv_bfloat16* x, const PfShared& s, int ys, PfTc& t,
+                     __nv_bfloat16* uo, int* s_abort)
+{
+    const int n = p.cols, m = p.m, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ua = pf_uatoms(n), N = pf_nb(m), kp = 2 * ((n + 15) / 16);   // K pieces the MMAs read
+    const uint32_t a_tile = t.tile, b_hi = a_tile + ua * kPfAtom, b_lo = b_hi + ua * N * 128;
+    const uint32_t b_atom = (uint32_t)N * 128u;
+    for (int e = threadIdx.x; e < N * kp; e += kPfThreads) {   // V^T pieces: rank r, d = 8 kc ..
+        const int r = e / kp, kc = e - r * kp;
+        float hi[8], lo[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+            const int c = 8 * kc + k;
+            const float v = (r < m && c < n) ? s.y[c * ys + r] : 0.f;
+            hi[k] = __bfloat162float(__float2bfloat16_rn(v));
+            lo[k] = v - hi[k];
+        }
+        const uint4 h = pack8(hi), l = pack8(lo);
+        ptx::sts128(b_hi + pf_piece(r, kc, b_atom), h.x, h.y, h.z, h.w);
+        ptx::sts128(b_lo + pf_piece(r, kc, b_atom), l.x, l.y, l.z, l.w);
+    }
+    const uint32_t idesc = ptx::idesc_bf16_f32(128, N);
+    const int ks = (n + 15) / 16;   // 16-element K slices
+    for (int t0 = 0; t0 < p.rows; t0 += 128) {
+        for (int e = threadIdx.x; e < 128 * kp; e += kPfThreads) {   // X rows t0.. as A, zero past n / rows
+            const int r = e / kp, kc = e - r * kp, tok = t0 + r;
+            uint4 v = make_uint4(0u, 0u, 0u, 0u);
+            if (tok < p.rows && 8 * kc < n)
+                v = *reinterpret_cast<const uint4*>(x + (int64_t)tok * p.row_stride + 8 * kc);
+            ptx::sts128(a_tile + pf_piece(r, kc, kPfAtom), v.x, v.y, v.z, v.w);
+        }
+        ptx::fence_proxy_async();
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            ptx::tc_fence_after();
+            for (int q = 0; q < ks; ++q) {
+                const uint32_t ko = (q >> 2), kb = (q & 3) * 32;
+                const uint64_t ad = ptx::desc_k_sw128(a_tile + ko * kPfAtom + kb);
+                ptx::umma_bf16(t.tmem, ad, ptx::desc_k_sw128(b_hi + ko * b_atom + kb), idesc, q > 0 ? 1u : 0u);
+                ptx::umma_bf16(t.tmem, ad, ptx::desc_k_sw128(b_lo + ko * b_atom + kb), idesc, 1u);
+            }
+            ptx::umma_commit(t.bar);
+        }
+        if (!pf_wait_mma(t, p.err, s_abort))
+            return false;
+        // TMEM lanes are tokens; warp w reads lanes 32 (w % 4).., 16-column groups g = w / 4, w / 4 + 4, ..
+        const int tok = t0 + 32 * (warp & 3) + lane;
+        for (int g = warp >> 2; g < N / 16; g += kPfWarps / 4) {
+            const uint32_t ta = t.tmem + ((uint32_t)(32 * (warp & 3)) << 16) + 16 * g;
+            uint32_t a[8], b[8];
+            ptx::tmem_ld8x2_issue(ta, ta + 8, a, b);
+            ptx::tmem_wait8x2(a, b);
+            if (tok < p.rows) {
+                __nv_bfloat16* dst = uo + (int64_t)tok * m + 16 * g;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    if (16 * g + k < m) dst[k] = __float2bfloat16_rn(__uint_as_float(a[k]));
+                    if (16 * g + 8 + k < m) dst[8 + k] = __float2bfloat16_rn(__uint_as_float(b[k]));
+                }
+            }
+        }
+        ptx::tc_fence_before();
+        __syncthreads();   // TMEM read and the A tile free before the next tile
+    }
+    return true;
+}
+
+// Householder tridiagonalisation of the scaled Gram in s.g (n >= 3 handled;
+// n is a multiple of 8 here).  Afterwards d, e hold T and column k of s.g,
+// rows k+1.., holds the reflector v_k (v_k[0] = 1) with scale beta_k.
+__device__ void tridiagonalise(int n, const PfShared& s)
+{
+    const int ld = n + 1, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int k = 0; k < n - 2; ++k) {
+        const int L = n - k - 1;
+        float* col = s.g + (k + 1) * ld + k;   // x_i = col[i * ld], i < L
+        if (warp == 0) {
+            float sig = 0.f;
+            for (int i = 1 + lane; i < L; i += 32) {
+                const float xi = col[i * ld];
+                sig = fmaf(xi, xi, sig);
+            }
+            sig = warp_sum(sig);
+            const float x0 = col[0];
+            float beta = 0.f, v0 = 1.f, mu = x0;
+            if (sig > 0.f) {   // H x = mu e_1 with H = I - beta v v^T, v_0 = 1
+                mu = sqrtf(fmaf(x0, x0, sig));
+                v0 = x0 <= 0.f ? x0 - mu : -__fdividef(sig, x0 + mu);
+                beta = __fdividef(2.f * v0 * v0, fmaf(v0, v0, sig));
+            }
+            const float inv = __fdividef(1.f, v0);
+            for (int i = lane; i < L; i += 32) {
+                const float vi = i == 0 ? 1.f : (sig > 0.f ? col[i * ld] * inv : 0.f);
+                s.vv[i] = vi;
+                col[i * ld] = vi;
+            }
+            if (lane == 0) {
+                s.d[k] = s.g[k * ld + k];
+                s.e[k] = mu;
+                s.beta[k] = beta;
+            }
+        }
+        __syncthreads();
+        const float beta = s.beta[k];
+        if (beta == 0.f)
+            continue;
+        // Four threads per row of G22, each over a quarter of its columns in an
+        // order rotated by 8 per quarter: the 32 lanes of a warp (8 rows x 4
+        // quarters) touch 32 different banks at every step.
+        float* a22 = s.g + (k + 1) * ld + (k + 1);
+        const int i = threadIdx.x >> 2, q = threadIdx.x & 3;
+        float* row = a22 + i * ld;
+        {   // p = beta G22 v
+            float acc = 0.f, acc2 = 0.f;
+            if (i < L) {
+#pragma unroll
+                for (int u = 0; u < 32; u += 2) {
+                    const int j = 32 * q + ((u + 8 * q) & 31), j2 = 32 * q + ((u + 1 + 8 * q) & 31);
+                    if (j < L)
+                        acc = fmaf(row[j], s.vv[j], acc);
+                    if (j2 < L)
+                        acc2 = fmaf(row[j2], s.vv[j2], acc2);
+                }
+            }
+            acc += acc2;
+            acc += __shfl_xor_sync(0xffffffffu, acc, 1);
+            acc += __shfl_xor_sync(0xffffffffu, acc, 2);
+            if (q == 0 && i < L)
+                s.pv[i] = beta * acc;
+        }
+        __syncthreads();
+        float kk = 0.f;   // w = p - (beta/2)(p.v) v, formed where it is used
+        for (int j = lane; j < L; j += 32)
+            kk = fmaf(s.pv[j], s.vv[j], kk);
+        kk = 0.5f * beta * warp_sum(kk);
+        if (i < L) {   // G22 -= v w^T + w v^T, eight columns loaded before any is stored
+            const float vi = s.vv[i], wi = fmaf(-kk, vi, s.pv[i]);
+            const int jl = min(32, L - 32 * q);   // columns of this quarter
+            for (int u0 = 0; u0 < 32; u0 += 8) {
+                float a[8], vj[8], pj[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int jj = (u0 + u + 8 * q) & 31, j = 32 * q + jj;
+                    const bool ok = jj < jl;
+                    a[u] = ok ? row[j] : 0.f;
+                    vj[u] = ok ? s.vv[j] : 0.f;
+                    pj[u] = ok ? s.pv[j] : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                    const int jj = (u0 + u + 8 * q) & 31, j = 32 * q + jj;
+                    if (jj < jl)
+                        row[j] = a[u] - vi * fmaf(-kk, vj[u], pj[u]) - wi * vj[u];
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (threadIdx.x == 0) {
+        s.d[n - 2] = s.g[(n - 2) * ld + n - 2];
+        s.d[n - 1] = s.g[(n - 1) * ld + n - 1];
+        s.e[n - 2] = s.g[(n - 1) * ld + n - 2];
     }
     __syncthreads();
-    // eigenvector update: a fixed pair per thread when the pairs divide the block
-    const bool zfixed = kPfThreads % n2 == 0;
-    const int za = threadIdx.x % n2, zi0 = threadIdx.x / n2, zstep = kPfThreads / n2;
-    for (int sweep = 0; sweep < kPfMaxSweeps; ++sweep) {
-        int swept = 0;
-        for (int r = 0; r < n - 1; ++r) {
-            int rot = 0;
-            if (threadIdx.x < n2) {
-                // circle method: position 0 fixed, the others turn by one each round
-                const int k = threadIdx.x;
-                const int p = k == 0 ? 0 : 1 + (k - 1 + r) % (n - 1);
-                const int q = 1 + (n - 2 - k + r) % (n - 1);
-                const float apq = s.g[p * ld + q], app = s.g[p * ld + p], aqq = s.g[q * ld + q];
-                float c = 1.f, sn = 0.f, t = 0.f;
-                if (fabsf(apq) > tol_abs && fabsf(apq) > tol_rel * sqrtf(fabsf(app) * fabsf(aqq))) {
-                    // the angle that zeroes g_pq (symmetric 2x2 Schur decomposition)
-                    const float tau = (aqq - app) / (2.f * apq);
-                    const float at = fabsf(tau);
-                    t = at > 1e18f ? 0.5f / tau : copysignf(1.f, tau) / (at + sqrtf(fmaf(tau, tau, 1.f)));
-                    if (t != 0.f) {
-                        c = rsqrtf(fmaf(t, t, 1.f));
-                        sn = t * c;
-                        rot = 1;
-                    } else {
-                        t = 0.f;
-                    }
-                }
-                s.prm[k] = make_float4(__uint_as_float((uint32_t)p | ((uint32_t)q << 16)), c, sn, t);
+}
+
+// Eigenvalues of T below x: the negative pivots of the LDL^T factorisation of
+// T - x I (Sylvester's law of inertia); tiny pivots are pushed to -piv.
+__device__ __forceinline__ int sturm_count(int n, const float* d, const float* e2, float x, float piv)
+{
+    float q = d[0] - x;
+    if (fabsf(q) < piv)
+        q = -piv;
+    int c = q < 0.f;
+    for (int i = 1; i < n; ++i) {
+        q = (d[i] - x) - __fdividef(e2[i - 1], q);
+        if (fabsf(q) < piv)
+            q = -piv;
+        c += q < 0.f;
+    }
+    return c;
+}
+
+// The m largest eigenvalues of T into s.lam (descending), by multisection.
+__device__ void bisect(int n, int m, const PfShared& s)
+{
+    __shared__ float s_lo, s_hi, s_piv;
+    const int lane = threadIdx.x & 31;
+    for (int i = threadIdx.x; i < n - 1; i += kPfThreads)
+        s.e2[i] = s.e[i] * s.e[i];
+    if (threadIdx.x < 32) {   // Gershgorin interval, pivot floor
+        float lo = 3.0e38f, hi = -3.0e38f, emax = 0.f;
+        for (int i = lane; i < n; i += 32) {
+            const float r = (i > 0 ? fabsf(s.e[i - 1]) : 0.f) + (i < n - 1 ? fabsf(s.e[i]) : 0.f);
+            lo = fminf(lo, s.d[i] - r);
+            hi = fmaxf(hi, s.d[i] + r);
+            if (i < n - 1)
+                emax = fmaxf(emax, s.e[i] * s.e[i]);
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) {
+            lo = fminf(lo, __shfl_xor_sync(0xffffffffu, lo, o));
+            hi = fmaxf(hi, __shfl_xor_sync(0xffffffffu, hi, o));
+            emax = fmaxf(emax, __shfl_xor_sync(0xffffffffu, emax, o));
+        }
+        if (lane == 0) {
+            const float pad = 1.2e-7f * fmaxf(fabsf(lo), fabsf(hi)) + 1e-30f;
+            s_lo = lo - pad;
+            s_hi = hi + pad;
+            s_piv = fmaxf(1e-30f, 1.2e-7f * emax);
+        }
+    }
+    __syncthreads();
+    const int S = m <= 32 ? 16 : (m <= 64 ? 8 : 4);        // lanes per eigenvalue
+    const int iters = S == 16 ? 9 : (S == 8 ? 12 : 15);     // (S+1)^iters > 2^32
+    const int r = threadIdx.x / S, sl = threadIdx.x - r * S;
+    const int k = n - 1 - min(r, m - 1);                    // ascending index of the r-th largest
+    const unsigned gmask = (S == 32 ? 0xffffffffu : ((1u << S) - 1u)) << (lane & ~(S - 1));
+    float lo = s_lo, hi = s_hi;
+    const float piv = s_piv;
+    for (int it = 0; it < iters; ++it) {
+        const float step = (hi - lo) / (float)(S + 1);
+        const int c = sturm_count(n, s.d, s.e2, lo + (float)(sl + 1) * step, piv);
+        const int st = __popc(__ballot_sync(0xffffffffu, c <= k) & gmask);   // points left of lambda
+        const float nlo = st > 0 ? lo + (float)st * step : lo;
+        const float nhi = st < S ? lo + (float)(st + 1) * step : hi;
+        lo = nlo;
+        hi = nhi;
+    }
+    if (r < m && sl == 0)
+        s.lam[r] = 0.5f * (lo + hi);
+    __syncthreads();
+}
+
+// A fixed pseudo-random start vector entry in [-1, 1) (integer hash of (i, r)).
+__device__ __forceinline__ float start_entry(int i, int r)
+{
+    uint32_t h = (uint32_t)i * 2654435761u ^ (uint32_t)(r + 1) * 40503u;
+    h *= 2246822519u;
+    h ^= h >> 15;
+    return (float)(h & 0xFFFFFFu) * (1.0f / 8388608.0f) - 1.0f;
+}
+
+// (T - lam I) y = b in place (b in y, stride ys), partial pivoting; u0/u1/u2
+// (stride ws) hold the three diagonals of U (the first inverted).  Zero pivots become 2^-23
+// (T is scaled to trace 1).  The result is scaled to unit length.
+__device__ void tridiag_solve(int n, const float* d, const float* e, float lam, float* y, int ys, float* u0,
+                              float* u1, float* u2, int ws)
+{
+    float c0 = d[0] - lam, c1 = n > 1 ? e[0] : 0.f, c2 = 0.f, rc = y[0];
+    for (int i = 0; i < n - 1; ++i) {
+        float n0 = e[i], n1 = d[i + 1] - lam, n2 = i + 1 < n - 1 ? e[i + 1] : 0.f, rn = y[(i + 1) * ys];
+        if (fabsf(n0) > fabsf(c0)) {   // row swap
+            float t;
+            t = c0; c0 = n0; n0 = t;
+            t = c1; c1 = n1; n1 = t;
+            t = c2; c2 = n2; n2 = t;
+            t = rc; rc = rn; rn = t;
+        }
+        if (c0 == 0.f)
+            c0 = 1.1920929e-7f;
+        const float rc0 = __fdividef(1.f, c0);
+        const float l = n0 * rc0;
+        u0[i * ws] = rc0;   // U's diagonal, stored inverted
+        u1[i * ws] = c1;
+        u2[i * ws] = c2;
+        y[i * ys] = rc;
+        c0 = fmaf(-l, c1, n1);
+        c1 = fmaf(-l, c2, n2);
+        c2 = 0.f;
+        rc = fmaf(-l, rc, rn);
+    }
+    if (c0 == 0.f)
+        c0 = 1.1920929e-7f;
+    u0[(n - 1) * ws] = __fdividef(1.f, c0);
+    y[(n - 1) * ys] = rc;
+    float x1 = 0.f, x2 = 0.f, amax = 0.f;
+    for (int i = n - 1; i >= 0; --i) {   // back substitution
+        const float xi = (y[i * ys] - u1[i * ws] * x1 - u2[i * ws] * x2) * u0[i * ws];
+        y[i * ys] = xi;
+        amax = fmaxf(amax, fabsf(xi));
+        x2 = x1;
+        x1 = xi;
+    }
+    const float inv = amax > 0.f ? 1.f / amax : 1.f;
+    float nrm = 0.f;
+    for (int i = 0; i < n; ++i) {
+        const float v = y[i * ys] * inv;
+        nrm = fmaf(v, v, nrm);
+    }
+    const float sc = inv * rsqrtf(fmaxf(nrm, 1e-30f));
+    for (int i = 0; i < n; ++i)
+        y[i * ys] *= sc;
+}
+
+// Eigenvectors of T for s.lam into s.y (row stride ys).
+__device__ void eigenvectors(int n, int m, int ys, const PfShared& s)
+{
+    const int ld = n + 1, warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int q = threadIdx.x; q < n * m; q += kPfThreads) {
+        const int i = q / m, r = q - i * m;
+        s.y[i * ys + r] = start_entry(i, r);
+    }
+    __syncthreads();
+    // batches of B vectors, one lane each; work arrays [3][n][B] in the z region
+    const int B = min(32, (n * ld) / (3 * n));
+    if (warp == 0) {
+        for (int b0 = 0; b0 < m; b0 += B) {
+            const int r = b0 + lane;
+            if (lane < B && r < m) {
+                for (int it = 0; it < kPfSolves; ++it)
+                    tridiag_solve(n, s.d, s.e, s.lam[r], s.y + r, ys, s.z + lane, s.z + n * B + lane,
+                                  s.z + 2 * n * B + lane, B);
             }
-            if (!__syncthreads_or(rot))
-                continue;   // nothing turns this round
-            swept = 1;
-            // G <- J^T G J over the pair blocks (a <= b), two blocks in flight
-            for (int e = threadIdx.x; e < ntri; e += 2 * kPfThreads) {
-                const int e2 = e + kPfThreads;
-                const uint32_t ab = s.tri[e], ab2 = e2 < ntri ? s.tri[e2] : 0u;
-                const int a = (int)(ab & 0xFFFF), b = (int)(ab >> 16);
-                const int a2 = (int)(ab2 & 0xFFFF), b2 = (int)(ab2 >> 16);
-                const float4 A = s.prm[a], B = s.prm[b];
-                const float4 A2 = s.prm[a2], B2 = s.prm[b2];
-                if (a == b) {
-                    if (A.w != 0.f)
-                        turn_diag(s.g, ld, A);
-                } else if (A.w != 0.f || B.w != 0.f) {
-                    turn_block(s.g, ld, A, B);
-                }
-                if (e2 < ntri) {
-                    if (a2 == b2) {
-                        if (A2.w != 0.f)
-                            turn_diag(s.g, ld, A2);
-                    } else if (A2.w != 0.f || B2.w != 0.f) {
-                        turn_block(s.g, ld, A2, B2);
-                    }
-                }
+            __syncwarp();
+        }
+    }
+    __syncthreads();
+    // classical Gram-Schmidt, twice, vector by vector
+    for (int j = 1; j < m; ++j) {
+        for (int pass = 0; pass < 2; ++pass) {
+            for (int i = warp; i < j; i += kPfWarps) {   // coefficients y_i . y_j
+                float acc = 0.f;
+                for (int t = lane; t < n; t += 32)
+                    acc = fmaf(s.y[t * ys + i], s.y[t * ys + j], acc);
+                acc = warp_sum(acc);
+                if (lane == 0)
+                    s.pv[i] = acc;
             }
-            // Z <- Z J (columns p, q of every row)
-            if (zfixed) {
-                const float4 A = s.prm[za];
-                if (A.w != 0.f) {
-#pragma unroll 4
-                    for (int i = zi0; i < n; i += zstep)
-                        turn_z(s.z + i * ld, A);
-                }
-            } else {
-                for (int e = threadIdx.x; e < n * n2; e += kPfThreads) {
-                    const int i = e / n2, a = e - i * n2;
-                    const float4 A = s.prm[a];
-                    if (A.w != 0.f)
-                        turn_z(s.z + i * ld, A);
-                }
+            __syncthreads();
+            for (int t = threadIdx.x; t < n; t += kPfThreads) {
+                float acc = s.y[t * ys + j];
+                for (int i = 0; i < j; ++i)
+                    acc = fmaf(-s.pv[i], s.y[t * ys + i], acc);
+                s.y[t * ys + j] = acc;
             }
             __syncthreads();
         }
-        if (!swept)
-            return true;
+        if (warp == 0) {
+            float acc = 0.f;
+            for (int t = lane; t < n; t += 32)
+                acc = fmaf(s.y[t * ys + j], s.y[t * ys + j], acc);
+            const float sc = rsqrtf(fmaxf(warp_sum(acc), 1e-30f));
+            for (int t = lane; t < n; t += 32)
+                s.y[t * ys + j] *= sc;
+        }
+        __syncthreads();
     }
-    return false;
+}
+
+// Z = Q Y = H_0 H_1 ... H_{n-3} Y, one reflector at a time over all columns:
+// S threads per column form v^T y_c over interleaved rows, then every thread
+// updates its share of the trailing rows.
+__device__ void back_transform(int n, int m, int ys, const PfShared& s)
+{
+    const int ld = n + 1;
+    const int S = m <= 16 ? 32 : (m <= 32 ? 16 : (m <= 64 ? 8 : 4));   // S * m <= kPfThreads
+    const int c = threadIdx.x / S, sg = threadIdx.x - c * S;
+    const int ustep = kPfThreads / m, uc = threadIdx.x % m, ui = threadIdx.x / m;   // update mapping
+    for (int k = n - 3; k >= 0; --k) {
+        const float beta = s.beta[k];
+        if (beta == 0.f)
+            continue;
+        const float* v = s.g + (k + 1) * ld + k;   // v_i = v[i * ld]
+        float* yk = s.y + (k + 1) * ys;            // y_ic = yk[i * ys + c]
+        const int L = n - k - 1;
+        float acc = 0.f;
+        if (c < m)
+            for (int i = sg; i < L; i += S)
+                acc = fmaf(v[i * ld], yk[i * ys + c], acc);
+        for (int o = S >> 1; o > 0; o >>= 1)
+            acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (c < m && sg == 0)
+            s.pv[c] = beta * acc;
+        __syncthreads();
+        if (ui < ustep) {   // column uc, rows ui, ui + ustep, ...
+            const float sc = s.pv[uc];
+            for (int i0 = ui; i0 < L; i0 += 4 * ustep) {
+                float yv[4], vv[4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * ustep;
+                    yv[u] = i < L ? yk[i * ys + uc] : 0.f;
+                    vv[u] = i < L ? v[i * ld] : 0.f;
+                }
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    const int i = i0 + u * ustep;
+                    if (i < L)
+                        yk[i * ys + uc] = fmaf(-sc, vv[u], yv[u]);
+                }
+            }
+        }
+        __syncthreads();
+    }
 }
 
 __global__ void __launch_bounds__(kPfThreads, 1) patch_form_kernel(const __grid_constant__ PatchFormParams p)
 {
-    extern __shared__ __align__(16) unsigned char smem[];
-    const int n = p.cols, ld = n + 1, n2 = n / 2, m = p.m;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    __shared__ float s_trace;
+    __shared__ uint32_t s_tmem;
+    __shared__ int s_abort;
+    __shared__ __align__(8) uint64_t s_bar;
+    const int n = p.cols, ld = n + 1, m = p.m, mp = pf_mpad(m), ys = pf_ystride(m);
+    const int warp = threadIdx.x >> 5;
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    unsigned char* smem = smem_raw + (((raw + 1023u) & ~1023u) - raw);
+    const PfLayout lay = pf_layout(n, m);
     PfShared s;
+    s.y = reinterpret_cast<float*>(smem + lay.y);
+    s.g = reinterpret_cast<float*>(smem + lay.g);
+    s.z = reinterpret_cast<float*>(smem + lay.z);
     {
-        unsigned char* q = smem;
-        s.g = reinterpret_cast<float*>(q);
-        q += pf_round16(n * ld * 4);
-        s.z = reinterpret_cast<float*>(q);
-        q += pf_round16(n * ld * 4);
-        s.prm = reinterpret_cast<float4*>(q);
-        q += pf_round16(n2 * 16);
-        s.tri = reinterpret_cast<uint32_t*>(q);
-        q += pf_round16(n2 * (n2 + 1) / 2 * 4);
-        s.order = reinterpret_cast<int*>(q);
+        float** vec[6] = {&s.d, &s.e, &s.e2, &s.beta, &s.vv, &s.pv};
+        for (int i = 0; i < 6; ++i)
+            *vec[i] = reinterpret_cast<float*>(smem + lay.vec + i * pf_round16(n * 4));
     }
+    s.lam = reinterpret_cast<float*>(smem + lay.lam);
     const int64_t blk = blockIdx.x;
     const int64_t bo = blk / p.n_inner, bi = blk - bo * p.n_inner;
     const __nv_bfloat16* x = p.x + bo * p.outer_stride + bi * p.inner_stride;
-
-    gram(p, x, s);
-
-    // absolute floor of the threshold: 2^-23 of trace(G) = ||X||_F^2
-    __shared__ float trace;
-    if (threadIdx.x < 32) {
-        float acc = 0.f;
-        for (int i = threadIdx.x; i < n; i += 32)
-            acc += fabsf(s.g[i * ld + i]);
-        for (int o = 16; o > 0; o >>= 1)
-            acc += __shfl_xor_sync(0xffffffffu, acc, o);
-        if (threadIdx.x == 0)
-            trace = acc;
-    }
-    __syncthreads();
-    const bool converged = jacobi(n, s, trace * 1.1920929e-7f);
-    if (!converged && threadIdx.x == 0)
-        raise_err(p.err, KAMERA_DEVERR_NOCONV);
-
-    // eigenvalues in descending order (ties by index); every rank starts at a
-    // valid index so that non-finite input still reads in bounds
-    for (int i = threadIdx.x; i < n; i += kPfThreads)
-        s.order[i] = i;
-    __syncthreads();
-    for (int i = threadIdx.x; i < n; i += kPfThreads) {
-        const float li = s.g[i * ld + i];
-        int rank = 0;
-        for (int j = 0; j < n; ++j) {
-            const float lj = s.g[j * ld + j];
-            rank += (lj > li) || (lj == li && j < i);
-        }
-        if (rank < m)
-            s.order[rank] = i;
-    }
-    __syncthreads();
-    // V = Z[:, order[:m]] (bf16 out, fp32 copy [n][mp] in the g region), sigma
-    const int mp = (m + 3) & ~3;
-    float* vt = s.g;   // G is no longer needed
-    if (p.sigma)
-        for (int r = threadIdx.x; r < m; r += kPfThreads) {
-            const float l = s.g[s.order[r] * ld + s.order[r]];
-            p.sigma[blk * m + r] = sqrtf(fmaxf(l, 0.f));
-        }
-    __syncthreads();
-    __nv_bfloat16* vo = p.v + blk * (int64_t)n * m;
-    for (int e = threadIdx.x; e < n * mp; e += kPfThreads) {
-        const int c = e / mp, r = e - c * mp;
-        const float z = r < m ? s.z[c * ld + s.order[r]] : 0.f;
-        vt[e] = z;
-        if (r < m)
-            vo[(int64_t)c * m + r] = __float2bfloat16_rn(z);
-    }
-    // U = X V: every thread owns 4 rows x 4 ranks of a staged row tile.  The
-    // tile's row stride n + 2 puts the rows that the threads of a warp read at
-    // once in different banks.
     __nv_bfloat16* uo = p.u + blk * (int64_t)p.rows * m;
-    const int sld = n + 2;
-    const int rg = mp / 4, rt = ((n * ld) / sld) & ~3;   // rows that fit the z region
-    for (int r0 = 0; r0 < p.rows; r0 += rt) {
-        const int nr = min(rt, p.rows - r0);
+
+    // The contractions run on the tensor cores when X is a plain bf16 block;
+    // the mean of several deficits (not exact in bf16) takes the CUDA cores.
+    const bool tc = p.n_terms == 1;
+    PfTc t;
+    t.tile = ptx::smem_addr(smem) + lay.tc;
+    t.bar = ptx::smem_addr(&s_bar);
+    t.phase = 0;
+    if (tc) {
+        if (warp == 0) {
+            ptx::tmem_alloc(ptx::smem_addr(&s_tmem), kPfTmemCols);
+            ptx::tmem_relinquish();
+        }
+        if (threadIdx.x == 32) {
+            ptx::mbar_init(t.bar, 1);
+            ptx::fence_barrier_init();
+        }
+        if (threadIdx.x == 0)
+            s_abort = 0;
+        ptx::tc_fence_before();
         __syncthreads();
-        stage_rows(p, x, r0, nr, s.z, sld);
+        ptx::tc_fence_after();
+        t.tmem = s_tmem;
+    }
+    bool ok = true;
+    if (tc)
+        ok = gram_tc(p, x, s, t, &s_abort);
+    else
+        gram(p, x, s);
+
+    if (ok) {
+        if (threadIdx.x < 32) {   // trace(G) = ||X||_F^2
+            float acc = 0.f;
+            for (int i = threadIdx.x; i < n; i += 32)
+                acc += s.g[i * ld + i];
+            acc = warp_sum(acc);
+            if (threadIdx.x == 0)
+                s_trace = acc;
+        }
         __syncthreads();
-        const int items = ((nr + 3) / 4) * rg;
-        for (int it = threadIdx.x; it < items; it += kPfThreads) {
-            const int tg = it / rg, k0 = 4 * (it - tg * rg), t0 = 4 * tg;
-            float acc[4][4];
+        const float trace = s_trace;
+        if (trace > 0.f) {
+            const float inv = 1.f / trace;
+            for (int q = threadIdx.x; q < n * n; q += kPfThreads) {
+                const int i = q / n, j = q - i * n;
+                s.g[i * ld + j] *= inv;
+            }
+            __syncthreads();
+            tridiagonalise(n, s);
+            bisect(n, m, s);
+            eigenvectors(n, m, ys, s);
+            back_transform(n, m, ys, s);
+        } else {   // X = 0: any orthonormal V, U = 0, sigma = 0
+            for (int q = threadIdx.x; q < n * m; q += kPfThreads) {
+                const int i = q / m, r = q - i * m;
+                s.y[i * ys + r] = i == r ? 1.f : 0.f;
+            }
+            for (int r = threadIdx.x; r < m; r += kPfThreads)
+                s.lam[r] = 0.f;
+            __syncthreads();
+        }
+
+        if (p.sigma)
+            for (int r = threadIdx.x; r < m; r += kPfThreads)
+                p.sigma[blk * m + r] = sqrtf(fmaxf(s.lam[r] * trace, 0.f));
+        __nv_bfloat16* vo = p.v + blk * (int64_t)n * m;
+        for (int q = threadIdx.x; q < n * m; q += kPfThreads) {
+            const int c = q / m, r = q - c * m;
+            vo[q] = __float2bfloat16_rn(s.y[c * ys + r]);
+        }
+        __syncthreads();
+        if (tc) {
+            u_tc(p, x, s, ys, t, uo, &s_abort);
+        } else {
+            // fp32 copy of V [n][mp] (16-byte rows, zero-padded) in the g region
+            float* vt = s.g;
+            for (int q = threadIdx.x; q < n * mp; q += kPfThreads) {
+                const int c = q / mp, r = q - c * mp;
+                vt[q] = r < m ? s.y[c * ys + r] : 0.f;
+            }
+            // U = X V: every thread owns 4 rows x 4 ranks of a staged row tile.  The
+            // tile's row stride n + 2 puts the rows that the threads of a warp read at
+            // once in different banks.
+            const int sld = n + 2;
+            const int rg = mp / 4, rt = ((n * ld) / sld) & ~3;   // rows that fit the z region
+            for (int r0 = 0; r0 < p.rows; r0 += rt) {
+                const int nr = min(rt, p.rows - r0);
+                __syncthreads();
+                stage_rows(p, x, r0, nr, s.z, sld);
+                __syncthreads();
+                const int items = ((nr + 3) / 4) * rg;
+                for (int it = threadIdx.x; it < items; it += kPfThreads) {
+                    const int tg = it / rg, k0 = 4 * (it - tg * rg), t0 = 4 * tg;
+                    float acc[4][4];
 #pragma unroll
-            for (int a = 0; a < 4; ++a)
+                    for (int a = 0; a < 4; ++a)
 #pragma unroll
-                for (int b = 0; b < 4; ++b)
-                    acc[a][b] = 0.f;
-            const int tr = min(4, nr - t0);
-            for (int c = 0; c < n; ++c) {
-                const float4 v4 = *reinterpret_cast<const float4*>(vt + c * mp + k0);
+                        for (int b = 0; b < 4; ++b)
+                            acc[a][b] = 0.f;
+                    const int tr = min(4, nr - t0);
+                    for (int c = 0; c < n; ++c) {
+                        const float4 v4 = *reinterpret_cast<const float4*>(vt + c * mp + k0);
 #pragma unroll
-                for (int a = 0; a < 4; ++a) {
-                    const float xv = a < tr ? s.z[(t0 + a) * sld + c] : 0.f;
-                    acc[a][0] = fmaf(xv, v4.x, acc[a][0]);
-                    acc[a][1] = fmaf(xv, v4.y, acc[a][1]);
-                    acc[a][2] = fmaf(xv, v4.z, acc[a][2]);
-                    acc[a][3] = fmaf(xv, v4.w, acc[a][3]);
+                        for (int a = 0; a < 4; ++a) {
+                            const float xv = a < tr ? s.z[(t0 + a) * sld + c] : 0.f;
+                            acc[a][0] = fmaf(xv, v4.x, acc[a][0]);
+                            acc[a][1] = fmaf(xv, v4.y, acc[a][1]);
+                            acc[a][2] = fmaf(xv, v4.z, acc[a][2]);
+                            acc[a][3] = fmaf(xv, v4.w, acc[a][3]);
+                        }
+                    }
+                    for (int a = 0; a < tr; ++a)
+#pragma unroll
+                        for (int b = 0; b < 4; ++b)
+                            if (k0 + b < m)
+                                uo[(int64_t)(r0 + t0 + a) * m + k0 + b] = __float2bfloat16_rn(acc[a][b]);
                 }
             }
-            for (int a = 0; a < tr; ++a)
-#pragma unroll
-                for (int b = 0; b < 4; ++b)
-                    if (k0 + b < m)
-                        uo[(int64_t)(r0 + t0 + a) * m + k0 + b] = __float2bfloat16_rn(acc[a][b]);
+        }
+    }
+    if (tc) {
+        if (*(volatile int*)&s_abort && threadIdx.x == 0) {   // let an MMA still in flight finish
+            const uint64_t t0 = ptx::globaltimer();
+            while (!ptx::mbar_try_wait(t.bar, t.phase & 1u) && ptx::globaltimer() - t0 < kPfTimeoutNs) {
+            }
+        }
+        ptx::tc_fence_before();
+        __syncthreads();
+        if (warp == 0) {
+            ptx::tc_fence_after();
+            ptx::tmem_dealloc(t.tmem, kPfTmemCols);
         }
     }
 }
@@ -394,7 +894,7 @@ bool patch_form_supported(int cols, int m)
 
 cudaError_t launch_patch_form(const PatchFormParams& p, int64_t n_blocks, cudaStream_t stream)
 {
-    const int bytes = pf_smem_bytes(p.cols);
+    const int bytes = pf_smem_bytes(p.cols, p.m);
     cudaError_t e = cudaFuncSetAttribute(patch_form_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess)
         return e;

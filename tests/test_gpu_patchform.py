@@ -5,7 +5,7 @@ Singular vectors are unique only up to sign, and only where the singular
 value is isolated, so each block is compared on what is unique:
   - singular values: |sigma_g^2 - sigma_o^2| <= 1e-4 sigma_1^2.  The GPU forms
     the Gram matrix in fp32 (relative error of an entry at most rows * 2^-24,
-    7.7e-5 at 1296 rows) and the Jacobi solve is backward stable to a few
+    7.7e-5 at 1296 rows) and the eigen-solve is backward stable to a few
     n * 2^-24 of its norm;
   - V has orthonormal columns: |V^T V - I| <= 8e-3 (bf16 entries carry a
     relative error <= 2^-9, so an inner product of unit vectors moves by at
