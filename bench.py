@@ -189,13 +189,20 @@ def time_launches(call, steps, flush_buf=None):
     return [a.elapsed_time(b) for a, b in evs]
 
 
-def sweep(K, dev, peak, skip):
+def kernel_of(spec) -> str:
+    """The kernel a workload's call spends its time in (the relocation calls of the
+    configured workloads all carry patches, so they take the tensor-core kernel)."""
+    return {"slide": "slide_kernel", "ingest": "ingest_kernel", "mla_ingest": "ingest_kernel"}.get(
+        spec.kind, "relocate_patch_umma_kernel")
+
+
+def sweep(K, dev, peak, skip, only=None):
     """Every configured workload, timed per launch (median) with L2 flushes."""
     out = {}
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
     specs = [(n, f()) for n, f in W.CONFIGS.items()] + [("tiny_gqa_x4096", W.tiny_gqa_x(4096))]
     for name, spec in specs:
-        if name in skip:
+        if name in skip or (only is not None and name not in only):
             continue
         try:
             wl = W.make(spec, dev)
@@ -209,13 +216,14 @@ def sweep(K, dev, peak, skip):
             b = W.algorithmic_bytes(spec)
             out[name] = {"gbs": b / t / 1e9, "tokens_per_s": W.tokens(spec) / t, "ms": t * 1e3,
                          "frac_of_hbm_peak": b / t / 1e9 / peak, "bytes": b, "l2": "flushed between launches",
+                         "kernel": kernel_of(spec), "traffic": traffic_record(kernel_of(spec), name),
                          "device_err": int(err.item())}
             del wl, ch, call
             torch.cuda.empty_cache()
         except Exception as e:  # report, keep the headline
             out[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
     for name, f in W.FORMATION.items():
-        if name in skip:
+        if name in skip or (only is not None and name not in only):
             continue
         try:
             out[name] = formation_entry(K, f(), dev, peak, flush)
@@ -244,7 +252,8 @@ def formation_entry(K, spec, dev, peak, flush):
     return {"ms": t * 1e3, "blocks": W.deficit_blocks(spec), "blocks_per_s": W.deficit_blocks(spec) / t,
             "tokens_per_s": spec.length / t, "gbs": b / t / 1e9, "frac_of_hbm_peak": b / t / 1e9 / peak,
             "bytes": b, "contraction_tflops": fl / t / 1e12, "rank": spec.m,
-            "l2": "flushed between launches", "device_err": int(err.item())}
+            "l2": "flushed between launches", "kernel": "patch_form_kernel",
+            "traffic": traffic_record("patch_form_kernel", spec.name), "device_err": int(err.item())}
 
 
 def _replica(wl):
@@ -489,8 +498,7 @@ def ours_arm(args):
             pg.destroy_process_group()
         return 0
 
-    kernel_name = {"slide": "slide_kernel", "ingest": "ingest_kernel", "mla_ingest": "ingest_kernel"}.get(
-        spec.kind, "relocate_patch_umma_kernel")
+    kernel_name = kernel_of(spec)
     e2e = e2e_measure(K, wl, max(2, min(args.steps, 10)), 1)
     e2e["value"] *= world
     line = {
@@ -517,7 +525,8 @@ def ours_arm(args):
     if world == 1 and not args.no_sweep:
         del wl, chunks_dev, call
         torch.cuda.empty_cache()
-        line["per_config"] = sweep(K, dev, peak, skip={args.config} if args.skip_headline_in_sweep else set())
+        line["per_config"] = sweep(K, dev, peak, skip={args.config} if args.skip_headline_in_sweep else set(),
+                                   only=set(args.sweep_only.split(",")) if args.sweep_only else None)
     print(json.dumps(line), flush=True)
     if pg:
         pg.barrier()
@@ -535,6 +544,7 @@ def main():
     ap.add_argument("--no-sweep", action="store_true", help="headline workload only")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--skip-headline-in-sweep", action="store_true")
+    ap.add_argument("--sweep-only", default="", help="comma-separated workloads the sweep is limited to")
     ap.add_argument("--ref-seconds", type=float, default=8.0, help="oracle seconds per sample")
     ap.add_argument("--layers", type=int, default=0,
                     help="run the workload with this many layers (a smaller case for profiler captures)")
