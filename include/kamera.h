@@ -382,8 +382,13 @@ typedef struct KameraDeficit {
  *          the Uk/Uv or Ur layout of KameraChunk for a [L][H] block grid)
  *   v      bf16 [n_outer*n_inner][cols][m] (written; the Vk/Vv or Vr layout)
  *   sigma  fp32 [n_outer*n_inner][m] singular values (written), or NULL
- * Supported: 8 <= cols <= 128 with cols % 8 == 0 (head_dim up to 128, MLA
- * k_rope), 1 <= m <= cols, rows >= 1, n_outer*n_inner < 2^31.  u, v and sigma
+ * Supported: cols % 8 == 0 and 8 <= cols <= 128 with 1 <= m <= cols (head_dim
+ * up to 128, MLA k_rope), or 128 < cols <= 512 with 1 <= m <= 32 (the MLA
+ * c_KV block); rows >= 1, n_outer*n_inner < 2^31.  Blocks wider than 128
+ * columns take subspace iteration on X^T X (three products of a basis of
+ * k = min(48, m + 16 rounded up to 16) columns) and a Rayleigh-Ritz step:
+ * exact to fp32 rounding when sigma_{k+1} is well below sigma_m (a deficit
+ * whose energy sits in fewer than k directions), near-optimal otherwise.  u, v and sigma
  * must not overlap each other or the deficit.  Non-finite input gives
  * non-finite factors.  No block (n_outer, n_inner or rows 0) is a successful
  * no-op.  d_err: reserved for device-side errors (none is raised by this

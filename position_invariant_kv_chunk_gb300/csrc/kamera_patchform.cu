@@ -885,15 +885,343 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_kernel(const __grid_
     }
 }
 
+// ------------------------------------------------------------ wide blocks --
+// Blocks wider than one SM can hold G for (128 < cols <= 512: the MLA c_KV
+// block) take subspace iteration with a Rayleigh-Ritz step (Golub & Van Loan,
+// section 8.2.4, orthogonal iteration; the Ritz step of section 8.1): a basis
+// Z of k = m + 16 (rounded to 16, at most 48) columns is multiplied by
+// G = X^T X kWideIters times, each product streamed over the rows of X as
+// X^T (X Z) without forming G, and re-orthonormalised; then C = Z^T G Z
+// (k x k) is solved by the routines above, V = Z W[:, :m] and U = X V.  The
+// top-m directions converge at the rate (sigma_{k+1} / sigma_m)^2 per
+// product.  All on the CUDA cores, one CTA per block.
+constexpr int kWideMaxCols = 512;
+constexpr int kWideMaxRank = 32;
+constexpr int kWideIters = 3;
+constexpr int kWideT = 32;   // rows of X per staged tile
+
+__host__ __device__ inline int pf_wide_k(int m) { return min(48, (m + 16 + 15) & ~15); }
+
+struct PfWideLayout {
+    int z, xt, yt, small, end;
+};
+
+// Basis Z (and later V) [c][k+1], X tile [T][c+4], X Z tile [T][k], then the
+// small eigenproblem's PfShared for n = k.
+__host__ __device__ inline PfWideLayout pf_wide_layout(int c, int m)
+{
+    const int k = pf_wide_k(m);
+    PfWideLayout L;
+    L.z = 0;
+    L.xt = pf_round16(c * (k + 1) * 4);
+    L.yt = L.xt + pf_round16(kWideT * (c + 4) * 4);
+    L.small = L.yt + pf_round16(kWideT * k * 4);
+    L.end = L.small + pf_round16(k * pf_ystride(m) * 4) + 2 * pf_round16(k * (k + 1) * 4) +
+            6 * pf_round16(k * 4) + pf_round16(m * 4);
+    return L;
+}
+
+// Column-wise classical Gram-Schmidt, twice, on Z [c][zs] (one row per thread),
+// every column normalised; coefficients reduced by shuffles and shared atomics
+// into coef[0 .. k-1], the squared norm into coef[kWideNormSlot].
+constexpr int kWideNormSlot = 63;
+__device__ void wide_cgs2(float* z, int zs, int c, int k, float* coef)
+{
+    const int lane = threadIdx.x & 31, t = threadIdx.x;
+    for (int j = 0; j < k; ++j) {
+        for (int pass = 0; pass < 2 && j > 0; ++pass) {
+            for (int i = t; i < j; i += kPfThreads)
+                coef[i] = 0.f;
+            __syncthreads();
+            const float zj = t < c ? z[t * zs + j] : 0.f;
+            for (int i = 0; i < j; ++i) {
+                float part = t < c ? z[t * zs + i] * zj : 0.f;
+                part = warp_sum(part);
+                if (lane == 0)
+                    atomicAdd(&coef[i], part);
+            }
+            __syncthreads();
+            if (t < c) {
+                float acc = zj;
+                for (int i = 0; i < j; ++i)
+                    acc = fmaf(-coef[i], z[t * zs + i], acc);
+                z[t * zs + j] = acc;
+            }
+            __syncthreads();
+        }
+        if (t == 0)
+            coef[kWideNormSlot] = 0.f;
+        __syncthreads();
+        const float v = t < c ? z[t * zs + j] : 0.f;
+        const float part = warp_sum(v * v);
+        if (lane == 0)
+            atomicAdd(&coef[kWideNormSlot], part);
+        __syncthreads();
+        const float sc = rsqrtf(fmaxf(coef[kWideNormSlot], 1e-30f));
+        if (t < c)
+            z[t * zs + j] = v * sc;
+        __syncthreads();
+    }
+}
+
+// Stage rows r0 .. r0 + kWideT - 1 of X (the mean of its terms) as fp32
+// [T][c + 4], zero past rows.
+__device__ __forceinline__ void wide_stage(const PatchFormParams& p, const __nv_bfloat16* x, int r0, float* xt)
+{
+    const int c = p.cols, vpr = c / 8, xs = c + 4;
+    const float inv = 1.0f / (float)p.n_terms;
+    for (int e = threadIdx.x; e < kWideT * vpr; e += kPfThreads) {
+        const int r = e / vpr, c8 = (e - r * vpr) * 8;
+        float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        if (r0 + r < p.rows) {
+            const __nv_bfloat16* src = x + (int64_t)(r0 + r) * p.row_stride + c8;
+            for (int tm = 0; tm < p.n_terms; ++tm) {
+                float w[8];
+                unpack8(*reinterpret_cast<const uint4*>(src + (int64_t)tm * p.term_stride), w);
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    v[q] += w[q];
+            }
+            if (p.n_terms > 1)
+#pragma unroll
+                for (int q = 0; q < 8; ++q)
+                    v[q] *= inv;
+        }
+        float* d = xt + r * xs + c8;
+#pragma unroll
+        for (int q = 0; q < 8; ++q)
+            d[q] = v[q];
+    }
+}
+
+// out[T][ncol] = Xt[T][c] B[c][ncol] (B row stride bs): each of four adjacent
+// threads sums a quarter of c for a 4-row x 4-column block, combined by shuffles.
+__device__ void wide_xb(const float* xt, int c, const float* b, int bs, int ncol, float* out, int os)
+{
+    const int xs = c + 4, cg = (ncol + 3) / 4, blocks = (kWideT / 4) * cg;
+    const int q = threadIdx.x & 3, blk = threadIdx.x >> 2;
+    float acc[4][4] = {};
+    const int t0 = 4 * (blk / cg), j0 = 4 * (blk % cg);
+    if (blk < blocks) {
+        for (int i = q; i < c; i += 4) {
+            float bv[4], xv[4];
+#pragma unroll
+            for (int u = 0; u < 4; ++u) {
+                bv[u] = j0 + u < ncol ? b[i * bs + j0 + u] : 0.f;
+                xv[u] = xt[(t0 + u) * xs + i];
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    acc[a][u] = fmaf(xv[a], bv[u], acc[a][u]);
+        }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int u = 0; u < 4; ++u) {
+            acc[a][u] += __shfl_xor_sync(0xffffffffu, acc[a][u], 1);
+            acc[a][u] += __shfl_xor_sync(0xffffffffu, acc[a][u], 2);
+        }
+    if (blk < blocks && q == 0)
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int u = 0; u < 4; ++u)
+                if (j0 + u < ncol)
+                    out[(t0 + a) * os + j0 + u] = acc[a][u];
+}
+
+__global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __grid_constant__ PatchFormParams p)
+{
+    extern __shared__ __align__(16) unsigned char smem[];
+    __shared__ float s_coef[kWideNormSlot + 1];
+    __shared__ float s_trace;
+    const int c = p.cols, m = p.m, k = pf_wide_k(m), zs = k + 1, ys = pf_ystride(m);
+    const PfWideLayout lay = pf_wide_layout(c, m);
+    float* z = reinterpret_cast<float*>(smem + lay.z);
+    float* xt = reinterpret_cast<float*>(smem + lay.xt);
+    float* yt = reinterpret_cast<float*>(smem + lay.yt);
+    PfShared s;   // the k x k Rayleigh-Ritz problem
+    {
+        unsigned char* q = smem + lay.small;
+        s.y = reinterpret_cast<float*>(q);
+        q += pf_round16(k * ys * 4);
+        s.g = reinterpret_cast<float*>(q);
+        q += pf_round16(k * (k + 1) * 4);
+        s.z = reinterpret_cast<float*>(q);
+        q += pf_round16(k * (k + 1) * 4);
+        float** vec[6] = {&s.d, &s.e, &s.e2, &s.beta, &s.vv, &s.pv};
+        for (int i = 0; i < 6; ++i) {
+            *vec[i] = reinterpret_cast<float*>(q);
+            q += pf_round16(k * 4);
+        }
+        s.lam = reinterpret_cast<float*>(q);
+    }
+    const int64_t blk = blockIdx.x;
+    const int64_t bo = blk / p.n_inner, bi = blk - bo * p.n_inner;
+    const __nv_bfloat16* x = p.x + bo * p.outer_stride + bi * p.inner_stride;
+    const int t = threadIdx.x;
+
+    for (int e = t; e < c * k; e += kPfThreads) {   // fixed pseudo-random start basis
+        const int i = e / k, j = e - i * k;
+        z[i * zs + j] = start_entry(i, j);
+    }
+    __syncthreads();
+    wide_cgs2(z, zs, c, k, s_coef);
+
+    // Z <- orth(X^T (X Z)), kWideIters times; the product accumulates in
+    // registers: thread -> rows 4 ig .. 4 ig + 3, columns jg * kq .. + kq
+    const int kq = k / 4, ig = t >> 2, jg = t & 3;
+    for (int it = 0; it < kWideIters; ++it) {
+        float acc[4][12] = {};
+        for (int r0 = 0; r0 < p.rows; r0 += kWideT) {
+            wide_stage(p, x, r0, xt);
+            __syncthreads();
+            wide_xb(xt, c, z, zs, k, yt, k);
+            __syncthreads();
+            if (4 * ig < c) {
+                for (int tt = 0; tt < kWideT; ++tt) {
+                    const float4 xv = *reinterpret_cast<const float4*>(xt + tt * (c + 4) + 4 * ig);
+                    const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                    for (int u = 0; u < 12; ++u) {
+                        if (u < kq) {
+                            const float yv = yt[tt * k + jg * kq + u];
+#pragma unroll
+                            for (int a = 0; a < 4; ++a)
+                                acc[a][u] = fmaf(xa[a], yv, acc[a][u]);
+                        }
+                    }
+                }
+            }
+            __syncthreads();
+        }
+        if (4 * ig < c)
+#pragma unroll
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int u = 0; u < 12; ++u)
+                    if (u < kq)
+                        z[(4 * ig + a) * zs + jg * kq + u] = acc[a][u];
+        __syncthreads();
+        wide_cgs2(z, zs, c, k, s_coef);
+    }
+
+    // Rayleigh-Ritz: C = (X Z)^T (X Z), accumulated per thread over its (a, b) entries
+    float cacc[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int r0 = 0; r0 < p.rows; r0 += kWideT) {
+        wide_stage(p, x, r0, xt);
+        __syncthreads();
+        wide_xb(xt, c, z, zs, k, yt, k);
+        __syncthreads();
+#pragma unroll
+        for (int u = 0; u < 5; ++u) {
+            const int e = t + u * kPfThreads;
+            if (e < k * k) {
+                const int a = e / k, b = e - a * k;
+                float sum = 0.f;
+                for (int tt = 0; tt < kWideT; ++tt)
+                    sum = fmaf(yt[tt * k + a], yt[tt * k + b], sum);
+                cacc[u] += sum;
+            }
+        }
+        __syncthreads();
+    }
+    const int ld = k + 1;
+#pragma unroll
+    for (int u = 0; u < 5; ++u) {
+        const int e = t + u * kPfThreads;
+        if (e < k * k)
+            s.g[(e / k) * ld + e % k] = cacc[u];
+    }
+    __syncthreads();
+    if (t < 32) {
+        float acc = 0.f;
+        for (int i = t; i < k; i += 32)
+            acc += s.g[i * ld + i];
+        acc = warp_sum(acc);
+        if (t == 0)
+            s_trace = acc;
+    }
+    __syncthreads();
+    const float trace = s_trace;
+    if (trace > 0.f) {
+        const float inv = 1.f / trace;
+        for (int q = t; q < k * k; q += kPfThreads)
+            s.g[(q / k) * ld + q % k] *= inv;
+        __syncthreads();
+        tridiagonalise(k, s);
+        bisect(k, m, s);
+        eigenvectors(k, m, ys, s);
+        back_transform(k, m, ys, s);
+    } else {
+        for (int q = t; q < k * m; q += kPfThreads) {
+            const int i = q / m, r = q - i * m;
+            s.y[i * ys + r] = i == r ? 1.f : 0.f;
+        }
+        for (int r = t; r < m; r += kPfThreads)
+            s.lam[r] = 0.f;
+        __syncthreads();
+    }
+    if (p.sigma)
+        for (int r = t; r < m; r += kPfThreads)
+            p.sigma[blk * m + r] = sqrtf(fmaxf(s.lam[r] * trace, 0.f));
+    // V = Z W (row t of Z -> row t of V, in place), bf16 out
+    __nv_bfloat16* vo = p.v + blk * (int64_t)c * m;
+    if (t < c) {
+        float zr[48];
+#pragma unroll
+        for (int j = 0; j < 48; ++j)
+            zr[j] = j < k ? z[t * zs + j] : 0.f;
+        for (int r = 0; r < m; ++r) {
+            float acc = 0.f;
+#pragma unroll
+            for (int j = 0; j < 48; ++j)
+                if (j < k)
+                    acc = fmaf(zr[j], s.y[j * ys + r], acc);
+            z[t * zs + r] = acc;
+            vo[(int64_t)t * m + r] = __float2bfloat16_rn(acc);
+        }
+    }
+    __syncthreads();
+    // U = X V
+    __nv_bfloat16* uo = p.u + blk * (int64_t)p.rows * m;
+    for (int r0 = 0; r0 < p.rows; r0 += kWideT) {
+        wide_stage(p, x, r0, xt);
+        __syncthreads();
+        wide_xb(xt, c, z, zs, m, yt, m);
+        __syncthreads();
+        for (int e = t; e < kWideT * m; e += kPfThreads) {
+            const int tt = e / m, r = e - tt * m;
+            if (r0 + tt < p.rows)
+                uo[(int64_t)(r0 + tt) * m + r] = __float2bfloat16_rn(yt[tt * m + r]);
+        }
+        __syncthreads();
+    }
+}
+
 }  // namespace
 
 bool patch_form_supported(int cols, int m)
 {
-    return cols >= 8 && cols <= kPfMaxCols && cols % 8 == 0 && m >= 1 && m <= cols;
+    if (cols < 8 || cols % 8 || m < 1 || m > cols)
+        return false;
+    return cols <= kPfMaxCols || (cols <= kWideMaxCols && m <= kWideMaxRank);
 }
 
 cudaError_t launch_patch_form(const PatchFormParams& p, int64_t n_blocks, cudaStream_t stream)
 {
+    if (p.cols > kPfMaxCols) {
+        const int bytes = pf_wide_layout(p.cols, p.m).end;
+        cudaError_t e = cudaFuncSetAttribute(patch_form_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             bytes);
+        if (e != cudaSuccess)
+            return e;
+        patch_form_wide_kernel<<<(unsigned)n_blocks, kPfThreads, bytes, stream>>>(p);
+        return cudaGetLastError();
+    }
     const int bytes = pf_smem_bytes(p.cols, p.m);
     cudaError_t e = cudaFuncSetAttribute(patch_form_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess)

@@ -178,10 +178,51 @@ def test_factors_feed_relocation():
                 assert err <= opt + 1e-2 * np.linalg.norm(blk), (kv, l, h, err, opt)
 
 
+@pytest.mark.parametrize("length,d,m", [(300, 512, 16), (4096, 512, 16), (300, 512, 32), (129, 136, 16),
+                                        (77, 256, 8)])
+def test_wide_blocks(length, d, m):
+    """Blocks wider than 128 columns (the 512-wide MLA c_KV block): subspace
+    iteration + Rayleigh-Ritz, held to the same bounds on the planted deficits,
+    whose spectrum falls off past the planted directions."""
+    run_and_check(W.DeficitSpec("pf_wide", L=2, length=length, H=1, d=d, m=m, kv=1))
+
+
+def near_optimal(spec: W.DeficitSpec, m: int):
+    """Without a gap after sigma_m the wide path's subspace is not the optimal
+    one; its rank-m factor still leaves at most 2% of ||X||^2 beyond the
+    Eckart-Young optimum, and V stays orthonormal."""
+    x = W.make_deficit(spec, DEV)
+    xb = _blocks(x)
+    u, v = K.kamera_form_patch(xb, m)
+    torch.cuda.synchronize()
+    xh, uh, vh = _f64(xb), _f64(u)[0, 0], _f64(v)[0, 0]
+    xh = xh.mean(axis=0)[0, 0] if xh.ndim == 5 else xh[0, 0]
+    so = np.linalg.svd(xh, compute_uv=False)
+    opt, tot = np.sum(so[m:] ** 2), np.sum(so ** 2)
+    res = np.linalg.norm(xh - uh @ vh.T) ** 2
+    assert res <= opt + 0.02 * tot, (res, opt, tot)
+    assert np.max(np.abs(vh.T @ vh - np.eye(m))) <= 8e-3
+
+
+def test_wide_flat_spectrum_is_near_optimal():
+    near_optimal(W.DeficitSpec("pf_flat", L=1, length=300, H=1, d=512, m=16, kv=1, planted=1, s_max=0.0,
+                               s_min=0.0, noise=1.0), 16)
+
+
+def test_wide_orbit_patch_is_near_optimal():
+    """The mean of three independently planted deficits spreads its energy over
+    ~96 directions (no gap after sigma_16): the near-optimality bound."""
+    near_optimal(W.DeficitSpec("pf_wide_orbit", L=1, length=200, H=1, d=512, m=16, kv=1, terms=3), 16)
+
+
 def test_host_errors():
-    x = torch.zeros(1, 1, 16, 256, dtype=torch.bfloat16, device=DEV)
+    x = torch.zeros(1, 1, 16, 520, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(K.KameraError) as e:
         K.kamera_form_patch(x, 8)
+    assert e.value.status == 3
+    x = torch.zeros(1, 1, 16, 512, dtype=torch.bfloat16, device=DEV)
+    with pytest.raises(K.KameraError) as e:   # wide blocks take ranks up to 32
+        K.kamera_form_patch(x, 33)
     assert e.value.status == 3
     x = torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16, device=DEV)
     with pytest.raises(K.KameraError) as e:

@@ -306,7 +306,13 @@ def make_deficit(spec: DeficitSpec, device="cpu") -> torch.Tensor:
     return x[0] if T == 1 else x
 
 
-FORMATION = {"qwen_patch_form": qwen_patch_form}
+def dsv2_patch_form() -> DeficitSpec:
+    """Rank-16 patch formation for one DeepSeek-V2-Lite shaped 4096-token chunk's
+    c_KV deficits: 27 layers, one 4096 x 512 block each (the wide-block path)."""
+    return DeficitSpec("dsv2_patch_form", L=27, length=4096, H=1, d=512, m=16, kv=1)
+
+
+FORMATION = {"qwen_patch_form": qwen_patch_form, "dsv2_patch_form": dsv2_patch_form}
 
 
 # ------------------------------------------------------------- workloads --
