@@ -16,6 +16,8 @@ technical summary):
 * section 2, patch formation (one conditioned forward, then an SVD keeping the
   top-m factors)                                                      -> ``form_patch``
 * section 3.2, sliding-window survival by rotation only               -> ``slide``
+* attention over reused chunks (the pages' attention-kernel hook, section 3):
+  softmax attention of a decode query over the reuse equation's rows -> ``attend``
 
 Pinned by ``tests/test_oracle_pins.py`` (closed forms, group laws of R, an
 independent complex-number RoPE, brute-force bf16 rounding, Eckart-Young by
@@ -346,6 +348,53 @@ class Oracle:
             raise ValueError("oracle: index out of range in the chunk list")
         del keep
         return sc if want_scale else None
+
+    def attend(self, store_k, store_v, chunks: Sequence[Chunk], seq_starts, q, layer: int, inv_freq,
+               rot_dim: int, rot_offset: int = 0, pairing: int = ROTATE_HALF, scale: float = None):
+        """Decode attention of one query token per sequence over its reused chunks,
+        each chunk's keys and values being the reuse equation's rows (technical
+        summary section 2: K = R(delta) K_canonical + U_k V_k^T, V = V_canonical +
+        U_v V_v^T), exact and unrounded (fp64), then softmax(scale q K^T) V.
+
+        ``store_*``: uint16 ``[N, H_kv, d]`` (one layer); ``q``: uint16
+        ``[S, H_q, d]`` (RoPE already applied at the query's position); sequence
+        s attends over chunks ``seq_starts[s] .. seq_starts[s+1]-1`` in order;
+        factors ``[L, H_kv, len, m]`` / ``[L, H_kv, d, m]`` read at ``layer``.
+        Returns (bf16 bits ``[S, H_q, d]``, fp64 output, magnitude scale
+        sum_j p_j |V_j| per element).  ``q`` and the factors may also be given
+        as fp64 values (for the pins)."""
+        N, H, d = store_k.shape
+        S, Hq, _ = q.shape
+        G = Hq // H
+        scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+        f64 = lambda a: a if np.asarray(a).dtype == np.float64 else self.bf16_to_f64(a)
+        kf, vf, qf = self.bf16_to_f64(store_k), self.bf16_to_f64(store_v), f64(q)
+        out = np.zeros((S, Hq, d))
+        mag = np.zeros((S, Hq, d))
+        for s in range(S):
+            for g in range(H):
+                Ks, Vs = [], []
+                for c in chunks[seq_starts[s]:seq_starts[s + 1]]:
+                    rows = slice(c.src_offset, c.src_offset + c.length)
+                    kk = self.rotate(kf[rows, g, :], c.delta, inv_freq, rot_dim, rot_offset, pairing)
+                    vv = vf[rows, g, :].copy()
+                    if c.rank > 0:
+                        uk, vk, uv, vvm = (f64(a)[layer, g] for a in c.patches)
+                        kk = kk + uk @ vk.T
+                        vv = vv + uv @ vvm.T
+                    Ks.append(kk)
+                    Vs.append(vv)
+                K = np.concatenate(Ks) if Ks else np.zeros((0, d))
+                V = np.concatenate(Vs) if Vs else np.zeros((0, d))
+                for h in range(g * G, (g + 1) * G):
+                    if K.shape[0] == 0:
+                        continue
+                    sc = scale * (K @ qf[s, h])
+                    w = np.exp(sc - sc.max())
+                    pr = w / w.sum()
+                    out[s, h] = pr @ V
+                    mag[s, h] = pr @ np.abs(V)
+        return self.bf16_rne(out), out, mag
 
     def num_threads(self) -> int:
         return int(self.lib.kamera_oracle_num_threads())

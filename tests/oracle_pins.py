@@ -576,6 +576,122 @@ def pin_ingest_recovers_canonical_keys(orc: O.Oracle):
         assert np.all(np.abs(rows - to_f64(pool[0, slots, 0])) <= tol)
 
 
+# --------------------------------------------------- attention over chunks
+def _attend_problem(rng, H=2, G=3, d=32, lens=(9, 5, 12, 3), deltas=(40, -7, 0, 1000), m=4, seqs=(0, 2, 4),
+                    L=2, layer=1, zero_rank=False):
+    N = sum(lens)
+    store_k = rand_bf16(rng, (L, N, H, d))
+    store_v = rand_bf16(rng, (L, N, H, d))
+    chunks, off = [], 0
+    for t, dl in zip(lens, deltas):
+        mm = 0 if zero_rank else m
+        pat = []
+        if mm:
+            pat = [rand_bf16(rng, (L, H, t, mm), .3), rand_bf16(rng, (L, H, d, mm), .3),
+                   rand_bf16(rng, (L, H, t, mm), .3), rand_bf16(rng, (L, H, d, mm), .3)]
+        chunks.append(O.Chunk(off, t, dl, mm, np.arange(t, dtype=np.int64), pat))
+        off += t
+    q = rand_bf16(rng, (len(seqs) - 1, H * G, d))
+    return store_k[layer], store_v[layer], chunks, list(seqs), q, layer
+
+
+def pin_attend_single_token(orc: O.Oracle):
+    """One token: the softmax weight is 1, so the output is that token's value row."""
+    rng = np.random.default_rng(31)
+    sk, sv, chunks, seqs, q, layer = _attend_problem(rng, lens=(1,), deltas=(77,), seqs=(0, 1), zero_rank=True)
+    th = orc.inv_freq(1e4, 32)
+    bits, out, _ = orc.attend(sk, sv, chunks, seqs, q, layer, th, 32)
+    for h in range(q.shape[1]):
+        assert np.array_equal(bits[0, h], sv[0, h // 3])
+
+
+def pin_attend_uniform_keys(orc: O.Oracle):
+    """Identical keys (delta 0, no patch): uniform weights, the mean of the values."""
+    rng = np.random.default_rng(32)
+    sk, sv, chunks, seqs, q, layer = _attend_problem(rng, lens=(6, 4), deltas=(0, 0), seqs=(0, 2), zero_rank=True)
+    sk[:] = sk[0]
+    th = orc.inv_freq(1e4, 32)
+    _, out, _ = orc.attend(sk, sv, chunks, seqs, q, layer, th, 32)
+    vmean = to_f64(sv).mean(axis=0)
+    for h in range(q.shape[1]):
+        assert np.max(np.abs(out[0, h] - vmean[h // 3])) < 1e-12
+
+
+def _attend_fused(orc, sk, sv, chunks, seqs, q, layer, th, r, o, pairing, scale):
+    """The same attention by the identity a fused kernel uses: the query turned by
+    -delta per chunk against the canonical keys, the patch as (V_k^T q) . u, and
+    the value patch folded in per chunk as V_v (sum_j p_j u_v,j); rotation by
+    complex multiplication (not the oracle's routine)."""
+    kf, vf, qf = to_f64(sk), to_f64(sv), to_f64(q)
+    S, Hq, d = qf.shape
+    H = kf.shape[1]
+    G = Hq // H
+    out = np.zeros((S, Hq, d))
+    for s in range(S):
+        cs = chunks[seqs[s]:seqs[s + 1]]
+        for h in range(Hq):
+            g = h // G
+            scores, parts = [], []
+            for c in cs:
+                rows = slice(c.src_offset, c.src_offset + c.length)
+                qr = complex_rotate(qf[s, h], -c.delta, th, r, o, pairing)
+                sc = kf[rows, g, :] @ qr
+                if c.rank:
+                    uk, vk, uv, vv = (to_f64(a)[layer, g] for a in c.patches)
+                    sc = sc + uk @ (vk.T @ qf[s, h])
+                scores.append(scale * sc)
+                parts.append(c)
+            allsc = np.concatenate(scores)
+            w = np.exp(allsc - allsc.max())
+            w /= w.sum()
+            acc, at = np.zeros(d), 0
+            for c, sc in zip(parts, scores):
+                pw = w[at:at + len(sc)]
+                at += len(sc)
+                rows = slice(c.src_offset, c.src_offset + c.length)
+                acc += pw @ vf[rows, g, :]
+                if c.rank:
+                    uk, vk, uv, vv = (to_f64(a)[layer, g] for a in c.patches)
+                    acc += vv @ (pw @ uv)
+            out[s, h] = acc
+    return out
+
+
+def pin_attend_fused_identity(orc: O.Oracle):
+    """The oracle's attention over the reuse equation's rows equals the fused
+    formulation (query turned per chunk, rank-m score and value corrections)."""
+    rng = np.random.default_rng(33)
+    for pairing, r, o in ((RH, 32, 0), (IL, 16, 8)):
+        sk, sv, chunks, seqs, q, layer = _attend_problem(rng)
+        th = orc.inv_freq(1e4, r)
+        _, out, _ = orc.attend(sk, sv, chunks, seqs, q, layer, th, r, o, pairing, scale=0.2)
+        ref = _attend_fused(orc, sk, sv, chunks, seqs, q, layer, th, r, o, pairing, 0.2)
+        assert np.max(np.abs(out - ref)) < 1e-10, (pairing, np.max(np.abs(out - ref)))
+
+
+def pin_attend_relative_position(orc: O.Oracle):
+    """Moving every chunk and the query by the same D changes nothing (RoPE
+    depends on relative position); with patches, V_k turned by R(D) as well (the
+    patch-frame identity R(D)(K + U V^T) = R(D) K + U (R(D) V)^T)."""
+    rng = np.random.default_rng(34)
+    for zero_rank in (True, False):
+        sk, sv, chunks, seqs, q, layer = _attend_problem(rng, zero_rank=zero_rank)
+        th = orc.inv_freq(1e4, 32)
+        _, out, _ = orc.attend(sk, sv, chunks, seqs, q, layer, th, 32)
+        D = 123
+        moved = []
+        for c in chunks:
+            pat = c.patches
+            if c.rank:
+                vk = to_f64(pat[1])
+                vk_t = np.swapaxes(complex_rotate(np.swapaxes(vk, -1, -2), D, th, 32, 0, RH), -1, -2)
+                pat = [to_f64(pat[0]), vk_t, to_f64(pat[2]), to_f64(pat[3])]
+            moved.append(O.Chunk(c.src_offset, c.length, c.delta + D, c.rank, c.slots, pat))
+        qm = complex_rotate(to_f64(q), D, th, 32, 0, RH)
+        _, out2, _ = orc.attend(sk, sv, moved, seqs, qm, layer, th, 32)
+        assert np.max(np.abs(out2 - out)) < 1e-9, (zero_rank, np.max(np.abs(out2 - out)))
+
+
 def pin_rejects_bad_indices(orc: O.Oracle):
     rng = np.random.default_rng(17)
     sk, sv, pk, pv, chunks = _small_gqa(rng)
