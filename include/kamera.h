@@ -77,7 +77,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
-#define KAMERA_ABI_VERSION 4
+#define KAMERA_ABI_VERSION 5
 
 /* Limits of this build. */
 #define KAMERA_MAX_RANK 128          /* largest patch rank m */
@@ -396,6 +396,56 @@ typedef struct KameraDeficit {
  */
 int kamera_form_patch(const KameraDeficit* deficit, int32_t m, void* u, void* v, float* sigma,
                       int32_t* d_err, struct CUstream_st* stream);
+
+/*
+ * Decode attention over reused chunks, without the pool (the pages serve reused
+ * chunks through a hook in the attention kernel: technical summary section 3,
+ * "Production Deployment").  Each sequence s has one query token per query
+ * head and attends, in one softmax, over the tokens of its chunks
+ * d_chunks[d_seq_start[s] .. d_seq_start[s+1]-1]; the keys and values of a
+ * chunk's token j are the reuse equation's rows, unrounded:
+ *     K_j = R(delta) k_j + Uk[j] Vk^T,   V_j = v_j + Uv[j] Vv^T
+ * (k_j, v_j: store row src_offset + j of this layer; factors as for
+ * kamera_relocate_patch, read at `layer`).  out = softmax(scale q K^T) V per
+ * query head; query head h reads KV head h / (num_q_heads / num_kv_heads).
+ * The kernel turns the query by -delta once per chunk and folds the patch into
+ * Vk^T q and Vv (sum_j p_j Uv[j]), so it reads only the store rows and the U
+ * rows.  fp32 arithmetic, one bf16 rounding of the output; a sequence with no
+ * token gets zeros.
+ *   kv      the canonical store of ONE layer: k, v bf16 [num_rows][num_kv_heads]
+ *           [head_dim], rows row_stride elements apart (16-byte aligned,
+ *           row_stride a multiple of 8); layer = the factors' layer index
+ *   query   q bf16 [n_seqs][num_q_heads][head_dim] (RoPE already applied at the
+ *           query's position), out bf16 of the same shape (written), scale
+ *   d_seq_start  device int32 [n_seqs + 1], non-decreasing, in [0, n_chunks]
+ *   dst_slot_mapping of the descriptors is not read; ranks <= max_rank <= 64.
+ * Supported: head_dim 64 or 128, num_q_heads / num_kv_heads in 1..8.
+ * Device errors (the chunk is skipped): SOURCE, DESCRIPTOR (also a malformed
+ * d_seq_start: the sequence is skipped), LEN, RANK.
+ */
+typedef struct KameraAttnKV {
+    const void* k;
+    const void* v;
+    int64_t num_rows;
+    int64_t row_stride;
+    int32_t num_kv_heads;
+    int32_t head_dim;
+    int32_t layer;
+    int32_t reserved;   /* 0 */
+} KameraAttnKV;
+
+typedef struct KameraAttnQuery {
+    const void* q;
+    void* out;
+    int32_t n_seqs;
+    int32_t num_q_heads;
+    float scale;
+    int32_t reserved;   /* 0 */
+} KameraAttnQuery;
+
+int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, const KameraRope* rope,
+                         const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
+                         int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream);
 
 /* KAMERA_ABI_VERSION of the loaded library. */
 int kamera_abi_version(void);

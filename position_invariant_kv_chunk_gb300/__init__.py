@@ -24,7 +24,7 @@ from . import build as _build
 __all__ = [
     "KameraError", "Rope", "ChunkSpec", "load_library", "pack_chunks",
     "kamera_relocate_patch", "kamera_slide_inplace", "kamera_mla_relocate_patch",
-    "kamera_ingest_canonical", "kamera_mla_ingest_canonical", "kamera_form_patch",
+    "kamera_ingest_canonical", "kamera_mla_ingest_canonical", "kamera_form_patch", "kamera_attend_reused",
     "kamera_validate_chunks", "kamera_status_string", "kamera_abi_version",
     "ROTATE_HALF", "INTERLEAVED", "DEVERR",
 ]
@@ -92,6 +92,17 @@ class _Deficit(C.Structure):
                 ("reserved", C.c_int32)]
 
 
+class _AttnKV(C.Structure):
+    _fields_ = [("k", C.c_void_p), ("v", C.c_void_p), ("num_rows", C.c_int64), ("row_stride", C.c_int64),
+                ("num_kv_heads", C.c_int32), ("head_dim", C.c_int32), ("layer", C.c_int32),
+                ("reserved", C.c_int32)]
+
+
+class _AttnQuery(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("out", C.c_void_p), ("n_seqs", C.c_int32), ("num_q_heads", C.c_int32),
+                ("scale", C.c_float), ("reserved", C.c_int32)]
+
+
 class _MlaStore(C.Structure):
     _fields_ = [("kv", C.c_void_p), ("num_rows", C.c_int64), ("layer_stride", C.c_int64),
                 ("row_stride", C.c_int64)]
@@ -133,6 +144,9 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C
     lib.kamera_form_patch.restype = C.c_int
     lib.kamera_form_patch.argtypes = [P(_Deficit), C.c_int32, C.c_void_p, C.c_void_p, C.c_void_p, C.c_void_p,
                                       C.c_void_p]
+    lib.kamera_attend_reused.restype = C.c_int
+    lib.kamera_attend_reused.argtypes = [P(_AttnKV), P(_AttnQuery), P(_Rope), C.c_void_p, C.c_void_p, C.c_int32,
+                                         C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
     lib.kamera_validate_chunks.restype = C.c_int
     lib.kamera_validate_chunks.argtypes = [P(_Chunk), C.c_int32, C.c_int64, C.c_int64, C.c_int32,
                                            C.c_int32, P(C.c_int32), P(C.c_int32)]
@@ -152,7 +166,7 @@ def kamera_status_string(status: int) -> str:
     return load_library().kamera_status_string(int(status)).decode()
 
 
-ABI_VERSION = 4   # the KAMERA_ABI_VERSION these bindings marshal for
+ABI_VERSION = 5   # the KAMERA_ABI_VERSION these bindings marshal for
 
 
 def kamera_abi_version() -> int:
@@ -457,3 +471,42 @@ def kamera_form_patch(delta: torch.Tensor, m: int, u: Optional[torch.Tensor] = N
                                           _stream_handle(stream))
     _check(rc, "kamera_form_patch")
     return u, v
+
+
+def kamera_attend_reused(store_k: torch.Tensor, store_v: torch.Tensor, q: torch.Tensor, rope: Rope,
+                         chunks: torch.Tensor, seq_start: torch.Tensor, n_chunks: int, max_len: int,
+                         max_rank: int, layer: int = 0, scale: Optional[float] = None,
+                         out: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None,
+                         stream=None) -> torch.Tensor:
+    """Decode attention of one query token per sequence over its reused chunks,
+    never writing a relocated row (see ``kamera_attend_reused`` in kamera.h).
+
+    store_k/v: bf16 ``[N, H_kv, d]`` (one layer; packed heads, any row stride);
+    q: bf16 ``[S, H_q, d]`` contiguous; seq_start: device int32 ``[S + 1]``;
+    chunks: packed descriptors; layer: the factors' layer index; scale:
+    default 1/sqrt(d).  Returns ``out`` (bf16 ``[S, H_q, d]``)."""
+    for t, nm in ((store_k, "store_k"), (store_v, "store_v"), (q, "q")):
+        _bf16(t, nm)
+    if store_k.dim() != 3 or store_k.stride(2) != 1 or store_k.stride(1) != store_k.shape[2]:
+        raise ValueError("store_k must be [N, H_kv, d] with packed heads")
+    if store_v.shape != store_k.shape or store_v.stride() != store_k.stride():
+        raise ValueError("store_k and store_v must share shape and strides")
+    N, H, d = store_k.shape
+    if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous():
+        raise ValueError("q must be a contiguous [S, H_q, d] tensor")
+    S, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if seq_start.dtype != torch.int32 or seq_start.numel() != S + 1:
+        raise ValueError("seq_start must hold S + 1 int32 values")
+    kv = _AttnKV(_addr(store_k), _addr(store_v), N, store_k.stride(0), H, d, int(layer), 0)
+    qq = _AttnQuery(_addr(q), _addr(out), S, Hq, float(d ** -0.5 if scale is None else scale), 0)
+    r, keep = rope._c()
+    rc = load_library().kamera_attend_reused(C.byref(kv), C.byref(qq), C.byref(r), _addr(chunks), _addr(seq_start),
+                                             int(n_chunks), int(max_len), int(max_rank), _addr(err),
+                                             _stream_handle(stream))
+    del keep
+    _check(rc, "kamera_attend_reused")
+    return out

@@ -91,6 +91,25 @@ struct PatchFormParams {
     int32_t* err;
 };
 
+// Decode attention over reused chunks: one layer's canonical store, sequences
+// of chunks, one query token per sequence.
+struct AttendParams {
+    const __nv_bfloat16* k;        // canonical keys / values of one layer: rows of H x d,
+    const __nv_bfloat16* v;        // row_stride elements apart
+    int64_t row_stride, num_rows;
+    int32_t H, d, G, layer;        // KV heads, head dim, query heads per KV head, factor layer
+    const KameraChunk* chunks;
+    const int32_t* seq_start;      // [n_seqs + 1]: sequence s = chunks seq_start[s] .. seq_start[s+1]-1
+    int32_t n_seqs, n_chunks;
+    const __nv_bfloat16* q;        // [n_seqs][H * G][d]
+    __nv_bfloat16* out;            // [n_seqs][H * G][d]
+    float scale;
+    int32_t max_len, max_rank;
+    int32_t cluster;               // CTAs per (sequence, KV head), 1..8
+    int32_t* err;
+    RopeParams rope;
+};
+
 // ------------------------------------------------------------------ bf16 --
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

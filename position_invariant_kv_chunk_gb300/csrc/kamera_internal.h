@@ -27,12 +27,18 @@ cudaError_t launch_slide(const RowsParams& p, cudaStream_t stream);
 struct IngestPass;
 struct IngestParams;
 struct PatchFormParams;
+struct AttendParams;
 int ingest_passes(const RowsParams& rp, bool values, IngestPass* out);
 cudaError_t launch_ingest(const IngestParams& p, cudaStream_t stream);
 
 // Patch formation: whether a block shape is handled; one CTA per block.
 bool patch_form_supported(int cols, int m);
 cudaError_t launch_patch_form(const PatchFormParams& p, int64_t n_blocks, cudaStream_t stream);
+
+// Decode attention over reused chunks: shapes handled; one CTA per (sequence, KV head).
+bool attend_supported(int head_dim, int G, int max_rank);
+int attend_cluster(int64_t units);
+cudaError_t launch_attend(const AttendParams& p, cudaStream_t stream);
 
 // Tensor-core path (tcgen05 MMA for the rank-m patch; relocation with rank > 0).
 bool umma_supported(const RowsParams& p, int family);

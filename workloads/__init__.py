@@ -315,6 +315,96 @@ def dsv2_patch_form() -> DeficitSpec:
 FORMATION = {"qwen_patch_form": qwen_patch_form, "dsv2_patch_form": dsv2_patch_form}
 
 
+# ------------------------------------------------------ attention inputs --
+@dataclass(frozen=True)
+class AttendSpec:
+    """Decode attention over reused chunks: ``seqs`` lists each sequence's chunk
+    lengths; every chunk has its own canonical rows in one layer's store
+    (K, V ~ N(0, 1)), a delta drawn from U{-dmax..dmax} and, when m > 0, factors
+    ~ N(0, 0.1^2) for ``L`` layers (read at ``layer``); one query token per
+    sequence and query head, N(0, 1)."""
+    name: str
+    H: int
+    G: int
+    d: int
+    seqs: tuple
+    m: int = 32
+    L: int = 2
+    layer: int = 1
+    base: float = 1e6
+    rot_dim: int = -1          # -1: the whole head
+    rot_offset: int = 0
+    pairing: int = ROTATE_HALF
+    dmax: int = 32768
+    zero_rank_every: int = 0   # > 0: every n-th chunk carries no patch
+    kind: str = "attend"
+
+
+@dataclass
+class AttendData:
+    spec: AttendSpec
+    store_k: torch.Tensor      # [N, H, d]
+    store_v: torch.Tensor
+    chunks: List["ChunkData"]
+    seq_start: List[int]
+    q: torch.Tensor            # [S, H * G, d]
+
+    @property
+    def rot_dim(self) -> int:
+        return self.spec.d if self.spec.rot_dim < 0 else self.spec.rot_dim
+
+
+def qwen_attend_reused() -> AttendSpec:
+    """A decode step over reused chunks, Qwen2.5-VL-7B shaped (4 KV heads, 28 query
+    heads, d = 128, base 1e6): 38 sequences, each the 8-chunk recall batch
+    (8 x 1296 tokens), rank 32 on K and V -- one CTA per (sequence, KV head),
+    152 in all."""
+    return AttendSpec("qwen_attend_reused", H=4, G=7, d=128, seqs=tuple((1296,) * 8 for _ in range(38)), m=32)
+
+
+def make_attend(spec: AttendSpec, device="cpu") -> AttendData:
+    rng = _np_rng("attend", spec.name, spec.H, spec.G, spec.d)
+    lens = [t for seq in spec.seqs for t in seq]
+    N = max(1, sum(lens))
+    gen = _gen(device, "attend", spec.name)
+    store_k = _randn_bf16((N, spec.H, spec.d), 1.0, gen, device)
+    store_v = _randn_bf16((N, spec.H, spec.d), 1.0, gen, device)
+    chunks, seq_start, off, idx = [], [0], 0, 0
+    for seq in spec.seqs:
+        for t in seq:
+            m = 0 if (spec.zero_rank_every and idx % spec.zero_rank_every == spec.zero_rank_every - 1) else spec.m
+            pat = []
+            if m > 0 and t > 0:
+                pat = [_randn_bf16((spec.L, spec.H, t, m), 0.1, gen, device),
+                       _randn_bf16((spec.L, spec.H, spec.d, m), 0.1, gen, device),
+                       _randn_bf16((spec.L, spec.H, t, m), 0.1, gen, device),
+                       _randn_bf16((spec.L, spec.H, spec.d, m), 0.1, gen, device)]
+            else:
+                m = 0
+            delta = int(rng.integers(-spec.dmax, spec.dmax + 1))
+            slots = torch.arange(max(t, 1), dtype=torch.int64, device=device)[:t]
+            chunks.append(ChunkData(off, t, delta, m, slots, pat))
+            off += t
+            idx += 1
+        seq_start.append(len(chunks))
+    q = _randn_bf16((len(spec.seqs), spec.H * spec.G, spec.d), 1.0, gen, device)
+    return AttendData(spec, store_k, store_v, chunks, seq_start, q)
+
+
+def attend_bytes(spec: AttendSpec) -> int:
+    """Bytes a decode step must move: each token's canonical K and V rows of each
+    KV head, its U rows (2m per head), each patched chunk's V factors (2 d m per
+    head), the queries read and the outputs written."""
+    B = 2
+    tok = sum(t for seq in spec.seqs for t in seq)
+    nch = sum(1 for seq in spec.seqs for t in seq if t > 0)
+    q = len(spec.seqs) * spec.H * spec.G * spec.d * B
+    return tok * spec.H * (2 * spec.d + 2 * spec.m) * B + nch * spec.H * 2 * spec.d * spec.m * B + 2 * q
+
+
+ATTENTION = {"qwen_attend_reused": qwen_attend_reused}
+
+
 # ------------------------------------------------------------- workloads --
 @dataclass
 class ChunkData:
