@@ -1,0 +1,83 @@
+"""Planted mistakes in the oracle's numpy functions must fail a pin.
+
+``test_oracle_mutants.py`` plants mistakes in the C source; the attention and
+patch-formation oracles are numpy code in ``oracle/__init__.py``.  Each mutant
+here is a one-line textual change to the source of ``Oracle.attend`` or
+``form_patch`` (a dropped term, a flipped sign, a wrong head, a missing scale,
+the wrong end of the spectrum), compiled into a stand-in and run through the
+pins of that function; it passes the test only by failing one of them.
+"""
+import inspect
+import textwrap
+import types
+
+import numpy as np
+import pytest
+
+import oracle as O
+from tests import oracle_pins as P
+
+ATTEND_MUTANTS = {
+    "value_patch_dropped": ("vv = vv + uv @ vvm.T", "vv = vv"),
+    "key_patch_dropped": ("kk = kk + uk @ vk.T", "kk = kk"),
+    "delta_sign": ("self.rotate(kf[rows, g, :], c.delta,", "self.rotate(kf[rows, g, :], -c.delta,"),
+    "scale_dropped": ("sc = scale * (K @ qf[s, h])", "sc = K @ qf[s, h]"),
+    "wrong_kv_head": ("for h in range(g * G, (g + 1) * G):", "for h in range(g, Hq, H):"),
+    "softmax_not_normalised": ("pr = w / w.sum()", "pr = w"),
+}
+
+FORM_PATCH_MUTANTS = {
+    "sigma_dropped": ("return w[:, :m] * s[:m], zt[:m, :].T.copy()", "return w[:, :m], zt[:m, :].T.copy()"),
+    "smallest_directions": ("return w[:, :m] * s[:m], zt[:m, :].T.copy()",
+                            "return w[:, -m:] * s[-m:], zt[-m:, :].T.copy()"),
+    "v_from_left_vectors": ("return w[:, :m] * s[:m], zt[:m, :].T.copy()",
+                            "return zt[:m, :].T.copy() * s[:m], w[:, :m]"),
+}
+
+ATTEND_PINS = [P.pin_attend_single_token, P.pin_attend_uniform_keys, P.pin_attend_fused_identity,
+               P.pin_attend_relative_position]
+FORM_PATCH_PINS = [P.pin_form_patch_full_rank, P.pin_eckart_young]
+
+
+def _mutated(fn, old, new, env):
+    src = textwrap.dedent(inspect.getsource(fn))
+    assert src.count(old) == 1, (fn.__name__, old)
+    ns = dict(env)
+    exec(compile(src.replace(old, new), f"<mutant {fn.__name__}>", "exec"), ns)
+    return ns[fn.__name__]
+
+
+def _fails_some(pins, orc):
+    for pin in pins:
+        try:
+            pin(orc)
+        except (AssertionError, ValueError, IndexError):
+            return True
+    return False
+
+
+@pytest.fixture(scope="module")
+def orc():
+    return O.default()
+
+
+def test_unmutated_functions_pass(orc):
+    for pin in ATTEND_PINS + FORM_PATCH_PINS:
+        pin(orc)
+
+
+@pytest.mark.parametrize("name", list(ATTEND_MUTANTS))
+def test_attend_mutant_is_caught(name, orc):
+    old, new = ATTEND_MUTANTS[name]
+    fn = _mutated(O.Oracle.attend, old, new, vars(O))
+    mut = O.Oracle()
+    mut.attend = types.MethodType(fn, mut)
+    assert _fails_some(ATTEND_PINS, mut), f"attend mutant {name} passed every pin"
+
+
+@pytest.mark.parametrize("name", list(FORM_PATCH_MUTANTS))
+def test_form_patch_mutant_is_caught(name, orc, monkeypatch):
+    old, new = FORM_PATCH_MUTANTS[name]
+    fn = _mutated(O.form_patch, old, new, vars(O))
+    monkeypatch.setattr(O, "form_patch", fn)
+    assert _fails_some(FORM_PATCH_PINS, orc), f"form_patch mutant {name} passed every pin"
