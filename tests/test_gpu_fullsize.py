@@ -158,3 +158,73 @@ def test_slide_fullsize_sampled():
                 got.append(after[a, h]); want.append(b); scale.append(s)
     _check_rows(got, want, scale, "qwen_slide (sampled)")
     assert np.array_equal(_u16(wl.pool_k[:, ev]), ev_before), "evicted slots changed"
+
+
+# ----------------------------------------------------- the NEXT rows, full size
+def test_patch_form_fullsize_sampled():
+    """qwen_patch_form as bench.py times it (224 blocks of 1296 x 128, rank 32, one
+    call): a seeded sample of blocks against the oracle's truncated SVD, the rest
+    checked for V^T V = I."""
+    from tests.test_gpu_patchform import check_factors
+    spec = W.qwen_patch_form()
+    x = W.make_deficit(spec, DEV)
+    xb = x.reshape(spec.kv * spec.L, spec.length, spec.H, spec.d).permute(0, 2, 1, 3)
+    sig = torch.empty(spec.kv * spec.L, spec.H, spec.m, dtype=torch.float32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    u, v = K.kamera_form_patch(xb, spec.m, sigma=sig, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    vt = v.float()
+    gram = torch.einsum("oicm,oicn->oimn", vt, vt)
+    assert float((gram - torch.eye(spec.m, device=DEV)).abs().max()) <= 8e-3
+    rng = np.random.default_rng(21)
+    for _ in range(12):
+        o, i = int(rng.integers(spec.kv * spec.L)), int(rng.integers(spec.H))
+        blk = xb[o, i].float().cpu().numpy().astype(np.float64)
+        check_factors(blk, u[o, i].float().cpu().numpy().astype(np.float64),
+                      v[o, i].float().cpu().numpy().astype(np.float64),
+                      sig[o, i].cpu().numpy().astype(np.float64), spec.m, f"block ({o},{i})")
+
+
+def test_wide_patch_form_fullsize_sampled():
+    """dsv2_patch_form (27 blocks of 4096 x 512, rank 16: the wide path), sampled blocks."""
+    from tests.test_gpu_patchform import check_factors
+    spec = W.dsv2_patch_form()
+    x = W.make_deficit(spec, DEV)
+    xb = x.reshape(spec.kv * spec.L, spec.length, spec.H, spec.d).permute(0, 2, 1, 3)
+    sig = torch.empty(spec.kv * spec.L, spec.H, spec.m, dtype=torch.float32, device=DEV)
+    u, v = K.kamera_form_patch(xb, spec.m, sigma=sig)
+    torch.cuda.synchronize()
+    for o in (0, 13, 26):
+        blk = xb[o, 0].float().cpu().numpy().astype(np.float64)
+        check_factors(blk, u[o, 0].float().cpu().numpy().astype(np.float64),
+                      v[o, 0].float().cpu().numpy().astype(np.float64),
+                      sig[o, 0].cpu().numpy().astype(np.float64), spec.m, f"block {o}")
+
+
+def test_attend_fullsize_sampled():
+    """qwen_attend_reused as bench.py times it (38 sequences x 8 chunks of 1296
+    tokens, one call): a seeded sample of sequences against the oracle."""
+    from tests.test_gpu_attend import _bits, _ulp_bf16
+    spec = W.qwen_attend_reused()
+    a = W.make_attend(spec, DEV)
+    chunks = K.pack_chunks(a.chunks, device=DEV)
+    seq = torch.tensor(a.seq_start, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = K.kamera_attend_reused(a.store_k, a.store_v, a.q, K.Rope(spec.base, spec.d), chunks, seq, len(a.chunks),
+                                 max(c.length for c in a.chunks), spec.m, layer=spec.layer, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    orc = O.default()
+    th = orc.inv_freq(spec.base, spec.d)
+    rng = np.random.default_rng(22)
+    for s in sorted(set(int(x) for x in rng.integers(0, len(spec.seqs), 3))):
+        cs = a.chunks[a.seq_start[s]:a.seq_start[s + 1]]
+        lo, hi = cs[0].src_offset, cs[-1].src_offset + cs[-1].length
+        oc = [O.Chunk(c.src_offset - lo, c.length, c.delta, c.rank, c.slots.cpu().numpy(),
+                      [_bits(t) for t in c.patches]) for c in cs]
+        _, ref, mag = orc.attend(_bits(a.store_k[lo:hi]), _bits(a.store_v[lo:hi]), oc, [0, len(cs)],
+                                 _bits(a.q[s:s + 1]), spec.layer, th, spec.d, scale=spec.d ** -0.5)
+        got = out[s:s + 1].float().cpu().numpy().astype(np.float64)
+        bad = np.abs(got - ref) > _ulp_bf16(ref) + 2.0 ** -16 * mag
+        assert not bad.any(), (s, int(bad.sum()))
