@@ -77,7 +77,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
-#define KAMERA_ABI_VERSION 5
+#define KAMERA_ABI_VERSION 6
 
 /* Limits of this build. */
 #define KAMERA_MAX_RANK 128          /* largest patch rank m */
@@ -147,17 +147,34 @@ typedef struct KameraChunk {
  *                      relative to the start of k_rope and rot_offset + rot_dim
  *                      <= rope_dim
  *   pairing            KAMERA_ROPE_ROTATE_HALF or KAMERA_ROPE_INTERLEAVED
- *   reserved           0
+ *   n_axes             0: every frequency turns by the chunk's delta.
+ *                      1..3: multi-axis RoPE (time, height, width), each
+ *                      frequency following one axis; frequency f of chunk c
+ *                      turns by d_axis_delta[c*n_axes + freq_axis[f]]; the
+ *                      descriptor's delta is then not used for the phases
+ *                      (it is still range-checked), and a chunk whose axis
+ *                      deltas are all 0 is copied, as delta = 0 is
  *   inv_freq_override  NULL, or a host array of rot_dim/2 fp64 frequencies
  *                      (e.g. a model's scaled table), read during the call
+ *   freq_axis          n_axes > 0: a host array of rot_dim/2 axis indices in
+ *                      [0, n_axes) (contiguous sections, e.g. 16/24/24 of 64
+ *                      frequencies, or interleaved), read during the call;
+ *                      NULL with n_axes = 0
+ *   d_axis_delta       n_axes > 0: a device array of n_chunks*n_axes int64
+ *                      position moves, 8-byte aligned, read by the kernels
+ *                      (|value| <= KAMERA_MAX_ABS_DELTA, else the chunk is
+ *                      skipped with KAMERA_DEVERR_DESCRIPTOR); NULL with
+ *                      n_axes = 0
  */
 typedef struct KameraRope {
     double base;
     int32_t rot_dim;
     int32_t rot_offset;
     int32_t pairing;
-    int32_t reserved;
+    int32_t n_axes;
     const double* inv_freq_override;
+    const uint8_t* freq_axis;
+    const int64_t* d_axis_delta;
 } KameraRope;
 
 /*

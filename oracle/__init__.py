@@ -362,7 +362,9 @@ class Oracle:
         factors ``[L, H_kv, len, m]`` / ``[L, H_kv, d, m]`` read at ``layer``.
         Returns (bf16 bits ``[S, H_q, d]``, fp64 output, magnitude scale
         sum_j p_j |V_j| per element).  ``q`` and the factors may also be given
-        as fp64 values (for the pins)."""
+        as fp64 values (for the pins).  ``inv_freq`` is one table, or one row
+        per chunk (chunks whose multi-axis moves differ: each chunk's phases
+        are its own per-frequency products delta_f * theta_f)."""
         N, H, d = store_k.shape
         S, Hq, _ = q.shape
         G = Hq // H
@@ -374,9 +376,11 @@ class Oracle:
         for s in range(S):
             for g in range(H):
                 Ks, Vs = [], []
-                for c in chunks[seq_starts[s]:seq_starts[s + 1]]:
+                for ci in range(seq_starts[s], seq_starts[s + 1]):
+                    c = chunks[ci]
+                    th = inv_freq[ci] if np.ndim(inv_freq) == 2 else inv_freq
                     rows = slice(c.src_offset, c.src_offset + c.length)
-                    kk = self.rotate(kf[rows, g, :], c.delta, inv_freq, rot_dim, rot_offset, pairing)
+                    kk = self.rotate(kf[rows, g, :], c.delta, th, rot_dim, rot_offset, pairing)
                     vv = vf[rows, g, :].copy()
                     if c.rank > 0:
                         uk, vk, uv, vvm = (f64(a)[layer, g] for a in c.patches)

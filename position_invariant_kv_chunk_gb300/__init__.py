@@ -58,8 +58,9 @@ class _Chunk(C.Structure):
 
 class _Rope(C.Structure):
     _fields_ = [("base", C.c_double), ("rot_dim", C.c_int32), ("rot_offset", C.c_int32),
-                ("pairing", C.c_int32), ("reserved", C.c_int32),
-                ("inv_freq_override", C.POINTER(C.c_double))]
+                ("pairing", C.c_int32), ("n_axes", C.c_int32),
+                ("inv_freq_override", C.POINTER(C.c_double)),
+                ("freq_axis", C.POINTER(C.c_uint8)), ("d_axis_delta", C.c_void_p)]
 
 
 class _GqaPool(C.Structure):
@@ -166,7 +167,7 @@ def kamera_status_string(status: int) -> str:
     return load_library().kamera_status_string(int(status)).decode()
 
 
-ABI_VERSION = 5   # the KAMERA_ABI_VERSION these bindings marshal for
+ABI_VERSION = 6   # the KAMERA_ABI_VERSION these bindings marshal for
 
 
 def kamera_abi_version() -> int:
@@ -177,21 +178,42 @@ def kamera_abi_version() -> int:
 @dataclass
 class Rope:
     """RoPE layout (see ``KameraRope``): theta_i = base^(-2i/rot_dim) unless
-    ``inv_freq`` is given."""
+    ``inv_freq`` is given.
+
+    Multi-axis RoPE: ``freq_axis`` gives, per frequency, the axis it follows
+    (0..n_axes-1) and ``axis_delta`` is a device int64 tensor [n_chunks, n_axes]
+    of each chunk's move along each axis; the chunks' own deltas are then not
+    used for the phases."""
     base: float
     rot_dim: int
     rot_offset: int = 0
     pairing: int = ROTATE_HALF
     inv_freq: Optional[Sequence[float]] = None
+    freq_axis: Optional[Sequence[int]] = None
+    axis_delta: Optional[torch.Tensor] = None
 
-    def _c(self):
-        keep = None
+    def _c(self, n_chunks: int = 0):
+        keep = []
         ptr = None
         if self.inv_freq is not None:
-            keep = np.ascontiguousarray(self.inv_freq, dtype=np.float64)
-            ptr = keep.ctypes.data_as(C.POINTER(C.c_double))
-        return _Rope(float(self.base), int(self.rot_dim), int(self.rot_offset), int(self.pairing), 0,
-                     ptr), keep
+            keep.append(np.ascontiguousarray(self.inv_freq, dtype=np.float64))
+            ptr = keep[-1].ctypes.data_as(C.POINTER(C.c_double))
+        n_axes, axes, dptr = 0, None, None
+        if self.axis_delta is not None:
+            if (self.freq_axis is None or self.axis_delta.dtype != torch.int64 or self.axis_delta.dim() != 2
+                    or not self.axis_delta.is_cuda):
+                raise ValueError("axis_delta needs freq_axis and a device int64 [n_chunks, n_axes] tensor")
+            if self.axis_delta.shape[0] < int(n_chunks) or len(self.freq_axis) != int(self.rot_dim) // 2:
+                raise ValueError("axis_delta needs a row per chunk and freq_axis an entry per frequency")
+            n_axes = int(self.axis_delta.shape[1])
+            keep.append(self.axis_delta.contiguous())
+            dptr = keep[-1].data_ptr()
+            keep.append(np.ascontiguousarray(self.freq_axis, dtype=np.uint8))
+            axes = keep[-1].ctypes.data_as(C.POINTER(C.c_uint8))
+        elif self.freq_axis is not None:
+            raise ValueError("freq_axis without axis_delta")
+        return _Rope(float(self.base), int(self.rot_dim), int(self.rot_offset), int(self.pairing), n_axes,
+                     ptr, axes, dptr), keep
 
 
 @dataclass
@@ -296,7 +318,7 @@ def kamera_relocate_patch(pool_k: torch.Tensor, pool_v: torch.Tensor, store_k: t
     if store_k.shape[0] != L or store_k.shape[2] != H or store_k.shape[3] != d:
         raise ValueError("store and pool disagree on L, H or d")
     store = _GqaStore(_addr(store_k), _addr(store_v), store_k.shape[1], store_k.stride(0), store_k.stride(1))
-    r, keep = rope._c()
+    r, keep = rope._c(n_chunks)
     rc = load_library().kamera_relocate_patch(C.byref(pool), C.byref(store), C.byref(r), _addr(chunks),
                                               _host_copy(chunks, host_chunks), int(n_chunks), int(max_len),
                                               int(max_rank), _addr(err), _stream_handle(stream))
@@ -315,7 +337,7 @@ def kamera_slide_inplace(pool_k: torch.Tensor, rope: Rope, chunks: torch.Tensor,
         raise ValueError("pool_k must be [L, S, H, d] with packed heads")
     L, S, H, d = pool_k.shape
     pool = _SlidePool(L, H, d, 0, _addr(pool_k), S, pool_k.stride(0), pool_k.stride(1))
-    r, keep = rope._c()
+    r, keep = rope._c(n_chunks)
     rc = load_library().kamera_slide_inplace(C.byref(pool), C.byref(r), _addr(chunks), int(n_chunks),
                                              int(max_len), _addr(err), _stream_handle(stream))
     del keep
@@ -338,7 +360,7 @@ def kamera_mla_relocate_patch(pool: torch.Tensor, store: torch.Tensor, kv_lora: 
         raise ValueError("store and pool disagree on L or row width")
     p = _MlaPool(L, int(kv_lora), W - int(kv_lora), 0, _addr(pool), S, pool.stride(0), pool.stride(1))
     s = _MlaStore(_addr(store), store.shape[1], store.stride(0), store.stride(1))
-    r, keep = rope._c()
+    r, keep = rope._c(n_chunks)
     rc = load_library().kamera_mla_relocate_patch(C.byref(p), C.byref(s), C.byref(r), _addr(chunks),
                                                   _host_copy(chunks, host_chunks), int(n_chunks), int(max_len),
                                                   int(max_rank), _addr(err), _stream_handle(stream))
@@ -367,7 +389,7 @@ def kamera_ingest_canonical(pool_k: torch.Tensor, pool_v: torch.Tensor, store_k:
         raise ValueError("store and pool disagree on L, H or d")
     pool = _GqaPool(L, H, d, 0, _addr(pool_k), _addr(pool_v), S, pool_k.stride(0), pool_k.stride(1))
     store = _GqaStore(_addr(store_k), _addr(store_v), store_k.shape[1], store_k.stride(0), store_k.stride(1))
-    r, keep = rope._c()
+    r, keep = rope._c(n_chunks)
     rc = load_library().kamera_ingest_canonical(C.byref(pool), C.byref(store), C.byref(r), _addr(chunks),
                                                 int(n_chunks), int(max_len), _addr(err), _stream_handle(stream))
     del keep
@@ -390,7 +412,7 @@ def kamera_mla_ingest_canonical(pool: torch.Tensor, store: torch.Tensor, kv_lora
         raise ValueError("store and pool disagree on L or row width")
     p = _MlaPool(L, int(kv_lora), Wd - int(kv_lora), 0, _addr(pool), S, pool.stride(0), pool.stride(1))
     s = _MlaStore(_addr(store), store.shape[1], store.stride(0), store.stride(1))
-    r, keep = rope._c()
+    r, keep = rope._c(n_chunks)
     rc = load_library().kamera_mla_ingest_canonical(C.byref(p), C.byref(s), C.byref(r), _addr(chunks),
                                                     int(n_chunks), int(max_len), _addr(err),
                                                     _stream_handle(stream))
@@ -503,7 +525,7 @@ def kamera_attend_reused(store_k: torch.Tensor, store_v: torch.Tensor, q: torch.
         raise ValueError("seq_start must hold S + 1 int32 values")
     kv = _AttnKV(_addr(store_k), _addr(store_v), N, store_k.stride(0), H, d, int(layer), 0)
     qq = _AttnQuery(_addr(q), _addr(out), S, Hq, float(d ** -0.5 if scale is None else scale), 0)
-    r, keep = rope._c()
+    r, keep = rope._c(n_chunks)
     rc = load_library().kamera_attend_reused(C.byref(kv), C.byref(qq), C.byref(r), _addr(chunks), _addr(seq_start),
                                              int(n_chunks), int(max_len), int(max_rank), _addr(err),
                                              _stream_handle(stream))

@@ -41,7 +41,12 @@ bool overlap(std::pair<uintptr_t, uintptr_t> a, std::pair<uintptr_t, uintptr_t> 
 // caller's table.  `width` is the extent the rotary range must fit in.
 int fill_rope(const KameraRope* r, int width, RopeParams* out)
 {
-    if (!r || r->reserved != 0)
+    if (!r || r->n_axes < 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (r->n_axes > 3)
+        return KAMERA_ERR_UNSUPPORTED;
+    if (r->n_axes == 0 ? (r->freq_axis || r->d_axis_delta)
+                       : (!r->freq_axis || !r->d_axis_delta || (reinterpret_cast<uintptr_t>(r->d_axis_delta) & 7)))
         return KAMERA_ERR_INVALID_ARGUMENT;
     if (r->rot_dim < 0 || (r->rot_dim & 1) || r->rot_offset < 0)
         return KAMERA_ERR_INVALID_ARGUMENT;
@@ -76,7 +81,14 @@ int fill_rope(const KameraRope* r, int width, RopeParams* out)
         if (!std::isfinite(t))
             return KAMERA_ERR_INVALID_ARGUMENT;
         out->inv_freq[i] = t;
+        if (r->n_axes > 0) {
+            if (r->freq_axis[i] >= r->n_axes)
+                return KAMERA_ERR_INVALID_ARGUMENT;
+            out->axis[i] = r->freq_axis[i];
+        }
     }
+    out->n_axes = r->n_axes;
+    out->axis_delta = r->d_axis_delta;
     return KAMERA_OK;
 }
 

@@ -74,9 +74,9 @@ __device__ __forceinline__ float at_warp_sum(float v)
 __device__ __forceinline__ float f2_lo(uint64_t x) { return __uint_as_float((uint32_t)x); }
 __device__ __forceinline__ float f2_hi(uint64_t x) { return __uint_as_float((uint32_t)(x >> 32)); }
 
-__device__ __forceinline__ int32_t attend_check(const KameraChunk& ch, const AttendParams& p)
+__device__ __forceinline__ int32_t attend_check(const KameraChunk& ch, int c, const AttendParams& p)
 {
-    int32_t bits = 0;
+    int32_t bits = check_axis_delta(p.rope, c);
     if (ch.len < 0 || ch.rank < 0 || ch.delta > KAMERA_MAX_ABS_DELTA || ch.delta < -KAMERA_MAX_ABS_DELTA)
         bits |= KAMERA_DEVERR_DESCRIPTOR;
     if (ch.src_offset < 0 || ch.src_offset + (int64_t)max(ch.len, 0) > p.num_rows)
@@ -158,7 +158,7 @@ __global__ void __launch_bounds__(kAtThreads, MAXM <= 32 ? 2 : 1) attend_kernel(
 
     for (int c = c0; c < c1; c += CL) {
         const KameraChunk ch = p.chunks[c];
-        const int32_t bad = attend_check(ch, p);
+        const int32_t bad = attend_check(ch, c, p);
         if (bad) {
             if (threadIdx.x == 0)
                 raise_err(p.err, bad);
@@ -171,7 +171,7 @@ __global__ void __launch_bounds__(kAtThreads, MAXM <= 32 ? 2 : 1) attend_kernel(
         __syncthreads();   // the previous chunk is done with every shared array
         for (int f = threadIdx.x; f < rp.n_freq; f += kAtThreads) {
             float cc, sn;
-            phase_cos_sin(-ch.delta, rp.inv_freq[f], cc, sn);
+            phase_cos_sin(-freq_delta(rp, ch, c, f), rp.inv_freq[f], cc, sn);
             s.cs[f] = make_float2(cc, sn);
         }
         __nv_bfloat16* vks = &s.kt[1][0][0];   // V_k staged in the second key buffer

@@ -21,6 +21,9 @@ struct RopeParams {
     int32_t pairing;       // KAMERA_ROPE_*
     int32_t n_freq;        // rot_dim / 2
     double inv_freq[KAMERA_MAX_ROT_DIM / 2];
+    const int64_t* axis_delta;              // multi-axis RoPE: [n_chunks][n_axes], else null
+    int32_t n_axes;                         // 0: every frequency turns by the chunk's delta
+    uint8_t axis[KAMERA_MAX_ROT_DIM / 2];   // frequency f follows axis[f] (n_axes > 0)
 };
 
 // A family-neutral description of one call: token rows are read from `src`
@@ -159,6 +162,36 @@ __device__ __forceinline__ void phase_cos_sin(int64_t delta, double theta, float
     sincosf((float)red, &s, &c);
 }
 
+// Multi-axis RoPE: frequency f of chunk c turns by that chunk's move along the
+// axis f follows; without axes, by the descriptor's delta.
+__device__ __forceinline__ int64_t freq_delta(const RopeParams& r, const KameraChunk& ch, int c, int f)
+{
+    return r.n_axes == 0 ? ch.delta : r.axis_delta[(int64_t)c * r.n_axes + r.axis[f]];
+}
+
+// Whether chunk c turns at all (a chunk that does not is copied bit for bit).
+__device__ __forceinline__ bool chunk_turns(const RopeParams& r, const KameraChunk& ch, int c)
+{
+    if (r.n_axes == 0)
+        return ch.delta != 0;
+    bool any = false;
+    for (int a = 0; a < r.n_axes; ++a)
+        any |= r.axis_delta[(int64_t)c * r.n_axes + a] != 0;
+    return any;
+}
+
+// KAMERA_DEVERR_DESCRIPTOR when one of chunk c's axis moves is out of range.
+__device__ __forceinline__ int32_t check_axis_delta(const RopeParams& r, int c)
+{
+    int32_t bits = 0;
+    for (int a = 0; a < r.n_axes; ++a) {
+        const int64_t v = r.axis_delta[(int64_t)c * r.n_axes + a];
+        if (v > KAMERA_MAX_ABS_DELTA || v < -KAMERA_MAX_ABS_DELTA)
+            bits |= KAMERA_DEVERR_DESCRIPTOR;
+    }
+    return bits;
+}
+
 // patch_ptrs[i] without dynamic indexing (keeps a descriptor in registers)
 __device__ __forceinline__ const __nv_bfloat16* patch_ptr(const KameraChunk& ch, int i)
 {
@@ -176,9 +209,9 @@ __device__ __forceinline__ void raise_err(int32_t* err, int32_t bits)
 // Checks one descriptor against the call; returns 0 when the chunk may run,
 // else the KAMERA_DEVERR_* bits (the chunk is then skipped whole).
 // in_place: the slide (src_offset ignored, rank must be 0).
-__device__ __forceinline__ int32_t check_chunk(const KameraChunk& ch, const RowsParams& p, bool in_place)
+__device__ __forceinline__ int32_t check_chunk(const KameraChunk& ch, int c, const RowsParams& p, bool in_place)
 {
-    int32_t bits = 0;
+    int32_t bits = check_axis_delta(p.rope, c);
     if (ch.len < 0 || ch.rank < 0 || ch.delta > KAMERA_MAX_ABS_DELTA || ch.delta < -KAMERA_MAX_ABS_DELTA)
         bits |= KAMERA_DEVERR_DESCRIPTOR;
     if (ch.len > 0 && (ch.dst_slot_mapping == nullptr || (reinterpret_cast<uintptr_t>(ch.dst_slot_mapping) & 15)))

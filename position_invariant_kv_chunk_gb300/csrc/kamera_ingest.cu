@@ -137,7 +137,7 @@ __global__ void __launch_bounds__(kIngestThreads, 2) ingest_kernel(const __grid_
     __shared__ int64_t slots[kIngestTile];
     const int chunk = blockIdx.x / tiles_per_chunk, tile = blockIdx.x - chunk * tiles_per_chunk;
     const KameraChunk ch = p.chunks[chunk];
-    int32_t bad = 0;
+    int32_t bad = check_axis_delta(p.rope, chunk);
     if (ch.len < 0 || ch.rank != 0 || ch.delta > KAMERA_MAX_ABS_DELTA || ch.delta < -KAMERA_MAX_ABS_DELTA ||
         (ch.len > 0 && (ch.dst_slot_mapping == nullptr || (reinterpret_cast<uintptr_t>(ch.dst_slot_mapping) & 15))))
         bad |= KAMERA_DEVERR_DESCRIPTOR;
@@ -154,11 +154,11 @@ __global__ void __launch_bounds__(kIngestThreads, 2) ingest_kernel(const __grid_
     if (t0 >= ch.len)
         return;
     const int ntok = min(kIngestTile, ch.len - t0);
-    const bool turn = ch.delta != 0;
+    const bool turn = chunk_turns(p.rope, ch, chunk);
     if (KIND != INGEST_COPY && turn)
         for (int f = threadIdx.x; f < p.rope.n_freq; f += kIngestThreads) {
             float c, s;
-            phase_cos_sin(ch.delta, p.rope.inv_freq[f], c, s);
+            phase_cos_sin(freq_delta(p.rope, ch, chunk, f), p.rope.inv_freq[f], c, s);
             cs[f] = make_float2(c, s);
         }
     for (int j = threadIdx.x; j < ntok; j += kIngestThreads) {

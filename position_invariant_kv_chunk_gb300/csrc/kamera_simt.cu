@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(256) rows_simt_kernel(const __grid_constant__ 
     const KameraChunk ch = p.chunks[chunk];
     const bool in_place = kFamily == FAMILY_SLIDE;
 
-    const int32_t bad = check_chunk(ch, p, in_place);
+    const int32_t bad = check_chunk(ch, chunk, p, in_place);
     if (bad) {
         if (tile == 0 && l == 0 && blockIdx.z == 0 && threadIdx.x == 0)
             raise_err(p.err, bad);
@@ -139,7 +139,7 @@ __global__ void __launch_bounds__(256) rows_simt_kernel(const __grid_constant__ 
     const int ntok = min(tile_tokens, ch.len - t0);
     const Segment sg = decode_segment(p, kFamily, blockIdx.z);
     const int m = ch.rank;
-    const bool rotate = sg.rot_dim > 0 && ch.delta != 0;
+    const bool rotate = sg.rot_dim > 0 && chunk_turns(p.rope, ch, chunk);
     const int half = sg.rot_dim / 2;
 
     // shared memory: cos/sin table, V_m^T (fp32 [m][w]), U tile (fp32 [ntok][m])
@@ -150,7 +150,7 @@ __global__ void __launch_bounds__(256) rows_simt_kernel(const __grid_constant__ 
     if (rotate)
         for (int i = threadIdx.x; i < half; i += blockDim.x) {
             float c, s;
-            phase_cos_sin(ch.delta, p.rope.inv_freq[i], c, s);
+            phase_cos_sin(freq_delta(p.rope, ch, chunk, i), p.rope.inv_freq[i], c, s);
             cs[i] = make_float2(c, s);
         }
     if (m > 0) {

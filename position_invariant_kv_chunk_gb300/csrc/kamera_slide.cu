@@ -37,19 +37,19 @@ __global__ void __launch_bounds__(kSlideThreads) slide_kernel(const __grid_const
     __shared__ int64_t slots[kSlideTile];
     const int chunk = blockIdx.x / tiles_per_chunk, tile = blockIdx.x - chunk * tiles_per_chunk;
     const KameraChunk ch = p.chunks[chunk];
-    const int32_t bad = check_chunk(ch, p, true);
+    const int32_t bad = check_chunk(ch, chunk, p, true);
     if (bad) {
         if (tile == 0 && blockIdx.y == 0 && threadIdx.x == 0)
             raise_err(p.err, bad);
         return;
     }
     const int t0 = tile * kSlideTile;
-    if (t0 >= ch.len || ch.delta == 0)
+    if (t0 >= ch.len || !chunk_turns(p.rope, ch, chunk))
         return;
     const int ntok = min(kSlideTile, ch.len - t0);
     for (int f = threadIdx.x; f < p.rope.n_freq; f += kSlideThreads) {
         float c, s;
-        phase_cos_sin(ch.delta, p.rope.inv_freq[f], c, s);
+        phase_cos_sin(freq_delta(p.rope, ch, chunk, f), p.rope.inv_freq[f], c, s);
         cs[f] = make_float2(c, s);
     }
     for (int j = threadIdx.x; j < ntok; j += kSlideThreads) {

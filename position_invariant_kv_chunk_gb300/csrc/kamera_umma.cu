@@ -155,9 +155,9 @@ __device__ __forceinline__ Seg segment(const UmmaParams& p, int z)
     return s;
 }
 
-__device__ __forceinline__ int chunk_tiles(const KameraChunk& ch, const RowsParams& r)
+__device__ __forceinline__ int chunk_tiles(const KameraChunk& ch, int c, const RowsParams& r)
 {
-    return check_chunk(ch, r, false) ? 0 : (ch.len + kTileM - 1) / kTileM;
+    return check_chunk(ch, c, r, false) ? 0 : (ch.len + kTileM - 1) / kTileM;
 }
 
 // Walks the CTA's tiles in (layer, chunk, segment, tile) order; every role
@@ -169,7 +169,7 @@ struct Cursor {
     __device__ void load(const UmmaParams& p)
     {
         ch = p.r.chunks[c];
-        ntile = chunk_tiles(ch, p.r);
+        ntile = chunk_tiles(ch, c, p.r);
     }
     __device__ void next(const UmmaParams& p)
     {
@@ -492,7 +492,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
 #pragma unroll 4
     for (int c = c_lo; c < c_hi; ++c) {
         const KameraChunk ch = r.chunks[c];
-        const int32_t bad = check_chunk(ch, r, false);
+        const int32_t bad = check_chunk(ch, c, r, false);
         if (bad) {
             if (blockIdx.x == 0)
                 raise_err(r.err, bad);
@@ -527,7 +527,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             int64_t acc = lo;
             for (int c = c_lo; c < c_hi; ++c) {
                 const KameraChunk ch = r.chunks[c];
-                const int nt = chunk_tiles(ch, r);
+                const int nt = chunk_tiles(ch, c, r);
                 if (rem < acc + (int64_t)p.Z * nt) {
                     const int64_t o = rem - acc;
                     sh.start_lz += (int32_t)(o / nt);
@@ -573,13 +573,13 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             const KameraChunk& ch = cur.ch;
             const int tok0 = cur.t * kTileM;
             const int ntok = min(kTileM, ch.len - tok0);
-            const bool rot = sg.rot && ch.delta != 0;
+            const bool rot = sg.rot && chunk_turns(r.rope, ch, cur.c);
             if (rot && sh.stage_tag[s] != cur.c) {   // cos/sin table in the epilogue's operand order
                 float* tab = reinterpret_cast<float*>(gbase + s * kStageBytes + kTabOff);
                 const bool half_pairs = r.rope.pairing == KAMERA_ROPE_ROTATE_HALF;
                 for (int f = lane; f < r.rope.n_freq; f += 32) {
                     float c_, s_;
-                    phase_cos_sin(ch.delta, r.rope.inv_freq[f], c_, s_);
+                    phase_cos_sin(freq_delta(r.rope, ch, cur.c, f), r.rope.inv_freq[f], c_, s_);
                     if (half_pairs) {
                         tab[f] = c_;
                         tab[64 + f] = s_;

@@ -17,6 +17,7 @@ head) block; bit-exact for copies and indexing):
 """
 from __future__ import annotations
 
+import copy
 from dataclasses import dataclass
 
 import numpy as np
@@ -81,9 +82,12 @@ def compare(gpu: np.ndarray, ref: np.ndarray, scale: np.ndarray, block_axes=None
 
 # ------------------------------------------------------------- execution
 def rope_of(wl: W.Workload) -> K.Rope:
-    if wl.kind in ("mla", "mla_ingest"):   # the ABI's MLA rotary range is relative to k_rope
-        return K.Rope(wl.base, wl.rot_dim, 0, wl.pairing, inv_freq=wl.inv_freq)
-    return K.Rope(wl.base, wl.rot_dim, wl.rot_offset, wl.pairing, inv_freq=wl.inv_freq)
+    axes = {}
+    if wl.axis_delta is not None:
+        axes = dict(freq_axis=wl.freq_axis,
+                    axis_delta=torch.as_tensor(wl.axis_delta, dtype=torch.int64, device=wl.pool_k.device))
+    off = 0 if wl.kind in ("mla", "mla_ingest") else wl.rot_offset   # the ABI's MLA range is relative to k_rope
+    return K.Rope(wl.base, wl.rot_dim, off, wl.pairing, inv_freq=wl.inv_freq, **axes)
 
 
 def theta_of(wl: W.Workload, orc: O.Oracle) -> np.ndarray:
@@ -156,9 +160,38 @@ def snapshot(wl: W.Workload) -> HostCopy:
     return h
 
 
+def axis_tables(wl: W.Workload, th: np.ndarray):
+    """Multi-axis RoPE, chunk by chunk: frequency f of chunk c turns by the
+    chunk's move along f's axis, which is R(1) over the table
+    theta'_f = move_c[axis_f] * theta_f (the same fp64 products, so the same
+    phases).  Returns (per-chunk tables, the delta each chunk then takes: 1,
+    or 0 for a chunk that does not move)."""
+    moves = np.asarray(wl.axis_delta, dtype=np.int64)
+    axis = np.asarray(wl.freq_axis, dtype=np.int64)
+    tabs = [moves[c][axis].astype(np.float64) * th for c in range(len(moves))]
+    return tabs, [1 if np.any(moves[c] != 0) else 0 for c in range(len(moves))]
+
+
 def run_oracle(wl: W.Workload, h: HostCopy, orc: O.Oracle = None):
     """Oracle result on host copies: returns (pool_k, pool_v, scale_k, scale_v)."""
     orc = orc or O.default()
+    if wl.axis_delta is not None:   # per-chunk tables: one oracle call per chunk, results merged
+        tabs, deltas = axis_tables(wl, theta_of(wl, orc))
+        acc = None
+        for c, (tab, de) in enumerate(zip(tabs, deltas)):
+            one = copy.copy(wl)
+            one.axis_delta, one.freq_axis, one.inv_freq = None, None, tab
+            hc = copy.copy(h)
+            ch = h.chunks[c]
+            hc.chunks = [O.Chunk(ch.src_offset, ch.length, de, ch.rank, ch.slots, ch.patches)]
+            if acc is not None:   # chunks write disjoint rows: chain the arrays through the calls
+                if wl.kind in ("ingest", "mla_ingest"):
+                    hc.store_k, hc.store_v = acc[0], acc[1]
+                else:
+                    hc.pool_k, hc.pool_v = acc[0], acc[1]
+            r = run_oracle(one, hc, orc)
+            acc = r if acc is None else (r[0], r[1], acc[2] + r[2], None if r[3] is None else acc[3] + r[3])
+        return acc
     pk = h.pool_k.copy()
     pv = h.pool_v.copy() if h.pool_v is not None else None
     if wl.kind == "gqa":

@@ -291,6 +291,16 @@ def pin_rotation_model_tables(orc: O.Oracle):
                     want = table_rope(k0, (start + np.array(move(dt), dtype=np.float64))[axis], th, pairing)
                     got = orc.rotate(kt, dt, tab, d, 0, pairing)
                     assert np.max(np.abs(got - want)) < 1e-8, (kind, dt, pairing, d)
+            # independent per-axis moves, contiguous or interleaved sections: R(1)
+            # over the table theta'_f = move[axis_f] * theta_f
+            for layout in ("sections", "interleaved"):
+                ax = W.freq_axes(d // 2, layout).astype(np.int64)
+                kt = table_rope(k0, start[ax], th, pairing)
+                for move in ((7, -3, 250), (0, 5, 0), (-30000, 12, 29999)):
+                    mv = np.array(move, dtype=np.int64)
+                    want = table_rope(k0, (start + mv)[ax], th, pairing)
+                    got = orc.rotate(kt, 1, mv[ax].astype(np.float64) * th, d, 0, pairing)
+                    assert np.max(np.abs(got - want)) < 1e-8, (layout, move, pairing, d)
 
 
 def pin_row_patch_is_matmul(orc: O.Oracle):
@@ -690,6 +700,45 @@ def pin_attend_relative_position(orc: O.Oracle):
         qm = complex_rotate(to_f64(q), D, th, 32, 0, RH)
         _, out2, _ = orc.attend(sk, sv, moved, seqs, qm, layer, th, 32)
         assert np.max(np.abs(out2 - out)) < 1e-9, (zero_rank, np.max(np.abs(out2 - out)))
+
+
+def pin_attend_per_chunk_tables(orc: O.Oracle):
+    """Chunks of one sequence moved by different multi-axis amounts: attention
+    over keys built independently at per-axis positions (table RoPE at
+    move_c[axis_f] per frequency, plus the key patch) equals the oracle given
+    one table per chunk, theta'_f = move_c[axis_f] * theta_f, at delta 1 (0
+    for a chunk that does not move)."""
+    rng = np.random.default_rng(35)
+    d, G = 32, 3
+    sk, sv, chunks, seqs, q, layer = _attend_problem(rng, d=d, G=G)
+    th = orc.inv_freq(1e4, d)
+    for layout in ("sections", "interleaved"):
+        axis = W.freq_axes(d // 2, layout).astype(np.int64)
+        moves = np.array([[40, 40, 40], [-7, 0, 0], [0, 0, 0], [900, -13, 250]], dtype=np.int64)
+        tabs = np.stack([mv[axis].astype(np.float64) * th for mv in moves])
+        run = [O.Chunk(c.src_offset, c.length, int(np.any(mv != 0)), c.rank, c.slots, c.patches)
+               for c, mv in zip(chunks, moves)]
+        _, out, _ = orc.attend(sk, sv, run, seqs, q, layer, tabs, d)
+        kf, vf, qf = to_f64(sk), to_f64(sv), to_f64(q)
+        for s in range(len(seqs) - 1):
+            for h in range(q.shape[1]):
+                g = h // G
+                Ks, Vs = [], []
+                for ci in range(seqs[s], seqs[s + 1]):
+                    c = chunks[ci]
+                    rows = slice(c.src_offset, c.src_offset + c.length)
+                    kk = table_rope(kf[rows, g], moves[ci][axis].astype(np.float64), th, RH)
+                    vv = vf[rows, g]
+                    if c.rank:
+                        uk, vk, uv, vvm = (to_f64(a)[layer, g] for a in c.patches)
+                        kk, vv = kk + uk @ vk.T, vv + uv @ vvm.T
+                    Ks.append(kk)
+                    Vs.append(vv)
+                K, V = np.concatenate(Ks), np.concatenate(Vs)
+                sc = (K @ qf[s, h]) / np.sqrt(d)
+                pr = np.exp(sc - sc.max())
+                want = (pr / pr.sum()) @ V
+                assert np.max(np.abs(out[s, h] - want)) < 1e-9, (layout, s, h)
 
 
 def pin_rejects_bad_indices(orc: O.Oracle):

@@ -175,3 +175,49 @@ def test_form_patch_argument_errors():
     assert e.value.status in (1, 3)
     # an empty block grid is a successful no-op
     K.kamera_form_patch(torch.zeros(0, 3, 16, 64, dtype=torch.bfloat16), 8, stream=0)
+
+
+class _RawRope:
+    """A KameraRope built field by field (the binding's own checks bypassed),
+    for the library's checks of the multi-axis fields.  The device pointer is
+    never dereferenced: each call is malformed and returns before any launch."""
+
+    def __init__(self, n_axes, axes, dptr, rot_dim=64):
+        self.n_axes, self.axes, self.dptr, self.rot_dim = n_axes, axes, dptr, rot_dim
+
+    def _c(self, n_chunks=0):
+        keep = None
+        ap = None
+        if self.axes is not None:
+            keep = np.ascontiguousarray(self.axes, dtype=np.uint8)
+            ap = keep.ctypes.data_as(C.POINTER(C.c_uint8))
+        return K._Rope(1e4, self.rot_dim, 0, K.ROTATE_HALF, self.n_axes, None, ap, self.dptr), keep
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-only argument checks; run where no GPU exists")
+def test_axis_rope_argument_errors():
+    pk = torch.zeros(1, 16, 2, 64, dtype=torch.bfloat16)
+    pv = torch.zeros_like(pk)
+    sk = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    sv = torch.zeros_like(sk)
+    ch = torch.zeros(64, dtype=torch.uint8)
+    fake = 1 << 20   # an 8-byte aligned address that is never read
+    axes = np.arange(32) % 3
+    for rope, status in ((_RawRope(4, np.zeros(32), fake), 3),            # more than 3 axes
+                         (_RawRope(-1, None, None), 1),                    # negative count
+                         (_RawRope(2, axes, fake), 1),                     # axis 2 of 2
+                         (_RawRope(3, axes, fake + 4), 1),                 # misaligned moves
+                         (_RawRope(3, axes, None), 1),                     # no moves
+                         (_RawRope(3, None, fake), 1),                     # no axis map
+                         (_RawRope(0, axes, None), 1),                     # map without axes
+                         (_RawRope(0, None, fake), 1)):                    # moves without axes
+        with pytest.raises(K.KameraError) as e:
+            K.kamera_relocate_patch(pk, pv, sk, sv, rope, ch, 1, 8, 0, stream=0)
+        assert e.value.status == status, (rope.n_axes, status)
+        with pytest.raises(K.KameraError) as e:
+            K.kamera_slide_inplace(pk, rope, ch, 1, 8, stream=0)
+        assert e.value.status == status
+    with pytest.raises(ValueError):   # the binding: moves must be a device int64 [n_chunks, n_axes] tensor
+        K.Rope(1e4, 64, freq_axis=axes, axis_delta=torch.zeros(1, 3, dtype=torch.int64))._c()
+    with pytest.raises(ValueError):
+        K.Rope(1e4, 64, freq_axis=axes)._c()

@@ -28,11 +28,14 @@ def _ulp_bf16(x: np.ndarray) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(ax)) - 7)
 
 
-def run_attend(a: W.AttendData, err=None, seq_start=None):
+def run_attend(a: W.AttendData, err=None, seq_start=None, freq_axis=None, axis_delta=None):
     spec = a.spec
     chunks = K.pack_chunks(a.chunks, device=DEV)
     seq = torch.tensor(a.seq_start if seq_start is None else seq_start, dtype=torch.int32, device=DEV)
-    rope = K.Rope(spec.base, a.rot_dim, spec.rot_offset, spec.pairing)
+    axes = {}
+    if axis_delta is not None:
+        axes = dict(freq_axis=freq_axis, axis_delta=torch.as_tensor(axis_delta, dtype=torch.int64, device=DEV))
+    rope = K.Rope(spec.base, a.rot_dim, spec.rot_offset, spec.pairing, **axes)
     max_len = max([c.length for c in a.chunks], default=0)
     max_rank = max([c.rank for c in a.chunks], default=0)
     out = K.kamera_attend_reused(a.store_k, a.store_v, a.q, rope, chunks, seq, len(a.chunks), max_len, max_rank,
@@ -41,18 +44,26 @@ def run_attend(a: W.AttendData, err=None, seq_start=None):
     return out
 
 
-def oracle_attend(a: W.AttendData):
+def oracle_attend(a: W.AttendData, freq_axis=None, axis_delta=None):
+    """The oracle on the same inputs; with multi-axis moves, one table per
+    chunk, theta'_f = move_c[axis_f] * theta_f, at delta 1 (0 for a chunk
+    that does not move)."""
     spec = a.spec
     orc = O.default()
     th = orc.inv_freq(spec.base, a.rot_dim)
-    oc = [O.Chunk(c.src_offset, c.length, c.delta, c.rank, c.slots.cpu().numpy(), [_bits(t) for t in c.patches])
-          for c in a.chunks]
+    deltas = [c.delta for c in a.chunks]
+    if axis_delta is not None:
+        ax = np.asarray(freq_axis, dtype=np.int64)
+        th = np.stack([mv[ax].astype(np.float64) * th for mv in axis_delta]) if len(axis_delta) else th
+        deltas = [int(np.any(mv != 0)) for mv in axis_delta]
+    oc = [O.Chunk(c.src_offset, c.length, de, c.rank, c.slots.cpu().numpy(), [_bits(t) for t in c.patches])
+          for c, de in zip(a.chunks, deltas)]
     return orc.attend(_bits(a.store_k), _bits(a.store_v), oc, a.seq_start, _bits(a.q), spec.layer, th, a.rot_dim,
                       spec.rot_offset, spec.pairing, scale=spec.d ** -0.5)
 
 
-def check(a: W.AttendData, out: torch.Tensor, what: str):
-    _, ref, mag = oracle_attend(a)
+def check(a: W.AttendData, out: torch.Tensor, what: str, **axes):
+    _, ref, mag = oracle_attend(a, **axes)
     got = out.float().cpu().numpy().astype(np.float64)
     err = np.abs(got - ref)
     allowed = _ulp_bf16(ref) + 2.0 ** -16 * mag
@@ -79,6 +90,28 @@ def test_attend_parity(name):
     out = run_attend(a, err=err)
     assert int(err.item()) == 0
     check(a, out, name)
+
+
+@pytest.mark.parametrize("layout", ["sections", "interleaved"])
+@pytest.mark.parametrize("name", ["qwen_gqa", "d64_interleaved_partial", "rank64"])
+def test_attend_multi_axis_moves(name, layout):
+    """Chunks of one sequence moved by different (time, height, width)
+    amounts; the descriptors' own deltas are not used."""
+    a = W.make_attend(CASES[name], DEV)
+    axes = dict(freq_axis=W.freq_axes(a.rot_dim // 2, layout), axis_delta=W.axis_moves(len(a.chunks), name, layout))
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_attend(a, err=err, **axes)
+    assert int(err.item()) == 0
+    check(a, out, f"{name} {layout}", **axes)
+
+
+def test_attend_axis_move_out_of_range():
+    a = W.make_attend(W.AttendSpec("at_axerr", H=2, G=2, d=64, seqs=((40,), (30,)), m=8), DEV)
+    moves = np.array([[1, 2, 3], [0, -2 ** 40, 0]], dtype=np.int64)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = run_attend(a, err=err, freq_axis=W.freq_axes(32), axis_delta=moves)
+    assert int(err.item()) & 4
+    assert torch.count_nonzero(out[1]).item() == 0   # the only chunk of sequence 1 was skipped
 
 
 def test_empty_sequences_give_zeros():

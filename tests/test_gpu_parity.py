@@ -79,6 +79,57 @@ def test_model_frequency_tables(name, table, path):
     assert int(err.item()) == 0
 
 
+@pytest.mark.parametrize("layout", ["sections", "interleaved"])
+@pytest.mark.parametrize("name", ["qwen_recall", "dsv2_mla", "qwen_slide", "qwen_ingest", "dsv2_mla_ingest",
+                                  "mha_reorder_recall"])
+def test_multi_axis_moves(name, layout, path):
+    """Multi-axis RoPE with per-chunk moves along (time, height, width): a
+    whole-segment move, a move along time only, independent axis moves and no
+    move, in one call, the frequencies following their axes in contiguous
+    sections or interleaved.  The descriptors' own deltas are not used.
+    Against the oracle run chunk by chunk over each chunk's table
+    theta'_f = move[axis_f] * theta_f."""
+    spec = W.scaled(W.CONFIGS[name](), L=2, lens=(300, 129, 7, 64, 33))
+    wl = W.make(spec, DEV)
+    wl.freq_axis = W.freq_axes(wl.rot_dim // 2, layout)
+    wl.axis_delta = W.axis_moves(len(wl.chunks), name, layout)
+    h = Hn.snapshot(wl)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    Hn.check_parity(wl, h, f"{name} {layout}")
+    assert int(err.item()) == 0
+    if wl.kind == "slide":   # a chunk that does not move is left as it was, bit for bit
+        for c, mv in zip(wl.chunks, wl.axis_delta):
+            if not mv.any():
+                sl = c.slots.cpu().numpy()
+                assert np.array_equal(Hn.u16(wl.pool_k)[:, sl], h.pool_k[:, sl])
+
+
+@pytest.mark.parametrize("kind", ["qwen_recall", "qwen_slide"])
+def test_device_error_axis_move_out_of_range(kind, path):
+    """A chunk with an axis move beyond 2^31 - 1 is skipped whole with the
+    descriptor bit; the other chunk is still right."""
+    spec = W.scaled(W.CONFIGS[kind](), L=2, lens=(70, 50))
+    wl = W.make(spec, DEV)
+    wl.freq_axis = W.freq_axes(wl.rot_dim // 2)
+    wl.axis_delta = np.array([[5, -3, 9], [0, 2 ** 40, 0]], dtype=np.int64)
+    h = Hn.snapshot(wl)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    Hn.run_gpu(wl, err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) & 4
+    gk = Hn.u16(wl.pool_k)
+    s1 = wl.chunks[1].slots.cpu().numpy()
+    assert np.array_equal(gk[:, s1], h.pool_k[:, s1])
+    good = W.Workload(wl.spec, wl.kind, [wl.chunks[0]], wl.store_k, wl.store_v, wl.pool_k, wl.pool_v,
+                      wl.rot_dim, wl.rot_offset, wl.pairing, wl.base, freq_axis=wl.freq_axis,
+                      axis_delta=wl.axis_delta[:1])
+    hg = Hn.HostCopy(h.store_k, h.store_v, h.pool_k, h.pool_v, [h.chunks[0]])
+    ok, ov, sk, sv = Hn.run_oracle(good, hg)
+    s0 = h.chunks[0].slots
+    Hn.compare(gk[:, s0], ok[:, s0], sk[:, s0], what="good chunk")
+
+
 @pytest.mark.parametrize("m", [1, 3, 8, 16, 17, 32, 48, 64, 96, 128])
 def test_gqa_ranks(m, path):
     spec = W.scaled(W.qwen_recall(), L=1, H=2, lens=(130, 5), m=m)

@@ -24,6 +24,7 @@ ATTEND_MUTANTS = {
     "scale_dropped": ("sc = scale * (K @ qf[s, h])", "sc = K @ qf[s, h]"),
     "wrong_kv_head": ("for h in range(g * G, (g + 1) * G):", "for h in range(g, Hq, H):"),
     "softmax_not_normalised": ("pr = w / w.sum()", "pr = w"),
+    "first_chunk_table_for_all": ("th = inv_freq[ci] if", "th = inv_freq[seq_starts[s]] if"),
 }
 
 FORM_PATCH_MUTANTS = {
@@ -35,7 +36,7 @@ FORM_PATCH_MUTANTS = {
 }
 
 ATTEND_PINS = [P.pin_attend_single_token, P.pin_attend_uniform_keys, P.pin_attend_fused_identity,
-               P.pin_attend_relative_position]
+               P.pin_attend_relative_position, P.pin_attend_per_chunk_tables]
 FORM_PATCH_PINS = [P.pin_form_patch_full_rank, P.pin_eckart_young]
 
 

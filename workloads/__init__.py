@@ -221,6 +221,38 @@ def mrope_sections(n_freq: int):
     return [(0, t), (t, t + hgt), (t + hgt, n_freq)]
 
 
+def freq_axes(n_freq: int, layout: str = "sections") -> np.ndarray:
+    """The axis (0 time, 1 height, 2 width) each frequency follows:
+    'sections'     contiguous ranges (``mrope_sections``)
+    'interleaved'  frequency f follows axis f mod 3 (an interleaved layout)"""
+    out = np.empty(n_freq, dtype=np.uint8)
+    if layout == "sections":
+        for a, (lo, hi) in enumerate(mrope_sections(n_freq)):
+            out[lo:hi] = a
+    else:
+        out[:] = np.arange(n_freq) % 3
+    return out
+
+
+def axis_moves(n_chunks: int, *tags) -> np.ndarray:
+    """Seeded per-chunk (time, height, width) moves, int64 [n_chunks, 3],
+    cycling through the kinds a multimodal prompt produces: a text or whole-
+    segment move (d, d, d), a move along time only (d, 0, 0), independent
+    axis moves, and no move (0, 0, 0)."""
+    rng = _np_rng("axis_moves", n_chunks, *tags)
+    out = np.zeros((n_chunks, 3), dtype=np.int64)
+    for c in range(n_chunks):
+        d = int(rng.integers(-5000, 30000))
+        kind = c % 4
+        if kind == 0:
+            out[c] = (d, d, d)
+        elif kind == 1:
+            out[c] = (d, 0, 0)
+        elif kind == 2:
+            out[c] = rng.integers(-2000, 2000, size=3)
+    return out
+
+
 def model_inv_freq(kind: str, base: float, rot_dim: int) -> np.ndarray:
     """A model's own rotary frequency table, passed to the operator as an input.
 
@@ -431,6 +463,8 @@ class Workload:
     base: float = 1e4
     kv_lora: int = 0
     inv_freq: Optional[np.ndarray] = None      # a model's own rotary frequency table (default: base^(-2i/r))
+    freq_axis: Optional[np.ndarray] = None     # multi-axis RoPE: the axis each frequency follows
+    axis_delta: Optional[np.ndarray] = None    # multi-axis RoPE: int64 [n_chunks, n_axes] per-chunk moves
 
     @property
     def tokens(self) -> int:
