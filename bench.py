@@ -233,7 +233,9 @@ def sweep(K, dev, peak, skip, only=None):
         if name in skip or (only is not None and name not in only):
             continue
         try:
-            out[name] = attend_entry(K, f(), dev, peak, flush)
+            spec = f()
+            entry = mla_attend_entry if spec.kind == "mla_attend" else attend_entry
+            out[name] = entry(K, spec, dev, peak, flush)
         except Exception as e:  # report, keep the headline
             out[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
     return out
@@ -263,6 +265,32 @@ def attend_entry(K, spec, dev, peak, flush):
             "tokens_attended_per_s": tok / t, "sequences": len(spec.seqs), "rank": spec.m,
             "l2": "flushed between launches", "kernel": "attend_kernel",
             "traffic": traffic_record("attend_kernel", spec.name), "device_err": int(err.item())}
+
+
+def mla_attend_entry(K, spec, dev, peak, flush):
+    """MLA decode attention over reused chunks (absorbed form, one query token per
+    sequence and query head), timed per launch with L2 flushes."""
+    a = W.make_mla_attend(spec, dev)
+    chunks = K.pack_chunks(a.chunks, device=dev)
+    seq = torch.tensor(a.seq_start, dtype=torch.int32, device=dev)
+    rope = K.Rope(spec.base, a.rot_dim, spec.rot_offset, spec.pairing)
+    ml, mr = max(c.length for c in a.chunks), max(c.rank for c in a.chunks)
+    out = torch.empty(a.q.shape[0], spec.Hq, spec.kv_lora, dtype=torch.bfloat16, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        K.kamera_mla_attend_reused(a.store, spec.kv_lora, a.q, rope, chunks, seq, len(a.chunks), ml, mr,
+                                   layer=spec.layer, out=out, err=err)
+
+    for _ in range(3):
+        call()
+    t = float(np.median(time_launches(call, 10, flush))) * 1e-3
+    b = W.mla_attend_bytes(spec)
+    tok = sum(c.length for c in a.chunks)
+    return {"ms": t * 1e3, "gbs": b / t / 1e9, "frac_of_hbm_peak": b / t / 1e9 / peak, "bytes": b,
+            "tokens_attended_per_s": tok / t, "sequences": len(spec.seqs), "rank": spec.m,
+            "l2": "flushed between launches", "kernel": "mla_attend_kernel",
+            "traffic": traffic_record("mla_attend_kernel", spec.name), "device_err": int(err.item())}
 
 
 def formation_entry(K, spec, dev, peak, flush):
@@ -375,6 +403,7 @@ KERNEL_UNITS = {   # the translation unit each timed kernel is compiled from
     "ingest_kernel": "kamera_ingest.cu",
     "patch_form_kernel": "kamera_patchform.cu",
     "attend_kernel": "kamera_attend.cu",
+    "mla_attend_kernel": "kamera_attend_mla.cu",
 }
 
 

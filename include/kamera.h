@@ -77,7 +77,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
-#define KAMERA_ABI_VERSION 6
+#define KAMERA_ABI_VERSION 7
 
 /* Limits of this build. */
 #define KAMERA_MAX_RANK 128          /* largest patch rank m */
@@ -463,6 +463,47 @@ typedef struct KameraAttnQuery {
 int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, const KameraRope* rope,
                          const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
                          int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream);
+
+/*
+ * MLA decode attention over reused chunks (absorbed form), without the pool.
+ * The rows of chunk c's token j are the MLA reuse rows, unrounded:
+ *     c'_j  = c_j + Uc[j] Vc^T           (latent, kv_lora_rank wide)
+ *     kr'_j = R(delta) kr_j + Ur[j] Vr^T  (k_rope, rope_dim wide)
+ * (c_j | kr_j: store row src_offset + j; factors as for
+ * kamera_mla_relocate_patch, read at `layer`).  Query head h of sequence s
+ * holds q_lat (the no-position query taken through the key up-projection,
+ * kv_lora_rank wide) then q_rope (rope_dim wide, RoPE applied at the query's
+ * position); out_h = softmax_j(scale (q_lat . c'_j + q_rope . kr'_j)) c'_j, the
+ * latent output the caller takes through the value up-projection.  All query
+ * heads share the one latent row.  fp32 accumulation on bf16 operands (values
+ * that are not bf16 enter as a hi + lo pair), one bf16 rounding of the output;
+ * a sequence with no token gets zeros.
+ *   kv      the canonical MLA store of ONE layer: bf16 [num_rows][kv_lora_rank +
+ *           rope_dim], rows row_stride elements apart (16-byte aligned, row_stride
+ *           a multiple of 8); layer = the factors' layer index
+ *   query   q bf16 [n_seqs][num_q_heads][kv_lora_rank + rope_dim], out bf16
+ *           [n_seqs][num_q_heads][kv_lora_rank] (written), scale; q and out
+ *           16-byte aligned
+ *   rope    rot_offset / rot_dim relative to k_rope
+ *   d_seq_start, descriptors: as for kamera_attend_reused; ranks even.
+ * Supported: kv_lora_rank 512, rope_dim 64 (DeepSeek-V2/V3), num_q_heads 1..16,
+ * max_rank <= 32.  Device errors (the chunk is skipped): SOURCE, DESCRIPTOR
+ * (also an odd rank, or a malformed d_seq_start: the sequence is skipped), LEN,
+ * RANK.
+ */
+typedef struct KameraAttnMlaKV {
+    const void* kv;
+    int64_t num_rows;
+    int64_t row_stride;
+    int32_t kv_lora_rank;
+    int32_t rope_dim;
+    int32_t layer;
+    int32_t reserved;   /* 0 */
+} KameraAttnMlaKV;
+
+int kamera_mla_attend_reused(const KameraAttnMlaKV* kv, const KameraAttnQuery* query, const KameraRope* rope,
+                             const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
+                             int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream);
 
 /* KAMERA_ABI_VERSION of the loaded library. */
 int kamera_abi_version(void);

@@ -17,7 +17,8 @@ technical summary):
   top-m factors)                                                      -> ``form_patch``
 * section 3.2, sliding-window survival by rotation only               -> ``slide``
 * attention over reused chunks (the pages' attention-kernel hook, section 3):
-  softmax attention of a decode query over the reuse equation's rows -> ``attend``
+  softmax attention of a decode query over the reuse equation's rows -> ``attend``,
+  and its MLA form over the latent rows (absorbed query)                 -> ``attend_mla``
 
 Pinned by ``tests/test_oracle_pins.py`` (closed forms, group laws of R, an
 independent complex-number RoPE, brute-force bf16 rounding, Eckart-Young by
@@ -398,6 +399,54 @@ class Oracle:
                     pr = w / w.sum()
                     out[s, h] = pr @ V
                     mag[s, h] = pr @ np.abs(V)
+        return self.bf16_rne(out), out, mag
+
+    def attend_mla(self, store, chunks: Sequence[Chunk], seq_starts, q, layer: int, kv_lora: int, inv_freq,
+                   rot_dim: int, rot_offset: int = 0, pairing: int = INTERLEAVED, scale: float = None):
+        """MLA decode attention (absorbed form) of one query token per sequence over
+        its reused chunks.  Each chunk's rows are the MLA reuse rows (technical
+        summary section 2, with section 3's MLA rule: c_KV carried over, the
+        decoupled k_rope turned), exact and unrounded (fp64):
+            c' = c + U_c V_c^T,   kr' = R(delta) kr + U_r V_r^T
+        and query head h (latent part q_lat, rope part q_rope) attends with
+        softmax_j(scale (q_lat . c'_j + q_rope . kr'_j)) over c'_j.
+
+        ``store``: uint16 ``[N, kv_lora + rope]`` (one layer); ``q``: uint16
+        ``[S, H_q, kv_lora + rope]``; factors Uc ``[L, len, m]``, Vc ``[L, kv_lora,
+        m]``, Ur ``[L, len, m]``, Vr ``[L, rope, m]`` read at ``layer``;
+        ``rot_offset`` is relative to k_rope; ``inv_freq`` one table or one row per
+        chunk.  Returns (bf16 bits ``[S, H_q, kv_lora]``, fp64 output, magnitude
+        sum_j p_j |c'_j| per element).  ``q`` and the factors may be fp64."""
+        N, Wd = store.shape
+        S, Hq, _ = q.shape
+        scale = 1.0 / np.sqrt(Wd) if scale is None else float(scale)
+        f64 = lambda a: a if np.asarray(a).dtype == np.float64 else self.bf16_to_f64(a)
+        sf, qf = self.bf16_to_f64(store), f64(q)
+        out = np.zeros((S, Hq, kv_lora))
+        mag = np.zeros((S, Hq, kv_lora))
+        for s in range(S):
+            lat, keys = [], []
+            for ci in range(seq_starts[s], seq_starts[s + 1]):
+                c = chunks[ci]
+                th = inv_freq[ci] if np.ndim(inv_freq) == 2 else inv_freq
+                rows = slice(c.src_offset, c.src_offset + c.length)
+                cl = sf[rows, :kv_lora].copy()
+                kr = self.rotate(sf[rows, kv_lora:], c.delta, th, rot_dim, rot_offset, pairing)
+                if c.rank > 0:
+                    uc, vc, ur, vr = (f64(a)[layer] for a in c.patches)
+                    cl = cl + uc @ vc.T
+                    kr = kr + ur @ vr.T
+                lat.append(cl)
+                keys.append(np.concatenate([cl, kr], axis=1))
+            if not keys or sum(k.shape[0] for k in keys) == 0:
+                continue
+            K, V = np.concatenate(keys), np.concatenate(lat)
+            for h in range(Hq):
+                sc = scale * (K @ qf[s, h])
+                w = np.exp(sc - sc.max())
+                pr = w / w.sum()
+                out[s, h] = pr @ V
+                mag[s, h] = pr @ np.abs(V)
         return self.bf16_rne(out), out, mag
 
     def num_threads(self) -> int:

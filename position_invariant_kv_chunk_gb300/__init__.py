@@ -104,6 +104,12 @@ class _AttnQuery(C.Structure):
                 ("scale", C.c_float), ("reserved", C.c_int32)]
 
 
+class _AttnMlaKV(C.Structure):
+    _fields_ = [("kv", C.c_void_p), ("num_rows", C.c_int64), ("row_stride", C.c_int64),
+                ("kv_lora_rank", C.c_int32), ("rope_dim", C.c_int32), ("layer", C.c_int32),
+                ("reserved", C.c_int32)]
+
+
 class _MlaStore(C.Structure):
     _fields_ = [("kv", C.c_void_p), ("num_rows", C.c_int64), ("layer_stride", C.c_int64),
                 ("row_stride", C.c_int64)]
@@ -148,6 +154,9 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C
     lib.kamera_attend_reused.restype = C.c_int
     lib.kamera_attend_reused.argtypes = [P(_AttnKV), P(_AttnQuery), P(_Rope), C.c_void_p, C.c_void_p, C.c_int32,
                                          C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
+    lib.kamera_mla_attend_reused.restype = C.c_int
+    lib.kamera_mla_attend_reused.argtypes = [P(_AttnMlaKV), P(_AttnQuery), P(_Rope), C.c_void_p, C.c_void_p,
+                                             C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
     lib.kamera_validate_chunks.restype = C.c_int
     lib.kamera_validate_chunks.argtypes = [P(_Chunk), C.c_int32, C.c_int64, C.c_int64, C.c_int32,
                                            C.c_int32, P(C.c_int32), P(C.c_int32)]
@@ -167,7 +176,7 @@ def kamera_status_string(status: int) -> str:
     return load_library().kamera_status_string(int(status)).decode()
 
 
-ABI_VERSION = 6   # the KAMERA_ABI_VERSION these bindings marshal for
+ABI_VERSION = 7   # the KAMERA_ABI_VERSION these bindings marshal for
 
 
 def kamera_abi_version() -> int:
@@ -531,4 +540,41 @@ def kamera_attend_reused(store_k: torch.Tensor, store_v: torch.Tensor, q: torch.
                                              _stream_handle(stream))
     del keep
     _check(rc, "kamera_attend_reused")
+    return out
+
+
+def kamera_mla_attend_reused(store: torch.Tensor, kv_lora: int, q: torch.Tensor, rope: Rope, chunks: torch.Tensor,
+                             seq_start: torch.Tensor, n_chunks: int, max_len: int, max_rank: int, layer: int = 0,
+                             scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
+                             err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """MLA decode attention (absorbed form) of one query token per sequence over
+    its reused chunks (see ``kamera_mla_attend_reused`` in kamera.h).
+
+    store: bf16 ``[N, kv_lora + rope_dim]`` (one layer, any row stride);
+    q: bf16 ``[S, H_q, kv_lora + rope_dim]`` contiguous (latent query, then
+    rope query); seq_start: device int32 ``[S + 1]``; rope: rot_offset
+    relative to k_rope; scale: default 1/sqrt(kv_lora + rope_dim).  Returns
+    ``out`` (bf16 ``[S, H_q, kv_lora]``)."""
+    for t, nm in ((store, "store"), (q, "q")):
+        _bf16(t, nm)
+    if store.dim() != 2 or store.stride(1) != 1:
+        raise ValueError("store must be [N, kv_lora + rope_dim] with packed rows")
+    N, W = store.shape
+    if q.dim() != 3 or q.shape[2] != W or not q.is_contiguous():
+        raise ValueError("q must be a contiguous [S, H_q, kv_lora + rope_dim] tensor")
+    S, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty(S, Hq, kv_lora, dtype=torch.bfloat16, device=q.device)
+    if tuple(out.shape) != (S, Hq, kv_lora) or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 [S, H_q, kv_lora] tensor")
+    if seq_start.dtype != torch.int32 or seq_start.numel() != S + 1:
+        raise ValueError("seq_start must hold S + 1 int32 values")
+    kv = _AttnMlaKV(_addr(store), N, store.stride(0), int(kv_lora), int(W - kv_lora), int(layer), 0)
+    qq = _AttnQuery(_addr(q), _addr(out), S, Hq, float(W ** -0.5 if scale is None else scale), 0)
+    r, keep = rope._c(n_chunks)
+    rc = load_library().kamera_mla_attend_reused(C.byref(kv), C.byref(qq), C.byref(r), _addr(chunks),
+                                                 _addr(seq_start), int(n_chunks), int(max_len), int(max_rank),
+                                                 _addr(err), _stream_handle(stream))
+    del keep
+    _check(rc, "kamera_mla_attend_reused")
     return out

@@ -605,4 +605,56 @@ int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, c
     return launch_attend(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
 }
 
+int kamera_mla_attend_reused(const KameraAttnMlaKV* kv, const KameraAttnQuery* query, const KameraRope* rope,
+                             const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
+                             int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream)
+{
+    if (!kv || !query || !rope || kv->reserved != 0 || query->reserved != 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (query->n_seqs < 0 || n_chunks < 0 || max_len < 0 || max_rank < 0 || kv->num_rows < 0 || kv->layer < 0 ||
+        kv->kv_lora_rank < 1 || kv->rope_dim < 0 || query->num_q_heads < 1 || !(query->scale == query->scale))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (!mla_attend_supported(kv->kv_lora_rank, kv->rope_dim, query->num_q_heads, max_rank) ||
+        query->n_seqs > 0x7FFFFFFF / 8)
+        return KAMERA_ERR_UNSUPPORTED;
+    if (query->n_seqs == 0)
+        return KAMERA_OK;
+    if (!kv->kv || !query->q || !query->out || !d_seq_start || (n_chunks > 0 && !d_chunks))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    const int64_t W = (int64_t)kv->kv_lora_rank + kv->rope_dim;
+    if (kv->row_stride < W)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(kv->kv) || !aligned16(d_chunks) || kv->row_stride % 8 || !aligned16(query->q) ||
+        !aligned16(query->out))
+        return KAMERA_ERR_MISALIGNED;
+    const auto ks = span(kv->kv, 1, 0, kv->num_rows, kv->row_stride, W);
+    const auto qs = span(query->q, 1, 0, 1, 0, (int64_t)query->n_seqs * query->num_q_heads * W);
+    const auto os = span(query->out, 1, 0, 1, 0, (int64_t)query->n_seqs * query->num_q_heads * kv->kv_lora_rank);
+    if (overlap(os, ks) || overlap(os, qs))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    MlaAttendParams p;
+    std::memset(&p, 0, sizeof(p));
+    int rc;
+    if ((rc = fill_rope(rope, kv->rope_dim, &p.rope)))
+        return rc;
+    p.kv = static_cast<const __nv_bfloat16*>(kv->kv);
+    p.row_stride = kv->row_stride;
+    p.num_rows = kv->num_rows;
+    p.kv_lora = kv->kv_lora_rank;
+    p.rope_dim = kv->rope_dim;
+    p.Hq = query->num_q_heads;
+    p.layer = kv->layer;
+    p.chunks = d_chunks;
+    p.seq_start = d_seq_start;
+    p.n_seqs = query->n_seqs;
+    p.n_chunks = n_chunks;
+    p.q = static_cast<const __nv_bfloat16*>(query->q);
+    p.out = static_cast<__nv_bfloat16*>(query->out);
+    p.scale = query->scale;
+    p.max_len = max_len;
+    p.max_rank = max_rank;
+    p.err = d_err;
+    return launch_mla_attend(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
+}
+
 }  // extern "C"

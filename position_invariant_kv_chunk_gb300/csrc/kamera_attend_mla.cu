@@ -1,0 +1,645 @@
+// kamera_attend_mla.cu -- MLA decode attention over reused chunks, without the pool.
+//
+// The MLA rows the reuse equation gives (the gist.science technical summary,
+// section 2; the MLA rule of section 3: c_KV is carried over, the decoupled
+// k_rope turned) are, for token j of chunk c,
+//     c'_j  = c_j + V_c u_j            (latent, kv_lora wide)
+//     kr'_j = R(delta_c) kr_j + V_r w_j  (rope_dim wide)
+// and absorbed MLA decode attends with the latent query (q_nope taken through
+// the key up-projection) and the rope query:
+//     score_hj = scale (q_lat_h . c'_j + q_rope_h . kr'_j),  out_h = sum_j p_hj c'_j
+// (the caller takes out_h through the value up-projection).  The patch and the
+// turn fold into per-chunk quantities, as for GQA attention:
+//     q_lat . c'_j  = q_lat . c_j + (V_c^T q_lat) . u_j
+//     q_rope . kr'_j = (R(-delta) q_rope) . kr_j + (V_r^T q_rope) . w_j
+//     sum_j p_j c'_j = sum_j p_j c_j + V_c (sum_j p_j u_j)
+// so a decode step streams the canonical rows and the U rows only.
+//
+// Every query head shares the one latent row, so the work is a dense
+// contraction per 64-token tile: S[16 heads x 64 tokens] over the key width
+// (kv_lora + rope_dim + 2 m), then O[16 x kv_lora] += P S-softmax'd x C.  The
+// 16 query heads are the rows of warp-level bf16 MMAs (m16n8k16, fp32
+// accumulate): a decode step has 16 query rows per latent head, below the
+// 64-row minimum of the tensor-memory MMA, and the warp-level form keeps the
+// score tile and the output accumulator in registers.  Warp w computes the
+// scores of tokens 8w .. 8w + 7 against all 16 heads with the latent query held
+// in registers for the whole kernel (loaded once), and owns output columns
+// 64w .. 64w + 63.  Operands that are not bf16 already (the turned rope query,
+// the folds, the softmax weights) enter as a bf16 hi + lo pair, so products
+// keep about 16 bits of their fp32 value; the canonical rows and U rows are
+// exact bf16.  Tiles are double-buffered 16-byte async copies into rows padded
+// to an odd number of 16-byte vectors, so the eight rows an 8x8 matrix load
+// reads fall in distinct banks.  A cluster of CL CTAs serves one sequence, CTA
+// r taking the r-th of CL even runs of the sequence's tiles (a chunk cut
+// between two CTAs is set up by both, each folding its own share of the value
+// patch); rank 0 merges the partial softmax states through distributed shared
+// memory.
+#include <cooperative_groups.h>
+#include <cstdint>
+#include <cuda_bf16.h>
+
+#include "kamera_common.cuh"
+#include "kamera_internal.h"
+#include "kamera_ptx.cuh"
+
+namespace kamera {
+
+namespace {
+
+constexpr int kMlThreads = 256;
+constexpr int kMlT = 64;             // tokens per tile
+constexpr int kMlH = 16;             // query heads: the rows of every MMA
+constexpr int kMlC = 512;            // kv_lora_rank
+constexpr int kMlR = 64;             // rope_dim
+constexpr int kMlDK = kMlC + kMlR;   // key width before the U columns
+constexpr int kMlQS = kMlC + 8;      // staged latent-query row (elements)
+constexpr int kMlMaxCL = 8;
+
+// MP: the padded rank the instantiation takes (0, 16 or 32).
+template <int MP>
+struct __align__(16) MlSmem {
+    static constexpr int KW = kMlDK + 2 * MP;   // tile row: c_KV | k_rope | u (V_c's factor) | w (V_r's)
+    static constexpr int RS = KW + 8;           // row stride: an odd number of 16-byte vectors
+    static constexpr int XW = kMlR + 2 * MP;    // per-chunk query part: R(-delta) q_rope | V_c^T q_lat | V_r^T q_rope
+    static constexpr int XS = XW + 8;
+    static constexpr int MPa = MP > 0 ? MP : 1;
+    __nv_bfloat16 kt[2][kMlT][RS];              // tiles; the latent queries at the start; partial outputs at the end
+    __nv_bfloat16 xh[kMlH][XS];                 // per-chunk query part, bf16 hi
+    __nv_bfloat16 xl[kMlH][XS];                 // and lo
+    float sc[kMlH][kMlT + 4];                   // scores of the tile
+    __nv_bfloat16 ph[kMlH][kMlT + 8];           // softmax weights, hi
+    __nv_bfloat16 pl[kMlH][kMlT + 8];           // and lo
+    float alpha[kMlH];                          // running-max rescale of the tile
+    float qr[kMlH][kMlR];                       // q_rope of the sequence (fp32)
+    float vr[kMlR][MPa];                        // V_r of the current chunk
+    float wsum[kMlH][MPa];                      // sum_j p_j u_j of the chunk, at its end
+    float2 cs[kMlR / 2];                        // cos/sin of -delta
+    float cm[kMlH], cl[kMlH];                   // this CTA's softmax state, for the merge
+    float fac[kMlH][kMlMaxCL];                  // merge weights (rank 0)
+};
+
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x4_t(uint32_t a, uint32_t (&r)[4])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t (&r)[2])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(a)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t a, uint32_t (&r)[2])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(a)
+                 : "memory");
+}
+// D += A B: A 16x16 (row-major fragments), B 16x8 (column fragments), fp32 D.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+                 "{%8, %9}, {%0, %1, %2, %3};"
+                 : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+                 : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// (x, y) as bf16 pairs hi and lo with hi + lo = (x, y) to about 2^-16 relative.
+__device__ __forceinline__ void split_hl(float x, float y, uint32_t& hi, uint32_t& lo)
+{
+    hi = pack_bf16x2(x, y);
+    lo = pack_bf16x2(x - bf16lo(hi), y - bf16hi(hi));
+}
+__device__ __forceinline__ void st_shared_u32(uint32_t a, uint32_t v)
+{
+    asm volatile("st.shared.u32 [%0], %1;" ::"r"(a), "r"(v) : "memory");
+}
+
+__device__ __forceinline__ int32_t mla_check(const KameraChunk& ch, int c, const MlaAttendParams& p)
+{
+    int32_t bits = check_axis_delta(p.rope, c);
+    if (ch.len < 0 || ch.rank < 0 || (ch.rank & 1) || ch.delta > KAMERA_MAX_ABS_DELTA ||
+        ch.delta < -KAMERA_MAX_ABS_DELTA)
+        bits |= KAMERA_DEVERR_DESCRIPTOR;
+    if (ch.src_offset < 0 || ch.src_offset + (int64_t)max(ch.len, 0) > p.num_rows)
+        bits |= KAMERA_DEVERR_SOURCE;
+    if (ch.len > p.max_len)
+        bits |= KAMERA_DEVERR_LEN;
+    if (ch.rank > p.max_rank)
+        bits |= KAMERA_DEVERR_RANK;
+    if (ch.rank > 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(patch_ptr(ch, i));
+            if (a == 0 || (a & 15))
+                bits |= KAMERA_DEVERR_DESCRIPTOR;
+        }
+    }
+    return bits;
+}
+
+// Copies tile rows j0 .. j0 + n - 1 of chunk `ch` into buffer b; rows past n
+// and U columns past the rank are zero.
+template <int MP>
+__device__ __forceinline__ void mla_load(const MlaAttendParams& p, const KameraChunk& ch, int j0, int n, int b,
+                                         MlSmem<MP>& s)
+{
+    // c_KV | k_rope: 72 16-byte vectors a row; eight threads a row, each taking
+    // vectors q, q + 8, ... (9) of rows r and r + 32
+    static_assert(kMlDK == 8 * 8 * 9 && kMlThreads == 8 * kMlT / 2, "row split");
+    const __nv_bfloat16* src = p.kv + (ch.src_offset + j0) * p.row_stride;
+    const int r0 = threadIdx.x >> 3, q = threadIdx.x & 7;
+#pragma unroll
+    for (int hf = 0; hf < 2; ++hf) {
+        const int t = r0 + 32 * hf;
+        const uint32_t dst = ptx::smem_addr(&s.kt[b][t][8 * q]);
+        if (t < n) {
+            const __nv_bfloat16* g = src + (int64_t)t * p.row_stride + 8 * q;
+#pragma unroll
+            for (int i = 0; i < 9; ++i)
+                ptx::cp_async16(dst + 128 * i, g + 64 * i);
+        } else {
+#pragma unroll
+            for (int i = 0; i < 9; ++i)
+                ptx::st_shared_zero16(dst + 128 * i);
+        }
+    }
+    if constexpr (MP > 0) {   // u and w rows: MP / 2 words each (the rank is even)
+        const int m = ch.rank;
+        const int64_t fo = ((int64_t)p.layer * ch.len + j0) * m;   // U [L][len][m]
+        const __nv_bfloat16* uc = patch_ptr(ch, 0);
+        const __nv_bfloat16* ur = patch_ptr(ch, 2);
+        for (int e = threadIdx.x; e < kMlT * MP; e += kMlThreads) {
+            const int t = e / MP, wd = e - t * MP;
+            const int f = wd >= MP / 2 ? 1 : 0, c2 = 2 * (wd - f * (MP / 2));
+            const uint32_t dst = ptx::smem_addr(&s.kt[b][t][kMlDK + f * MP + c2]);
+            if (t < n && c2 < m)
+                ptx::cp_async_small<4>(dst, (f ? ur : uc) + fo + (int64_t)t * m + c2);
+            else
+                st_shared_u32(dst, 0u);
+        }
+    }
+    ptx::cp_async_commit();
+}
+
+template <int MP>
+__global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_constant__ MlaAttendParams p)
+{
+    using SM = MlSmem<MP>;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    SM& s = *reinterpret_cast<SM*>(smem_raw);
+    namespace cg = cooperative_groups;
+    const int CL = p.cluster, rank = (int)(blockIdx.x % (unsigned)CL), seq = blockIdx.x / CL;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
+    const int Hq = p.Hq;
+    // 8x8 matrix-load addressing: A (row-major 16 x 16) and B^T (token rows)
+    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
+
+    int c0 = p.seq_start[seq], c1 = p.seq_start[seq + 1];
+    if (c0 < 0 || c1 < c0 || c1 > p.n_chunks) {
+        if (rank == 0 && threadIdx.x == 0)
+            raise_err(p.err, KAMERA_DEVERR_DESCRIPTOR);
+        c0 = c1 = 0;
+    }
+    // this CTA's share: tiles [lo, hi) of the sequence's valid chunks' tiles, in order
+    int64_t total = 0;
+    for (int c = c0; c < c1; ++c) {
+        const KameraChunk& ch = p.chunks[c];
+        if (!mla_check(ch, c, p))
+            total += (ch.len + kMlT - 1) / kMlT;
+    }
+    const int64_t lo = total * rank / CL, hi = total * (rank + 1) / CL;
+
+    // the latent queries (rows past Hq zero) staged in the second tile buffer; q_rope as fp32
+    __nv_bfloat16* qls = &s.kt[1][0][0];
+    for (int e = threadIdx.x; e < kMlH * (kMlC / 8); e += kMlThreads) {
+        const int h = e / (kMlC / 8), v = e - h * (kMlC / 8);
+        uint4 w = make_uint4(0u, 0u, 0u, 0u);
+        if (h < Hq)
+            w = *reinterpret_cast<const uint4*>(p.q + ((int64_t)seq * Hq + h) * kMlDK + 8 * v);
+        *reinterpret_cast<uint4*>(qls + h * kMlQS + 8 * v) = w;
+    }
+    for (int e = threadIdx.x; e < kMlH * kMlR; e += kMlThreads) {
+        const int h = e / kMlR, i = e - h * kMlR;
+        s.qr[h][i] = h < Hq ? __bfloat162float(p.q[((int64_t)seq * Hq + h) * kMlDK + kMlC + i]) : 0.f;
+    }
+    __syncthreads();
+    uint32_t qc[kMlC / 16][4];   // A fragments of the latent query, every k-step
+    {
+        const uint32_t base = ptx::smem_addr(qls + arow * kMlQS + acol);
+#pragma unroll
+        for (int ks = 0; ks < kMlC / 16; ++ks)
+            ldsm_x4(base + 32 * ks, qc[ks]);
+    }
+
+    float o[8][4];   // output rows g, g + 8; columns 64 warp + 8 nt + 2 t4, + 1
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt)
+        o[nt][0] = o[nt][1] = o[nt][2] = o[nt][3] = 0.f;
+    float wc[4] = {0.f, 0.f, 0.f, 0.f};   // sum_j p_j u_j, columns 8 warp + 2 t4 (warps < MP / 8)
+    float m_run = -INFINITY, l_run = 0.f;  // head threadIdx.x / 16
+    const RopeParams& rp = p.rope;
+    const int ro = rp.rot_offset, rr = rp.rot_dim, half = rr / 2;
+    const uint32_t kt0 = ptx::smem_addr(&s.kt[0][0][0]);
+    constexpr uint32_t kBuf = (uint32_t)(kMlT * SM::RS * 2);   // bytes per tile buffer
+
+    int64_t pos = 0;   // tiles of the sequence before chunk c
+    for (int c = c0; c < c1; ++c) {
+        const KameraChunk& ch = p.chunks[c];
+        const int32_t bad = mla_check(ch, c, p);
+        if (bad) {
+            if (rank == 0 && threadIdx.x == 0)
+                raise_err(p.err, bad);
+            continue;
+        }
+        const int len = ch.len;
+        const int nt = (len + kMlT - 1) / kMlT;
+        const int64_t a0 = lo - pos, a1 = hi - pos;
+        const int t_lo = a0 > 0 ? (int)a0 : 0, t_hi = a1 < nt ? (int)a1 : nt;
+        pos += nt;
+        if (t_lo >= t_hi)
+            continue;
+        const int m = ch.rank;
+        __syncthreads();   // the previous chunk (or the query staging) is done with every shared array
+        mla_load<MP>(p, ch, t_lo * kMlT, min(kMlT, len - t_lo * kMlT), 0, s);   // lands while the chunk is set up
+        for (int f = threadIdx.x; f < rp.n_freq; f += kMlThreads) {
+            float cc, sn;
+            phase_cos_sin(-freq_delta(rp, ch, c, f), rp.inv_freq[f], cc, sn);
+            s.cs[f] = make_float2(cc, sn);
+        }
+        if constexpr (MP > 0) {
+            const __nv_bfloat16* vrg = patch_ptr(ch, 3) + (int64_t)p.layer * kMlR * m;   // V_r [L][rope][m]
+            for (int e = threadIdx.x; e < kMlR * MP; e += kMlThreads) {
+                const int i = e / MP, r = e - i * MP;
+                s.vr[i][r] = r < m ? __bfloat162float(vrg[i * m + r]) : 0.f;
+            }
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < kMlH * kMlR; e += kMlThreads) {   // q_rope turned by -delta
+            const int h = e / kMlR, i = e - h * kMlR, k = i - ro;
+            float v = s.qr[h][i];
+            if (k >= 0 && k < rr) {
+                if (rp.pairing == KAMERA_ROPE_ROTATE_HALF) {
+                    const float2 t = s.cs[k < half ? k : k - half];
+                    v = k < half ? fmaf(v, t.x, -(s.qr[h][i + half] * t.y)) : fmaf(v, t.x, s.qr[h][i - half] * t.y);
+                } else {
+                    const float2 t = s.cs[k >> 1];
+                    v = (k & 1) == 0 ? fmaf(v, t.x, -(s.qr[h][i + 1] * t.y)) : fmaf(v, t.x, s.qr[h][i - 1] * t.y);
+                }
+            }
+            const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+            s.xh[h][i] = hi;
+            s.xl[h][i] = __float2bfloat16_rn(v - __bfloat162float(hi));
+        }
+        if constexpr (MP > 0) {
+            for (int e = threadIdx.x; e < kMlH * MP; e += kMlThreads) {   // V_r^T q_rope (un-turned)
+                const int h = e / MP, r = e - h * MP;
+                float a0 = 0.f, a1 = 0.f;
+#pragma unroll 8
+                for (int i = 0; i < kMlR; i += 2) {
+                    a0 = fmaf(s.qr[h][i], s.vr[i][r], a0);
+                    a1 = fmaf(s.qr[h][i + 1], s.vr[i + 1][r], a1);
+                }
+                const float v = a0 + a1;
+                const __nv_bfloat16 hi = __float2bfloat16_rn(v);
+                s.xh[h][kMlR + MP + r] = hi;
+                s.xl[h][kMlR + MP + r] = __float2bfloat16_rn(v - __bfloat162float(hi));
+            }
+            if (warp < MP / 8) {   // V_c^T q_lat, columns 8 warp .. + 7, by MMA over the latent dimension
+                float y[4] = {0.f, 0.f, 0.f, 0.f};
+                const int r = 8 * warp + g;   // the B column this lane feeds
+                const uint16_t* vc =
+                    reinterpret_cast<const uint16_t*>(patch_ptr(ch, 1)) + (int64_t)p.layer * kMlC * m;
+#pragma unroll
+                for (int ks = 0; ks < kMlC / 16; ++ks) {
+                    uint32_t b0 = 0u, b1 = 0u;
+                    if (r < m) {
+                        const int i0 = 16 * ks + 2 * t4;
+                        b0 = (uint32_t)vc[i0 * m + r] | ((uint32_t)vc[(i0 + 1) * m + r] << 16);
+                        b1 = (uint32_t)vc[(i0 + 8) * m + r] | ((uint32_t)vc[(i0 + 9) * m + r] << 16);
+                    }
+                    mma_bf16(y, qc[ks], b0, b1);
+                }
+                const int col = kMlR + 8 * warp + 2 * t4;
+                uint32_t hi, lo;
+                split_hl(y[0], y[1], hi, lo);
+                *reinterpret_cast<uint32_t*>(&s.xh[g][col]) = hi;
+                *reinterpret_cast<uint32_t*>(&s.xl[g][col]) = lo;
+                split_hl(y[2], y[3], hi, lo);
+                *reinterpret_cast<uint32_t*>(&s.xh[g + 8][col]) = hi;
+                *reinterpret_cast<uint32_t*>(&s.xl[g + 8][col]) = lo;
+            }
+        }
+
+        for (int tl = t_lo; tl < t_hi; ++tl) {
+            const int b = (tl - t_lo) & 1, ntok = min(kMlT, len - tl * kMlT);
+            ptx::cp_async_wait<0>();   // this thread's copies of tile tl (the only group in flight)
+            __syncthreads();   // tile b (and, first, the chunk's query part) in place; every warp is
+                               // done with tile tl - 1, its buffer and its scores and weights
+            if (tl + 1 < t_hi)
+                mla_load<MP>(p, ch, (tl + 1) * kMlT, min(kMlT, len - (tl + 1) * kMlT), b ^ 1, s);
+            const uint32_t kb = kt0 + b * kBuf;
+            {   // scores of tokens 8 warp .. + 7 against the 16 heads (four partial sums: independent MMA chains)
+                float sa[4][4];
+#pragma unroll
+                for (int u = 0; u < 4; ++u)
+                    sa[u][0] = sa[u][1] = sa[u][2] = sa[u][3] = 0.f;
+                const uint32_t krow = kb + (uint32_t)(((8 * warp + (lane & 7)) * SM::RS + 8 * (lane >> 3)) * 2);
+#pragma unroll
+                for (int ks = 0; ks < kMlC / 16; ks += 2) {
+                    uint32_t bb[4];
+                    ldsm_x4(krow + 32 * ks, bb);
+                    mma_bf16(sa[ks & 3], qc[ks], bb[0], bb[1]);
+                    mma_bf16(sa[(ks + 1) & 3], qc[ks + 1], bb[2], bb[3]);
+                }
+                // the per-chunk part, hi and lo: k_rope (4 k-steps), then the u columns into
+                // sums 0/1 and the w columns into sums 2/3, so the padded columns of a
+                // wider instantiation add exact zeros to the same sums in the same order
+                const uint32_t xa = ptx::smem_addr(&s.xh[arow][acol]), xla = ptx::smem_addr(&s.xl[arow][acol]);
+                const uint32_t kx = krow + 32 * (kMlC / 16);
+#pragma unroll
+                for (int ks = 0; ks < kMlR / 16; ks += 2) {
+                    uint32_t bb[4], ah[4], al[4], ah2[4], al2[4];
+                    ldsm_x4(kx + 32 * ks, bb);
+                    ldsm_x4(xa + 32 * ks, ah);
+                    ldsm_x4(xla + 32 * ks, al);
+                    ldsm_x4(xa + 32 * (ks + 1), ah2);
+                    ldsm_x4(xla + 32 * (ks + 1), al2);
+                    mma_bf16(sa[0], ah, bb[0], bb[1]);
+                    mma_bf16(sa[1], al, bb[0], bb[1]);
+                    mma_bf16(sa[2], ah2, bb[2], bb[3]);
+                    mma_bf16(sa[3], al2, bb[2], bb[3]);
+                }
+#pragma unroll
+                for (int j = 0; j < 2 * (MP / 16); ++j) {
+                    const int ks = kMlR / 16 + j, q = j < MP / 16 ? 0 : 2;
+                    uint32_t bb[2], ah[4], al[4];
+                    ldsm_x2(kx + 32 * ks, bb);
+                    ldsm_x4(xa + 32 * ks, ah);
+                    ldsm_x4(xla + 32 * ks, al);
+                    mma_bf16(sa[q], ah, bb[0], bb[1]);
+                    mma_bf16(sa[q + 1], al, bb[0], bb[1]);
+                }
+                const int tk = 8 * warp + 2 * t4;
+                *reinterpret_cast<float2*>(&s.sc[g][tk]) =
+                    make_float2((sa[0][0] + sa[1][0]) + (sa[2][0] + sa[3][0]), (sa[0][1] + sa[1][1]) + (sa[2][1] + sa[3][1]));
+                *reinterpret_cast<float2*>(&s.sc[g + 8][tk]) =
+                    make_float2((sa[0][2] + sa[1][2]) + (sa[2][2] + sa[3][2]), (sa[0][3] + sa[1][3]) + (sa[2][3] + sa[3][3]));
+            }
+            __syncthreads();
+            {   // online softmax: 16 threads per head, 4 tokens each
+                const int h = threadIdx.x >> 4, j0 = 4 * (threadIdx.x & 15);
+                float sv[4], tmax = -INFINITY;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    sv[u] = j0 + u < ntok ? p.scale * s.sc[h][j0 + u] : -INFINITY;
+                    tmax = fmaxf(tmax, sv[u]);
+                }
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1)
+                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+                const float mnew = fmaxf(m_run, tmax);    // finite: the tile holds a token
+                const float alpha = __expf(m_run - mnew);  // 0 while nothing was seen
+                float e[4], sum = 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    e[u] = __expf(sv[u] - mnew);
+                    sum += e[u];
+                }
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1)
+                    sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                l_run = fmaf(l_run, alpha, sum);
+                m_run = mnew;
+                uint32_t h01, l01, h23, l23;
+                split_hl(e[0], e[1], h01, l01);
+                split_hl(e[2], e[3], h23, l23);
+                *reinterpret_cast<uint2*>(&s.ph[h][j0]) = make_uint2(h01, h23);
+                *reinterpret_cast<uint2*>(&s.pl[h][j0]) = make_uint2(l01, l23);
+                if ((threadIdx.x & 15) == 0)
+                    s.alpha[h] = alpha;
+            }
+            __syncthreads();
+            {   // O[:, 64 warp ..] += P C; sum_j p_j u_j on warps < MP / 8
+                const float a0 = s.alpha[g], a1 = s.alpha[g + 8];
+                if (!__all_sync(0xffffffffu, a0 == 1.f && a1 == 1.f)) {   // a new running max in some row
+#pragma unroll
+                    for (int nt = 0; nt < 8; ++nt) {
+                        o[nt][0] *= a0;
+                        o[nt][1] *= a0;
+                        o[nt][2] *= a1;
+                        o[nt][3] *= a1;
+                    }
+                    wc[0] *= a0;
+                    wc[1] *= a0;
+                    wc[2] *= a1;
+                    wc[3] *= a1;
+                }
+                const uint32_t pha = ptx::smem_addr(&s.ph[arow][acol]), pla = ptx::smem_addr(&s.pl[arow][acol]);
+                const uint32_t vb = kb + (uint32_t)((arow * SM::RS + 64 * warp + acol) * 2);
+                const uint32_t ub = kb + (uint32_t)((arow * SM::RS + kMlDK + 8 * warp) * 2);
+#pragma unroll
+                for (int ks = 0; ks < kMlT / 16; ++ks) {
+                    uint32_t ah[4], al[4];
+                    ldsm_x4(pha + 32 * ks, ah);
+                    ldsm_x4(pla + 32 * ks, al);
+                    const uint32_t vrow = vb + (uint32_t)(ks * 16 * SM::RS * 2);
+#pragma unroll
+                    for (int np = 0; np < 4; ++np) {
+                        uint32_t bb[4];
+                        ldsm_x4_t(vrow + 32 * np, bb);
+                        mma_bf16(o[2 * np], ah, bb[0], bb[1]);
+                        mma_bf16(o[2 * np], al, bb[0], bb[1]);
+                        mma_bf16(o[2 * np + 1], ah, bb[2], bb[3]);
+                        mma_bf16(o[2 * np + 1], al, bb[2], bb[3]);
+                    }
+                    if constexpr (MP > 0) {
+                        if (warp < MP / 8) {
+                            uint32_t bu[2];
+                            ldsm_x2_t(ub + (uint32_t)(ks * 16 * SM::RS * 2), bu);
+                            mma_bf16(wc, ah, bu[0], bu[1]);
+                            mma_bf16(wc, al, bu[0], bu[1]);
+                        }
+                    }
+                }
+            }
+        }
+        if constexpr (MP > 0) {
+            if (m > 0) {   // fold sum_j p_j u_j through V_c: O += W V_c^T
+                if (warp < MP / 8) {
+                    const int col = 8 * warp + 2 * t4;
+                    s.wsum[g][col] = wc[0];
+                    s.wsum[g][col + 1] = wc[1];
+                    s.wsum[g + 8][col] = wc[2];
+                    s.wsum[g + 8][col + 1] = wc[3];
+                }
+                __syncthreads();
+                const uint32_t* vcw =
+                    reinterpret_cast<const uint32_t*>(patch_ptr(ch, 1) + (int64_t)p.layer * kMlC * m);   // pairs (r, r+1)
+#pragma unroll
+                for (int ks = 0; ks < MP / 16; ++ks) {
+                    const int r0 = 16 * ks + 2 * t4;
+                    uint32_t ah[4], al[4];
+                    split_hl(s.wsum[g][r0], s.wsum[g][r0 + 1], ah[0], al[0]);
+                    split_hl(s.wsum[g + 8][r0], s.wsum[g + 8][r0 + 1], ah[1], al[1]);
+                    split_hl(s.wsum[g][r0 + 8], s.wsum[g][r0 + 9], ah[2], al[2]);
+                    split_hl(s.wsum[g + 8][r0 + 8], s.wsum[g + 8][r0 + 9], ah[3], al[3]);
+                    uint32_t bv[8][2];
+#pragma unroll
+                    for (int nt = 0; nt < 8; ++nt) {
+                        const int64_t i = 64 * warp + 8 * nt + g;
+                        bv[nt][0] = r0 < m ? vcw[(i * m + r0) >> 1] : 0u;
+                        bv[nt][1] = r0 + 8 < m ? vcw[(i * m + r0 + 8) >> 1] : 0u;
+                    }
+#pragma unroll
+                    for (int nt = 0; nt < 8; ++nt) {
+                        mma_bf16(o[nt], ah, bv[nt][0], bv[nt][1]);
+                        mma_bf16(o[nt], al, bv[nt][0], bv[nt][1]);
+                    }
+                }
+                wc[0] = wc[1] = wc[2] = wc[3] = 0.f;
+            }
+        }
+    }
+
+    // merge: every CTA publishes (max, sum, unnormalised output); rank 0 combines
+    __syncthreads();   // all copies have landed (the last wait took every group); the tile buffers are free
+    float* ob = reinterpret_cast<float*>(&s.kt[0][0][0]);   // [kMlH][kMlC]
+#pragma unroll
+    for (int nt = 0; nt < 8; ++nt) {
+        const int col = 64 * warp + 8 * nt + 2 * t4;
+        *reinterpret_cast<float2*>(&ob[g * kMlC + col]) = make_float2(o[nt][0], o[nt][1]);
+        *reinterpret_cast<float2*>(&ob[(g + 8) * kMlC + col]) = make_float2(o[nt][2], o[nt][3]);
+    }
+    if ((threadIdx.x & 15) == 0) {
+        s.cm[threadIdx.x >> 4] = m_run;
+        s.cl[threadIdx.x >> 4] = l_run;
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (rank == 0) {
+        if (threadIdx.x < kMlH) {
+            const int h = threadIdx.x;
+            float mx = -INFINITY;
+            for (int r = 0; r < CL; ++r)
+                mx = fmaxf(mx, *cluster.map_shared_rank(&s.cm[h], r));
+            float l = 0.f;
+            for (int r = 0; r < CL; ++r) {
+                const float mr = *cluster.map_shared_rank(&s.cm[h], r);
+                if (mr != -INFINITY)
+                    l = fmaf(*cluster.map_shared_rank(&s.cl[h], r), expf(mr - mx), l);
+            }
+            for (int r = 0; r < CL; ++r) {
+                const float mr = *cluster.map_shared_rank(&s.cm[h], r);
+                s.fac[h][r] = (mr == -INFINITY || !(l > 0.f)) ? 0.f : expf(mr - mx) / l;
+            }
+        }
+        __syncthreads();
+        for (int e = threadIdx.x; e < Hq * (kMlC / 4); e += kMlThreads) {
+            const int h = e / (kMlC / 4), i = 4 * (e - h * (kMlC / 4));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < CL; ++r) {
+                const float f = s.fac[h][r];
+                if (f == 0.f)
+                    continue;
+                const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(&ob[h * kMlC + i], r));
+                acc.x = fmaf(v.x, f, acc.x);
+                acc.y = fmaf(v.y, f, acc.y);
+                acc.z = fmaf(v.z, f, acc.z);
+                acc.w = fmaf(v.w, f, acc.w);
+            }
+            uint2 w;
+            w.x = pack_bf16x2(acc.x, acc.y);
+            w.y = pack_bf16x2(acc.z, acc.w);
+            *reinterpret_cast<uint2*>(p.out + ((int64_t)seq * Hq + h) * kMlC + i) = w;
+        }
+    }
+    cluster.sync();   // peers stay until rank 0 has read them
+}
+
+}  // namespace
+
+bool mla_attend_supported(int kv_lora, int rope_dim, int num_q_heads, int max_rank)
+{
+    return kv_lora == kMlC && rope_dim == kMlR && num_q_heads >= 1 && num_q_heads <= kMlH && max_rank >= 0 &&
+           max_rank <= 32;
+}
+
+// Cluster size.  One CTA fills an SM, and a cluster's CTAs must share a GPC, so
+// clusters of CL can leave SMs of a GPC unused: the number of clusters that fit
+// at once (the occupancy query) can fall short of the grid and push the last
+// ones into a second wave.  The CTAs of a cluster split the sequence's tiles
+// evenly, so each size (1 to 8) is costed as waves / CL and the cheapest taken
+// (ties: the smaller cluster).
+template <int MP>
+static int mla_pick_cluster(int64_t n_seqs, int bytes)
+{
+    int best = 1;
+    double best_t = 1e300;
+    for (int cl = 1; cl <= kMlMaxCL; ++cl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(n_seqs * cl));
+        cfg.blockDim = dim3(kMlThreads);
+        cfg.dynamicSmemBytes = bytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int fit = 0;
+        if (cudaOccupancyMaxActiveClusters(&fit, mla_attend_kernel<MP>, &cfg) != cudaSuccess || fit < 1) {
+            (void)cudaGetLastError();
+            continue;
+        }
+        const double t = (double)((n_seqs + fit - 1) / fit) / cl;
+        if (t < best_t * 0.999) {
+            best_t = t;
+            best = cl;
+        }
+    }
+    return best;
+}
+
+template <int MP>
+static cudaError_t launch_mla_attend_m(MlaAttendParams p, cudaStream_t stream)
+{
+    const int bytes = (int)sizeof(MlSmem<MP>);
+    cudaError_t e = cudaFuncSetAttribute(mla_attend_kernel<MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    if (e != cudaSuccess)
+        return e;
+    p.cluster = mla_pick_cluster<MP>(p.n_seqs, bytes);
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)(p.n_seqs * p.cluster));
+    cfg.blockDim = dim3(kMlThreads);
+    cfg.dynamicSmemBytes = bytes;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)p.cluster;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, mla_attend_kernel<MP>, p);
+}
+
+cudaError_t launch_mla_attend(const MlaAttendParams& p, cudaStream_t stream)
+{
+    if (p.max_rank == 0)
+        return launch_mla_attend_m<0>(p, stream);
+    return p.max_rank <= 16 ? launch_mla_attend_m<16>(p, stream) : launch_mla_attend_m<32>(p, stream);
+}
+
+}  // namespace kamera

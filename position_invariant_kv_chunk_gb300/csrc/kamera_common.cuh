@@ -113,6 +113,25 @@ struct AttendParams {
     RopeParams rope;
 };
 
+// MLA decode attention over reused chunks: one layer's latent store (rows of
+// c_KV (kv_lora) then k_rope (rope_dim)), absorbed queries (the latent part
+// then the rope part), one query token per sequence and query head.
+struct MlaAttendParams {
+    const __nv_bfloat16* kv;       // [num_rows] rows of kv_lora + rope_dim, row_stride elements apart
+    int64_t row_stride, num_rows;
+    int32_t kv_lora, rope_dim, Hq, layer;
+    const KameraChunk* chunks;     // factors Uc [L][len][m], Vc [L][kv_lora][m], Ur [L][len][m], Vr [L][rope_dim][m]
+    const int32_t* seq_start;      // [n_seqs + 1]
+    int32_t n_seqs, n_chunks;
+    const __nv_bfloat16* q;        // [n_seqs][Hq][kv_lora + rope_dim]
+    __nv_bfloat16* out;            // [n_seqs][Hq][kv_lora]
+    float scale;
+    int32_t max_len, max_rank;
+    int32_t cluster;               // CTAs per sequence, 1..8
+    int32_t* err;
+    RopeParams rope;               // rot_offset relative to k_rope
+};
+
 // ------------------------------------------------------------------ bf16 --
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

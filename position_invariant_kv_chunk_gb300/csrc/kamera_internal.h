@@ -39,6 +39,8 @@ cudaError_t launch_patch_form(const PatchFormParams& p, int64_t n_blocks, cudaSt
 bool attend_supported(int head_dim, int G, int max_rank);
 int attend_cluster(int64_t units);
 cudaError_t launch_attend(const AttendParams& p, cudaStream_t stream);
+bool mla_attend_supported(int kv_lora, int rope_dim, int num_q_heads, int max_rank);
+cudaError_t launch_mla_attend(const MlaAttendParams& p, cudaStream_t stream);   // picks p.cluster
 
 // Tensor-core path (tcgen05 MMA for the rank-m patch; relocation with rank > 0).
 bool umma_supported(const RowsParams& p, int family);

@@ -741,6 +741,83 @@ def pin_attend_per_chunk_tables(orc: O.Oracle):
                 assert np.max(np.abs(out[s, h] - want)) < 1e-9, (layout, s, h)
 
 
+def _mla_attend_problem(rng, C=32, R=16, Hq=5, lens=(9, 5, 12, 3), deltas=(40, -7, 0, 1000), m=4, seqs=(0, 2, 4),
+                        L=2, layer=1, zero_rank=False):
+    store = rand_bf16(rng, (sum(lens), C + R))
+    chunks, off = [], 0
+    for t, dl in zip(lens, deltas):
+        mm = 0 if zero_rank else m
+        pat = []
+        if mm:
+            pat = [rand_bf16(rng, (L, t, mm), .3), rand_bf16(rng, (L, C, mm), .3),
+                   rand_bf16(rng, (L, t, mm), .3), rand_bf16(rng, (L, R, mm), .3)]
+        chunks.append(O.Chunk(off, t, dl, mm, np.arange(t, dtype=np.int64), pat))
+        off += t
+    q = rand_bf16(rng, (len(seqs) - 1, Hq, C + R))
+    return store, chunks, list(seqs), q, layer
+
+
+def pin_attend_mla_is_gqa_attention(orc: O.Oracle):
+    """MLA attention is GQA attention with one KV head whose key is the whole
+    row [c_KV | k_rope] turned on k_rope only, and whose value is the same row:
+    the first kv_lora output columns agree.  The MLA factors become the key and
+    value factors [U_c | U_r] and blockdiag(V_c, V_r) of rank 2m."""
+    rng = np.random.default_rng(36)
+    C, R = 32, 16
+    for pairing in (IL, RH):
+        for zero_rank in (False, True):
+            store, chunks, seqs, q, layer = _mla_attend_problem(rng, C, R, zero_rank=zero_rank)
+            th = orc.inv_freq(1e4, R)
+            _, out, _ = orc.attend_mla(store, chunks, seqs, q, layer, C, th, R, 0, pairing)
+            gch = []
+            for c in chunks:
+                pat = []
+                if c.rank:
+                    uc, vc, ur, vr = (to_f64(a) for a in c.patches)
+                    u = np.concatenate([uc, ur], axis=2)[:, None]
+                    v = np.zeros((uc.shape[0], 1, C + R, 2 * c.rank))
+                    v[:, 0, :C, :c.rank] = vc
+                    v[:, 0, C:, c.rank:] = vr
+                    pat = [u, v, u, v]
+                gch.append(O.Chunk(c.src_offset, c.length, c.delta, 2 * c.rank, c.slots, pat))
+            rows = store[:, None, :]
+            _, gout, _ = orc.attend(rows, rows, gch, seqs, q, layer, th, R, C, pairing, scale=(C + R) ** -0.5)
+            assert np.max(np.abs(gout[..., :C] - out)) < 1e-10, (pairing, zero_rank)
+
+
+def pin_attend_mla_single_token(orc: O.Oracle):
+    """One token, no patch: every head's output is that token's c_KV row, bit for bit."""
+    rng = np.random.default_rng(37)
+    store, chunks, seqs, q, layer = _mla_attend_problem(rng, lens=(1,), deltas=(77,), seqs=(0, 1), zero_rank=True)
+    bits, _, _ = orc.attend_mla(store, chunks, seqs, q, layer, 32, orc.inv_freq(1e4, 16), 16)
+    for h in range(q.shape[1]):
+        assert np.array_equal(bits[0, h], store[0, :32])
+
+
+def pin_attend_mla_relative_position(orc: O.Oracle):
+    """Moving every chunk and the rope query by the same D changes nothing; with
+    patches, V_r turned by R(D) as well (the patch-frame identity on k_rope)."""
+    rng = np.random.default_rng(38)
+    C, R = 32, 16
+    for zero_rank in (True, False):
+        store, chunks, seqs, q, layer = _mla_attend_problem(rng, C, R, zero_rank=zero_rank)
+        th = orc.inv_freq(1e4, R)
+        _, out, _ = orc.attend_mla(store, chunks, seqs, q, layer, C, th, R, 0, IL)
+        D = 321
+        moved = []
+        for c in chunks:
+            pat = c.patches
+            if c.rank:
+                vr = to_f64(pat[3])
+                vr_t = np.swapaxes(complex_rotate(np.swapaxes(vr, -1, -2), D, th, R, 0, IL), -1, -2)
+                pat = [to_f64(pat[0]), to_f64(pat[1]), to_f64(pat[2]), vr_t]
+            moved.append(O.Chunk(c.src_offset, c.length, c.delta + D, c.rank, c.slots, pat))
+        qm = to_f64(q)
+        qm[..., C:] = complex_rotate(qm[..., C:], D, th, R, 0, IL)
+        _, out2, _ = orc.attend_mla(store, moved, seqs, qm, layer, C, th, R, 0, IL)
+        assert np.max(np.abs(out2 - out)) < 1e-9, (zero_rank, np.max(np.abs(out2 - out)))
+
+
 def pin_rejects_bad_indices(orc: O.Oracle):
     rng = np.random.default_rng(17)
     sk, sv, pk, pv, chunks = _small_gqa(rng)

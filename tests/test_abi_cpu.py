@@ -26,7 +26,8 @@ def test_header_declares_the_entry_points():
     names = declared_functions()
     for n in ("kamera_relocate_patch", "kamera_slide_inplace", "kamera_mla_relocate_patch",
               "kamera_ingest_canonical", "kamera_mla_ingest_canonical", "kamera_form_patch",
-              "kamera_attend_reused", "kamera_validate_chunks", "kamera_status_string", "kamera_abi_version"):
+              "kamera_attend_reused", "kamera_mla_attend_reused", "kamera_validate_chunks", "kamera_status_string",
+              "kamera_abi_version"):
         assert n in names
 
 
@@ -47,6 +48,7 @@ def test_struct_layouts_match_header(tmp_path):
         "KameraGqaStore": K._GqaStore, "KameraSlidePool": K._SlidePool, "KameraMlaPool": K._MlaPool,
         "KameraMlaStore": K._MlaStore, "KameraGqaStoreOut": K._GqaStore, "KameraMlaStoreOut": K._MlaStore,
         "KameraDeficit": K._Deficit, "KameraAttnKV": K._AttnKV, "KameraAttnQuery": K._AttnQuery,
+        "KameraAttnMlaKV": K._AttnMlaKV,
     }
     lines = ['#include <stdio.h>', '#include <stddef.h>', '#include "kamera.h"', 'int main(void){']
     for cname, py in structs.items():

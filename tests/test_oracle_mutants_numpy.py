@@ -2,8 +2,8 @@
 
 ``test_oracle_mutants.py`` plants mistakes in the C source; the attention and
 patch-formation oracles are numpy code in ``oracle/__init__.py``.  Each mutant
-here is a one-line textual change to the source of ``Oracle.attend`` or
-``form_patch`` (a dropped term, a flipped sign, a wrong head, a missing scale,
+here is a one-line textual change to the source of ``Oracle.attend``,
+``Oracle.attend_mla`` or ``form_patch`` (a dropped term, a flipped sign, a wrong head, a missing scale,
 the wrong end of the spectrum), compiled into a stand-in and run through the
 pins of that function; it passes the test only by failing one of them.
 """
@@ -27,6 +27,17 @@ ATTEND_MUTANTS = {
     "first_chunk_table_for_all": ("th = inv_freq[ci] if", "th = inv_freq[seq_starts[s]] if"),
 }
 
+MLA_ATTEND_MUTANTS = {
+    "c_patch_dropped": ("cl = cl + uc @ vc.T", "cl = cl"),
+    "key_c_patch_dropped": ("keys.append(np.concatenate([cl, kr], axis=1))",
+                            "keys.append(np.concatenate([sf[rows, :kv_lora], kr], axis=1))"),
+    "values_unpatched": ("lat.append(cl)", "lat.append(sf[rows, :kv_lora].copy())"),
+    "rope_patch_dropped": ("kr = kr + ur @ vr.T", "kr = kr"),
+    "delta_sign": ("self.rotate(sf[rows, kv_lora:], c.delta,", "self.rotate(sf[rows, kv_lora:], -c.delta,"),
+    "scale_dropped": ("sc = scale * (K @ qf[s, h])", "sc = K @ qf[s, h]"),
+    "softmax_not_normalised": ("pr = w / w.sum()", "pr = w"),
+}
+
 FORM_PATCH_MUTANTS = {
     "sigma_dropped": ("return w[:, :m] * s[:m], zt[:m, :].T.copy()", "return w[:, :m], zt[:m, :].T.copy()"),
     "smallest_directions": ("return w[:, :m] * s[:m], zt[:m, :].T.copy()",
@@ -38,6 +49,8 @@ FORM_PATCH_MUTANTS = {
 ATTEND_PINS = [P.pin_attend_single_token, P.pin_attend_uniform_keys, P.pin_attend_fused_identity,
                P.pin_attend_relative_position, P.pin_attend_per_chunk_tables]
 FORM_PATCH_PINS = [P.pin_form_patch_full_rank, P.pin_eckart_young]
+MLA_ATTEND_PINS = [P.pin_attend_mla_is_gqa_attention, P.pin_attend_mla_single_token,
+                   P.pin_attend_mla_relative_position]
 
 
 def _mutated(fn, old, new, env):
@@ -63,7 +76,7 @@ def orc():
 
 
 def test_unmutated_functions_pass(orc):
-    for pin in ATTEND_PINS + FORM_PATCH_PINS:
+    for pin in ATTEND_PINS + FORM_PATCH_PINS + MLA_ATTEND_PINS:
         pin(orc)
 
 
@@ -74,6 +87,15 @@ def test_attend_mutant_is_caught(name, orc):
     mut = O.Oracle()
     mut.attend = types.MethodType(fn, mut)
     assert _fails_some(ATTEND_PINS, mut), f"attend mutant {name} passed every pin"
+
+
+@pytest.mark.parametrize("name", list(MLA_ATTEND_MUTANTS))
+def test_mla_attend_mutant_is_caught(name, orc):
+    old, new = MLA_ATTEND_MUTANTS[name]
+    fn = _mutated(O.Oracle.attend_mla, old, new, vars(O))
+    mut = O.Oracle()
+    mut.attend_mla = types.MethodType(fn, mut)
+    assert _fails_some(MLA_ATTEND_PINS, mut), f"attend_mla mutant {name} passed every pin"
 
 
 @pytest.mark.parametrize("name", list(FORM_PATCH_MUTANTS))

@@ -434,7 +434,93 @@ def attend_bytes(spec: AttendSpec) -> int:
     return tok * spec.H * (2 * spec.d + 2 * spec.m) * B + nch * spec.H * 2 * spec.d * spec.m * B + 2 * q
 
 
-ATTENTION = {"qwen_attend_reused": qwen_attend_reused}
+@dataclass
+class MlaAttendSpec:
+    """MLA decode attention over reused chunks (absorbed form): ``seqs`` lists
+    each sequence's chunk lengths; every chunk has its own canonical rows
+    (c_KV | k_rope ~ N(0, 1)) in one layer's store, a delta drawn from
+    U{-dmax..dmax} and, when m > 0, factors Uc, Vc, Ur, Vr ~ N(0, 0.1^2) for ``L``
+    layers (read at ``layer``); one query token per sequence and query head
+    (latent part | rope part ~ N(0, 1)).  DeepSeek's plain RoPE pairs
+    interleaved components."""
+    name: str
+    Hq: int
+    seqs: tuple
+    m: int = 16
+    kv_lora: int = 512
+    rope: int = 64
+    L: int = 2
+    layer: int = 1
+    base: float = 1e4
+    rot_dim: int = -1          # -1: all of k_rope
+    rot_offset: int = 0
+    pairing: int = INTERLEAVED
+    dmax: int = 16384
+    zero_rank_every: int = 0   # > 0: every n-th chunk carries no patch
+    kind: str = "mla_attend"
+
+
+@dataclass
+class MlaAttendData:
+    spec: MlaAttendSpec
+    store: torch.Tensor        # [N, kv_lora + rope]
+    chunks: List["ChunkData"]
+    seq_start: List[int]
+    q: torch.Tensor            # [S, Hq, kv_lora + rope]
+
+    @property
+    def rot_dim(self) -> int:
+        return self.spec.rope if self.spec.rot_dim < 0 else self.spec.rot_dim
+
+
+def make_mla_attend(spec: MlaAttendSpec, device="cpu") -> MlaAttendData:
+    rng = _np_rng("mla_attend", spec.name, spec.Hq)
+    lens = [t for seq in spec.seqs for t in seq]
+    W = spec.kv_lora + spec.rope
+    gen = _gen(device, "mla_attend", spec.name)
+    store = _randn_bf16((max(1, sum(lens)), W), 1.0, gen, device)
+    chunks, seq_start, off, idx = [], [0], 0, 0
+    for seq in spec.seqs:
+        for t in seq:
+            m = 0 if (spec.zero_rank_every and idx % spec.zero_rank_every == spec.zero_rank_every - 1) else spec.m
+            pat = []
+            if m > 0 and t > 0:
+                pat = [_randn_bf16((spec.L, t, m), 0.1, gen, device),
+                       _randn_bf16((spec.L, spec.kv_lora, m), 0.1, gen, device),
+                       _randn_bf16((spec.L, t, m), 0.1, gen, device),
+                       _randn_bf16((spec.L, spec.rope, m), 0.1, gen, device)]
+            else:
+                m = 0
+            delta = int(rng.integers(-spec.dmax, spec.dmax + 1))
+            slots = torch.arange(max(t, 1), dtype=torch.int64, device=device)[:t]
+            chunks.append(ChunkData(off, t, delta, m, slots, pat))
+            off += t
+            idx += 1
+        seq_start.append(len(chunks))
+    q = _randn_bf16((len(spec.seqs), spec.Hq, W), 1.0, gen, device)
+    return MlaAttendData(spec, store, chunks, seq_start, q)
+
+
+def dsv2_attend_reused() -> MlaAttendSpec:
+    """A decode step over reused chunks, DeepSeek-V2-Lite shaped (16 query heads on
+    one 512 + 64 latent row, base 1e4): 38 sequences, each four of the MLA
+    workload's 4096-token chunks, rank 16 on both channels."""
+    return MlaAttendSpec("dsv2_attend_reused", Hq=16, seqs=tuple((4096,) * 4 for _ in range(38)), m=16)
+
+
+def mla_attend_bytes(spec: MlaAttendSpec) -> int:
+    """Bytes an MLA decode step must move: each token's canonical row and its two
+    U rows (2m), each patched chunk's V factors ((kv_lora + rope) m), the queries
+    read and the latent outputs written."""
+    B = 2
+    W = spec.kv_lora + spec.rope
+    tok = sum(t for seq in spec.seqs for t in seq)
+    nch = sum(1 for seq in spec.seqs for t in seq if t > 0)
+    S = len(spec.seqs)
+    return (tok * (W + 2 * spec.m) + nch * W * spec.m + S * spec.Hq * (W + spec.kv_lora)) * B
+
+
+ATTENTION = {"qwen_attend_reused": qwen_attend_reused, "dsv2_attend_reused": dsv2_attend_reused}
 
 
 # ------------------------------------------------------------- workloads --
