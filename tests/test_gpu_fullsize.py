@@ -228,3 +228,34 @@ def test_attend_fullsize_sampled():
         got = out[s:s + 1].float().cpu().numpy().astype(np.float64)
         bad = np.abs(got - ref) > _ulp_bf16(ref) + 2.0 ** -16 * mag
         assert not bad.any(), (s, int(bad.sum()))
+
+
+def test_mla_attend_fullsize_sampled():
+    """dsv2_attend_reused as bench.py times it (38 sequences x 4 chunks of 4096
+    tokens, one call, the cluster split it launches with): a seeded sample of
+    sequences against the oracle."""
+    from tests.test_gpu_attend_mla import _bits, _ulp_bf16
+    spec = W.dsv2_attend_reused()
+    a = W.make_mla_attend(spec, DEV)
+    chunks = K.pack_chunks(a.chunks, device=DEV)
+    seq = torch.tensor(a.seq_start, dtype=torch.int32, device=DEV)
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    out = K.kamera_mla_attend_reused(a.store, spec.kv_lora, a.q, K.Rope(spec.base, spec.rope, 0, spec.pairing), chunks,
+                                     seq, len(a.chunks), max(c.length for c in a.chunks), spec.m, layer=spec.layer,
+                                     err=err)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 0
+    orc = O.default()
+    th = orc.inv_freq(spec.base, spec.rope)
+    Wd = spec.kv_lora + spec.rope
+    rng = np.random.default_rng(23)
+    for s in sorted(set(int(x) for x in rng.integers(0, len(spec.seqs), 2))):
+        cs = a.chunks[a.seq_start[s]:a.seq_start[s + 1]]
+        lo, hi = cs[0].src_offset, cs[-1].src_offset + cs[-1].length
+        oc = [O.Chunk(c.src_offset - lo, c.length, c.delta, c.rank, c.slots.cpu().numpy(),
+                      [_bits(t) for t in c.patches]) for c in cs]
+        _, ref, mag = orc.attend_mla(_bits(a.store[lo:hi]), oc, [0, len(cs)], _bits(a.q[s:s + 1]), spec.layer,
+                                     spec.kv_lora, th, spec.rope, 0, spec.pairing, scale=Wd ** -0.5)
+        got = out[s:s + 1].float().cpu().numpy().astype(np.float64)
+        bad = np.abs(got - ref) > _ulp_bf16(ref) + 2.0 ** -16 * mag
+        assert not bad.any(), (s, int(bad.sum()))
