@@ -16,7 +16,8 @@
 // so each row is read once for all of them; CTA r of the cluster takes chunks
 // r, r + CL, ... of the sequence, and rank 0 merges the CL partial softmax
 // states (running max, sum, output accumulator) through distributed shared
-// memory.  CL grows (up to 8) until the grid has about four CTAs per SM.  Per chunk: the cos/sin table of -delta (fp64
+// memory.  CL (1 to 8) is chosen from the occupancy query so that the clusters
+// fill the GPU in as few waves as possible (a cluster must sit in one GPC).  Per chunk: the cos/sin table of -delta (fp64
 // phase), the turned queries and V_k^T q in shared memory.  Per 64-token tile
 // (double-buffered 16-byte async copies): the scores of all heads, four lanes
 // per token over quarters of the head dimension; then warp h keeps query
@@ -415,13 +416,53 @@ bool attend_supported(int head_dim, int G, int max_rank)
     return (head_dim == 64 || head_dim == 128) && G >= 1 && G <= kAtMaxG && max_rank >= 0 && max_rank <= 64;
 }
 
+// Cluster size.  CTA r of a cluster takes chunks r, r + CL, ... of its (sequence,
+// KV head), and a cluster's CTAs must share a GPC, so the clusters that fit at
+// once (the occupancy query) can fall short of the grid and leave a last,
+// mostly idle wave.  Each size 1..8 is costed as waves x chunks a CTA takes
+// (from the chunks a sequence has on average) and the cheapest taken (ties:
+// the smaller cluster); `fallback` if the query is unavailable.
 template <int MAXM>
-static cudaError_t launch_attend_m(const AttendParams& p, cudaStream_t stream)
+static int attend_pick_cluster(const AttendParams& p, int bytes, int fallback)
+{
+    const int64_t units = (int64_t)p.n_seqs * p.H;
+    const int64_t per_seq = p.n_seqs > 0 ? (p.n_chunks + p.n_seqs - 1) / p.n_seqs : 1;
+    int best = fallback;
+    double best_t = 1e300;
+    for (int cl = 1; cl <= 8; ++cl) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(p.n_seqs * cl), (unsigned)p.H);
+        cfg.blockDim = dim3(kAtThreads);
+        cfg.dynamicSmemBytes = bytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)cl;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        int fit = 0;
+        if (cudaOccupancyMaxActiveClusters(&fit, attend_kernel<MAXM>, &cfg) != cudaSuccess || fit < 1) {
+            (void)cudaGetLastError();
+            continue;
+        }
+        const double t = (double)((units + fit - 1) / fit) * (double)((per_seq + cl - 1) / cl);
+        if (t < best_t * 0.999) {
+            best_t = t;
+            best = cl;
+        }
+    }
+    return best;
+}
+
+template <int MAXM>
+static cudaError_t launch_attend_m(AttendParams p, cudaStream_t stream)
 {
     const int bytes = (int)sizeof(AtSmem<MAXM>);
     cudaError_t e = cudaFuncSetAttribute(attend_kernel<MAXM>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess)
         return e;
+    p.cluster = attend_pick_cluster<MAXM>(p, bytes, p.cluster);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.n_seqs * p.cluster), (unsigned)p.H);
     cfg.blockDim = dim3(kAtThreads);
@@ -437,8 +478,8 @@ static cudaError_t launch_attend_m(const AttendParams& p, cudaStream_t stream)
     return cudaLaunchKernelEx(&cfg, attend_kernel<MAXM>, p);
 }
 
-// Cluster size: the smallest power of two (at most 8) that gives the grid about
-// four CTAs per SM.
+// Default cluster size (used when the occupancy query is unavailable): the
+// smallest power of two (at most 8) that gives the grid about four CTAs per SM.
 int attend_cluster(int64_t units)
 {
     int dev = 0, sms = 0;
