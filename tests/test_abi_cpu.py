@@ -223,3 +223,32 @@ def test_axis_rope_argument_errors():
         K.Rope(1e4, 64, freq_axis=axes, axis_delta=torch.zeros(1, 3, dtype=torch.int64))._c()
     with pytest.raises(ValueError):
         K.Rope(1e4, 64, freq_axis=axes)._c()
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="host-only argument checks; run where no GPU exists")
+def test_mla_attend_argument_errors():
+    """Malformed MLA attention calls return before touching CUDA; no sequences is a no-op."""
+    store = torch.zeros(64, 576, dtype=torch.bfloat16)
+    q = torch.zeros(2, 16, 576, dtype=torch.bfloat16)
+    ch = torch.zeros(64, dtype=torch.uint8)
+    seq = torch.zeros(3, dtype=torch.int32)
+    rope = K.Rope(1e4, 64, 0, K.INTERLEAVED)
+    cases = [
+        (dict(q=torch.zeros(2, 17, 576, dtype=torch.bfloat16)), 3),      # more than 16 query heads
+        (dict(max_rank=34), 3),                                          # rank above 32
+        (dict(store=torch.zeros(64, 320, dtype=torch.bfloat16), kv_lora=256,
+              q=torch.zeros(2, 16, 320, dtype=torch.bfloat16)), 3),      # a latent width other than 512
+        (dict(store=torch.zeros(64, 580, dtype=torch.bfloat16)[:, :576]), 2),   # row stride not a multiple of 8
+        (dict(rope=_RawRope(4, np.zeros(32), 1 << 20)), 3),               # more than 3 RoPE axes
+        (dict(max_len=-1), 1),
+    ]
+    for over, status in cases:
+        a = dict(store=store, kv_lora=512, q=q, rope=rope, max_len=8, max_rank=16)
+        a.update(over)
+        with pytest.raises(K.KameraError) as e:
+            K.kamera_mla_attend_reused(a["store"], a["kv_lora"], a["q"], a["rope"], ch, seq, 1, a["max_len"],
+                                       a["max_rank"], stream=0)
+        assert e.value.status == status, (over, e.value.status)
+    out = K.kamera_mla_attend_reused(store, 512, torch.zeros(0, 16, 576, dtype=torch.bfloat16), rope, ch,
+                                     torch.zeros(1, dtype=torch.int32), 0, 8, 16, stream=0)
+    assert out.shape == (0, 16, 512)
