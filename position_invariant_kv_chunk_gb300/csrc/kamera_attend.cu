@@ -13,18 +13,23 @@
 // elements per token and KV head) and never writes a relocated row.
 //
 // A cluster of CL CTAs owns (sequence, KV head) and serves its G query heads,
-// so each row is read once for all of them; CTA r of the cluster takes chunks
-// r, r + CL, ... of the sequence, and rank 0 merges the CL partial softmax
-// states (running max, sum, output accumulator) through distributed shared
-// memory.  CL (1 to 8) is chosen from the occupancy query so that the clusters
-// fill the GPU in as few waves as possible (a cluster must sit in one GPC).  Per chunk: the cos/sin table of -delta (fp64
-// phase), the turned queries and V_k^T q in shared memory.  Per 64-token tile
-// (double-buffered 16-byte async copies): the scores of all heads, four lanes
-// per token over quarters of the head dimension; then warp h keeps query
-// head h's online softmax (running max and sum) and its output accumulator in
-// registers (head_dim / 32 columns per lane), and the chunk's sum_j p_j u'_j in
-// shared memory, folded through V_v when the chunk ends.  fp32 throughout,
-// one rounding to bf16 at the end.
+// so each row is read once for all of them.  Per 64-token tile the work is two
+// small dense products: S[G x 64] = [R(-delta) q | V_k^T q] [k | u]^T and
+// [O | W][G x (d + m)] += P [v | u'], with W = sum_j p_j u'_j folded through V_v
+// when the chunk ends.  The G query heads (padded to 16) are the rows of
+// warp-level bf16 MMAs (m16n8k16, fp32 accumulate): a decode step has at most
+// 8 query rows per KV head, far below the 64-row minimum of the tensor-memory
+// MMA.  The per-chunk query part and the softmax weights are not bf16 values,
+// so they enter as bf16 hi + lo pairs (about 16 significant bits); the rows and
+// U rows are exact bf16.  Warp w computes the scores of tokens 8w .. 8w + 7
+// and owns value-side column tiles w, w + 8, ...; the online softmax runs with
+// 16 threads per head.  Tiles are double-buffered 16-byte async copies into
+// rows padded to an odd number of 16-byte vectors, so the 8x8 matrix loads are
+// bank-conflict-free.  The CTAs of a cluster split the (sequence, head)'s tiles
+// evenly (a chunk cut between CTAs is set up by each, and each folds its own
+// share of the value patch), CL chosen from the occupancy query so the grid
+// runs in as few waves as possible (a cluster must sit in one GPC); rank 0
+// merges the partial softmax states through distributed shared memory.
 #include <cooperative_groups.h>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -38,42 +43,74 @@ namespace kamera {
 namespace {
 
 constexpr int kAtThreads = 256;
-constexpr int kAtT = 64;                  // tokens per tile
-constexpr int kAtMaxG = kAtThreads / 32;  // query heads per KV head (one warp each)
-constexpr int kAtMaxD = 128;
-constexpr int kAtKS = kAtMaxD + 8;        // tile row stride (elements): 272 bytes, spreads rows over banks
-constexpr int kAtQS = kAtMaxD + 16;       // turned-query row: 4 floats of padding per 32 columns
+constexpr int kAtT = 64;      // tokens per tile
+constexpr int kAtH = 16;      // MMA rows: a KV head's query heads, padded
+constexpr int kAtMaxG = 8;    // query heads per KV head
+constexpr int kAtMaxCL = 8;
 
-// Column i of a turned query sits at i + 4 (i / 32): the four lanes of a token,
-// which read quarter-rows 32 columns apart, then hit four different bank groups.
-__device__ __forceinline__ int qpad(int i) { return i + ((i >> 5) << 2); }
-
-// MAXM: the largest rank the instantiation takes (32: two CTAs fit an SM; 64: one).
-template <int MAXM>
-struct AtSmem {
-    float q[kAtMaxG][kAtMaxD];            // the queries (target frame)
-    float qr[kAtMaxG][kAtQS];             // turned by -delta (padded); V_v ac at a chunk's end
-    float w[kAtMaxG][MAXM];               // V_k^T q
-    float ac[kAtMaxG][MAXM];              // sum_j p_j u'_j of the current chunk (running scale)
-    float p[kAtMaxG][kAtT];               // scores, then weights, of the current tile
-    float2 cs[kAtMaxD / 2];
-    __nv_bfloat16 kt[2][kAtT][kAtKS];     // also V_k [d][m] while a chunk starts
-    __nv_bfloat16 vt[2][kAtT][kAtKS];     // also V_v^T [m][d] when a chunk ends
-    __nv_bfloat16 ukt[2][kAtT * MAXM];
-    __nv_bfloat16 uvt[2][kAtT * MAXM];
-    float cm[kAtMaxG], cl[kAtMaxG];       // this CTA's running max and sum per query head
+// D: head dim (64 or 128); MP: the padded rank the instantiation takes (0, 16, 32, 64).
+template <int D, int MP>
+struct __align__(16) AtSmem {
+    static constexpr int KW = D + MP;    // tile row: k | u (key tile), v | u' (value tile)
+    static constexpr int RS = KW + 8;    // row stride: an odd number of 16-byte vectors
+    static constexpr int NT = KW / 8;    // 8-column tiles of the value side
+    static constexpr int MPa = MP > 0 ? MP : 1;
+    __nv_bfloat16 kt[2][kAtT][RS];       // key tiles; the partial outputs at the end
+    __nv_bfloat16 vt[2][kAtT][RS];       // value tiles
+    __nv_bfloat16 xh[kAtH][RS];          // per-chunk query part R(-delta) q | V_k^T q, bf16 hi
+    __nv_bfloat16 xl[kAtH][RS];          // and lo
+    __nv_bfloat16 q[kAtH][D];            // the queries (target frame; rows past G zero)
+    float sc[kAtH][kAtT + 4];            // scores of the tile
+    __nv_bfloat16 ph[kAtH][kAtT + 8];    // softmax weights, hi
+    __nv_bfloat16 pl[kAtH][kAtT + 8];    // and lo
+    float alpha[kAtH];                   // running-max rescale of the tile
+    float2 cs[D / 2];                    // cos/sin of -delta
+    __nv_bfloat16 vk[D][MPa];            // V_k of this (layer, head), staged per chunk
+    float wsum[kAtH][MPa];               // sum_j p_j u'_j of the chunk, at its end
+    float cm[kAtH], cl[kAtH];            // this CTA's softmax state, for the merge
+    float fac[kAtH][kAtMaxCL];           // merge weights (rank 0)
 };
 
-__device__ __forceinline__ float at_warp_sum(float v)
+__device__ __forceinline__ void ldsm_x4(uint32_t a, uint32_t (&r)[4])
 {
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1)
-        v += __shfl_xor_sync(0xffffffffu, v, o);
-    return v;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(a)
+                 : "memory");
 }
-
-__device__ __forceinline__ float f2_lo(uint64_t x) { return __uint_as_float((uint32_t)x); }
-__device__ __forceinline__ float f2_hi(uint64_t x) { return __uint_as_float((uint32_t)(x >> 32)); }
+__device__ __forceinline__ void ldsm_x2(uint32_t a, uint32_t (&r)[2])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(a)
+                 : "memory");
+}
+__device__ __forceinline__ void ldsm_x2_t(uint32_t a, uint32_t (&r)[2])
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r[0]), "=r"(r[1])
+                 : "r"(a)
+                 : "memory");
+}
+// D += A B: A 16x16 (row-major fragments), B 16x8 (column fragments), fp32 D.
+__device__ __forceinline__ void mma_bf16(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+// (x, y) as bf16 pairs hi and lo with hi + lo = (x, y) to about 2^-16 relative.
+__device__ __forceinline__ void split_hl(float x, float y, uint32_t& hi, uint32_t& lo)
+{
+    hi = pack_bf16x2(x, y);
+    lo = pack_bf16x2(x - bf16lo(hi), y - bf16hi(hi));
+}
+__device__ __forceinline__ void split1(float v, __nv_bfloat16& hi, __nv_bfloat16& lo)
+{
+    hi = __float2bfloat16_rn(v);
+    lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
 
 __device__ __forceinline__ int32_t attend_check(const KameraChunk& ch, int c, const AttendParams& p)
 {
@@ -97,49 +134,78 @@ __device__ __forceinline__ int32_t attend_check(const KameraChunk& ch, int c, co
     return bits;
 }
 
-// Copies tile rows j0 .. j0 + n - 1 of chunk `ch` into buffer b.
-template <int MAXM>
+// Copies tile rows j0 .. j0 + n - 1 of chunk `ch` (KV head g) into buffer b;
+// rows past n and U columns past the rank are zero.
+template <int D, int MP>
 __device__ __forceinline__ void attend_load(const AttendParams& p, const KameraChunk& ch, int g, int j0, int n,
-                                            int b, AtSmem<MAXM>& s)
+                                            int b, AtSmem<D, MP>& s)
 {
-    const int d = p.d, vpr = d / 8, m = ch.rank;
+    constexpr int VPR = D / 8;   // 16-byte vectors of a head row
     const int64_t row0 = ch.src_offset + j0;
-    for (int e = threadIdx.x; e < n * vpr; e += kAtThreads) {
-        const int t = e / vpr, c8 = (e - t * vpr) * 8;
-        const int64_t off = (row0 + t) * p.row_stride + (int64_t)g * d + c8;
-        ptx::cp_async16(ptx::smem_addr(&s.kt[b][t][c8]), p.k + off);
-        ptx::cp_async16(ptx::smem_addr(&s.vt[b][t][c8]), p.v + off);
-    }
-    if (m > 0) {
-        const int64_t fo = ((int64_t)(p.layer * p.H + g) * ch.len + j0) * m;   // U [L][H][len][m]
-        const __nv_bfloat16* uk = patch_ptr(ch, 0) + fo;
-        const __nv_bfloat16* uv = patch_ptr(ch, 2) + fo;
-        if ((m & 7) == 0) {   // rows of whole 16-byte vectors: the tile is one contiguous run
-            for (int e = threadIdx.x; e < n * m / 8; e += kAtThreads) {
-                ptx::cp_async16(ptx::smem_addr(&s.ukt[b][8 * e]), uk + 8 * e);
-                ptx::cp_async16(ptx::smem_addr(&s.uvt[b][8 * e]), uv + 8 * e);
-            }
+    const __nv_bfloat16* kg = p.k + row0 * p.row_stride + (int64_t)g * D;
+    const __nv_bfloat16* vg = p.v + row0 * p.row_stride + (int64_t)g * D;
+    for (int e = threadIdx.x; e < kAtT * VPR; e += kAtThreads) {
+        const int t = e / VPR, v = e - t * VPR;
+        const uint32_t dk = ptx::smem_addr(&s.kt[b][t][8 * v]), dv = ptx::smem_addr(&s.vt[b][t][8 * v]);
+        if (t < n) {
+            const int64_t off = (int64_t)t * p.row_stride + 8 * v;
+            ptx::cp_async16(dk, kg + off);
+            ptx::cp_async16(dv, vg + off);
         } else {
-            for (int e = threadIdx.x; e < n * m; e += kAtThreads) {
-                s.ukt[b][e] = uk[e];
-                s.uvt[b][e] = uv[e];
+            ptx::st_shared_zero16(dk);
+            ptx::st_shared_zero16(dv);
+        }
+    }
+    if constexpr (MP > 0) {
+        const int m = ch.rank;
+        const int64_t fo = ((int64_t)(p.layer * p.H + g) * ch.len + j0) * m;   // U [L][H][len][m]
+        const __nv_bfloat16* uk = patch_ptr(ch, 0);
+        const __nv_bfloat16* uv = patch_ptr(ch, 2);
+        if ((m & 7) == 0) {   // whole 16-byte vectors (m = 0 too: all zeros)
+            constexpr int UV = MP / 8;
+            for (int e = threadIdx.x; e < kAtT * UV; e += kAtThreads) {
+                const int t = e / UV, v = e - t * UV;
+                const uint32_t dk = ptx::smem_addr(&s.kt[b][t][D + 8 * v]);
+                const uint32_t dv = ptx::smem_addr(&s.vt[b][t][D + 8 * v]);
+                if (t < n && 8 * v < m) {
+                    const int64_t off = fo + (int64_t)t * m + 8 * v;
+                    ptx::cp_async16(dk, uk + off);
+                    ptx::cp_async16(dv, uv + off);
+                } else {
+                    ptx::st_shared_zero16(dk);
+                    ptx::st_shared_zero16(dv);
+                }
+            }
+        } else {   // other ranks: element by element
+            for (int e = threadIdx.x; e < kAtT * MP; e += kAtThreads) {
+                const int t = e / MP, r = e - t * MP;
+                __nv_bfloat16 a = __float2bfloat16_rn(0.f), c = a;
+                if (t < n && r < m) {
+                    a = uk[fo + (int64_t)t * m + r];
+                    c = uv[fo + (int64_t)t * m + r];
+                }
+                s.kt[b][t][D + r] = a;
+                s.vt[b][t][D + r] = c;
             }
         }
     }
     ptx::cp_async_commit();
 }
 
-template <int MAXM>
-__global__ void __launch_bounds__(kAtThreads, MAXM <= 32 ? 2 : 1) attend_kernel(const __grid_constant__ AttendParams p)
+template <int D, int MP>
+__global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_constant__ AttendParams p)
 {
+    using SM = AtSmem<D, MP>;
+    constexpr int NTW = (SM::NT + 7) / 8;   // value-side column tiles per warp
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    AtSmem<MAXM>& s = *reinterpret_cast<AtSmem<MAXM>*>(smem_raw);
+    SM& s = *reinterpret_cast<SM*>(smem_raw);
     namespace cg = cooperative_groups;
     const int CL = p.cluster, rank = (int)(blockIdx.x % (unsigned)CL);
     const int seq = blockIdx.x / CL, g = blockIdx.y;
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int d = p.d, G = p.G, dpl = d / 32, dq = d / 4;
-    const int HQ = p.H * G;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, t4 = lane & 3;
+    const int G = p.G, HQ = p.H * G;
+    // 8x8 matrix-load addressing: A (row-major 16 x 16) and B^T (token rows)
+    const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
 
     int c0 = p.seq_start[seq], c1 = p.seq_start[seq + 1];
     if (c0 < 0 || c1 < c0 || c1 > p.n_chunks) {
@@ -147,266 +213,289 @@ __global__ void __launch_bounds__(kAtThreads, MAXM <= 32 ? 2 : 1) attend_kernel(
             raise_err(p.err, KAMERA_DEVERR_DESCRIPTOR);
         c0 = c1 = 0;
     }
-    c0 += rank;   // this CTA's chunks: c0, c0 + CL, ...
-    for (int e = threadIdx.x; e < G * d; e += kAtThreads) {
-        const int h = e / d, i = e - h * d;
-        s.q[h][i] = __bfloat162float(p.q[((int64_t)seq * HQ + g * G + h) * d + i]);
+    // this CTA's share: tiles [lo, hi) of the sequence's valid chunks' tiles, in order
+    int64_t total = 0;
+    for (int c = c0; c < c1; ++c) {
+        const KameraChunk& ch = p.chunks[c];
+        if (!attend_check(ch, c, p))
+            total += (ch.len + kAtT - 1) / kAtT;
     }
-    uint64_t acc01 = 0, acc23 = 0;   // output columns dpl*lane .. + 3 as fp32 pairs
-    float m_run = -INFINITY, l_run = 0.f;
+    const int64_t lo = total * rank / CL, hi = total * (rank + 1) / CL;
+
+    for (int e = threadIdx.x; e < kAtH * D; e += kAtThreads) {
+        const int h = e / D, i = e - h * D;
+        s.q[h][i] = h < G ? p.q[((int64_t)seq * HQ + g * G + h) * D + i] : __float2bfloat16_rn(0.f);
+    }
+
+    float o[NTW][4];   // value-side tile warp + 8 k: rows gq, gq + 8; columns 2 t4, + 1
+#pragma unroll
+    for (int k = 0; k < NTW; ++k)
+        o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+    float m_run = -INFINITY, l_run = 0.f;   // head threadIdx.x / 16
     const RopeParams& rp = p.rope;
     const int ro = rp.rot_offset, rr = rp.rot_dim, half = rr / 2;
+    const uint32_t kt0 = ptx::smem_addr(&s.kt[0][0][0]), vt0 = ptx::smem_addr(&s.vt[0][0][0]);
+    constexpr uint32_t kBuf = (uint32_t)(kAtT * SM::RS * 2);   // bytes per tile buffer
 
-    for (int c = c0; c < c1; c += CL) {
-        const KameraChunk ch = p.chunks[c];
+    int64_t pos = 0;   // tiles of the sequence before chunk c
+    for (int c = c0; c < c1; ++c) {
+        const KameraChunk& ch = p.chunks[c];
         const int32_t bad = attend_check(ch, c, p);
         if (bad) {
-            if (threadIdx.x == 0)
+            if (rank == 0 && threadIdx.x == 0)
                 raise_err(p.err, bad);
             continue;
         }
-        if (ch.len == 0)
+        const int len = ch.len;
+        const int nt = (len + kAtT - 1) / kAtT;
+        const int64_t a0 = lo - pos, a1 = hi - pos;
+        const int t_lo = a0 > 0 ? (int)a0 : 0, t_hi = a1 < nt ? (int)a1 : nt;
+        pos += nt;
+        if (t_lo >= t_hi)
             continue;
         const int m = ch.rank;
-        const int64_t fo = (int64_t)(p.layer * p.H + g) * d * m;   // this (layer, head)'s V factors
-        __syncthreads();   // the previous chunk is done with every shared array
+        __syncthreads();   // the previous chunk (or the query staging) is done with every shared array
+        attend_load<D, MP>(p, ch, g, t_lo * kAtT, min(kAtT, len - t_lo * kAtT), 0, s);   // lands during set-up
         for (int f = threadIdx.x; f < rp.n_freq; f += kAtThreads) {
             float cc, sn;
             phase_cos_sin(-freq_delta(rp, ch, c, f), rp.inv_freq[f], cc, sn);
             s.cs[f] = make_float2(cc, sn);
         }
-        __nv_bfloat16* vks = &s.kt[1][0][0];   // V_k staged in the second key buffer
-        if (m > 0) {
-            const __nv_bfloat16* vkg = patch_ptr(ch, 1) + fo;
-            for (int e = threadIdx.x; e < d * m; e += kAtThreads)
-                vks[e] = vkg[e];
+        const int64_t fo = (int64_t)(p.layer * p.H + g) * D * m;   // this (layer, head)'s V factors [d][m]
+        if constexpr (MP > 0) {
+            const __nv_bfloat16* vkg = patch_ptr(ch, 1);
+            for (int e = threadIdx.x; e < D * MP; e += kAtThreads) {
+                const int i = e / MP, r = e - i * MP;
+                s.vk[i][r] = r < m ? vkg[fo + (int64_t)i * m + r] : __float2bfloat16_rn(0.f);
+            }
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < G * d; e += kAtThreads) {   // q turned by -delta
-            const int h = e / d, i = e - h * d, k = i - ro;
-            float v = s.q[h][i];
+        for (int e = threadIdx.x; e < kAtH * D; e += kAtThreads) {   // q turned by -delta
+            const int h = e / D, i = e - h * D, k = i - ro;
+            float v = __bfloat162float(s.q[h][i]);
             if (k >= 0 && k < rr) {
                 if (rp.pairing == KAMERA_ROPE_ROTATE_HALF) {
                     const float2 t = s.cs[k < half ? k : k - half];
-                    v = k < half ? fmaf(v, t.x, -(s.q[h][i + half] * t.y)) : fmaf(v, t.x, s.q[h][i - half] * t.y);
+                    v = k < half ? fmaf(v, t.x, -(__bfloat162float(s.q[h][i + half]) * t.y))
+                                 : fmaf(v, t.x, __bfloat162float(s.q[h][i - half]) * t.y);
                 } else {
                     const float2 t = s.cs[k >> 1];
-                    v = (k & 1) == 0 ? fmaf(v, t.x, -(s.q[h][i + 1] * t.y)) : fmaf(v, t.x, s.q[h][i - 1] * t.y);
+                    v = (k & 1) == 0 ? fmaf(v, t.x, -(__bfloat162float(s.q[h][i + 1]) * t.y))
+                                     : fmaf(v, t.x, __bfloat162float(s.q[h][i - 1]) * t.y);
                 }
             }
-            s.qr[h][qpad(i)] = v;
+            split1(v, s.xh[h][i], s.xl[h][i]);
         }
-        for (int e = threadIdx.x; e < G * m; e += kAtThreads) {   // w = V_k^T q
-            const int h = e / m, r = e - h * m;
-            float a[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll 4
-            for (int i = 0; i < d; i += 4) {
+        if constexpr (MP > 0) {
+            for (int e = threadIdx.x; e < kAtH * MP; e += kAtThreads) {   // V_k^T q (the un-turned query)
+                const int h = e / MP, r = e - h * MP;
+                float u0 = 0.f, u1 = 0.f;
+#pragma unroll 8
+                for (int i = 0; i < D; i += 2) {
+                    u0 = fmaf(__bfloat162float(s.q[h][i]), __bfloat162float(s.vk[i][r]), u0);
+                    u1 = fmaf(__bfloat162float(s.q[h][i + 1]), __bfloat162float(s.vk[i + 1][r]), u1);
+                }
+                split1(u0 + u1, s.xh[h][D + r], s.xl[h][D + r]);
+            }
+        }
+
+        for (int tl = t_lo; tl < t_hi; ++tl) {
+            const int b = (tl - t_lo) & 1, ntok = min(kAtT, len - tl * kAtT);
+            ptx::cp_async_wait<0>();   // this thread's copies of tile tl (the only group in flight)
+            __syncthreads();   // tile b (and, first, the chunk's query part) in place; every warp is
+                               // done with tile tl - 1, its buffers and its scores and weights
+            if (tl + 1 < t_hi)
+                attend_load<D, MP>(p, ch, g, (tl + 1) * kAtT, min(kAtT, len - (tl + 1) * kAtT), b ^ 1, s);
+            const uint32_t kb = kt0 + b * kBuf, vb = vt0 + b * kBuf;
+            {   // scores of tokens 8 warp .. + 7 against the (padded) 16 heads; k-step ks adds
+                // its hi and lo products to sums 2 (ks & 1) and 2 (ks & 1) + 1, so a wider
+                // instantiation's padded U columns add exact zeros at the chains' ends
+                float sa[4][4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
-                    a[u] = fmaf(__bfloat162float(vks[(i + u) * m + r]), s.q[h][i + u], a[u]);
-            }
-            s.w[h][r] = (a[0] + a[1]) + (a[2] + a[3]);
-            s.ac[h][r] = 0.f;
-        }
-        __syncthreads();   // the staged V_k is read; buffer 1 may take tile 1
-        const int ntile = (ch.len + kAtT - 1) / kAtT;
-        attend_load(p, ch, g, 0, min(kAtT, ch.len), 0, s);
-        for (int tl = 0; tl < ntile; ++tl) {
-            const int b = tl & 1, ntok = min(kAtT, ch.len - tl * kAtT);
-            if (tl + 1 < ntile) {
-                attend_load(p, ch, g, (tl + 1) * kAtT, min(kAtT, ch.len - (tl + 1) * kAtT), b ^ 1, s);
-                ptx::cp_async_wait<1>();
-            } else {
-                ptx::cp_async_wait<0>();
-            }
-            __syncthreads();
-            {   // scores: warp w takes tokens 8w .. 8w + 7, four lanes per token
-                const int t = 8 * warp + (lane >> 2), qd = lane & 3;
-                uint64_t part[kAtMaxG];
+                    sa[u][0] = sa[u][1] = sa[u][2] = sa[u][3] = 0.f;
+                const uint32_t krow = kb + (uint32_t)(((8 * warp + (lane & 7)) * SM::RS + 8 * ((lane >> 3) & 1)) * 2);
+                const uint32_t xa = ptx::smem_addr(&s.xh[arow][acol]), xla = ptx::smem_addr(&s.xl[arow][acol]);
 #pragma unroll
-                for (int h = 0; h < kAtMaxG; ++h)
-                    part[h] = 0;
-                for (int i0 = qd * dq; i0 < (qd + 1) * dq; i0 += 8) {
-                    const uint4 kw = *reinterpret_cast<const uint4*>(&s.kt[b][t][i0]);
-                    const uint64_t k01 = ptx::f2_from_bf16x2(kw.x), k23 = ptx::f2_from_bf16x2(kw.y);
-                    const uint64_t k45 = ptx::f2_from_bf16x2(kw.z), k67 = ptx::f2_from_bf16x2(kw.w);
-#pragma unroll
-                    for (int h = 0; h < kAtMaxG; ++h) {
-                        if (h < G) {
-                            const uint4 a = *reinterpret_cast<const uint4*>(&s.qr[h][qpad(i0)]);
-                            const uint4 a2 = *reinterpret_cast<const uint4*>(&s.qr[h][qpad(i0) + 4]);
-                            part[h] = ptx::f2_fma(ptx::f2_make(a.x, a.y), k01, part[h]);
-                            part[h] = ptx::f2_fma(ptx::f2_make(a.z, a.w), k23, part[h]);
-                            part[h] = ptx::f2_fma(ptx::f2_make(a2.x, a2.y), k45, part[h]);
-                            part[h] = ptx::f2_fma(ptx::f2_make(a2.z, a2.w), k67, part[h]);
-                        }
-                    }
+                for (int ks = 0; ks < SM::KW / 16; ++ks) {
+                    uint32_t bb[2], ah[4], al[4];
+                    ldsm_x2(krow + 32 * ks, bb);
+                    ldsm_x4(xa + 32 * ks, ah);
+                    ldsm_x4(xla + 32 * ks, al);
+                    mma_bf16(sa[2 * (ks & 1)], ah, bb[0], bb[1]);
+                    mma_bf16(sa[2 * (ks & 1) + 1], al, bb[0], bb[1]);
                 }
-                float sc[kAtMaxG];
-#pragma unroll
-                for (int h = 0; h < kAtMaxG; ++h)
-                    sc[h] = f2_lo(part[h]) + f2_hi(part[h]);
-                if (m > 0 && t < ntok) {
-                    for (int r = qd; r < m; r += 4) {
-                        const float u = __bfloat162float(s.ukt[b][t * m + r]);
-#pragma unroll
-                        for (int h = 0; h < kAtMaxG; ++h)
-                            if (h < G)
-                                sc[h] = fmaf(s.w[h][r], u, sc[h]);
-                    }
-                }
-#pragma unroll
-                for (int h = 0; h < kAtMaxG; ++h) {
-                    sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], 1);
-                    sc[h] += __shfl_xor_sync(0xffffffffu, sc[h], 2);
-                }
-                if (qd == 0)
-#pragma unroll
-                    for (int h = 0; h < kAtMaxG; ++h)
-                        if (h < G)
-                            s.p[h][t] = t < ntok ? p.scale * sc[h] : -INFINITY;
+                const int tk = 8 * warp + 2 * t4;
+                *reinterpret_cast<float2*>(&s.sc[gq][tk]) =
+                    make_float2((sa[0][0] + sa[1][0]) + (sa[2][0] + sa[3][0]), (sa[0][1] + sa[1][1]) + (sa[2][1] + sa[3][1]));
+                *reinterpret_cast<float2*>(&s.sc[gq + 8][tk]) =
+                    make_float2((sa[0][2] + sa[1][2]) + (sa[2][2] + sa[3][2]), (sa[0][3] + sa[1][3]) + (sa[2][3] + sa[3][3]));
             }
             __syncthreads();
-            if (warp < G) {   // online softmax and P V for query head `warp`
-                const int h = warp;
-                const float s0 = s.p[h][lane], s1 = s.p[h][lane + 32];
-                float tmax = fmaxf(s0, s1);
+            {   // online softmax: 16 threads per head, 4 tokens each
+                const int h = threadIdx.x >> 4, j0 = 4 * (threadIdx.x & 15);
+                float sv[4], tmax = -INFINITY;
 #pragma unroll
-                for (int o = 16; o > 0; o >>= 1)
-                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, o));
-                const float mnew = fmaxf(m_run, tmax);
-                float alpha = 1.f, e0 = 0.f, e1 = 0.f;
-                if (mnew != -INFINITY) {
-                    alpha = expf(m_run - mnew);
-                    e0 = expf(s0 - mnew);
-                    e1 = expf(s1 - mnew);
+                for (int u = 0; u < 4; ++u) {
+                    sv[u] = j0 + u < ntok ? p.scale * s.sc[h][j0 + u] : -INFINITY;
+                    tmax = fmaxf(tmax, sv[u]);
                 }
-                s.p[h][lane] = e0;
-                s.p[h][lane + 32] = e1;
-                l_run = fmaf(l_run, alpha, at_warp_sum(e0 + e1));
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1)
+                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
+                const float mnew = fmaxf(m_run, tmax);    // finite: the tile holds a token
+                const float alpha = __expf(m_run - mnew);  // 0 while nothing was seen
+                float e[4], sum = 0.f;
+#pragma unroll
+                for (int u = 0; u < 4; ++u) {
+                    e[u] = __expf(sv[u] - mnew);
+                    sum += e[u];
+                }
+#pragma unroll
+                for (int off = 8; off > 0; off >>= 1)
+                    sum += __shfl_xor_sync(0xffffffffu, sum, off);
+                l_run = fmaf(l_run, alpha, sum);
                 m_run = mnew;
-                const uint32_t ab = __float_as_uint(alpha);
-                acc01 = ptx::f2_mul(acc01, ptx::f2_make(ab, ab));
-                acc23 = ptx::f2_mul(acc23, ptx::f2_make(ab, ab));
-                for (int r = lane; r < m; r += 32)
-                    s.ac[h][r] *= alpha;
-                __syncwarp();
-                // the weights of tokens past ntok are 0 and their stale rows are not read
-                for (int t0 = 0; t0 < ntok; t0 += 8) {
-                    float pt[8];
-                    uint2 vv[8];
+                uint32_t h01, l01, h23, l23;
+                split_hl(e[0], e[1], h01, l01);
+                split_hl(e[2], e[3], h23, l23);
+                *reinterpret_cast<uint2*>(&s.ph[h][j0]) = make_uint2(h01, h23);
+                *reinterpret_cast<uint2*>(&s.pl[h][j0]) = make_uint2(l01, l23);
+                if ((threadIdx.x & 15) == 0)
+                    s.alpha[h] = alpha;
+            }
+            __syncthreads();
+            {   // [O | W] += P [v | u']: column tiles warp, warp + 8, ...
+                const float r0 = s.alpha[gq], r1 = s.alpha[gq + 8];
+                if (!__all_sync(0xffffffffu, r0 == 1.f && r1 == 1.f)) {   // a new running max in some row
 #pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const int t = t0 + u;
-                        pt[u] = s.p[h][t];
-                        vv[u] = make_uint2(0u, 0u);
-                        if (t < ntok) {
-                            if (dpl == 4)
-                                vv[u] = *reinterpret_cast<const uint2*>(&s.vt[b][t][4 * lane]);
-                            else
-                                vv[u].x = *reinterpret_cast<const uint32_t*>(&s.vt[b][t][2 * lane]);
-                        }
-                    }
-#pragma unroll
-                    for (int u = 0; u < 8; ++u) {
-                        const uint32_t pb = __float_as_uint(pt[u]);
-                        const uint64_t pp = ptx::f2_make(pb, pb);
-                        acc01 = ptx::f2_fma(pp, ptx::f2_from_bf16x2(vv[u].x), acc01);
-                        acc23 = ptx::f2_fma(pp, ptx::f2_from_bf16x2(vv[u].y), acc23);
+                    for (int k = 0; k < NTW; ++k) {
+                        o[k][0] *= r0;
+                        o[k][1] *= r0;
+                        o[k][2] *= r1;
+                        o[k][3] *= r1;
                     }
                 }
-                for (int r = lane; r < m; r += 32) {
-                    float a = s.ac[h][r], a2 = 0.f;
-                    for (int t0 = 0; t0 < ntok; t0 += 8) {
-                        float pt[8], uu[8];
+                const uint32_t pha = ptx::smem_addr(&s.ph[arow][acol]), pla = ptx::smem_addr(&s.pl[arow][acol]);
+                const uint32_t vrow = vb + (uint32_t)(((lane & 15) * SM::RS) * 2);
 #pragma unroll
-                        for (int u = 0; u < 8; ++u) {
-                            const int t = t0 + u;
-                            pt[u] = s.p[h][t];
-                            uu[u] = t < ntok ? __bfloat162float(s.uvt[b][t * m + r]) : 0.f;
-                        }
+                for (int ks = 0; ks < kAtT / 16; ++ks) {
+                    uint32_t ah[4], al[4];
+                    ldsm_x4(pha + 32 * ks, ah);
+                    ldsm_x4(pla + 32 * ks, al);
 #pragma unroll
-                        for (int u = 0; u < 8; u += 2) {
-                            a = fmaf(pt[u], uu[u], a);
-                            a2 = fmaf(pt[u + 1], uu[u + 1], a2);
+                    for (int k = 0; k < NTW; ++k) {
+                        const int ntile = warp + 8 * k;
+                        if (ntile < SM::NT) {
+                            uint32_t bb[2];
+                            ldsm_x2_t(vrow + (uint32_t)((ks * 16 * SM::RS + 8 * ntile) * 2), bb);
+                            mma_bf16(o[k], ah, bb[0], bb[1]);
+                            mma_bf16(o[k], al, bb[0], bb[1]);
                         }
                     }
-                    s.ac[h][r] = a + a2;
                 }
             }
-            __syncthreads();   // buffer b is free for the tile after next
         }
-        if (m > 0) {   // fold sum_j p_j u'_j through V_v: qr[h][i] <- sum_r V_v[i][r] ac[h][r]
-            __nv_bfloat16* vvs = &s.vt[0][0][0];   // V_v^T staged in the first value buffer
-            const __nv_bfloat16* vvg = patch_ptr(ch, 3) + fo;
-            for (int e = threadIdx.x; e < d * m; e += kAtThreads) {
-                const int i = e / m, r = e - i * m;
-                vvs[r * d + i] = vvg[e];
-            }
-            __syncthreads();
-            for (int e = threadIdx.x; e < G * d; e += kAtThreads) {
-                const int h = e / d, i = e - h * d;
-                float a = 0.f;
-                for (int r = 0; r < m; ++r)
-                    a = fmaf(__bfloat162float(vvs[r * d + i]), s.ac[h][r], a);
-                s.qr[h][i] = a;
-            }
-            __syncthreads();
-            if (warp < G) {
-                float* f = &s.qr[warp][dpl * lane];
-                acc01 = ptx::f2_add(acc01, ptx::f2_make(__float_as_uint(f[0]), __float_as_uint(f[1])));
-                if (dpl == 4)
-                    acc23 = ptx::f2_add(acc23, ptx::f2_make(__float_as_uint(f[2]), __float_as_uint(f[3])));
+        if constexpr (MP > 0) {
+            if (m > 0) {   // fold W = sum_j p_j u'_j through V_v: O += W V_v^T
+#pragma unroll
+                for (int k = 0; k < NTW; ++k) {
+                    const int ntile = warp + 8 * k;
+                    if (ntile >= D / 8 && ntile < SM::NT) {
+                        const int col = 8 * ntile - D + 2 * t4;
+                        s.wsum[gq][col] = o[k][0];
+                        s.wsum[gq][col + 1] = o[k][1];
+                        s.wsum[gq + 8][col] = o[k][2];
+                        s.wsum[gq + 8][col + 1] = o[k][3];
+                        o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
+                    }
+                }
+                __syncthreads();
+                const __nv_bfloat16* vvg = patch_ptr(ch, 3) + fo;   // V_v [d][m]
+#pragma unroll
+                for (int ks = 0; ks < MP / 16; ++ks) {
+                    const int q0 = 16 * ks + 2 * t4;
+                    uint32_t ah[4], al[4];
+                    split_hl(s.wsum[gq][q0], s.wsum[gq][q0 + 1], ah[0], al[0]);
+                    split_hl(s.wsum[gq + 8][q0], s.wsum[gq + 8][q0 + 1], ah[1], al[1]);
+                    split_hl(s.wsum[gq][q0 + 8], s.wsum[gq][q0 + 9], ah[2], al[2]);
+                    split_hl(s.wsum[gq + 8][q0 + 8], s.wsum[gq + 8][q0 + 9], ah[3], al[3]);
+#pragma unroll
+                    for (int k = 0; k < NTW; ++k) {
+                        const int ntile = warp + 8 * k;
+                        if (ntile < D / 8) {
+                            const int64_t i = 8 * ntile + gq;
+                            const uint16_t* vr = reinterpret_cast<const uint16_t*>(vvg + i * m);
+                            const uint32_t b0 = (q0 < m ? (uint32_t)vr[q0] : 0u) |
+                                                ((q0 + 1 < m ? (uint32_t)vr[q0 + 1] : 0u) << 16);
+                            const uint32_t b1 = (q0 + 8 < m ? (uint32_t)vr[q0 + 8] : 0u) |
+                                                ((q0 + 9 < m ? (uint32_t)vr[q0 + 9] : 0u) << 16);
+                            mma_bf16(o[k], ah, b0, b1);
+                            mma_bf16(o[k], al, b0, b1);
+                        }
+                    }
+                }
             }
         }
     }
-    float r4[4] = {f2_lo(acc01), f2_hi(acc01), f2_lo(acc23), f2_hi(acc23)};
-    if (CL > 1) {   // publish this CTA's state (acc in qr), then rank 0 merges
-        cg::cluster_group cluster = cg::this_cluster();
-        __syncthreads();
-        if (warp < G) {
+
+    // merge: every CTA publishes (max, sum, unnormalised output); rank 0 combines
+    ptx::cp_async_wait<0>();
+    __syncthreads();   // the tile buffers are free
+    float* ob = reinterpret_cast<float*>(&s.kt[0][0][0]);   // [kAtH][D]
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-                if (e < dpl)
-                    s.qr[warp][dpl * lane + e] = r4[e];
-            if (lane == 0) {
-                s.cm[warp] = m_run;
-                s.cl[warp] = l_run;
-            }
+    for (int k = 0; k < NTW; ++k) {
+        const int ntile = warp + 8 * k;
+        if (ntile < D / 8) {
+            const int col = 8 * ntile + 2 * t4;
+            *reinterpret_cast<float2*>(&ob[gq * D + col]) = make_float2(o[k][0], o[k][1]);
+            *reinterpret_cast<float2*>(&ob[(gq + 8) * D + col]) = make_float2(o[k][2], o[k][3]);
         }
-        cluster.sync();
-        if (rank == 0 && warp < G) {
+    }
+    if ((threadIdx.x & 15) == 0) {
+        s.cm[threadIdx.x >> 4] = m_run;
+        s.cl[threadIdx.x >> 4] = l_run;
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (rank == 0) {
+        if (threadIdx.x < kAtH) {
+            const int h = threadIdx.x;
             float mx = -INFINITY;
             for (int r = 0; r < CL; ++r)
-                mx = fmaxf(mx, *cluster.map_shared_rank(&s.cm[warp], r));
-            float l = 0.f, o[4] = {0.f, 0.f, 0.f, 0.f};
+                mx = fmaxf(mx, *cluster.map_shared_rank(&s.cm[h], r));
+            float l = 0.f;
             for (int r = 0; r < CL; ++r) {
-                const float mr = *cluster.map_shared_rank(&s.cm[warp], r);
-                if (mr == -INFINITY)
-                    continue;
-                const float f = expf(mr - mx);
-                l = fmaf(*cluster.map_shared_rank(&s.cl[warp], r), f, l);
-                const float* ar = cluster.map_shared_rank(&s.qr[warp][dpl * lane], r);
-#pragma unroll
-                for (int e = 0; e < 4; ++e)
-                    if (e < dpl)
-                        o[e] = fmaf(ar[e], f, o[e]);
+                const float mr = *cluster.map_shared_rank(&s.cm[h], r);
+                if (mr != -INFINITY)
+                    l = fmaf(*cluster.map_shared_rank(&s.cl[h], r), expf(mr - mx), l);
             }
-            l_run = l;
-#pragma unroll
-            for (int e = 0; e < 4; ++e)
-                r4[e] = o[e];
+            for (int r = 0; r < CL; ++r) {
+                const float mr = *cluster.map_shared_rank(&s.cm[h], r);
+                s.fac[h][r] = (mr == -INFINITY || !(l > 0.f)) ? 0.f : expf(mr - mx) / l;
+            }
         }
-        cluster.sync();   // peers stay until rank 0 has read them
+        __syncthreads();
+        for (int e = threadIdx.x; e < G * (D / 4); e += kAtThreads) {
+            const int h = e / (D / 4), i = 4 * (e - h * (D / 4));
+            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            for (int r = 0; r < CL; ++r) {
+                const float f = s.fac[h][r];
+                if (f == 0.f)
+                    continue;
+                const float4 v = *reinterpret_cast<const float4*>(cluster.map_shared_rank(&ob[h * D + i], r));
+                acc.x = fmaf(v.x, f, acc.x);
+                acc.y = fmaf(v.y, f, acc.y);
+                acc.z = fmaf(v.z, f, acc.z);
+                acc.w = fmaf(v.w, f, acc.w);
+            }
+            uint2 w;
+            w.x = pack_bf16x2(acc.x, acc.y);
+            w.y = pack_bf16x2(acc.z, acc.w);
+            *reinterpret_cast<uint2*>(p.out + ((int64_t)seq * HQ + g * G + h) * D + i) = w;
+        }
     }
-    if (rank == 0 && warp < G) {
-        const float inv = l_run > 0.f ? 1.f / l_run : 0.f;
-        __nv_bfloat16* o = p.out + ((int64_t)seq * HQ + g * G + warp) * d + dpl * lane;
-#pragma unroll
-        for (int e = 0; e < 4; ++e)
-            if (e < dpl)
-                o[e] = __float2bfloat16_rn(r4[e] * inv);
-    }
+    cluster.sync();   // peers stay until rank 0 has read them
 }
 
 }  // namespace
@@ -416,20 +505,19 @@ bool attend_supported(int head_dim, int G, int max_rank)
     return (head_dim == 64 || head_dim == 128) && G >= 1 && G <= kAtMaxG && max_rank >= 0 && max_rank <= 64;
 }
 
-// Cluster size.  CTA r of a cluster takes chunks r, r + CL, ... of its (sequence,
-// KV head), and a cluster's CTAs must share a GPC, so the clusters that fit at
-// once (the occupancy query) can fall short of the grid and leave a last,
-// mostly idle wave.  Each size 1..8 is costed as waves x chunks a CTA takes
-// (from the chunks a sequence has on average) and the cheapest taken (ties:
-// the smaller cluster); `fallback` if the query is unavailable.
-template <int MAXM>
+// Cluster size.  One CTA fills an SM, and a cluster's CTAs must share a GPC, so
+// the clusters that fit at once (the occupancy query) can fall short of the
+// grid and push the last ones into another wave.  The CTAs of a cluster split
+// the (sequence, head)'s tiles evenly, so each size 1..8 is costed as
+// waves / CL and the cheapest taken (ties: the smaller cluster); `fallback` if
+// the query is unavailable.
+template <int D, int MP>
 static int attend_pick_cluster(const AttendParams& p, int bytes, int fallback)
 {
     const int64_t units = (int64_t)p.n_seqs * p.H;
-    const int64_t per_seq = p.n_seqs > 0 ? (p.n_chunks + p.n_seqs - 1) / p.n_seqs : 1;
     int best = fallback;
     double best_t = 1e300;
-    for (int cl = 1; cl <= 8; ++cl) {
+    for (int cl = 1; cl <= kAtMaxCL; ++cl) {
         cudaLaunchConfig_t cfg = {};
         cfg.gridDim = dim3((unsigned)(p.n_seqs * cl), (unsigned)p.H);
         cfg.blockDim = dim3(kAtThreads);
@@ -442,11 +530,11 @@ static int attend_pick_cluster(const AttendParams& p, int bytes, int fallback)
         cfg.attrs = attr;
         cfg.numAttrs = 1;
         int fit = 0;
-        if (cudaOccupancyMaxActiveClusters(&fit, attend_kernel<MAXM>, &cfg) != cudaSuccess || fit < 1) {
+        if (cudaOccupancyMaxActiveClusters(&fit, attend_kernel<D, MP>, &cfg) != cudaSuccess || fit < 1) {
             (void)cudaGetLastError();
             continue;
         }
-        const double t = (double)((units + fit - 1) / fit) * (double)((per_seq + cl - 1) / cl);
+        const double t = (double)((units + fit - 1) / fit) / cl;
         if (t < best_t * 0.999) {
             best_t = t;
             best = cl;
@@ -455,14 +543,14 @@ static int attend_pick_cluster(const AttendParams& p, int bytes, int fallback)
     return best;
 }
 
-template <int MAXM>
+template <int D, int MP>
 static cudaError_t launch_attend_m(AttendParams p, cudaStream_t stream)
 {
-    const int bytes = (int)sizeof(AtSmem<MAXM>);
-    cudaError_t e = cudaFuncSetAttribute(attend_kernel<MAXM>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+    const int bytes = (int)sizeof(AtSmem<D, MP>);
+    cudaError_t e = cudaFuncSetAttribute(attend_kernel<D, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess)
         return e;
-    p.cluster = attend_pick_cluster<MAXM>(p, bytes, p.cluster);
+    p.cluster = attend_pick_cluster<D, MP>(p, bytes, p.cluster);
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.n_seqs * p.cluster), (unsigned)p.H);
     cfg.blockDim = dim3(kAtThreads);
@@ -475,11 +563,23 @@ static cudaError_t launch_attend_m(AttendParams p, cudaStream_t stream)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attend_kernel<MAXM>, p);
+    return cudaLaunchKernelEx(&cfg, attend_kernel<D, MP>, p);
+}
+
+template <int D>
+static cudaError_t launch_attend_d(const AttendParams& p, cudaStream_t stream)
+{
+    if (p.max_rank == 0)
+        return launch_attend_m<D, 0>(p, stream);
+    if (p.max_rank <= 16)
+        return launch_attend_m<D, 16>(p, stream);
+    if (p.max_rank <= 32)
+        return launch_attend_m<D, 32>(p, stream);
+    return launch_attend_m<D, 64>(p, stream);
 }
 
 // Default cluster size (used when the occupancy query is unavailable): the
-// smallest power of two (at most 8) that gives the grid about four CTAs per SM.
+// smallest power of two (at most 8) that gives the grid about one CTA per SM.
 int attend_cluster(int64_t units)
 {
     int dev = 0, sms = 0;
@@ -487,14 +587,14 @@ int attend_cluster(int64_t units)
                                                   cudaSuccess || sms < 1)
         sms = 1;
     int cl = 1;
-    while (cl < 8 && units * cl < 4LL * sms)
+    while (cl < kAtMaxCL && units * cl < sms)
         cl *= 2;
     return cl;
 }
 
 cudaError_t launch_attend(const AttendParams& p, cudaStream_t stream)
 {
-    return p.max_rank <= 32 ? launch_attend_m<32>(p, stream) : launch_attend_m<64>(p, stream);
+    return p.d == 64 ? launch_attend_d<64>(p, stream) : launch_attend_d<128>(p, stream);
 }
 
 }  // namespace kamera
