@@ -1,11 +1,13 @@
 """GPU parity of decode attention over reused chunks (kamera_attend_reused)
 against the oracle's fp64 attention over the reuse equation's unrounded rows.
 
-Tolerance: the kernel computes in fp32 and rounds the output once to bf16, so
-every element must lie within one bf16 ulp of the fp64 result, plus 2^-16 of
-sum_j p_j |V_j| (the magnitude the fp32 sums are made of: where the output is
-a small difference of large terms, fp32 rounding of the terms is what moves
-it; 2^-16 is ~100 fp32 ulps of that scale)."""
+Tolerance: the kernel accumulates in fp32 on bf16 MMA operands (the canonical
+rows and U rows are bf16 already; the turned query, V_k^T q and the softmax
+weights enter as bf16 hi + lo pairs, about 16 significant bits) and rounds the
+output once to bf16, so every element must lie within one bf16 ulp of the fp64
+result, plus 2^-16 of sum_j p_j |V_j| (the magnitude the sums are made of:
+where the output is a small difference of large terms, rounding of the terms
+is what moves it)."""
 import numpy as np
 import pytest
 import torch
