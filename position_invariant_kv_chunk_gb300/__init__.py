@@ -296,6 +296,18 @@ def _check(rc: int, where: str):
         raise KameraError(rc, where)
 
 
+def _on_device(where: str, **tensors):
+    """Every tensor a compute entry point reads or writes must live in device
+    memory: a host address handed to a kernel is not a valid device address.
+    Checked wherever CUDA is present (without it no call reaches a kernel, and
+    the library's own argument checks can be exercised with host tensors)."""
+    if not torch.cuda.is_available():
+        return
+    for name, t in tensors.items():
+        if t is not None and not t.is_cuda:
+            raise ValueError(f"{where}: {name} must be a CUDA tensor")
+
+
 def _bf16(t: torch.Tensor, name: str):
     if t.dtype != torch.bfloat16:
         raise TypeError(f"{name} must be bfloat16, got {t.dtype}")
@@ -314,6 +326,8 @@ def kamera_relocate_patch(pool_k: torch.Tensor, pool_v: torch.Tensor, store_k: t
     host copy of ``chunks`` (default: the one ``pack_chunks`` attached; False:
     none, every U tile then moves by per-thread copies).
     """
+    _on_device("kamera_relocate_patch", pool_k=pool_k, pool_v=pool_v, store_k=store_k, store_v=store_v,
+               chunks=chunks, err=err)
     for t, nm in ((pool_k, "pool_k"), (pool_v, "pool_v"), (store_k, "store_k"), (store_v, "store_v")):
         _bf16(t, nm)
         if t.dim() != 4 or t.stride(3) != 1 or t.stride(2) != t.shape[3]:
@@ -341,6 +355,7 @@ def kamera_slide_inplace(pool_k: torch.Tensor, rope: Rope, chunks: torch.Tensor,
 
     pool_k: bf16 ``[L, S, H, d]`` (for MLA k_rope: ``[L, S, 1, kv_lora + rope]``
     with ``rope.rot_offset = kv_lora``)."""
+    _on_device("kamera_slide_inplace", pool_k=pool_k, chunks=chunks, err=err)
     _bf16(pool_k, "pool_k")
     if pool_k.dim() != 4 or pool_k.stride(3) != 1 or pool_k.stride(2) != pool_k.shape[3]:
         raise ValueError("pool_k must be [L, S, H, d] with packed heads")
@@ -359,6 +374,7 @@ def kamera_mla_relocate_patch(pool: torch.Tensor, store: torch.Tensor, kv_lora: 
     """MLA relocate + patch + paged scatter.  pool: bf16 ``[L, S, kv_lora + rope]``;
     store: bf16 ``[L, N, kv_lora + rope]``; rope offsets relative to k_rope;
     host_chunks as for ``kamera_relocate_patch``."""
+    _on_device("kamera_mla_relocate_patch", pool=pool, store=store, chunks=chunks, err=err)
     _bf16(pool, "pool")
     _bf16(store, "store")
     for t, nm in ((pool, "pool"), (store, "store")):
@@ -385,6 +401,8 @@ def kamera_ingest_canonical(pool_k: torch.Tensor, pool_v: torch.Tensor, store_k:
     (delta = minus the chunk's start position in the live cache), copy the values,
     and write store rows ``src_offset``.. .  pool_*: bf16 ``[L, S, H, d]``;
     store_*: bf16 ``[L, N, H, d]`` (written); rank 0 descriptors."""
+    _on_device("kamera_ingest_canonical", pool_k=pool_k, pool_v=pool_v, store_k=store_k, store_v=store_v,
+               chunks=chunks, err=err)
     for t, nm in ((pool_k, "pool_k"), (pool_v, "pool_v"), (store_k, "store_k"), (store_v, "store_v")):
         _bf16(t, nm)
         if t.dim() != 4 or t.stride(3) != 1 or t.stride(2) != t.shape[3]:
@@ -411,6 +429,7 @@ def kamera_mla_ingest_canonical(pool: torch.Tensor, store: torch.Tensor, kv_lora
     """MLA canonical ingest: c_KV copied, k_rope turned by R(delta).  pool: bf16
     ``[L, S, kv_lora + rope]``; store: bf16 ``[L, N, kv_lora + rope]`` (written);
     rope offsets relative to k_rope."""
+    _on_device("kamera_mla_ingest_canonical", pool=pool, store=store, chunks=chunks, err=err)
     _bf16(pool, "pool")
     _bf16(store, "store")
     for t, nm in ((pool, "pool"), (store, "store")):
@@ -475,6 +494,7 @@ def kamera_form_patch(delta: torch.Tensor, m: int, u: Optional[torch.Tensor] = N
     ``[T, O, I, rows, cols]`` to factor the mean over T (the orbit patch).
     u: bf16 ``[O, I, rows, m]``, v: bf16 ``[O, I, cols, m]`` (allocated when
     None), sigma: optional fp32 ``[O, I, m]``.  Returns ``(u, v)``."""
+    _on_device("kamera_form_patch", delta=delta, u=u, v=v, sigma=sigma, err=err)
     _bf16(delta, "delta")
     if delta.dim() == 4:
         delta5, t_stride = delta.unsqueeze(0), 0
@@ -516,6 +536,8 @@ def kamera_attend_reused(store_k: torch.Tensor, store_v: torch.Tensor, q: torch.
     q: bf16 ``[S, H_q, d]`` contiguous; seq_start: device int32 ``[S + 1]``;
     chunks: packed descriptors; layer: the factors' layer index; scale:
     default 1/sqrt(d).  Returns ``out`` (bf16 ``[S, H_q, d]``)."""
+    _on_device("kamera_attend_reused", store_k=store_k, store_v=store_v, q=q, chunks=chunks, seq_start=seq_start,
+               out=out, err=err)
     for t, nm in ((store_k, "store_k"), (store_v, "store_v"), (q, "q")):
         _bf16(t, nm)
     if store_k.dim() != 3 or store_k.stride(2) != 1 or store_k.stride(1) != store_k.shape[2]:
@@ -555,6 +577,7 @@ def kamera_mla_attend_reused(store: torch.Tensor, kv_lora: int, q: torch.Tensor,
     rope query); seq_start: device int32 ``[S + 1]``; rope: rot_offset
     relative to k_rope; scale: default 1/sqrt(kv_lora + rope_dim).  Returns
     ``out`` (bf16 ``[S, H_q, kv_lora]``)."""
+    _on_device("kamera_mla_attend_reused", store=store, q=q, chunks=chunks, seq_start=seq_start, out=out, err=err)
     for t, nm in ((store, "store"), (q, "q")):
         _bf16(t, nm)
     if store.dim() != 2 or store.stride(1) != 1:

@@ -252,3 +252,28 @@ def test_mla_attend_argument_errors():
     out = K.kamera_mla_attend_reused(store, 512, torch.zeros(0, 16, 576, dtype=torch.bfloat16), rope, ch,
                                      torch.zeros(1, dtype=torch.int32), 0, 8, 16, stream=0)
     assert out.shape == (0, 16, 512)
+
+
+def test_compute_calls_take_cuda_tensors_only(monkeypatch):
+    """Where CUDA is present, every tensor a compute entry point reads or writes
+    must be a CUDA tensor (a host address is not a device address); the binding
+    refuses host tensors before anything reaches the library."""
+    monkeypatch.setattr(torch.cuda, "is_available", lambda: True)
+    pk = torch.zeros(1, 16, 2, 64, dtype=torch.bfloat16)
+    sk = torch.zeros(1, 8, 2, 64, dtype=torch.bfloat16)
+    ch = torch.zeros(64, dtype=torch.uint8)
+    rope = K.Rope(1e4, 64)
+    calls = [
+        lambda: K.kamera_relocate_patch(pk, pk.clone(), sk, sk.clone(), rope, ch, 1, 8, 0, stream=0),
+        lambda: K.kamera_slide_inplace(pk, rope, ch, 1, 8, stream=0),
+        lambda: K.kamera_ingest_canonical(pk, pk.clone(), sk, sk.clone(), rope, ch, 1, 8, stream=0),
+        lambda: K.kamera_form_patch(torch.zeros(1, 1, 16, 64, dtype=torch.bfloat16), 8, stream=0),
+        lambda: K.kamera_attend_reused(sk[0], sk[0].clone(), torch.zeros(1, 2, 64, dtype=torch.bfloat16), rope, ch,
+                                       torch.zeros(2, dtype=torch.int32), 1, 8, 0, stream=0),
+        lambda: K.kamera_mla_attend_reused(torch.zeros(8, 576, dtype=torch.bfloat16), 512,
+                                           torch.zeros(1, 16, 576, dtype=torch.bfloat16), K.Rope(1e4, 64), ch,
+                                           torch.zeros(2, dtype=torch.int32), 1, 8, 0, stream=0),
+    ]
+    for call in calls:
+        with pytest.raises(ValueError, match="CUDA tensor"):
+            call()
