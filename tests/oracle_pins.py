@@ -818,6 +818,43 @@ def pin_attend_mla_relative_position(orc: O.Oracle):
         assert np.max(np.abs(out2 - out)) < 1e-9, (zero_rank, np.max(np.abs(out2 - out)))
 
 
+def pin_attend_mla_per_chunk_tables(orc: O.Oracle):
+    """MLA chunks of one sequence moved by different multi-axis amounts: attention
+    over latent rows whose k_rope is built independently at per-axis positions
+    (table RoPE at move_c[axis_f] per frequency, plus the patches) equals the
+    oracle given one table per chunk at delta 1 (0 for a chunk that does not move)."""
+    rng = np.random.default_rng(39)
+    C, R = 32, 16
+    store, chunks, seqs, q, layer = _mla_attend_problem(rng, C, R)
+    th = orc.inv_freq(1e4, R)
+    for layout in ("sections", "interleaved"):
+        axis = W.freq_axes(R // 2, layout).astype(np.int64)
+        moves = np.array([[40, 40, 40], [-7, 0, 0], [0, 0, 0], [900, -13, 250]], dtype=np.int64)
+        tabs = np.stack([mv[axis].astype(np.float64) * th for mv in moves])
+        run = [O.Chunk(c.src_offset, c.length, int(np.any(mv != 0)), c.rank, c.slots, c.patches)
+               for c, mv in zip(chunks, moves)]
+        _, out, _ = orc.attend_mla(store, run, seqs, q, layer, C, tabs, R, 0, IL)
+        sf, qf = to_f64(store), to_f64(q)
+        for s in range(len(seqs) - 1):
+            lat, keys = [], []
+            for ci in range(seqs[s], seqs[s + 1]):
+                c = chunks[ci]
+                rows = slice(c.src_offset, c.src_offset + c.length)
+                cl = sf[rows, :C]
+                kr = table_rope(sf[rows, C:], moves[ci][axis].astype(np.float64), th, IL)
+                if c.rank:
+                    uc, vc, ur, vr = (to_f64(a)[layer] for a in c.patches)
+                    cl, kr = cl + uc @ vc.T, kr + ur @ vr.T
+                lat.append(cl)
+                keys.append(np.concatenate([cl, kr], axis=1))
+            K, V = np.concatenate(keys), np.concatenate(lat)
+            for h in range(q.shape[1]):
+                sc = (K @ qf[s, h]) / np.sqrt(C + R)
+                pr = np.exp(sc - sc.max())
+                want = (pr / pr.sum()) @ V
+                assert np.max(np.abs(out[s, h] - want)) < 1e-9, (layout, s, h)
+
+
 def pin_rejects_bad_indices(orc: O.Oracle):
     rng = np.random.default_rng(17)
     sk, sv, pk, pv, chunks = _small_gqa(rng)

@@ -36,6 +36,7 @@ MLA_ATTEND_MUTANTS = {
     "delta_sign": ("self.rotate(sf[rows, kv_lora:], c.delta,", "self.rotate(sf[rows, kv_lora:], -c.delta,"),
     "scale_dropped": ("sc = scale * (K @ qf[s, h])", "sc = K @ qf[s, h]"),
     "softmax_not_normalised": ("pr = w / w.sum()", "pr = w"),
+    "first_chunk_table_for_all": ("th = inv_freq[ci] if", "th = inv_freq[seq_starts[s]] if"),
 }
 
 FORM_PATCH_MUTANTS = {
@@ -50,7 +51,7 @@ ATTEND_PINS = [P.pin_attend_single_token, P.pin_attend_uniform_keys, P.pin_atten
                P.pin_attend_relative_position, P.pin_attend_per_chunk_tables]
 FORM_PATCH_PINS = [P.pin_form_patch_full_rank, P.pin_eckart_young]
 MLA_ATTEND_PINS = [P.pin_attend_mla_is_gqa_attention, P.pin_attend_mla_single_token,
-                   P.pin_attend_mla_relative_position]
+                   P.pin_attend_mla_relative_position, P.pin_attend_mla_per_chunk_tables]
 
 
 def _mutated(fn, old, new, env):
