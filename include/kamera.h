@@ -427,8 +427,8 @@ int kamera_form_patch(const KameraDeficit* deficit, int32_t m, void* u, void* v,
  * query head; query head h reads KV head h / (num_q_heads / num_kv_heads).
  * The kernel turns the query by -delta once per chunk and folds the patch into
  * Vk^T q and Vv (sum_j p_j Uv[j]), so it reads only the store rows and the U
- * rows.  fp32 arithmetic, one bf16 rounding of the output; a sequence with no
- * token gets zeros.
+ * rows.  fp32 sums of bf16 products (hi + lo pairs for non-bf16 values), one
+ * bf16 rounding of the output; a sequence with no token gets zeros.
  *   kv      the canonical store of ONE layer: k, v bf16 [num_rows][num_kv_heads]
  *           [head_dim], rows row_stride elements apart (16-byte aligned,
  *           row_stride a multiple of 8); layer = the factors' layer index
