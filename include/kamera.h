@@ -79,7 +79,7 @@ struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
 #define KAMERA_ABI_VERSION 7
 
-/* Limits of this build. */
+/* Limits of this library. */
 #define KAMERA_MAX_RANK 128          /* largest patch rank m */
 #define KAMERA_MAX_ROT_DIM 256       /* largest rotary width (128 frequencies) */
 #define KAMERA_MAX_ROW_ELEMS 4096    /* largest head_dim (GQA) / row width (MLA) */
@@ -90,7 +90,7 @@ enum {
     KAMERA_OK = 0,
     KAMERA_ERR_INVALID_ARGUMENT = 1, /* NULL pointer, negative count or size, bad stride */
     KAMERA_ERR_MISALIGNED = 2,       /* a base pointer or stride is not 16-byte aligned */
-    KAMERA_ERR_UNSUPPORTED = 3,      /* a shape or RoPE layout this build does not handle */
+    KAMERA_ERR_UNSUPPORTED = 3,      /* a shape or RoPE layout the library does not handle */
     KAMERA_ERR_CUDA = 4              /* a CUDA launch or attribute call failed */
 };
 

@@ -165,7 +165,7 @@ const char* kamera_status_string(int status)
     case KAMERA_OK: return "ok";
     case KAMERA_ERR_INVALID_ARGUMENT: return "invalid argument";
     case KAMERA_ERR_MISALIGNED: return "pointer or stride not 16-byte aligned";
-    case KAMERA_ERR_UNSUPPORTED: return "shape or RoPE layout not supported by this build";
+    case KAMERA_ERR_UNSUPPORTED: return "shape or RoPE layout not supported by this library";
     case KAMERA_ERR_CUDA: return "CUDA launch failed";
     default: return "unknown status";
     }
