@@ -599,8 +599,8 @@ int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, c
     p.max_len = max_len;
     p.max_rank = max_rank;
     p.err = d_err;
-    p.cluster = attend_cluster((int64_t)query->n_seqs * kv->num_kv_heads);
-    if ((int64_t)query->n_seqs * p.cluster > 0x7FFFFFFF)
+    p.cluster = attend_cluster((int64_t)query->n_seqs * kv->num_kv_heads);   // the launch may pick up to 8
+    if ((int64_t)query->n_seqs * 8 > 0x7FFFFFFF)
         return KAMERA_ERR_UNSUPPORTED;
     return launch_attend(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
 }
