@@ -855,6 +855,63 @@ def pin_attend_mla_per_chunk_tables(orc: O.Oracle):
                 assert np.max(np.abs(out[s, h] - want)) < 1e-9, (layout, s, h)
 
 
+def _softmax_attend(K, V, q, scale):
+    sc = scale * (K @ q)
+    w = np.exp(sc - sc.max())
+    return (w / w.sum()) @ V
+
+
+def pin_attend_rows_are_the_row_oracle(orc: O.Oracle):
+    """The attention oracles build each chunk's rows (numpy rotation and factor
+    products) exactly as the C row oracle defines one output row of the reuse
+    equation: attention over rows taken from ``row`` (fp64 values) agrees with
+    ``attend`` (GQA) and ``attend_mla`` to 1e-10, both pairings."""
+    rng = np.random.default_rng(40)
+    for pairing in (RH, IL):
+        sk, sv, chunks, seqs, q, layer = _attend_problem(rng)
+        H, d = sk.shape[1], sk.shape[2]
+        G = q.shape[1] // H
+        th = orc.inv_freq(1e4, d)
+        _, out, _ = orc.attend(sk, sv, chunks, seqs, q, layer, th, d, 0, pairing)
+        qf = to_f64(q)
+        for s in range(len(seqs) - 1):
+            for g in range(H):
+                K, V = [], []
+                for c in chunks[seqs[s]:seqs[s + 1]]:
+                    for j in range(c.length):
+                        r = c.src_offset + j
+                        pk = pv = {}
+                        if c.rank:
+                            pk = dict(u=c.patches[0][layer, g, j], vm=c.patches[1][layer, g])
+                            pv = dict(u=c.patches[2][layer, g, j], vm=c.patches[3][layer, g])
+                        K.append(orc.row(sk[r, g], True, c.delta, th, d, 0, pairing, **pk)[1])
+                        V.append(orc.row(sv[r, g], False, 0, th, d, 0, pairing, **pv)[1])
+                for h in range(g * G, (g + 1) * G):
+                    want = _softmax_attend(np.array(K), np.array(V), qf[s, h], d ** -0.5)
+                    assert np.max(np.abs(out[s, h] - want)) < 1e-10, ("gqa", pairing, s, h)
+        C, R = 32, 16
+        store, chunks, seqs, q, layer = _mla_attend_problem(rng, C, R)
+        th = orc.inv_freq(1e4, R)
+        _, out, _ = orc.attend_mla(store, chunks, seqs, q, layer, C, th, R, 0, pairing)
+        qf = to_f64(q)
+        for s in range(len(seqs) - 1):
+            K, V = [], []
+            for c in chunks[seqs[s]:seqs[s + 1]]:
+                for j in range(c.length):
+                    r = c.src_offset + j
+                    pc = pr = {}
+                    if c.rank:
+                        pc = dict(u=c.patches[0][layer, j], vm=c.patches[1][layer])
+                        pr = dict(u=c.patches[2][layer, j], vm=c.patches[3][layer])
+                    cl = orc.row(store[r, :C], False, 0, th, R, 0, pairing, **pc)[1]
+                    kr = orc.row(store[r, C:], True, c.delta, th, R, 0, pairing, **pr)[1]
+                    K.append(np.concatenate([cl, kr]))
+                    V.append(cl)
+            for h in range(q.shape[1]):
+                want = _softmax_attend(np.array(K), np.array(V), qf[s, h], (C + R) ** -0.5)
+                assert np.max(np.abs(out[s, h] - want)) < 1e-10, ("mla", pairing, s, h)
+
+
 def pin_rejects_bad_indices(orc: O.Oracle):
     rng = np.random.default_rng(17)
     sk, sv, pk, pv, chunks = _small_gqa(rng)

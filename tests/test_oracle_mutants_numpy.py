@@ -48,10 +48,11 @@ FORM_PATCH_MUTANTS = {
 }
 
 ATTEND_PINS = [P.pin_attend_single_token, P.pin_attend_uniform_keys, P.pin_attend_fused_identity,
-               P.pin_attend_relative_position, P.pin_attend_per_chunk_tables]
+               P.pin_attend_relative_position, P.pin_attend_per_chunk_tables, P.pin_attend_rows_are_the_row_oracle]
 FORM_PATCH_PINS = [P.pin_form_patch_full_rank, P.pin_eckart_young]
 MLA_ATTEND_PINS = [P.pin_attend_mla_is_gqa_attention, P.pin_attend_mla_single_token,
-                   P.pin_attend_mla_relative_position, P.pin_attend_mla_per_chunk_tables]
+                   P.pin_attend_mla_relative_position, P.pin_attend_mla_per_chunk_tables,
+                   P.pin_attend_rows_are_the_row_oracle]
 
 
 def _mutated(fn, old, new, env):
