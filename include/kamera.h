@@ -102,7 +102,13 @@ enum {
                                       misaligned factor or slot map: chunk skipped */
     KAMERA_DEVERR_LEN = 8,         /* len > max_len: chunk skipped */
     KAMERA_DEVERR_RANK = 16,       /* rank > max_rank: chunk skipped */
-    KAMERA_DEVERR_TIMEOUT = 32     /* an internal pipeline wait gave up: results incomplete */
+    KAMERA_DEVERR_TIMEOUT = 32     /* an internal pipeline wait gave up: results incomplete
+                                      (every wait of the tensor-core kernels is bounded by
+                                      1 s; the environment variable KAMERA_WAIT_LIMIT_NS,
+                                      read at each call, overrides the bound -- a test hook:
+                                      with a bound of a few ns the kernels give up at once,
+                                      drain their own copies and MMAs, free their tensor
+                                      memory and return with this bit set) */
 };
 
 /* RoPE pairings. */
@@ -256,11 +262,13 @@ typedef struct KameraMlaStore {
  *                       read during the call.  It lets the library describe
  *                       each chunk's U factors to the tensor-memory-access
  *                       engine, which then moves the U tiles of chunks of rank
- *                       16, 32, 64 or 128 (the first 112 chunks of a call)
+ *                       16, 32, 64 or 128 (the first 104 chunks of a call)
  *                       without the copy work of a warp.  Results are the same
- *                       with or without it.  Its pointers and sizes are the ones
- *                       the copies use, so it must hold exactly d_chunks'
- *                       contents; any other contents are undefined behaviour.
+ *                       with or without it.  The device checks each such chunk
+ *                       against its device descriptor (rank, len and the two U
+ *                       addresses): a chunk whose host copy differs takes the
+ *                       copy path (the result follows d_chunks) and the call
+ *                       ORs KAMERA_DEVERR_DESCRIPTOR into *d_err.
  *   max_len, max_rank   upper bounds of len and rank over the chunks (size the
  *                       launch; larger chunks are skipped with a d_err bit)
  *   d_err               device int32 or NULL

@@ -17,6 +17,20 @@
 
 using namespace kamera;
 
+namespace kamera {
+
+uint64_t wait_limit_ns()
+{
+    const char* v = std::getenv("KAMERA_WAIT_LIMIT_NS");
+    if (!v || !*v)
+        return 1000000000ull;
+    char* end = nullptr;
+    const unsigned long long n = std::strtoull(v, &end, 10);
+    return (end && *end == '\0') ? (uint64_t)n : 1000000000ull;
+}
+
+}  // namespace kamera
+
 namespace {
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -541,6 +555,7 @@ int kamera_form_patch(const KameraDeficit* df, int32_t m, void* u, void* v, floa
     p.v = static_cast<__nv_bfloat16*>(v);
     p.sigma = sigma;
     p.err = d_err;
+    p.wait_ns = wait_limit_ns();
     return launch_patch_form(p, nb, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KAMERA_OK
                                                                                           : KAMERA_ERR_CUDA;
 }

@@ -92,6 +92,7 @@ struct PatchFormParams {
     __nv_bfloat16* v;              // [blocks][cols][m]
     float* sigma;                  // [blocks][m] or null
     int32_t* err;
+    uint64_t wait_ns;              // bound of each MMA completion wait (wait_limit_ns())
 };
 
 // Decode attention over reused chunks: one layer's canonical store, sequences

@@ -3,6 +3,7 @@
 #pragma once
 
 #include <cstddef>
+#include <cstdint>
 #include <cuda_runtime.h>
 
 #include "kamera.h"
@@ -12,6 +13,12 @@ namespace kamera {
 enum Family { FAMILY_GQA = 0, FAMILY_MLA = 1, FAMILY_SLIDE = 2 };
 
 struct RowsParams;
+
+// Bound, in ns, of the pipeline waits of the tensor-core kernels: 1 s, or the
+// value of the environment variable KAMERA_WAIT_LIMIT_NS when it is set (a
+// test hook: a short bound makes the kernels give up early and report
+// KAMERA_DEVERR_TIMEOUT).  Read on the host at each launch.
+uint64_t wait_limit_ns();
 
 // CUDA-core streaming path (any rank within the shared-memory budget).
 cudaError_t launch_simt(const RowsParams& p, int family, cudaStream_t stream);

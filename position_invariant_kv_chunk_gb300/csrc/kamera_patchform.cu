@@ -214,12 +214,12 @@ __device__ __forceinline__ uint32_t pf_piece(int r, int kc, uint32_t atom_bytes)
 
 // Thread 0 waits for the next MMA completion (bounded); the result reaches
 // every thread through the barrier that follows.
-__device__ __forceinline__ bool pf_wait_mma(PfTc& t, int32_t* err, int* s_abort)
+__device__ __forceinline__ bool pf_wait_mma(PfTc& t, int32_t* err, int* s_abort, uint64_t p_wait_ns)
 {
     if (threadIdx.x == 0) {
         const uint64_t t0 = ptx::globaltimer();
         while (!ptx::mbar_try_wait(t.bar, t.phase & 1u)) {
-            if (ptx::globaltimer() - t0 > kPfTimeoutNs) {
+            if (ptx::globaltimer() - t0 > p_wait_ns) {
                 *s_abort = 1;
                 raise_err(err, KAMERA_DEVERR_TIMEOUT);
                 break;
@@ -277,7 +277,7 @@ __device__ bool gram_tc(const PatchFormParams& p, const __nv_bfloat16* x, const 
                                      : make_uint4(0u, 0u, 0u, 0u);
             }
         }
-        if (t0 > 0 && !pf_wait_mma(t, p.err, s_abort))   // the previous tile's MMAs have read the tile
+        if (t0 > 0 && !pf_wait_mma(t, p.err, s_abort, p.wait_ns))   // the previous tile's MMAs have read the tile
             return false;
         if (threadIdx.x < items) {
             uint4 out[8];
@@ -298,7 +298,7 @@ __device__ bool gram_tc(const PatchFormParams& p, const __nv_bfloat16* x, const 
             ptx::umma_commit(t.bar);
         }
     }
-    if (!pf_wait_mma(t, p.err, s_abort))
+    if (!pf_wait_mma(t, p.err, s_abort, p.wait_ns))
         return false;
     {   // TMEM lanes are rows of G; warp w reads lanes 32 (w % 4).., columns 32 (w / 4)..
         const int i = 32 * (warp & 3) + lane, c0 = 32 * (warp >> 2);
@@ -370,7 +370,7 @@ __device__ bool u_tc(const PatchFormParams& p, const __nv_bfloat16* x, const PfS
             }
             ptx::umma_commit(t.bar);
         }
-        if (!pf_wait_mma(t, p.err, s_abort))
+        if (!pf_wait_mma(t, p.err, s_abort, p.wait_ns))
             return false;
         // TMEM lanes are tokens; warp w reads lanes 32 (w % 4).., 16-column groups g = w / 4, w / 4 + 4, ..
         const int tok = t0 + 32 * (warp & 3) + lane;
@@ -871,9 +871,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_kernel(const __grid_
         }
     }
     if (tc) {
-        if (*(volatile int*)&s_abort && threadIdx.x == 0) {   // let an MMA still in flight finish
+        // After a timeout the completion that was waited for last (index
+        // t.phase - 1) may still be pending: let that MMA finish before TMEM and
+        // the operand tiles are released (no MMA is issued after a timeout).
+        if (*(volatile int*)&s_abort && threadIdx.x == 0) {
             const uint64_t t0 = ptx::globaltimer();
-            while (!ptx::mbar_try_wait(t.bar, t.phase & 1u) && ptx::globaltimer() - t0 < kPfTimeoutNs) {
+            while (!ptx::mbar_try_wait(t.bar, (t.phase - 1u) & 1u) && ptx::globaltimer() - t0 < kPfTimeoutNs) {
             }
         }
         ptx::tc_fence_before();

@@ -71,7 +71,7 @@ constexpr uint32_t kTmemCols = 2 * kWMax;       // two accumulators
 constexpr uint64_t kTimeoutNs = 1000000000ull;
 constexpr int kTailRows = 16;                   // box height of the tail tensor maps
 constexpr int kMapChunksFew = 8;                // U map tables: calls of <= 8 chunks ...
-constexpr int kMapChunksMany = 112;             // ... and larger ones (the parameter block stays < 32 KB)
+constexpr int kMapChunksMany = 104;             // ... and larger ones (the parameter block stays < 32 KB)
 
 struct UmmaParams {
     CUtensorMap map_full[2];   // per array (K|V, or the MLA row): 64 x 128 boxes
@@ -79,23 +79,43 @@ struct UmmaParams {
     RowsParams r;
     int32_t family;
     int32_t Z;                 // row segments
+    uint64_t wait_ns;          // bound of every pipeline wait (drains keep kTimeoutNs)
 };
 
 // Per-call U tensor maps (from a host copy of the descriptors): chunk c < MC
-// with u_rank[c] == its rank > 0 has maps 2c (K or c_KV factor) and 2c+1
-// (V or k_rope factor) over its [L*FH][len][m] U array; boxes of
-// min(m, 64) ranks x 128 rows, swizzled to match the MMA operand layout.
+// with u_rank[c] > 0 has maps 2c (K or c_KV factor) and 2c+1 (V or k_rope
+// factor) over its [L*FH][len][m] U array; boxes of min(m, 64) ranks x 128
+// rows, swizzled to match the MMA operand layout.  Beside each map sit the
+// host copy's rank, length and the two U base addresses the maps were encoded
+// from: a tile moves through a map only when the device descriptor names the
+// same four values, so a host copy that disagrees with the device array can
+// never point a load at memory the descriptor does not name.
 template <int MC>
 struct UmmaLaunch {
     UmmaParams core;
     CUtensorMap map_u[2 * MC];
+    const void* u_base[MC][2];
     int32_t u_rank[MC];
+    int32_t u_len[MC];
 };
 
+// Whether chunk c's U tiles move by its tensor maps.
+static_assert(sizeof(UmmaLaunch<kMapChunksMany>) <= 32764, "kernel parameter block too large");
+
 template <int MC>
-__device__ __forceinline__ bool u_mapped(const UmmaLaunch<MC>& P, int c, int rank)
+__device__ __forceinline__ bool u_mapped(const UmmaLaunch<MC>& P, int c, const KameraChunk& ch)
 {
-    return rank > 0 && c < MC && P.u_rank[c] == rank;
+    return ch.rank > 0 && c < MC && P.u_rank[c] == ch.rank && P.u_len[c] == ch.len &&
+           P.u_base[c][0] == ch.patch_ptrs[0] && P.u_base[c][1] == ch.patch_ptrs[2];
+}
+
+// A chunk the host mapped whose device descriptor names other U factors (a
+// host copy that does not match the device array): its tiles take the copy
+// path and the call reports KAMERA_DEVERR_DESCRIPTOR.
+template <int MC>
+__device__ __forceinline__ bool u_map_stale(const UmmaLaunch<MC>& P, int c, const KameraChunk& ch)
+{
+    return c < MC && P.u_rank[c] > 0 && !u_mapped(P, c, ch);
 }
 
 template <int KA>
@@ -205,18 +225,20 @@ struct Shared {
     int64_t part[kThreads];
 };
 
-__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag, int32_t* err)
+__device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag, int32_t* err,
+                                         uint64_t limit)
 {
     if (ptx::mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = ptx::globaltimer();
+    const uint32_t every = limit < 100000u ? 0u : 63u;   // a short bound is checked at every poll
     for (uint32_t it = 1;; ++it) {
         if (ptx::mbar_try_wait(bar, parity))
             return true;
-        if ((it & 63) == 0) {
+        if ((it & every) == 0) {
             if (*abort_flag)
                 return false;
-            if (ptx::globaltimer() - t0 > kTimeoutNs) {
+            if (ptx::globaltimer() - t0 > limit) {
                 *abort_flag = 1;
                 raise_err(err, KAMERA_DEVERR_TIMEOUT);
                 return false;
@@ -227,9 +249,10 @@ __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile
 
 // The whole warp waits; a timeout seen by any lane is seen by all (the abort
 // flag reaches every polling lane), so the result is warp-uniform.
-__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag, int32_t* err)
+__device__ __forceinline__ bool warp_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag, int32_t* err,
+                                          uint64_t limit)
 {
-    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, err)) != 0;
+    return __all_sync(0xffffffffu, wait_bar(bar, parity, abort_flag, err, limit)) != 0;
 }
 
 // time-bounded wait that ignores the abort flag (used while draining)
@@ -566,7 +589,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
         uint32_t upar = 0, uload = 0;   // per U buffer: phase parity of its TMA loads; last use was a TMA load
         for (int i = 0; i < count; ++i, cur.next(p)) {
             const int s = i % G::S, rnd = i / G::S;
-            if (!warp_wait(ptx::smem_addr(&sh.empty[s]), (rnd & 1) ^ 1, abort_flag, r.err))
+            if (!warp_wait(ptx::smem_addr(&sh.empty[s]), (rnd & 1) ^ 1, abort_flag, r.err, p.wait_ns))
                 break;
             const int l = cur.lz / p.Z, z = cur.lz - l * p.Z;
             const Seg sg = segment(p, z);
@@ -595,10 +618,12 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                 if (lane == 0)
                     sh.stage_tag[s] = cur.c;
             }
+            if (cur.t == 0 && lane == 0 && u_map_stale(P, cur.c, ch))
+                raise_err(r.err, KAMERA_DEVERR_DESCRIPTOR);
             if (ch.rank > 0) {   // U tile of a mapped chunk: one or two swizzled boxes into the U ring
                 const int u = pu % G::D;
-                if (u_mapped(P, cur.c, ch.rank)) {
-                    if (!warp_wait(ptx::smem_addr(&sh.uempty[u]), ((pu / G::D) & 1) ^ 1, abort_flag, r.err))
+                if (u_mapped(P, cur.c, ch)) {
+                    if (!warp_wait(ptx::smem_addr(&sh.uempty[u]), ((pu / G::D) & 1) ^ 1, abort_flag, r.err, p.wait_ns))
                         break;
                     if (lane == 0) {
                         const int nbox = ch.rank > 64 ? 2 : 1;
@@ -682,7 +707,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                     if (new_job) {
                         ++ld_v;
                         if (!warp_wait(ptx::smem_addr(&sh.vmempty[ld_v & 1]), ((ld_v >> 1) & 1) ^ 1, abort_flag,
-                                       r.err))
+                                       r.err, p.wait_ns))
                             stop = true;
                         else
                             load_operand(vbase + (ld_v & 1) * G::kVBytes,
@@ -691,9 +716,9 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                                          sg.w, m, mpad, (uint32_t)sg.w * 128u, lane);
                     }
                     const int u = ld_u % G::D;
-                    const bool by_tma = u_mapped(P, ld.c, m);   // the producer loads this U tile
+                    const bool by_tma = u_mapped(P, ld.c, ch);   // the producer loads this U tile
                     if (!by_tma && !stop &&
-                        !warp_wait(ptx::smem_addr(&sh.uempty[u]), ((ld_u / G::D) & 1) ^ 1, abort_flag, r.err))
+                        !warp_wait(ptx::smem_addr(&sh.uempty[u]), ((ld_u / G::D) & 1) ^ 1, abort_flag, r.err, p.wait_ns))
                         stop = true;
                     if (!by_tma && !stop) {
                         const int tok0 = ld.t * kTileM;
@@ -724,20 +749,20 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             plz = cur.lz;
             pc = cur.c;
             const int lz_now = cur.lz, c_now = cur.c;
+            const bool by_tma = u_mapped(P, c_now, cur.ch);
             cur.next(p);
             const bool last_of_job = (i == count - 1) || cur.lz != lz_now || cur.c != c_now;
             if (m > 0) {
                 if (new_job)
                     ++vjob;
-                const bool by_tma = u_mapped(P, c_now, m);
                 if (lane == 0) {
                     const int acc = k & 1, u = k % G::D;
                     bool ok = true;
                     if (by_tma) {
-                        ok = wait_bar(ptx::smem_addr(&sh.ufull[u]), (upar >> u) & 1u, abort_flag, r.err);
+                        ok = wait_bar(ptx::smem_addr(&sh.ufull[u]), (upar >> u) & 1u, abort_flag, r.err, p.wait_ns);
                         upar ^= 1u << u;
                     }
-                    if (!ok || !wait_bar(ptx::smem_addr(&sh.tempty[acc]), ((k >> 1) & 1) ^ 1, abort_flag, r.err)) {
+                    if (!ok || !wait_bar(ptx::smem_addr(&sh.tempty[acc]), ((k >> 1) & 1) ^ 1, abort_flag, r.err, p.wait_ns)) {
                         stop = true;
                     } else {
                         ptx::tc_fence_after();
@@ -785,7 +810,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
         int k = 0;
         for (int i = 0; i < count; ++i) {
             const int s = i % G::S, rnd = i / G::S;
-            if (!warp_wait(ptx::smem_addr(&sh.full[s]), rnd & 1, abort_flag, r.err))
+            if (!warp_wait(ptx::smem_addr(&sh.full[s]), rnd & 1, abort_flag, r.err, p.wait_ns))
                 break;
             const TileInfo ti = sh.tinfo[s];   // the producer's description of the tile in this stage
             const int l = ti.l, m = ti.m, ntok = ti.ntok;
@@ -793,7 +818,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             const Seg sg = segment(p, ti.z);
             const int acc = k & 1;
             if (m > 0) {
-                if (!warp_wait(ptx::smem_addr(&sh.tfull[acc]), (k >> 1) & 1, abort_flag, r.err))
+                if (!warp_wait(ptx::smem_addr(&sh.tfull[acc]), (k >> 1) & 1, abort_flag, r.err, p.wait_ns))
                     break;
                 ptx::tc_fence_after();
             }
@@ -969,8 +994,12 @@ cudaError_t launch_kernel(const UmmaParams& core, const KameraChunk* h_chunks, i
             if ((m != 16 && m != 32 && m != 64 && m != 128) || m > rp.max_rank || ch.len < 1)
                 continue;
             if (make_u_map(&local.map_u[2 * c], ch.patch_ptrs[0], planes, ch.len, m) &&
-                make_u_map(&local.map_u[2 * c + 1], ch.patch_ptrs[2], planes, ch.len, m))
+                make_u_map(&local.map_u[2 * c + 1], ch.patch_ptrs[2], planes, ch.len, m)) {
                 local.u_rank[c] = m;
+                local.u_len[c] = ch.len;
+                local.u_base[c][0] = ch.patch_ptrs[0];
+                local.u_base[c][1] = ch.patch_ptrs[2];
+            }
         }
     }
     const size_t smem = smem_bytes_for<KA>();
@@ -991,6 +1020,7 @@ cudaError_t launch_umma(const RowsParams& rp, int family, const KameraChunk* h_c
     p.r = rp;
     p.family = family;
     p.Z = family == FAMILY_GQA ? 2 * rp.H : rp.kv_lora / kWMax + 1;
+    p.wait_ns = wait_limit_ns();
     const int64_t width = family == FAMILY_GQA ? (int64_t)rp.H * rp.d : rp.d;
     const void* arrays[2] = {rp.src_k, family == FAMILY_GQA ? rp.src_v : rp.src_k};
     for (int a = 0; a < 2; ++a) {

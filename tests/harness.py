@@ -33,25 +33,60 @@ def u16(t: torch.Tensor) -> np.ndarray:
     return t.detach().contiguous().view(torch.int16).cpu().numpy().view(np.uint16)
 
 
+def _ordered_table() -> np.ndarray:
+    b = np.arange(65536, dtype=np.int32)
+    return np.where(b & 0x8000, -(b & 0x7FFF), b).astype(np.int32)
+
+
+_ORDERED = _ordered_table()
+
+
 def ordered(bits: np.ndarray) -> np.ndarray:
-    b = bits.astype(np.int32)
-    return np.where(b & 0x8000, -(b & 0x7FFF), b)
+    """bf16 bit patterns -> integers whose differences count representable steps
+    (+0 and -0 both map to 0)."""
+    return _ORDERED[np.asarray(bits, dtype=np.uint16)]
 
 
 def to_f64(bits: np.ndarray) -> np.ndarray:
     return (bits.astype(np.uint32) << 16).view(np.float32).astype(np.float64)
 
 
+def to_f32(bits: np.ndarray) -> np.ndarray:
+    return (bits.astype(np.uint32) << 16).view(np.float32)
+
+
 @dataclass
 class Stats:
-    n: int
-    over_1ulp: int
-    cancellation: int
-    max_ulp: int
-    worst_frob: float
+    """Outcome of one comparison (or of several, summed with +): elements
+    compared, elements beyond 1 ulp (every one accepted as cancellation, see
+    above; compare raises otherwise), the largest ulp distance and the worst
+    relative Frobenius error of a (layer, head) block."""
+    n: int = 0
+    cancellation: int = 0
+    max_ulp: int = 0
+    worst_frob: float = 0.0
 
-    def ok(self) -> bool:
-        return True
+    def __add__(self, o: "Stats") -> "Stats":
+        return Stats(self.n + o.n, self.cancellation + o.cancellation, max(self.max_ulp, o.max_ulp),
+                     max(self.worst_frob, o.worst_frob))
+
+    def line(self, what: str) -> str:
+        return (f"{what}: {self.n} elements, {self.cancellation} beyond 1 ulp (cancellation, scale-relative "
+                f"pass), max {self.max_ulp} ulp, worst block Frobenius {self.worst_frob:.2e}")
+
+
+# Lines the GPU parity tests record; tests/conftest.py prints them at the end of
+# the session (the count of elements beyond 1 ulp per case).
+REPORT = []
+
+
+def report(what: str, stats) -> None:
+    if isinstance(stats, Stats):
+        stats = [stats]
+    tot = Stats()
+    for st in stats:
+        tot = tot + st
+    REPORT.append(tot.line(what))
 
 
 def compare(gpu: np.ndarray, ref: np.ndarray, scale: np.ndarray, block_axes=None, what="") -> Stats:
@@ -70,14 +105,17 @@ def compare(gpu: np.ndarray, ref: np.ndarray, scale: np.ndarray, block_axes=None
         assert n_over <= 1e-4 * gpu.size + 2, f"{what}: {n_over} of {gpu.size} elements beyond 1 ulp"
     worst = 0.0
     if block_axes is not None:
-        g = to_f64(gpu)
-        r = to_f64(ref)
-        num = np.sqrt(((g - r) ** 2).sum(axis=block_axes))
-        den = np.sqrt((r ** 2).sum(axis=block_axes))
+        # bf16 -> fp32 is exact, and so is the difference of two bf16 values in
+        # fp32 (their exponents differ by far less than 16 here); squares and
+        # sums in fp64
+        g = to_f32(gpu)
+        r = to_f32(ref)
+        num = np.sqrt(np.square(g - r, dtype=np.float64).sum(axis=block_axes))
+        den = np.sqrt(np.square(r, dtype=np.float64).sum(axis=block_axes))
         rel = np.where(den > 0, num / np.where(den > 0, den, 1), num)
         worst = float(rel.max()) if rel.size else 0.0
         assert worst <= 4e-3, f"{what}: relative Frobenius error {worst:.3g} > 4e-3"
-    return Stats(gpu.size, n_over, n_over, int(d.max()) if d.size else 0, worst)
+    return Stats(gpu.size, n_over, int(d.max()) if d.size else 0, worst)
 
 
 # ------------------------------------------------------------- execution
@@ -285,3 +323,80 @@ def check_parity(wl: W.Workload, h: HostCopy, what: str):
         assert np.array_equal(gv[:, ~touched], h.pool_v[:, ~touched]), f"{what}: untouched V slots changed"
         stats.append(compare(gv[:, touched], ov[:, touched], sv[:, touched], block_axes=(1, 3), what=what + " V"))
     return stats
+
+
+# ------------------------------------------------ whole outputs, layer by layer
+def _layer_chunks(wl: W.Workload, l: int, slots):
+    """The chunks with their factors cut to layer l (host copies)."""
+    out = []
+    for c, s in zip(wl.chunks, slots):
+        out.append(O.Chunk(c.src_offset, c.length, c.delta, c.rank, s,
+                           [u16(p[l:l + 1]) for p in c.patches] if c.rank else []))
+    return out
+
+
+def check_layers(wl: W.Workload, layers, what: str, pool_before: torch.Tensor = None, workers: int = 8):
+    """Every output row of the given layers against the oracle, after one GPU
+    call over the whole workload (the launch under test).  Layer by layer: the
+    layer's store rows, factors and pool are copied to the host, the oracle
+    computes the layer (the pools start as canary, or as ``pool_before`` for
+    the in-place slide), and every targeted slot is compared element by
+    element, with the Frobenius bound per (layer, head) block, while every
+    other slot must keep its bytes.  Comparisons run in worker threads while
+    the oracle computes the next layer.  Returns the summed Stats per array."""
+    from concurrent.futures import ThreadPoolExecutor
+    if wl.pool_k.is_cuda:
+        torch.cuda.synchronize()
+    orc = O.default()
+    th = theta_of(wl, orc)
+    slots = [c.slots.detach().cpu().numpy().astype(np.int64) for c in wl.chunks]
+    S = wl.pool_k.shape[1]
+    touched = np.zeros(S, dtype=bool)
+    if slots:
+        touched[np.concatenate(slots)] = True
+    canary = np.uint16(W.CANARY_BITS)
+
+    def cmp(tag, l, got, want, scale, before, axes, split=None):
+        assert np.array_equal(got[:, ~touched], before[:, ~touched]), f"{what} {tag} layer {l}: untouched slots changed"
+        g, r, s = got[:, touched], want[:, touched], scale[:, touched]
+        if split is None:
+            return {tag: compare(g, r, s, block_axes=axes, what=f"{what} {tag} layer {l}")}
+        return {f"{tag} c_KV": compare(g[..., :split], r[..., :split], s[..., :split], block_axes=axes,
+                                       what=f"{what} c_KV layer {l}"),
+                f"{tag} k_rope": compare(g[..., split:], r[..., split:], s[..., split:], block_axes=axes,
+                                         what=f"{what} k_rope layer {l}")}
+
+    totals = {}
+    pending = []
+
+    def collect(block):
+        while len(pending) > block:
+            for k, st in pending.pop(0).result().items():
+                totals[k] = totals.get(k, Stats()) + st
+
+    with ThreadPoolExecutor(max_workers=workers) as ex:
+        for l in layers:
+            ch = _layer_chunks(wl, l, slots)
+            if wl.kind == "gqa":
+                pk = np.full((1,) + tuple(wl.pool_k.shape[1:]), canary, dtype=np.uint16)
+                pv = pk.copy()
+                sk, sv = orc.gqa(u16(wl.store_k[l:l + 1]), u16(wl.store_v[l:l + 1]), pk, pv, ch, th, wl.rot_dim,
+                                 wl.rot_offset, wl.pairing, want_scale=True)
+                canaries = np.full_like(pk, canary)
+                pending.append(ex.submit(cmp, "K", l, u16(wl.pool_k[l:l + 1]), pk, sk, canaries, (1, 3)))
+                pending.append(ex.submit(cmp, "V", l, u16(wl.pool_v[l:l + 1]), pv, sv, canaries, (1, 3)))
+            elif wl.kind == "mla":
+                pk = np.full((1,) + tuple(wl.pool_k.shape[1:]), canary, dtype=np.uint16)
+                sk = orc.mla(u16(wl.store_k[l:l + 1]), pk, ch, wl.kv_lora, th, wl.pairing, want_scale=True)
+                pending.append(ex.submit(cmp, "row", l, u16(wl.pool_k[l:l + 1]), pk, sk, np.full_like(pk, canary),
+                                         (1, 2), wl.kv_lora))
+            elif wl.kind == "slide":
+                before = u16(pool_before[l:l + 1])
+                pk = before.copy()
+                sk = orc.slide(pk, ch, th, wl.rot_dim, wl.rot_offset, wl.pairing, want_scale=True)
+                pending.append(ex.submit(cmp, "K", l, u16(wl.pool_k[l:l + 1]), pk, sk, before, (1, 3)))
+            else:
+                raise ValueError(f"check_layers: {wl.kind} not handled")
+            collect(workers)
+        collect(0)
+    return totals

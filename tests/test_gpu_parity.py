@@ -470,3 +470,44 @@ def test_ingest_device_errors(bad):
     # chunk 0 was ingested regardless
     rows0 = np.arange(0, 100)
     assert not np.array_equal(Hn.u16(wl.store_k)[:, rows0], h.store_k[:, rows0])
+
+
+@pytest.mark.parametrize("family,stale", [("gqa", "pointers"), ("gqa", "len"), ("mla", "pointers")])
+def test_stale_host_copy_takes_the_copy_path(family, stale):
+    """A host descriptor copy that disagrees with the device array: its U
+    pointers name other live tensors of the same shape (or its len differs).
+    The device descriptors decide: the output matches the oracle on them, the
+    mismatched chunks' factor tiles move by per-thread copies, and the call
+    reports KAMERA_DEVERR_DESCRIPTOR.  Every address involved stays valid."""
+    base = W.qwen_recall() if family == "gqa" else W.dsv2_mla()
+    spec = W.scaled(base, L=2, lens=(300, 129, 200))
+    wl = W.make(spec, DEV)
+    h = Hn.snapshot(wl)
+    chunks = K.pack_chunks(wl.chunks, device=DEV)
+    decoys = []
+    host = []
+    for i, c in enumerate(wl.chunks):
+        if i == 1:   # the middle chunk is described differently on the host
+            if stale == "pointers":
+                d = [torch.randn_like(c.patches[0], dtype=torch.float32).to(torch.bfloat16), c.patches[1],
+                     torch.randn_like(c.patches[2], dtype=torch.float32).to(torch.bfloat16), c.patches[3]]
+                decoys.append(d)
+                host.append(W.ChunkData(c.src_offset, c.length, c.delta, c.rank, c.slots, d))
+            else:
+                host.append(W.ChunkData(c.src_offset, c.length - 64, c.delta, c.rank, c.slots[:c.length - 64],
+                                        c.patches))
+        else:
+            host.append(c)
+    hc = K.pack_chunks(host, device="cpu")
+    err = torch.zeros(1, dtype=torch.int32, device=DEV)
+    n, ml, mr = len(wl.chunks), wl.max_len, Hn.max_rank(wl)
+    if family == "gqa":
+        K.kamera_relocate_patch(wl.pool_k, wl.pool_v, wl.store_k, wl.store_v, Hn.rope_of(wl), chunks, n, ml, mr,
+                                err, host_chunks=hc)
+    else:
+        K.kamera_mla_relocate_patch(wl.pool_k, wl.store_k, wl.kv_lora, Hn.rope_of(wl), chunks, n, ml, mr, err,
+                                    host_chunks=hc)
+    torch.cuda.synchronize()
+    assert int(err.item()) == 4, int(err.item())   # KAMERA_DEVERR_DESCRIPTOR alone
+    Hn.check_parity(wl, h, f"stale host copy ({family}, {stale})")
+    del decoys
