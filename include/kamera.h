@@ -50,8 +50,10 @@
  *  - Memory: every pointer in the structs below, and every pointer inside the
  *    chunk descriptors, is caller-owned device memory (except the RoPE
  *    override table, which is host memory read during the call).  The library
- *    allocates nothing, keeps no state between calls, never synchronises, and
- *    is safe to call from several host threads.  Work is enqueued on `stream`
+ *    allocates nothing, keeps no state between calls (apart from a cache of
+ *    the device's answers to cluster-occupancy queries, per kernel and
+ *    device), never synchronises, and is safe to call from several host
+ *    threads.  Work is enqueued on `stream`
  *    (a cudaStream_t of the current device; NULL = legacy default stream).
  *  - Synchronous status: the return value (KAMERA_OK or a KAMERA_ERR_* code).
  *    On any error nothing is enqueued.  n_chunks == 0 or max_len == 0 is a
@@ -106,7 +108,9 @@ enum {
                                       (every wait of the tensor-core kernels is bounded by
                                       1 s; the environment variable KAMERA_WAIT_LIMIT_NS,
                                       read at each call, overrides the bound -- a test hook:
-                                      with a bound of a few ns the kernels give up at once,
+                                      with a bound of 0 the kernels give up at their first
+                                      pipeline wait that is not met at once (patch formation:
+                                      at its first wait), so they give up early,
                                       drain their own copies and MMAs, free their tensor
                                       memory and return with this bit set) */
 };
@@ -413,7 +417,10 @@ typedef struct KameraDeficit {
  * columns take subspace iteration on X^T X (three products of a basis of
  * k = min(48, m + 16 rounded up to 16) columns) and a Rayleigh-Ritz step:
  * exact to fp32 rounding when sigma_{k+1} is well below sigma_m (a deficit
- * whose energy sits in fewer than k directions), near-optimal otherwise.  u, v and sigma
+ * whose energy sits in fewer than k directions), near-optimal otherwise; in
+ * that case sigma holds the Ritz values ||X v_r|| of the returned directions
+ * (what U = X V carries), which approach the singular values as the gap after
+ * sigma_m grows and are exact only with such a gap.  u, v and sigma
  * must not overlap each other or the deficit.  Non-finite input gives
  * non-finite factors.  No block (n_outer, n_inner or rows 0) is a successful
  * no-op.  d_err: reserved for device-side errors (none is raised by this
@@ -494,8 +501,9 @@ int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, c
  *           16-byte aligned
  *   rope    rot_offset / rot_dim relative to k_rope
  *   d_seq_start, descriptors: as for kamera_attend_reused; ranks even.
- * Supported: kv_lora_rank 512, rope_dim 64 (DeepSeek-V2/V3), num_q_heads 1..16,
- * max_rank <= 32.  Device errors (the chunk is skipped): SOURCE, DESCRIPTOR
+ * Supported: kv_lora_rank 512, rope_dim 64 (DeepSeek-V2/V3), num_q_heads 1..128
+ * (served in groups of 16: each group beyond the first is one more pass over the
+ * rows), max_rank <= 32.  Device errors (the chunk is skipped): SOURCE, DESCRIPTOR
  * (also an odd rank, or a malformed d_seq_start: the sequence is skipped), LEN,
  * RANK.
  */

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <utility>
 #include <vector>
 
@@ -27,6 +28,46 @@ uint64_t wait_limit_ns()
     char* end = nullptr;
     const unsigned long long n = std::strtoull(v, &end, 10);
     return (end && *end == '\0') ? (uint64_t)n : 1000000000ull;
+}
+
+int cluster_fit(const void* kernel, int block_threads, int smem_bytes, int cl)
+{
+    struct Entry {
+        const void* kernel;
+        int dev, block, bytes, cl, fit;
+    };
+    static std::mutex mu;
+    static std::vector<Entry> cache;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;
+    }
+    {
+        std::lock_guard<std::mutex> g(mu);
+        for (const Entry& e : cache)
+            if (e.kernel == kernel && e.dev == dev && e.block == block_threads && e.bytes == smem_bytes && e.cl == cl)
+                return e.fit;
+    }
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((unsigned)cl);
+    cfg.blockDim = dim3((unsigned)block_threads);
+    cfg.dynamicSmemBytes = (size_t)smem_bytes;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = (unsigned)cl;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int fit = 0;
+    if (cudaOccupancyMaxActiveClusters(&fit, kernel, &cfg) != cudaSuccess) {
+        (void)cudaGetLastError();
+        return 0;   // not cached: a later call asks again
+    }
+    std::lock_guard<std::mutex> g(mu);
+    cache.push_back(Entry{kernel, dev, block_threads, smem_bytes, cl, fit});
+    return fit;
 }
 
 }  // namespace kamera

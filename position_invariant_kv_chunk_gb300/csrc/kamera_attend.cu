@@ -55,8 +55,9 @@ struct __align__(16) AtSmem {
     static constexpr int RS = KW + 8;    // row stride: an odd number of 16-byte vectors
     static constexpr int NT = KW / 8;    // 8-column tiles of the value side
     static constexpr int MPa = MP > 0 ? MP : 1;
-    __nv_bfloat16 kt[2][kAtT][RS];       // key tiles; the partial outputs at the end
-    __nv_bfloat16 vt[2][kAtT][RS];       // value tiles
+    static constexpr int NS = KW > 160 ? 3 : 4;   // tile buffers: NS - 1 tiles in flight while one is used
+    __nv_bfloat16 kt[NS][kAtT][RS];      // key tiles; the partial outputs at the end
+    __nv_bfloat16 vt[NS][kAtT][RS];      // value tiles
     __nv_bfloat16 xh[kAtH][RS];          // per-chunk query part R(-delta) q | V_k^T q, bf16 hi
     __nv_bfloat16 xl[kAtH][RS];          // and lo
     __nv_bfloat16 q[kAtH][D];            // the queries (target frame; rows past G zero)
@@ -65,7 +66,8 @@ struct __align__(16) AtSmem {
     __nv_bfloat16 pl[kAtH][kAtT + 8];    // and lo
     float alpha[kAtH];                   // running-max rescale of the tile
     float2 cs[D / 2];                    // cos/sin of -delta
-    __nv_bfloat16 vk[D][MPa];            // V_k of this (layer, head), staged per chunk
+    static constexpr int VKS = MPa + 8;  // V_k row stride: an odd number of 16-byte vectors
+    __nv_bfloat16 vk[D][VKS];            // V_k of this (layer, head), staged per chunk
     float wsum[kAtH][MPa];               // sum_j p_j u'_j of the chunk, at its end
     float cm[kAtH], cl[kAtH];            // this CTA's softmax state, for the merge
     float fac[kAtH][kAtMaxCL];           // merge weights (rank 0)
@@ -255,20 +257,40 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
             continue;
         const int m = ch.rank;
         __syncthreads();   // the previous chunk (or the query staging) is done with every shared array
-        attend_load<D, MP>(p, ch, g, t_lo * kAtT, min(kAtT, len - t_lo * kAtT), 0, s);   // lands during set-up
+        const int64_t fo = (int64_t)(p.layer * p.H + g) * D * m;   // this (layer, head)'s V factors [d][m]
+        if constexpr (MP > 0) {   // V_k [d][m], zero past the rank: one copy group, older than the tiles'
+            const __nv_bfloat16* vkg = patch_ptr(ch, 1);
+            if ((m & 7) == 0) {
+                constexpr int VV = MP / 8;
+                for (int e = threadIdx.x; e < D * VV; e += kAtThreads) {
+                    const int i = e / VV, v = e - i * VV;
+                    const uint32_t dst = ptx::smem_addr(&s.vk[i][8 * v]);
+                    if (8 * v < m)
+                        ptx::cp_async16(dst, vkg + fo + (int64_t)i * m + 8 * v);
+                    else
+                        ptx::st_shared_zero16(dst);
+                }
+            } else {
+                for (int e = threadIdx.x; e < D * MP; e += kAtThreads) {
+                    const int i = e / MP, r = e - i * MP;
+                    s.vk[i][r] = r < m ? vkg[fo + (int64_t)i * m + r] : __float2bfloat16_rn(0.f);
+                }
+            }
+        }
+        ptx::cp_async_commit();
+        for (int j = 0; j < SM::NS - 1; ++j) {   // the first NS - 1 tiles land during set-up
+            const int tj = t_lo + j;
+            if (tj < t_hi)
+                attend_load<D, MP>(p, ch, g, tj * kAtT, min(kAtT, len - tj * kAtT), j, s);
+            else
+                ptx::cp_async_commit();   // one copy group per tile slot, empty or not
+        }
         for (int f = threadIdx.x; f < rp.n_freq; f += kAtThreads) {
             float cc, sn;
             phase_cos_sin(-freq_delta(rp, ch, c, f), rp.inv_freq[f], cc, sn);
             s.cs[f] = make_float2(cc, sn);
         }
-        const int64_t fo = (int64_t)(p.layer * p.H + g) * D * m;   // this (layer, head)'s V factors [d][m]
-        if constexpr (MP > 0) {
-            const __nv_bfloat16* vkg = patch_ptr(ch, 1);
-            for (int e = threadIdx.x; e < D * MP; e += kAtThreads) {
-                const int i = e / MP, r = e - i * MP;
-                s.vk[i][r] = r < m ? vkg[fo + (int64_t)i * m + r] : __float2bfloat16_rn(0.f);
-            }
-        }
+        ptx::cp_async_wait<SM::NS - 1>();   // V_k has landed (the tiles may still be in flight)
         __syncthreads();
         for (int e = threadIdx.x; e < kAtH * D; e += kAtThreads) {   // q turned by -delta
             const int h = e / D, i = e - h * D, k = i - ro;
@@ -286,26 +308,38 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
             }
             split1(v, s.xh[h][i], s.xl[h][i]);
         }
-        if constexpr (MP > 0) {
-            for (int e = threadIdx.x; e < kAtH * MP; e += kAtThreads) {   // V_k^T q (the un-turned query)
-                const int h = e / MP, r = e - h * MP;
-                float u0 = 0.f, u1 = 0.f;
-#pragma unroll 8
-                for (int i = 0; i < D; i += 2) {
-                    u0 = fmaf(__bfloat162float(s.q[h][i]), __bfloat162float(s.vk[i][r]), u0);
-                    u1 = fmaf(__bfloat162float(s.q[h][i + 1]), __bfloat162float(s.vk[i + 1][r]), u1);
+        if constexpr (MP > 0) {   // V_k^T q (the un-turned query) by warp MMAs: warp w takes ranks 8w .. 8w + 7
+            if (warp < MP / 8) {
+                float y[4] = {0.f, 0.f, 0.f, 0.f};
+                const uint32_t qa = ptx::smem_addr(&s.q[arow][acol]);
+                const uint32_t vka = ptx::smem_addr(&s.vk[lane & 15][8 * warp]);
+#pragma unroll
+                for (int ks = 0; ks < D / 16; ++ks) {
+                    uint32_t a[4], bb[2];
+                    ldsm_x4(qa + 32 * ks, a);
+                    ldsm_x2_t(vka + (uint32_t)(16 * ks * SM::VKS * 2), bb);
+                    mma_bf16(y, a, bb[0], bb[1]);
                 }
-                split1(u0 + u1, s.xh[h][D + r], s.xl[h][D + r]);
+                const int col = D + 8 * warp + 2 * t4;   // rows gq, gq + 8 (heads); columns col, col + 1
+                split1(y[0], s.xh[gq][col], s.xl[gq][col]);
+                split1(y[1], s.xh[gq][col + 1], s.xl[gq][col + 1]);
+                split1(y[2], s.xh[gq + 8][col], s.xl[gq + 8][col]);
+                split1(y[3], s.xh[gq + 8][col + 1], s.xl[gq + 8][col + 1]);
             }
         }
 
         for (int tl = t_lo; tl < t_hi; ++tl) {
-            const int b = (tl - t_lo) & 1, ntok = min(kAtT, len - tl * kAtT);
-            ptx::cp_async_wait<0>();   // this thread's copies of tile tl (the only group in flight)
+            const int i = tl - t_lo, b = i % SM::NS, ntok = min(kAtT, len - tl * kAtT);
+            ptx::cp_async_wait<SM::NS - 2>();   // this thread's copies of tile tl (NS - 2 newer groups may fly)
             __syncthreads();   // tile b (and, first, the chunk's query part) in place; every warp is
-                               // done with tile tl - 1, its buffers and its scores and weights
-            if (tl + 1 < t_hi)
-                attend_load<D, MP>(p, ch, g, (tl + 1) * kAtT, min(kAtT, len - (tl + 1) * kAtT), b ^ 1, s);
+                               // done with tile tl - 1, its buffer and its scores and weights
+            {   // tile tl + NS - 1 into the buffer tile tl - 1 has left
+                const int tn = tl + SM::NS - 1;
+                if (tn < t_hi)
+                    attend_load<D, MP>(p, ch, g, tn * kAtT, min(kAtT, len - tn * kAtT), (i + SM::NS - 1) % SM::NS, s);
+                else
+                    ptx::cp_async_commit();
+            }
             const uint32_t kb = kt0 + b * kBuf, vb = vt0 + b * kBuf;
             {   // scores of tokens 8 warp .. + 7 against the (padded) 16 heads; k-step ks adds
                 // its hi and lo products to sums 2 (ks & 1) and 2 (ks & 1) + 1, so a wider
@@ -510,7 +544,8 @@ bool attend_supported(int head_dim, int G, int max_rank)
 // grid and push the last ones into another wave.  The CTAs of a cluster split
 // the (sequence, head)'s tiles evenly, so each size 1..8 is costed as
 // waves / CL and the cheapest taken (ties: the smaller cluster); `fallback` if
-// the query is unavailable.
+// the query is unavailable.  The occupancy answers are cached per kernel and
+// device (cluster_fit), so a decode step pays only this arithmetic.
 template <int D, int MP>
 static int attend_pick_cluster(const AttendParams& p, int bytes, int fallback)
 {
@@ -518,22 +553,9 @@ static int attend_pick_cluster(const AttendParams& p, int bytes, int fallback)
     int best = fallback;
     double best_t = 1e300;
     for (int cl = 1; cl <= kAtMaxCL; ++cl) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(p.n_seqs * cl), (unsigned)p.H);
-        cfg.blockDim = dim3(kAtThreads);
-        cfg.dynamicSmemBytes = bytes;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)cl;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int fit = 0;
-        if (cudaOccupancyMaxActiveClusters(&fit, attend_kernel<D, MP>, &cfg) != cudaSuccess || fit < 1) {
-            (void)cudaGetLastError();
+        const int fit = cluster_fit(reinterpret_cast<const void*>(attend_kernel<D, MP>), kAtThreads, bytes, cl);
+        if (fit < 1)
             continue;
-        }
         const double t = (double)((units + fit - 1) / fit) / cl;
         if (t < best_t * 0.999) {
             best_t = t;

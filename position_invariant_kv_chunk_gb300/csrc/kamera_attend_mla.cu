@@ -33,7 +33,9 @@
 // r taking the r-th of CL even runs of the sequence's tiles (a chunk cut
 // between two CTAs is set up by both, each folding its own share of the value
 // patch); rank 0 merges the partial softmax states through distributed shared
-// memory.
+// memory.  More than 16 query heads (DeepSeek-V3's 128) are served in groups of
+// 16, one CTA row per group (grid y): each group is one more pass over the
+// rows, and the clusters of all groups share the GPU in the same waves.
 #include <cooperative_groups.h>
 #include <cstdint>
 #include <cuda_bf16.h>
@@ -54,6 +56,7 @@ constexpr int kMlR = 64;             // rope_dim
 constexpr int kMlDK = kMlC + kMlR;   // key width before the U columns
 constexpr int kMlQS = kMlC + 8;      // staged latent-query row (elements)
 constexpr int kMlMaxCL = 8;
+constexpr int kMlMaxHeads = 128;     // query heads per latent row: groups of 16, one pass over the rows each
 
 // MP: the padded rank the instantiation takes (0, 16 or 32).
 template <int MP>
@@ -200,8 +203,10 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
     SM& s = *reinterpret_cast<SM*>(smem_raw);
     namespace cg = cooperative_groups;
     const int CL = p.cluster, rank = (int)(blockIdx.x % (unsigned)CL), seq = blockIdx.x / CL;
+    // query heads h0 .. h0 + Hg - 1 (a group of up to 16: the rows of every MMA)
+    const int h0 = (int)blockIdx.y * kMlH;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-    const int Hq = p.Hq;
+    const int Hq = p.Hq, Hg = min(kMlH, Hq - h0);
     // 8x8 matrix-load addressing: A (row-major 16 x 16) and B^T (token rows)
     const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
 
@@ -225,13 +230,13 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
     for (int e = threadIdx.x; e < kMlH * (kMlC / 8); e += kMlThreads) {
         const int h = e / (kMlC / 8), v = e - h * (kMlC / 8);
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
-        if (h < Hq)
-            w = *reinterpret_cast<const uint4*>(p.q + ((int64_t)seq * Hq + h) * kMlDK + 8 * v);
+        if (h < Hg)
+            w = *reinterpret_cast<const uint4*>(p.q + ((int64_t)seq * Hq + h0 + h) * kMlDK + 8 * v);
         *reinterpret_cast<uint4*>(qls + h * kMlQS + 8 * v) = w;
     }
     for (int e = threadIdx.x; e < kMlH * kMlR; e += kMlThreads) {
         const int h = e / kMlR, i = e - h * kMlR;
-        s.qr[h][i] = h < Hq ? __bfloat162float(p.q[((int64_t)seq * Hq + h) * kMlDK + kMlC + i]) : 0.f;
+        s.qr[h][i] = h < Hg ? __bfloat162float(p.q[((int64_t)seq * Hq + h0 + h) * kMlDK + kMlC + i]) : 0.f;
     }
     __syncthreads();
     uint32_t qc[kMlC / 16][4];   // A fragments of the latent query, every k-step
@@ -545,7 +550,7 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
             }
         }
         __syncthreads();
-        for (int e = threadIdx.x; e < Hq * (kMlC / 4); e += kMlThreads) {
+        for (int e = threadIdx.x; e < Hg * (kMlC / 4); e += kMlThreads) {
             const int h = e / (kMlC / 4), i = 4 * (e - h * (kMlC / 4));
             float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
             for (int r = 0; r < CL; ++r) {
@@ -561,7 +566,7 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
             uint2 w;
             w.x = pack_bf16x2(acc.x, acc.y);
             w.y = pack_bf16x2(acc.z, acc.w);
-            *reinterpret_cast<uint2*>(p.out + ((int64_t)seq * Hq + h) * kMlC + i) = w;
+            *reinterpret_cast<uint2*>(p.out + ((int64_t)seq * Hq + h0 + h) * kMlC + i) = w;
         }
     }
     cluster.sync();   // peers stay until rank 0 has read them
@@ -571,8 +576,8 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
 
 bool mla_attend_supported(int kv_lora, int rope_dim, int num_q_heads, int max_rank)
 {
-    return kv_lora == kMlC && rope_dim == kMlR && num_q_heads >= 1 && num_q_heads <= kMlH && max_rank >= 0 &&
-           max_rank <= 32;
+    return kv_lora == kMlC && rope_dim == kMlR && num_q_heads >= 1 && num_q_heads <= kMlMaxHeads &&
+           max_rank >= 0 && max_rank <= 32;
 }
 
 // Cluster size.  One CTA fills an SM, and a cluster's CTAs must share a GPC, so
@@ -580,30 +585,18 @@ bool mla_attend_supported(int kv_lora, int rope_dim, int num_q_heads, int max_ra
 // at once (the occupancy query) can fall short of the grid and push the last
 // ones into a second wave.  The CTAs of a cluster split the sequence's tiles
 // evenly, so each size (1 to 8) is costed as waves / CL and the cheapest taken
-// (ties: the smaller cluster).
+// (ties: the smaller cluster).  The occupancy answers are cached per kernel and
+// device (cluster_fit).
 template <int MP>
-static int mla_pick_cluster(int64_t n_seqs, int bytes)
+static int mla_pick_cluster(int64_t units, int bytes)
 {
     int best = 1;
     double best_t = 1e300;
     for (int cl = 1; cl <= kMlMaxCL; ++cl) {
-        cudaLaunchConfig_t cfg = {};
-        cfg.gridDim = dim3((unsigned)(n_seqs * cl));
-        cfg.blockDim = dim3(kMlThreads);
-        cfg.dynamicSmemBytes = bytes;
-        cudaLaunchAttribute attr[1];
-        attr[0].id = cudaLaunchAttributeClusterDimension;
-        attr[0].val.clusterDim.x = (unsigned)cl;
-        attr[0].val.clusterDim.y = 1;
-        attr[0].val.clusterDim.z = 1;
-        cfg.attrs = attr;
-        cfg.numAttrs = 1;
-        int fit = 0;
-        if (cudaOccupancyMaxActiveClusters(&fit, mla_attend_kernel<MP>, &cfg) != cudaSuccess || fit < 1) {
-            (void)cudaGetLastError();
+        const int fit = cluster_fit(reinterpret_cast<const void*>(mla_attend_kernel<MP>), kMlThreads, bytes, cl);
+        if (fit < 1)
             continue;
-        }
-        const double t = (double)((n_seqs + fit - 1) / fit) / cl;
+        const double t = (double)((units + fit - 1) / fit) / cl;
         if (t < best_t * 0.999) {
             best_t = t;
             best = cl;
@@ -619,9 +612,10 @@ static cudaError_t launch_mla_attend_m(MlaAttendParams p, cudaStream_t stream)
     cudaError_t e = cudaFuncSetAttribute(mla_attend_kernel<MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess)
         return e;
-    p.cluster = mla_pick_cluster<MP>(p.n_seqs, bytes);
+    const int groups = (p.Hq + kMlH - 1) / kMlH;
+    p.cluster = mla_pick_cluster<MP>((int64_t)p.n_seqs * groups, bytes);
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3((unsigned)(p.n_seqs * p.cluster));
+    cfg.gridDim = dim3((unsigned)(p.n_seqs * p.cluster), (unsigned)groups);
     cfg.blockDim = dim3(kMlThreads);
     cfg.dynamicSmemBytes = bytes;
     cfg.stream = stream;

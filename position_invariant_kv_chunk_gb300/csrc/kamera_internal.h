@@ -42,6 +42,12 @@ cudaError_t launch_ingest(const IngestParams& p, cudaStream_t stream);
 bool patch_form_supported(int cols, int m);
 cudaError_t launch_patch_form(const PatchFormParams& p, int64_t n_blocks, cudaStream_t stream);
 
+// Clusters of `cl` CTAs (block_threads threads, smem_bytes of dynamic shared
+// memory) of `kernel` that fit on the current device at once, from
+// cudaOccupancyMaxActiveClusters; 0 if the query fails.  The answer depends
+// only on these arguments and the device, so it is cached (thread-safe).
+int cluster_fit(const void* kernel, int block_threads, int smem_bytes, int cl);
+
 // Decode attention over reused chunks: shapes handled; one CTA per (sequence, KV head).
 bool attend_supported(int head_dim, int G, int max_rank);
 int attend_cluster(int64_t units);

@@ -217,12 +217,24 @@ __device__ __forceinline__ uint32_t pf_piece(int r, int kc, uint32_t atom_bytes)
 __device__ __forceinline__ bool pf_wait_mma(PfTc& t, int32_t* err, int* s_abort, uint64_t p_wait_ns)
 {
     if (threadIdx.x == 0) {
-        const uint64_t t0 = ptx::globaltimer();
-        while (!ptx::mbar_try_wait(t.bar, t.phase & 1u)) {
-            if (ptx::globaltimer() - t0 > p_wait_ns) {
-                *s_abort = 1;
-                raise_err(err, KAMERA_DEVERR_TIMEOUT);
-                break;
+        // A short bound (the test hook) polls without suspending.  A bound of 0
+        // gives up at once, without polling: the wait it stands for is then
+        // certainly still pending (every wait here follows an MMA issue), so the
+        // exit path must drain that MMA.
+        const bool quick = p_wait_ns < 100000u;
+        auto poll = [&]() {
+            return quick ? ptx::mbar_test_wait(t.bar, t.phase & 1u) : ptx::mbar_try_wait(t.bar, t.phase & 1u);
+        };
+        if (p_wait_ns == 0 || !poll()) {
+            const uint64_t t0 = p_wait_ns == 0 ? 0 : ptx::globaltimer();
+            for (;;) {
+                if (p_wait_ns == 0 || ptx::globaltimer() - t0 > p_wait_ns) {
+                    *s_abort = 1;
+                    raise_err(err, KAMERA_DEVERR_TIMEOUT);
+                    break;
+                }
+                if (poll())
+                    break;
             }
         }
     }

@@ -118,17 +118,25 @@ __device__ __forceinline__ bool u_map_stale(const UmmaLaunch<MC>& P, int c, cons
     return c < MC && P.u_rank[c] > 0 && !u_mapped(P, c, ch);
 }
 
+// Operand buffering by the call's largest rank.  KA = 0 (ranks <= 16): U and
+// V_m are K-major with 32-byte rows (one 16-rank step, 32-byte swizzle), 4 KB
+// each, so the copies of every operand can start five tiles ahead (a call
+// whose jobs are one tile long -- short chunks -- needs a new V_m every tile).
+// KA = 1 (ranks <= 64) and 2 (<= 128): 64-rank atoms of 128-byte rows.
 template <int KA>
 struct Geometry {
-    static constexpr int LA = KA == 1 ? 2 : 1;  // operand lookahead (tiles)
-    static constexpr int D = LA + 1;            // U operand buffers
-    static constexpr int S = KA == 1 ? 4 : 2;   // row stages
-    static constexpr int kUBytes = KA * kAtomBytes;
-    static constexpr int kVBytes = KA * kWMax * 128;
+    static constexpr int LA = KA == 0 ? 5 : KA == 1 ? 2 : 1;   // operand lookahead (tiles)
+    static constexpr int D = LA + 1;                            // U operand buffers
+    static constexpr int NV = KA == 0 ? D : 2;                  // V_m buffers (one job each)
+    static constexpr int S = KA == 2 ? 2 : 4;                   // row stages
+    static constexpr bool kSw32 = KA == 0;                      // 32-byte operand rows
+    static constexpr int kUBytes = KA == 0 ? kTileM * 32 : KA * kAtomBytes;
+    static constexpr int kVBytes = KA == 0 ? kWMax * 32 : KA * kWMax * 128;
     static constexpr int kUOff = S * kStageBytes;
     static constexpr int kVOff = kUOff + D * kUBytes;
-    static constexpr int kSharedOff = kVOff + 2 * kVBytes;
+    static constexpr int kSharedOff = kVOff + NV * kVBytes;
 };
+constexpr int kMaxD = 6, kMaxNV = 6;   // barrier arrays sized for the deepest geometry
 
 struct Seg {
     int array, e0, w, rot, u_idx, v_idx, fh, FH, vm_row0, vm_rows;
@@ -216,7 +224,7 @@ struct TileInfo {
 };
 
 struct Shared {
-    uint64_t full[4], empty[4], tfull[2], tempty[2], uempty[3], ufull[3], vmempty[2], mmadone;
+    uint64_t full[4], empty[4], tfull[2], tempty[2], uempty[kMaxD], ufull[kMaxD], vmempty[kMaxNV], mmadone;
     uint32_t tmem_base;
     int32_t abort_flag;
     int32_t start_lz, start_rem, start_c, start_t, count;
@@ -228,17 +236,21 @@ struct Shared {
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag, int32_t* err,
                                          uint64_t limit)
 {
-    if (ptx::mbar_try_wait(bar, parity))
+    // A short bound (the test hook) polls without suspending and checks the
+    // clock at every poll, so a wait that is not met at once does run out.
+    const bool quick = limit < 100000u;
+    auto poll = [&]() { return quick ? ptx::mbar_test_wait(bar, parity) : ptx::mbar_try_wait(bar, parity); };
+    if (poll())
         return true;
     const uint64_t t0 = ptx::globaltimer();
-    const uint32_t every = limit < 100000u ? 0u : 63u;   // a short bound is checked at every poll
+    const uint32_t every = quick ? 0u : 63u;
     for (uint32_t it = 1;; ++it) {
-        if (ptx::mbar_try_wait(bar, parity))
+        if (poll())
             return true;
         if ((it & every) == 0) {
             if (*abort_flag)
                 return false;
-            if (ptx::globaltimer() - t0 > limit) {
+            if (limit == 0 || ptx::globaltimer() - t0 > limit) {
                 *abort_flag = 1;
                 raise_err(err, KAMERA_DEVERR_TIMEOUT);
                 return false;
@@ -265,9 +277,14 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity)
 }
 
 // Byte offset of the 16-byte piece (row r, piece kc) in a 128B-swizzled
-// K-major operand with atoms of `atom_bytes` (64 ranks per atom).
+// K-major operand with atoms of `atom_bytes` (64 ranks per atom); with
+// atom_bytes == 0, in a 32B-swizzled operand of 32-byte rows (16 ranks; the
+// swizzle XORs address bit 4 with bit 7: the two pieces of rows 4..7 of every
+// 8-row group trade places).
 __device__ __forceinline__ uint32_t operand_offset(int r, int kc, uint32_t atom_bytes)
 {
+    if (atom_bytes == 0)
+        return r * 32 + ((kc ^ ((r >> 2) & 1)) << 4);
     return (kc >> 3) * atom_bytes + r * 128 + ((((kc & 7) ^ (r & 7))) << 4);
 }
 
@@ -490,8 +507,9 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(ptx::smem_addr(&sh.tfull[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&sh.tempty[i]), kEpiWarps);
-            ptx::mbar_init(ptx::smem_addr(&sh.vmempty[i]), 1);
         }
+        for (int i = 0; i < G::NV; ++i)
+            ptx::mbar_init(ptx::smem_addr(&sh.vmempty[i]), 1);
         for (int i = 0; i < G::D; ++i) {
             ptx::mbar_init(ptx::smem_addr(&sh.uempty[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&sh.ufull[i]), 1);
@@ -523,16 +541,38 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             mine += (ch.len + kTileM - 1) / kTileM;
         }
     }
-    sh.part[tid] = mine;
+    // exclusive prefix of the per-thread tile counts: within each warp by
+    // shuffles, then over the warp totals in warp 0
+    int64_t incl = mine;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+        const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
+        if (lane >= o)
+            incl += y;
+    }
+    if (lane == 31)
+        sh.part[warp] = incl;
     __syncthreads();
-    if (tid == 0) {
-        int64_t run = 0;
-        for (int i = 0; i < kThreads; ++i) {
-            const int64_t v = sh.part[i];
-            sh.part[i] = run;
-            run += v;
+    if (warp == 0) {
+        constexpr int NW = kThreads / 32;
+        const int64_t w = lane < NW ? sh.part[lane] : 0;
+        int64_t wi = w;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, wi, o);
+            if (lane >= o)
+                wi += y;
         }
-        const int64_t TC = run;
+        __syncwarp();
+        if (lane < NW)
+            sh.part[NW + lane] = wi - w;   // exclusive prefix of warp `lane`
+        if (lane == NW - 1)
+            sh.part[2 * NW] = wi;          // all tiles of one layer and segment
+    }
+    __syncthreads();
+    const int64_t my_prefix = sh.part[kThreads / 32 + warp] + incl - mine;
+    if (tid == 0) {
+        const int64_t TC = sh.part[2 * (kThreads / 32)];
         const int64_t T = TC * r.L * p.Z;
         const int64_t b0 = T * blockIdx.x / gridDim.x, b1 = T * (blockIdx.x + 1) / gridDim.x;
         sh.count = (int32_t)(b1 - b0);
@@ -545,7 +585,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
     __syncthreads();
     if (sh.count > 0) {
         const int64_t rem = sh.start_rem;
-        const int64_t lo = (int64_t)p.Z * sh.part[tid];   // a chunk holds Z * (its tiles) of a layer
+        const int64_t lo = (int64_t)p.Z * my_prefix;   // a chunk holds Z * (its tiles) of a layer
         if (rem >= lo && rem < lo + (int64_t)p.Z * mine) {   // exactly one thread owns the starting tile
             int64_t acc = lo;
             for (int c = c_lo; c < c_hi; ++c) {
@@ -706,14 +746,14 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                     const int64_t lh = (int64_t)l * sg.FH + sg.fh;
                     if (new_job) {
                         ++ld_v;
-                        if (!warp_wait(ptx::smem_addr(&sh.vmempty[ld_v & 1]), ((ld_v >> 1) & 1) ^ 1, abort_flag,
-                                       r.err, p.wait_ns))
+                        if (!warp_wait(ptx::smem_addr(&sh.vmempty[ld_v % G::NV]), ((ld_v / G::NV) & 1) ^ 1,
+                                       abort_flag, r.err, p.wait_ns))
                             stop = true;
                         else
-                            load_operand(vbase + (ld_v & 1) * G::kVBytes,
+                            load_operand(vbase + (ld_v % G::NV) * G::kVBytes,
                                          patch_ptr(ch, sg.v_idx) +
                                              (lh * sg.vm_rows + sg.vm_row0) * m,
-                                         sg.w, m, mpad, (uint32_t)sg.w * 128u, lane);
+                                         sg.w, m, mpad, G::kSw32 ? 0u : (uint32_t)sg.w * 128u, lane);
                     }
                     const int u = ld_u % G::D;
                     const bool by_tma = u_mapped(P, ld.c, ch);   // the producer loads this U tile
@@ -725,7 +765,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                         load_operand(ubase + u * G::kUBytes,
                                      patch_ptr(ch, sg.u_idx) +
                                          (lh * ch.len + tok0) * m,
-                                     min(kTileM, ch.len - tok0), m, mpad, kAtomBytes, lane);
+                                     min(kTileM, ch.len - tok0), m, mpad, G::kSw32 ? 0u : (uint32_t)kAtomBytes, lane);
                     }
                     ++ld_u;
                 }
@@ -767,23 +807,25 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                     } else {
                         ptx::tc_fence_after();
                         const uint32_t a0 = ubase + u * G::kUBytes;
-                        const uint32_t b0 = vbase + (vjob & 1) * G::kVBytes;
+                        const uint32_t b0 = vbase + (vjob % G::NV) * G::kVBytes;
                         const uint32_t idesc = ptx::idesc_bf16_f32(kTileM, sg.w);
                         const uint32_t d = tmem + acc * kWMax;
                         const int steps = (m + 15) >> 4;
                         for (int q = 0; q < steps; ++q) {
                             const uint32_t koff = (q & 3) * 32;
-                            // A as the TMA load laid it out (rows of 2m bytes, m < 64) or in 64-rank atoms
-                            const uint64_t ad = by_tma && m == 16   ? ptx::desc_k_sw32(a0)
+                            // A as the TMA load laid it out (rows of 2m bytes, m < 64), as the
+                            // copies laid it out (32-byte rows for ranks <= 16), or in 64-rank atoms
+                            const uint64_t ad = G::kSw32 || (by_tma && m == 16) ? ptx::desc_k_sw32(a0)
                                                 : by_tma && m == 32 ? ptx::desc_k_sw64(a0 + koff)
                                                                     : ptx::desc_k_sw128(a0 + (q >> 2) * kAtomBytes + koff);
-                            const uint64_t bd = ptx::desc_k_sw128(b0 + (q >> 2) * (uint32_t)sg.w * 128u + koff);
+                            const uint64_t bd = G::kSw32 ? ptx::desc_k_sw32(b0)
+                                                         : ptx::desc_k_sw128(b0 + (q >> 2) * (uint32_t)sg.w * 128u + koff);
                             ptx::umma_bf16(d, ad, bd, idesc, q > 0 ? 1u : 0u);
                         }
                         ptx::umma_commit(ptx::smem_addr(&sh.tfull[acc]));
                         ptx::umma_commit(ptx::smem_addr(&sh.uempty[k % G::D]));
                         if (last_of_job)
-                            ptx::umma_commit(ptx::smem_addr(&sh.vmempty[vjob & 1]));
+                            ptx::umma_commit(ptx::smem_addr(&sh.vmempty[vjob % G::NV]));
                         ++issued_mma;
                     }
                 }
@@ -920,7 +962,7 @@ static size_t smem_bytes_for()
 
 size_t umma_smem_bytes(const RowsParams& p)
 {
-    return p.max_rank > 64 ? smem_bytes_for<2>() : smem_bytes_for<1>();
+    return p.max_rank > 64 ? smem_bytes_for<2>() : p.max_rank > 16 ? smem_bytes_for<1>() : smem_bytes_for<0>();
 }
 
 namespace {
@@ -1039,8 +1081,11 @@ cudaError_t launch_umma(const RowsParams& rp, int family, const KameraChunk* h_c
     if (rp.max_rank > 64)
         return few ? launch_kernel<2, kMapChunksFew>(p, h_chunks, sms, stream)
                    : launch_kernel<2, kMapChunksMany>(p, h_chunks, sms, stream);
-    return few ? launch_kernel<1, kMapChunksFew>(p, h_chunks, sms, stream)
-               : launch_kernel<1, kMapChunksMany>(p, h_chunks, sms, stream);
+    if (rp.max_rank > 16)
+        return few ? launch_kernel<1, kMapChunksFew>(p, h_chunks, sms, stream)
+                   : launch_kernel<1, kMapChunksMany>(p, h_chunks, sms, stream);
+    return few ? launch_kernel<0, kMapChunksFew>(p, h_chunks, sms, stream)
+               : launch_kernel<0, kMapChunksMany>(p, h_chunks, sms, stream);
 }
 
 }  // namespace kamera

@@ -98,6 +98,10 @@ CASES = {
     "one_sequence_ten_chunks": W.MlaAttendSpec("mla_10", Hq=16, seqs=((70,) * 10,), m=16),
     "one_head": W.MlaAttendSpec("mla_h1", Hq=1, seqs=((65, 64),), m=16, base=1e6),
     "one_long_chunk_cut_across_the_cluster": W.MlaAttendSpec("mla_long", Hq=16, seqs=((1000,),), m=32),
+    # more than 16 query heads per latent row: groups of 16, the last one partial
+    "heads_17": W.MlaAttendSpec("mla_h17", Hq=17, seqs=((130, 40), (64,)), m=16),
+    "heads_40_ragged": W.MlaAttendSpec("mla_h40", Hq=40, seqs=((300, 7), (1,), (129, 64, 65)), m=8),
+    "deepseek_v3_128_heads": W.MlaAttendSpec("mla_h128", Hq=128, seqs=((500, 77), (256,)), m=32),
 }
 
 
@@ -182,8 +186,8 @@ def test_mla_attend_device_errors():
 
 
 def test_mla_attend_host_errors():
-    a = W.make_mla_attend(W.MlaAttendSpec("mla_h17", Hq=17, seqs=((10,),), m=8), DEV)
-    with pytest.raises(K.KameraError) as e:        # more than 16 query heads
+    a = W.make_mla_attend(W.MlaAttendSpec("mla_h129", Hq=129, seqs=((10,),), m=8), DEV)
+    with pytest.raises(K.KameraError) as e:        # more than 128 query heads
         run_mla(a)
     assert e.value.status == 3
     a = W.make_mla_attend(W.MlaAttendSpec("mla_m34", Hq=16, seqs=((10,),), m=34), DEV)

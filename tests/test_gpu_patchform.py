@@ -193,7 +193,8 @@ def near_optimal(spec: W.DeficitSpec, m: int):
     Eckart-Young optimum, and V stays orthonormal."""
     x = W.make_deficit(spec, DEV)
     xb = _blocks(x)
-    u, v = K.kamera_form_patch(xb, m)
+    sig = torch.empty(1, 1, m, dtype=torch.float32, device=DEV)
+    u, v = K.kamera_form_patch(xb, m, sigma=sig)
     torch.cuda.synchronize()
     xh, uh, vh = _f64(xb), _f64(u)[0, 0], _f64(v)[0, 0]
     xh = xh.mean(axis=0)[0, 0] if xh.ndim == 5 else xh[0, 0]
@@ -202,6 +203,11 @@ def near_optimal(spec: W.DeficitSpec, m: int):
     res = np.linalg.norm(xh - uh @ vh.T) ** 2
     assert res <= opt + 0.02 * tot, (res, opt, tot)
     assert np.max(np.abs(vh.T @ vh - np.eye(m))) <= 8e-3
+    # sigma holds the Ritz values ||X v_r|| of the returned directions (not the
+    # singular values, which they only bound from below without a gap)
+    ritz = np.linalg.norm(xh @ vh, axis=0)
+    assert np.all(np.abs(sig[0, 0].cpu().numpy() - ritz) <= 1e-2 * so[0]), (sig[0, 0].cpu().numpy(), ritz)
+    assert np.all(sig[0, 0].cpu().numpy() <= so[:m] * (1 + 1e-2))
 
 
 def test_wide_flat_spectrum_is_near_optimal():
