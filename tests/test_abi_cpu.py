@@ -234,7 +234,7 @@ def test_mla_attend_argument_errors():
     seq = torch.zeros(3, dtype=torch.int32)
     rope = K.Rope(1e4, 64, 0, K.INTERLEAVED)
     cases = [
-        (dict(q=torch.zeros(2, 17, 576, dtype=torch.bfloat16)), 3),      # more than 16 query heads
+        (dict(q=torch.zeros(2, 129, 576, dtype=torch.bfloat16)), 3),     # more than 128 query heads
         (dict(max_rank=34), 3),                                          # rank above 32
         (dict(store=torch.zeros(64, 320, dtype=torch.bfloat16), kv_lora=256,
               q=torch.zeros(2, 16, 320, dtype=torch.bfloat16)), 3),      # a latent width other than 512
