@@ -93,6 +93,7 @@ struct PatchFormParams {
     float* sigma;                  // [blocks][m] or null
     int32_t* err;
     uint64_t wait_ns;              // bound of each MMA completion wait (wait_limit_ns())
+    int32_t cluster;               // wide blocks: CTAs of a cluster sharing one block's rows
 };
 
 // Decode attention over reused chunks: one layer's canonical store, sequences

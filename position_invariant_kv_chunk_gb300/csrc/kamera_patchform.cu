@@ -29,6 +29,7 @@
 //      also separates vectors of clustered (or repeated) eigenvalues.
 //   4. Back-transformation Z = Q Y, reflector by reflector over all columns.
 // Shared-memory traffic is O(n^3) words once instead of once per Jacobi sweep.
+#include <cooperative_groups.h>
 #include <cstdint>
 #include <cuda_bf16.h>
 
@@ -909,7 +910,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_kernel(const __grid_
 // X^T (X Z) without forming G, and re-orthonormalised; then C = Z^T G Z
 // (k x k) is solved by the routines above, V = Z W[:, :m] and U = X V.  The
 // top-m directions converge at the rate (sigma_{k+1} / sigma_m)^2 per
-// product.  All on the CUDA cores, one CTA per block.
+// product.  All on the CUDA cores.  A cluster of CL CTAs shares a block: each
+// streams its own share of the rows, and the partial products X^T (X Z) and
+// the partial Rayleigh-Ritz sums are added over the cluster through
+// distributed shared memory in rank order, so every CTA holds the same basis;
+// rank 0 writes V and sigma, every CTA its rows of U.
 constexpr int kWideMaxCols = 512;
 constexpr int kWideMaxRank = 32;
 constexpr int kWideIters = 3;
@@ -980,15 +985,16 @@ __device__ void wide_cgs2(float* z, int zs, int c, int k, float* coef)
 }
 
 // Stage rows r0 .. r0 + kWideT - 1 of X (the mean of its terms) as fp32
-// [T][c + 4], zero past rows.
-__device__ __forceinline__ void wide_stage(const PatchFormParams& p, const __nv_bfloat16* x, int r0, float* xt)
+// [T][c + 4], zero from row r_end on.
+__device__ __forceinline__ void wide_stage(const PatchFormParams& p, const __nv_bfloat16* x, int r0, int r_end,
+                                           float* xt)
 {
     const int c = p.cols, vpr = c / 8, xs = c + 4;
     const float inv = 1.0f / (float)p.n_terms;
     for (int e = threadIdx.x; e < kWideT * vpr; e += kPfThreads) {
         const int r = e / vpr, c8 = (e - r * vpr) * 8;
         float v[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-        if (r0 + r < p.rows) {
+        if (r0 + r < r_end) {
             const __nv_bfloat16* src = x + (int64_t)(r0 + r) * p.row_stride + c8;
             for (int tm = 0; tm < p.n_terms; ++tm) {
                 float w[8];
@@ -1074,7 +1080,12 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
         }
         s.lam = reinterpret_cast<float*>(q);
     }
-    const int64_t blk = blockIdx.x;
+    // a cluster of CL CTAs shares one block: CTA `crank` streams rows [row_lo, row_hi)
+    namespace cg = cooperative_groups;
+    cg::cluster_group cluster = cg::this_cluster();
+    const int CL = p.cluster, crank = (int)(blockIdx.x % (unsigned)CL);
+    const int64_t blk = blockIdx.x / CL;
+    const int row_lo = (int)((int64_t)p.rows * crank / CL), row_hi = (int)((int64_t)p.rows * (crank + 1) / CL);
     const int64_t bo = blk / p.n_inner, bi = blk - bo * p.n_inner;
     const __nv_bfloat16* x = p.x + bo * p.outer_stride + bi * p.inner_stride;
     const int t = threadIdx.x;
@@ -1091,8 +1102,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
     const int kq = k / 4, ig = t >> 2, jg = t & 3;
     for (int it = 0; it < kWideIters; ++it) {
         float acc[4][12] = {};
-        for (int r0 = 0; r0 < p.rows; r0 += kWideT) {
-            wide_stage(p, x, r0, xt);
+        for (int r0 = row_lo; r0 < row_hi; r0 += kWideT) {
+            wide_stage(p, x, r0, row_hi, xt);
             __syncthreads();
             wide_xb(xt, c, z, zs, k, yt, k);
             __syncthreads();
@@ -1120,14 +1131,35 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
                 for (int u = 0; u < 12; ++u)
                     if (u < kq)
                         z[(4 * ig + a) * zs + jg * kq + u] = acc[a][u];
+        if (CL > 1) {   // add the cluster's partial products, in rank order (the same sum in every CTA)
+            cluster.sync();
+            float sum[48];
+#pragma unroll
+            for (int j = 0; j < 48; ++j)
+                sum[j] = 0.f;
+            if (t < c)
+                for (int q = 0; q < CL; ++q) {
+                    const float* zq = cluster.map_shared_rank(z, q) + t * zs;
+#pragma unroll
+                    for (int j = 0; j < 48; ++j)
+                        if (j < k)
+                            sum[j] += zq[j];
+                }
+            cluster.sync();   // every CTA has read every partial
+            if (t < c)
+#pragma unroll
+                for (int j = 0; j < 48; ++j)
+                    if (j < k)
+                        z[t * zs + j] = sum[j];
+        }
         __syncthreads();
         wide_cgs2(z, zs, c, k, s_coef);
     }
 
     // Rayleigh-Ritz: C = (X Z)^T (X Z), accumulated per thread over its (a, b) entries
     float cacc[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int r0 = 0; r0 < p.rows; r0 += kWideT) {
-        wide_stage(p, x, r0, xt);
+    for (int r0 = row_lo; r0 < row_hi; r0 += kWideT) {
+        wide_stage(p, x, r0, row_hi, xt);
         __syncthreads();
         wide_xb(xt, c, z, zs, k, yt, k);
         __syncthreads();
@@ -1150,6 +1182,24 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
         const int e = t + u * kPfThreads;
         if (e < k * k)
             s.g[(e / k) * ld + e % k] = cacc[u];
+    }
+    if (CL > 1) {   // the cluster's partial Rayleigh-Ritz sums, in rank order
+        cluster.sync();
+#pragma unroll
+        for (int u = 0; u < 5; ++u) {
+            const int e = t + u * kPfThreads;
+            cacc[u] = 0.f;
+            if (e < k * k)
+                for (int q = 0; q < CL; ++q)
+                    cacc[u] += cluster.map_shared_rank(s.g, q)[(e / k) * ld + e % k];
+        }
+        cluster.sync();
+#pragma unroll
+        for (int u = 0; u < 5; ++u) {
+            const int e = t + u * kPfThreads;
+            if (e < k * k)
+                s.g[(e / k) * ld + e % k] = cacc[u];
+        }
     }
     __syncthreads();
     if (t < 32) {
@@ -1180,10 +1230,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
             s.lam[r] = 0.f;
         __syncthreads();
     }
-    if (p.sigma)
+    if (p.sigma && crank == 0)
         for (int r = t; r < m; r += kPfThreads)
             p.sigma[blk * m + r] = sqrtf(fmaxf(s.lam[r] * trace, 0.f));
-    // V = Z W (row t of Z -> row t of V, in place), bf16 out
+    // V = Z W (row t of Z -> row t of V, in place), bf16 out (every CTA of the
+    // cluster forms V for its U rows; rank 0 writes it)
     __nv_bfloat16* vo = p.v + blk * (int64_t)c * m;
     if (t < c) {
         float zr[48];
@@ -1197,20 +1248,21 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
                 if (j < k)
                     acc = fmaf(zr[j], s.y[j * ys + r], acc);
             z[t * zs + r] = acc;
-            vo[(int64_t)t * m + r] = __float2bfloat16_rn(acc);
+            if (crank == 0)
+                vo[(int64_t)t * m + r] = __float2bfloat16_rn(acc);
         }
     }
     __syncthreads();
     // U = X V
     __nv_bfloat16* uo = p.u + blk * (int64_t)p.rows * m;
-    for (int r0 = 0; r0 < p.rows; r0 += kWideT) {
-        wide_stage(p, x, r0, xt);
+    for (int r0 = row_lo; r0 < row_hi; r0 += kWideT) {
+        wide_stage(p, x, r0, row_hi, xt);
         __syncthreads();
         wide_xb(xt, c, z, zs, m, yt, m);
         __syncthreads();
         for (int e = t; e < kWideT * m; e += kPfThreads) {
             const int tt = e / m, r = e - tt * m;
-            if (r0 + tt < p.rows)
+            if (r0 + tt < row_hi)
                 uo[(int64_t)(r0 + tt) * m + r] = __float2bfloat16_rn(yt[tt * m + r]);
         }
         __syncthreads();
@@ -1234,8 +1286,35 @@ cudaError_t launch_patch_form(const PatchFormParams& p, int64_t n_blocks, cudaSt
                                              bytes);
         if (e != cudaSuccess)
             return e;
-        patch_form_wide_kernel<<<(unsigned)n_blocks, kPfThreads, bytes, stream>>>(p);
-        return cudaGetLastError();
+        // Cluster size: the blocks' rows are split over CL CTAs; each size 1..8
+        // is costed as waves / CL (a cluster must sit in one GPC, so the clusters
+        // that fit at once can fall short of the blocks), the cheapest taken.
+        PatchFormParams q = p;
+        q.cluster = 1;
+        double best = 1e300;
+        for (int cl = 1; cl <= 8; ++cl) {
+            const int fit = cluster_fit(reinterpret_cast<const void*>(patch_form_wide_kernel), kPfThreads, bytes, cl);
+            if (fit < 1 || (int64_t)n_blocks * cl > 0x7FFFFFFFll)
+                continue;
+            const double cost = (double)((n_blocks + fit - 1) / fit) / cl;
+            if (cost < best * 0.999) {
+                best = cost;
+                q.cluster = cl;
+            }
+        }
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3((unsigned)(n_blocks * q.cluster));
+        cfg.blockDim = dim3(kPfThreads);
+        cfg.dynamicSmemBytes = (size_t)bytes;
+        cfg.stream = stream;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = (unsigned)q.cluster;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        return cudaLaunchKernelEx(&cfg, patch_form_wide_kernel, q);
     }
     const int bytes = pf_smem_bytes(p.cols, p.m);
     cudaError_t e = cudaFuncSetAttribute(patch_form_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);

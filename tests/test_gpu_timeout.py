@@ -62,3 +62,4 @@ def test_patch_form_wait_runs_out_then_recovers(monkeypatch):
             rec = u[o, i].float().cpu().numpy().astype(np.float64) @ v[o, i].float().cpu().numpy().astype(np.float64).T
             ref = uo @ vo.T
             assert np.linalg.norm(rec - ref) <= 8e-3 * np.linalg.norm(ref)
+
