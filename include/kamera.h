@@ -453,7 +453,10 @@ int kamera_form_patch(const KameraDeficit* deficit, int32_t m, void* u, void* v,
  *   dst_slot_mapping of the descriptors is not read; ranks <= max_rank <= 64.
  * Supported: head_dim 64 or 128, num_q_heads / num_kv_heads in 1..8.
  * Device errors (the chunk is skipped): SOURCE, DESCRIPTOR (also a malformed
- * d_seq_start: the sequence is skipped), LEN, RANK.
+ * d_seq_start: the sequence is skipped), LEN, RANK; TIMEOUT if a tile's copy
+ * wait runs past its bound (outputs of the call then undefined).  Host error
+ * UNSUPPORTED also for num_rows > 2^31 - 1 (tile rows are addressed by 32-bit
+ * coordinates).
  */
 typedef struct KameraAttnKV {
     const void* k;

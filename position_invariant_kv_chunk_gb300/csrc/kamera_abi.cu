@@ -614,7 +614,7 @@ int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, c
         return KAMERA_ERR_INVALID_ARGUMENT;
     const int G = query->num_q_heads / kv->num_kv_heads;
     if (!attend_supported(kv->head_dim, G, max_rank) || kv->num_kv_heads > 65535 ||
-        query->n_seqs > 0x7FFFFFFF)
+        query->n_seqs > 0x7FFFFFFF || kv->num_rows > 0x7FFFFFFF)
         return KAMERA_ERR_UNSUPPORTED;
     if (query->n_seqs == 0)
         return KAMERA_OK;

@@ -23,15 +23,20 @@
 // so they enter as bf16 hi + lo pairs (about 16 significant bits); the rows and
 // U rows are exact bf16.  Warp w computes the scores of tokens 8w .. 8w + 7
 // and owns value-side column tiles w, w + 8, ...; the online softmax runs with
-// 16 threads per head.  Tiles are double-buffered 16-byte async copies into
-// rows padded to an odd number of 16-byte vectors, so the 8x8 matrix loads are
-// bank-conflict-free.  The CTAs of a cluster split the (sequence, head)'s tiles
+// 16 threads per head.  A ring of three or four tile buffers keeps the next
+// tiles in flight: the key and value rows arrive as 128B-swizzled TMA boxes
+// (one thread issues them; completion on an mbarrier, every wait bounded in
+// time), the U rows as 16-byte async copies into rows padded to an odd number
+// of 16-byte vectors; both layouts keep the 8x8 matrix loads free of bank
+// conflicts.  The CTAs of a cluster split the (sequence, head)'s tiles
 // evenly (a chunk cut between CTAs is set up by each, and each folds its own
 // share of the value patch), CL chosen from the occupancy query so the grid
 // runs in as few waves as possible (a cluster must sit in one GPC); rank 0
 // merges the partial softmax states through distributed shared memory.
 #include <cooperative_groups.h>
 #include <cstdint>
+#include <cstring>
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "kamera_common.cuh"
@@ -52,15 +57,25 @@ constexpr int kAtMaxG = 8;    // query heads per KV head
 constexpr int kAtMaxCL = 8;
 
 // D: head dim (64 or 128); MP: the padded rank the instantiation takes (0, 16, 32, 64).
+// The canonical rows of a tile arrive by TMA as 128B-swizzled boxes of 64
+// columns x 64 tokens (16-byte piece c of row r at piece c ^ (r & 7)); the U
+// rows, narrower and per chunk, by 16-byte async copies into rows padded to an
+// odd number of 16-byte vectors.  Both layouts keep the 8x8 matrix loads free
+// of bank conflicts.
 template <int D, int MP>
-struct __align__(16) AtSmem {
+struct AtSmem {
     static constexpr int KW = D + MP;    // tile row: k | u (key tile), v | u' (value tile)
-    static constexpr int RS = KW + 8;    // row stride: an odd number of 16-byte vectors
+    static constexpr int NB = D / 64;    // 64-column boxes of a head row
+    static constexpr int RS = KW + 8;    // query-part row stride: an odd number of 16-byte vectors
     static constexpr int NT = KW / 8;    // 8-column tiles of the value side
     static constexpr int MPa = MP > 0 ? MP : 1;
+    static constexpr int URS = MP + 8;   // U row stride
     static constexpr int NS = KW > 160 ? 3 : 4;   // tile buffers: NS - 1 tiles in flight while one is used
-    __nv_bfloat16 kt[NS][kAtT][RS];      // key tiles; the partial outputs at the end
-    __nv_bfloat16 vt[NS][kAtT][RS];      // value tiles
+    static constexpr uint32_t kBoxBytes = kAtT * 128;
+    __nv_bfloat16 kt[NS][NB][kAtT][64];  // key rows (TMA boxes); the partial outputs at the end
+    __nv_bfloat16 vt[NS][NB][kAtT][64];  // value rows
+    __nv_bfloat16 ut[NS][kAtT][URS];     // U rows of the key tiles
+    __nv_bfloat16 uv[NS][kAtT][URS];     // U' rows of the value tiles
     __nv_bfloat16 xh[kAtH][RS];          // per-chunk query part R(-delta) q | V_k^T q, bf16 hi
     __nv_bfloat16 xl[kAtH][RS];          // and lo
     __nv_bfloat16 q[kAtH][D];            // the queries (target frame; rows past G zero)
@@ -74,6 +89,16 @@ struct __align__(16) AtSmem {
     float wsum[kAtH][MPa];               // sum_j p_j u'_j of the chunk, at its end
     float cm[kAtH], cl[kAtH];            // this CTA's softmax state, for the merge
     float fac[kAtH][kAtMaxCL];           // merge weights (rank 0)
+    uint64_t full[NS];                   // the TMA boxes of buffer b have landed
+    int32_t abort;                       // a wait ran out: the rest of the work is skipped
+};
+
+// The launch: parameters and the tensor maps of the key and value rows
+// ([num_rows][H * d], boxes of 64 columns x 64 rows).
+struct AttendLaunch {
+    AttendParams p;
+    CUtensorMap map_k, map_v;
+    uint64_t wait_ns;
 };
 
 __device__ __forceinline__ int32_t attend_check(const KameraChunk& ch, int c, const AttendParams& p)
@@ -98,26 +123,25 @@ __device__ __forceinline__ int32_t attend_check(const KameraChunk& ch, int c, co
     return bits;
 }
 
-// Copies tile rows j0 .. j0 + n - 1 of chunk `ch` (KV head g) into buffer b;
-// rows past n and U columns past the rank are zero.
+// Starts the copies of tile rows j0 .. j0 + n - 1 of chunk `ch` (KV head g)
+// into buffer b: one thread issues the TMA boxes of the key and value rows
+// (rows past the chunk come from the store or read as zero; the caller clears
+// the value rows past n once they land), every thread the async copies of the
+// U rows (zero past n and past the rank).  One copy group per call.
 template <int D, int MP>
-__device__ __forceinline__ void attend_load(const AttendParams& p, const KameraChunk& ch, int g, int j0, int n,
-                                            int b, AtSmem<D, MP>& s)
+__device__ __forceinline__ void attend_load(const AttendLaunch& P, const KameraChunk& ch, int g, int j0, int n, int b,
+                                            AtSmem<D, MP>& s)
 {
-    constexpr int VPR = D / 8;   // 16-byte vectors of a head row
-    const int64_t row0 = ch.src_offset + j0;
-    const __nv_bfloat16* kg = p.k + row0 * p.row_stride + (int64_t)g * D;
-    const __nv_bfloat16* vg = p.v + row0 * p.row_stride + (int64_t)g * D;
-    for (int e = threadIdx.x; e < kAtT * VPR; e += kAtThreads) {
-        const int t = e / VPR, v = e - t * VPR;
-        const uint32_t dk = ptx::smem_addr(&s.kt[b][t][8 * v]), dv = ptx::smem_addr(&s.vt[b][t][8 * v]);
-        if (t < n) {
-            const int64_t off = (int64_t)t * p.row_stride + 8 * v;
-            ptx::cp_async16(dk, kg + off);
-            ptx::cp_async16(dv, vg + off);
-        } else {
-            ptx::st_shared_zero16(dk);
-            ptx::st_shared_zero16(dv);
+    using SM = AtSmem<D, MP>;
+    const AttendParams& p = P.p;
+    if (threadIdx.x == 0) {
+        const uint32_t bar = ptx::smem_addr(&s.full[b]);
+        const int y = (int)(ch.src_offset + j0);
+        ptx::mbar_arrive_expect_tx(bar, 2u * SM::NB * SM::kBoxBytes);
+#pragma unroll
+        for (int x = 0; x < SM::NB; ++x) {
+            ptx::tma_load_2d(ptx::smem_addr(&s.kt[b][x][0][0]), &P.map_k, g * D + 64 * x, y, bar);
+            ptx::tma_load_2d(ptx::smem_addr(&s.vt[b][x][0][0]), &P.map_v, g * D + 64 * x, y, bar);
         }
     }
     if constexpr (MP > 0) {
@@ -129,8 +153,8 @@ __device__ __forceinline__ void attend_load(const AttendParams& p, const KameraC
             constexpr int UV = MP / 8;
             for (int e = threadIdx.x; e < kAtT * UV; e += kAtThreads) {
                 const int t = e / UV, v = e - t * UV;
-                const uint32_t dk = ptx::smem_addr(&s.kt[b][t][D + 8 * v]);
-                const uint32_t dv = ptx::smem_addr(&s.vt[b][t][D + 8 * v]);
+                const uint32_t dk = ptx::smem_addr(&s.ut[b][t][8 * v]);
+                const uint32_t dv = ptx::smem_addr(&s.uv[b][t][8 * v]);
                 if (t < n && 8 * v < m) {
                     const int64_t off = fo + (int64_t)t * m + 8 * v;
                     ptx::cp_async16(dk, uk + off);
@@ -148,21 +172,47 @@ __device__ __forceinline__ void attend_load(const AttendParams& p, const KameraC
                     a = uk[fo + (int64_t)t * m + r];
                     c = uv[fo + (int64_t)t * m + r];
                 }
-                s.kt[b][t][D + r] = a;
-                s.vt[b][t][D + r] = c;
+                s.ut[b][t][r] = a;
+                s.uv[b][t][r] = c;
             }
         }
     }
     ptx::cp_async_commit();
 }
 
+// Bounded wait on buffer b's TMA boxes.  On expiry the call reports
+// KAMERA_DEVERR_TIMEOUT, every later wait of the CTA returns at once, and the
+// kernel runs its barriers to the end (its output is then undefined).
+__device__ __forceinline__ bool attend_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort, int32_t* err,
+                                            uint64_t limit)
+{
+    if (ptx::mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 63u) == 0) {
+            if (*abort)
+                return false;
+            if (ptx::globaltimer() - t0 > limit) {
+                *abort = 1;
+                raise_err(err, KAMERA_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
+}
+
 template <int D, int MP>
-__global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_constant__ AttendParams p)
+__global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_constant__ AttendLaunch P)
 {
     using SM = AtSmem<D, MP>;
+    const AttendParams& p = P.p;
     constexpr int NTW = (SM::NT + 7) / 8;   // value-side column tiles per warp
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    SM& s = *reinterpret_cast<SM*>(smem_raw);
+    // swizzled TMA boxes want 1024-byte alignment (the same offset in every CTA)
+    SM& s = *reinterpret_cast<SM*>(smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u));
     namespace cg = cooperative_groups;
     const int CL = p.cluster, rank = (int)(blockIdx.x % (unsigned)CL);
     const int seq = blockIdx.x / CL, g = blockIdx.y;
@@ -190,6 +240,17 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
         const int h = e / D, i = e - h * D;
         s.q[h][i] = h < G ? p.q[((int64_t)seq * HQ + g * G + h) * D + i] : __float2bfloat16_rn(0.f);
     }
+    if (threadIdx.x == 0) {
+        for (int b = 0; b < SM::NS; ++b)
+            ptx::mbar_init(ptx::smem_addr(&s.full[b]), 1);
+        s.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (threadIdx.x == 32) {
+        ptx::prefetch_tmap(&P.map_k);
+        ptx::prefetch_tmap(&P.map_v);
+    }
+    uint32_t ph = 0;   // phase parity of each buffer's barrier
 
     float o[NTW][4];   // value-side tile warp + 8 k: rows gq, gq + 8; columns 2 t4, + 1
 #pragma unroll
@@ -198,8 +259,10 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
     float m_run = -INFINITY, l_run = 0.f;   // head threadIdx.x / 16
     const RopeParams& rp = p.rope;
     const int ro = rp.rot_offset, rr = rp.rot_dim, half = rr / 2;
-    const uint32_t kt0 = ptx::smem_addr(&s.kt[0][0][0]), vt0 = ptx::smem_addr(&s.vt[0][0][0]);
-    constexpr uint32_t kBuf = (uint32_t)(kAtT * SM::RS * 2);   // bytes per tile buffer
+    const uint32_t kt0 = ptx::smem_addr(&s.kt[0][0][0][0]), vt0 = ptx::smem_addr(&s.vt[0][0][0][0]);
+    const uint32_t ut0 = ptx::smem_addr(&s.ut[0][0][0]), uv0 = ptx::smem_addr(&s.uv[0][0][0]);
+    constexpr uint32_t kBuf = SM::NB * SM::kBoxBytes;            // bytes per row buffer
+    constexpr uint32_t kUBuf = (uint32_t)(kAtT * SM::URS * 2);   // bytes per U buffer
 
     int64_t pos = 0;   // tiles of the sequence before chunk c
     for (int c = c0; c < c1; ++c) {
@@ -243,7 +306,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
         for (int j = 0; j < SM::NS - 1; ++j) {   // the first NS - 1 tiles land during set-up
             const int tj = t_lo + j;
             if (tj < t_hi)
-                attend_load<D, MP>(p, ch, g, tj * kAtT, min(kAtT, len - tj * kAtT), j, s);
+                attend_load<D, MP>(P, ch, g, tj * kAtT, min(kAtT, len - tj * kAtT), j, s);
             else
                 ptx::cp_async_commit();   // one copy group per tile slot, empty or not
         }
@@ -293,16 +356,26 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
         for (int tl = t_lo; tl < t_hi; ++tl) {
             const int i = tl - t_lo, b = i % SM::NS, ntok = min(kAtT, len - tl * kAtT);
             ptx::cp_async_wait<SM::NS - 2>();   // this thread's copies of tile tl (NS - 2 newer groups may fly)
+            attend_wait(ptx::smem_addr(&s.full[b]), (ph >> b) & 1u, &s.abort, p.err, P.wait_ns);
+            ph ^= 1u << b;
+            const uint32_t kb = kt0 + b * kBuf, vb = vt0 + b * kBuf;
+            if (ntok < kAtT) {   // value rows past the chunk: zero, so that their zero weights add nothing
+                for (int e = threadIdx.x; e < (kAtT - ntok) * 8 * SM::NB; e += kAtThreads) {
+                    const int r = ntok + e / (8 * SM::NB), c = e % (8 * SM::NB);
+                    ptx::st_shared_zero16(vb + (c >> 3) * SM::kBoxBytes + r * 128 + (c & 7) * 16);
+                }
+                ptx::fence_proxy_async();   // before a later TMA load refills the buffer
+            }
             __syncthreads();   // tile b (and, first, the chunk's query part) in place; every warp is
                                // done with tile tl - 1, its buffer and its scores and weights
             {   // tile tl + NS - 1 into the buffer tile tl - 1 has left
                 const int tn = tl + SM::NS - 1;
                 if (tn < t_hi)
-                    attend_load<D, MP>(p, ch, g, tn * kAtT, min(kAtT, len - tn * kAtT), (i + SM::NS - 1) % SM::NS, s);
+                    attend_load<D, MP>(P, ch, g, tn * kAtT, min(kAtT, len - tn * kAtT), (i + SM::NS - 1) % SM::NS, s);
                 else
                     ptx::cp_async_commit();
             }
-            const uint32_t kb = kt0 + b * kBuf, vb = vt0 + b * kBuf;
+            const uint32_t ub = ut0 + b * kUBuf, uvb = uv0 + b * kUBuf;
             {   // scores of tokens 8 warp .. + 7 against the (padded) 16 heads; k-step ks adds
                 // its hi and lo products to sums 2 (ks & 1) and 2 (ks & 1) + 1, so a wider
                 // instantiation's padded U columns add exact zeros at the chains' ends
@@ -310,12 +383,18 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     sa[u][0] = sa[u][1] = sa[u][2] = sa[u][3] = 0.f;
-                const uint32_t krow = kb + (uint32_t)(((8 * warp + (lane & 7)) * SM::RS + 8 * ((lane >> 3) & 1)) * 2);
+                // key row r = 8 warp + (lane & 7), 16-byte piece 2 ks + hi of the row
+                const int kr = 8 * warp + (lane & 7), hi = (lane >> 3) & 1;
+                const uint32_t krow = kb + (uint32_t)(kr * 128), lx = (uint32_t)(hi ^ (lane & 7));
+                const uint32_t urow = ub + (uint32_t)((kr * SM::URS + 8 * hi) * 2);
                 const uint32_t xa = ptx::smem_addr(&s.xh[arow][acol]), xla = ptx::smem_addr(&s.xl[arow][acol]);
 #pragma unroll
                 for (int ks = 0; ks < SM::KW / 16; ++ks) {
                     uint32_t bb[2], ah[4], al[4];
-                    ldsm_x2(krow + 32 * ks, bb);
+                    if (ks < D / 16)
+                        ldsm_x2(krow + (uint32_t)((2 * ks) >> 3) * SM::kBoxBytes + ((((uint32_t)(2 * ks) & 7u) ^ lx) << 4), bb);
+                    else
+                        ldsm_x2(urow + 32 * (ks - D / 16), bb);
                     ldsm_x4(xa + 32 * ks, ah);
                     ldsm_x4(xla + 32 * ks, al);
                     mma_bf16(sa[2 * (ks & 1)], ah, bb[0], bb[1]);
@@ -373,7 +452,9 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
                     }
                 }
                 const uint32_t pha = ptx::smem_addr(&s.ph[arow][acol]), pla = ptx::smem_addr(&s.pl[arow][acol]);
-                const uint32_t vrow = vb + (uint32_t)(((lane & 15) * SM::RS) * 2);
+                // value row 16 ks + (lane & 15); column tile ntile = 16-byte piece ntile of the row
+                const uint32_t vrow = vb + (uint32_t)((lane & 15) * 128) + ((uint32_t)(warp ^ (lane & 7)) << 4);
+                const uint32_t uvrow = uvb + (uint32_t)(((lane & 15) * SM::URS + 8 * warp) * 2);
 #pragma unroll
                 for (int ks = 0; ks < kAtT / 16; ++ks) {
                     uint32_t ah[4], al[4];
@@ -384,7 +465,10 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
                         const int ntile = warp + 8 * k;
                         if (ntile < SM::NT) {
                             uint32_t bb[2];
-                            ldsm_x2_t(vrow + (uint32_t)((ks * 16 * SM::RS + 8 * ntile) * 2), bb);
+                            if (8 * k < D / 8)   // a canonical column tile: box k, piece warp
+                                ldsm_x2_t(vrow + (uint32_t)k * SM::kBoxBytes + (uint32_t)(ks * 16 * 128), bb);
+                            else                 // a U' column tile
+                                ldsm_x2_t(uvrow + (uint32_t)(((ks * 16) * SM::URS + 8 * (8 * k - D / 8)) * 2), bb);
                             mma_bf16(o[k], ah, bb[0], bb[1]);
                             mma_bf16(o[k], al, bb[0], bb[1]);
                         }
@@ -438,7 +522,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
     // merge: every CTA publishes (max, sum, unnormalised output); rank 0 combines
     ptx::cp_async_wait<0>();
     __syncthreads();   // the tile buffers are free
-    float* ob = reinterpret_cast<float*>(&s.kt[0][0][0]);   // [kAtH][D]
+    float* ob = reinterpret_cast<float*>(&s.kt[0][0][0][0]);   // [kAtH][D]
 #pragma unroll
     for (int k = 0; k < NTW; ++k) {
         const int ntile = warp + 8 * k;
@@ -528,9 +612,20 @@ static int attend_pick_cluster(const AttendParams& p, int bytes, int fallback)
 }
 
 template <int D, int MP>
-static cudaError_t launch_attend_m(AttendParams p, cudaStream_t stream)
+static cudaError_t launch_attend_m(const AttendParams& p0, cudaStream_t stream)
 {
-    const int bytes = (int)sizeof(AtSmem<D, MP>);
+    AttendLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    L.p = p0;
+    AttendParams& p = L.p;
+    L.wait_ns = wait_limit_ns();
+    // key and value rows: [num_rows][H * d] (an empty store gets a one-row map no tile reads)
+    const int64_t rows = p.num_rows > 0 ? p.num_rows : 1, width = (int64_t)p.H * D;
+    if (!make_rows_map(&L.map_k, p.k, rows, width, p.row_stride, 64, kAtT) ||
+        !make_rows_map(&L.map_v, p.v, rows, width, p.row_stride, 64, kAtT))
+        return cudaErrorInvalidValue;
+    static_assert(sizeof(AtSmem<D, MP>) + 1024 <= 227 * 1024, "attention tile buffers exceed shared memory");
+    const int bytes = (int)sizeof(AtSmem<D, MP>) + 1024;   // + the 1024-byte alignment
     cudaError_t e = cudaFuncSetAttribute(attend_kernel<D, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess)
         return e;
@@ -547,7 +642,7 @@ static cudaError_t launch_attend_m(AttendParams p, cudaStream_t stream)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, attend_kernel<D, MP>, p);
+    return cudaLaunchKernelEx(&cfg, attend_kernel<D, MP>, L);
 }
 
 template <int D>

@@ -55,6 +55,13 @@ cudaError_t launch_attend(const AttendParams& p, cudaStream_t stream);
 bool mla_attend_supported(int kv_lora, int rope_dim, int num_q_heads, int max_rank);
 cudaError_t launch_mla_attend(const MlaAttendParams& p, cudaStream_t stream);   // picks p.cluster
 
+// 2-D tensor map (a CUtensorMap, 64-byte aligned, at `map`) over a bf16 array
+// of `rows` rows of `width` elements, row_stride elements apart: boxes of
+// box_cols x box_rows, 128-byte swizzle, rows past the end read as zero.
+// False if the driver has no encoder or refuses the shape.
+bool make_rows_map(void* map, const void* base, int64_t rows, int64_t width, int64_t row_stride, int box_cols,
+                   int box_rows);
+
 // Tensor-core path (tcgen05 MMA for the rank-m patch; relocation with rank > 0).
 bool umma_supported(const RowsParams& p, int family);
 size_t umma_smem_bytes(const RowsParams& p);

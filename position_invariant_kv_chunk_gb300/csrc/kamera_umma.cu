@@ -1055,6 +1055,21 @@ cudaError_t launch_kernel(const UmmaParams& core, const KameraChunk* h_chunks, i
 
 }  // namespace
 
+bool make_rows_map(void* map, const void* base, int64_t rows, int64_t width, int64_t row_stride, int box_cols,
+                   int box_rows)
+{
+    auto fn = encode_fn();
+    if (!fn || rows < 1 || width < 1)
+        return false;
+    cuuint64_t dims[2] = {(cuuint64_t)width, (cuuint64_t)rows};
+    cuuint64_t strides[1] = {(cuuint64_t)row_stride * 2u};
+    cuuint32_t box[2] = {(cuuint32_t)box_cols, (cuuint32_t)box_rows};
+    cuuint32_t estr[2] = {1u, 1u};
+    return fn(static_cast<CUtensorMap*>(map), CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims,
+              strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+              CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 cudaError_t launch_umma(const RowsParams& rp, int family, const KameraChunk* h_chunks, cudaStream_t stream)
 {
     UmmaParams p;

@@ -254,6 +254,23 @@ def test_mla_attend_argument_errors():
     assert out.shape == (0, 16, 512)
 
 
+def test_attend_store_row_bound():
+    """Attention addresses tile rows with 32-bit coordinates: a store of more
+    than 2^31 - 1 rows is UNSUPPORTED, checked before any pointer is used."""
+    lib = K.load_library()
+    fake = 1 << 20   # never dereferenced: the call returns first
+    kv = K._AttnKV(fake, fake, 1 << 31, 128, 2, 64, 0, 0)
+    q = K._AttnQuery(fake, fake + (1 << 16), 1, 4, 0.125, 0)
+    r, keep = K.Rope(1e4, 64)._c(1)
+    rc = lib.kamera_attend_reused(C.byref(kv), C.byref(q), C.byref(r), C.c_void_p(fake), C.c_void_p(fake), 1, 8, 0,
+                                  None, None)
+    assert rc == 3
+    kv.num_rows = -1
+    assert lib.kamera_attend_reused(C.byref(kv), C.byref(q), C.byref(r), C.c_void_p(fake), C.c_void_p(fake), 1, 8,
+                                    0, None, None) == 1
+    del keep
+
+
 def test_compute_calls_take_cuda_tensors_only(monkeypatch):
     """Where CUDA is present, every tensor a compute entry point reads or writes
     must be a CUDA tensor (a host address is not a device address); the binding
