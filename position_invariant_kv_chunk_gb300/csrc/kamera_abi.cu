@@ -182,28 +182,32 @@ int check_strided(const void* base, int64_t L, int64_t ls, int64_t rows, int64_t
 
 // Kernel choice: the tensor-core path whenever the call carries patches and
 // its shape fits (head_dim 64/128, whole-head rotary; MLA c_KV in 128-blocks
-// and a 64/128 k_rope), the slide kernel for the in-place rotation when its
-// rotary units tile a block, the CUDA-core path otherwise.  KAMERA_PATH=simt
-// or =umma in the environment pins one of them (testing both on one input).
+// and a 64/128 k_rope), except for short chunks with tiny ranks; the slide
+// kernel for the in-place rotation when its rotary units tile a block; the
+// CUDA-core path otherwise.  Chunks of at most 128 tokens with ranks <= 8 go to
+// the CUDA-core path: its independent CTAs (8 FMAs an element for the patch)
+// beat the tensor-core pipeline, whose fixed cost per tile dominates one-tile
+// jobs (4096 chunks of 128 tokens, rank 4: 244 against 428 us; rank 8: 333
+// against 354 us; rank 16, or rank 8 on 1296-token chunks, favours the tensor
+// cores).  KAMERA_PATH=simt in the environment pins the CUDA-core path,
+// KAMERA_PATH=umma the tensor-core path wherever it applies (testing both on
+// one input).
 int launch(const RowsParams& p, int family, const KameraChunk* h_chunks, cudaStream_t stream)
 {
     const char* force = std::getenv("KAMERA_PATH");
     const bool want_simt = force && std::strcmp(force, "simt") == 0;
     const bool want_umma = force && std::strcmp(force, "umma") == 0;
-    if (!want_simt && family != FAMILY_SLIDE && umma_supported(p, family)) {
-        if (umma_smem_bytes(p) > 227u * 1024u)
-            return KAMERA_ERR_UNSUPPORTED;
+    const bool tc_ok = family != FAMILY_SLIDE && umma_supported(p, family) && umma_smem_bytes(p) <= 227u * 1024u;
+    const int64_t tiles = (p.max_len + 63) / 64;
+    const bool simt_ok = simt_smem_bytes(p, family, 64) <= 227u * 1024u &&
+                         (int64_t)p.n_chunks * tiles <= 0x7FFFFFFFll && p.L <= 65535;
+    const bool short_small = p.max_rank <= 8 && p.max_len <= 128;
+    const bool use_tc = !want_simt && tc_ok && (want_umma || !(short_small && simt_ok));
+    if (use_tc)
         return launch_umma(p, family, h_chunks, stream) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
-    }
-    if (want_umma)
-        return KAMERA_ERR_UNSUPPORTED;
     if (!want_simt && family == FAMILY_SLIDE && p.L <= 65535 && slide_supported(p))
         return launch_slide(p, stream) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
-    const size_t smem = simt_smem_bytes(p, family, 64);
-    if (smem > 227u * 1024u)
-        return KAMERA_ERR_UNSUPPORTED;
-    const int64_t tiles = (p.max_len + 63) / 64;
-    if ((int64_t)p.n_chunks * tiles > 0x7FFFFFFFll || p.L > 65535)
+    if (!simt_ok)
         return KAMERA_ERR_UNSUPPORTED;
     return launch_simt(p, family, stream) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
 }

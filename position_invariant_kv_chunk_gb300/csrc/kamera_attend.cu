@@ -13,26 +13,32 @@
 // elements per token and KV head) and never writes a relocated row.
 //
 // A cluster of CL CTAs owns (sequence, KV head) and serves its G query heads,
-// so each row is read once for all of them.  Per 64-token tile the work is two
-// small dense products: S[G x 64] = [R(-delta) q | V_k^T q] [k | u]^T and
-// [O | W][G x (d + m)] += P [v | u'], with W = sum_j p_j u'_j folded through V_v
-// when the chunk ends.  The G query heads (padded to 16) are the rows of
-// warp-level bf16 MMAs (m16n8k16, fp32 accumulate): a decode step has at most
-// 8 query rows per KV head, far below the 64-row minimum of the tensor-memory
-// MMA.  The per-chunk query part and the softmax weights are not bf16 values,
-// so they enter as bf16 hi + lo pairs (about 16 significant bits); the rows and
-// U rows are exact bf16.  Warp w computes the scores of tokens 8w .. 8w + 7
-// and owns value-side column tiles w, w + 8, ...; the online softmax runs with
-// 16 threads per head.  A ring of three or four tile buffers keeps the next
-// tiles in flight: the key and value rows arrive as 128B-swizzled TMA boxes
-// (one thread issues them; completion on an mbarrier, every wait bounded in
-// time), the U rows as 16-byte async copies into rows padded to an odd number
-// of 16-byte vectors; both layouts keep the 8x8 matrix loads free of bank
-// conflicts.  The CTAs of a cluster split the (sequence, head)'s tiles
-// evenly (a chunk cut between CTAs is set up by each, and each folds its own
-// share of the value patch), CL chosen from the occupancy query so the grid
-// runs in as few waves as possible (a cluster must sit in one GPC); rank 0
-// merges the partial softmax states through distributed shared memory.
+// so each row is read once for all of them.  The G query heads (padded to 16)
+// are the rows of warp-level bf16 MMAs (m16n8k16, fp32 accumulate): a decode
+// step has at most 8 query rows per KV head, far below the 64-row minimum of
+// the tensor-memory MMA.  The per-chunk query part and the softmax weights are
+// not bf16 values, so they enter as bf16 hi + lo pairs (about 16 significant
+// bits); the rows and U rows are exact bf16.
+//
+// Tiles hold 128 tokens; warp w owns tokens 16w .. 16w + 15 of every
+// tile and runs the whole of attention over them in registers: the scores
+// S[16 x 16] = [R(-delta) q | V_k^T q] [k | u]^T, its own online softmax
+// (running max and sum per head), and [O | W][16 x (d + m)] += P [v | u'] with
+// the weights passed from the score fragments straight into the value MMA's
+// A operand; W = sum_j p_j u'_j is folded through V_v when the chunk ends.
+// A warp reads only its own 16 rows of a tile, so it also loads them itself,
+// NS - 1 tiles ahead into its slice of a ring of NS tile buffers: the key and
+// value rows as 128B-swizzled TMA boxes of 16 rows (lane 0 issues them), the U
+// rows as 16-byte async copies into rows padded to an odd number of 16-byte
+// vectors (both layouts keep the 8x8 matrix loads free of bank conflicts);
+// one mbarrier per warp and buffer counts both, and every wait is bounded in
+// time.  The warps meet only at chunk boundaries (the chunk's query part) and
+// at the end, where their softmax states merge through shared memory.  The CTAs of a
+// cluster split the (sequence, head)'s tiles evenly (a chunk cut between CTAs
+// is set up by each, and each folds its own share of the value patch), CL
+// chosen from the occupancy query so the grid runs in as few waves as
+// possible (a cluster must sit in one GPC); rank 0 merges the CTAs' softmax
+// states through distributed shared memory.
 #include <cooperative_groups.h>
 #include <cstdint>
 #include <cstring>
@@ -50,51 +56,48 @@ namespace {
 
 using namespace wmma16;
 
-constexpr int kAtThreads = 256;
-constexpr int kAtT = 64;      // tokens per tile
-constexpr int kAtH = 16;      // MMA rows: a KV head's query heads, padded
-constexpr int kAtMaxG = 8;    // query heads per KV head
+constexpr int kAtCW = 8;                       // warps: each owns 16 tokens of every tile
+constexpr int kAtThreads = 32 * kAtCW;
+constexpr int kAtT = 16 * kAtCW;               // tokens per tile
+constexpr int kAtWR = 16;                      // rows per warp
+constexpr int kAtH = 16;                       // MMA rows: a KV head's query heads, padded
+constexpr int kAtMaxG = 8;                     // query heads per KV head
 constexpr int kAtMaxCL = 8;
 
 // D: head dim (64 or 128); MP: the padded rank the instantiation takes (0, 16, 32, 64).
 // The canonical rows of a tile arrive by TMA as 128B-swizzled boxes of 64
-// columns x 64 tokens (16-byte piece c of row r at piece c ^ (r & 7)); the U
-// rows, narrower and per chunk, by 16-byte async copies into rows padded to an
-// odd number of 16-byte vectors.  Both layouts keep the 8x8 matrix loads free
-// of bank conflicts.
+// columns x 16 tokens, one per warp (16-byte piece c of row r at piece
+// c ^ (r & 7)); the U rows by 16-byte async copies into rows padded to an odd
+// number of 16-byte vectors.
 template <int D, int MP>
 struct AtSmem {
-    static constexpr int KW = D + MP;    // tile row: k | u (key tile), v | u' (value tile)
+    static constexpr int KW = D + MP;    // tile row: k | u (key side), v | u' (value side)
     static constexpr int NB = D / 64;    // 64-column boxes of a head row
     static constexpr int RS = KW + 8;    // query-part row stride: an odd number of 16-byte vectors
     static constexpr int NT = KW / 8;    // 8-column tiles of the value side
-    static constexpr int MPa = MP > 0 ? MP : 1;
     static constexpr int URS = MP + 8;   // U row stride
-    static constexpr int NS = KW > 160 ? 3 : 4;   // tile buffers: NS - 1 tiles in flight while one is used
+    static constexpr int UB = MP > 0 ? 1 : 0;
     static constexpr uint32_t kBoxBytes = kAtT * 128;
-    __nv_bfloat16 kt[NS][NB][kAtT][64];  // key rows (TMA boxes); the partial outputs at the end
-    __nv_bfloat16 vt[NS][NB][kAtT][64];  // value rows
-    __nv_bfloat16 ut[NS][kAtT][URS];     // U rows of the key tiles
-    __nv_bfloat16 uv[NS][kAtT][URS];     // U' rows of the value tiles
+    static constexpr uint32_t kBufBytes = 2 * NB * kBoxBytes + UB * 2 * kAtT * URS * 2;
+    static constexpr int NS = kBufBytes <= 48 * 1024 ? 4 : kBufBytes <= 64 * 1024 ? 3 : 2;   // tile buffers
+    __nv_bfloat16 kt[NS][NB][kAtT][64];  // key rows (TMA boxes); the warps' partial outputs at the end
+    __nv_bfloat16 vt[NS][NB][kAtT][64];  // value rows; the CTA's output at the end
+    __nv_bfloat16 ut[UB ? NS : 1][kAtT][URS];   // U rows of the key side
+    __nv_bfloat16 uv[UB ? NS : 1][kAtT][URS];   // U' rows of the value side
     __nv_bfloat16 xh[kAtH][RS];          // per-chunk query part R(-delta) q | V_k^T q, bf16 hi
     __nv_bfloat16 xl[kAtH][RS];          // and lo
     __nv_bfloat16 q[kAtH][D];            // the queries (target frame; rows past G zero)
-    float sc[kAtH][kAtT + 4];            // scores of the tile
-    __nv_bfloat16 ph[kAtH][kAtT + 8];    // softmax weights, hi
-    __nv_bfloat16 pl[kAtH][kAtT + 8];    // and lo
-    float alpha[kAtH];                   // running-max rescale of the tile
     float2 cs[D / 2];                    // cos/sin of -delta
-    static constexpr int VKS = MPa + 8;  // V_k row stride: an odd number of 16-byte vectors
-    __nv_bfloat16 vk[D][VKS];            // V_k of this (layer, head), staged per chunk
-    float wsum[kAtH][MPa];               // sum_j p_j u'_j of the chunk, at its end
-    float cm[kAtH], cl[kAtH];            // this CTA's softmax state, for the merge
-    float fac[kAtH][kAtMaxCL];           // merge weights (rank 0)
-    uint64_t full[NS];                   // the TMA boxes of buffer b have landed
-    int32_t abort;                       // a wait ran out: the rest of the work is skipped
+    float wm[kAtCW][kAtH], wl[kAtCW][kAtH];   // the warps' softmax states
+    float wf[kAtH][kAtCW];               // their merge weights
+    float cm[kAtH], cl[kAtH];            // this CTA's softmax state, for the cluster merge
+    float fac[kAtH][kAtMaxCL];           // cluster merge weights (rank 0)
+    uint64_t full[kAtCW][NS];            // warp w's rows of buffer b: TMA bytes + its lanes' copies
+    int32_t abort;                       // a wait ran out: every later wait returns at once
 };
 
 // The launch: parameters and the tensor maps of the key and value rows
-// ([num_rows][H * d], boxes of 64 columns x 64 rows).
+// ([num_rows][H * d], boxes of 64 columns x 16 rows).
 struct AttendLaunch {
     AttendParams p;
     CUtensorMap map_k, map_v;
@@ -123,64 +126,7 @@ __device__ __forceinline__ int32_t attend_check(const KameraChunk& ch, int c, co
     return bits;
 }
 
-// Starts the copies of tile rows j0 .. j0 + n - 1 of chunk `ch` (KV head g)
-// into buffer b: one thread issues the TMA boxes of the key and value rows
-// (rows past the chunk come from the store or read as zero; the caller clears
-// the value rows past n once they land), every thread the async copies of the
-// U rows (zero past n and past the rank).  One copy group per call.
-template <int D, int MP>
-__device__ __forceinline__ void attend_load(const AttendLaunch& P, const KameraChunk& ch, int g, int j0, int n, int b,
-                                            AtSmem<D, MP>& s)
-{
-    using SM = AtSmem<D, MP>;
-    const AttendParams& p = P.p;
-    if (threadIdx.x == 0) {
-        const uint32_t bar = ptx::smem_addr(&s.full[b]);
-        const int y = (int)(ch.src_offset + j0);
-        ptx::mbar_arrive_expect_tx(bar, 2u * SM::NB * SM::kBoxBytes);
-#pragma unroll
-        for (int x = 0; x < SM::NB; ++x) {
-            ptx::tma_load_2d(ptx::smem_addr(&s.kt[b][x][0][0]), &P.map_k, g * D + 64 * x, y, bar);
-            ptx::tma_load_2d(ptx::smem_addr(&s.vt[b][x][0][0]), &P.map_v, g * D + 64 * x, y, bar);
-        }
-    }
-    if constexpr (MP > 0) {
-        const int m = ch.rank;
-        const int64_t fo = ((int64_t)(p.layer * p.H + g) * ch.len + j0) * m;   // U [L][H][len][m]
-        const __nv_bfloat16* uk = patch_ptr(ch, 0);
-        const __nv_bfloat16* uv = patch_ptr(ch, 2);
-        if ((m & 7) == 0) {   // whole 16-byte vectors (m = 0 too: all zeros)
-            constexpr int UV = MP / 8;
-            for (int e = threadIdx.x; e < kAtT * UV; e += kAtThreads) {
-                const int t = e / UV, v = e - t * UV;
-                const uint32_t dk = ptx::smem_addr(&s.ut[b][t][8 * v]);
-                const uint32_t dv = ptx::smem_addr(&s.uv[b][t][8 * v]);
-                if (t < n && 8 * v < m) {
-                    const int64_t off = fo + (int64_t)t * m + 8 * v;
-                    ptx::cp_async16(dk, uk + off);
-                    ptx::cp_async16(dv, uv + off);
-                } else {
-                    ptx::st_shared_zero16(dk);
-                    ptx::st_shared_zero16(dv);
-                }
-            }
-        } else {   // other ranks: element by element
-            for (int e = threadIdx.x; e < kAtT * MP; e += kAtThreads) {
-                const int t = e / MP, r = e - t * MP;
-                __nv_bfloat16 a = __float2bfloat16_rn(0.f), c = a;
-                if (t < n && r < m) {
-                    a = uk[fo + (int64_t)t * m + r];
-                    c = uv[fo + (int64_t)t * m + r];
-                }
-                s.ut[b][t][r] = a;
-                s.uv[b][t][r] = c;
-            }
-        }
-    }
-    ptx::cp_async_commit();
-}
-
-// Bounded wait on buffer b's TMA boxes.  On expiry the call reports
+// Bounded wait on an mbarrier phase.  On expiry the call reports
 // KAMERA_DEVERR_TIMEOUT, every later wait of the CTA returns at once, and the
 // kernel runs its barriers to the end (its output is then undefined).
 __device__ __forceinline__ bool attend_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort, int32_t* err,
@@ -204,12 +150,87 @@ __device__ __forceinline__ bool attend_wait(uint32_t bar, uint32_t parity, volat
     }
 }
 
+// The CTA's share of a sequence: tiles [lo, hi) of its valid chunks' tiles in
+// order; for chunk c (nt tiles, pos tiles before it) the tiles [t_lo, t_hi).
+__device__ __forceinline__ void share_of_chunk(int64_t lo, int64_t hi, int64_t pos, int nt, int& t_lo, int& t_hi)
+{
+    const int64_t a0 = lo - pos, a1 = hi - pos;
+    t_lo = a0 > 0 ? (int)a0 : 0;
+    t_hi = a1 < nt ? (int)a1 : nt;
+}
+
+// Moves (c, tl) to the next tile of the CTA's share (t_hi: end of chunk c's
+// share, pos: tiles of the sequence before chunk c + 1); false past the last.
+__device__ __forceinline__ bool next_tile(const AttendParams& p, int c1, int64_t lo, int64_t hi, int& c, int& tl,
+                                          int& t_hi, int64_t& pos)
+{
+    if (++tl < t_hi)
+        return true;
+    for (++c; c < c1; ++c) {
+        const KameraChunk& ch = p.chunks[c];
+        if (attend_check(ch, c, p))
+            continue;
+        const int nt = (ch.len + kAtT - 1) / kAtT;
+        int a, b;
+        share_of_chunk(lo, hi, pos, nt, a, b);
+        pos += nt;
+        if (a < b) {
+            tl = a;
+            t_hi = b;
+            return true;
+        }
+    }
+    return false;
+}
+
+// Warp w starts the copies of its rows (16w .. 16w + 15) of tile tl of chunk c
+// into buffer b: lane 0 the TMA boxes of the key and value rows (rows past the
+// chunk come from the store or read as zero: the warp clears the value rows
+// past it once they land), every lane the async copies of U rows whose rank
+// is a multiple of 8.  Nothing when the chunk ends before the warp's rows.
+template <int D, int MP>
+__device__ __forceinline__ void warp_load(const AttendLaunch& P, AtSmem<D, MP>& s, int c, int tl, int g, int warp,
+                                          int lane, int b)
+{
+    using SM = AtSmem<D, MP>;
+    const AttendParams& p = P.p;
+    const KameraChunk& ch = p.chunks[c];
+    const int len = ch.len, m = ch.rank, j0 = tl * kAtT, r0 = kAtWR * warp;
+    const int n = min(kAtT, len - j0);
+    if (r0 >= n)
+        return;
+    const uint32_t full = ptx::smem_addr(&s.full[warp][b]);
+    if (lane == 0) {
+        const int y = (int)(ch.src_offset + j0 + r0);
+        ptx::mbar_arrive_expect_tx(full, 2u * SM::NB * kAtWR * 128u);
+#pragma unroll
+        for (int x = 0; x < SM::NB; ++x) {
+            ptx::tma_load_2d(ptx::smem_addr(&s.kt[b][x][r0][0]), &P.map_k, g * D + 64 * x, y, full);
+            ptx::tma_load_2d(ptx::smem_addr(&s.vt[b][x][r0][0]), &P.map_v, g * D + 64 * x, y, full);
+        }
+    }
+    if constexpr (MP > 0) {
+        if (m > 0 && (m & 7) == 0) {
+            const int64_t fo = ((int64_t)(p.layer * p.H + g) * len + j0) * m;   // U [L][H][len][m]
+            const __nv_bfloat16* uk = patch_ptr(ch, 0) + fo;
+            const __nv_bfloat16* uvp = patch_ptr(ch, 2) + fo;
+            const int vpr = m >> 3, rows = min(kAtWR, n - r0);
+            for (int e = lane; e < rows * vpr; e += 32) {
+                const int t = r0 + e / vpr, v = e - (e / vpr) * vpr;
+                ptx::cp_async16(ptx::smem_addr(&s.ut[b][t][8 * v]), uk + (int64_t)t * m + 8 * v);
+                ptx::cp_async16(ptx::smem_addr(&s.uv[b][t][8 * v]), uvp + (int64_t)t * m + 8 * v);
+            }
+        }
+    }
+    ptx::cp_async_mbar_arrive_noinc(full);
+}
+
 template <int D, int MP>
 __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_constant__ AttendLaunch P)
 {
     using SM = AtSmem<D, MP>;
+    constexpr int NT = SM::NT, NS = SM::NS;
     const AttendParams& p = P.p;
-    constexpr int NTW = (SM::NT + 7) / 8;   // value-side column tiles per warp
     extern __shared__ __align__(16) unsigned char smem_raw[];
     // swizzled TMA boxes want 1024-byte alignment (the same offset in every CTA)
     SM& s = *reinterpret_cast<SM*>(smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u));
@@ -218,7 +239,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
     const int seq = blockIdx.x / CL, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, t4 = lane & 3;
     const int G = p.G, HQ = p.H * G;
-    // 8x8 matrix-load addressing: A (row-major 16 x 16) and B^T (token rows)
+    // 8x8 matrix-load addressing of a row-major 16 x 16 A operand
     const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
 
     int c0 = p.seq_start[seq], c1 = p.seq_start[seq + 1];
@@ -227,7 +248,6 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
             raise_err(p.err, KAMERA_DEVERR_DESCRIPTOR);
         c0 = c1 = 0;
     }
-    // this CTA's share: tiles [lo, hi) of the sequence's valid chunks' tiles, in order
     int64_t total = 0;
     for (int c = c0; c < c1; ++c) {
         const KameraChunk& ch = p.chunks[c];
@@ -241,8 +261,9 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
         s.q[h][i] = h < G ? p.q[((int64_t)seq * HQ + g * G + h) * D + i] : __float2bfloat16_rn(0.f);
     }
     if (threadIdx.x == 0) {
-        for (int b = 0; b < SM::NS; ++b)
-            ptx::mbar_init(ptx::smem_addr(&s.full[b]), 1);
+        for (int w = 0; w < kAtCW; ++w)
+            for (int b = 0; b < NS; ++b)
+                ptx::mbar_init(ptx::smem_addr(&s.full[w][b]), 1 + 32);   // the TMA issue + the lanes' copies
         s.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -250,292 +271,329 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
         ptx::prefetch_tmap(&P.map_k);
         ptx::prefetch_tmap(&P.map_v);
     }
-    uint32_t ph = 0;   // phase parity of each buffer's barrier
-
-    float o[NTW][4];   // value-side tile warp + 8 k: rows gq, gq + 8; columns 2 t4, + 1
-#pragma unroll
-    for (int k = 0; k < NTW; ++k)
-        o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
-    float m_run = -INFINITY, l_run = 0.f;   // head threadIdx.x / 16
+    __syncthreads();
     const RopeParams& rp = p.rope;
-    const int ro = rp.rot_offset, rr = rp.rot_dim, half = rr / 2;
-    const uint32_t kt0 = ptx::smem_addr(&s.kt[0][0][0][0]), vt0 = ptx::smem_addr(&s.vt[0][0][0][0]);
-    const uint32_t ut0 = ptx::smem_addr(&s.ut[0][0][0]), uv0 = ptx::smem_addr(&s.uv[0][0][0]);
-    constexpr uint32_t kBuf = SM::NB * SM::kBoxBytes;            // bytes per row buffer
-    constexpr uint32_t kUBuf = (uint32_t)(kAtT * SM::URS * 2);   // bytes per U buffer
 
-    int64_t pos = 0;   // tiles of the sequence before chunk c
-    for (int c = c0; c < c1; ++c) {
-        const KameraChunk& ch = p.chunks[c];
-        const int32_t bad = attend_check(ch, c, p);
-        if (bad) {
-            if (rank == 0 && threadIdx.x == 0)
-                raise_err(p.err, bad);
-            continue;
-        }
-        const int len = ch.len;
-        const int nt = (len + kAtT - 1) / kAtT;
-        const int64_t a0 = lo - pos, a1 = hi - pos;
-        const int t_lo = a0 > 0 ? (int)a0 : 0, t_hi = a1 < nt ? (int)a1 : nt;
-        pos += nt;
-        if (t_lo >= t_hi)
-            continue;
-        const int m = ch.rank;
-        __syncthreads();   // the previous chunk (or the query staging) is done with every shared array
-        const int64_t fo = (int64_t)(p.layer * p.H + g) * D * m;   // this (layer, head)'s V factors [d][m]
-        if constexpr (MP > 0) {   // V_k [d][m], zero past the rank: one copy group, older than the tiles'
-            const __nv_bfloat16* vkg = patch_ptr(ch, 1);
-            if ((m & 7) == 0) {
-                constexpr int VV = MP / 8;
-                for (int e = threadIdx.x; e < D * VV; e += kAtThreads) {
-                    const int i = e / VV, v = e - i * VV;
-                    const uint32_t dst = ptx::smem_addr(&s.vk[i][8 * v]);
-                    if (8 * v < m)
-                        ptx::cp_async16(dst, vkg + fo + (int64_t)i * m + 8 * v);
-                    else
-                        ptx::st_shared_zero16(dst);
-                }
-            } else {
-                for (int e = threadIdx.x; e < D * MP; e += kAtThreads) {
-                    const int i = e / MP, r = e - i * MP;
-                    s.vk[i][r] = r < m ? vkg[fo + (int64_t)i * m + r] : __float2bfloat16_rn(0.f);
-                }
-            }
-        }
-        ptx::cp_async_commit();
-        for (int j = 0; j < SM::NS - 1; ++j) {   // the first NS - 1 tiles land during set-up
-            const int tj = t_lo + j;
-            if (tj < t_hi)
-                attend_load<D, MP>(P, ch, g, tj * kAtT, min(kAtT, len - tj * kAtT), j, s);
-            else
-                ptx::cp_async_commit();   // one copy group per tile slot, empty or not
-        }
-        for (int f = threadIdx.x; f < rp.n_freq; f += kAtThreads) {
-            float cc, sn;
-            phase_cos_sin(-freq_delta(rp, ch, c, f), rp.inv_freq[f], cc, sn);
-            s.cs[f] = make_float2(cc, sn);
-        }
-        ptx::cp_async_wait<SM::NS - 1>();   // V_k has landed (the tiles may still be in flight)
-        __syncthreads();
-        for (int e = threadIdx.x; e < kAtH * D; e += kAtThreads) {   // q turned by -delta
-            const int h = e / D, i = e - h * D, k = i - ro;
-            float v = __bfloat162float(s.q[h][i]);
-            if (k >= 0 && k < rr) {
-                if (rp.pairing == KAMERA_ROPE_ROTATE_HALF) {
-                    const float2 t = s.cs[k < half ? k : k - half];
-                    v = k < half ? fmaf(v, t.x, -(__bfloat162float(s.q[h][i + half]) * t.y))
-                                 : fmaf(v, t.x, __bfloat162float(s.q[h][i - half]) * t.y);
-                } else {
-                    const float2 t = s.cs[k >> 1];
-                    v = (k & 1) == 0 ? fmaf(v, t.x, -(__bfloat162float(s.q[h][i + 1]) * t.y))
-                                     : fmaf(v, t.x, __bfloat162float(s.q[h][i - 1]) * t.y);
-                }
-            }
-            split1(v, s.xh[h][i], s.xl[h][i]);
-        }
-        if constexpr (MP > 0) {   // V_k^T q (the un-turned query) by warp MMAs: warp w takes ranks 8w .. 8w + 7
-            if (warp < MP / 8) {
-                float y[4] = {0.f, 0.f, 0.f, 0.f};
-                const uint32_t qa = ptx::smem_addr(&s.q[arow][acol]);
-                const uint32_t vka = ptx::smem_addr(&s.vk[lane & 15][8 * warp]);
+    {
+        // ------------------------------------------------------------ the warps
+        float o[NT][4];   // [O | W] of this warp's tokens: column tile j, rows gq and gq + 8
 #pragma unroll
-                for (int ks = 0; ks < D / 16; ++ks) {
-                    uint32_t a[4], bb[2];
-                    ldsm_x4(qa + 32 * ks, a);
-                    ldsm_x2_t(vka + (uint32_t)(16 * ks * SM::VKS * 2), bb);
-                    mma_bf16(y, a, bb[0], bb[1]);
-                }
-                const int col = D + 8 * warp + 2 * t4;   // rows gq, gq + 8 (heads); columns col, col + 1
-                split1(y[0], s.xh[gq][col], s.xl[gq][col]);
-                split1(y[1], s.xh[gq][col + 1], s.xl[gq][col + 1]);
-                split1(y[2], s.xh[gq + 8][col], s.xl[gq + 8][col]);
-                split1(y[3], s.xh[gq + 8][col + 1], s.xl[gq + 8][col + 1]);
-            }
-        }
+        for (int j = 0; j < NT; ++j)
+            o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
+        float m_run[2] = {-INFINITY, -INFINITY}, l_run[2] = {0.f, 0.f};   // heads gq, gq + 8
+        const int ro = rp.rot_offset, rr = rp.rot_dim, half = rr / 2;
+        const uint32_t kt0 = ptx::smem_addr(&s.kt[0][0][0][0]), vt0 = ptx::smem_addr(&s.vt[0][0][0][0]);
+        const uint32_t ut0 = ptx::smem_addr(&s.ut[0][0][0]), uv0 = ptx::smem_addr(&s.uv[0][0][0]);
+        constexpr uint32_t kBuf = SM::NB * SM::kBoxBytes;               // bytes per row buffer
+        constexpr uint32_t kUBuf = (uint32_t)(kAtT * SM::URS * 2);      // bytes per U buffer
+        const int r0 = 16 * warp;                                       // this warp's first token row
+        // score B operand (key rows): matrices (tokens 0-7 | 8-15) x (k 0-7 | 8-15)
+        const int kr = r0 + (lane & 7) + 8 * (lane >> 4), khi = (lane >> 3) & 1;
+        const uint32_t klx = (uint32_t)(khi ^ (lane & 7));
+        // value B operand (value rows, transposed): (tokens 0-7 | 8-15) x (tile j | j + 1)
+        const int vr = r0 + (lane & 7) + 8 * ((lane >> 3) & 1);
+        const uint32_t vlx = (uint32_t)((lane >> 4) ^ (lane & 7));
+        const uint32_t xa = ptx::smem_addr(&s.xh[arow][acol]), xla = ptx::smem_addr(&s.xl[arow][acol]);
 
-        for (int tl = t_lo; tl < t_hi; ++tl) {
-            const int i = tl - t_lo, b = i % SM::NS, ntok = min(kAtT, len - tl * kAtT);
-            ptx::cp_async_wait<SM::NS - 2>();   // this thread's copies of tile tl (NS - 2 newer groups may fly)
-            attend_wait(ptx::smem_addr(&s.full[b]), (ph >> b) & 1u, &s.abort, p.err, P.wait_ns);
-            ph ^= 1u << b;
-            const uint32_t kb = kt0 + b * kBuf, vb = vt0 + b * kBuf;
-            if (ntok < kAtT) {   // value rows past the chunk: zero, so that their zero weights add nothing
-                for (int e = threadIdx.x; e < (kAtT - ntok) * 8 * SM::NB; e += kAtThreads) {
-                    const int r = ntok + e / (8 * SM::NB), c = e % (8 * SM::NB);
-                    ptx::st_shared_zero16(vb + (c >> 3) * SM::kBoxBytes + r * 128 + (c & 7) * 16);
-                }
-                ptx::fence_proxy_async();   // before a later TMA load refills the buffer
+        // load cursor: the tile NS - 1 ahead of the one being computed
+        int lc = c0 - 1, ltl = 0, lthi = 0;
+        int64_t lpos = 0;
+        bool lmore = next_tile(p, c1, lo, hi, lc, ltl, lthi, lpos);
+        for (int j = 0; j < NS - 1 && lmore; ++j) {
+            warp_load<D, MP>(P, s, lc, ltl, g, warp, lane, j);
+            lmore = next_tile(p, c1, lo, hi, lc, ltl, lthi, lpos);
+        }
+        uint32_t ph = 0;   // phase parity of this warp's barrier per buffer
+        int gi = 0;
+        int64_t pos = 0;
+        for (int c = c0; c < c1; ++c) {
+            const KameraChunk& ch = p.chunks[c];
+            const int32_t bad = attend_check(ch, c, p);
+            if (bad) {
+                if (rank == 0 && threadIdx.x == 0)
+                    raise_err(p.err, bad);
+                continue;
             }
-            __syncthreads();   // tile b (and, first, the chunk's query part) in place; every warp is
-                               // done with tile tl - 1, its buffer and its scores and weights
-            {   // tile tl + NS - 1 into the buffer tile tl - 1 has left
-                const int tn = tl + SM::NS - 1;
-                if (tn < t_hi)
-                    attend_load<D, MP>(P, ch, g, tn * kAtT, min(kAtT, len - tn * kAtT), (i + SM::NS - 1) % SM::NS, s);
-                else
-                    ptx::cp_async_commit();
-            }
-            const uint32_t ub = ut0 + b * kUBuf, uvb = uv0 + b * kUBuf;
-            {   // scores of tokens 8 warp .. + 7 against the (padded) 16 heads; k-step ks adds
-                // its hi and lo products to sums 2 (ks & 1) and 2 (ks & 1) + 1, so a wider
-                // instantiation's padded U columns add exact zeros at the chains' ends
-                float sa[4][4];
-#pragma unroll
-                for (int u = 0; u < 4; ++u)
-                    sa[u][0] = sa[u][1] = sa[u][2] = sa[u][3] = 0.f;
-                // key row r = 8 warp + (lane & 7), 16-byte piece 2 ks + hi of the row
-                const int kr = 8 * warp + (lane & 7), hi = (lane >> 3) & 1;
-                const uint32_t krow = kb + (uint32_t)(kr * 128), lx = (uint32_t)(hi ^ (lane & 7));
-                const uint32_t urow = ub + (uint32_t)((kr * SM::URS + 8 * hi) * 2);
-                const uint32_t xa = ptx::smem_addr(&s.xh[arow][acol]), xla = ptx::smem_addr(&s.xl[arow][acol]);
-#pragma unroll
-                for (int ks = 0; ks < SM::KW / 16; ++ks) {
-                    uint32_t bb[2], ah[4], al[4];
-                    if (ks < D / 16)
-                        ldsm_x2(krow + (uint32_t)((2 * ks) >> 3) * SM::kBoxBytes + ((((uint32_t)(2 * ks) & 7u) ^ lx) << 4), bb);
-                    else
-                        ldsm_x2(urow + 32 * (ks - D / 16), bb);
-                    ldsm_x4(xa + 32 * ks, ah);
-                    ldsm_x4(xla + 32 * ks, al);
-                    mma_bf16(sa[2 * (ks & 1)], ah, bb[0], bb[1]);
-                    mma_bf16(sa[2 * (ks & 1) + 1], al, bb[0], bb[1]);
-                }
-                const int tk = 8 * warp + 2 * t4;
-                *reinterpret_cast<float2*>(&s.sc[gq][tk]) =
-                    make_float2((sa[0][0] + sa[1][0]) + (sa[2][0] + sa[3][0]), (sa[0][1] + sa[1][1]) + (sa[2][1] + sa[3][1]));
-                *reinterpret_cast<float2*>(&s.sc[gq + 8][tk]) =
-                    make_float2((sa[0][2] + sa[1][2]) + (sa[2][2] + sa[3][2]), (sa[0][3] + sa[1][3]) + (sa[2][3] + sa[3][3]));
+            const int len = ch.len, nt = (len + kAtT - 1) / kAtT, m = ch.rank;
+            int t_lo, t_hi;
+            share_of_chunk(lo, hi, pos, nt, t_lo, t_hi);
+            pos += nt;
+            if (t_lo >= t_hi)
+                continue;
+            const int64_t fo = (int64_t)(p.layer * p.H + g) * D * m;   // this (layer, head)'s V factors [d][m]
+            // ---- the chunk's query part (every warp is done with the previous one)
+            __syncthreads();
+            for (int f = threadIdx.x; f < rp.n_freq; f += kAtThreads) {
+                float cc, sn;
+                phase_cos_sin(-freq_delta(rp, ch, c, f), rp.inv_freq[f], cc, sn);
+                s.cs[f] = make_float2(cc, sn);
             }
             __syncthreads();
-            {   // online softmax: 16 threads per head, 4 tokens each
-                const int h = threadIdx.x >> 4, j0 = 4 * (threadIdx.x & 15);
-                float sv[4], tmax = -INFINITY;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    sv[u] = j0 + u < ntok ? p.scale * s.sc[h][j0 + u] : -INFINITY;
-                    tmax = fmaxf(tmax, sv[u]);
+            for (int e = threadIdx.x; e < kAtH * D; e += kAtThreads) {   // q turned by -delta
+                const int h = e / D, i = e - h * D, k = i - ro;
+                float v = __bfloat162float(s.q[h][i]);
+                if (k >= 0 && k < rr) {
+                    if (rp.pairing == KAMERA_ROPE_ROTATE_HALF) {
+                        const float2 t = s.cs[k < half ? k : k - half];
+                        v = k < half ? fmaf(v, t.x, -(__bfloat162float(s.q[h][i + half]) * t.y))
+                                     : fmaf(v, t.x, __bfloat162float(s.q[h][i - half]) * t.y);
+                    } else {
+                        const float2 t = s.cs[k >> 1];
+                        v = (k & 1) == 0 ? fmaf(v, t.x, -(__bfloat162float(s.q[h][i + 1]) * t.y))
+                                         : fmaf(v, t.x, __bfloat162float(s.q[h][i - 1]) * t.y);
+                    }
                 }
+                split1(v, s.xh[h][i], s.xl[h][i]);
+            }
+            if constexpr (MP > 0) {   // V_k^T q (the un-turned query) by warp MMAs: warp w takes ranks 8w .. 8w + 7
+                if (warp < MP / 8) {
+                    const uint16_t* vkg = reinterpret_cast<const uint16_t*>(patch_ptr(ch, 1) + fo);   // V_k [d][m]
+                    const int r = 8 * warp + gq;
+                    float y[4] = {0.f, 0.f, 0.f, 0.f};
+                    const uint32_t qa = ptx::smem_addr(&s.q[arow][acol]);
 #pragma unroll
-                for (int off = 8; off > 0; off >>= 1)
-                    tmax = fmaxf(tmax, __shfl_xor_sync(0xffffffffu, tmax, off));
-                const float mnew = fmaxf(m_run, tmax);    // finite: the tile holds a token
-                const float alpha = __expf(m_run - mnew);  // 0 while nothing was seen
-                float e[4], sum = 0.f;
-#pragma unroll
-                for (int u = 0; u < 4; ++u) {
-                    e[u] = __expf(sv[u] - mnew);
-                    sum += e[u];
+                    for (int ks = 0; ks < D / 16; ++ks) {
+                        uint32_t a[4];
+                        ldsm_x4(qa + 32 * ks, a);
+                        const int i0 = 16 * ks + 2 * t4;
+                        uint32_t b0 = 0, b1 = 0;
+                        if (r < m) {
+                            b0 = (uint32_t)vkg[(int64_t)i0 * m + r] | ((uint32_t)vkg[(int64_t)(i0 + 1) * m + r] << 16);
+                            b1 = (uint32_t)vkg[(int64_t)(i0 + 8) * m + r] |
+                                 ((uint32_t)vkg[(int64_t)(i0 + 9) * m + r] << 16);
+                        }
+                        mma_bf16(y, a, b0, b1);
+                    }
+                    const int col = D + 8 * warp + 2 * t4;   // rows gq, gq + 8 (heads); columns col, col + 1
+                    split1(y[0], s.xh[gq][col], s.xl[gq][col]);
+                    split1(y[1], s.xh[gq][col + 1], s.xl[gq][col + 1]);
+                    split1(y[2], s.xh[gq + 8][col], s.xl[gq + 8][col]);
+                    split1(y[3], s.xh[gq + 8][col + 1], s.xl[gq + 8][col + 1]);
                 }
-#pragma unroll
-                for (int off = 8; off > 0; off >>= 1)
-                    sum += __shfl_xor_sync(0xffffffffu, sum, off);
-                l_run = fmaf(l_run, alpha, sum);
-                m_run = mnew;
-                uint32_t h01, l01, h23, l23;
-                split_hl(e[0], e[1], h01, l01);
-                split_hl(e[2], e[3], h23, l23);
-                *reinterpret_cast<uint2*>(&s.ph[h][j0]) = make_uint2(h01, h23);
-                *reinterpret_cast<uint2*>(&s.pl[h][j0]) = make_uint2(l01, l23);
-                if ((threadIdx.x & 15) == 0)
-                    s.alpha[h] = alpha;
             }
             __syncthreads();
-            {   // [O | W] += P [v | u']: column tiles warp, warp + 8, ...
-                const float r0 = s.alpha[gq], r1 = s.alpha[gq + 8];
-                if (!__all_sync(0xffffffffu, r0 == 1.f && r1 == 1.f)) {   // a new running max in some row
-#pragma unroll
-                    for (int k = 0; k < NTW; ++k) {
-                        o[k][0] *= r0;
-                        o[k][1] *= r0;
-                        o[k][2] *= r1;
-                        o[k][3] *= r1;
-                    }
+
+            for (int tl = t_lo; tl < t_hi; ++tl, ++gi) {
+                const int b = gi % NS, j0 = tl * kAtT, ntok = min(kAtT, len - j0);
+                if (lmore) {   // tile gi + NS - 1 into the buffer tile gi - 1 has left
+                    warp_load<D, MP>(P, s, lc, ltl, g, warp, lane, (gi + NS - 1) % NS);
+                    lmore = next_tile(p, c1, lo, hi, lc, ltl, lthi, lpos);
                 }
-                const uint32_t pha = ptx::smem_addr(&s.ph[arow][acol]), pla = ptx::smem_addr(&s.pl[arow][acol]);
-                // value row 16 ks + (lane & 15); column tile ntile = 16-byte piece ntile of the row
-                const uint32_t vrow = vb + (uint32_t)((lane & 15) * 128) + ((uint32_t)(warp ^ (lane & 7)) << 4);
-                const uint32_t uvrow = uvb + (uint32_t)(((lane & 15) * SM::URS + 8 * warp) * 2);
-#pragma unroll
-                for (int ks = 0; ks < kAtT / 16; ++ks) {
-                    uint32_t ah[4], al[4];
-                    ldsm_x4(pha + 32 * ks, ah);
-                    ldsm_x4(pla + 32 * ks, al);
-#pragma unroll
-                    for (int k = 0; k < NTW; ++k) {
-                        const int ntile = warp + 8 * k;
-                        if (ntile < SM::NT) {
-                            uint32_t bb[2];
-                            if (8 * k < D / 8)   // a canonical column tile: box k, piece warp
-                                ldsm_x2_t(vrow + (uint32_t)k * SM::kBoxBytes + (uint32_t)(ks * 16 * 128), bb);
-                            else                 // a U' column tile
-                                ldsm_x2_t(uvrow + (uint32_t)(((ks * 16) * SM::URS + 8 * (8 * k - D / 8)) * 2), bb);
-                            mma_bf16(o[k], ah, bb[0], bb[1]);
-                            mma_bf16(o[k], al, bb[0], bb[1]);
+                const uint32_t kb = kt0 + b * kBuf, vb = vt0 + b * kBuf;
+                const uint32_t ub = ut0 + (SM::UB ? b : 0) * kUBuf, uvb = uv0 + (SM::UB ? b : 0) * kUBuf;
+                const bool active = r0 < ntok;
+                if (active) {
+                    attend_wait(ptx::smem_addr(&s.full[warp][b]), (ph >> b) & 1u, &s.abort, p.err, P.wait_ns);
+                    ph ^= 1u << b;
+                    // ---- this warp's rows of the buffer: U rows of ranks that are not whole
+                    // 16-byte vectors, U columns past the rank, value rows past the chunk
+                    if constexpr (MP > 0) {
+                        if ((m & 7) != 0) {   // ranks that are not whole 16-byte vectors: element copies
+                            const int64_t fu = ((int64_t)(p.layer * p.H + g) * len + j0) * m;
+                            const __nv_bfloat16* uk = patch_ptr(ch, 0) + fu;
+                            const __nv_bfloat16* uvp = patch_ptr(ch, 2) + fu;
+                            for (int e = lane; e < 16 * MP; e += 32) {
+                                const int t = r0 + e / MP, k = e % MP;
+                                const bool in = t < ntok && k < m;
+                                s.ut[b][t][k] = in ? uk[(int64_t)t * m + k] : __float2bfloat16_rn(0.f);
+                                s.uv[b][t][k] = in ? uvp[(int64_t)t * m + k] : __float2bfloat16_rn(0.f);
+                            }
+                        } else if (m < MP) {
+                            const int zv = (MP - m) >> 3;
+                            for (int e = lane; e < 16 * zv; e += 32) {
+                                const int t = r0 + e / zv, v = (m >> 3) + e % zv;
+                                ptx::st_shared_zero16(ptx::smem_addr(&s.ut[b][t][8 * v]));
+                                ptx::st_shared_zero16(ptx::smem_addr(&s.uv[b][t][8 * v]));
+                            }
                         }
                     }
+                    if (ntok < r0 + 16) {   // value rows past the chunk: zero, so zero weights add nothing
+                        const int nz = r0 + 16 - ntok;
+                        for (int e = lane; e < nz * 8 * SM::NB; e += 32) {
+                            const int t = ntok + e / (8 * SM::NB), c8 = e % (8 * SM::NB);
+                            ptx::st_shared_zero16(vb + (c8 >> 3) * SM::kBoxBytes + t * 128 + (c8 & 7) * 16);
+                        }
+                        if constexpr (MP > 0)
+                            for (int e = lane; e < nz * (MP / 8); e += 32)
+                                ptx::st_shared_zero16(
+                                    ptx::smem_addr(&s.uv[b][ntok + e / (MP / 8)][8 * (e % (MP / 8))]));
+                    }
+                    __syncwarp();
+
+                    // ---- scores S[16 heads x 16 tokens]: two 8-token column tiles, the hi and
+                    // lo products in separate chains (padded U columns add exact zeros at
+                    // their ends, so every instantiation gives the same scores)
+                    float sa[2][2][4];
+#pragma unroll
+                    for (int nt2 = 0; nt2 < 2; ++nt2)
+#pragma unroll
+                        for (int u = 0; u < 2; ++u)
+                            sa[nt2][u][0] = sa[nt2][u][1] = sa[nt2][u][2] = sa[nt2][u][3] = 0.f;
+                    const uint32_t krow = kb + (uint32_t)(kr * 128);
+                    const uint32_t urow = ub + (uint32_t)((kr * SM::URS + 8 * khi) * 2);
+                    auto score_step = [&](uint32_t baddr, int ks) {
+                        uint32_t bb[4], ah[4], al[4];
+                        ldsm_x4(baddr, bb);
+                        ldsm_x4(xa + 32 * ks, ah);
+                        ldsm_x4(xla + 32 * ks, al);
+                        mma_bf16(sa[0][0], ah, bb[0], bb[1]);
+                        mma_bf16(sa[0][1], al, bb[0], bb[1]);
+                        mma_bf16(sa[1][0], ah, bb[2], bb[3]);
+                        mma_bf16(sa[1][1], al, bb[2], bb[3]);
+                    };
+#pragma unroll 4
+                    for (int ks = 0; ks < D / 16; ++ks)   // key rows
+                        score_step(krow + (uint32_t)(ks >> 2) * SM::kBoxBytes + ((((uint32_t)(2 * ks) & 7u) ^ klx) << 4),
+                                   ks);
+#pragma unroll 4
+                    for (int ks = D / 16; ks < SM::KW / 16; ++ks)   // U rows
+                        score_step(urow + 32 * (ks - D / 16), ks);
+
+                    // ---- online softmax over this warp's 16 tokens (rows gq, gq + 8)
+                    float e[2][4], mx[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+                    for (int nt2 = 0; nt2 < 2; ++nt2)
+#pragma unroll
+                        for (int f = 0; f < 4; ++f) {
+                            const int tok = r0 + 8 * nt2 + 2 * t4 + (f & 1);
+                            const float sc = sa[nt2][0][f] + sa[nt2][1][f];
+                            e[nt2][f] = tok < ntok ? p.scale * sc : -INFINITY;
+                            mx[f >> 1] = fmaxf(mx[f >> 1], e[nt2][f]);
+                        }
+                    float alpha[2], sum[2];
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 1));
+                        mx[r] = fmaxf(mx[r], __shfl_xor_sync(0xffffffffu, mx[r], 2));
+                        const float mnew = fmaxf(m_run[r], mx[r]);   // finite: token r0 is in the chunk
+                        alpha[r] = __expf(m_run[r] - mnew);         // 0 while nothing was seen
+                        m_run[r] = mnew;
+                        sum[r] = 0.f;
+                    }
+#pragma unroll
+                    for (int nt2 = 0; nt2 < 2; ++nt2)
+#pragma unroll
+                        for (int f = 0; f < 4; ++f) {
+                            e[nt2][f] = __expf(e[nt2][f] - m_run[f >> 1]);
+                            sum[f >> 1] += e[nt2][f];
+                        }
+#pragma unroll
+                    for (int r = 0; r < 2; ++r) {
+                        sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], 1);
+                        sum[r] += __shfl_xor_sync(0xffffffffu, sum[r], 2);
+                        l_run[r] = fmaf(l_run[r], alpha[r], sum[r]);
+                    }
+                    if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {   // a new running max
+#pragma unroll
+                        for (int j = 0; j < NT; ++j) {
+                            o[j][0] *= alpha[0];
+                            o[j][1] *= alpha[0];
+                            o[j][2] *= alpha[1];
+                            o[j][3] *= alpha[1];
+                        }
+                    }
+                    // the weights as the A operand (heads x tokens), hi + lo
+                    uint32_t ph[4], pl[4];
+                    split_hl(e[0][0], e[0][1], ph[0], pl[0]);
+                    split_hl(e[0][2], e[0][3], ph[1], pl[1]);
+                    split_hl(e[1][0], e[1][1], ph[2], pl[2]);
+                    split_hl(e[1][2], e[1][3], ph[3], pl[3]);
+
+                    // ---- [O | W] += P [v | u']: column tiles in pairs
+                    const uint32_t vrow = vb + (uint32_t)(vr * 128);
+                    const uint32_t uvrow = uvb + (uint32_t)((vr * SM::URS + 8 * (lane >> 4)) * 2);
+#pragma unroll
+                    for (int j = 0; j < NT; j += 2) {
+                        uint32_t bb[4];
+                        if (j < D / 8)
+                            ldsm_x4_t(vrow + (uint32_t)(j >> 3) * SM::kBoxBytes + ((((uint32_t)j & 7u) ^ vlx) << 4), bb);
+                        else
+                            ldsm_x4_t(uvrow + 16 * (j - D / 8), bb);
+                        mma_bf16(o[j], ph, bb[0], bb[1]);
+                        mma_bf16(o[j], pl, bb[0], bb[1]);
+                        mma_bf16(o[j + 1], ph, bb[2], bb[3]);
+                        mma_bf16(o[j + 1], pl, bb[2], bb[3]);
+                    }
+                    if (ntok < r0 + 16)
+                        ptx::fence_proxy_async();   // zeroed rows precede a later TMA refill of the buffer
+                }
+                __syncwarp();   // the warp is done with its rows of buffer b before it refills them
+            }
+            if constexpr (MP > 0) {
+                if (m > 0) {   // fold W = sum_j p_j u'_j through V_v: O += W V_v^T (W's fragments -> A operand)
+                    const uint16_t* vvg = reinterpret_cast<const uint16_t*>(patch_ptr(ch, 3) + fo);   // V_v [d][m]
+#pragma unroll
+                    for (int kk = 0; kk < MP / 16; ++kk) {
+                        const int j0 = D / 8 + 2 * kk, q0 = 16 * kk + 2 * t4;
+                        uint32_t ah[4], al[4];
+                        split_hl(o[j0][0], o[j0][1], ah[0], al[0]);
+                        split_hl(o[j0][2], o[j0][3], ah[1], al[1]);
+                        split_hl(o[j0 + 1][0], o[j0 + 1][1], ah[2], al[2]);
+                        split_hl(o[j0 + 1][2], o[j0 + 1][3], ah[3], al[3]);
+#pragma unroll
+                        for (int j = 0; j < D / 8; ++j) {
+                            const uint16_t* vrw = vvg + (int64_t)(8 * j + gq) * m;
+                            const uint32_t b0 = (q0 < m ? (uint32_t)vrw[q0] : 0u) |
+                                                ((q0 + 1 < m ? (uint32_t)vrw[q0 + 1] : 0u) << 16);
+                            const uint32_t b1 = (q0 + 8 < m ? (uint32_t)vrw[q0 + 8] : 0u) |
+                                                ((q0 + 9 < m ? (uint32_t)vrw[q0 + 9] : 0u) << 16);
+                            mma_bf16(o[j], ah, b0, b1);
+                            mma_bf16(o[j], al, b0, b1);
+                        }
+                    }
+#pragma unroll
+                    for (int j = D / 8; j < NT; ++j)
+                        o[j][0] = o[j][1] = o[j][2] = o[j][3] = 0.f;
                 }
             }
         }
-        if constexpr (MP > 0) {
-            if (m > 0) {   // fold W = sum_j p_j u'_j through V_v: O += W V_v^T
+        // ---- publish this warp's state for the CTA merge (after every tile is consumed)
+        ptx::cp_async_wait<0>();
+        __syncthreads();   // no tile buffer is in use any more
+        float* ow = reinterpret_cast<float*>(&s.kt[0][0][0][0]);   // [kAtCW][kAtH][D]
 #pragma unroll
-                for (int k = 0; k < NTW; ++k) {
-                    const int ntile = warp + 8 * k;
-                    if (ntile >= D / 8 && ntile < SM::NT) {
-                        const int col = 8 * ntile - D + 2 * t4;
-                        s.wsum[gq][col] = o[k][0];
-                        s.wsum[gq][col + 1] = o[k][1];
-                        s.wsum[gq + 8][col] = o[k][2];
-                        s.wsum[gq + 8][col + 1] = o[k][3];
-                        o[k][0] = o[k][1] = o[k][2] = o[k][3] = 0.f;
-                    }
-                }
-                __syncthreads();
-                const __nv_bfloat16* vvg = patch_ptr(ch, 3) + fo;   // V_v [d][m]
-#pragma unroll
-                for (int ks = 0; ks < MP / 16; ++ks) {
-                    const int q0 = 16 * ks + 2 * t4;
-                    uint32_t ah[4], al[4];
-                    split_hl(s.wsum[gq][q0], s.wsum[gq][q0 + 1], ah[0], al[0]);
-                    split_hl(s.wsum[gq + 8][q0], s.wsum[gq + 8][q0 + 1], ah[1], al[1]);
-                    split_hl(s.wsum[gq][q0 + 8], s.wsum[gq][q0 + 9], ah[2], al[2]);
-                    split_hl(s.wsum[gq + 8][q0 + 8], s.wsum[gq + 8][q0 + 9], ah[3], al[3]);
-#pragma unroll
-                    for (int k = 0; k < NTW; ++k) {
-                        const int ntile = warp + 8 * k;
-                        if (ntile < D / 8) {
-                            const int64_t i = 8 * ntile + gq;
-                            const uint16_t* vr = reinterpret_cast<const uint16_t*>(vvg + i * m);
-                            const uint32_t b0 = (q0 < m ? (uint32_t)vr[q0] : 0u) |
-                                                ((q0 + 1 < m ? (uint32_t)vr[q0 + 1] : 0u) << 16);
-                            const uint32_t b1 = (q0 + 8 < m ? (uint32_t)vr[q0 + 8] : 0u) |
-                                                ((q0 + 9 < m ? (uint32_t)vr[q0 + 9] : 0u) << 16);
-                            mma_bf16(o[k], ah, b0, b1);
-                            mma_bf16(o[k], al, b0, b1);
-                        }
-                    }
-                }
-            }
+        for (int j = 0; j < D / 8; ++j) {
+            const int col = 8 * j + 2 * t4;
+            *reinterpret_cast<float2*>(&ow[(warp * kAtH + gq) * D + col]) = make_float2(o[j][0], o[j][1]);
+            *reinterpret_cast<float2*>(&ow[(warp * kAtH + gq + 8) * D + col]) = make_float2(o[j][2], o[j][3]);
         }
+        if (t4 == 0) {
+            s.wm[warp][gq] = m_run[0];
+            s.wm[warp][gq + 8] = m_run[1];
+            s.wl[warp][gq] = l_run[0];
+            s.wl[warp][gq + 8] = l_run[1];
+        }
+    }
+    __syncthreads();   // every warp's state published
+
+    // ---- CTA merge of the warps' softmax states -> (cm, cl, ob)
+    float* ow = reinterpret_cast<float*>(&s.kt[0][0][0][0]);
+    float* ob = reinterpret_cast<float*>(&s.vt[0][0][0][0]);   // [kAtH][D]
+    if (threadIdx.x < kAtH) {
+        const int h = threadIdx.x;
+        float mx = -INFINITY;
+        for (int w = 0; w < kAtCW; ++w)
+            mx = fmaxf(mx, s.wm[w][h]);
+        float l = 0.f;
+        for (int w = 0; w < kAtCW; ++w) {
+            const float f = s.wm[w][h] == -INFINITY ? 0.f : expf(s.wm[w][h] - mx);
+            s.wf[h][w] = f;
+            l = fmaf(s.wl[w][h], f, l);
+        }
+        s.cm[h] = mx;
+        s.cl[h] = l;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < kAtH * D; e += kAtThreads) {
+        const int h = e / D;
+        float acc = 0.f;
+#pragma unroll
+        for (int w = 0; w < kAtCW; ++w)
+            acc = fmaf(ow[(w * kAtH) * D + e], s.wf[h][w], acc);
+        ob[e] = acc;
     }
 
-    // merge: every CTA publishes (max, sum, unnormalised output); rank 0 combines
-    ptx::cp_async_wait<0>();
-    __syncthreads();   // the tile buffers are free
-    float* ob = reinterpret_cast<float*>(&s.kt[0][0][0][0]);   // [kAtH][D]
-#pragma unroll
-    for (int k = 0; k < NTW; ++k) {
-        const int ntile = warp + 8 * k;
-        if (ntile < D / 8) {
-            const int col = 8 * ntile + 2 * t4;
-            *reinterpret_cast<float2*>(&ob[gq * D + col]) = make_float2(o[k][0], o[k][1]);
-            *reinterpret_cast<float2*>(&ob[(gq + 8) * D + col]) = make_float2(o[k][2], o[k][3]);
-        }
-    }
-    if ((threadIdx.x & 15) == 0) {
-        s.cm[threadIdx.x >> 4] = m_run;
-        s.cl[threadIdx.x >> 4] = l_run;
-    }
+    // ---- cluster merge: every CTA publishes (max, sum, unnormalised output); rank 0 combines
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     if (rank == 0) {
@@ -621,8 +679,8 @@ static cudaError_t launch_attend_m(const AttendParams& p0, cudaStream_t stream)
     L.wait_ns = wait_limit_ns();
     // key and value rows: [num_rows][H * d] (an empty store gets a one-row map no tile reads)
     const int64_t rows = p.num_rows > 0 ? p.num_rows : 1, width = (int64_t)p.H * D;
-    if (!make_rows_map(&L.map_k, p.k, rows, width, p.row_stride, 64, kAtT) ||
-        !make_rows_map(&L.map_v, p.v, rows, width, p.row_stride, 64, kAtT))
+    if (!make_rows_map(&L.map_k, p.k, rows, width, p.row_stride, 64, kAtWR) ||
+        !make_rows_map(&L.map_v, p.v, rows, width, p.row_stride, 64, kAtWR))
         return cudaErrorInvalidValue;
     static_assert(sizeof(AtSmem<D, MP>) + 1024 <= 227 * 1024, "attention tile buffers exceed shared memory");
     const int bytes = (int)sizeof(AtSmem<D, MP>) + 1024;   // + the 1024-byte alignment

@@ -15,13 +15,15 @@ pytestmark = pytest.mark.gpu
 DEV = "cuda"
 
 
-@pytest.fixture(params=["auto", "copies", "simt"])
+@pytest.fixture(params=["auto", "copies", "simt", "umma"])
 def path(request, monkeypatch):
     """Run the case on the default kernel choice (tensor-core path for patched
-    GQA/MHA/MLA calls; factor tiles by tensor-map loads where the host copy of
-    the descriptors allows), on the same choice without the host copy (every
-    factor tile by per-thread copies), and pinned to the CUDA-core path."""
-    monkeypatch.setenv("KAMERA_PATH", "simt" if request.param == "simt" else "auto")
+    GQA/MHA/MLA calls but short chunks with tiny ranks; factor tiles by
+    tensor-map loads where the host copy of the descriptors allows), on the same
+    choice without the host copy (every factor tile by per-thread copies),
+    pinned to the CUDA-core path, and on the tensor-core path wherever it
+    applies."""
+    monkeypatch.setenv("KAMERA_PATH", request.param if request.param in ("simt", "umma") else "auto")
     monkeypatch.setattr(Hn, "USE_HOST_COPY", request.param != "copies")
     return request.param
 
