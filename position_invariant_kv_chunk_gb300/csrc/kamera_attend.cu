@@ -126,30 +126,6 @@ __device__ __forceinline__ int32_t attend_check(const KameraChunk& ch, int c, co
     return bits;
 }
 
-// Bounded wait on an mbarrier phase.  On expiry the call reports
-// KAMERA_DEVERR_TIMEOUT, every later wait of the CTA returns at once, and the
-// kernel runs its barriers to the end (its output is then undefined).
-__device__ __forceinline__ bool attend_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort, int32_t* err,
-                                            uint64_t limit)
-{
-    if (ptx::mbar_try_wait(bar, parity))
-        return true;
-    const uint64_t t0 = ptx::globaltimer();
-    for (uint32_t it = 1;; ++it) {
-        if (ptx::mbar_try_wait(bar, parity))
-            return true;
-        if ((it & 63u) == 0) {
-            if (*abort)
-                return false;
-            if (ptx::globaltimer() - t0 > limit) {
-                *abort = 1;
-                raise_err(err, KAMERA_DEVERR_TIMEOUT);
-                return false;
-            }
-        }
-    }
-}
-
 // The CTA's share of a sequence: tiles [lo, hi) of its valid chunks' tiles in
 // order; for chunk c (nt tiles, pos tiles before it) the tiles [t_lo, t_hi).
 __device__ __forceinline__ void share_of_chunk(int64_t lo, int64_t hi, int64_t pos, int nt, int& t_lo, int& t_hi)
@@ -383,7 +359,7 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
                 const uint32_t ub = ut0 + (SM::UB ? b : 0) * kUBuf, uvb = uv0 + (SM::UB ? b : 0) * kUBuf;
                 const bool active = r0 < ntok;
                 if (active) {
-                    attend_wait(ptx::smem_addr(&s.full[warp][b]), (ph >> b) & 1u, &s.abort, p.err, P.wait_ns);
+                    tile_wait(ptx::smem_addr(&s.full[warp][b]), (ph >> b) & 1u, &s.abort, p.err, P.wait_ns);
                     ph ^= 1u << b;
                     // ---- this warp's rows of the buffer: U rows of ranks that are not whole
                     // 16-byte vectors, U columns past the rank, value rows past the chunk

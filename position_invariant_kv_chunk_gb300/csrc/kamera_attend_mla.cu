@@ -27,9 +27,12 @@
 // 64w .. 64w + 63.  Operands that are not bf16 already (the turned rope query,
 // the folds, the softmax weights) enter as a bf16 hi + lo pair, so products
 // keep about 16 bits of their fp32 value; the canonical rows and U rows are
-// exact bf16.  Tiles are double-buffered 16-byte async copies into rows padded
-// to an odd number of 16-byte vectors, so the eight rows an 8x8 matrix load
-// reads fall in distinct banks.  A cluster of CL CTAs serves one sequence, CTA
+// exact bf16.  Tiles are double-buffered: the 576-wide canonical rows arrive
+// as nine 128B-swizzled TMA boxes of 64 columns x 64 tokens (one thread issues
+// them; completion on an mbarrier, every wait bounded in time), the u and w
+// rows as async copies into rows padded to an odd number of 16-byte vectors;
+// both layouts put the eight rows an 8x8 matrix load reads in distinct banks.
+// A cluster of CL CTAs serves one sequence, CTA
 // r taking the r-th of CL even runs of the sequence's tiles (a chunk cut
 // between two CTAs is set up by both, each folding its own share of the value
 // patch); rank 0 merges the partial softmax states through distributed shared
@@ -38,6 +41,8 @@
 // rows, and the clusters of all groups share the GPU in the same waves.
 #include <cooperative_groups.h>
 #include <cstdint>
+#include <cstring>
+#include <cuda.h>
 #include <cuda_bf16.h>
 
 #include "kamera_common.cuh"
@@ -63,13 +68,16 @@ constexpr int kMlMaxHeads = 128;     // query heads per latent row: groups of 16
 
 // MP: the padded rank the instantiation takes (0, 16 or 32).
 template <int MP>
-struct __align__(16) MlSmem {
-    static constexpr int KW = kMlDK + 2 * MP;   // tile row: c_KV | k_rope | u (V_c's factor) | w (V_r's)
-    static constexpr int RS = KW + 8;           // row stride: an odd number of 16-byte vectors
+struct MlSmem {
+    static constexpr int NBX = kMlDK / 64;      // 64-column boxes of a canonical row: c_KV (8) | k_rope (1)
+    static constexpr int URS = 2 * MP + 8;      // u (V_c's factor) | w (V_r's) row: an odd number of 16-byte vectors
     static constexpr int XW = kMlR + 2 * MP;    // per-chunk query part: R(-delta) q_rope | V_c^T q_lat | V_r^T q_rope
     static constexpr int XS = XW + 8;
     static constexpr int MPa = MP > 0 ? MP : 1;
-    __nv_bfloat16 kt[2][kMlT][RS];              // tiles; the latent queries at the start; partial outputs at the end
+    static constexpr uint32_t kBoxBytes = kMlT * 128;
+    __nv_bfloat16 kt[2][NBX][kMlT][64];         // canonical rows (TMA boxes); the latent queries at the
+                                                // start; the partial outputs at the end
+    __nv_bfloat16 ux[2][kMlT][URS];             // u | w rows
     __nv_bfloat16 xh[kMlH][XS];                 // per-chunk query part, bf16 hi
     __nv_bfloat16 xl[kMlH][XS];                 // and lo
     float sc[kMlH][kMlT + 4];                   // scores of the tile
@@ -82,6 +90,16 @@ struct __align__(16) MlSmem {
     float2 cs[kMlR / 2];                        // cos/sin of -delta
     float cm[kMlH], cl[kMlH];                   // this CTA's softmax state, for the merge
     float fac[kMlH][kMlMaxCL];                  // merge weights (rank 0)
+    uint64_t full[2];                           // buffer b's TMA boxes have landed
+    int32_t abort;                              // a wait ran out: every later wait returns at once
+};
+
+// The launch: parameters and the tensor map of the canonical rows
+// ([num_rows][kv_lora + rope_dim], boxes of 64 columns x 64 rows).
+struct MlaLaunch {
+    MlaAttendParams p;
+    CUtensorMap map;
+    uint64_t wait_ns;
 };
 
 __device__ __forceinline__ void st_shared_u32(uint32_t a, uint32_t v)
@@ -112,31 +130,24 @@ __device__ __forceinline__ int32_t mla_check(const KameraChunk& ch, int c, const
     return bits;
 }
 
-// Copies tile rows j0 .. j0 + n - 1 of chunk `ch` into buffer b; rows past n
-// and U columns past the rank are zero.
+// Starts the copies of tile rows j0 .. j0 + n - 1 of chunk `ch` into buffer
+// b: thread 0 issues the nine TMA boxes of the canonical rows (rows past the
+// chunk come from the store or read as zero; the c_KV rows past n are cleared
+// once they land), every thread the async copies of the u and w rows (zero past
+// n and past the rank).  One copy group per call.
 template <int MP>
-__device__ __forceinline__ void mla_load(const MlaAttendParams& p, const KameraChunk& ch, int j0, int n, int b,
+__device__ __forceinline__ void mla_load(const MlaLaunch& P, const KameraChunk& ch, int j0, int n, int b,
                                          MlSmem<MP>& s)
 {
-    // c_KV | k_rope: 72 16-byte vectors a row; eight threads a row, each taking
-    // vectors q, q + 8, ... (9) of rows r and r + 32
-    static_assert(kMlDK == 8 * 8 * 9 && kMlThreads == 8 * kMlT / 2, "row split");
-    const __nv_bfloat16* src = p.kv + (ch.src_offset + j0) * p.row_stride;
-    const int r0 = threadIdx.x >> 3, q = threadIdx.x & 7;
+    using SM = MlSmem<MP>;
+    const MlaAttendParams& p = P.p;
+    if (threadIdx.x == 0) {
+        const uint32_t bar = ptx::smem_addr(&s.full[b]);
+        const int y = (int)(ch.src_offset + j0);
+        ptx::mbar_arrive_expect_tx(bar, SM::NBX * SM::kBoxBytes);
 #pragma unroll
-    for (int hf = 0; hf < 2; ++hf) {
-        const int t = r0 + 32 * hf;
-        const uint32_t dst = ptx::smem_addr(&s.kt[b][t][8 * q]);
-        if (t < n) {
-            const __nv_bfloat16* g = src + (int64_t)t * p.row_stride + 8 * q;
-#pragma unroll
-            for (int i = 0; i < 9; ++i)
-                ptx::cp_async16(dst + 128 * i, g + 64 * i);
-        } else {
-#pragma unroll
-            for (int i = 0; i < 9; ++i)
-                ptx::st_shared_zero16(dst + 128 * i);
-        }
+        for (int x = 0; x < SM::NBX; ++x)
+            ptx::tma_load_2d(ptx::smem_addr(&s.kt[b][x][0][0]), &P.map, 64 * x, y, bar);
     }
     if constexpr (MP > 0) {   // u and w rows: MP / 2 words each (the rank is even)
         const int m = ch.rank;
@@ -146,7 +157,7 @@ __device__ __forceinline__ void mla_load(const MlaAttendParams& p, const KameraC
         for (int e = threadIdx.x; e < kMlT * MP; e += kMlThreads) {
             const int t = e / MP, wd = e - t * MP;
             const int f = wd >= MP / 2 ? 1 : 0, c2 = 2 * (wd - f * (MP / 2));
-            const uint32_t dst = ptx::smem_addr(&s.kt[b][t][kMlDK + f * MP + c2]);
+            const uint32_t dst = ptx::smem_addr(&s.ux[b][t][f * MP + c2]);
             if (t < n && c2 < m)
                 ptx::cp_async_small<4>(dst, (f ? ur : uc) + fo + (int64_t)t * m + c2);
             else
@@ -157,11 +168,13 @@ __device__ __forceinline__ void mla_load(const MlaAttendParams& p, const KameraC
 }
 
 template <int MP>
-__global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_constant__ MlaAttendParams p)
+__global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_constant__ MlaLaunch P)
 {
     using SM = MlSmem<MP>;
+    const MlaAttendParams& p = P.p;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    SM& s = *reinterpret_cast<SM*>(smem_raw);
+    // swizzled TMA boxes want 1024-byte alignment (the same offset in every CTA)
+    SM& s = *reinterpret_cast<SM*>(smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u));
     namespace cg = cooperative_groups;
     const int CL = p.cluster, rank = (int)(blockIdx.x % (unsigned)CL), seq = blockIdx.x / CL;
     // query heads h0 .. h0 + Hg - 1 (a group of up to 16: the rows of every MMA)
@@ -187,7 +200,15 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
     const int64_t lo = total * rank / CL, hi = total * (rank + 1) / CL;
 
     // the latent queries (rows past Hq zero) staged in the second tile buffer; q_rope as fp32
-    __nv_bfloat16* qls = &s.kt[1][0][0];
+    __nv_bfloat16* qls = &s.kt[1][0][0][0];
+    if (threadIdx.x == 0) {
+        ptx::mbar_init(ptx::smem_addr(&s.full[0]), 1);
+        ptx::mbar_init(ptx::smem_addr(&s.full[1]), 1);
+        s.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (threadIdx.x == 32)
+        ptx::prefetch_tmap(&P.map);
     for (int e = threadIdx.x; e < kMlH * (kMlC / 8); e += kMlThreads) {
         const int h = e / (kMlC / 8), v = e - h * (kMlC / 8);
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
@@ -199,6 +220,7 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
         const int h = e / kMlR, i = e - h * kMlR;
         s.qr[h][i] = h < Hg ? __bfloat162float(p.q[((int64_t)seq * Hq + h0 + h) * kMlDK + kMlC + i]) : 0.f;
     }
+    ptx::fence_proxy_async();   // the staged queries precede the TMA loads that later refill that buffer
     __syncthreads();
     uint32_t qc[kMlC / 16][4];   // A fragments of the latent query, every k-step
     {
@@ -216,8 +238,14 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
     float m_run = -INFINITY, l_run = 0.f;  // head threadIdx.x / 16
     const RopeParams& rp = p.rope;
     const int ro = rp.rot_offset, rr = rp.rot_dim, half = rr / 2;
-    const uint32_t kt0 = ptx::smem_addr(&s.kt[0][0][0]);
-    constexpr uint32_t kBuf = (uint32_t)(kMlT * SM::RS * 2);   // bytes per tile buffer
+    const uint32_t kt0 = ptx::smem_addr(&s.kt[0][0][0][0]), ux0 = ptx::smem_addr(&s.ux[0][0][0]);
+    constexpr uint32_t kBuf = SM::NBX * SM::kBoxBytes;          // bytes per row buffer
+    constexpr uint32_t kUBuf = (uint32_t)(kMlT * SM::URS * 2);  // bytes per u | w buffer
+    uint32_t ph = 0;   // phase parity of each buffer's barrier
+    // 8x8 matrix-load addressing in the swizzled boxes: score B operand (rows 8 warp + (lane & 7),
+    // pieces 4k + lane / 8) and value B operand (rows (lane & 7) + 8 ((lane / 8) & 1), pieces 2np + lane / 16)
+    const int kr = 8 * warp + (lane & 7);
+    const uint32_t klx = (uint32_t)((lane >> 3) ^ (lane & 7)), vlx = (uint32_t)((lane >> 4) ^ (lane & 7));
 
     int64_t pos = 0;   // tiles of the sequence before chunk c
     for (int c = c0; c < c1; ++c) {
@@ -237,7 +265,7 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
             continue;
         const int m = ch.rank;
         __syncthreads();   // the previous chunk (or the query staging) is done with every shared array
-        mla_load<MP>(p, ch, t_lo * kMlT, min(kMlT, len - t_lo * kMlT), 0, s);   // lands while the chunk is set up
+        mla_load<MP>(P, ch, t_lo * kMlT, min(kMlT, len - t_lo * kMlT), 0, s);   // lands while the chunk is set up
         for (int f = threadIdx.x; f < rp.n_freq; f += kMlThreads) {
             float cc, sn;
             phase_cos_sin(-freq_delta(rp, ch, c, f), rp.inv_freq[f], cc, sn);
@@ -309,22 +337,31 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
 
         for (int tl = t_lo; tl < t_hi; ++tl) {
             const int b = (tl - t_lo) & 1, ntok = min(kMlT, len - tl * kMlT);
+            tile_wait(ptx::smem_addr(&s.full[b]), (ph >> b) & 1u, &s.abort, p.err, P.wait_ns);
+            ph ^= 1u << b;
             ptx::cp_async_wait<0>();   // this thread's copies of tile tl (the only group in flight)
+            const uint32_t kb = kt0 + b * kBuf, uxb = ux0 + b * kUBuf;
+            if (ntok < kMlT) {   // c_KV rows past the chunk: zero, so that their zero weights add nothing
+                for (int e = threadIdx.x; e < (kMlT - ntok) * 64; e += kMlThreads) {
+                    const int t = ntok + (e >> 6), c8 = e & 63;
+                    ptx::st_shared_zero16(kb + (c8 >> 3) * SM::kBoxBytes + t * 128 + (c8 & 7) * 16);
+                }
+                ptx::fence_proxy_async();   // before a later TMA load refills the buffer
+            }
             __syncthreads();   // tile b (and, first, the chunk's query part) in place; every warp is
                                // done with tile tl - 1, its buffer and its scores and weights
             if (tl + 1 < t_hi)
-                mla_load<MP>(p, ch, (tl + 1) * kMlT, min(kMlT, len - (tl + 1) * kMlT), b ^ 1, s);
-            const uint32_t kb = kt0 + b * kBuf;
+                mla_load<MP>(P, ch, (tl + 1) * kMlT, min(kMlT, len - (tl + 1) * kMlT), b ^ 1, s);
             {   // scores of tokens 8 warp .. + 7 against the 16 heads (four partial sums: independent MMA chains)
                 float sa[4][4];
 #pragma unroll
                 for (int u = 0; u < 4; ++u)
                     sa[u][0] = sa[u][1] = sa[u][2] = sa[u][3] = 0.f;
-                const uint32_t krow = kb + (uint32_t)(((8 * warp + (lane & 7)) * SM::RS + 8 * (lane >> 3)) * 2);
+                const uint32_t krow = kb + (uint32_t)(kr * 128);
 #pragma unroll
                 for (int ks = 0; ks < kMlC / 16; ks += 2) {
                     uint32_t bb[4];
-                    ldsm_x4(krow + 32 * ks, bb);
+                    ldsm_x4(krow + (uint32_t)(ks >> 2) * SM::kBoxBytes + ((((uint32_t)(2 * ks) & 7u) ^ klx) << 4), bb);
                     mma_bf16(sa[ks & 3], qc[ks], bb[0], bb[1]);
                     mma_bf16(sa[(ks + 1) & 3], qc[ks + 1], bb[2], bb[3]);
                 }
@@ -332,11 +369,12 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
                 // sums 0/1 and the w columns into sums 2/3, so the padded columns of a
                 // wider instantiation add exact zeros to the same sums in the same order
                 const uint32_t xa = ptx::smem_addr(&s.xh[arow][acol]), xla = ptx::smem_addr(&s.xl[arow][acol]);
-                const uint32_t kx = krow + 32 * (kMlC / 16);
+                const uint32_t kx = krow + (kMlC / 64) * SM::kBoxBytes;   // the k_rope box
+                const uint32_t ukx = uxb + (uint32_t)((kr * SM::URS + 8 * ((lane >> 3) & 1)) * 2);
 #pragma unroll
                 for (int ks = 0; ks < kMlR / 16; ks += 2) {
                     uint32_t bb[4], ah[4], al[4], ah2[4], al2[4];
-                    ldsm_x4(kx + 32 * ks, bb);
+                    ldsm_x4(kx + ((((uint32_t)(2 * ks) & 7u) ^ klx) << 4), bb);
                     ldsm_x4(xa + 32 * ks, ah);
                     ldsm_x4(xla + 32 * ks, al);
                     ldsm_x4(xa + 32 * (ks + 1), ah2);
@@ -350,7 +388,7 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
                 for (int j = 0; j < 2 * (MP / 16); ++j) {
                     const int ks = kMlR / 16 + j, q = j < MP / 16 ? 0 : 2;
                     uint32_t bb[2], ah[4], al[4];
-                    ldsm_x2(kx + 32 * ks, bb);
+                    ldsm_x2(ukx + 32 * j, bb);
                     ldsm_x4(xa + 32 * ks, ah);
                     ldsm_x4(xla + 32 * ks, al);
                     mma_bf16(sa[q], ah, bb[0], bb[1]);
@@ -412,18 +450,18 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
                     wc[3] *= a1;
                 }
                 const uint32_t pha = ptx::smem_addr(&s.ph[arow][acol]), pla = ptx::smem_addr(&s.pl[arow][acol]);
-                const uint32_t vb = kb + (uint32_t)((arow * SM::RS + 64 * warp + acol) * 2);
-                const uint32_t ub = kb + (uint32_t)((arow * SM::RS + kMlDK + 8 * warp) * 2);
+                const uint32_t vb = kb + (uint32_t)warp * SM::kBoxBytes + (uint32_t)(arow * 128);   // box warp: columns 64 warp ..
+                const uint32_t ub = uxb + (uint32_t)((arow * SM::URS + 8 * warp) * 2);
 #pragma unroll
                 for (int ks = 0; ks < kMlT / 16; ++ks) {
                     uint32_t ah[4], al[4];
                     ldsm_x4(pha + 32 * ks, ah);
                     ldsm_x4(pla + 32 * ks, al);
-                    const uint32_t vrow = vb + (uint32_t)(ks * 16 * SM::RS * 2);
+                    const uint32_t vrow = vb + (uint32_t)(ks * 16 * 128);
 #pragma unroll
                     for (int np = 0; np < 4; ++np) {
                         uint32_t bb[4];
-                        ldsm_x4_t(vrow + 32 * np, bb);
+                        ldsm_x4_t(vrow + ((((uint32_t)(2 * np)) ^ vlx) << 4), bb);
                         mma_bf16(o[2 * np], ah, bb[0], bb[1]);
                         mma_bf16(o[2 * np], al, bb[0], bb[1]);
                         mma_bf16(o[2 * np + 1], ah, bb[2], bb[3]);
@@ -432,7 +470,7 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
                     if constexpr (MP > 0) {
                         if (warp < MP / 8) {
                             uint32_t bu[2];
-                            ldsm_x2_t(ub + (uint32_t)(ks * 16 * SM::RS * 2), bu);
+                            ldsm_x2_t(ub + (uint32_t)(ks * 16 * SM::URS * 2), bu);
                             mma_bf16(wc, ah, bu[0], bu[1]);
                             mma_bf16(wc, al, bu[0], bu[1]);
                         }
@@ -480,7 +518,7 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
 
     // merge: every CTA publishes (max, sum, unnormalised output); rank 0 combines
     __syncthreads();   // all copies have landed (the last wait took every group); the tile buffers are free
-    float* ob = reinterpret_cast<float*>(&s.kt[0][0][0]);   // [kMlH][kMlC]
+    float* ob = reinterpret_cast<float*>(&s.kt[0][0][0][0]);   // [kMlH][kMlC]
 #pragma unroll
     for (int nt = 0; nt < 8; ++nt) {
         const int col = 64 * warp + 8 * nt + 2 * t4;
@@ -567,9 +605,18 @@ static int mla_pick_cluster(int64_t units, int bytes)
 }
 
 template <int MP>
-static cudaError_t launch_mla_attend_m(MlaAttendParams p, cudaStream_t stream)
+static cudaError_t launch_mla_attend_m(const MlaAttendParams& p0, cudaStream_t stream)
 {
-    const int bytes = (int)sizeof(MlSmem<MP>);
+    MlaLaunch L;
+    std::memset(&L, 0, sizeof(L));
+    L.p = p0;
+    MlaAttendParams& p = L.p;
+    L.wait_ns = wait_limit_ns();
+    // canonical rows [num_rows][kv_lora + rope_dim] (an empty store gets a one-row map no tile reads)
+    if (!make_rows_map(&L.map, p.kv, p.num_rows > 0 ? p.num_rows : 1, kMlDK, p.row_stride, 64, kMlT))
+        return cudaErrorInvalidValue;
+    static_assert(sizeof(MlSmem<MP>) + 1024 <= 227 * 1024, "MLA tile buffers exceed shared memory");
+    const int bytes = (int)sizeof(MlSmem<MP>) + 1024;   // + the 1024-byte alignment
     cudaError_t e = cudaFuncSetAttribute(mla_attend_kernel<MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess)
         return e;
@@ -587,7 +634,7 @@ static cudaError_t launch_mla_attend_m(MlaAttendParams p, cudaStream_t stream)
     attr[0].val.clusterDim.z = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
-    return cudaLaunchKernelEx(&cfg, mla_attend_kernel<MP>, p);
+    return cudaLaunchKernelEx(&cfg, mla_attend_kernel<MP>, L);
 }
 
 cudaError_t launch_mla_attend(const MlaAttendParams& p, cudaStream_t stream)

@@ -1,13 +1,14 @@
-// kamera_warpmma.cuh -- warp-level tensor-core helpers of the attention
-// kernels (sm_103a): 8x8 matrix loads from shared memory, the m16n8k16 bf16
-// MMA with fp32 accumulation, and bf16 hi + lo splits of fp32 values (about
-// 16 significant bits as a pair).
+// kamera_warpmma.cuh -- helpers shared by the attention kernels (sm_103a):
+// 8x8 matrix loads from shared memory, the m16n8k16 bf16 MMA with fp32
+// accumulation, bf16 hi + lo splits of fp32 values (about 16 significant bits
+// as a pair), and the time-bounded wait on a tile buffer's mbarrier.
 #pragma once
 
 #include <cstdint>
 #include <cuda_bf16.h>
 
 #include "kamera_common.cuh"
+#include "kamera_ptx.cuh"
 
 namespace kamera {
 namespace wmma16 {
@@ -58,6 +59,31 @@ __device__ __forceinline__ void split1(float v, __nv_bfloat16& hi, __nv_bfloat16
 {
     hi = __float2bfloat16_rn(v);
     lo = __float2bfloat16_rn(v - __bfloat162float(hi));
+}
+
+// Bounded wait on an mbarrier phase.  On expiry the call reports
+// KAMERA_DEVERR_TIMEOUT, every later wait of the CTA returns at once (the abort
+// flag), and the kernel runs its barriers to the end (its output is then
+// undefined).
+__device__ __forceinline__ bool tile_wait(uint32_t bar, uint32_t parity, volatile int32_t* abort, int32_t* err,
+                                          uint64_t limit)
+{
+    if (ptx::mbar_try_wait(bar, parity))
+        return true;
+    const uint64_t t0 = ptx::globaltimer();
+    for (uint32_t it = 1;; ++it) {
+        if (ptx::mbar_try_wait(bar, parity))
+            return true;
+        if ((it & 63u) == 0) {
+            if (*abort)
+                return false;
+            if (ptx::globaltimer() - t0 > limit) {
+                *abort = 1;
+                raise_err(err, KAMERA_DEVERR_TIMEOUT);
+                return false;
+            }
+        }
+    }
 }
 
 }  // namespace wmma16
