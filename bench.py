@@ -195,8 +195,12 @@ def time_launches(call, steps, flush_buf=None):
 
 
 def kernel_of(spec) -> str:
-    """The kernel a workload's call spends its time in (the relocation calls of the
-    configured workloads all carry patches, so they take the tensor-core kernel)."""
+    """The kernel a workload's call spends its time in: the relocation calls of the
+    configured workloads all carry patches, so they take the tensor-core kernel,
+    except calls of short chunks (<= 128 tokens) with ranks <= 8, which the
+    library sends to the CUDA-core kernel."""
+    if spec.kind in ("gqa", "mla") and spec.m <= 8 and max(spec.lens) <= 128:
+        return "rows_simt_kernel"
     return {"slide": "slide_kernel", "ingest": "ingest_kernel", "mla_ingest": "ingest_kernel"}.get(
         spec.kind, "relocate_patch_umma_kernel")
 
@@ -404,6 +408,7 @@ def e2e_measure(K, wl, steps, warmup):
 
 KERNEL_UNITS = {   # the translation unit each timed kernel is compiled from
     "relocate_patch_umma_kernel": "kamera_umma.cu",
+    "rows_simt_kernel": "kamera_simt.cu",
     "slide_kernel": "kamera_slide.cu",
     "ingest_kernel": "kamera_ingest.cu",
     "patch_form_kernel": "kamera_patchform.cu",

@@ -267,6 +267,22 @@ int simt_segments(const RowsParams& p, int family)
     return p.H;
 }
 
+// Threads per CTA.  A CTA's time is a chain of dependent loads (descriptor,
+// factors, slots, rows), so when the grid is many waves deep the CTAs resident
+// at once set the rate: 64-thread CTAs let 32 share an SM where 256-thread CTAs
+// let 8 (4096 one-tile chunks: 244 us with 256 threads, 203 with 128, 187 with
+// 64).  A grid that fits one wave of 256-thread CTAs keeps them, so each CTA's
+// items are spread over the most threads (one tiny chunk: 10 us with 256
+// threads, 17 with 64).
+static int simt_threads(int64_t blocks)
+{
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) !=
+                                                  cudaSuccess || sms < 1)
+        return 256;
+    return blocks <= 8ll * sms ? 256 : blocks <= 16ll * sms ? 128 : 64;
+}
+
 cudaError_t launch_simt(const RowsParams& p, int family, cudaStream_t stream)
 {
     const int tile_tokens = 64;
@@ -275,22 +291,23 @@ cudaError_t launch_simt(const RowsParams& p, int family, cudaStream_t stream)
     const size_t smem = simt_smem_bytes(q, family, tile_tokens);
     const dim3 grid((unsigned)((int64_t)p.n_chunks * q.tiles_per_chunk), (unsigned)p.L,
                     (unsigned)simt_segments(q, family));
+    const int threads = simt_threads((int64_t)grid.x * grid.y * grid.z);
     cudaError_t e = cudaSuccess;
     switch (family) {
     case FAMILY_GQA:
         e = cudaFuncSetAttribute(rows_simt_kernel<FAMILY_GQA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            rows_simt_kernel<FAMILY_GQA><<<grid, 256, smem, stream>>>(q, tile_tokens);
+            rows_simt_kernel<FAMILY_GQA><<<grid, threads, smem, stream>>>(q, tile_tokens);
         break;
     case FAMILY_MLA:
         e = cudaFuncSetAttribute(rows_simt_kernel<FAMILY_MLA>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            rows_simt_kernel<FAMILY_MLA><<<grid, 256, smem, stream>>>(q, tile_tokens);
+            rows_simt_kernel<FAMILY_MLA><<<grid, threads, smem, stream>>>(q, tile_tokens);
         break;
     default:
         e = cudaFuncSetAttribute(rows_simt_kernel<FAMILY_SLIDE>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
         if (e == cudaSuccess)
-            rows_simt_kernel<FAMILY_SLIDE><<<grid, 256, smem, stream>>>(q, tile_tokens);
+            rows_simt_kernel<FAMILY_SLIDE><<<grid, threads, smem, stream>>>(q, tile_tokens);
         break;
     }
     if (e != cudaSuccess)
