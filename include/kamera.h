@@ -71,6 +71,7 @@
 #ifndef KAMERA_H
 #define KAMERA_H
 
+#include <stddef.h>
 #include <stdint.h>
 
 #ifdef __cplusplus
@@ -79,7 +80,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
-#define KAMERA_ABI_VERSION 7
+#define KAMERA_ABI_VERSION 8
 
 /* Limits of this library. */
 #define KAMERA_MAX_RANK 128          /* largest patch rank m */
@@ -452,6 +453,17 @@ int kamera_form_patch(const KameraDeficit* deficit, int32_t m, void* u, void* v,
  *   d_seq_start  device int32 [n_seqs + 1], non-decreasing, in [0, n_chunks]
  *   dst_slot_mapping of the descriptors is not read; ranks <= max_rank <= 64.
  * Supported: head_dim 64 or 128, num_q_heads / num_kv_heads in 1..8.
+ *   d_workspace, workspace_bytes  NULL / 0, or device scratch of at least
+ *           kamera_attend_workspace_bytes(n_seqs, num_kv_heads, head_dim) bytes,
+ *           16-byte aligned, disjoint from the call's arrays; owned by the
+ *           caller, overwritten by the call (calls that overlap on the GPU must
+ *           not share one).  With it the call may spread every (sequence, KV
+ *           head)'s tiles over all SMs, each CTA leaving a partial softmax
+ *           state per unit it touches in the workspace, and merge them in a
+ *           second launch on the same stream; without it the units' tiles are
+ *           split only within clusters of at most 8 CTAs (the same results to
+ *           fp32 rounding order).  A workspace that is too small, misaligned or
+ *           overlapping: INVALID_ARGUMENT / MISALIGNED.
  * Device errors (the chunk is skipped): SOURCE, DESCRIPTOR (also a malformed
  * d_seq_start: the sequence is skipped), LEN, RANK; TIMEOUT if a tile's copy
  * wait runs past its bound (outputs of the call then undefined).  Host error
@@ -480,7 +492,14 @@ typedef struct KameraAttnQuery {
 
 int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, const KameraRope* rope,
                          const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
-                         int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream);
+                         int32_t max_len, int32_t max_rank, void* d_workspace, size_t workspace_bytes,
+                         int32_t* d_err, struct CUstream_st* stream);
+
+/* Workspace bytes kamera_attend_reused may use for this batch on the current
+ * device ((SM count + n_seqs * num_kv_heads - 1) partial states of
+ * 4 (32 + 16 head_dim) bytes); 0 for an unsupported head_dim or empty batch,
+ * or when the device cannot be queried. */
+size_t kamera_attend_workspace_bytes(int32_t n_seqs, int32_t num_kv_heads, int32_t head_dim);
 
 /*
  * MLA decode attention over reused chunks (absorbed form), without the pool.
@@ -506,9 +525,12 @@ int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, c
  *   d_seq_start, descriptors: as for kamera_attend_reused; ranks even.
  * Supported: kv_lora_rank 512, rope_dim 64 (DeepSeek-V2/V3), num_q_heads 1..128
  * (served in groups of 16: each group beyond the first is one more pass over the
- * rows), max_rank <= 32.  Device errors (the chunk is skipped): SOURCE, DESCRIPTOR
- * (also an odd rank, or a malformed d_seq_start: the sequence is skipped), LEN,
- * RANK.
+ * rows), max_rank <= 32.  d_workspace, workspace_bytes: as for
+ * kamera_attend_reused, sized by kamera_mla_attend_workspace_bytes (the units
+ * are (sequence, group of 16 query heads)).  Device errors (the chunk is
+ * skipped): SOURCE, DESCRIPTOR (also an odd rank, or a malformed d_seq_start:
+ * the sequence is skipped), LEN, RANK; TIMEOUT as for kamera_attend_reused.
+ * Host error UNSUPPORTED also for num_rows > 2^31 - 1.
  */
 typedef struct KameraAttnMlaKV {
     const void* kv;
@@ -522,7 +544,14 @@ typedef struct KameraAttnMlaKV {
 
 int kamera_mla_attend_reused(const KameraAttnMlaKV* kv, const KameraAttnQuery* query, const KameraRope* rope,
                              const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
-                             int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream);
+                             int32_t max_len, int32_t max_rank, void* d_workspace, size_t workspace_bytes,
+                             int32_t* d_err, struct CUstream_st* stream);
+
+/* Workspace bytes kamera_mla_attend_reused may use for this batch on the
+ * current device ((SM count + n_seqs * ceil(num_q_heads / 16) - 1) partial
+ * states of 4 (32 + 16 * 512) bytes); 0 for an empty batch or when the device
+ * cannot be queried. */
+size_t kamera_mla_attend_workspace_bytes(int32_t n_seqs, int32_t num_q_heads);
 
 /* KAMERA_ABI_VERSION of the loaded library. */
 int kamera_abi_version(void);

@@ -153,10 +153,15 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C
                                       C.c_void_p]
     lib.kamera_attend_reused.restype = C.c_int
     lib.kamera_attend_reused.argtypes = [P(_AttnKV), P(_AttnQuery), P(_Rope), C.c_void_p, C.c_void_p, C.c_int32,
-                                         C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
+                                         C.c_int32, C.c_int32, C.c_void_p, C.c_size_t, C.c_void_p, C.c_void_p]
     lib.kamera_mla_attend_reused.restype = C.c_int
     lib.kamera_mla_attend_reused.argtypes = [P(_AttnMlaKV), P(_AttnQuery), P(_Rope), C.c_void_p, C.c_void_p,
-                                             C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
+                                             C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_size_t, C.c_void_p,
+                                             C.c_void_p]
+    lib.kamera_attend_workspace_bytes.restype = C.c_size_t
+    lib.kamera_attend_workspace_bytes.argtypes = [C.c_int32, C.c_int32, C.c_int32]
+    lib.kamera_mla_attend_workspace_bytes.restype = C.c_size_t
+    lib.kamera_mla_attend_workspace_bytes.argtypes = [C.c_int32, C.c_int32]
     lib.kamera_validate_chunks.restype = C.c_int
     lib.kamera_validate_chunks.argtypes = [P(_Chunk), C.c_int32, C.c_int64, C.c_int64, C.c_int32,
                                            C.c_int32, P(C.c_int32), P(C.c_int32)]
@@ -176,7 +181,7 @@ def kamera_status_string(status: int) -> str:
     return load_library().kamera_status_string(int(status)).decode()
 
 
-ABI_VERSION = 7   # the KAMERA_ABI_VERSION these bindings marshal for
+ABI_VERSION = 8   # the KAMERA_ABI_VERSION these bindings marshal for
 
 
 def kamera_abi_version() -> int:
@@ -524,18 +529,47 @@ def kamera_form_patch(delta: torch.Tensor, m: int, u: Optional[torch.Tensor] = N
     return u, v
 
 
+# Attention workspaces the binding keeps, per (device, stream): a call's
+# partial softmax states live there until its merge launch has read them, so
+# calls on one stream (which run in order) may share one, and calls on
+# different streams get their own.
+_WORKSPACES = {}
+
+
+def _workspace(workspace, need: int, device, stream):
+    """(address, bytes) of the attention workspace: the caller's tensor, none
+    (workspace=False or nothing needed), or the binding's cached buffer for this
+    device and stream, grown to `need` bytes."""
+    if workspace is False or (workspace is None and need == 0):
+        return None, 0
+    if isinstance(workspace, torch.Tensor):
+        _on_device("attention workspace", workspace=workspace)
+        if not workspace.is_contiguous():
+            raise ValueError("workspace must be contiguous")
+        return workspace.data_ptr(), workspace.numel() * workspace.element_size()
+    key = (torch.device(device).index, _stream_handle(stream))
+    buf = _WORKSPACES.get(key)
+    if buf is None or buf.numel() < need:
+        buf = torch.empty(need, dtype=torch.uint8, device=device)
+        _WORKSPACES[key] = buf
+    return buf.data_ptr(), buf.numel()
+
+
 def kamera_attend_reused(store_k: torch.Tensor, store_v: torch.Tensor, q: torch.Tensor, rope: Rope,
                          chunks: torch.Tensor, seq_start: torch.Tensor, n_chunks: int, max_len: int,
                          max_rank: int, layer: int = 0, scale: Optional[float] = None,
                          out: Optional[torch.Tensor] = None, err: Optional[torch.Tensor] = None,
-                         stream=None) -> torch.Tensor:
+                         stream=None, workspace=None) -> torch.Tensor:
     """Decode attention of one query token per sequence over its reused chunks,
     never writing a relocated row (see ``kamera_attend_reused`` in kamera.h).
 
     store_k/v: bf16 ``[N, H_kv, d]`` (one layer; packed heads, any row stride);
     q: bf16 ``[S, H_q, d]`` contiguous; seq_start: device int32 ``[S + 1]``;
     chunks: packed descriptors; layer: the factors' layer index; scale:
-    default 1/sqrt(d).  Returns ``out`` (bf16 ``[S, H_q, d]``)."""
+    default 1/sqrt(d); workspace: None (a buffer this module keeps per device
+    and stream, sized by ``kamera_attend_workspace_bytes``), False (none: the
+    cluster path) or a CUDA tensor of the caller's.  Returns ``out`` (bf16
+    ``[S, H_q, d]``)."""
     _on_device("kamera_attend_reused", store_k=store_k, store_v=store_v, q=q, chunks=chunks, seq_start=seq_start,
                out=out, err=err)
     for t, nm in ((store_k, "store_k"), (store_v, "store_v"), (q, "q")):
@@ -556,10 +590,13 @@ def kamera_attend_reused(store_k: torch.Tensor, store_v: torch.Tensor, q: torch.
         raise ValueError("seq_start must hold S + 1 int32 values")
     kv = _AttnKV(_addr(store_k), _addr(store_v), N, store_k.stride(0), H, d, int(layer), 0)
     qq = _AttnQuery(_addr(q), _addr(out), S, Hq, float(d ** -0.5 if scale is None else scale), 0)
+    lib = load_library()
+    need = lib.kamera_attend_workspace_bytes(S, H, d) if workspace is None and S > 0 else 0
+    ws, ws_bytes = _workspace(workspace, need, q.device, stream)
     r, keep = rope._c(n_chunks)
-    rc = load_library().kamera_attend_reused(C.byref(kv), C.byref(qq), C.byref(r), _addr(chunks), _addr(seq_start),
-                                             int(n_chunks), int(max_len), int(max_rank), _addr(err),
-                                             _stream_handle(stream))
+    rc = lib.kamera_attend_reused(C.byref(kv), C.byref(qq), C.byref(r), _addr(chunks), _addr(seq_start),
+                                  int(n_chunks), int(max_len), int(max_rank), ws, ws_bytes, _addr(err),
+                                  _stream_handle(stream))
     del keep
     _check(rc, "kamera_attend_reused")
     return out
@@ -568,15 +605,15 @@ def kamera_attend_reused(store_k: torch.Tensor, store_v: torch.Tensor, q: torch.
 def kamera_mla_attend_reused(store: torch.Tensor, kv_lora: int, q: torch.Tensor, rope: Rope, chunks: torch.Tensor,
                              seq_start: torch.Tensor, n_chunks: int, max_len: int, max_rank: int, layer: int = 0,
                              scale: Optional[float] = None, out: Optional[torch.Tensor] = None,
-                             err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+                             err: Optional[torch.Tensor] = None, stream=None, workspace=None) -> torch.Tensor:
     """MLA decode attention (absorbed form) of one query token per sequence over
     its reused chunks (see ``kamera_mla_attend_reused`` in kamera.h).
 
     store: bf16 ``[N, kv_lora + rope_dim]`` (one layer, any row stride);
     q: bf16 ``[S, H_q, kv_lora + rope_dim]`` contiguous (latent query, then
     rope query); seq_start: device int32 ``[S + 1]``; rope: rot_offset
-    relative to k_rope; scale: default 1/sqrt(kv_lora + rope_dim).  Returns
-    ``out`` (bf16 ``[S, H_q, kv_lora]``)."""
+    relative to k_rope; scale: default 1/sqrt(kv_lora + rope_dim); workspace:
+    as for ``kamera_attend_reused``.  Returns ``out`` (bf16 ``[S, H_q, kv_lora]``)."""
     _on_device("kamera_mla_attend_reused", store=store, q=q, chunks=chunks, seq_start=seq_start, out=out, err=err)
     for t, nm in ((store, "store"), (q, "q")):
         _bf16(t, nm)
@@ -594,10 +631,13 @@ def kamera_mla_attend_reused(store: torch.Tensor, kv_lora: int, q: torch.Tensor,
         raise ValueError("seq_start must hold S + 1 int32 values")
     kv = _AttnMlaKV(_addr(store), N, store.stride(0), int(kv_lora), int(W - kv_lora), int(layer), 0)
     qq = _AttnQuery(_addr(q), _addr(out), S, Hq, float(W ** -0.5 if scale is None else scale), 0)
+    lib = load_library()
+    need = lib.kamera_mla_attend_workspace_bytes(S, Hq) if workspace is None and S > 0 else 0
+    ws, ws_bytes = _workspace(workspace, need, q.device, stream)
     r, keep = rope._c(n_chunks)
-    rc = load_library().kamera_mla_attend_reused(C.byref(kv), C.byref(qq), C.byref(r), _addr(chunks),
-                                                 _addr(seq_start), int(n_chunks), int(max_len), int(max_rank),
-                                                 _addr(err), _stream_handle(stream))
+    rc = lib.kamera_mla_attend_reused(C.byref(kv), C.byref(qq), C.byref(r), _addr(chunks), _addr(seq_start),
+                                      int(n_chunks), int(max_len), int(max_rank), ws, ws_bytes, _addr(err),
+                                      _stream_handle(stream))
     del keep
     _check(rc, "kamera_mla_attend_reused")
     return out

@@ -8,6 +8,7 @@
 #include <cstdint>
 #include <cstdlib>
 #include <cstring>
+#include <initializer_list>
 #include <mutex>
 #include <utility>
 #include <vector>
@@ -210,6 +211,35 @@ int launch(const RowsParams& p, int family, const KameraChunk* h_chunks, cudaStr
     if (!simt_ok)
         return KAMERA_ERR_UNSUPPORTED;
     return launch_simt(p, family, stream) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
+}
+
+// Workspace of the attention split path on the current device: one slot per
+// (CTA, unit) pair the split can make, CTAs resident at once (<= the SM count)
+// + units - 1, of attend_slot_bytes(dout) each; 0 if the device is unknown.
+size_t attend_workspace_for(int64_t units, int dout)
+{
+    int dev = 0, sms = 0;
+    if (units < 1 || cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || sms < 1)
+        return 0;
+    return (size_t)(sms + units - 1) * attend_slot_bytes(dout);
+}
+
+// The caller's workspace: NULL (the cluster path) or 16-byte aligned, at least
+// `need` bytes, and disjoint from the call's arrays.
+int check_workspace(const void* ws, size_t bytes, size_t need, std::initializer_list<std::pair<uintptr_t, uintptr_t>> arrays)
+{
+    if (!ws)
+        return KAMERA_OK;
+    if (!aligned16(ws))
+        return KAMERA_ERR_MISALIGNED;
+    if (need == 0 || bytes < need)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    const uintptr_t lo = reinterpret_cast<uintptr_t>(ws);
+    for (const auto& a : arrays)
+        if (overlap({lo, lo + bytes}, a))
+            return KAMERA_ERR_INVALID_ARGUMENT;
+    return KAMERA_OK;
 }
 
 }  // namespace
@@ -605,9 +635,24 @@ int kamera_form_patch(const KameraDeficit* df, int32_t m, void* u, void* v, floa
                                                                                           : KAMERA_ERR_CUDA;
 }
 
+size_t kamera_attend_workspace_bytes(int32_t n_seqs, int32_t num_kv_heads, int32_t head_dim)
+{
+    if (n_seqs < 1 || num_kv_heads < 1 || (head_dim != 64 && head_dim != 128))
+        return 0;
+    return attend_workspace_for((int64_t)n_seqs * num_kv_heads, head_dim);
+}
+
+size_t kamera_mla_attend_workspace_bytes(int32_t n_seqs, int32_t num_q_heads)
+{
+    if (n_seqs < 1 || num_q_heads < 1)
+        return 0;
+    return attend_workspace_for((int64_t)n_seqs * ((num_q_heads + 15) / 16), 512);
+}
+
 int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, const KameraRope* rope,
                          const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
-                         int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream)
+                         int32_t max_len, int32_t max_rank, void* d_workspace, size_t workspace_bytes,
+                         int32_t* d_err, struct CUstream_st* stream)
 {
     if (!kv || !query || !rope || kv->reserved != 0 || query->reserved != 0)
         return KAMERA_ERR_INVALID_ARGUMENT;
@@ -636,9 +681,13 @@ int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, c
     const auto qs = span(query->q, 1, 0, 1, 0, qn);
     if (overlap(os, ks) || overlap(os, vs) || overlap(os, qs))
         return KAMERA_ERR_INVALID_ARGUMENT;
+    int rc = check_workspace(d_workspace, workspace_bytes,
+                             attend_workspace_for((int64_t)query->n_seqs * kv->num_kv_heads, kv->head_dim),
+                             {ks, vs, qs, os});
+    if (rc)
+        return rc;
     AttendParams p;
     std::memset(&p, 0, sizeof(p));
-    int rc;
     if ((rc = fill_rope(rope, kv->head_dim, &p.rope)))
         return rc;
     p.k = static_cast<const __nv_bfloat16*>(kv->k);
@@ -662,12 +711,15 @@ int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, c
     p.cluster = attend_cluster((int64_t)query->n_seqs * kv->num_kv_heads);   // the launch may pick up to 8
     if ((int64_t)query->n_seqs * 8 > 0x7FFFFFFF)
         return KAMERA_ERR_UNSUPPORTED;
-    return launch_attend(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
+    return launch_attend(p, d_workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KAMERA_OK
+               : KAMERA_ERR_CUDA;
 }
 
 int kamera_mla_attend_reused(const KameraAttnMlaKV* kv, const KameraAttnQuery* query, const KameraRope* rope,
                              const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
-                             int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream)
+                             int32_t max_len, int32_t max_rank, void* d_workspace, size_t workspace_bytes,
+                             int32_t* d_err, struct CUstream_st* stream)
 {
     if (!kv || !query || !rope || kv->reserved != 0 || query->reserved != 0)
         return KAMERA_ERR_INVALID_ARGUMENT;
@@ -675,7 +727,7 @@ int kamera_mla_attend_reused(const KameraAttnMlaKV* kv, const KameraAttnQuery* q
         kv->kv_lora_rank < 1 || kv->rope_dim < 0 || query->num_q_heads < 1 || !(query->scale == query->scale))
         return KAMERA_ERR_INVALID_ARGUMENT;
     if (!mla_attend_supported(kv->kv_lora_rank, kv->rope_dim, query->num_q_heads, max_rank) ||
-        query->n_seqs > 0x7FFFFFFF / 8)
+        query->n_seqs > 0x7FFFFFFF / 8 || kv->num_rows > 0x7FFFFFFF)
         return KAMERA_ERR_UNSUPPORTED;
     if (query->n_seqs == 0)
         return KAMERA_OK;
@@ -692,9 +744,13 @@ int kamera_mla_attend_reused(const KameraAttnMlaKV* kv, const KameraAttnQuery* q
     const auto os = span(query->out, 1, 0, 1, 0, (int64_t)query->n_seqs * query->num_q_heads * kv->kv_lora_rank);
     if (overlap(os, ks) || overlap(os, qs))
         return KAMERA_ERR_INVALID_ARGUMENT;
+    int rc = check_workspace(
+        d_workspace, workspace_bytes,
+        attend_workspace_for((int64_t)query->n_seqs * ((query->num_q_heads + 15) / 16), kv->kv_lora_rank), {ks, qs, os});
+    if (rc)
+        return rc;
     MlaAttendParams p;
     std::memset(&p, 0, sizeof(p));
-    int rc;
     if ((rc = fill_rope(rope, kv->rope_dim, &p.rope)))
         return rc;
     p.kv = static_cast<const __nv_bfloat16*>(kv->kv);
@@ -714,7 +770,9 @@ int kamera_mla_attend_reused(const KameraAttnMlaKV* kv, const KameraAttnQuery* q
     p.max_len = max_len;
     p.max_rank = max_rank;
     p.err = d_err;
-    return launch_mla_attend(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
+    return launch_mla_attend(p, d_workspace, workspace_bytes, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? KAMERA_OK
+               : KAMERA_ERR_CUDA;
 }
 
 }  // extern "C"

@@ -102,6 +102,7 @@ struct AttendLaunch {
     AttendParams p;
     CUtensorMap map_k, map_v;
     uint64_t wait_ns;
+    float* ws;       // split path: the partial softmax states (NULL: the cluster path)
 };
 
 __device__ __forceinline__ int32_t attend_check(const KameraChunk& ch, int c, const AttendParams& p)
@@ -211,31 +212,21 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
     // swizzled TMA boxes want 1024-byte alignment (the same offset in every CTA)
     SM& s = *reinterpret_cast<SM*>(smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u));
     namespace cg = cooperative_groups;
-    const int CL = p.cluster, rank = (int)(blockIdx.x % (unsigned)CL);
-    const int seq = blockIdx.x / CL, g = blockIdx.y;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, gq = lane >> 2, t4 = lane & 3;
     const int G = p.G, HQ = p.H * G;
     // 8x8 matrix-load addressing of a row-major 16 x 16 A operand
     const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
+    // The units this CTA serves (unit u: sequence u / H, KV head u % H).  Cluster
+    // path: one unit, its tiles split evenly over the cluster's CTAs by rank.  Split
+    // path: CTA k of NC takes the unit-fraction range [k U / NC, (k + 1) U / NC) and
+    // leaves one partial softmax state per unit it touches in the workspace (slot
+    // k + u); a second kernel merges them.
+    const bool split = P.ws != nullptr;
+    const int CL = split ? 1 : p.cluster, rank = split ? 0 : (int)(blockIdx.x % (unsigned)CL);
+    const int64_t U = (int64_t)p.n_seqs * p.H, NC = gridDim.x, kc = blockIdx.x;
+    const int64_t u_begin = split ? kc * U / NC : (int64_t)(blockIdx.x / CL) * p.H + blockIdx.y;
+    const int64_t u_end = split ? ((kc + 1) * U + NC - 1) / NC : u_begin + 1;
 
-    int c0 = p.seq_start[seq], c1 = p.seq_start[seq + 1];
-    if (c0 < 0 || c1 < c0 || c1 > p.n_chunks) {
-        if (g == 0 && rank == 0 && threadIdx.x == 0)
-            raise_err(p.err, KAMERA_DEVERR_DESCRIPTOR);
-        c0 = c1 = 0;
-    }
-    int64_t total = 0;
-    for (int c = c0; c < c1; ++c) {
-        const KameraChunk& ch = p.chunks[c];
-        if (!attend_check(ch, c, p))
-            total += (ch.len + kAtT - 1) / kAtT;
-    }
-    const int64_t lo = total * rank / CL, hi = total * (rank + 1) / CL;
-
-    for (int e = threadIdx.x; e < kAtH * D; e += kAtThreads) {
-        const int h = e / D, i = e - h * D;
-        s.q[h][i] = h < G ? p.q[((int64_t)seq * HQ + g * G + h) * D + i] : __float2bfloat16_rn(0.f);
-    }
     if (threadIdx.x == 0) {
         for (int w = 0; w < kAtCW; ++w)
             for (int b = 0; b < NS; ++b)
@@ -247,8 +238,42 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
         ptx::prefetch_tmap(&P.map_k);
         ptx::prefetch_tmap(&P.map_v);
     }
-    __syncthreads();
     const RopeParams& rp = p.rope;
+    uint32_t ph = 0;   // phase parity of this warp's barrier per buffer (kept across units)
+
+    for (int64_t u = u_begin; u < u_end; ++u) {
+    const int seq = (int)(u / p.H), g = (int)(u % p.H);
+    int c0 = p.seq_start[seq], c1 = p.seq_start[seq + 1];
+    if (c0 < 0 || c1 < c0 || c1 > p.n_chunks) {
+        if (g == 0 && rank == 0 && threadIdx.x == 0 && (!split || kc * U <= u * NC))
+            raise_err(p.err, KAMERA_DEVERR_DESCRIPTOR);
+        c0 = c1 = 0;
+    }
+    int64_t total = 0;
+    for (int c = c0; c < c1; ++c) {
+        const KameraChunk& ch = p.chunks[c];
+        if (!attend_check(ch, c, p))
+            total += (ch.len + kAtT - 1) / kAtT;
+    }
+    // this CTA's share of the unit's tiles; `first`: the share that starts the unit
+    int64_t lo, hi;
+    bool first;
+    if (split) {
+        const int64_t a = max(kc * U, u * NC), e = min((kc + 1) * U, (u + 1) * NC);
+        lo = total * (a - u * NC) / NC;
+        hi = total * (e - u * NC) / NC;
+        first = a == u * NC;
+    } else {
+        lo = total * rank / CL;
+        hi = total * (rank + 1) / CL;
+        first = rank == 0;
+    }
+
+    __syncthreads();   // the previous unit is done with every shared array (first: barriers initialised)
+    for (int e = threadIdx.x; e < kAtH * D; e += kAtThreads) {
+        const int h = e / D, i = e - h * D;
+        s.q[h][i] = h < G ? p.q[((int64_t)seq * HQ + g * G + h) * D + i] : __float2bfloat16_rn(0.f);
+    }
 
     {
         // ------------------------------------------------------------ the warps
@@ -279,14 +304,13 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
             warp_load<D, MP>(P, s, lc, ltl, g, warp, lane, j);
             lmore = next_tile(p, c1, lo, hi, lc, ltl, lthi, lpos);
         }
-        uint32_t ph = 0;   // phase parity of this warp's barrier per buffer
         int gi = 0;
         int64_t pos = 0;
         for (int c = c0; c < c1; ++c) {
             const KameraChunk& ch = p.chunks[c];
             const int32_t bad = attend_check(ch, c, p);
             if (bad) {
-                if (rank == 0 && threadIdx.x == 0)
+                if (first && threadIdx.x == 0)
                     raise_err(p.err, bad);
                 continue;
             }
@@ -569,6 +593,18 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
         ob[e] = acc;
     }
 
+    if (split) {   // ---- this CTA's partial state of unit u -> workspace slot k + u
+        float* wp = P.ws + (size_t)(kc + u) * (2 * kAtH + kAtH * D);
+        __syncthreads();
+        if (threadIdx.x < kAtH) {
+            wp[threadIdx.x] = s.cm[threadIdx.x];
+            wp[kAtH + threadIdx.x] = s.cl[threadIdx.x];
+        }
+        for (int e = threadIdx.x; e < kAtH * D / 4; e += kAtThreads)
+            reinterpret_cast<float4*>(wp + 2 * kAtH)[e] = reinterpret_cast<const float4*>(ob)[e];
+        ptx::fence_proxy_async();   // the merge's shared writes precede the next unit's TMA refills
+        continue;
+    }
     // ---- cluster merge: every CTA publishes (max, sum, unnormalised output); rank 0 combines
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
@@ -610,9 +646,74 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
         }
     }
     cluster.sync();   // peers stay until rank 0 has read them
+    }
+}
+
+// Merge of the split path (one CTA per unit u): the CTAs k that overlapped u
+// (k U / NC < u + 1 and (k + 1) U / NC > u) left (max, sum, unnormalised
+// output) per head in slot k + u; out = sum_k e^(m_k - M) O_k / sum_k
+// e^(m_k - M) l_k, rounded once to bf16.  Unit u's rows start at row
+// (u / groups) Hq + (u % groups) 16 of `out` ([*][dout]); `rows` of them.
+__global__ void __launch_bounds__(128) attend_merge_kernel(const float* __restrict__ ws, int64_t U, int64_t NC,
+                                                           int dout, int groups, int Hq, int rows_max,
+                                                           __nv_bfloat16* __restrict__ out)
+{
+    __shared__ float mx[kAtH], sum[kAtH];
+    const int64_t u = blockIdx.x;
+    const int64_t k_lo = u * NC / U, k_hi = ((u + 1) * NC + U - 1) / U;   // CTAs [k_lo, k_hi)
+    const size_t slot = (size_t)(2 * kAtH + kAtH * dout);
+    const int grp = (int)(u % groups), rows = min(rows_max, Hq - grp * kAtH);
+    const int64_t row0 = (u / groups) * Hq + grp * kAtH;
+    if (threadIdx.x < kAtH) {
+        const int h = threadIdx.x;
+        float m = -INFINITY;
+        for (int64_t k = k_lo; k < k_hi; ++k)
+            m = fmaxf(m, ws[(size_t)(k + u) * slot + h]);
+        float l = 0.f;
+        for (int64_t k = k_lo; k < k_hi; ++k) {
+            const float mk = ws[(size_t)(k + u) * slot + h];
+            if (mk != -INFINITY)
+                l = fmaf(ws[(size_t)(k + u) * slot + kAtH + h], expf(mk - m), l);
+        }
+        mx[h] = m;
+        sum[h] = l;
+    }
+    __syncthreads();
+    for (int e = threadIdx.x; e < rows * (dout / 4); e += blockDim.x) {
+        const int h = e / (dout / 4), i = 4 * (e - h * (dout / 4));
+        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (sum[h] > 0.f) {
+            for (int64_t k = k_lo; k < k_hi; ++k) {
+                const float* wk = ws + (size_t)(k + u) * slot;
+                if (wk[h] == -INFINITY)
+                    continue;
+                const float f = expf(wk[h] - mx[h]) / sum[h];
+                const float4 v = *reinterpret_cast<const float4*>(wk + 2 * kAtH + h * dout + i);
+                acc.x = fmaf(v.x, f, acc.x);
+                acc.y = fmaf(v.y, f, acc.y);
+                acc.z = fmaf(v.z, f, acc.z);
+                acc.w = fmaf(v.w, f, acc.w);
+            }
+        }
+        uint2 w;
+        w.x = pack_bf16x2(acc.x, acc.y);
+        w.y = pack_bf16x2(acc.z, acc.w);
+        *reinterpret_cast<uint2*>(out + (row0 + h) * dout + i) = w;
+    }
 }
 
 }  // namespace
+
+cudaError_t launch_attend_merge(const float* ws, int64_t units, int64_t ctas, int dout, int groups, int Hq,
+                                int rows, __nv_bfloat16* out, cudaStream_t stream)
+{
+    if (units < 1)
+        return cudaSuccess;
+    attend_merge_kernel<<<(unsigned)units, 128, 0, stream>>>(ws, units, ctas, dout, groups, Hq, rows, out);
+    return cudaGetLastError();
+}
+
+size_t attend_slot_bytes(int dout) { return sizeof(float) * (size_t)(2 * kAtH + kAtH * dout); }
 
 bool attend_supported(int head_dim, int G, int max_rank)
 {
@@ -627,11 +728,11 @@ bool attend_supported(int head_dim, int G, int max_rank)
 // the query is unavailable.  The occupancy answers are cached per kernel and
 // device (cluster_fit), so a decode step pays only this arithmetic.
 template <int D, int MP>
-static int attend_pick_cluster(const AttendParams& p, int bytes, int fallback)
+static int attend_pick_cluster(const AttendParams& p, int bytes, int fallback, double& best_t)
 {
     const int64_t units = (int64_t)p.n_seqs * p.H;
     int best = fallback;
-    double best_t = 1e300;
+    best_t = 1e300;
     for (int cl = 1; cl <= kAtMaxCL; ++cl) {
         const int fit = cluster_fit(reinterpret_cast<const void*>(attend_kernel<D, MP>), kAtThreads, bytes, cl);
         if (fit < 1)
@@ -645,8 +746,13 @@ static int attend_pick_cluster(const AttendParams& p, int bytes, int fallback)
     return best;
 }
 
+// Split path or cluster path.  With a workspace, the split path spreads the
+// units' tiles over every CTA that fits at once (NC), evenly to a tile, at the
+// cost of a second, small launch that merges the partial states: its time is
+// U / NC units against the cluster path's waves / CL; it is taken when that is
+// at least 3% less.
 template <int D, int MP>
-static cudaError_t launch_attend_m(const AttendParams& p0, cudaStream_t stream)
+static cudaError_t launch_attend_m(const AttendParams& p0, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
     AttendLaunch L;
     std::memset(&L, 0, sizeof(L));
@@ -663,7 +769,19 @@ static cudaError_t launch_attend_m(const AttendParams& p0, cudaStream_t stream)
     cudaError_t e = cudaFuncSetAttribute(attend_kernel<D, MP>, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
     if (e != cudaSuccess)
         return e;
-    p.cluster = attend_pick_cluster<D, MP>(p, bytes, p.cluster);
+    double t_cluster;
+    p.cluster = attend_pick_cluster<D, MP>(p, bytes, p.cluster, t_cluster);
+    const int64_t units = (int64_t)p.n_seqs * p.H;
+    const int nc = cluster_fit(reinterpret_cast<const void*>(attend_kernel<D, MP>), kAtThreads, bytes, 1);
+    if (ws && nc >= 1 && (size_t)(nc + units - 1) * attend_slot_bytes(D) <= ws_bytes &&
+        (double)units / nc < 0.97 * t_cluster) {
+        L.ws = static_cast<float*>(ws);
+        p.cluster = 1;
+        attend_kernel<D, MP><<<(unsigned)nc, kAtThreads, bytes, stream>>>(L);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+        return launch_attend_merge(L.ws, units, nc, D, 1, p.G, p.G, p.out, stream);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.n_seqs * p.cluster), (unsigned)p.H);
     cfg.blockDim = dim3(kAtThreads);
@@ -680,15 +798,15 @@ static cudaError_t launch_attend_m(const AttendParams& p0, cudaStream_t stream)
 }
 
 template <int D>
-static cudaError_t launch_attend_d(const AttendParams& p, cudaStream_t stream)
+static cudaError_t launch_attend_d(const AttendParams& p, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
     if (p.max_rank == 0)
-        return launch_attend_m<D, 0>(p, stream);
+        return launch_attend_m<D, 0>(p, ws, ws_bytes, stream);
     if (p.max_rank <= 16)
-        return launch_attend_m<D, 16>(p, stream);
+        return launch_attend_m<D, 16>(p, ws, ws_bytes, stream);
     if (p.max_rank <= 32)
-        return launch_attend_m<D, 32>(p, stream);
-    return launch_attend_m<D, 64>(p, stream);
+        return launch_attend_m<D, 32>(p, ws, ws_bytes, stream);
+    return launch_attend_m<D, 64>(p, ws, ws_bytes, stream);
 }
 
 // Default cluster size (used when the occupancy query is unavailable): the
@@ -705,9 +823,9 @@ int attend_cluster(int64_t units)
     return cl;
 }
 
-cudaError_t launch_attend(const AttendParams& p, cudaStream_t stream)
+cudaError_t launch_attend(const AttendParams& p, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
-    return p.d == 64 ? launch_attend_d<64>(p, stream) : launch_attend_d<128>(p, stream);
+    return p.d == 64 ? launch_attend_d<64>(p, ws, ws_bytes, stream) : launch_attend_d<128>(p, ws, ws_bytes, stream);
 }
 
 }  // namespace kamera

@@ -100,6 +100,7 @@ struct MlaLaunch {
     MlaAttendParams p;
     CUtensorMap map;
     uint64_t wait_ns;
+    float* ws;       // split path: the partial softmax states (NULL: the cluster path)
 };
 
 __device__ __forceinline__ void st_shared_u32(uint32_t a, uint32_t v)
@@ -176,31 +177,20 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
     // swizzled TMA boxes want 1024-byte alignment (the same offset in every CTA)
     SM& s = *reinterpret_cast<SM*>(smem_raw + ((1024u - (ptx::smem_addr(smem_raw) & 1023u)) & 1023u));
     namespace cg = cooperative_groups;
-    const int CL = p.cluster, rank = (int)(blockIdx.x % (unsigned)CL), seq = blockIdx.x / CL;
-    // query heads h0 .. h0 + Hg - 1 (a group of up to 16: the rows of every MMA)
-    const int h0 = (int)blockIdx.y * kMlH;
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31, g = lane >> 2, t4 = lane & 3;
-    const int Hq = p.Hq, Hg = min(kMlH, Hq - h0);
+    const int Hq = p.Hq, groups = (Hq + kMlH - 1) / kMlH;
     // 8x8 matrix-load addressing: A (row-major 16 x 16) and B^T (token rows)
     const int arow = (lane & 7) + ((lane >> 3) & 1) * 8, acol = (lane >> 4) * 8;
-
-    int c0 = p.seq_start[seq], c1 = p.seq_start[seq + 1];
-    if (c0 < 0 || c1 < c0 || c1 > p.n_chunks) {
-        if (rank == 0 && threadIdx.x == 0)
-            raise_err(p.err, KAMERA_DEVERR_DESCRIPTOR);
-        c0 = c1 = 0;
-    }
-    // this CTA's share: tiles [lo, hi) of the sequence's valid chunks' tiles, in order
-    int64_t total = 0;
-    for (int c = c0; c < c1; ++c) {
-        const KameraChunk& ch = p.chunks[c];
-        if (!mla_check(ch, c, p))
-            total += (ch.len + kMlT - 1) / kMlT;
-    }
-    const int64_t lo = total * rank / CL, hi = total * (rank + 1) / CL;
-
-    // the latent queries (rows past Hq zero) staged in the second tile buffer; q_rope as fp32
-    __nv_bfloat16* qls = &s.kt[1][0][0][0];
+    // The units this CTA serves (unit u: sequence u / groups, head group u % groups).
+    // Cluster path: one unit, its tiles split evenly over the cluster's CTAs by rank.
+    // Split path: CTA k of NC takes the unit-fraction range [k U / NC, (k + 1) U / NC)
+    // and leaves one partial softmax state per unit it touches in the workspace
+    // (slot k + u); a second kernel merges them.
+    const bool split = P.ws != nullptr;
+    const int CL = split ? 1 : p.cluster, rank = split ? 0 : (int)(blockIdx.x % (unsigned)CL);
+    const int64_t U = (int64_t)p.n_seqs * groups, NC = gridDim.x, kc = blockIdx.x;
+    const int64_t u_begin = split ? kc * U / NC : (int64_t)(blockIdx.x / CL) * groups + blockIdx.y;
+    const int64_t u_end = split ? ((kc + 1) * U + NC - 1) / NC : u_begin + 1;
     if (threadIdx.x == 0) {
         ptx::mbar_init(ptx::smem_addr(&s.full[0]), 1);
         ptx::mbar_init(ptx::smem_addr(&s.full[1]), 1);
@@ -209,6 +199,44 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
     }
     if (threadIdx.x == 32)
         ptx::prefetch_tmap(&P.map);
+    uint32_t ph = 0;   // phase parity of each buffer's barrier (kept across units)
+
+    for (int64_t u = u_begin; u < u_end; ++u) {
+    const int seq = (int)(u / groups);
+    // query heads h0 .. h0 + Hg - 1 (a group of up to 16: the rows of every MMA)
+    const int h0 = (int)(u % groups) * kMlH, Hg = min(kMlH, Hq - h0);
+    int c0 = p.seq_start[seq], c1 = p.seq_start[seq + 1];
+    // this CTA's share of the unit's tiles; `first`: the share that starts the unit
+    int64_t lo, hi;
+    bool first;
+    if (split) {
+        const int64_t a = max(kc * U, u * NC), e = min((kc + 1) * U, (u + 1) * NC);
+        first = a == u * NC;
+        lo = a - u * NC;   // scaled below by the unit's tiles
+        hi = e - u * NC;
+    } else {
+        first = rank == 0;
+        lo = rank;
+        hi = rank + 1;
+    }
+    const int64_t den = split ? NC : CL;
+    if (c0 < 0 || c1 < c0 || c1 > p.n_chunks) {
+        if (first && h0 == 0 && threadIdx.x == 0)
+            raise_err(p.err, KAMERA_DEVERR_DESCRIPTOR);
+        c0 = c1 = 0;
+    }
+    int64_t total = 0;
+    for (int c = c0; c < c1; ++c) {
+        const KameraChunk& ch = p.chunks[c];
+        if (!mla_check(ch, c, p))
+            total += (ch.len + kMlT - 1) / kMlT;
+    }
+    lo = total * lo / den;
+    hi = total * hi / den;
+
+    // the latent queries (rows past Hq zero) staged in the second tile buffer; q_rope as fp32
+    __nv_bfloat16* qls = &s.kt[1][0][0][0];
+    __syncthreads();   // the previous unit is done with every shared array (first: barriers initialised)
     for (int e = threadIdx.x; e < kMlH * (kMlC / 8); e += kMlThreads) {
         const int h = e / (kMlC / 8), v = e - h * (kMlC / 8);
         uint4 w = make_uint4(0u, 0u, 0u, 0u);
@@ -241,7 +269,6 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
     const uint32_t kt0 = ptx::smem_addr(&s.kt[0][0][0][0]), ux0 = ptx::smem_addr(&s.ux[0][0][0]);
     constexpr uint32_t kBuf = SM::NBX * SM::kBoxBytes;          // bytes per row buffer
     constexpr uint32_t kUBuf = (uint32_t)(kMlT * SM::URS * 2);  // bytes per u | w buffer
-    uint32_t ph = 0;   // phase parity of each buffer's barrier
     // 8x8 matrix-load addressing in the swizzled boxes: score B operand (rows 8 warp + (lane & 7),
     // pieces 4k + lane / 8) and value B operand (rows (lane & 7) + 8 ((lane / 8) & 1), pieces 2np + lane / 16)
     const int kr = 8 * warp + (lane & 7);
@@ -252,7 +279,7 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
         const KameraChunk& ch = p.chunks[c];
         const int32_t bad = mla_check(ch, c, p);
         if (bad) {
-            if (rank == 0 && threadIdx.x == 0)
+            if (first && h0 == 0 && threadIdx.x == 0)
                 raise_err(p.err, bad);
             continue;
         }
@@ -529,6 +556,18 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
         s.cm[threadIdx.x >> 4] = m_run;
         s.cl[threadIdx.x >> 4] = l_run;
     }
+    if (split) {   // ---- this CTA's partial state of unit u -> workspace slot k + u
+        float* wp = P.ws + (size_t)(kc + u) * (2 * kMlH + kMlH * kMlC);
+        __syncthreads();
+        if (threadIdx.x < kMlH) {
+            wp[threadIdx.x] = s.cm[threadIdx.x];
+            wp[kMlH + threadIdx.x] = s.cl[threadIdx.x];
+        }
+        for (int e = threadIdx.x; e < kMlH * kMlC / 4; e += kMlThreads)
+            reinterpret_cast<float4*>(wp + 2 * kMlH)[e] = reinterpret_cast<const float4*>(ob)[e];
+        ptx::fence_proxy_async();   // the partial outputs' shared writes precede the next unit's TMA refills
+        continue;
+    }
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     if (rank == 0) {
@@ -569,6 +608,7 @@ __global__ void __launch_bounds__(kMlThreads, 1) mla_attend_kernel(const __grid_
         }
     }
     cluster.sync();   // peers stay until rank 0 has read them
+    }
 }
 
 }  // namespace
@@ -587,10 +627,10 @@ bool mla_attend_supported(int kv_lora, int rope_dim, int num_q_heads, int max_ra
 // (ties: the smaller cluster).  The occupancy answers are cached per kernel and
 // device (cluster_fit).
 template <int MP>
-static int mla_pick_cluster(int64_t units, int bytes)
+static int mla_pick_cluster(int64_t units, int bytes, double& best_t)
 {
     int best = 1;
-    double best_t = 1e300;
+    best_t = 1e300;
     for (int cl = 1; cl <= kMlMaxCL; ++cl) {
         const int fit = cluster_fit(reinterpret_cast<const void*>(mla_attend_kernel<MP>), kMlThreads, bytes, cl);
         if (fit < 1)
@@ -604,8 +644,11 @@ static int mla_pick_cluster(int64_t units, int bytes)
     return best;
 }
 
+// Split path (with a workspace) or cluster path, chosen as for GQA attention:
+// the split path's U / NC against the cluster path's waves / CL, taken when at
+// least 3% less (for 38 sequences of 16 heads: 0.26 against CL = 3's 0.33).
 template <int MP>
-static cudaError_t launch_mla_attend_m(const MlaAttendParams& p0, cudaStream_t stream)
+static cudaError_t launch_mla_attend_m(const MlaAttendParams& p0, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
     MlaLaunch L;
     std::memset(&L, 0, sizeof(L));
@@ -621,7 +664,19 @@ static cudaError_t launch_mla_attend_m(const MlaAttendParams& p0, cudaStream_t s
     if (e != cudaSuccess)
         return e;
     const int groups = (p.Hq + kMlH - 1) / kMlH;
-    p.cluster = mla_pick_cluster<MP>((int64_t)p.n_seqs * groups, bytes);
+    const int64_t units = (int64_t)p.n_seqs * groups;
+    double t_cluster;
+    p.cluster = mla_pick_cluster<MP>(units, bytes, t_cluster);
+    const int nc = cluster_fit(reinterpret_cast<const void*>(mla_attend_kernel<MP>), kMlThreads, bytes, 1);
+    if (ws && nc >= 1 && (size_t)(nc + units - 1) * attend_slot_bytes(kMlC) <= ws_bytes &&
+        (double)units / nc < 0.97 * t_cluster) {
+        L.ws = static_cast<float*>(ws);
+        p.cluster = 1;
+        mla_attend_kernel<MP><<<(unsigned)nc, kMlThreads, bytes, stream>>>(L);
+        if ((e = cudaGetLastError()) != cudaSuccess)
+            return e;
+        return launch_attend_merge(L.ws, units, nc, kMlC, groups, p.Hq, kMlH, p.out, stream);
+    }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3((unsigned)(p.n_seqs * p.cluster), (unsigned)groups);
     cfg.blockDim = dim3(kMlThreads);
@@ -637,11 +692,12 @@ static cudaError_t launch_mla_attend_m(const MlaAttendParams& p0, cudaStream_t s
     return cudaLaunchKernelEx(&cfg, mla_attend_kernel<MP>, L);
 }
 
-cudaError_t launch_mla_attend(const MlaAttendParams& p, cudaStream_t stream)
+cudaError_t launch_mla_attend(const MlaAttendParams& p, void* ws, size_t ws_bytes, cudaStream_t stream)
 {
     if (p.max_rank == 0)
-        return launch_mla_attend_m<0>(p, stream);
-    return p.max_rank <= 16 ? launch_mla_attend_m<16>(p, stream) : launch_mla_attend_m<32>(p, stream);
+        return launch_mla_attend_m<0>(p, ws, ws_bytes, stream);
+    return p.max_rank <= 16 ? launch_mla_attend_m<16>(p, ws, ws_bytes, stream)
+                            : launch_mla_attend_m<32>(p, ws, ws_bytes, stream);
 }
 
 }  // namespace kamera

@@ -4,6 +4,7 @@
 
 #include <cstddef>
 #include <cstdint>
+#include <cuda_bf16.h>
 #include <cuda_runtime.h>
 
 #include "kamera.h"
@@ -49,11 +50,18 @@ cudaError_t launch_patch_form(const PatchFormParams& p, int64_t n_blocks, cudaSt
 int cluster_fit(const void* kernel, int block_threads, int smem_bytes, int cl);
 
 // Decode attention over reused chunks: shapes handled; one CTA per (sequence, KV head).
+// With a workspace (ws non-NULL, ws_bytes of it) a call may take the split
+// path: partial softmax states per (CTA, unit) in the workspace, then a merge
+// launch; the workspace needs (CTAs resident at once + units - 1) slots of
+// attend_slot_bytes(output width) bytes.
 bool attend_supported(int head_dim, int G, int max_rank);
 int attend_cluster(int64_t units);
-cudaError_t launch_attend(const AttendParams& p, cudaStream_t stream);
+cudaError_t launch_attend(const AttendParams& p, void* ws, size_t ws_bytes, cudaStream_t stream);
 bool mla_attend_supported(int kv_lora, int rope_dim, int num_q_heads, int max_rank);
-cudaError_t launch_mla_attend(const MlaAttendParams& p, cudaStream_t stream);   // picks p.cluster
+cudaError_t launch_mla_attend(const MlaAttendParams& p, void* ws, size_t ws_bytes, cudaStream_t stream);
+size_t attend_slot_bytes(int dout);
+cudaError_t launch_attend_merge(const float* ws, int64_t units, int64_t ctas, int dout, int groups, int Hq,
+                                int rows, __nv_bfloat16* out, cudaStream_t stream);
 
 // 2-D tensor map (a CUtensorMap, 64-byte aligned, at `map`) over a bf16 array
 // of `rows` rows of `width` elements, row_stride elements apart: boxes of

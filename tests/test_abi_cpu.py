@@ -19,7 +19,7 @@ HEADER = os.path.join(B.INCLUDE, "kamera.h")
 
 def declared_functions():
     src = open(HEADER).read()
-    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(kamera_\w+)\s*\(", src, re.M)))
+    return sorted(set(re.findall(r"^(?:int|size_t|const char\*)\s+(kamera_\w+)\s*\(", src, re.M)))
 
 
 def test_header_declares_the_entry_points():
@@ -263,11 +263,11 @@ def test_attend_store_row_bound():
     q = K._AttnQuery(fake, fake + (1 << 16), 1, 4, 0.125, 0)
     r, keep = K.Rope(1e4, 64)._c(1)
     rc = lib.kamera_attend_reused(C.byref(kv), C.byref(q), C.byref(r), C.c_void_p(fake), C.c_void_p(fake), 1, 8, 0,
-                                  None, None)
+                                  None, 0, None, None)
     assert rc == 3
     kv.num_rows = -1
     assert lib.kamera_attend_reused(C.byref(kv), C.byref(q), C.byref(r), C.c_void_p(fake), C.c_void_p(fake), 1, 8,
-                                    0, None, None) == 1
+                                    0, None, 0, None, None) == 1
     del keep
 
 

@@ -8,6 +8,8 @@ output once to bf16, so every element must lie within one bf16 ulp of the fp64
 result, plus 2^-16 of sum_j p_j |V_j| (the magnitude the sums are made of:
 where the output is a small difference of large terms, rounding of the terms
 is what moves it)."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -17,6 +19,16 @@ import position_invariant_kv_chunk_gb300 as K
 import workloads as W
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, params=["workspace", "clusters"])
+def attend_path(request, monkeypatch):
+    """Every case twice: with the binding's workspace (the call spreads the
+    units' tiles over all SMs and merges the partial states in a second
+    launch) and without one (the units' tiles split within clusters)."""
+    if request.param == "clusters":
+        monkeypatch.setattr(K, "kamera_attend_reused", functools.partial(K.kamera_attend_reused, workspace=False))
+    return request.param
 
 DEV = "cuda"
 
@@ -168,3 +180,34 @@ def test_host_errors():
     with pytest.raises(K.KameraError) as e:        # more than 8 query heads per KV head
         run_attend(a)
     assert e.value.status == 3
+
+
+def test_one_unit_over_every_sm():
+    """One sequence of one KV head: with a workspace its 11 tiles spread over
+    every CTA that fits, so most CTAs hold an empty share and leave an empty
+    partial state, which the merge must skip."""
+    a = W.make_attend(W.AttendSpec("at_one", H=1, G=2, d=128, seqs=((1000, 300),), m=16), DEV)
+    check(a, run_attend(a), "one unit")
+
+
+def test_workspace_errors():
+    """A workspace that is too small or misaligned is refused before any launch."""
+    a = W.make_attend(W.AttendSpec("at_ws", H=2, G=2, d=64, seqs=((40,), (30,)), m=8), DEV)
+    chunks = K.pack_chunks(a.chunks, device=DEV)
+    seq = torch.tensor(a.seq_start, dtype=torch.int32, device=DEV)
+    rope = K.Rope(a.spec.base, a.rot_dim, a.spec.rot_offset, a.spec.pairing)
+    need = K.load_library().kamera_attend_workspace_bytes(2, 2, 64)
+    assert need > 0
+    small = torch.empty(need - 16, dtype=torch.uint8, device=DEV)
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_attend_reused(a.store_k, a.store_v, a.q, rope, chunks, seq, 2, 40, 8, workspace=small)
+    assert e.value.status == 1
+    odd = torch.empty(need + 16, dtype=torch.uint8, device=DEV)[8:]
+    with pytest.raises(K.KameraError) as e:
+        K.kamera_attend_reused(a.store_k, a.store_v, a.q, rope, chunks, seq, 2, 40, 8, workspace=odd)
+    assert e.value.status == 2
+    exact = torch.empty(need, dtype=torch.uint8, device=DEV)
+    out = K.kamera_attend_reused(a.store_k, a.store_v, a.q, rope, chunks, seq, 2, 40, 8, layer=a.spec.layer,
+                                 workspace=exact)
+    torch.cuda.synchronize()
+    check(a, out, "caller's workspace")

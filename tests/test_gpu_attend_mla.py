@@ -8,6 +8,8 @@ query, the per-chunk folds, the softmax weights) enter as a bf16 hi + lo pair
 element must lie within one bf16 ulp of the fp64 result, plus 2^-16 of
 sum_j p_j |c'_j| (the scale of the terms the weighted sum is made of), as for
 GQA attention."""
+import functools
+
 import numpy as np
 import pytest
 import torch
@@ -17,6 +19,16 @@ import position_invariant_kv_chunk_gb300 as K
 import workloads as W
 
 pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(autouse=True, params=["workspace", "clusters"])
+def attend_path(request, monkeypatch):
+    """Every case twice: with the binding's workspace (the call spreads the
+    units' tiles over all SMs and merges the partial states in a second
+    launch) and without one (the units' tiles split within clusters)."""
+    if request.param == "clusters":
+        monkeypatch.setattr(K, "kamera_mla_attend_reused", functools.partial(K.kamera_mla_attend_reused, workspace=False))
+    return request.param
 
 DEV = "cuda"
 
