@@ -553,6 +553,33 @@ int kamera_mla_attend_reused(const KameraAttnMlaKV* kv, const KameraAttnQuery* q
  * cannot be queried. */
 size_t kamera_mla_attend_workspace_bytes(int32_t n_seqs, int32_t num_q_heads);
 
+/*
+ * kamera_attend_reused for callers that cannot allocate device memory.  The
+ * pages have no counterpart: this is an interface of this library only.
+ * A plug-in whose host process gives all device memory to its own caching
+ * allocator (with no hook to borrow from it), or a serving loop that must not
+ * call cudaMalloc once it runs (the call can synchronise the device), has no
+ * workspace to pass.  This entry point takes the same arguments as
+ * kamera_attend_reused without d_workspace / workspace_bytes, and uses as the
+ * workspace a fixed 4 MiB scratch array that the library keeps in device
+ * memory on every GPU that loads it, for the life of the process; it calls no
+ * allocating routine.  The caller still provides every input and the output.
+ *   - Limit: the batch must fit the scratch, kamera_attend_workspace_bytes(
+ *     n_seqs, num_kv_heads, head_dim) <= 4 MiB (for head_dim 128 on a 148-SM
+ *     GB300: n_seqs * num_kv_heads <= 357); a larger batch returns
+ *     KAMERA_ERR_UNSUPPORTED and nothing is launched.
+ *   - The first call on a device looks up the scratch's device address
+ *     (cudaGetSymbolAddress); make that first call before any stream capture.
+ *   - Every call on a device shares the one scratch and leaves its partial
+ *     states in it; nothing in it has to start at zero (each call writes every
+ *     slot it reads), but calls that can overlap on the GPU (on different
+ *     streams without an ordering between them) race on it.
+ * Other arguments, results and errors: as for kamera_attend_reused.
+ */
+int kamera_attend_reused_static(const KameraAttnKV* kv, const KameraAttnQuery* query, const KameraRope* rope,
+                                const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
+                                int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream);
+
 /* KAMERA_ABI_VERSION of the loaded library. */
 int kamera_abi_version(void);
 

@@ -158,6 +158,9 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C
     lib.kamera_mla_attend_reused.argtypes = [P(_AttnMlaKV), P(_AttnQuery), P(_Rope), C.c_void_p, C.c_void_p,
                                              C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_size_t, C.c_void_p,
                                              C.c_void_p]
+    lib.kamera_attend_reused_static.restype = C.c_int
+    lib.kamera_attend_reused_static.argtypes = [P(_AttnKV), P(_AttnQuery), P(_Rope), C.c_void_p, C.c_void_p,
+                                                C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
     lib.kamera_attend_workspace_bytes.restype = C.c_size_t
     lib.kamera_attend_workspace_bytes.argtypes = [C.c_int32, C.c_int32, C.c_int32]
     lib.kamera_mla_attend_workspace_bytes.restype = C.c_size_t
@@ -599,6 +602,41 @@ def kamera_attend_reused(store_k: torch.Tensor, store_v: torch.Tensor, q: torch.
                                   _stream_handle(stream))
     del keep
     _check(rc, "kamera_attend_reused")
+    return out
+
+
+def kamera_attend_reused_static(store_k: torch.Tensor, store_v: torch.Tensor, q: torch.Tensor, rope: Rope,
+                                chunks: torch.Tensor, seq_start: torch.Tensor, n_chunks: int, max_len: int,
+                                max_rank: int, out: torch.Tensor, layer: int = 0, scale: Optional[float] = None,
+                                err: Optional[torch.Tensor] = None, stream=None) -> torch.Tensor:
+    """``kamera_attend_reused`` for callers that cannot allocate device memory
+    (see ``kamera_attend_reused_static`` in kamera.h): the library's fixed
+    scratch serves as the workspace, and this binding allocates nothing either,
+    so the caller passes ``out`` (bf16, shaped like ``q``).  Returns ``out``."""
+    _on_device("kamera_attend_reused_static", store_k=store_k, store_v=store_v, q=q, chunks=chunks,
+               seq_start=seq_start, out=out, err=err)
+    for t, nm in ((store_k, "store_k"), (store_v, "store_v"), (q, "q"), (out, "out")):
+        _bf16(t, nm)
+    if store_k.dim() != 3 or store_k.stride(2) != 1 or store_k.stride(1) != store_k.shape[2]:
+        raise ValueError("store_k must be [N, H_kv, d] with packed heads")
+    if store_v.shape != store_k.shape or store_v.stride() != store_k.stride():
+        raise ValueError("store_k and store_v must share shape and strides")
+    N, H, d = store_k.shape
+    if q.dim() != 3 or q.shape[2] != d or not q.is_contiguous():
+        raise ValueError("q must be a contiguous [S, H_q, d] tensor")
+    S, Hq, _ = q.shape
+    if out.shape != q.shape or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if seq_start.dtype != torch.int32 or seq_start.numel() != S + 1:
+        raise ValueError("seq_start must hold S + 1 int32 values")
+    kv = _AttnKV(_addr(store_k), _addr(store_v), N, store_k.stride(0), H, d, int(layer), 0)
+    qq = _AttnQuery(_addr(q), _addr(out), S, Hq, float(d ** -0.5 if scale is None else scale), 0)
+    r, keep = rope._c(n_chunks)
+    rc = load_library().kamera_attend_reused_static(C.byref(kv), C.byref(qq), C.byref(r), _addr(chunks),
+                                                    _addr(seq_start), int(n_chunks), int(max_len), int(max_rank),
+                                                    _addr(err), _stream_handle(stream))
+    del keep
+    _check(rc, "kamera_attend_reused_static")
     return out
 
 
