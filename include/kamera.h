@@ -108,12 +108,13 @@ enum {
     KAMERA_DEVERR_TIMEOUT = 32     /* an internal pipeline wait gave up: results incomplete
                                       (every wait of the tensor-core kernels is bounded by
                                       1 s; the environment variable KAMERA_WAIT_LIMIT_NS,
-                                      read at each call, overrides the bound -- a test hook:
-                                      with a bound of 0 the kernels give up at their first
-                                      pipeline wait that is not met at once (patch formation:
-                                      at its first wait), so they give up early,
-                                      drain their own copies and MMAs, free their tensor
-                                      memory and return with this bit set) */
+                                      read at each call, overrides the bound.  Test hooks:
+                                      KAMERA_TEST_WITHHOLD_LOADS=1 makes the relocation
+                                      kernel's producer issue no loads, and for patch
+                                      formation a bound of 0 gives up at its first wait;
+                                      the kernels then give up early, drain their own
+                                      copies and MMAs, free their tensor memory and
+                                      return with this bit set) */
 };
 
 /* RoPE pairings. */

@@ -31,6 +31,12 @@ uint64_t wait_limit_ns()
     return (end && *end == '\0') ? (uint64_t)n : 1000000000ull;
 }
 
+bool test_withhold_loads()
+{
+    const char* v = std::getenv("KAMERA_TEST_WITHHOLD_LOADS");
+    return v && v[0] == '1' && v[1] == '\0';
+}
+
 int cluster_fit(const void* kernel, int block_threads, int smem_bytes, int cl)
 {
     struct Entry {

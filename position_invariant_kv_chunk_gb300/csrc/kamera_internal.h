@@ -21,6 +21,11 @@ struct RowsParams;
 // KAMERA_DEVERR_TIMEOUT).  Read on the host at each launch.
 uint64_t wait_limit_ns();
 
+// Test hook: KAMERA_TEST_WITHHOLD_LOADS=1 in the environment makes the
+// relocation kernel's producer issue no loads, so its first pipeline waits
+// run out after the bound above (read on the host at each launch).
+bool test_withhold_loads();
+
 // CUDA-core streaming path (any rank within the shared-memory budget).
 cudaError_t launch_simt(const RowsParams& p, int family, cudaStream_t stream);
 size_t simt_smem_bytes(const RowsParams& p, int family, int tile_tokens);

@@ -10,15 +10,18 @@
 //
 //   warp 0    producer: canonical rows of the tile with tiled TMA loads from a
 //             tensor map of the store (128B-swizzled boxes of 64 columns x 128
-//             rows; 16-row boxes for the ragged tail) and the per-chunk
-//             cos/sin table (phase formed and reduced in fp64).
-//   warp 1    operands + MMA: 16-byte async copies build the U tile and V_m in
-//             the 128B-swizzled K-major layout ahead of use; the copying lanes
-//             fence their writes into the async proxy; one lane issues the
-//             MMAs and commits them to mbarriers.  Also owns TMEM.
-//   warps 2-9 epilogue: two warps per TMEM sub-partition, each owning half of
-//             the columns (whole RoPE pairs) of the same 32 token rows; thread
-//             = token row = TMEM lane.  tcgen05.ld the patch, read the canonical
+//             rows; 16-row boxes for the ragged tail), the U tiles of chunks
+//             the host mapped (TMA boxes swizzled like the MMA operand), the
+//             tile's pool slots, and the per-chunk cos/sin table (phase formed
+//             and reduced in fp64).
+//   warp 1    operands + MMA: 16-byte async copies build the U tiles the maps
+//             do not cover and V_m in the 128B-swizzled K-major layout ahead of
+//             use; the copying lanes fence their writes into the async proxy;
+//             one lane issues the MMAs and commits them to mbarriers.  Also
+//             owns TMEM.
+//   warps 4-15 epilogue: three warps per TMEM sub-partition, each owning a
+//             third of the columns (whole RoPE pairs) of the same 32 token
+//             rows; thread = token row = TMEM lane.  tcgen05.ld the patch, read the canonical
 //             row (swizzled, conflict-free), rotate the RoPE pairs in fp32, add,
 //             round once to bf16 and write back in place; then each warp stores
 //             its columns of its 32 rows to their pool slots with coalesced
@@ -79,6 +82,7 @@ struct UmmaParams {
     RowsParams r;
     int32_t family;
     int32_t Z;                 // row segments
+    int32_t withhold;          // test hook: the producer issues no loads, so the first waits run out
     uint64_t wait_ns;          // bound of every pipeline wait (drains keep kTimeoutNs)
 };
 
@@ -86,57 +90,45 @@ struct UmmaParams {
 // with u_rank[c] > 0 has maps 2c (K or c_KV factor) and 2c+1 (V or k_rope
 // factor) over its [L*FH][len][m] U array; boxes of min(m, 64) ranks x 128
 // rows, swizzled to match the MMA operand layout.  Beside each map sit the
-// host copy's rank, length and the two U base addresses the maps were encoded
-// from: a tile moves through a map only when the device descriptor names the
-// same four values, so a host copy that disagrees with the device array can
-// never point a load at memory the descriptor does not name.
+// host copy's rank, length and the two U base addresses it was encoded from:
+// a chunk's tiles move through its maps only when the device descriptor names
+// the same four values, so a host copy that disagrees with the device array
+// can never point a load at memory the descriptor does not name.
 template <int MC>
 struct UmmaLaunch {
     UmmaParams core;
     CUtensorMap map_u[2 * MC];
-    const void* u_base[MC][2];
     int32_t u_rank[MC];
     int32_t u_len[MC];
+    const void* u_base[MC][2];
 };
 
-// Whether chunk c's U tiles move by its tensor maps.
-static_assert(sizeof(UmmaLaunch<kMapChunksMany>) <= 32764, "kernel parameter block too large");
-
 template <int MC>
-__device__ __forceinline__ bool u_mapped(const UmmaLaunch<MC>& P, int c, const KameraChunk& ch)
+__device__ __forceinline__ bool u_map_matches(const UmmaLaunch<MC>& P, int c, const KameraChunk& ch)
 {
-    return ch.rank > 0 && c < MC && P.u_rank[c] == ch.rank && P.u_len[c] == ch.len &&
-           P.u_base[c][0] == ch.patch_ptrs[0] && P.u_base[c][1] == ch.patch_ptrs[2];
+    return ch.rank > 0 && P.u_rank[c] == ch.rank && P.u_len[c] == ch.len && P.u_base[c][0] == ch.patch_ptrs[0] &&
+           P.u_base[c][1] == ch.patch_ptrs[2];
 }
 
-// A chunk the host mapped whose device descriptor names other U factors (a
-// host copy that does not match the device array): its tiles take the copy
-// path and the call reports KAMERA_DEVERR_DESCRIPTOR.
+// Whether chunk c's U tiles move by its tensor map: bit c of the mask the
+// prologue builds from u_map_matches (one check per chunk and CTA).
 template <int MC>
-__device__ __forceinline__ bool u_map_stale(const UmmaLaunch<MC>& P, int c, const KameraChunk& ch)
+__device__ __forceinline__ bool u_mapped(const uint32_t* umask, int c, int rank)
 {
-    return c < MC && P.u_rank[c] > 0 && !u_mapped(P, c, ch);
+    return rank > 0 && c < MC && ((umask[c >> 5] >> (c & 31)) & 1u);
 }
 
-// Operand buffering by the call's largest rank.  KA = 0 (ranks <= 16): U and
-// V_m are K-major with 32-byte rows (one 16-rank step, 32-byte swizzle), 4 KB
-// each, so the copies of every operand can start five tiles ahead (a call
-// whose jobs are one tile long -- short chunks -- needs a new V_m every tile).
-// KA = 1 (ranks <= 64) and 2 (<= 128): 64-rank atoms of 128-byte rows.
 template <int KA>
 struct Geometry {
-    static constexpr int LA = KA == 0 ? 5 : KA == 1 ? 2 : 1;   // operand lookahead (tiles)
-    static constexpr int D = LA + 1;                            // U operand buffers
-    static constexpr int NV = KA == 0 ? D : 2;                  // V_m buffers (one job each)
-    static constexpr int S = KA == 2 ? 2 : 4;                   // row stages
-    static constexpr bool kSw32 = KA == 0;                      // 32-byte operand rows
-    static constexpr int kUBytes = KA == 0 ? kTileM * 32 : KA * kAtomBytes;
-    static constexpr int kVBytes = KA == 0 ? kWMax * 32 : KA * kWMax * 128;
+    static constexpr int LA = KA == 1 ? 2 : 1;  // operand lookahead (tiles)
+    static constexpr int D = LA + 1;            // U operand buffers
+    static constexpr int S = KA == 1 ? 4 : 2;   // row stages
+    static constexpr int kUBytes = KA * kAtomBytes;
+    static constexpr int kVBytes = KA * kWMax * 128;
     static constexpr int kUOff = S * kStageBytes;
     static constexpr int kVOff = kUOff + D * kUBytes;
-    static constexpr int kSharedOff = kVOff + NV * kVBytes;
+    static constexpr int kSharedOff = kVOff + 2 * kVBytes;
 };
-constexpr int kMaxD = 6, kMaxNV = 6;   // barrier arrays sized for the deepest geometry
 
 struct Seg {
     int array, e0, w, rot, u_idx, v_idx, fh, FH, vm_row0, vm_rows;
@@ -224,33 +216,29 @@ struct TileInfo {
 };
 
 struct Shared {
-    uint64_t full[4], empty[4], tfull[2], tempty[2], uempty[kMaxD], ufull[kMaxD], vmempty[kMaxNV], mmadone;
+    uint64_t full[4], empty[4], tfull[2], tempty[2], uempty[3], ufull[3], vmempty[2], mmadone;
     uint32_t tmem_base;
     int32_t abort_flag;
     int32_t start_lz, start_rem, start_c, start_t, count;
     int32_t stage_tag[4];
     TileInfo tinfo[4];
+    uint32_t umask[(kMapChunksMany + 31) / 32];
     int64_t part[kThreads];
 };
 
 __device__ __forceinline__ bool wait_bar(uint32_t bar, uint32_t parity, volatile int32_t* abort_flag, int32_t* err,
                                          uint64_t limit)
 {
-    // A short bound (the test hook) polls without suspending and checks the
-    // clock at every poll, so a wait that is not met at once does run out.
-    const bool quick = limit < 100000u;
-    auto poll = [&]() { return quick ? ptx::mbar_test_wait(bar, parity) : ptx::mbar_try_wait(bar, parity); };
-    if (poll())
+    if (ptx::mbar_try_wait(bar, parity))
         return true;
     const uint64_t t0 = ptx::globaltimer();
-    const uint32_t every = quick ? 0u : 63u;
     for (uint32_t it = 1;; ++it) {
-        if (poll())
+        if (ptx::mbar_try_wait(bar, parity))
             return true;
-        if ((it & every) == 0) {
+        if ((it & 63) == 0) {
             if (*abort_flag)
                 return false;
-            if (limit == 0 || ptx::globaltimer() - t0 > limit) {
+            if (ptx::globaltimer() - t0 > limit) {
                 *abort_flag = 1;
                 raise_err(err, KAMERA_DEVERR_TIMEOUT);
                 return false;
@@ -277,14 +265,9 @@ __device__ __forceinline__ void drain_bar(uint32_t bar, uint32_t parity)
 }
 
 // Byte offset of the 16-byte piece (row r, piece kc) in a 128B-swizzled
-// K-major operand with atoms of `atom_bytes` (64 ranks per atom); with
-// atom_bytes == 0, in a 32B-swizzled operand of 32-byte rows (16 ranks; the
-// swizzle XORs address bit 4 with bit 7: the two pieces of rows 4..7 of every
-// 8-row group trade places).
+// K-major operand with atoms of `atom_bytes` (64 ranks per atom).
 __device__ __forceinline__ uint32_t operand_offset(int r, int kc, uint32_t atom_bytes)
 {
-    if (atom_bytes == 0)
-        return r * 32 + ((kc ^ ((r >> 2) & 1)) << 4);
     return (kc >> 3) * atom_bytes + r * 128 + ((((kc & 7) ^ (r & 7))) << 4);
 }
 
@@ -507,9 +490,8 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(ptx::smem_addr(&sh.tfull[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&sh.tempty[i]), kEpiWarps);
-        }
-        for (int i = 0; i < G::NV; ++i)
             ptx::mbar_init(ptx::smem_addr(&sh.vmempty[i]), 1);
+        }
         for (int i = 0; i < G::D; ++i) {
             ptx::mbar_init(ptx::smem_addr(&sh.uempty[i]), 1);
             ptx::mbar_init(ptx::smem_addr(&sh.ufull[i]), 1);
@@ -524,6 +506,22 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             ptx::prefetch_tmap(&p.map_full[i]);
             ptx::prefetch_tmap(&p.map_tail[i]);
         }
+    }
+    // chunks whose U tiles may move by their tensor maps: the host copy the maps
+    // were encoded from must name the device descriptor's rank, length and U
+    // factors; a mapped chunk that differs takes the copy path and reports
+    // KAMERA_DEVERR_DESCRIPTOR
+    if (tid < 32 * ((MC + 31) / 32)) {
+        bool ok = false;
+        if (tid < MC && tid < r.n_chunks && P.u_rank[tid] > 0) {
+            const KameraChunk ch = r.chunks[tid];
+            ok = u_map_matches(P, tid, ch);
+            if (!ok && blockIdx.x == 0)
+                raise_err(r.err, KAMERA_DEVERR_DESCRIPTOR);
+        }
+        const uint32_t bits = __ballot_sync(0xffffffffu, ok);
+        if (lane == 0)
+            sh.umask[warp] = bits;
     }
     // tiles per chunk: each thread sums a contiguous block of chunks
     const int n = r.n_chunks;
@@ -541,38 +539,16 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             mine += (ch.len + kTileM - 1) / kTileM;
         }
     }
-    // exclusive prefix of the per-thread tile counts: within each warp by
-    // shuffles, then over the warp totals in warp 0
-    int64_t incl = mine;
-#pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-        const int64_t y = __shfl_up_sync(0xffffffffu, incl, o);
-        if (lane >= o)
-            incl += y;
-    }
-    if (lane == 31)
-        sh.part[warp] = incl;
+    sh.part[tid] = mine;
     __syncthreads();
-    if (warp == 0) {
-        constexpr int NW = kThreads / 32;
-        const int64_t w = lane < NW ? sh.part[lane] : 0;
-        int64_t wi = w;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-            const int64_t y = __shfl_up_sync(0xffffffffu, wi, o);
-            if (lane >= o)
-                wi += y;
-        }
-        __syncwarp();
-        if (lane < NW)
-            sh.part[NW + lane] = wi - w;   // exclusive prefix of warp `lane`
-        if (lane == NW - 1)
-            sh.part[2 * NW] = wi;          // all tiles of one layer and segment
-    }
-    __syncthreads();
-    const int64_t my_prefix = sh.part[kThreads / 32 + warp] + incl - mine;
     if (tid == 0) {
-        const int64_t TC = sh.part[2 * (kThreads / 32)];
+        int64_t run = 0;
+        for (int i = 0; i < kThreads; ++i) {
+            const int64_t v = sh.part[i];
+            sh.part[i] = run;
+            run += v;
+        }
+        const int64_t TC = run;
         const int64_t T = TC * r.L * p.Z;
         const int64_t b0 = T * blockIdx.x / gridDim.x, b1 = T * (blockIdx.x + 1) / gridDim.x;
         sh.count = (int32_t)(b1 - b0);
@@ -585,7 +561,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
     __syncthreads();
     if (sh.count > 0) {
         const int64_t rem = sh.start_rem;
-        const int64_t lo = (int64_t)p.Z * my_prefix;   // a chunk holds Z * (its tiles) of a layer
+        const int64_t lo = (int64_t)p.Z * sh.part[tid];   // a chunk holds Z * (its tiles) of a layer
         if (rem >= lo && rem < lo + (int64_t)p.Z * mine) {   // exactly one thread owns the starting tile
             int64_t acc = lo;
             for (int c = c_lo; c < c_hi; ++c) {
@@ -623,7 +599,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
 
     if (warp < kEpiWarp0) {
     ptx::setmaxnreg_dec<kRegsLow>();
-    if (warp == 0 && count > 0) {
+    if (warp == 0 && count > 0 && !p.withhold) {
         // ------------------------------------------------------ producer
         int issued = 0, pu = 0;
         uint32_t upar = 0, uload = 0;   // per U buffer: phase parity of its TMA loads; last use was a TMA load
@@ -658,11 +634,9 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                 if (lane == 0)
                     sh.stage_tag[s] = cur.c;
             }
-            if (cur.t == 0 && lane == 0 && u_map_stale(P, cur.c, ch))
-                raise_err(r.err, KAMERA_DEVERR_DESCRIPTOR);
             if (ch.rank > 0) {   // U tile of a mapped chunk: one or two swizzled boxes into the U ring
                 const int u = pu % G::D;
-                if (u_mapped(P, cur.c, ch)) {
+                if (u_mapped<MC>(sh.umask, cur.c, ch.rank)) {
                     if (!warp_wait(ptx::smem_addr(&sh.uempty[u]), ((pu / G::D) & 1) ^ 1, abort_flag, r.err, p.wait_ns))
                         break;
                     if (lane == 0) {
@@ -746,17 +720,17 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                     const int64_t lh = (int64_t)l * sg.FH + sg.fh;
                     if (new_job) {
                         ++ld_v;
-                        if (!warp_wait(ptx::smem_addr(&sh.vmempty[ld_v % G::NV]), ((ld_v / G::NV) & 1) ^ 1,
-                                       abort_flag, r.err, p.wait_ns))
+                        if (!warp_wait(ptx::smem_addr(&sh.vmempty[ld_v & 1]), ((ld_v >> 1) & 1) ^ 1, abort_flag,
+                                       r.err, p.wait_ns))
                             stop = true;
                         else
-                            load_operand(vbase + (ld_v % G::NV) * G::kVBytes,
+                            load_operand(vbase + (ld_v & 1) * G::kVBytes,
                                          patch_ptr(ch, sg.v_idx) +
                                              (lh * sg.vm_rows + sg.vm_row0) * m,
-                                         sg.w, m, mpad, G::kSw32 ? 0u : (uint32_t)sg.w * 128u, lane);
+                                         sg.w, m, mpad, (uint32_t)sg.w * 128u, lane);
                     }
                     const int u = ld_u % G::D;
-                    const bool by_tma = u_mapped(P, ld.c, ch);   // the producer loads this U tile
+                    const bool by_tma = u_mapped<MC>(sh.umask, ld.c, m);   // the producer loads this U tile
                     if (!by_tma && !stop &&
                         !warp_wait(ptx::smem_addr(&sh.uempty[u]), ((ld_u / G::D) & 1) ^ 1, abort_flag, r.err, p.wait_ns))
                         stop = true;
@@ -765,7 +739,7 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                         load_operand(ubase + u * G::kUBytes,
                                      patch_ptr(ch, sg.u_idx) +
                                          (lh * ch.len + tok0) * m,
-                                     min(kTileM, ch.len - tok0), m, mpad, G::kSw32 ? 0u : (uint32_t)kAtomBytes, lane);
+                                     min(kTileM, ch.len - tok0), m, mpad, kAtomBytes, lane);
                     }
                     ++ld_u;
                 }
@@ -789,12 +763,12 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
             plz = cur.lz;
             pc = cur.c;
             const int lz_now = cur.lz, c_now = cur.c;
-            const bool by_tma = u_mapped(P, c_now, cur.ch);
             cur.next(p);
             const bool last_of_job = (i == count - 1) || cur.lz != lz_now || cur.c != c_now;
             if (m > 0) {
                 if (new_job)
                     ++vjob;
+                const bool by_tma = u_mapped<MC>(sh.umask, c_now, m);
                 if (lane == 0) {
                     const int acc = k & 1, u = k % G::D;
                     bool ok = true;
@@ -807,25 +781,23 @@ __global__ void __maxnreg__(kRegCap) relocate_patch_umma_kernel(const __grid_con
                     } else {
                         ptx::tc_fence_after();
                         const uint32_t a0 = ubase + u * G::kUBytes;
-                        const uint32_t b0 = vbase + (vjob % G::NV) * G::kVBytes;
+                        const uint32_t b0 = vbase + (vjob & 1) * G::kVBytes;
                         const uint32_t idesc = ptx::idesc_bf16_f32(kTileM, sg.w);
                         const uint32_t d = tmem + acc * kWMax;
                         const int steps = (m + 15) >> 4;
                         for (int q = 0; q < steps; ++q) {
                             const uint32_t koff = (q & 3) * 32;
-                            // A as the TMA load laid it out (rows of 2m bytes, m < 64), as the
-                            // copies laid it out (32-byte rows for ranks <= 16), or in 64-rank atoms
-                            const uint64_t ad = G::kSw32 || (by_tma && m == 16) ? ptx::desc_k_sw32(a0)
+                            // A as the TMA load laid it out (rows of 2m bytes, m < 64) or in 64-rank atoms
+                            const uint64_t ad = by_tma && m == 16   ? ptx::desc_k_sw32(a0)
                                                 : by_tma && m == 32 ? ptx::desc_k_sw64(a0 + koff)
                                                                     : ptx::desc_k_sw128(a0 + (q >> 2) * kAtomBytes + koff);
-                            const uint64_t bd = G::kSw32 ? ptx::desc_k_sw32(b0)
-                                                         : ptx::desc_k_sw128(b0 + (q >> 2) * (uint32_t)sg.w * 128u + koff);
+                            const uint64_t bd = ptx::desc_k_sw128(b0 + (q >> 2) * (uint32_t)sg.w * 128u + koff);
                             ptx::umma_bf16(d, ad, bd, idesc, q > 0 ? 1u : 0u);
                         }
                         ptx::umma_commit(ptx::smem_addr(&sh.tfull[acc]));
                         ptx::umma_commit(ptx::smem_addr(&sh.uempty[k % G::D]));
                         if (last_of_job)
-                            ptx::umma_commit(ptx::smem_addr(&sh.vmempty[vjob % G::NV]));
+                            ptx::umma_commit(ptx::smem_addr(&sh.vmempty[vjob & 1]));
                         ++issued_mma;
                     }
                 }
@@ -962,7 +934,7 @@ static size_t smem_bytes_for()
 
 size_t umma_smem_bytes(const RowsParams& p)
 {
-    return p.max_rank > 64 ? smem_bytes_for<2>() : p.max_rank > 16 ? smem_bytes_for<1>() : smem_bytes_for<0>();
+    return p.max_rank > 64 ? smem_bytes_for<2>() : smem_bytes_for<1>();
 }
 
 namespace {
@@ -1078,6 +1050,7 @@ cudaError_t launch_umma(const RowsParams& rp, int family, const KameraChunk* h_c
     p.family = family;
     p.Z = family == FAMILY_GQA ? 2 * rp.H : rp.kv_lora / kWMax + 1;
     p.wait_ns = wait_limit_ns();
+    p.withhold = test_withhold_loads() ? 1 : 0;
     const int64_t width = family == FAMILY_GQA ? (int64_t)rp.H * rp.d : rp.d;
     const void* arrays[2] = {rp.src_k, family == FAMILY_GQA ? rp.src_v : rp.src_k};
     for (int a = 0; a < 2; ++a) {
@@ -1096,11 +1069,8 @@ cudaError_t launch_umma(const RowsParams& rp, int family, const KameraChunk* h_c
     if (rp.max_rank > 64)
         return few ? launch_kernel<2, kMapChunksFew>(p, h_chunks, sms, stream)
                    : launch_kernel<2, kMapChunksMany>(p, h_chunks, sms, stream);
-    if (rp.max_rank > 16)
-        return few ? launch_kernel<1, kMapChunksFew>(p, h_chunks, sms, stream)
-                   : launch_kernel<1, kMapChunksMany>(p, h_chunks, sms, stream);
-    return few ? launch_kernel<0, kMapChunksFew>(p, h_chunks, sms, stream)
-               : launch_kernel<0, kMapChunksMany>(p, h_chunks, sms, stream);
+    return few ? launch_kernel<1, kMapChunksFew>(p, h_chunks, sms, stream)
+               : launch_kernel<1, kMapChunksMany>(p, h_chunks, sms, stream);
 }
 
 }  // namespace kamera

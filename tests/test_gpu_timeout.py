@@ -2,13 +2,16 @@
 
 Every pipeline wait of relocate_patch_umma_kernel and patch_form_kernel gives
 up after a bound (1 s; the environment variable KAMERA_WAIT_LIMIT_NS, read at
-each call, overrides it).  With a bound of 0 the first poll that finds a wait
-unmet gives up (polls then never suspend, and no clock tick is needed): the call must still return, report KAMERA_DEVERR_TIMEOUT, and
-leave the device usable -- each CTA drained its own tensor-map loads, copies
-and MMAs and released its tensor memory -- which a normal call right after,
-on the same stream, shows by matching the oracle (a CTA that kept its tensor
-memory would leave the next launch's allocation waiting).  Nothing here
-faults: every address stays valid and every wait is bounded."""
+each call, overrides it).  Relocation: KAMERA_TEST_WITHHOLD_LOADS=1 makes the
+producer issue no loads, so the other roles' first waits cannot be met and
+run out after the bound (here 1 ms).  Patch formation: with a bound of 0 the
+first poll that finds a wait unmet gives up.  Either way the call must still
+return, report KAMERA_DEVERR_TIMEOUT, and leave the device usable -- each CTA
+drained its own loads, copies and MMAs and released its tensor memory --
+which a normal call right after, on the same stream, shows by matching the
+oracle (a CTA that kept its tensor memory would leave the next launch's
+allocation waiting).  Nothing here faults: every address stays valid and
+every wait is bounded."""
 import numpy as np
 import pytest
 import torch
@@ -28,11 +31,13 @@ def test_relocate_wait_runs_out_then_recovers(name, monkeypatch):
     spec = W.scaled(W.CONFIGS[name](), L=3, lens=(1296, 200, 65, 900))
     wl = W.make(spec, DEV)
     err = torch.zeros(1, dtype=torch.int32, device=DEV)
-    monkeypatch.setenv("KAMERA_WAIT_LIMIT_NS", "0")
+    monkeypatch.setenv("KAMERA_WAIT_LIMIT_NS", "1000000")
+    monkeypatch.setenv("KAMERA_TEST_WITHHOLD_LOADS", "1")
     Hn.run_gpu(wl, err=err)
     torch.cuda.synchronize()
     assert int(err.item()) & TIMEOUT, f"no wait ran out (d_err = {int(err.item())})"
     monkeypatch.delenv("KAMERA_WAIT_LIMIT_NS")
+    monkeypatch.delenv("KAMERA_TEST_WITHHOLD_LOADS")
     again = W.make(spec, DEV)
     h = Hn.snapshot(again)
     err2 = torch.zeros(1, dtype=torch.int32, device=DEV)
