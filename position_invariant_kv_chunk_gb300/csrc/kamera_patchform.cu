@@ -1100,9 +1100,17 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
     // Z <- orth(X^T (X Z)), kWideIters times; the product accumulates in
     // registers: thread -> rows 4 ig .. 4 ig + 3, columns jg * kq .. + kq
     const int kq = k / 4, ig = t >> 2, jg = t & 3;
-    for (int it = 0; it < kWideIters; ++it) {
+    // The five passes over the rows alternate direction: each pass starts on the
+    // rows the one before it read last, which are still in L2 (the 27 blocks of a
+    // DeepSeek-V2-Lite chunk stream about as many bytes per pass as L2 holds, so
+    // passes that all ran forward found nothing left of the previous one).
+    const int n_tiles = (row_hi - row_lo + kWideT - 1) / kWideT;
+    int pass = 0;
+    auto tile_r0 = [&](int q) { return row_lo + ((pass & 1) ? n_tiles - 1 - q : q) * kWideT; };
+    for (int it = 0; it < kWideIters; ++it, ++pass) {
         float acc[4][12] = {};
-        for (int r0 = row_lo; r0 < row_hi; r0 += kWideT) {
+        for (int q = 0; q < n_tiles; ++q) {
+            const int r0 = tile_r0(q);
             wide_stage(p, x, r0, row_hi, xt);
             __syncthreads();
             wide_xb(xt, c, z, zs, k, yt, k);
@@ -1158,7 +1166,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
 
     // Rayleigh-Ritz: C = (X Z)^T (X Z), accumulated per thread over its (a, b) entries
     float cacc[5] = {0.f, 0.f, 0.f, 0.f, 0.f};
-    for (int r0 = row_lo; r0 < row_hi; r0 += kWideT) {
+    for (int q = 0; q < n_tiles; ++q) {
+        const int r0 = tile_r0(q);
         wide_stage(p, x, r0, row_hi, xt);
         __syncthreads();
         wide_xb(xt, c, z, zs, k, yt, k);
@@ -1255,7 +1264,9 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
     __syncthreads();
     // U = X V
     __nv_bfloat16* uo = p.u + blk * (int64_t)p.rows * m;
-    for (int r0 = row_lo; r0 < row_hi; r0 += kWideT) {
+    ++pass;
+    for (int q = 0; q < n_tiles; ++q) {
+        const int r0 = tile_r0(q);
         wide_stage(p, x, r0, row_hi, xt);
         __syncthreads();
         wide_xb(xt, c, z, zs, m, yt, m);
