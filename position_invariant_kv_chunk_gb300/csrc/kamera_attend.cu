@@ -649,56 +649,70 @@ __global__ void __launch_bounds__(kAtThreads, 1) attend_kernel(const __grid_cons
     }
 }
 
-// Merge of the split path (one CTA per unit u): the CTAs k that overlapped u
-// (k U / NC < u + 1 and (k + 1) U / NC > u) left (max, sum, unnormalised
-// output) per head in slot k + u; out = sum_k e^(m_k - M) O_k / sum_k
-// e^(m_k - M) l_k, rounded once to bf16.  Unit u's rows start at row
+// Merge of the split path, one CTA per (unit u, head h): the CTAs k that
+// overlapped u (k U / NC < u + 1 and (k + 1) U / NC > u) left (max, sum,
+// unnormalised output) per head in slot k + u; out = sum_k e^(m_k - M) O_k /
+// sum_k e^(m_k - M) l_k, rounded once to bf16.  Unit u's rows start at row
 // (u / groups) Hq + (u % groups) 16 of `out` ([*][dout]); `rows` of them.
 __global__ void __launch_bounds__(128) attend_merge_kernel(const float* __restrict__ ws, int64_t U, int64_t NC,
                                                            int dout, int groups, int Hq, int rows_max,
                                                            __nv_bfloat16* __restrict__ out)
 {
-    __shared__ float mx[kAtH], sum[kAtH];
+    constexpr int kMaxK = 64;   // overlapping CTAs whose weights are staged (more: computed in place)
+    __shared__ float wf[kMaxK];
+    __shared__ float stat[2];
     const int64_t u = blockIdx.x;
-    const int64_t k_lo = u * NC / U, k_hi = ((u + 1) * NC + U - 1) / U;   // CTAs [k_lo, k_hi)
-    const size_t slot = (size_t)(2 * kAtH + kAtH * dout);
+    const int h = blockIdx.y;
     const int grp = (int)(u % groups), rows = min(rows_max, Hq - grp * kAtH);
-    const int64_t row0 = (u / groups) * Hq + grp * kAtH;
-    if (threadIdx.x < kAtH) {
-        const int h = threadIdx.x;
+    if (h >= rows)
+        return;
+    const int64_t k_lo = u * NC / U, k_hi = ((u + 1) * NC + U - 1) / U;   // CTAs [k_lo, k_hi)
+    const int nk = (int)(k_hi - k_lo);
+    const size_t slot = (size_t)(2 * kAtH + kAtH * dout);
+    const float* w0 = ws + (size_t)(k_lo + u) * slot;   // slot of CTA k_lo; CTA k_lo + i is i slots on
+    if (threadIdx.x == 0) {
         float m = -INFINITY;
-        for (int64_t k = k_lo; k < k_hi; ++k)
-            m = fmaxf(m, ws[(size_t)(k + u) * slot + h]);
+        for (int i = 0; i < nk; ++i)
+            m = fmaxf(m, w0[(size_t)i * slot + h]);
         float l = 0.f;
-        for (int64_t k = k_lo; k < k_hi; ++k) {
-            const float mk = ws[(size_t)(k + u) * slot + h];
+        for (int i = 0; i < nk; ++i) {
+            const float mk = w0[(size_t)i * slot + h];
             if (mk != -INFINITY)
-                l = fmaf(ws[(size_t)(k + u) * slot + kAtH + h], expf(mk - m), l);
+                l = fmaf(w0[(size_t)i * slot + kAtH + h], expf(mk - m), l);
         }
-        mx[h] = m;
-        sum[h] = l;
+        stat[0] = m;
+        stat[1] = l;
     }
     __syncthreads();
-    for (int e = threadIdx.x; e < rows * (dout / 4); e += blockDim.x) {
-        const int h = e / (dout / 4), i = 4 * (e - h * (dout / 4));
+    const float m = stat[0], l = stat[1];
+    for (int i = threadIdx.x; i < min(nk, kMaxK); i += blockDim.x) {
+        const float mk = w0[(size_t)i * slot + h];
+        wf[i] = (mk == -INFINITY || !(l > 0.f)) ? 0.f : expf(mk - m) / l;
+    }
+    __syncthreads();
+    const int64_t row = (u / groups) * Hq + grp * kAtH + h;
+    for (int i = 4 * threadIdx.x; i < dout; i += 4 * blockDim.x) {
         float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (sum[h] > 0.f) {
-            for (int64_t k = k_lo; k < k_hi; ++k) {
-                const float* wk = ws + (size_t)(k + u) * slot;
-                if (wk[h] == -INFINITY)
-                    continue;
-                const float f = expf(wk[h] - mx[h]) / sum[h];
-                const float4 v = *reinterpret_cast<const float4*>(wk + 2 * kAtH + h * dout + i);
-                acc.x = fmaf(v.x, f, acc.x);
-                acc.y = fmaf(v.y, f, acc.y);
-                acc.z = fmaf(v.z, f, acc.z);
-                acc.w = fmaf(v.w, f, acc.w);
+        for (int k = 0; k < nk; ++k) {
+            float f;
+            if (k < kMaxK) {
+                f = wf[k];
+            } else {
+                const float mk = w0[(size_t)k * slot + h];
+                f = (mk == -INFINITY || !(l > 0.f)) ? 0.f : expf(mk - m) / l;
             }
+            if (f == 0.f)
+                continue;
+            const float4 v = *reinterpret_cast<const float4*>(w0 + (size_t)k * slot + 2 * kAtH + h * dout + i);
+            acc.x = fmaf(v.x, f, acc.x);
+            acc.y = fmaf(v.y, f, acc.y);
+            acc.z = fmaf(v.z, f, acc.z);
+            acc.w = fmaf(v.w, f, acc.w);
         }
         uint2 w;
         w.x = pack_bf16x2(acc.x, acc.y);
         w.y = pack_bf16x2(acc.z, acc.w);
-        *reinterpret_cast<uint2*>(out + (row0 + h) * dout + i) = w;
+        *reinterpret_cast<uint2*>(out + row * dout + i) = w;
     }
 }
 
@@ -709,7 +723,8 @@ cudaError_t launch_attend_merge(const float* ws, int64_t units, int64_t ctas, in
 {
     if (units < 1)
         return cudaSuccess;
-    attend_merge_kernel<<<(unsigned)units, 128, 0, stream>>>(ws, units, ctas, dout, groups, Hq, rows, out);
+    attend_merge_kernel<<<dim3((unsigned)units, (unsigned)rows), 128, 0, stream>>>(ws, units, ctas, dout, groups, Hq,
+                                                                                    rows, out);
     return cudaGetLastError();
 }
 
