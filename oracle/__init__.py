@@ -18,7 +18,8 @@ technical summary):
 * section 3.2, sliding-window survival by rotation only               -> ``slide``
 * attention over reused chunks (the pages' attention-kernel hook, section 3):
   softmax attention of a decode query over the reuse equation's rows -> ``attend``,
-  and its MLA form over the latent rows (absorbed query)                 -> ``attend_mla``
+  and its MLA form over the latent rows (absorbed query)                 -> ``attend_mla``;
+  many new query tokens at once (prefill), with each row's log-sum-exp -> ``attend_prefill``
 
 Pinned by ``tests/test_oracle_pins.py`` (closed forms, group laws of R, an
 independent complex-number RoPE, brute-force bf16 rounding, Eckart-Young by
@@ -400,6 +401,59 @@ class Oracle:
                     out[s, h] = pr @ V
                     mag[s, h] = pr @ np.abs(V)
         return self.bf16_rne(out), out, mag
+
+    def attend_prefill(self, store_k, store_v, chunks: Sequence[Chunk], seq_starts, q, layer: int, inv_freq,
+                       rot_dim: int, rot_offset: int = 0, pairing: int = ROTATE_HALF, scale: float = None):
+        """Prefill attention of T new query tokens per sequence over its reused
+        chunks: every token attends, in one softmax and with no mask (the chunks
+        precede the new tokens), over the reuse equation's rows of the sequence's
+        chunks (technical summary section 2; served by the attention-kernel hook
+        of section 3), exact and unrounded (fp64), and also gets the
+        log-sum-exp of its scores, lse = log sum_j exp(scale q . K_j).
+
+        ``q``: uint16 ``[S, T, H_q, d]`` (or fp64); the rest as for ``attend``.
+        Returns (bf16 bits ``[S, T, H_q, d]``, fp64 output, magnitude scale
+        sum_j p_j |V_j| per element, lse ``[S, T, H_q]``; -inf and zeros for a
+        sequence with no token)."""
+        N, H, d = store_k.shape
+        S, T, Hq, _ = q.shape
+        G = Hq // H
+        scale = 1.0 / np.sqrt(d) if scale is None else float(scale)
+        f64 = lambda a: a if np.asarray(a).dtype == np.float64 else self.bf16_to_f64(a)
+        kf, vf, qf = self.bf16_to_f64(store_k), self.bf16_to_f64(store_v), f64(q)
+        out = np.zeros((S, T, Hq, d))
+        mag = np.zeros((S, T, Hq, d))
+        lse = np.full((S, T, Hq), -np.inf)
+        for s in range(S):
+            for g in range(H):
+                # the rows of this KV head over the sequence's chunks, in order
+                Ks, Vs = [], []
+                for ci in range(seq_starts[s], seq_starts[s + 1]):
+                    c = chunks[ci]
+                    th = inv_freq[ci] if np.ndim(inv_freq) == 2 else inv_freq
+                    rows = slice(c.src_offset, c.src_offset + c.length)
+                    kk = self.rotate(kf[rows, g, :], c.delta, th, rot_dim, rot_offset, pairing)
+                    vv = vf[rows, g, :].copy()
+                    if c.rank > 0:
+                        uk, vk, uv, vvm = (f64(a)[layer, g] for a in c.patches)
+                        kk = kk + uk @ vk.T
+                        vv = vv + uv @ vvm.T
+                    Ks.append(kk)
+                    Vs.append(vv)
+                if not Ks or sum(k.shape[0] for k in Ks) == 0:
+                    continue
+                K, V = np.concatenate(Ks), np.concatenate(Vs)
+                for t in range(T):
+                    for h in range(g * G, (g + 1) * G):
+                        sc = scale * (K @ qf[s, t, h])
+                        mx = sc.max()
+                        w = np.exp(sc - mx)
+                        den = w.sum()
+                        pr = w / den
+                        out[s, t, h] = pr @ V
+                        mag[s, t, h] = pr @ np.abs(V)
+                        lse[s, t, h] = mx + np.log(den)
+        return self.bf16_rne(out), out, mag, lse
 
     def attend_mla(self, store, chunks: Sequence[Chunk], seq_starts, q, layer: int, kv_lora: int, inv_freq,
                    rot_dim: int, rot_offset: int = 0, pairing: int = INTERLEAVED, scale: float = None):

@@ -924,4 +924,70 @@ def pin_rejects_bad_indices(orc: O.Oracle):
     raise AssertionError("out-of-range slot accepted")
 
 
+def _prefill_q(rng, seqs, T, Hq, d):
+    return rand_bf16(rng, (len(seqs) - 1, T, Hq, d))
+
+
+def pin_attend_prefill_is_per_token_decode(orc: O.Oracle):
+    """No mask applies among the chunk tokens, so prefill attention of T tokens
+    is T independent decode attentions (the pinned decode oracle, ``attend``),
+    one per token, both pairings, with patches, to 1e-12."""
+    rng = np.random.default_rng(41)
+    for pairing, r, o in ((RH, 32, 0), (IL, 16, 8)):
+        sk, sv, chunks, seqs, _, layer = _attend_problem(rng)
+        H, d = sk.shape[1], sk.shape[2]
+        q = _prefill_q(rng, seqs, 5, 3 * H, d)
+        th = orc.inv_freq(1e4, r)
+        _, out, _, lse = orc.attend_prefill(sk, sv, chunks, seqs, q, layer, th, r, o, pairing, scale=0.3)
+        for t in range(q.shape[1]):
+            _, want, _ = orc.attend(sk, sv, chunks, seqs, q[:, t], layer, th, r, o, pairing, scale=0.3)
+            assert np.max(np.abs(out[:, t] - want)) < 1e-12, (pairing, t)
+        assert np.all(np.isfinite(lse))
+
+
+def pin_attend_prefill_lse_closed_form(orc: O.Oracle):
+    """Closed forms of the log-sum-exp: with every key the same row k (delta 0,
+    no patch) over L tokens, lse = log L + scale q . k; with q = 0, lse = log L
+    for any keys; a sequence with no token gets lse = -inf and zeros."""
+    rng = np.random.default_rng(42)
+    sk, sv, chunks, seqs, _, layer = _attend_problem(rng, lens=(6, 4), deltas=(0, 0), seqs=(0, 2, 2),
+                                                     zero_rank=True)
+    sk[:] = sk[0]
+    H, d = sk.shape[1], sk.shape[2]
+    q = _prefill_q(rng, seqs, 3, 3 * H, d)
+    th = orc.inv_freq(1e4, 32)
+    _, out, _, lse = orc.attend_prefill(sk, sv, chunks, seqs, q, layer, th, 32, scale=0.25)
+    kf, qf = to_f64(sk), to_f64(q)
+    for t in range(3):
+        for h in range(3 * H):
+            want = math.log(10) + 0.25 * float(kf[0, h // 3] @ qf[0, t, h])
+            assert abs(lse[0, t, h] - want) < 1e-12, (t, h, lse[0, t, h], want)
+    assert np.all(lse[1] == -np.inf) and not np.any(out[1])
+    sk2, sv2, chunks2, seqs2, _, layer2 = _attend_problem(rng)
+    q0 = np.zeros((len(seqs2) - 1, 2, 3 * H, d))
+    _, _, _, lse0 = orc.attend_prefill(sk2, sv2, chunks2, seqs2, q0, layer2, th, 32)
+    for s in range(len(seqs2) - 1):
+        L = sum(c.length for c in chunks2[seqs2[s]:seqs2[s + 1]])
+        assert np.max(np.abs(lse0[s] - math.log(L))) < 1e-12, s
+
+
+def pin_attend_prefill_lse_merge(orc: O.Oracle):
+    """The log-sum-exp merges softmaxes: attention over a sequence's chunks
+    equals the two halves' outputs weighted by e^lse (and its lse is
+    log(e^lse1 + e^lse2)), which is how a prefill joins the reused chunks'
+    softmax with the one over its own new tokens."""
+    rng = np.random.default_rng(43)
+    sk, sv, chunks, _, _, layer = _attend_problem(rng, seqs=(0, 4))
+    H, d = sk.shape[1], sk.shape[2]
+    q = _prefill_q(rng, (0, 1), 4, 3 * H, d)
+    th = orc.inv_freq(1e4, 32)
+    _, out, _, lse = orc.attend_prefill(sk, sv, chunks, [0, 4], q, layer, th, 32, scale=0.4)
+    _, o1, _, l1 = orc.attend_prefill(sk, sv, chunks[:1], [0, 1], q, layer, th, 32, scale=0.4)
+    _, o2, _, l2 = orc.attend_prefill(sk, sv, chunks[1:], [0, 3], q, layer, th, 32, scale=0.4)
+    mx = np.maximum(l1, l2)
+    w1, w2 = np.exp(l1 - mx)[..., None], np.exp(l2 - mx)[..., None]
+    assert np.max(np.abs(out - (w1 * o1 + w2 * o2) / (w1 + w2))) < 1e-12
+    assert np.max(np.abs(lse - np.logaddexp(l1, l2))) < 1e-12
+
+
 ALL_PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]
