@@ -42,6 +42,7 @@ import workloads as W  # noqa: E402
 METRIC = "relocated KV GB/s (read+write) & tokens reinstated/s; % of GB300 HBM peak"
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
 
 
 # ------------------------------------------------------------------ utils
@@ -53,6 +54,15 @@ def measured_peaks():
         return float(j["hbm_gbs"]), "measured"
     except Exception:
         return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_bf16_peak():
+    """Dense bf16 tensor peak (TFLOP/s, the burst figure: a kernel timed alone)."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except Exception:
+        return FALLBACK_BF16_TFLOPS, "fallback"
 
 
 def max_over_ranks(value: float, dist=None, device="cpu") -> float:
@@ -243,7 +253,7 @@ def sweep(K, dev, peak, skip, only=None):
             continue
         try:
             spec = f()
-            entry = mla_attend_entry if spec.kind == "mla_attend" else attend_entry
+            entry = {"mla_attend": mla_attend_entry, "prefill": prefill_entry}.get(spec.kind, attend_entry)
             out[name] = entry(K, spec, dev, peak, flush)
         except Exception as e:  # report, keep the headline
             out[name] = {"error": f"{type(e).__name__}: {e}"[:300]}
@@ -274,6 +284,37 @@ def attend_entry(K, spec, dev, peak, flush):
             "tokens_attended_per_s": tok / t, "sequences": len(spec.seqs), "rank": spec.m,
             "l2": "flushed between launches", "kernel": "attend_kernel",
             "traffic": traffic_record("attend_kernel", spec.name), "device_err": int(err.item())}
+
+
+def prefill_entry(K, spec, dev, peak, flush):
+    """Prefill attention over reused chunks (T new query tokens per sequence),
+    timed per launch with L2 flushes; a dense contraction on the tensor cores,
+    so its roofline is the bf16 tensor peak (the folded form's flops)."""
+    a = W.make_attend(spec, dev)
+    chunks = K.pack_chunks(a.chunks, device=dev)
+    seq = torch.tensor(a.seq_start, dtype=torch.int32, device=dev)
+    rope = K.Rope(spec.base, a.rot_dim, spec.rot_offset, spec.pairing)
+    ml, mr = max(c.length for c in a.chunks), max(c.rank for c in a.chunks)
+    out = torch.empty_like(a.q)
+    lse = torch.empty(a.q.shape[:3], dtype=torch.float32, device=dev)
+    err = torch.zeros(1, dtype=torch.int32, device=dev)
+
+    def call():
+        K.kamera_prefill_attend_reused(a.store_k, a.store_v, a.q, rope, chunks, seq, len(a.chunks), ml, mr,
+                                       layer=spec.layer, out=out, lse=lse, err=err)
+
+    for _ in range(3):
+        call()
+    t = float(np.median(time_launches(call, 10, flush))) * 1e-3
+    fl = W.prefill_flops(spec)
+    tf_peak, tf_src = measured_bf16_peak()
+    tok = sum(c.length for c in a.chunks)
+    return {"ms": t * 1e3, "tflops": fl / t / 1e12, "frac_of_bf16_peak": fl / t / 1e12 / tf_peak,
+            "bf16_peak_tflops": tf_peak, "bf16_peak_source": tf_src, "flops": fl,
+            "query_tokens_per_s": len(spec.seqs) * spec.T / t, "tokens_attended_per_s": tok * spec.T / t,
+            "sequences": len(spec.seqs), "query_tokens": spec.T, "rank": spec.m,
+            "l2": "flushed between launches", "kernel": "prefill_kernel",
+            "traffic": traffic_record("prefill_kernel", spec.name), "device_err": int(err.item())}
 
 
 def mla_attend_entry(K, spec, dev, peak, flush):
@@ -414,6 +455,7 @@ KERNEL_UNITS = {   # the translation unit each timed kernel is compiled from
     "patch_form_kernel": "kamera_patchform.cu",
     "attend_kernel": "kamera_attend.cu",
     "mla_attend_kernel": "kamera_attend_mla.cu",
+    "prefill_kernel": "kamera_prefill.cu",
 }
 
 

@@ -80,7 +80,7 @@ extern "C" {
 
 struct CUstream_st; /* cudaStream_t == struct CUstream_st* */
 
-#define KAMERA_ABI_VERSION 8
+#define KAMERA_ABI_VERSION 9
 
 /* Limits of this library. */
 #define KAMERA_MAX_RANK 128          /* largest patch rank m */
@@ -109,8 +109,9 @@ enum {
                                       (every wait of the tensor-core kernels is bounded by
                                       1 s; the environment variable KAMERA_WAIT_LIMIT_NS,
                                       read at each call, overrides the bound.  Test hooks:
-                                      KAMERA_TEST_WITHHOLD_LOADS=1 makes the relocation
-                                      kernel's producer issue no loads, and for patch
+                                      KAMERA_TEST_WITHHOLD_LOADS=1 makes the producers of
+                                      the relocation and prefill attention kernels issue
+                                      no tile loads, and for patch
                                       formation a bound of 0 gives up at its first wait;
                                       the kernels then give up early, drain their own
                                       copies and MMAs, free their tensor memory and
@@ -553,6 +554,50 @@ int kamera_mla_attend_reused(const KameraAttnMlaKV* kv, const KameraAttnQuery* q
  * states of 4 (32 + 16 * 512) bytes); 0 for an empty batch or when the device
  * cannot be queried. */
 size_t kamera_mla_attend_workspace_bytes(int32_t n_seqs, int32_t num_q_heads);
+
+/*
+ * Prefill attention over reused chunks, without the pool (technical summary
+ * section 3, "Production Deployment": the attention-kernel hook; the rows are
+ * section 2's reuse equation).  Each sequence s brings q_tokens new query
+ * tokens; every one of them attends, in one softmax and with no mask, over the
+ * tokens of the sequence's chunks d_chunks[d_seq_start[s] .. d_seq_start[s+1]-1]
+ * (they precede the new tokens), whose keys and values are, unrounded,
+ *     K_j = R(delta) k_j + Uk[j] Vk^T,   V_j = v_j + Uv[j] Vv^T
+ * as for kamera_attend_reused.  out = softmax(scale q K^T) V per query token
+ * and head, and lse = log sum_j exp(scale q . K_j) (natural log), so a caller
+ * merges this softmax with the one over the new tokens themselves:
+ * out = (e^lse1 out1 + e^lse2 out2) / (e^lse1 + e^lse2).  fp32 accumulation of
+ * bf16 products on the tensor cores (hi + lo bf16 pairs for the turned query,
+ * V_k^T q and the softmax weights), one bf16 rounding of the output; a
+ * sequence with no token gets zeros and lse = -infinity.
+ *   kv      as for kamera_attend_reused (one layer's canonical store, layer =
+ *           the factors' layer index)
+ *   query   q bf16 [n_seqs][q_tokens][num_q_heads][head_dim] (RoPE already
+ *           applied at each token's position, 16-byte aligned), out bf16 of the
+ *           same shape (written, 16-byte aligned), lse float
+ *           [n_seqs][q_tokens][num_q_heads] (written) or NULL, scale
+ *   d_seq_start, descriptors: as for kamera_attend_reused.
+ * Supported: head_dim 64 or 128, num_q_heads a multiple of num_kv_heads,
+ * ranks <= max_rank <= 64.  Device errors (the chunk is skipped): SOURCE,
+ * DESCRIPTOR (also a malformed d_seq_start: the sequence is skipped), LEN,
+ * RANK; TIMEOUT if a pipeline wait runs past its bound (outputs of the call
+ * then undefined).  Host errors: INVALID_ARGUMENT (also out overlapping q, the
+ * store or lse), MISALIGNED, UNSUPPORTED (also num_rows > 2^31 - 1 or more
+ * than 2^31 - 1 blocks of 128 query rows).
+ */
+typedef struct KameraPrefillQuery {
+    const void* q;
+    void* out;
+    float* lse;
+    int32_t n_seqs;
+    int32_t q_tokens;
+    int32_t num_q_heads;
+    float scale;
+} KameraPrefillQuery;
+
+int kamera_prefill_attend_reused(const KameraAttnKV* kv, const KameraPrefillQuery* query, const KameraRope* rope,
+                                 const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
+                                 int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream);
 
 /*
  * kamera_attend_reused for callers that cannot allocate device memory.  The

@@ -25,6 +25,7 @@ __all__ = [
     "KameraError", "Rope", "ChunkSpec", "load_library", "pack_chunks",
     "kamera_relocate_patch", "kamera_slide_inplace", "kamera_mla_relocate_patch",
     "kamera_ingest_canonical", "kamera_mla_ingest_canonical", "kamera_form_patch", "kamera_attend_reused",
+    "kamera_prefill_attend_reused",
     "kamera_validate_chunks", "kamera_status_string", "kamera_abi_version",
     "ROTATE_HALF", "INTERLEAVED", "DEVERR",
 ]
@@ -104,6 +105,11 @@ class _AttnQuery(C.Structure):
                 ("scale", C.c_float), ("reserved", C.c_int32)]
 
 
+class _PrefillQuery(C.Structure):
+    _fields_ = [("q", C.c_void_p), ("out", C.c_void_p), ("lse", C.c_void_p), ("n_seqs", C.c_int32),
+                ("q_tokens", C.c_int32), ("num_q_heads", C.c_int32), ("scale", C.c_float)]
+
+
 class _AttnMlaKV(C.Structure):
     _fields_ = [("kv", C.c_void_p), ("num_rows", C.c_int64), ("row_stride", C.c_int64),
                 ("kv_lora_rank", C.c_int32), ("rope_dim", C.c_int32), ("layer", C.c_int32),
@@ -158,6 +164,9 @@ def load_library(path: Optional[str] = None, build_if_missing: bool = True) -> C
     lib.kamera_mla_attend_reused.argtypes = [P(_AttnMlaKV), P(_AttnQuery), P(_Rope), C.c_void_p, C.c_void_p,
                                              C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_size_t, C.c_void_p,
                                              C.c_void_p]
+    lib.kamera_prefill_attend_reused.restype = C.c_int
+    lib.kamera_prefill_attend_reused.argtypes = [P(_AttnKV), P(_PrefillQuery), P(_Rope), C.c_void_p, C.c_void_p,
+                                                 C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
     lib.kamera_attend_reused_static.restype = C.c_int
     lib.kamera_attend_reused_static.argtypes = [P(_AttnKV), P(_AttnQuery), P(_Rope), C.c_void_p, C.c_void_p,
                                                 C.c_int32, C.c_int32, C.c_int32, C.c_void_p, C.c_void_p]
@@ -184,7 +193,7 @@ def kamera_status_string(status: int) -> str:
     return load_library().kamera_status_string(int(status)).decode()
 
 
-ABI_VERSION = 8   # the KAMERA_ABI_VERSION these bindings marshal for
+ABI_VERSION = 9   # the KAMERA_ABI_VERSION these bindings marshal for
 
 
 def kamera_abi_version() -> int:
@@ -638,6 +647,54 @@ def kamera_attend_reused_static(store_k: torch.Tensor, store_v: torch.Tensor, q:
     del keep
     _check(rc, "kamera_attend_reused_static")
     return out
+
+
+def kamera_prefill_attend_reused(store_k: torch.Tensor, store_v: torch.Tensor, q: torch.Tensor, rope: Rope,
+                                 chunks: torch.Tensor, seq_start: torch.Tensor, n_chunks: int, max_len: int,
+                                 max_rank: int, layer: int = 0, scale: Optional[float] = None,
+                                 out: Optional[torch.Tensor] = None, lse=None, err: Optional[torch.Tensor] = None,
+                                 stream=None):
+    """Prefill attention of T new query tokens per sequence over its reused
+    chunks (see ``kamera_prefill_attend_reused`` in kamera.h).
+
+    store_k/v: bf16 ``[N, H_kv, d]`` (one layer; packed heads, any row stride);
+    q: bf16 ``[S, T, H_q, d]`` contiguous; seq_start: device int32 ``[S + 1]``;
+    lse: None (allocated: fp32 ``[S, T, H_q]``), False (not computed) or a
+    contiguous fp32 tensor of that shape.  Returns ``(out, lse)`` (lse None
+    when not computed)."""
+    _on_device("kamera_prefill_attend_reused", store_k=store_k, store_v=store_v, q=q, chunks=chunks,
+               seq_start=seq_start, out=out, err=err, lse=lse if isinstance(lse, torch.Tensor) else None)
+    for t, nm in ((store_k, "store_k"), (store_v, "store_v"), (q, "q")):
+        _bf16(t, nm)
+    if store_k.dim() != 3 or store_k.stride(2) != 1 or store_k.stride(1) != store_k.shape[2]:
+        raise ValueError("store_k must be [N, H_kv, d] with packed heads")
+    if store_v.shape != store_k.shape or store_v.stride() != store_k.stride():
+        raise ValueError("store_k and store_v must share shape and strides")
+    N, H, d = store_k.shape
+    if q.dim() != 4 or q.shape[3] != d or not q.is_contiguous():
+        raise ValueError("q must be a contiguous [S, T, H_q, d] tensor")
+    S, T, Hq, _ = q.shape
+    if out is None:
+        out = torch.empty_like(q)
+    if out.shape != q.shape or out.dtype != torch.bfloat16 or not out.is_contiguous():
+        raise ValueError("out must be a contiguous bf16 tensor shaped like q")
+    if lse is None:
+        lse = torch.empty(S, T, Hq, dtype=torch.float32, device=q.device)
+    elif lse is False:
+        lse = None
+    if lse is not None and (tuple(lse.shape) != (S, T, Hq) or lse.dtype != torch.float32 or not lse.is_contiguous()):
+        raise ValueError("lse must be a contiguous fp32 [S, T, H_q] tensor")
+    if seq_start.dtype != torch.int32 or seq_start.numel() != S + 1:
+        raise ValueError("seq_start must hold S + 1 int32 values")
+    kv = _AttnKV(_addr(store_k), _addr(store_v), N, store_k.stride(0), H, d, int(layer), 0)
+    qq = _PrefillQuery(_addr(q), _addr(out), _addr(lse), S, T, Hq, float(d ** -0.5 if scale is None else scale))
+    r, keep = rope._c(n_chunks)
+    rc = load_library().kamera_prefill_attend_reused(C.byref(kv), C.byref(qq), C.byref(r), _addr(chunks),
+                                                     _addr(seq_start), int(n_chunks), int(max_len), int(max_rank),
+                                                     _addr(err), _stream_handle(stream))
+    del keep
+    _check(rc, "kamera_prefill_attend_reused")
+    return out, lse
 
 
 def kamera_mla_attend_reused(store: torch.Tensor, kv_lora: int, q: torch.Tensor, rope: Rope, chunks: torch.Tensor,

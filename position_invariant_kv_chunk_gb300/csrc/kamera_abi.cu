@@ -722,6 +722,76 @@ int kamera_attend_reused(const KameraAttnKV* kv, const KameraAttnQuery* query, c
                : KAMERA_ERR_CUDA;
 }
 
+int kamera_prefill_attend_reused(const KameraAttnKV* kv, const KameraPrefillQuery* query, const KameraRope* rope,
+                                 const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
+                                 int32_t max_len, int32_t max_rank, int32_t* d_err, struct CUstream_st* stream)
+{
+    if (!kv || !query || !rope || kv->reserved != 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (query->n_seqs < 0 || query->q_tokens < 0 || n_chunks < 0 || max_len < 0 || max_rank < 0 ||
+        kv->num_rows < 0 || kv->layer < 0)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (kv->num_kv_heads < 1 || kv->head_dim < 8 || query->num_q_heads < 1 ||
+        query->num_q_heads % kv->num_kv_heads != 0 || !(query->scale == query->scale))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    const int G = query->num_q_heads / kv->num_kv_heads;
+    if (!prefill_supported(kv->head_dim, max_rank) || kv->num_rows > 0x7FFFFFFF)
+        return KAMERA_ERR_UNSUPPORTED;
+    const int64_t rows = (int64_t)query->q_tokens * G;   // query rows of one (sequence, KV head)
+    const int64_t blocks = (rows + 127) / 128;
+    if (rows > 0x7FFFFFFF || (int64_t)query->n_seqs * kv->num_kv_heads * blocks > 0x7FFFFFFF)
+        return KAMERA_ERR_UNSUPPORTED;
+    if (query->n_seqs == 0 || query->q_tokens == 0)
+        return KAMERA_OK;
+    if (!kv->k || !kv->v || !query->q || !query->out || !d_seq_start || (n_chunks > 0 && !d_chunks))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    const int64_t W = (int64_t)kv->num_kv_heads * kv->head_dim;
+    if (kv->row_stride < W)
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (!aligned16(kv->k) || !aligned16(kv->v) || !aligned16(d_chunks) || kv->row_stride % 8 ||
+        !aligned16(query->q) || !aligned16(query->out) || (reinterpret_cast<uintptr_t>(query->lse) & 3))
+        return KAMERA_ERR_MISALIGNED;
+    const auto ks = span(kv->k, 1, 0, kv->num_rows, kv->row_stride, W);
+    const auto vs = span(kv->v, 1, 0, kv->num_rows, kv->row_stride, W);
+    const int64_t qn = (int64_t)query->n_seqs * query->q_tokens * query->num_q_heads;
+    const auto os = span(query->out, 1, 0, 1, 0, qn * kv->head_dim);
+    const auto qs = span(query->q, 1, 0, 1, 0, qn * kv->head_dim);
+    if (overlap(os, ks) || overlap(os, vs) || overlap(os, qs))
+        return KAMERA_ERR_INVALID_ARGUMENT;
+    if (query->lse) {
+        const auto ls = span(query->lse, 1, 0, 1, 0, 2 * qn);   // fp32: two bf16 widths each
+        if (overlap(ls, ks) || overlap(ls, vs) || overlap(ls, qs) || overlap(ls, os))
+            return KAMERA_ERR_INVALID_ARGUMENT;
+    }
+    PrefillParams p;
+    std::memset(&p, 0, sizeof(p));
+    int rc = fill_rope(rope, kv->head_dim, &p.rope);
+    if (rc)
+        return rc;
+    p.k = static_cast<const __nv_bfloat16*>(kv->k);
+    p.v = static_cast<const __nv_bfloat16*>(kv->v);
+    p.row_stride = kv->row_stride;
+    p.num_rows = kv->num_rows;
+    p.H = kv->num_kv_heads;
+    p.d = kv->head_dim;
+    p.G = G;
+    p.layer = kv->layer;
+    p.chunks = d_chunks;
+    p.seq_start = d_seq_start;
+    p.n_seqs = query->n_seqs;
+    p.n_chunks = n_chunks;
+    p.T = query->q_tokens;
+    p.blocks = (int32_t)blocks;
+    p.q = static_cast<const __nv_bfloat16*>(query->q);
+    p.out = static_cast<__nv_bfloat16*>(query->out);
+    p.lse = query->lse;
+    p.scale = query->scale;
+    p.max_len = max_len;
+    p.max_rank = max_rank;
+    p.err = d_err;
+    return launch_prefill(p, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess ? KAMERA_OK : KAMERA_ERR_CUDA;
+}
+
 int kamera_mla_attend_reused(const KameraAttnMlaKV* kv, const KameraAttnQuery* query, const KameraRope* rope,
                              const KameraChunk* d_chunks, const int32_t* d_seq_start, int32_t n_chunks,
                              int32_t max_len, int32_t max_rank, void* d_workspace, size_t workspace_bytes,

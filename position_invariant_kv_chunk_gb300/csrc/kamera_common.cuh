@@ -134,6 +134,28 @@ struct MlaAttendParams {
     RopeParams rope;               // rot_offset relative to k_rope
 };
 
+// Prefill attention over reused chunks: T new query tokens per sequence, each
+// attending over the reuse equation's rows of the sequence's chunks (which all
+// precede the new tokens, so no mask applies among them).
+struct PrefillParams {
+    const __nv_bfloat16* k;        // canonical keys / values of one layer: rows of H x d,
+    const __nv_bfloat16* v;        // row_stride elements apart
+    int64_t row_stride, num_rows;
+    int32_t H, d, G, layer;        // KV heads, head dim, query heads per KV head, factor layer
+    const KameraChunk* chunks;
+    const int32_t* seq_start;      // [n_seqs + 1]
+    int32_t n_seqs, n_chunks;
+    int32_t T;                     // query tokens per sequence
+    int32_t blocks;                // 128-row blocks of one (sequence, KV head)'s T x G query rows
+    const __nv_bfloat16* q;        // [n_seqs][T][H * G][d]
+    __nv_bfloat16* out;            // [n_seqs][T][H * G][d]
+    float* lse;                    // [n_seqs][T][H * G] (natural log), or NULL
+    float scale;
+    int32_t max_len, max_rank;
+    int32_t* err;
+    RopeParams rope;
+};
+
 // ------------------------------------------------------------------ bf16 --
 __device__ __forceinline__ float bf16lo(uint32_t w) { return __uint_as_float(w << 16); }
 __device__ __forceinline__ float bf16hi(uint32_t w) { return __uint_as_float(w & 0xFFFF0000u); }

@@ -22,8 +22,9 @@ struct RowsParams;
 uint64_t wait_limit_ns();
 
 // Test hook: KAMERA_TEST_WITHHOLD_LOADS=1 in the environment makes the
-// relocation kernel's producer issue no loads, so its first pipeline waits
-// run out after the bound above (read on the host at each launch).
+// producers of the relocation and prefill attention kernels issue no loads,
+// so their first pipeline waits run out after the bound above (read on the
+// host at each launch).
 bool test_withhold_loads();
 
 // CUDA-core streaming path (any rank within the shared-memory budget).
@@ -41,6 +42,7 @@ struct IngestPass;
 struct IngestParams;
 struct PatchFormParams;
 struct AttendParams;
+struct PrefillParams;
 int ingest_passes(const RowsParams& rp, bool values, IngestPass* out);
 cudaError_t launch_ingest(const IngestParams& p, cudaStream_t stream);
 
@@ -67,6 +69,11 @@ cudaError_t launch_mla_attend(const MlaAttendParams& p, void* ws, size_t ws_byte
 size_t attend_slot_bytes(int dout);
 cudaError_t launch_attend_merge(const float* ws, int64_t units, int64_t ctas, int dout, int groups, int Hq,
                                 int rows, __nv_bfloat16* out, cudaStream_t stream);
+
+// Prefill attention over reused chunks (tensor cores): shapes handled; one CTA
+// per 128 query rows of a (sequence, KV head).
+bool prefill_supported(int head_dim, int max_rank);
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream);
 
 // 2-D tensor map (a CUtensorMap, 64-byte aligned, at `map`) over a bf16 array
 // of `rows` rows of `width` elements, row_stride elements apart: boxes of

@@ -1,0 +1,834 @@
+// kamera_prefill.cu -- prefill attention over reused chunks, on the tensor cores.
+//
+// A prefill that reuses chunks attends from its T new query tokens over the
+// reuse equation's rows of the chunks (gist.science technical summary, section
+// 2), which the pages serve through a hook in the attention kernel (section 3,
+// "Production Deployment"):
+//     K_j = R(delta_c) k_j + V_k u_j,    V_j = v_j + V_v u'_j
+// The chunks precede the new tokens, so no mask applies among them; each query
+// row also gets its log-sum-exp, which merges this softmax with the one over
+// the new tokens themselves.  As in decode, the turn and the patch fold into
+// per-chunk query quantities, so no relocated row is ever formed:
+//     q . K_j        = (R(-delta_c) q) . k_j + (V_k^T q) . u_j
+//     sum_j p_j V_j  = sum_j p_j v_j + V_v (sum_j p_j u'_j)
+//
+// A (sequence, KV head) has T x G query rows (token-major: row r is token
+// r / G, query head r % G of the KV head); one CTA owns 128 of them, the M of
+// the 5th-generation tensor-core MMA (tcgen05.mma, fp32 accumulators in TMEM),
+// and streams the sequence's rows in 64-token tiles:
+//     S   [128 x 64]   = [Q' | X] [k | u]^T      Q' = R(-delta) q, X = V_k^T q
+//     O_v [128 x d]   += P v                     P = the softmax weights
+//     O_u [128 x 64]  += P u'                    folded through V_v per chunk
+// Q', X and P are not bf16 values: each enters as a bf16 hi + lo pair (two
+// MMAs, about 16 significant bits); the rows and U rows are exact bf16.  The
+// A operands (Q', X, P) live in TMEM, so the MMAs read only the tile's rows
+// from shared memory; P overwrites its S columns.
+// Roles (192 threads):
+//   warps 0-3  softmax: thread = query row = TMEM lane.  Per tile: the S row,
+//              running max with lazy rescaling (O is rescaled in TMEM only when
+//              the max grows by more than 2^8, so the weights stay below 256),
+//              the weights as hi + lo into TMEM.  Per chunk: Q' and X into TMEM,
+//              and at its end O_v += (sum_j p_j u'_j) V_v^T on the CUDA cores.
+//              At the end: out = O_v / l and lse = m + log l.
+//   warp 4     producer: key and value rows of a tile as 128B-swizzled TMA
+//              boxes (64 columns x 64 rows), U and U' rows by 16-byte loads into
+//              the same layout (ranks padded to 64 with zeros); the value rows
+//              of a chunk's last, partial tile by loads too, zero past the chunk.
+//   warp 5     MMA: one lane issues S of tile n, then P v and P u' of tile
+//              n - 1 (so the softmax of tile n - 1 overlaps the scores of tile
+//              n), and commits each to an mbarrier; the warp owns TMEM.
+// Every wait is bounded in time: on expiry KAMERA_DEVERR_TIMEOUT is raised, the
+// waits that follow return at once, the softmax warps run their loops to the
+// end without waiting (so their CTA-internal barriers still meet), the MMA
+// warp drains what it issued and the producer the copies it started, and TMEM
+// is freed.
+#include <cstdint>
+#include <cstring>
+#include <cuda.h>
+#include <cuda_bf16.h>
+
+#include "kamera_common.cuh"
+#include "kamera_internal.h"
+#include "kamera_ptx.cuh"
+#include "kamera_warpmma.cuh"
+
+namespace kamera {
+
+namespace {
+
+constexpr int kPfRows = 128;          // query rows per CTA = MMA M = TMEM lanes
+constexpr int kPfTok = 64;            // tokens per tile
+constexpr int kPfMP = 64;             // ranks, padded: the U tiles' width
+constexpr int kPfThreads = 192;       // warps 0-3 softmax, 4 producer, 5 MMA
+constexpr int kPfProd = 4, kPfMma = 5;
+constexpr float kPfLazy = 8.0f;       // log2 of the growth of the running max that forces a rescale
+constexpr uint32_t kBox = 8192;       // one TMA box: 64 rows x 128 bytes
+
+// Shared memory from a 1024-byte aligned base: the tile ring (per stage the
+// key boxes, the value boxes, U and U'), V_k and V_v of the current chunk
+// ([d][64] bf16, ranks padded), the cos/sin of -delta, the barriers.
+template <int D>
+struct PfLayout {
+    static constexpr int NB = D / 64;                          // 64-column boxes of a head row
+    static constexpr int NS = D == 128 ? 3 : 4;                 // stages
+    static constexpr uint32_t kK = 0, kV = NB * kBox, kU = 2 * NB * kBox, kU2 = kU + kBox;
+    static constexpr uint32_t kStage = kU2 + kBox;
+    static constexpr uint32_t kVk = NS * kStage;                // V_k [d][64]
+    static constexpr uint32_t kVv = kVk + D * 128;              // V_v [d][64]
+    static constexpr uint32_t kCs = kVv + D * 128;              // float2 [64]
+    static constexpr uint32_t kBar = kCs + 512;
+    static constexpr uint32_t kBytes = kBar + 256 + 1024;       // + alignment slack
+    // TMEM columns: S (and P) of tiles 2i and 2i + 1, O_v, O_u, Q' hi and lo, X hi and lo
+    static constexpr uint32_t kTmS = 0, kTmOv = 2 * kPfTok, kTmOu = kTmOv + D, kTmQh = kTmOu + kPfMP;
+    static constexpr uint32_t kTmQl = kTmQh + D / 2, kTmXh = kTmQl + D / 2, kTmXl = kTmXh + kPfMP / 2;
+    static_assert(kTmXl + kPfMP / 2 <= 512, "TMEM columns");
+    static_assert(kBytes <= 227 * 1024, "shared memory");
+};
+
+struct PfBars {
+    uint64_t full[4], empty[4];        // tile ring: loads landed / MMAs done with the stage
+    uint64_t s_full[2], p_full[2];     // S of tile n in TMEM / P of tile n in TMEM
+    uint64_t pv_done[2];               // P v and P u' of tile n done
+    uint64_t a_ready;                  // the chunk's Q' and X in TMEM
+    uint64_t drained;                  // every MMA of the CTA done
+    uint32_t tmem;
+    int32_t abort;
+};
+static_assert(sizeof(PfBars) <= 256, "barrier block");
+
+struct PrefillLaunch {
+    PrefillParams p;
+    CUtensorMap map_k, map_v;          // [num_rows][H * d], boxes of 64 columns x 64 rows
+    uint64_t wait_ns;
+    int32_t withhold;                  // test hook: the producer starts no tile copy
+};
+
+__device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+        "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(ta)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld8(uint32_t ta, uint32_t (&r)[8])
+{
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
+        "tcgen05.wait::ld.sync.aligned;"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
+        : "r"(ta)
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32])
+{
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+        "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(ta),
+        "r"(r[0]), "r"(r[1]), "r"(r[2]), "r"(r[3]), "r"(r[4]), "r"(r[5]), "r"(r[6]), "r"(r[7]), "r"(r[8]),
+        "r"(r[9]), "r"(r[10]), "r"(r[11]), "r"(r[12]), "r"(r[13]), "r"(r[14]), "r"(r[15]), "r"(r[16]), "r"(r[17]),
+        "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
+        "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
+        : "memory");
+}
+
+__device__ __forceinline__ void tmem_st4(uint32_t ta, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(ta), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
+
+// D[tmem] (+)= A[tmem] * B[smem]^T (kind::f16, bf16 in, fp32 accumulate); A's
+// row r sits in TMEM lane r, elements 2c and 2c + 1 in the low and high half
+// of column c.
+__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
+                                        uint32_t accumulate)
+{
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// B operand whose N dimension is contiguous (MN-major), 128-byte swizzle: the
+// rows of a TMA box are K (tokens), 64-element atoms along N are `lbo` bytes
+// apart, 8-row groups along K 1024 bytes apart.
+__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t lbo)
+{
+    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
+           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
+}
+
+// 16-byte piece c of row r of a 128B-swizzled tile of 128-byte rows (the TMA
+// and MMA layout): piece c ^ (r & 7).
+__device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+__device__ __forceinline__ void bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
+
+__device__ __forceinline__ int32_t prefill_check(const KameraChunk& ch, int c, const PrefillParams& p)
+{
+    int32_t bits = check_axis_delta(p.rope, c);
+    if (ch.len < 0 || ch.rank < 0 || ch.delta > KAMERA_MAX_ABS_DELTA || ch.delta < -KAMERA_MAX_ABS_DELTA)
+        bits |= KAMERA_DEVERR_DESCRIPTOR;
+    if (ch.src_offset < 0 || ch.src_offset + (int64_t)max(ch.len, 0) > p.num_rows)
+        bits |= KAMERA_DEVERR_SOURCE;
+    if (ch.len > p.max_len)
+        bits |= KAMERA_DEVERR_LEN;
+    if (ch.rank > p.max_rank)
+        bits |= KAMERA_DEVERR_RANK;
+    if (ch.rank > 0) {
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const uintptr_t a = reinterpret_cast<uintptr_t>(patch_ptr(ch, i));
+            if (a == 0 || (a & 15))
+                bits |= KAMERA_DEVERR_DESCRIPTOR;
+        }
+    }
+    return bits;
+}
+
+// The sequence's chunk range, [c0, c1); empty if d_seq_start is malformed.
+__device__ __forceinline__ void seq_chunks(const PrefillParams& p, int seq, int& c0, int& c1)
+{
+    c0 = p.seq_start[seq];
+    c1 = p.seq_start[seq + 1];
+    if (c0 < 0 || c1 < c0 || c1 > p.n_chunks)
+        c0 = c1 = 0;
+}
+
+// Waits for a phase whatever the abort flag says, up to `limit` ns: the drain
+// of copies and MMAs a role started before it leaves.
+__device__ __forceinline__ void pf_drain_wait(uint32_t bar, uint32_t parity, uint64_t limit)
+{
+    const uint64_t t0 = ptx::globaltimer();
+    while (!ptx::mbar_try_wait(bar, parity))
+        if (ptx::globaltimer() - t0 > limit)
+            return;
+}
+
+// Rows [0, ntok) of an m-wide factor block (`src`: its first row) into a tile
+// of 64 rows x 64 ranks (128B-swizzled); the ranks past m and the rows past
+// ntok zero.
+__device__ __forceinline__ void pf_load_u(uint32_t dst, const __nv_bfloat16* src, int m, int ntok, int lane)
+{
+    if ((m & 7) == 0) {
+        const int vpr = m >> 3, nv = ntok * vpr;   // the block's rows are contiguous: nv 16-byte pieces
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        for (int e0 = lane; e0 < nv; e0 += 128) {
+            uint4 v[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k)
+                if (e0 + 32 * k < nv)
+                    v[k] = __ldg(s4 + e0 + 32 * k);
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const int e = e0 + 32 * k;
+                if (e < nv) {
+                    const int r = e / vpr, c = e - r * vpr;
+                    ptx::sts128(dst + sw128(r, c), v[k].x, v[k].y, v[k].z, v[k].w);
+                }
+            }
+        }
+        for (int e = lane; e < kPfTok * 8; e += 32) {
+            const int r = e >> 3, c = e & 7;
+            if (r >= ntok || c >= vpr)
+                ptx::st_shared_zero16(dst + sw128(r, c));
+        }
+    } else {   // ranks that are not whole 16-byte pieces: element loads
+        const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
+        for (int e = lane; e < kPfTok * 8; e += 32) {
+            const int r = e >> 3, c = e & 7;
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (r < ntok) {
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const int j = 8 * c + k;
+                    if (j < m)
+                        w[k >> 1] |= (uint32_t)__ldg(s16 + (int64_t)r * m + j) << (16 * (k & 1));
+                }
+            }
+            ptx::sts128(dst + sw128(r, c), w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// The producer warp: every tile of the unit, in order, into the ring.
+template <int D>
+__device__ void pf_producer(const PrefillLaunch& P, uint32_t sbase, PfBars& b, int seq, int h, int lane)
+{
+    using L = PfLayout<D>;
+    const PrefillParams& p = P.p;
+    int c0, c1;
+    seq_chunks(p, seq, c0, c1);
+    uint32_t n = 0;   // tiles started
+    bool ok = true;
+    for (int c = c0; c < c1 && ok; ++c) {
+        const KameraChunk& ch = p.chunks[c];
+        if (prefill_check(ch, c, p))
+            continue;
+        const int len = ch.len, m = ch.rank, nt = (len + kPfTok - 1) / kPfTok;
+        const int64_t fo = (int64_t)(p.layer * p.H + h) * len * m;   // U [L][H][len][m]
+        for (int tl = 0; tl < nt; ++tl, ++n) {
+            const int st = (int)(n % L::NS);
+            if (n >= (uint32_t)L::NS) {   // the MMAs of tile n - NS are done with the stage
+                bool got = true;
+                if (lane == 0)
+                    got = wmma16::tile_wait(ptx::smem_addr(&b.empty[st]), ((n / L::NS) & 1u) ^ 1u, &b.abort, p.err,
+                                            P.wait_ns);
+                if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) {
+                    ok = false;
+                    break;
+                }
+            }
+            const uint32_t s0 = sbase + st * L::kStage, full = ptx::smem_addr(&b.full[st]);
+            const int j0 = tl * kPfTok, ntok = min(kPfTok, len - j0);
+            const bool tail = ntok < kPfTok;
+            if (lane == 0 && !P.withhold) {
+                const int y = (int)(ch.src_offset + j0);
+                ptx::mbar_arrive_expect_tx(full, (tail ? 1u : 2u) * L::NB * kBox);
+#pragma unroll
+                for (int x = 0; x < L::NB; ++x)
+                    ptx::tma_load_2d(s0 + L::kK + x * kBox, &P.map_k, h * D + 64 * x, y, full);
+                if (!tail) {
+#pragma unroll
+                    for (int x = 0; x < L::NB; ++x)
+                        ptx::tma_load_2d(s0 + L::kV + x * kBox, &P.map_v, h * D + 64 * x, y, full);
+                }
+            }
+            if (m > 0) {
+                pf_load_u(s0 + L::kU, patch_ptr(ch, 0) + fo + (int64_t)j0 * m, m, ntok, lane);
+                pf_load_u(s0 + L::kU2, patch_ptr(ch, 2) + fo + (int64_t)j0 * m, m, ntok, lane);
+            }
+            if (tail) {   // the chunk's last value rows by loads, zero past the chunk
+                const __nv_bfloat16* vr = p.v + (ch.src_offset + j0) * p.row_stride + (int64_t)h * D;
+                for (int e = lane; e < kPfTok * 8 * L::NB; e += 32) {
+                    const int r = e / (8 * L::NB), x = (e >> 3) % L::NB, c = e & 7;
+                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    if (r < ntok)
+                        v = __ldg(reinterpret_cast<const uint4*>(vr + (int64_t)r * p.row_stride + 64 * x + 8 * c));
+                    ptx::sts128(s0 + L::kV + x * kBox + sw128(r, c), v.x, v.y, v.z, v.w);
+                }
+            }
+            ptx::fence_proxy_async();   // the stores above, visible to the MMAs
+            ptx::mbar_arrive(full);
+        }
+    }
+    // the copies this warp started land before the CTA leaves
+    if (lane == 0)
+        for (uint32_t k = n > (uint32_t)L::NS ? n - L::NS : 0u; k < n; ++k)
+            pf_drain_wait(ptx::smem_addr(&b.full[k % L::NS]), (k / L::NS) & 1u, P.wait_ns);
+    __syncwarp();
+}
+
+// The MMA lane.  Per tile n: S(n) = [Q'hi | Q'lo | Xhi | Xlo] [k | k | u | u]^T
+// into the S columns of n & 1, then [O_v | O_u] += [Phi | Plo] [v | u'] of tile
+// n - 1.  MMAs of one thread run in issue order, so S(n + 1), issued after the
+// P v of tile n - 1, never overwrites a P that is still to be read.
+template <int D>
+__device__ void pf_mma(const PrefillLaunch& P, uint32_t sbase, PfBars& b, uint32_t tm, int seq)
+{
+    using L = PfLayout<D>;
+    const PrefillParams& p = P.p;
+    constexpr uint32_t idS = ptx::idesc_bf16_f32(kPfRows, kPfTok);
+    constexpr uint32_t idV = ptx::idesc_bf16_f32(kPfRows, D) | (1u << 16);        // B (value rows) MN-major
+    constexpr uint32_t idU = ptx::idesc_bf16_f32(kPfRows, kPfMP) | (1u << 16);    // B (U' rows) MN-major
+    int c0, c1;
+    seq_chunks(p, seq, c0, c1);
+    // P v (and P u' when the chunk has a patch) of tile i, its stage st; `first`:
+    // the chunk's first tile (O_u starts from zero there)
+    auto pv = [&](uint32_t i, int st, int m, bool first) -> bool {
+        if (!wmma16::tile_wait(ptx::smem_addr(&b.p_full[i & 1]), (i >> 1) & 1u, &b.abort, p.err, P.wait_ns))
+            return false;
+        ptx::tc_fence_after();
+        const uint32_t s0 = sbase + st * L::kStage, aP = tm + L::kTmS + (i & 1) * kPfTok;
+#pragma unroll
+        for (int ks = 0; ks < kPfTok / 16; ++ks)
+            umma_ts(tm + L::kTmOv, aP + 8 * ks, desc_mn_sw128(s0 + L::kV + 2048 * ks, kBox), idV,
+                    (i > 0 || ks > 0) ? 1u : 0u);
+#pragma unroll
+        for (int ks = 0; ks < kPfTok / 16; ++ks)
+            umma_ts(tm + L::kTmOv, aP + kPfTok / 2 + 8 * ks, desc_mn_sw128(s0 + L::kV + 2048 * ks, kBox), idV, 1u);
+        if (m > 0) {
+#pragma unroll
+            for (int ks = 0; ks < kPfTok / 16; ++ks)
+                umma_ts(tm + L::kTmOu, aP + 8 * ks, desc_mn_sw128(s0 + L::kU2 + 2048 * ks, kBox), idU,
+                        (first && ks == 0) ? 0u : 1u);
+#pragma unroll
+            for (int ks = 0; ks < kPfTok / 16; ++ks)
+                umma_ts(tm + L::kTmOu, aP + kPfTok / 2 + 8 * ks, desc_mn_sw128(s0 + L::kU2 + 2048 * ks, kBox), idU,
+                        1u);
+        }
+        ptx::umma_commit(ptx::smem_addr(&b.pv_done[i & 1]));
+        ptx::umma_commit(ptx::smem_addr(&b.empty[st]));
+        return true;
+    };
+    uint32_t n = 0, k = 0;   // tiles, chunks
+    int pst = 0, pm = 0;
+    bool pfirst = false, ok = true;
+    for (int c = c0; c < c1 && ok; ++c) {
+        const KameraChunk& ch = p.chunks[c];
+        if (prefill_check(ch, c, p))
+            continue;
+        const int m = ch.rank, nt = (ch.len + kPfTok - 1) / kPfTok, ksu = (m + 15) / 16;
+        for (int tl = 0; tl < nt; ++tl, ++n) {
+            if (tl == 0) {   // the chunk's Q' and X are in TMEM
+                if (!wmma16::tile_wait(ptx::smem_addr(&b.a_ready), k & 1u, &b.abort, p.err, P.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                ++k;
+            }
+            const int st = (int)(n % L::NS);
+            if (!wmma16::tile_wait(ptx::smem_addr(&b.full[st]), (n / L::NS) & 1u, &b.abort, p.err, P.wait_ns)) {
+                ok = false;
+                break;
+            }
+            ptx::tc_fence_after();
+            const uint32_t s0 = sbase + st * L::kStage, dS = tm + L::kTmS + (n & 1) * kPfTok;
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                umma_ts(dS, tm + L::kTmQh + 8 * ks, ptx::desc_k_sw128(s0 + L::kK + (ks >> 2) * kBox + 32 * (ks & 3)),
+                        idS, ks > 0 ? 1u : 0u);
+#pragma unroll
+            for (int ks = 0; ks < D / 16; ++ks)
+                umma_ts(dS, tm + L::kTmQl + 8 * ks, ptx::desc_k_sw128(s0 + L::kK + (ks >> 2) * kBox + 32 * (ks & 3)),
+                        idS, 1u);
+            for (int ks = 0; ks < ksu; ++ks) {
+                umma_ts(dS, tm + L::kTmXh + 8 * ks, ptx::desc_k_sw128(s0 + L::kU + 32 * ks), idS, 1u);
+                umma_ts(dS, tm + L::kTmXl + 8 * ks, ptx::desc_k_sw128(s0 + L::kU + 32 * ks), idS, 1u);
+            }
+            ptx::umma_commit(ptx::smem_addr(&b.s_full[n & 1]));
+            if (n > 0 && !pv(n - 1, pst, pm, pfirst)) {
+                ok = false;
+                break;
+            }
+            pst = st;
+            pm = m;
+            pfirst = tl == 0;
+        }
+    }
+    if (ok && n > 0)
+        pv(n - 1, pst, pm, pfirst);
+    // every MMA issued here completes before TMEM is freed
+    ptx::umma_commit(ptx::smem_addr(&b.drained));
+    pf_drain_wait(ptx::smem_addr(&b.drained), 0u, P.wait_ns);
+}
+
+// An m-wide V factor block [d][m] (`src`) into a [d][64] bf16 array of 128-byte
+// rows, the ranks past m up to the next multiple of 8 zero (128 threads).
+template <int D>
+__device__ __forceinline__ void pf_stage_v(uint32_t dst, const __nv_bfloat16* src, int m, int r)
+{
+    const int vpr = (m + 7) >> 3;
+    if ((m & 7) == 0) {
+        const uint4* s4 = reinterpret_cast<const uint4*>(src);
+        for (int e = r; e < D * vpr; e += kPfRows) {
+            const uint4 v = __ldg(s4 + e);
+            const int i = e / vpr, c = e - i * vpr;
+            ptx::sts128(dst + i * 128 + 16 * c, v.x, v.y, v.z, v.w);
+        }
+    } else {
+        const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
+        for (int e = r; e < D * vpr; e += kPfRows) {
+            const int i = e / vpr, c = e - i * vpr;
+            uint32_t w[4] = {0u, 0u, 0u, 0u};
+#pragma unroll
+            for (int k = 0; k < 8; ++k) {
+                const int j = 8 * c + k;
+                if (j < m)
+                    w[k >> 1] |= (uint32_t)__ldg(s16 + (int64_t)i * m + j) << (16 * (k & 1));
+            }
+            ptx::sts128(dst + i * 128 + 16 * c, w[0], w[1], w[2], w[3]);
+        }
+    }
+}
+
+// O_v += O_u V_v^T for this thread's row: the value patch of the chunk just
+// finished (O_u = sum_j p_j u'_j, ranks past m zero), V_v staged at `vv`.
+template <int D>
+__device__ __forceinline__ void pf_fold(uint32_t lane_base, uint32_t vv, int m)
+{
+    using L = PfLayout<D>;
+    const int mb = (m + 7) >> 3;
+#pragma unroll 1
+    for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + L::kTmOv + 32 * cb, o);
+#pragma unroll 1
+        for (int jb = 0; jb < mb; ++jb) {
+            uint32_t w8[8];
+            tmem_ld8(lane_base + L::kTmOu + 8 * jb, w8);
+#pragma unroll
+            for (int c = 0; c < 32; ++c) {
+                uint32_t v[4];
+                ptx::lds128(vv + (32 * cb + c) * 128 + 16 * jb, v);
+                float a = __uint_as_float(o[c]);
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    a = fmaf(__uint_as_float(w8[2 * k]), bf16lo(v[k]), a);
+                    a = fmaf(__uint_as_float(w8[2 * k + 1]), bf16hi(v[k]), a);
+                }
+                o[c] = __float_as_uint(a);
+            }
+        }
+        tmem_st32(lane_base + L::kTmOv + 32 * cb, o);
+    }
+    tmem_wait_st();
+}
+
+// O_v (and O_u when `with_u`) times f, in TMEM, for this thread's row.
+template <int D>
+__device__ __forceinline__ void pf_rescale(uint32_t lane_base, float f, bool with_u)
+{
+    using L = PfLayout<D>;
+#pragma unroll 1
+    for (int cb = 0; cb < (D + (with_u ? kPfMP : 0)) / 32; ++cb) {
+        uint32_t o[32];
+        tmem_ld32(lane_base + L::kTmOv + 32 * cb, o);   // O_u follows O_v
+#pragma unroll
+        for (int c = 0; c < 32; ++c)
+            o[c] = __float_as_uint(__uint_as_float(o[c]) * f);
+        tmem_st32(lane_base + L::kTmOv + 32 * cb, o);
+    }
+    tmem_wait_st();
+}
+
+// The softmax warps: thread r holds query row blk * 128 + r (TMEM lane r).
+// Waits that run out (abort) make the rest of the loops run without waiting,
+// so the four warps still meet at every barrier among them.
+template <int D>
+__device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, uint32_t tm, int seq, int h, int blk,
+                           int r)
+{
+    using L = PfLayout<D>;
+    const PrefillParams& p = P.p;
+    const RopeParams& rp = p.rope;
+    const int G = p.G, HQ = p.H * G;
+    const int row = blk * kPfRows + r;
+    const bool valid = row < p.T * G;
+    const int tok = valid ? row / G : 0, gq = valid ? row - (row / G) * G : 0;
+    const int64_t qoff = (((int64_t)seq * p.T + tok) * HQ + (int64_t)h * G + gq) * D;
+    const __nv_bfloat16* qg = p.q + qoff;
+    const uint16_t* qg16 = reinterpret_cast<const uint16_t*>(qg);
+    const uint32_t lane_base = tm + ((uint32_t)(r & ~31) << 16);   // this warp's 32 TMEM lanes
+    const uint32_t vk = sbase + L::kVk, vv = sbase + L::kVv;
+    float2* cs = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(&b) - L::kBar + L::kCs);
+    const float sl2 = p.scale * 1.4426950408889634f;   // scores in log2 units
+    const int ro = rp.rot_offset, rr = rp.rot_dim, half = rr / 2;
+    const bool rot_half = rp.pairing == KAMERA_ROPE_ROTATE_HALF;
+    float m_run = -INFINITY, l_run = 0.f;
+    int c0, c1;
+    seq_chunks(p, seq, c0, c1);
+    if (r == 0 && blk == 0 && h == 0 && (p.seq_start[seq] != c0 || p.seq_start[seq + 1] != c1))
+        raise_err(p.err, KAMERA_DEVERR_DESCRIPTOR);
+    uint32_t n = 0;   // tiles
+    int prev_m = -1;  // rank of the previous chunk (-1: none yet)
+    for (int c = c0; c < c1; ++c) {
+        const KameraChunk& ch = p.chunks[c];
+        const int32_t bad = prefill_check(ch, c, p);
+        if (bad) {
+            if (r == 0 && blk == 0 && h == 0)
+                raise_err(p.err, bad);
+            continue;
+        }
+        const int len = ch.len, m = ch.rank, nt = (len + kPfTok - 1) / kPfTok;
+        if (nt == 0)
+            continue;
+        const int64_t fv = (int64_t)(p.layer * p.H + h) * D * m;   // V factors [L][H][d][m]
+        // ---- the chunk's query part: Q' = R(-delta) q and X = V_k^T q
+        bar_softmax();   // every thread is done with the previous chunk's V_k and cos/sin
+        for (int f = r; f < rp.n_freq; f += kPfRows) {
+            float cc, sn;
+            phase_cos_sin(-freq_delta(rp, ch, c, f), rp.inv_freq[f], cc, sn);
+            cs[f] = make_float2(cc, sn);
+        }
+        if (m > 0)
+            pf_stage_v<D>(vk, patch_ptr(ch, 1) + fv, m, r);
+        bar_softmax();
+        uint32_t qv[D / 2];   // the query row, bf16 pairs (zero for rows past T x G), read again per chunk
+#pragma unroll
+        for (int i = 0; i < D / 8; ++i) {
+            uint4 x = make_uint4(0u, 0u, 0u, 0u);
+            if (valid)
+                x = __ldg(reinterpret_cast<const uint4*>(qg) + i);
+            qv[4 * i] = x.x;
+            qv[4 * i + 1] = x.y;
+            qv[4 * i + 2] = x.z;
+            qv[4 * i + 3] = x.w;
+        }
+#pragma unroll
+        for (int piece = 0; piece < D / 64; ++piece) {
+            uint32_t hi[32], lo[32];
+#pragma unroll
+            for (int cc = 0; cc < 32; ++cc) {
+                float v2[2];
+#pragma unroll
+                for (int e = 0; e < 2; ++e) {
+                    const int i = 64 * piece + 2 * cc + e;
+                    float v = e ? bf16hi(qv[i >> 1]) : bf16lo(qv[i >> 1]);
+                    const int kk = i - ro;
+                    if (kk >= 0 && kk < rr) {
+                        int f, pi;
+                        bool neg;
+                        if (rot_half) {
+                            neg = kk < half;
+                            f = neg ? kk : kk - half;
+                            pi = neg ? i + half : i - half;
+                        } else {
+                            neg = (kk & 1) == 0;
+                            f = kk >> 1;
+                            pi = neg ? i + 1 : i - 1;
+                        }
+                        const float2 t = cs[f];
+                        const float pv = valid ? __uint_as_float((uint32_t)__ldg(qg16 + pi) << 16) : 0.f;
+                        v = fmaf(v, t.x, neg ? -(pv * t.y) : pv * t.y);
+                    }
+                    v2[e] = v;
+                }
+                wmma16::split_hl(v2[0], v2[1], hi[cc], lo[cc]);
+            }
+            tmem_st32(lane_base + L::kTmQh + 32 * piece, hi);
+            tmem_st32(lane_base + L::kTmQl + 32 * piece, lo);
+        }
+        {
+            const int mb = (m + 7) >> 3;
+#pragma unroll 1
+            for (int jb = 0; jb < kPfMP / 8; ++jb) {
+                uint32_t xh[4] = {0u, 0u, 0u, 0u}, xl[4] = {0u, 0u, 0u, 0u};
+                if (jb < mb) {
+                    float acc[8];
+#pragma unroll
+                    for (int k = 0; k < 8; ++k)
+                        acc[k] = 0.f;
+#pragma unroll
+                    for (int i = 0; i < D; ++i) {
+                        const float qi = (i & 1) ? bf16hi(qv[i >> 1]) : bf16lo(qv[i >> 1]);
+                        uint32_t w[4];
+                        ptx::lds128(vk + i * 128 + 16 * jb, w);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            acc[2 * k] = fmaf(qi, bf16lo(w[k]), acc[2 * k]);
+                            acc[2 * k + 1] = fmaf(qi, bf16hi(w[k]), acc[2 * k + 1]);
+                        }
+                    }
+#pragma unroll
+                    for (int k = 0; k < 4; ++k)
+                        wmma16::split_hl(acc[2 * k], acc[2 * k + 1], xh[k], xl[k]);
+                }
+                tmem_st4(lane_base + L::kTmXh + 4 * jb, xh[0], xh[1], xh[2], xh[3]);
+                tmem_st4(lane_base + L::kTmXl + 4 * jb, xl[0], xl[1], xl[2], xl[3]);
+            }
+        }
+        tmem_wait_st();
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_addr(&b.a_ready));
+        // ---- the previous chunk's value patch, once its last P u' is done
+        if (prev_m >= 0) {
+            wmma16::tile_wait(ptx::smem_addr(&b.pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1u, &b.abort, p.err,
+                              P.wait_ns);
+            ptx::tc_fence_after();
+            if (prev_m > 0)
+                pf_fold<D>(lane_base, vv, prev_m);
+        }
+        bar_softmax();   // the fold is done with the previous V_v
+        if (m > 0)
+            pf_stage_v<D>(vv, patch_ptr(ch, 3) + fv, m, r);
+        bar_softmax();
+        // ---- the tiles
+        for (int tl = 0; tl < nt; ++tl, ++n) {
+            const int ntok = min(kPfTok, len - tl * kPfTok);
+            const uint32_t sb = L::kTmS + (n & 1) * kPfTok;
+            wmma16::tile_wait(ptx::smem_addr(&b.s_full[n & 1]), (n >> 1) & 1u, &b.abort, p.err, P.wait_ns);
+            ptx::tc_fence_after();
+            uint32_t s0[32], s1[32];   // the S row; scores in log2 units in place
+            tmem_ld32(lane_base + sb, s0);
+            tmem_ld32(lane_base + sb + 32, s1);
+            float mt = -INFINITY;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const float a0 = j < ntok ? __uint_as_float(s0[j]) * sl2 : -INFINITY;
+                const float a1 = j + 32 < ntok ? __uint_as_float(s1[j]) * sl2 : -INFINITY;
+                s0[j] = __float_as_uint(a0);
+                s1[j] = __float_as_uint(a1);
+                mt = fmaxf(mt, fmaxf(a0, a1));
+            }
+            const float m_new = fmaxf(m_run, mt);
+            if (n == 0) {
+                m_run = m_new;   // O is still empty
+            } else if (__any_sync(0xFFFFFFFFu, m_new > m_run + kPfLazy)) {
+                const float f = exp2f(m_run - m_new);
+                l_run *= f;
+                m_run = m_new;
+                wmma16::tile_wait(ptx::smem_addr(&b.pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1u, &b.abort, p.err,
+                                  P.wait_ns);
+                ptx::tc_fence_after();
+                pf_rescale<D>(lane_base, f, m > 0 && tl > 0);
+            }
+            uint32_t ph[32], pl[32];
+            float sum = 0.f;
+#pragma unroll
+            for (int j = 0; j < 32; ++j) {
+                const uint32_t* src = j < 16 ? s0 : s1;
+                const int jj = 2 * (j & 15);
+                const float p0 = exp2f(__uint_as_float(src[jj]) - m_run);
+                const float p1 = exp2f(__uint_as_float(src[jj + 1]) - m_run);
+                sum += p0 + p1;
+                wmma16::split_hl(p0, p1, ph[j], pl[j]);
+            }
+            l_run += sum;
+            tmem_st32(lane_base + sb, ph);
+            tmem_st32(lane_base + sb + kPfTok / 2, pl);
+            tmem_wait_st();
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_addr(&b.p_full[n & 1]));
+        }
+        prev_m = m;
+    }
+    // ---- the end: the last value patch, then out = O_v / l and the log-sum-exp
+    if (n > 0) {
+        wmma16::tile_wait(ptx::smem_addr(&b.pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1u, &b.abort, p.err, P.wait_ns);
+        ptx::tc_fence_after();
+        if (prev_m > 0)
+            pf_fold<D>(lane_base, vv, prev_m);
+    }
+    const float inv = n > 0 ? 1.f / l_run : 0.f;
+    __nv_bfloat16* og = p.out + qoff;
+#pragma unroll 1
+    for (int cb = 0; cb < D / 32; ++cb) {
+        uint32_t o[32];
+        if (n > 0) {
+            tmem_ld32(lane_base + L::kTmOv + 32 * cb, o);
+        } else {
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                o[c] = 0u;
+        }
+        if (valid && !*static_cast<volatile int32_t*>(&b.abort)) {
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                uint32_t w[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    w[k] = pack_bf16x2(__uint_as_float(o[8 * q + 2 * k]) * inv, __uint_as_float(o[8 * q + 2 * k + 1]) * inv);
+                ptx::stg128(og + 32 * cb + 8 * q, w);
+            }
+        }
+    }
+    if (valid && p.lse != nullptr)
+        p.lse[((int64_t)seq * p.T + tok) * HQ + (int64_t)h * G + gq] =
+            n > 0 ? (m_run + log2f(l_run)) * 0.6931471805599453f : -INFINITY;
+}
+
+// One CTA per unit u = (sequence, KV head, 128-row block), the block fastest so
+// the CTAs that read the same rows run together and share them in L2.
+template <int D>
+__global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_constant__ PrefillLaunch P)
+{
+    using L = PfLayout<D>;
+    const PrefillParams& p = P.p;
+    extern __shared__ __align__(16) unsigned char smem_raw[];
+    const uint32_t raw = ptx::smem_addr(smem_raw);
+    const uint32_t pad = (1024u - (raw & 1023u)) & 1023u;   // swizzled tiles sit on 1024-byte boundaries
+    const uint32_t sbase = raw + pad;
+    PfBars& b = *reinterpret_cast<PfBars*>(smem_raw + pad + L::kBar);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int64_t u = blockIdx.x;
+    const int blk = (int)(u % p.blocks), h = (int)((u / p.blocks) % p.H);
+    const int seq = (int)(u / ((int64_t)p.blocks * p.H));
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::NS; ++s) {
+            ptx::mbar_init(ptx::smem_addr(&b.full[s]), 1 + 32);   // the TMA issue + the warp's stores
+            ptx::mbar_init(ptx::smem_addr(&b.empty[s]), 1);
+        }
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(ptx::smem_addr(&b.s_full[i]), 1);
+            ptx::mbar_init(ptx::smem_addr(&b.p_full[i]), kPfRows);
+            ptx::mbar_init(ptx::smem_addr(&b.pv_done[i]), 1);
+        }
+        ptx::mbar_init(ptx::smem_addr(&b.a_ready), kPfRows);
+        ptx::mbar_init(ptx::smem_addr(&b.drained), 1);
+        b.abort = 0;
+        ptx::fence_barrier_init();
+    }
+    if (warp == kPfProd && lane == 0) {
+        ptx::prefetch_tmap(&P.map_k);
+        ptx::prefetch_tmap(&P.map_v);
+    }
+    if (warp == kPfMma) {
+        ptx::tmem_alloc(ptx::smem_addr(&b.tmem), 512);
+        ptx::tmem_relinquish();
+    }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tm = b.tmem;
+
+    if (warp < 4)
+        pf_softmax<D>(P, sbase, b, tm, seq, h, blk, threadIdx.x);
+    else if (warp == kPfProd)
+        pf_producer<D>(P, sbase, b, seq, h, lane);
+    else if (lane == 0)
+        pf_mma<D>(P, sbase, b, tm, seq);
+
+    ptx::tc_fence_before();
+    __syncthreads();
+    if (warp == kPfMma) {
+        ptx::tc_fence_after();
+        ptx::tmem_dealloc(tm, 512);
+    }
+}
+
+template <int D>
+cudaError_t launch_prefill_d(const PrefillParams& p, cudaStream_t stream)
+{
+    using L = PfLayout<D>;
+    PrefillLaunch P;
+    std::memset(&P, 0, sizeof(P));
+    P.p = p;
+    P.wait_ns = wait_limit_ns();
+    P.withhold = test_withhold_loads() ? 1 : 0;
+    const int64_t width = (int64_t)p.H * D;
+    if (!make_rows_map(&P.map_k, p.k, p.num_rows, width, p.row_stride, 64, kPfTok) ||
+        !make_rows_map(&P.map_v, p.v, p.num_rows, width, p.row_stride, 64, kPfTok))
+        return cudaErrorInvalidValue;
+    static bool attr_done = false;   // per process: the attribute is per function, not per device
+    if (!attr_done) {
+        const cudaError_t e =
+            cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
+        if (e != cudaSuccess)
+            return e;
+        attr_done = true;
+    }
+    const int64_t units = (int64_t)p.n_seqs * p.H * p.blocks;
+    prefill_kernel<D><<<(unsigned)units, kPfThreads, L::kBytes, stream>>>(P);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool prefill_supported(int head_dim, int max_rank)
+{
+    return (head_dim == 64 || head_dim == 128) && max_rank >= 0 && max_rank <= kPfMP;
+}
+
+cudaError_t launch_prefill(const PrefillParams& p, cudaStream_t stream)
+{
+    if ((int64_t)p.n_seqs * p.H * p.blocks < 1)
+        return cudaSuccess;
+    return p.d == 128 ? launch_prefill_d<128>(p, stream) : launch_prefill_d<64>(p, stream);
+}
+
+}  // namespace kamera

@@ -370,6 +370,7 @@ class AttendSpec:
     dmax: int = 32768
     zero_rank_every: int = 0   # > 0: every n-th chunk carries no patch
     kind: str = "attend"
+    T: int = 0                 # > 0: prefill, T query tokens per sequence (q [S, T, H * G, d])
 
 
 @dataclass
@@ -419,8 +420,34 @@ def make_attend(spec: AttendSpec, device="cpu") -> AttendData:
             off += t
             idx += 1
         seq_start.append(len(chunks))
-    q = _randn_bf16((len(spec.seqs), spec.H * spec.G, spec.d), 1.0, gen, device)
+    qshape = (len(spec.seqs),) + ((spec.T,) if spec.T > 0 else ()) + (spec.H * spec.G, spec.d)
+    q = _randn_bf16(qshape, 1.0, gen, device)
     return AttendData(spec, store_k, store_v, chunks, seq_start, q)
+
+
+def qwen_prefill_reused() -> AttendSpec:
+    """A prefill over reused chunks, Qwen2.5-VL-7B shaped (4 KV heads, 28 query
+    heads, d = 128, base 1e6): 38 sequences, each recalling the 8-chunk batch
+    (8 x 1296 tokens, rank 32 on K and V) and bringing 256 new query tokens
+    that attend over it -- 256 x 7 = 1792 query rows per (sequence, KV head),
+    14 CTAs of 128 rows each."""
+    return AttendSpec("qwen_prefill_reused", H=4, G=7, d=128, seqs=tuple((1296,) * 8 for _ in range(38)), m=32,
+                      kind="prefill", T=256)
+
+
+def prefill_flops(spec: AttendSpec) -> int:
+    """Floating-point operations of prefill attention in the folded form (the
+    rows are never formed): per query row and token, 2 (d + m) for the score
+    (q'.k + x.u) and 2 (d + m) for the weighted sums (p v and p u'); per query
+    row and patched chunk, 2 d m for V_k^T q and 2 d m for the V_v fold."""
+    rows = spec.T * spec.H * spec.G * len(spec.seqs)
+    per_seq_tok = [sum(seq) for seq in spec.seqs]
+    per_seq_ch = [sum(1 for t in seq if t > 0) for seq in spec.seqs]
+    rows_per_seq = spec.T * spec.H * spec.G
+    tok = sum(rows_per_seq * t for t in per_seq_tok)
+    ch = sum(rows_per_seq * c for c in per_seq_ch)
+    assert rows == rows_per_seq * len(spec.seqs)
+    return 4 * tok * (spec.d + spec.m) + 4 * ch * spec.d * spec.m
 
 
 def attend_bytes(spec: AttendSpec) -> int:
@@ -520,7 +547,8 @@ def mla_attend_bytes(spec: MlaAttendSpec) -> int:
     return (tok * (W + 2 * spec.m) + nch * W * spec.m + S * spec.Hq * (W + spec.kv_lora)) * B
 
 
-ATTENTION = {"qwen_attend_reused": qwen_attend_reused, "dsv2_attend_reused": dsv2_attend_reused}
+ATTENTION = {"qwen_attend_reused": qwen_attend_reused, "dsv2_attend_reused": dsv2_attend_reused,
+             "qwen_prefill_reused": qwen_prefill_reused}
 
 
 # ------------------------------------------------------------- workloads --
