@@ -218,53 +218,61 @@ __device__ __forceinline__ void pf_drain_wait(uint32_t bar, uint32_t parity, uin
             return;
 }
 
-// Rows [0, ntok) of an m-wide factor block (`src`: its first row) into a tile
-// of 64 rows x 64 ranks (128B-swizzled); the ranks past m and the rows past
-// ntok zero.
-__device__ __forceinline__ void pf_load_u(uint32_t dst, const __nv_bfloat16* src, int m, int ntok, int lane)
+// Rows [0, ntok) of the tile's U and U' blocks (m-wide factor rows, `uk` and
+// `uv`: the tile's first row) into 64 x 64-rank tiles (128B-swizzled), by
+// 16-byte async copies when m is a multiple of 8, else by element loads.  Only
+// what an MMA reads must be finite: U' rows past ntok (zero weights times the
+// row) and, in both, the ranks from m up to the next multiple of 16 (zero
+// query parts and zero V_v columns times them); those are written as zeros.
+// Other padding is left as it is: it reaches only masked scores or O_u columns
+// past m, which nothing reads.
+__device__ __forceinline__ void pf_load_u(uint32_t du, uint32_t dv, const __nv_bfloat16* uk,
+                                          const __nv_bfloat16* uv, int m, int ntok, int lane)
 {
+    const int vpr = (m + 7) >> 3, vp16 = 2 * ((m + 15) >> 4);   // pieces with data / read by the S MMAs
     if ((m & 7) == 0) {
-        const int vpr = m >> 3, nv = ntok * vpr;   // the block's rows are contiguous: nv 16-byte pieces
-        const uint4* s4 = reinterpret_cast<const uint4*>(src);
-        for (int e0 = lane; e0 < nv; e0 += 128) {
-            uint4 v[4];
-#pragma unroll
-            for (int k = 0; k < 4; ++k)
-                if (e0 + 32 * k < nv)
-                    v[k] = __ldg(s4 + e0 + 32 * k);
-#pragma unroll
-            for (int k = 0; k < 4; ++k) {
-                const int e = e0 + 32 * k;
-                if (e < nv) {
-                    const int r = e / vpr, c = e - r * vpr;
-                    ptx::sts128(dst + sw128(r, c), v[k].x, v[k].y, v[k].z, v[k].w);
-                }
+        const int nv = ntok * vpr;   // the block's rows are contiguous: nv 16-byte pieces
+        for (int e = lane; e < nv; e += 32) {
+            const int r = e / vpr, c = e - r * vpr;
+            ptx::cp_async16(du + sw128(r, c), uk + 8 * e);
+            ptx::cp_async16(dv + sw128(r, c), uv + 8 * e);
+        }
+        if (vp16 > vpr)
+            for (int e = lane; e < kPfTok; e += 32) {
+                ptx::st_shared_zero16(du + sw128(e, vpr));
+                ptx::st_shared_zero16(dv + sw128(e, vpr));
             }
-        }
+        for (int e = ntok * 8 + lane; e < kPfTok * 8; e += 32)
+            ptx::st_shared_zero16(dv + sw128(e >> 3, e & 7));
+    } else {   // ranks that are not whole 16-byte pieces
+        const uint16_t* k16 = reinterpret_cast<const uint16_t*>(uk);
+        const uint16_t* v16 = reinterpret_cast<const uint16_t*>(uv);
         for (int e = lane; e < kPfTok * 8; e += 32) {
             const int r = e >> 3, c = e & 7;
-            if (r >= ntok || c >= vpr)
-                ptx::st_shared_zero16(dst + sw128(r, c));
-        }
-    } else {   // ranks that are not whole 16-byte pieces: element loads
-        const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
-        for (int e = lane; e < kPfTok * 8; e += 32) {
-            const int r = e >> 3, c = e & 7;
-            uint32_t w[4] = {0u, 0u, 0u, 0u};
+            if (c >= vp16 && r < ntok)
+                continue;
+            uint32_t a[4] = {0u, 0u, 0u, 0u}, b[4] = {0u, 0u, 0u, 0u};
             if (r < ntok) {
 #pragma unroll
                 for (int k = 0; k < 8; ++k) {
                     const int j = 8 * c + k;
-                    if (j < m)
-                        w[k >> 1] |= (uint32_t)__ldg(s16 + (int64_t)r * m + j) << (16 * (k & 1));
+                    if (j < m) {
+                        a[k >> 1] |= (uint32_t)__ldg(k16 + (int64_t)r * m + j) << (16 * (k & 1));
+                        b[k >> 1] |= (uint32_t)__ldg(v16 + (int64_t)r * m + j) << (16 * (k & 1));
+                    }
                 }
             }
-            ptx::sts128(dst + sw128(r, c), w[0], w[1], w[2], w[3]);
+            ptx::sts128(du + sw128(r, c), a[0], a[1], a[2], a[3]);
+            ptx::sts128(dv + sw128(r, c), b[0], b[1], b[2], b[3]);
         }
     }
 }
 
-// The producer warp: every tile of the unit, in order, into the ring.
+// The producer warp: every tile of the unit, in order, into the ring.  The
+// key and value rows come by TMA (completion counted in bytes); the U rows
+// (and a partial tile's value rows) by async copies, whose landing the warp
+// waits for one tile later -- so two tiles' copies are in flight -- before it
+// makes them visible to the MMAs and arrives.
 template <int D>
 __device__ void pf_producer(const PrefillLaunch& P, uint32_t sbase, PfBars& b, int seq, int h, int lane)
 {
@@ -307,23 +315,32 @@ __device__ void pf_producer(const PrefillLaunch& P, uint32_t sbase, PfBars& b, i
                         ptx::tma_load_2d(s0 + L::kV + x * kBox, &P.map_v, h * D + 64 * x, y, full);
                 }
             }
-            if (m > 0) {
-                pf_load_u(s0 + L::kU, patch_ptr(ch, 0) + fo + (int64_t)j0 * m, m, ntok, lane);
-                pf_load_u(s0 + L::kU2, patch_ptr(ch, 2) + fo + (int64_t)j0 * m, m, ntok, lane);
-            }
-            if (tail) {   // the chunk's last value rows by loads, zero past the chunk
+            if (m > 0)
+                pf_load_u(s0 + L::kU, s0 + L::kU2, patch_ptr(ch, 0) + fo + (int64_t)j0 * m,
+                          patch_ptr(ch, 2) + fo + (int64_t)j0 * m, m, ntok, lane);
+            if (tail) {   // the chunk's last value rows by async copies, zero past the chunk
                 const __nv_bfloat16* vr = p.v + (ch.src_offset + j0) * p.row_stride + (int64_t)h * D;
                 for (int e = lane; e < kPfTok * 8 * L::NB; e += 32) {
-                    const int r = e / (8 * L::NB), x = (e >> 3) % L::NB, c = e & 7;
-                    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+                    const int r = e / (8 * L::NB), x = (e >> 3) % L::NB, c8 = e & 7;
+                    const uint32_t dst = s0 + L::kV + x * kBox + sw128(r, c8);
                     if (r < ntok)
-                        v = __ldg(reinterpret_cast<const uint4*>(vr + (int64_t)r * p.row_stride + 64 * x + 8 * c));
-                    ptx::sts128(s0 + L::kV + x * kBox + sw128(r, c), v.x, v.y, v.z, v.w);
+                        ptx::cp_async16(dst, vr + (int64_t)r * p.row_stride + 64 * x + 8 * c8);
+                    else
+                        ptx::st_shared_zero16(dst);
                 }
             }
-            ptx::fence_proxy_async();   // the stores above, visible to the MMAs
-            ptx::mbar_arrive(full);
+            ptx::cp_async_commit();
+            if (n > 0) {   // the previous tile's copies have landed: visible to the MMAs
+                ptx::cp_async_wait<1>();
+                ptx::fence_proxy_async();
+                ptx::mbar_arrive(ptx::smem_addr(&b.full[(n - 1) % L::NS]));
+            }
         }
+    }
+    ptx::cp_async_wait<0>();
+    if (n > 0) {
+        ptx::fence_proxy_async();
+        ptx::mbar_arrive(ptx::smem_addr(&b.full[(n - 1) % L::NS]));
     }
     // the copies this warp started land before the CTA leaves
     if (lane == 0)
