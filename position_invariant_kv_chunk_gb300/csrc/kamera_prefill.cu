@@ -505,6 +505,42 @@ __device__ __forceinline__ void pf_fold(uint32_t lane_base, uint32_t vv, int m)
     tmem_wait_st();
 }
 
+// 2^x (the MUFU approximation: relative error near 2^-22, subnormal results
+// flushed to zero).
+__device__ __forceinline__ float pf_ex2(float x)
+{
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// The largest (`neg`: smallest) of the row's first ntok raw scores.
+__device__ __forceinline__ float pf_extreme(const uint32_t (&a)[32], const uint32_t (&b)[32], int ntok, bool neg)
+{
+    float e = neg ? INFINITY : -INFINITY;
+    if (ntok >= kPfTok) {
+        if (neg) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                e = fminf(e, fminf(__uint_as_float(a[j]), __uint_as_float(b[j])));
+        } else {
+#pragma unroll
+            for (int j = 0; j < 32; ++j)
+                e = fmaxf(e, fmaxf(__uint_as_float(a[j]), __uint_as_float(b[j])));
+        }
+    } else {
+#pragma unroll
+        for (int j = 0; j < 32; ++j) {
+            const float x = __uint_as_float(a[j]), y = __uint_as_float(b[j]);
+            if (j < ntok)
+                e = neg ? fminf(e, x) : fmaxf(e, x);
+            if (j + 32 < ntok)
+                e = neg ? fminf(e, y) : fmaxf(e, y);
+        }
+    }
+    return e;
+}
+
 // O_v (and O_u when `with_u`) times f, in TMEM, for this thread's row.
 template <int D>
 __device__ __forceinline__ void pf_rescale(uint32_t lane_base, float f, bool with_u)
@@ -669,23 +705,16 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
             const uint32_t sb = L::kTmS + (n & 1) * kPfTok;
             wmma16::tile_wait(ptx::smem_addr(&b.s_full[n & 1]), (n >> 1) & 1u, &b.abort, p.err, P.wait_ns);
             ptx::tc_fence_after();
-            uint32_t s0[32], s1[32];   // the S row; scores in log2 units in place
+            uint32_t s0[32], s1[32];   // the S row (raw scores)
             tmem_ld32(lane_base + sb, s0);
             tmem_ld32(lane_base + sb + 32, s1);
-            float mt = -INFINITY;
-#pragma unroll
-            for (int j = 0; j < 32; ++j) {
-                const float a0 = j < ntok ? __uint_as_float(s0[j]) * sl2 : -INFINITY;
-                const float a1 = j + 32 < ntok ? __uint_as_float(s1[j]) * sl2 : -INFINITY;
-                s0[j] = __float_as_uint(a0);
-                s1[j] = __float_as_uint(a1);
-                mt = fmaxf(mt, fmaxf(a0, a1));
-            }
+            const bool tail = ntok < kPfTok;
+            const float mt = sl2 * pf_extreme(s0, s1, ntok, sl2 < 0.f);   // the tile's largest score, log2 units
             const float m_new = fmaxf(m_run, mt);
             if (n == 0) {
                 m_run = m_new;   // O is still empty
             } else if (__any_sync(0xFFFFFFFFu, m_new > m_run + kPfLazy)) {
-                const float f = exp2f(m_run - m_new);
+                const float f = pf_ex2(m_run - m_new);
                 l_run *= f;
                 m_run = m_new;
                 wmma16::tile_wait(ptx::smem_addr(&b.pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1u, &b.abort, p.err,
@@ -693,18 +722,34 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
                 ptx::tc_fence_after();
                 pf_rescale<D>(lane_base, f, m > 0 && tl > 0);
             }
+            // weights p_j = 2^(sl2 s_j - m) as bf16 hi + lo pairs; pairs of fp32 lanes at a time
             uint32_t ph[32], pl[32];
-            float sum = 0.f;
+            const uint64_t sl2x2 = ptx::f2_make(__float_as_uint(sl2), __float_as_uint(sl2));
+            const uint64_t nmx2 = ptx::f2_make(__float_as_uint(-m_run), __float_as_uint(-m_run));
+            const uint64_t neg1 = ptx::f2_make(__float_as_uint(-1.f), __float_as_uint(-1.f));
+            uint64_t sum2 = 0ull;
 #pragma unroll
             for (int j = 0; j < 32; ++j) {
                 const uint32_t* src = j < 16 ? s0 : s1;
-                const int jj = 2 * (j & 15);
-                const float p0 = exp2f(__uint_as_float(src[jj]) - m_run);
-                const float p1 = exp2f(__uint_as_float(src[jj + 1]) - m_run);
-                sum += p0 + p1;
-                wmma16::split_hl(p0, p1, ph[j], pl[j]);
+                const int jj = 2 * (j & 15), col = (j < 16 ? 0 : 32) + jj;
+                uint32_t a0, a1;
+                asm("mov.b64 {%0, %1}, %2;" : "=r"(a0), "=r"(a1)
+                    : "l"(ptx::f2_fma(ptx::f2_make(src[jj], src[jj + 1]), sl2x2, nmx2)));
+                float p0 = pf_ex2(__uint_as_float(a0)), p1 = pf_ex2(__uint_as_float(a1));
+                if (tail) {
+                    p0 = col < ntok ? p0 : 0.f;
+                    p1 = col + 1 < ntok ? p1 : 0.f;
+                }
+                const uint64_t pp = ptx::f2_make(__float_as_uint(p0), __float_as_uint(p1));
+                sum2 = ptx::f2_add(sum2, pp);
+                ph[j] = pack_bf16x2(p0, p1);
+                pl[j] = ptx::f2_to_bf16x2(ptx::f2_fma(ptx::f2_from_bf16x2(ph[j]), neg1, pp));
             }
-            l_run += sum;
+            {
+                uint32_t x0, x1;
+                asm("mov.b64 {%0, %1}, %2;" : "=r"(x0), "=r"(x1) : "l"(sum2));
+                l_run += __uint_as_float(x0) + __uint_as_float(x1);
+            }
             tmem_st32(lane_base + sb, ph);
             tmem_st32(lane_base + sb + kPfTok / 2, pl);
             tmem_wait_st();
