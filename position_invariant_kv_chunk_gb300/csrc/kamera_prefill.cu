@@ -71,7 +71,9 @@ template <int D>
 struct PfLayout {
     static constexpr int NB = D / 64;                          // 64-column boxes of a head row
     static constexpr int NS = D == 128 ? 3 : 4;                 // stages
-    static constexpr uint32_t kK = 0, kV = NB * kBox, kU = 2 * NB * kBox, kU2 = kU + kBox;
+    // per stage: key boxes, U, value boxes, U' -- the value boxes and U' are one
+    // MN-major operand of D + 64 columns (64-column atoms kBox apart)
+    static constexpr uint32_t kK = 0, kU = NB * kBox, kV = kU + kBox, kU2 = kV + NB * kBox;
     static constexpr uint32_t kStage = kU2 + kBox;
     static constexpr uint32_t kVk = NS * kStage;                // V_k [d][64]
     static constexpr uint32_t kVv = kVk + D * 128;              // V_v [d][64]
@@ -147,29 +149,6 @@ __device__ __forceinline__ void tmem_st4(uint32_t ta, uint32_t a, uint32_t b, ui
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
-
-// D[tmem] (+)= A[tmem] * B[smem]^T (kind::f16, bf16 in, fp32 accumulate); A's
-// row r sits in TMEM lane r, elements 2c and 2c + 1 in the low and high half
-// of column c.
-__device__ __forceinline__ void umma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc, uint32_t idesc,
-                                        uint32_t accumulate)
-{
-    asm volatile(
-        "{\n\t.reg .pred p;\n\t"
-        "setp.ne.b32 p, %4, 0;\n\t"
-        "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
-        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
-        : "memory");
-}
-
-// B operand whose N dimension is contiguous (MN-major), 128-byte swizzle: the
-// rows of a TMA box are K (tokens), 64-element atoms along N are `lbo` bytes
-// apart, 8-row groups along K 1024 bytes apart.
-__device__ __forceinline__ uint64_t desc_mn_sw128(uint32_t saddr, uint32_t lbo)
-{
-    return (uint64_t)((saddr >> 4) & 0x3FFFu) | ((uint64_t)(lbo >> 4) << 16) | ((uint64_t)(1024 >> 4) << 32) |
-           ((uint64_t)1 << 46) | ((uint64_t)2 << 61);
-}
 
 // 16-byte piece c of row r of a 128B-swizzled tile of 128-byte rows (the TMA
 // and MMA layout): piece c ^ (r & 7).
@@ -349,58 +328,91 @@ __device__ void pf_producer(const PrefillLaunch& P, uint32_t sbase, PfBars& b, i
     __syncwarp();
 }
 
+// Shared-memory matrix descriptors as (low word, high word): the low word holds
+// the start address (bytes >> 4) and the leading byte offset, so a step inside
+// an operand is one 32-bit add.  High word: stride byte offset 1024 (8-row
+// groups), descriptor version 1, 128-byte swizzle.  A K-major operand (the key
+// and U rows) ignores the leading offset; for an MN-major one (the value and U'
+// rows: the rows of a TMA box are K, the N dimension is contiguous) it is the
+// distance between 64-element atoms along N.
+constexpr uint32_t kDescHi = (1024u >> 4) | (1u << 14) | (2u << 29);
+__device__ __forceinline__ uint64_t pf_desc(uint32_t lo)
+{
+    uint64_t d;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(d) : "r"(lo), "r"(kDescHi));
+    return d;
+}
+
+// D[tmem] (+)= A[tmem] * B[smem]^T (kind::f16: bf16 in, fp32 accumulate), the
+// accumulate flag a compile-time constant.  A's row r sits in TMEM lane r,
+// elements 2c and 2c + 1 in the low and high half of column c.
+template <bool ACC>
+__device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_t b_lo, uint32_t idesc)
+{
+    if constexpr (ACC)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "r"(a_tmem), "l"(pf_desc(b_lo)), "r"(idesc)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, 1, 1;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "r"(a_tmem), "l"(pf_desc(b_lo)), "r"(idesc)
+                     : "memory");
+}
+
 // The MMA lane.  Per tile n: S(n) = [Q'hi | Q'lo | Xhi | Xlo] [k | k | u | u]^T
 // into the S columns of n & 1, then [O_v | O_u] += [Phi | Plo] [v | u'] of tile
-// n - 1.  MMAs of one thread run in issue order, so S(n + 1), issued after the
-// P v of tile n - 1, never overwrites a P that is still to be read.
+// n - 1 as one MMA of N = d + 16 ceil(m / 16) per step.  MMAs of one thread run
+// in issue order, so S(n + 1), issued after the P v of tile n - 1, never
+// overwrites a P that is still to be read.  Everything per MMA is precomputed
+// but one add: the issue rate of this one thread bounds the tile rate.
 template <int D>
 __device__ void pf_mma(const PrefillLaunch& P, uint32_t sbase, PfBars& b, uint32_t tm, int seq)
 {
     using L = PfLayout<D>;
     const PrefillParams& p = P.p;
     constexpr uint32_t idS = ptx::idesc_bf16_f32(kPfRows, kPfTok);
-    constexpr uint32_t idV = ptx::idesc_bf16_f32(kPfRows, D) | (1u << 16);        // B (value rows) MN-major
-    constexpr uint32_t idU = ptx::idesc_bf16_f32(kPfRows, kPfMP) | (1u << 16);    // B (U' rows) MN-major
+    // descriptor low words of stage 0: K-major (LBO field 1, unused), MN-major (LBO = one box)
+    const uint32_t k_lo = ((sbase + L::kK) >> 4) | (1u << 16), u_lo = ((sbase + L::kU) >> 4) | (1u << 16);
+    const uint32_t v_lo = ((sbase + L::kV) >> 4) | ((kBox >> 4) << 16);
+    constexpr uint32_t kStep = L::kStage >> 4;
+    const uint32_t aQh = tm + L::kTmQh, aQl = tm + L::kTmQl, aXh = tm + L::kTmXh, aXl = tm + L::kTmXl;
+    const uint32_t dO = tm + L::kTmOv;
     int c0, c1;
     seq_chunks(p, seq, c0, c1);
-    // P v (and P u' when the chunk has a patch) of tile i, its stage st; `first`:
-    // the chunk's first tile (O_u starts from zero there)
-    auto pv = [&](uint32_t i, int st, int m, bool first) -> bool {
+    // P v (and P u' when the chunk has a patch) of tile i from stage st; idPV: N = d (+ the ranks)
+    auto pv = [&](uint32_t i, int st, uint32_t idPV) -> bool {
         if (!wmma16::tile_wait(ptx::smem_addr(&b.p_full[i & 1]), (i >> 1) & 1u, &b.abort, p.err, P.wait_ns))
             return false;
         ptx::tc_fence_after();
-        const uint32_t s0 = sbase + st * L::kStage, aP = tm + L::kTmS + (i & 1) * kPfTok;
+        const uint32_t aP = tm + L::kTmS + (i & 1) * kPfTok, bv = v_lo + st * kStep;
+        if (i == 0)
+            mma_ts<false>(dO, aP, bv, idPV);
+        else
+            mma_ts<true>(dO, aP, bv, idPV);
+#pragma unroll
+        for (int ks = 1; ks < kPfTok / 16; ++ks)
+            mma_ts<true>(dO, aP + 8 * ks, bv + (2048 >> 4) * ks, idPV);
 #pragma unroll
         for (int ks = 0; ks < kPfTok / 16; ++ks)
-            umma_ts(tm + L::kTmOv, aP + 8 * ks, desc_mn_sw128(s0 + L::kV + 2048 * ks, kBox), idV,
-                    (i > 0 || ks > 0) ? 1u : 0u);
-#pragma unroll
-        for (int ks = 0; ks < kPfTok / 16; ++ks)
-            umma_ts(tm + L::kTmOv, aP + kPfTok / 2 + 8 * ks, desc_mn_sw128(s0 + L::kV + 2048 * ks, kBox), idV, 1u);
-        if (m > 0) {
-#pragma unroll
-            for (int ks = 0; ks < kPfTok / 16; ++ks)
-                umma_ts(tm + L::kTmOu, aP + 8 * ks, desc_mn_sw128(s0 + L::kU2 + 2048 * ks, kBox), idU,
-                        (first && ks == 0) ? 0u : 1u);
-#pragma unroll
-            for (int ks = 0; ks < kPfTok / 16; ++ks)
-                umma_ts(tm + L::kTmOu, aP + kPfTok / 2 + 8 * ks, desc_mn_sw128(s0 + L::kU2 + 2048 * ks, kBox), idU,
-                        1u);
-        }
+            mma_ts<true>(dO, aP + kPfTok / 2 + 8 * ks, bv + (2048 >> 4) * ks, idPV);
         ptx::umma_commit(ptx::smem_addr(&b.pv_done[i & 1]));
         ptx::umma_commit(ptx::smem_addr(&b.empty[st]));
         return true;
     };
     uint32_t n = 0, k = 0;   // tiles, chunks
-    int pst = 0, pm = 0;
-    bool pfirst = false, ok = true;
+    int pst = 0;
+    uint32_t pid = 0;
+    bool ok = true;
     for (int c = c0; c < c1 && ok; ++c) {
         const KameraChunk& ch = p.chunks[c];
         if (prefill_check(ch, c, p))
             continue;
         const int m = ch.rank, nt = (ch.len + kPfTok - 1) / kPfTok, ksu = (m + 15) / 16;
+        const uint32_t idPV = ptx::idesc_bf16_f32(kPfRows, D + 16 * ksu) | (1u << 16);   // B MN-major
         for (int tl = 0; tl < nt; ++tl, ++n) {
-            if (tl == 0) {   // the chunk's Q' and X are in TMEM
+            if (tl == 0) {   // the chunk's Q' and X are in TMEM (and O_u is zero)
                 if (!wmma16::tile_wait(ptx::smem_addr(&b.a_ready), k & 1u, &b.abort, p.err, P.wait_ns)) {
                     ok = false;
                     break;
@@ -413,31 +425,32 @@ __device__ void pf_mma(const PrefillLaunch& P, uint32_t sbase, PfBars& b, uint32
                 break;
             }
             ptx::tc_fence_after();
-            const uint32_t s0 = sbase + st * L::kStage, dS = tm + L::kTmS + (n & 1) * kPfTok;
+            const uint32_t dS = tm + L::kTmS + (n & 1) * kPfTok;
+            const uint32_t bk = k_lo + st * kStep, bu = u_lo + st * kStep;
+            mma_ts<false>(dS, aQh, bk, idS);
+#pragma unroll
+            for (int ks = 1; ks < D / 16; ++ks)
+                mma_ts<true>(dS, aQh + 8 * ks, bk + (ks >> 2) * (kBox >> 4) + 2 * (ks & 3), idS);
 #pragma unroll
             for (int ks = 0; ks < D / 16; ++ks)
-                umma_ts(dS, tm + L::kTmQh + 8 * ks, ptx::desc_k_sw128(s0 + L::kK + (ks >> 2) * kBox + 32 * (ks & 3)),
-                        idS, ks > 0 ? 1u : 0u);
+                mma_ts<true>(dS, aQl + 8 * ks, bk + (ks >> 2) * (kBox >> 4) + 2 * (ks & 3), idS);
 #pragma unroll
-            for (int ks = 0; ks < D / 16; ++ks)
-                umma_ts(dS, tm + L::kTmQl + 8 * ks, ptx::desc_k_sw128(s0 + L::kK + (ks >> 2) * kBox + 32 * (ks & 3)),
-                        idS, 1u);
-            for (int ks = 0; ks < ksu; ++ks) {
-                umma_ts(dS, tm + L::kTmXh + 8 * ks, ptx::desc_k_sw128(s0 + L::kU + 32 * ks), idS, 1u);
-                umma_ts(dS, tm + L::kTmXl + 8 * ks, ptx::desc_k_sw128(s0 + L::kU + 32 * ks), idS, 1u);
-            }
+            for (int ks = 0; ks < 4; ++ks)
+                if (ks < ksu) {
+                    mma_ts<true>(dS, aXh + 8 * ks, bu + 2 * ks, idS);
+                    mma_ts<true>(dS, aXl + 8 * ks, bu + 2 * ks, idS);
+                }
             ptx::umma_commit(ptx::smem_addr(&b.s_full[n & 1]));
-            if (n > 0 && !pv(n - 1, pst, pm, pfirst)) {
+            if (n > 0 && !pv(n - 1, pst, pid)) {
                 ok = false;
                 break;
             }
             pst = st;
-            pm = m;
-            pfirst = tl == 0;
+            pid = idPV;
         }
     }
     if (ok && n > 0)
-        pv(n - 1, pst, pm, pfirst);
+        pv(n - 1, pst, pid);
     // every MMA issued here completes before TMEM is freed
     ptx::umma_commit(ptx::smem_addr(&b.drained));
     pf_drain_wait(ptx::smem_addr(&b.drained), 0u, P.wait_ns);
@@ -694,6 +707,15 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
             ptx::tc_fence_after();
             if (prev_m > 0)
                 pf_fold<D>(lane_base, vv, prev_m);
+        }
+        if (m > 0) {   // O_u starts from zero: the value MMAs of the chunk accumulate onto it
+            uint32_t z[32];
+#pragma unroll
+            for (int c = 0; c < 32; ++c)
+                z[c] = 0u;
+            tmem_st32(lane_base + L::kTmOu, z);
+            tmem_st32(lane_base + L::kTmOu + 32, z);
+            tmem_wait_st();
         }
         bar_softmax();   // the fold is done with the previous V_v
         if (m > 0)
