@@ -251,7 +251,8 @@ __device__ __forceinline__ void pf_load_u(uint32_t du, uint32_t dv, const __nv_b
 // key and value rows come by TMA (completion counted in bytes); the U rows
 // (and a partial tile's value rows) by async copies, whose landing the warp
 // waits for one tile later -- so two tiles' copies are in flight -- before it
-// makes them visible to the MMAs and arrives.
+// makes them visible to the MMAs and arrives; when the next stage is not free
+// yet, it publishes the pending tile at once instead.
 template <int D>
 __device__ void pf_producer(const PrefillLaunch& P, uint32_t sbase, PfBars& b, int seq, int h, int lane)
 {
@@ -260,7 +261,7 @@ __device__ void pf_producer(const PrefillLaunch& P, uint32_t sbase, PfBars& b, i
     int c0, c1;
     seq_chunks(p, seq, c0, c1);
     uint32_t n = 0;   // tiles started
-    bool ok = true;
+    bool ok = true, pending = false;   // pending: tile n - 1 started but not yet published
     for (int c = c0; c < c1 && ok; ++c) {
         const KameraChunk& ch = p.chunks[c];
         if (prefill_check(ch, c, p))
@@ -270,10 +271,19 @@ __device__ void pf_producer(const PrefillLaunch& P, uint32_t sbase, PfBars& b, i
         for (int tl = 0; tl < nt; ++tl, ++n) {
             const int st = (int)(n % L::NS);
             if (n >= (uint32_t)L::NS) {   // the MMAs of tile n - NS are done with the stage
+                // if the stage is not free yet, publish the previous tile first rather than
+                // hold it back while this warp waits
+                const uint32_t par = ((n / L::NS) & 1u) ^ 1u;
+                if (pending && !__shfl_sync(0xFFFFFFFFu, ptx::mbar_test_wait(ptx::smem_addr(&b.empty[st]), par) ? 1 : 0,
+                                            0)) {
+                    ptx::cp_async_wait<0>();
+                    ptx::fence_proxy_async();
+                    ptx::mbar_arrive(ptx::smem_addr(&b.full[(n - 1) % L::NS]));
+                    pending = false;
+                }
                 bool got = true;
                 if (lane == 0)
-                    got = wmma16::tile_wait(ptx::smem_addr(&b.empty[st]), ((n / L::NS) & 1u) ^ 1u, &b.abort, p.err,
-                                            P.wait_ns);
+                    got = wmma16::tile_wait(ptx::smem_addr(&b.empty[st]), par, &b.abort, p.err, P.wait_ns);
                 if (!__shfl_sync(0xFFFFFFFFu, got ? 1 : 0, 0)) {
                     ok = false;
                     break;
@@ -309,15 +319,16 @@ __device__ void pf_producer(const PrefillLaunch& P, uint32_t sbase, PfBars& b, i
                 }
             }
             ptx::cp_async_commit();
-            if (n > 0) {   // the previous tile's copies have landed: visible to the MMAs
+            if (pending) {   // the previous tile's copies have landed: visible to the MMAs
                 ptx::cp_async_wait<1>();
                 ptx::fence_proxy_async();
                 ptx::mbar_arrive(ptx::smem_addr(&b.full[(n - 1) % L::NS]));
             }
+            pending = true;
         }
     }
     ptx::cp_async_wait<0>();
-    if (n > 0) {
+    if (pending) {
         ptx::fence_proxy_async();
         ptx::mbar_arrive(ptx::smem_addr(&b.full[(n - 1) % L::NS]));
     }
