@@ -23,20 +23,25 @@
 // MMAs, about 16 significant bits); the rows and U rows are exact bf16.  The
 // A operands (Q', X, P) live in TMEM, so the MMAs read only the tile's rows
 // from shared memory; P overwrites its S columns.
+// Per chunk two more products run on the tensor cores: X = q V_k (the query
+// rows, exact bf16, from shared memory) and the fold O_v += W V_v^T of the
+// chunk's value patch, W = sum_j p_j u'_j (O_u, as hi + lo).
 // Roles (192 threads):
 //   warps 0-3  softmax: thread = query row = TMEM lane.  Per tile: the S row,
 //              running max with lazy rescaling (O is rescaled in TMEM only when
 //              the max grows by more than 2^8, so the weights stay below 256),
-//              the weights as hi + lo into TMEM.  Per chunk: Q' and X into TMEM,
-//              and at its end O_v += (sum_j p_j u'_j) V_v^T on the CUDA cores.
-//              At the end: out = O_v / l and lse = m + log l.
+//              the weights as hi + lo into TMEM.  Per chunk: V_k, V_v and the
+//              cos/sin of -delta into shared memory, Q' (CUDA cores) and X as
+//              hi + lo into TMEM, and W from O_u once the chunk's last P u' is
+//              done.  At the end: out = O_v / l and lse = m + log l.
 //   warp 4     producer: key and value rows of a tile as 128B-swizzled TMA
-//              boxes (64 columns x 64 rows), U and U' rows by 16-byte loads into
-//              the same layout (ranks padded to 64 with zeros); the value rows
-//              of a chunk's last, partial tile by loads too, zero past the chunk.
+//              boxes (64 columns x 64 rows), U and U' rows by 16-byte async
+//              copies into the same layout; the value rows of a chunk's last,
+//              partial tile by async copies too, zero past the chunk.
 //   warp 5     MMA: one lane issues S of tile n, then P v and P u' of tile
 //              n - 1 (so the softmax of tile n - 1 overlaps the scores of tile
-//              n), and commits each to an mbarrier; the warp owns TMEM.
+//              n), the per-chunk X and fold, and commits each to an mbarrier;
+//              the warp owns TMEM.
 // Every wait is bounded in time: on expiry KAMERA_DEVERR_TIMEOUT is raised, the
 // waits that follow return at once, the softmax warps run their loops to the
 // end without waiting (so their CTA-internal barriers still meet), the MMA
@@ -65,8 +70,9 @@ constexpr float kPfLazy = 8.0f;       // log2 of the growth of the running max t
 constexpr uint32_t kBox = 8192;       // one TMA box: 64 rows x 128 bytes
 
 // Shared memory from a 1024-byte aligned base: the tile ring (per stage the
-// key boxes, the value boxes, U and U'), V_k and V_v of the current chunk
-// ([d][64] bf16, ranks padded), the cos/sin of -delta, the barriers.
+// key boxes, U, the value boxes and U'), the CTA's query rows (the A operand
+// of X = q V_k), V_k of the current chunk and V_v of the last two ([d][64]
+// bf16, ranks padded, 128B-swizzled rows), the cos/sin of -delta, the barriers.
 template <int D>
 struct PfLayout {
     static constexpr int NB = D / 64;                          // 64-column boxes of a head row
@@ -75,9 +81,10 @@ struct PfLayout {
     // MN-major operand of D + 64 columns (64-column atoms kBox apart)
     static constexpr uint32_t kK = 0, kU = NB * kBox, kV = kU + kBox, kU2 = kV + NB * kBox;
     static constexpr uint32_t kStage = kU2 + kBox;
-    static constexpr uint32_t kVk = NS * kStage;                // V_k [d][64]
-    static constexpr uint32_t kVv = kVk + D * 128;              // V_v [d][64]
-    static constexpr uint32_t kCs = kVv + D * 128;              // float2 [64]
+    static constexpr uint32_t kQ = NS * kStage;                 // q [128][D], K-major, NB atoms of 16 KB
+    static constexpr uint32_t kVk = kQ + NB * 16384;            // V_k [d][64]
+    static constexpr uint32_t kVv = kVk + D * 128;              // V_v [2][d][64]
+    static constexpr uint32_t kCs = kVv + 2 * D * 128;          // float2 [64]
     static constexpr uint32_t kBar = kCs + 512;
     static constexpr uint32_t kBytes = kBar + 256 + 1024;       // + alignment slack
     // TMEM columns: S (and P) of tiles 2i and 2i + 1, O_v, O_u, Q' hi and lo, X hi and lo
@@ -91,7 +98,11 @@ struct PfBars {
     uint64_t full[4], empty[4];        // tile ring: loads landed / MMAs done with the stage
     uint64_t s_full[2], p_full[2];     // S of tile n in TMEM / P of tile n in TMEM
     uint64_t pv_done[2];               // P v and P u' of tile n done
-    uint64_t a_ready;                  // the chunk's Q' and X in TMEM
+    uint64_t vk_ready;                 // per chunk: V_k (and, first, q) in shared memory
+    uint64_t x_done;                   // per chunk: q V_k in TMEM
+    uint64_t a_ready;                  // per chunk: Q' and X (hi + lo) in TMEM
+    uint64_t w_ready;                  // per chunk after the first: the last one's sum p u' as hi + lo
+    uint64_t fold_done;                // per chunk after the first: its value patch added to O_v
     uint64_t drained;                  // every MMA of the CTA done
     uint32_t tmem;
     int32_t abort;
@@ -119,16 +130,6 @@ __device__ __forceinline__ void tmem_ld32(uint32_t ta, uint32_t (&r)[32])
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_ld8(uint32_t ta, uint32_t (&r)[8])
-{
-    asm volatile(
-        "tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];\n\t"
-        "tcgen05.wait::ld.sync.aligned;"
-        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7])
-        : "r"(ta)
-        : "memory");
-}
-
 __device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32])
 {
     asm volatile(
@@ -139,13 +140,6 @@ __device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32])
         "r"(r[18]), "r"(r[19]), "r"(r[20]), "r"(r[21]), "r"(r[22]), "r"(r[23]), "r"(r[24]), "r"(r[25]), "r"(r[26]),
         "r"(r[27]), "r"(r[28]), "r"(r[29]), "r"(r[30]), "r"(r[31])
         : "memory");
-}
-
-__device__ __forceinline__ void tmem_st4(uint32_t ta, uint32_t a, uint32_t b, uint32_t c, uint32_t d)
-{
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(ta), "r"(a), "r"(b), "r"(c),
-                 "r"(d)
-                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -372,63 +366,126 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint32_
                      : "memory");
 }
 
+// D[tmem] (+)= A[smem] * B[smem]^T (kind::f16), accumulate flag constant.
+template <bool ACC>
+__device__ __forceinline__ void mma_ss(uint32_t d_tmem, uint32_t a_lo, uint32_t b_lo, uint32_t idesc)
+{
+    if constexpr (ACC)
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.eq.u32 p, 1, 1;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(pf_desc(a_lo)), "l"(pf_desc(b_lo)), "r"(idesc)
+                     : "memory");
+    else
+        asm volatile("{\n\t.reg .pred p;\n\tsetp.ne.u32 p, 1, 1;\n\t"
+                     "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+                     "l"(pf_desc(a_lo)), "l"(pf_desc(b_lo)), "r"(idesc)
+                     : "memory");
+}
+
 // The MMA lane.  Per tile n: S(n) = [Q'hi | Q'lo | Xhi | Xlo] [k | k | u | u]^T
 // into the S columns of n & 1, then [O_v | O_u] += [Phi | Plo] [v | u'] of tile
-// n - 1 as one MMA of N = d + 16 ceil(m / 16) per step.  MMAs of one thread run
-// in issue order, so S(n + 1), issued after the P v of tile n - 1, never
-// overwrites a P that is still to be read.  Everything per MMA is precomputed
-// but one add: the issue rate of this one thread bounds the tile rate.
+// n - 1, one MMA of N = d + 16 ceil(m / 16) per step (on a chunk's first tile
+// O_u restarts from zero, so there the two parts are separate MMAs).  Per
+// chunk, before its first S: X = q V_k (q and V_k in shared memory) into the S
+// columns of that tile, for the softmax warps to split; after the previous
+// chunk's last P u': the fold O_v += W V_v^T of that chunk, W = its sum_j p_j
+// u'_j as hi + lo in the O_u columns.  MMAs of one thread run in issue order,
+// so an MMA never overwrites an operand an earlier one has still to read.
+// Everything per MMA is precomputed but one add: the issue rate of this one
+// thread bounds the tile rate.
 template <int D>
 __device__ void pf_mma(const PrefillLaunch& P, uint32_t sbase, PfBars& b, uint32_t tm, int seq)
 {
     using L = PfLayout<D>;
     const PrefillParams& p = P.p;
     constexpr uint32_t idS = ptx::idesc_bf16_f32(kPfRows, kPfTok);
+    constexpr uint32_t idV = ptx::idesc_bf16_f32(kPfRows, D) | (1u << 16);   // B (value rows) MN-major
+    constexpr uint32_t idF = ptx::idesc_bf16_f32(kPfRows, D);                // fold: B = V_v, K-major
     // descriptor low words of stage 0: K-major (LBO field 1, unused), MN-major (LBO = one box)
     const uint32_t k_lo = ((sbase + L::kK) >> 4) | (1u << 16), u_lo = ((sbase + L::kU) >> 4) | (1u << 16);
     const uint32_t v_lo = ((sbase + L::kV) >> 4) | ((kBox >> 4) << 16);
+    const uint32_t u2_lo = ((sbase + L::kU2) >> 4) | ((kBox >> 4) << 16);
+    const uint32_t q_lo = ((sbase + L::kQ) >> 4) | (1u << 16), vk_lo = ((sbase + L::kVk) >> 4) | ((kBox >> 4) << 16);
+    const uint32_t vv_lo = ((sbase + L::kVv) >> 4) | (1u << 16);
     constexpr uint32_t kStep = L::kStage >> 4;
     const uint32_t aQh = tm + L::kTmQh, aQl = tm + L::kTmQl, aXh = tm + L::kTmXh, aXl = tm + L::kTmXl;
-    const uint32_t dO = tm + L::kTmOv;
+    const uint32_t dO = tm + L::kTmOv, dU = tm + L::kTmOu;
     int c0, c1;
     seq_chunks(p, seq, c0, c1);
-    // P v (and P u' when the chunk has a patch) of tile i from stage st; idPV: N = d (+ the ranks)
-    auto pv = [&](uint32_t i, int st, uint32_t idPV) -> bool {
+    // [O_v | O_u] += P [v | u'] of tile i from stage st (m: its chunk's rank; first: its chunk's first tile)
+    auto pv = [&](uint32_t i, int st, int m, bool first) -> bool {
         if (!wmma16::tile_wait(ptx::smem_addr(&b.p_full[i & 1]), (i >> 1) & 1u, &b.abort, p.err, P.wait_ns))
             return false;
         ptx::tc_fence_after();
         const uint32_t aP = tm + L::kTmS + (i & 1) * kPfTok, bv = v_lo + st * kStep;
-        if (i == 0)
-            mma_ts<false>(dO, aP, bv, idPV);
-        else
-            mma_ts<true>(dO, aP, bv, idPV);
+        const int ksu = (m + 15) >> 4;
+        if (!first || m == 0) {
+            const uint32_t id = ptx::idesc_bf16_f32(kPfRows, D + 16 * ksu) | (1u << 16);
+            if (i == 0)
+                mma_ts<false>(dO, aP, bv, id);
+            else
+                mma_ts<true>(dO, aP, bv, id);
 #pragma unroll
-        for (int ks = 1; ks < kPfTok / 16; ++ks)
-            mma_ts<true>(dO, aP + 8 * ks, bv + (2048 >> 4) * ks, idPV);
+            for (int ks = 1; ks < kPfTok / 16; ++ks)
+                mma_ts<true>(dO, aP + 8 * ks, bv + (2048 >> 4) * ks, id);
 #pragma unroll
-        for (int ks = 0; ks < kPfTok / 16; ++ks)
-            mma_ts<true>(dO, aP + kPfTok / 2 + 8 * ks, bv + (2048 >> 4) * ks, idPV);
+            for (int ks = 0; ks < kPfTok / 16; ++ks)
+                mma_ts<true>(dO, aP + kPfTok / 2 + 8 * ks, bv + (2048 >> 4) * ks, id);
+        } else {
+            const uint32_t bu = u2_lo + st * kStep, idU = ptx::idesc_bf16_f32(kPfRows, 16 * ksu) | (1u << 16);
+            if (i == 0)
+                mma_ts<false>(dO, aP, bv, idV);
+            else
+                mma_ts<true>(dO, aP, bv, idV);
+            mma_ts<false>(dU, aP, bu, idU);
+#pragma unroll
+            for (int ks = 1; ks < kPfTok / 16; ++ks) {
+                mma_ts<true>(dO, aP + 8 * ks, bv + (2048 >> 4) * ks, idV);
+                mma_ts<true>(dU, aP + 8 * ks, bu + (2048 >> 4) * ks, idU);
+            }
+#pragma unroll
+            for (int ks = 0; ks < kPfTok / 16; ++ks) {
+                mma_ts<true>(dO, aP + kPfTok / 2 + 8 * ks, bv + (2048 >> 4) * ks, idV);
+                mma_ts<true>(dU, aP + kPfTok / 2 + 8 * ks, bu + (2048 >> 4) * ks, idU);
+            }
+        }
         ptx::umma_commit(ptx::smem_addr(&b.pv_done[i & 1]));
         ptx::umma_commit(ptx::smem_addr(&b.empty[st]));
         return true;
     };
     uint32_t n = 0, k = 0;   // tiles, chunks
-    int pst = 0;
-    uint32_t pid = 0;
-    bool ok = true;
+    int pst = 0, pm = 0, prev_chunk_m = -1;
+    bool pfirst = false, ok = true;
     for (int c = c0; c < c1 && ok; ++c) {
         const KameraChunk& ch = p.chunks[c];
         if (prefill_check(ch, c, p))
             continue;
         const int m = ch.rank, nt = (ch.len + kPfTok - 1) / kPfTok, ksu = (m + 15) / 16;
-        const uint32_t idPV = ptx::idesc_bf16_f32(kPfRows, D + 16 * ksu) | (1u << 16);   // B MN-major
+        if (nt == 0)
+            continue;
         for (int tl = 0; tl < nt; ++tl, ++n) {
-            if (tl == 0) {   // the chunk's Q' and X are in TMEM (and O_u is zero)
+            if (tl == 0) {
+                // X = q V_k into the S columns of this tile (free: their P was read by an earlier MMA)
+                if (!wmma16::tile_wait(ptx::smem_addr(&b.vk_ready), k & 1u, &b.abort, p.err, P.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                if (m > 0) {
+                    const uint32_t dX = tm + L::kTmS + (n & 1) * kPfTok;
+                    const uint32_t idX = ptx::idesc_bf16_f32(kPfRows, 16 * ksu) | (1u << 16);   // B MN-major
+                    mma_ss<false>(dX, q_lo, vk_lo, idX);
+#pragma unroll
+                    for (int ks = 1; ks < D / 16; ++ks)
+                        mma_ss<true>(dX, q_lo + (ks >> 2) * (16384 >> 4) + 2 * (ks & 3), vk_lo + (2048 >> 4) * ks,
+                                     idX);
+                }
+                ptx::umma_commit(ptx::smem_addr(&b.x_done));
+                // the chunk's Q' and X are in TMEM
                 if (!wmma16::tile_wait(ptx::smem_addr(&b.a_ready), k & 1u, &b.abort, p.err, P.wait_ns)) {
                     ok = false;
                     break;
                 }
-                ++k;
             }
             const int st = (int)(n % L::NS);
             if (!wmma16::tile_wait(ptx::smem_addr(&b.full[st]), (n / L::NS) & 1u, &b.abort, p.err, P.wait_ns)) {
@@ -452,38 +509,72 @@ __device__ void pf_mma(const PrefillLaunch& P, uint32_t sbase, PfBars& b, uint32
                     mma_ts<true>(dS, aXl + 8 * ks, bu + 2 * ks, idS);
                 }
             ptx::umma_commit(ptx::smem_addr(&b.s_full[n & 1]));
-            if (n > 0 && !pv(n - 1, pst, pid)) {
+            if (n > 0 && !pv(n - 1, pst, pm, pfirst)) {
                 ok = false;
                 break;
             }
+            if (tl == 0 && k > 0) {   // the previous chunk's value patch: O_v += W V_v^T
+                if (!wmma16::tile_wait(ptx::smem_addr(&b.w_ready), (k - 1) & 1u, &b.abort, p.err, P.wait_ns)) {
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
+                const int pk = (prev_chunk_m + 15) >> 4;
+                const uint32_t bvv = vv_lo + ((k - 1) & 1) * ((D * 128) >> 4);
+                for (int ks = 0; ks < pk; ++ks) {
+                    mma_ts<true>(dO, dU + 8 * ks, bvv + 2 * ks, idF);
+                    mma_ts<true>(dO, dU + 32 + 8 * ks, bvv + 2 * ks, idF);
+                }
+                ptx::umma_commit(ptx::smem_addr(&b.fold_done));
+            }
+            if (tl == 0)
+                ++k;
             pst = st;
-            pid = idPV;
+            pm = m;
+            pfirst = tl == 0;
+        }
+        prev_chunk_m = m;
+    }
+    if (ok && n > 0) {
+        if (pv(n - 1, pst, pm, pfirst) &&
+            wmma16::tile_wait(ptx::smem_addr(&b.w_ready), (k - 1) & 1u, &b.abort, p.err, P.wait_ns)) {
+            ptx::tc_fence_after();   // the last chunk's value patch
+            const int pk = (prev_chunk_m + 15) >> 4;
+            const uint32_t bvv = vv_lo + ((k - 1) & 1) * ((D * 128) >> 4);
+            for (int ks = 0; ks < pk; ++ks) {
+                mma_ts<true>(dO, dU + 8 * ks, bvv + 2 * ks, idF);
+                mma_ts<true>(dO, dU + 32 + 8 * ks, bvv + 2 * ks, idF);
+            }
+            ptx::umma_commit(ptx::smem_addr(&b.fold_done));
         }
     }
-    if (ok && n > 0)
-        pv(n - 1, pst, pid);
     // every MMA issued here completes before TMEM is freed
     ptx::umma_commit(ptx::smem_addr(&b.drained));
     pf_drain_wait(ptx::smem_addr(&b.drained), 0u, P.wait_ns);
 }
 
-// An m-wide V factor block [d][m] (`src`) into a [d][64] bf16 array of 128-byte
-// rows, the ranks past m up to the next multiple of 8 zero (128 threads).
+// An m-wide V factor block [d][m] (`src`) into a [d][64] bf16 tile of
+// 128B-swizzled 128-byte rows (an MMA operand: MN-major for X = q V_k, K-major
+// for the fold), the ranks past m up to the next multiple of 16 zero (128
+// threads).
 template <int D>
 __device__ __forceinline__ void pf_stage_v(uint32_t dst, const __nv_bfloat16* src, int m, int r)
 {
-    const int vpr = (m + 7) >> 3;
+    const int vpr = (m + 7) >> 3, vp16 = 2 * ((m + 15) >> 4);
     if ((m & 7) == 0) {
         const uint4* s4 = reinterpret_cast<const uint4*>(src);
         for (int e = r; e < D * vpr; e += kPfRows) {
             const uint4 v = __ldg(s4 + e);
             const int i = e / vpr, c = e - i * vpr;
-            ptx::sts128(dst + i * 128 + 16 * c, v.x, v.y, v.z, v.w);
+            ptx::sts128(dst + sw128(i, c), v.x, v.y, v.z, v.w);
         }
+        if (vp16 > vpr)
+            for (int i = r; i < D; i += kPfRows)
+                ptx::st_shared_zero16(dst + sw128(i, vpr));
     } else {
         const uint16_t* s16 = reinterpret_cast<const uint16_t*>(src);
-        for (int e = r; e < D * vpr; e += kPfRows) {
-            const int i = e / vpr, c = e - i * vpr;
+        for (int e = r; e < D * vp16; e += kPfRows) {
+            const int i = e / vp16, c = e - i * vp16;
             uint32_t w[4] = {0u, 0u, 0u, 0u};
 #pragma unroll
             for (int k = 0; k < 8; ++k) {
@@ -491,41 +582,29 @@ __device__ __forceinline__ void pf_stage_v(uint32_t dst, const __nv_bfloat16* sr
                 if (j < m)
                     w[k >> 1] |= (uint32_t)__ldg(s16 + (int64_t)i * m + j) << (16 * (k & 1));
             }
-            ptx::sts128(dst + i * 128 + 16 * c, w[0], w[1], w[2], w[3]);
+            ptx::sts128(dst + sw128(i, c), w[0], w[1], w[2], w[3]);
         }
     }
 }
 
-// O_v += O_u V_v^T for this thread's row: the value patch of the chunk just
-// finished (O_u = sum_j p_j u'_j, ranks past m zero), V_v staged at `vv`.
+// O_u (fp32, the last chunk's sum_j p_j u'_j) -> hi + lo bf16 pairs in place:
+// rank pair (2c, 2c + 1) hi in O_u column c, lo in column 32 + c -- the A
+// operand of the fold O_v += W V_v^T.
 template <int D>
-__device__ __forceinline__ void pf_fold(uint32_t lane_base, uint32_t vv, int m)
+__device__ __forceinline__ void pf_split_w(uint32_t lane_base)
 {
     using L = PfLayout<D>;
-    const int mb = (m + 7) >> 3;
-#pragma unroll 1
-    for (int cb = 0; cb < D / 32; ++cb) {
-        uint32_t o[32];
-        tmem_ld32(lane_base + L::kTmOv + 32 * cb, o);
-#pragma unroll 1
-        for (int jb = 0; jb < mb; ++jb) {
-            uint32_t w8[8];
-            tmem_ld8(lane_base + L::kTmOu + 8 * jb, w8);
+    uint32_t w0[32], w1[32], hi[32], lo[32];
+    tmem_ld32(lane_base + L::kTmOu, w0);
+    tmem_ld32(lane_base + L::kTmOu + 32, w1);
 #pragma unroll
-            for (int c = 0; c < 32; ++c) {
-                uint32_t v[4];
-                ptx::lds128(vv + (32 * cb + c) * 128 + 16 * jb, v);
-                float a = __uint_as_float(o[c]);
-#pragma unroll
-                for (int k = 0; k < 4; ++k) {
-                    a = fmaf(__uint_as_float(w8[2 * k]), bf16lo(v[k]), a);
-                    a = fmaf(__uint_as_float(w8[2 * k + 1]), bf16hi(v[k]), a);
-                }
-                o[c] = __float_as_uint(a);
-            }
-        }
-        tmem_st32(lane_base + L::kTmOv + 32 * cb, o);
+    for (int c = 0; c < 32; ++c) {
+        const uint32_t* src = c < 16 ? w0 : w1;
+        const int k = 2 * (c & 15);
+        wmma16::split_hl(__uint_as_float(src[k]), __uint_as_float(src[k + 1]), hi[c], lo[c]);
     }
+    tmem_st32(lane_base + L::kTmOu, hi);
+    tmem_st32(lane_base + L::kTmOu + 32, lo);
     tmem_wait_st();
 }
 
@@ -600,18 +679,26 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
     const __nv_bfloat16* qg = p.q + qoff;
     const uint16_t* qg16 = reinterpret_cast<const uint16_t*>(qg);
     const uint32_t lane_base = tm + ((uint32_t)(r & ~31) << 16);   // this warp's 32 TMEM lanes
-    const uint32_t vk = sbase + L::kVk, vv = sbase + L::kVv;
+    const uint32_t qs = sbase + L::kQ, vk = sbase + L::kVk, vv = sbase + L::kVv;
     float2* cs = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(&b) - L::kBar + L::kCs);
     const float sl2 = p.scale * 1.4426950408889634f;   // scores in log2 units
     const int ro = rp.rot_offset, rr = rp.rot_dim, half = rr / 2;
-    const bool rot_half = rp.pairing == KAMERA_ROPE_ROTATE_HALF;
+    const bool rot_half = rp.pairing == KAMERA_ROPE_ROTATE_HALF, full_rot = ro == 0 && rr == D;
     float m_run = -INFINITY, l_run = 0.f;
     int c0, c1;
     seq_chunks(p, seq, c0, c1);
     if (r == 0 && blk == 0 && h == 0 && (p.seq_start[seq] != c0 || p.seq_start[seq + 1] != c1))
         raise_err(p.err, KAMERA_DEVERR_DESCRIPTOR);
-    uint32_t n = 0;   // tiles
-    int prev_m = -1;  // rank of the previous chunk (-1: none yet)
+    // this thread's query row into the A operand of X = q V_k (K-major, 128B-swizzled; zero past T x G)
+#pragma unroll
+    for (int i = 0; i < D / 8; ++i) {
+        uint4 x = make_uint4(0u, 0u, 0u, 0u);
+        if (valid)
+            x = __ldg(reinterpret_cast<const uint4*>(qg) + i);
+        ptx::sts128(qs + (i >> 3) * 16384 + sw128(r, i & 7), x.x, x.y, x.z, x.w);
+    }
+    uint32_t n = 0, k = 0;   // tiles, chunks with tiles
+    int prev_m = -1;         // rank of the previous chunk (-1: none yet)
     for (int c = c0; c < c1; ++c) {
         const KameraChunk& ch = p.chunks[c];
         const int32_t bad = prefill_check(ch, c, p);
@@ -624,8 +711,8 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
         if (nt == 0)
             continue;
         const int64_t fv = (int64_t)(p.layer * p.H + h) * D * m;   // V factors [L][H][d][m]
-        // ---- the chunk's query part: Q' = R(-delta) q and X = V_k^T q
-        bar_softmax();   // every thread is done with the previous chunk's V_k and cos/sin
+        // ---- V_k and the cos/sin of -delta; X = q V_k goes to the MMA lane
+        bar_softmax();   // every thread is done with the previous chunk's cos/sin (and X(k-1) read V_k)
         for (int f = r; f < rp.n_freq; f += kPfRows) {
             float cc, sn;
             phase_cos_sin(-freq_delta(rp, ch, c, f), rp.inv_freq[f], cc, sn);
@@ -633,105 +720,106 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
         }
         if (m > 0)
             pf_stage_v<D>(vk, patch_ptr(ch, 1) + fv, m, r);
+        ptx::fence_proxy_async();   // q and V_k, visible to the MMAs
         bar_softmax();
-        uint32_t qv[D / 2];   // the query row, bf16 pairs (zero for rows past T x G), read again per chunk
+        ptx::mbar_arrive(ptx::smem_addr(&b.vk_ready));
+        // ---- Q' = R(-delta) q, hi + lo, into TMEM (the query row from shared memory)
+        {
+            uint32_t qv[D / 2];
 #pragma unroll
-        for (int i = 0; i < D / 8; ++i) {
-            uint4 x = make_uint4(0u, 0u, 0u, 0u);
-            if (valid)
-                x = __ldg(reinterpret_cast<const uint4*>(qg) + i);
-            qv[4 * i] = x.x;
-            qv[4 * i + 1] = x.y;
-            qv[4 * i + 2] = x.z;
-            qv[4 * i + 3] = x.w;
+            for (int i = 0; i < D / 8; ++i) {
+                uint32_t w[4];
+                ptx::lds128(qs + (i >> 3) * 16384 + sw128(r, i & 7), w);
+                qv[4 * i] = w[0];
+                qv[4 * i + 1] = w[1];
+                qv[4 * i + 2] = w[2];
+                qv[4 * i + 3] = w[3];
+            }
+#pragma unroll
+            for (int piece = 0; piece < D / 64; ++piece) {
+                uint32_t hi[32], lo[32];
+#pragma unroll
+                for (int cc = 0; cc < 32; ++cc) {
+                    float v2[2];
+#pragma unroll
+                    for (int e = 0; e < 2; ++e) {
+                        const int i = 64 * piece + 2 * cc + e;
+                        float v = e ? bf16hi(qv[i >> 1]) : bf16lo(qv[i >> 1]);
+                        if (full_rot) {   // the partner is a register: i ^ D/2 (rotate-half) or i ^ 1
+                            const int ph_ = i ^ (D / 2), pi_ = i ^ 1;
+                            const float pvh = (ph_ & 1) ? bf16hi(qv[ph_ >> 1]) : bf16lo(qv[ph_ >> 1]);
+                            const float pvi = (pi_ & 1) ? bf16hi(qv[pi_ >> 1]) : bf16lo(qv[pi_ >> 1]);
+                            const float2 t = rot_half ? cs[i & (D / 2 - 1)] : cs[i >> 1];
+                            const float pv = rot_half ? pvh : pvi;
+                            const bool neg = rot_half ? i < D / 2 : (i & 1) == 0;
+                            v = fmaf(v, t.x, neg ? -(pv * t.y) : pv * t.y);
+                        } else {
+                            const int kk = i - ro;
+                            if (kk >= 0 && kk < rr) {
+                                int f, pi;
+                                bool neg;
+                                if (rot_half) {
+                                    neg = kk < half;
+                                    f = neg ? kk : kk - half;
+                                    pi = neg ? i + half : i - half;
+                                } else {
+                                    neg = (kk & 1) == 0;
+                                    f = kk >> 1;
+                                    pi = neg ? i + 1 : i - 1;
+                                }
+                                const float2 t = cs[f];
+                                const float pv = valid ? __uint_as_float((uint32_t)__ldg(qg16 + pi) << 16) : 0.f;
+                                v = fmaf(v, t.x, neg ? -(pv * t.y) : pv * t.y);
+                            }
+                        }
+                        v2[e] = v;
+                    }
+                    wmma16::split_hl(v2[0], v2[1], hi[cc], lo[cc]);
+                }
+                tmem_st32(lane_base + L::kTmQh + 32 * piece, hi);
+                tmem_st32(lane_base + L::kTmQl + 32 * piece, lo);
+            }
         }
-#pragma unroll
-        for (int piece = 0; piece < D / 64; ++piece) {
-            uint32_t hi[32], lo[32];
+        // ---- X (from the MMA, in the S columns of this chunk's first tile), hi + lo
+        {
+            wmma16::tile_wait(ptx::smem_addr(&b.x_done), k & 1u, &b.abort, p.err, P.wait_ns);
+            ptx::tc_fence_after();
+            uint32_t x0[32], x1[32], xh[32], xl[32];
+            const uint32_t sx = lane_base + L::kTmS + (n & 1) * kPfTok;
+            tmem_ld32(sx, x0);
+            tmem_ld32(sx + 32, x1);
+            const int mz = m > 0 ? 16 * ((m + 15) >> 4) : 0;   // ranks the MMA wrote
 #pragma unroll
             for (int cc = 0; cc < 32; ++cc) {
-                float v2[2];
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int i = 64 * piece + 2 * cc + e;
-                    float v = e ? bf16hi(qv[i >> 1]) : bf16lo(qv[i >> 1]);
-                    const int kk = i - ro;
-                    if (kk >= 0 && kk < rr) {
-                        int f, pi;
-                        bool neg;
-                        if (rot_half) {
-                            neg = kk < half;
-                            f = neg ? kk : kk - half;
-                            pi = neg ? i + half : i - half;
-                        } else {
-                            neg = (kk & 1) == 0;
-                            f = kk >> 1;
-                            pi = neg ? i + 1 : i - 1;
-                        }
-                        const float2 t = cs[f];
-                        const float pv = valid ? __uint_as_float((uint32_t)__ldg(qg16 + pi) << 16) : 0.f;
-                        v = fmaf(v, t.x, neg ? -(pv * t.y) : pv * t.y);
-                    }
-                    v2[e] = v;
-                }
-                wmma16::split_hl(v2[0], v2[1], hi[cc], lo[cc]);
+                const uint32_t* src = cc < 16 ? x0 : x1;
+                const int kk = 2 * (cc & 15), rank = 2 * cc;
+                const float a0 = rank < mz ? __uint_as_float(src[kk]) : 0.f;
+                const float a1 = rank < mz ? __uint_as_float(src[kk + 1]) : 0.f;
+                wmma16::split_hl(a0, a1, xh[cc], xl[cc]);
             }
-            tmem_st32(lane_base + L::kTmQh + 32 * piece, hi);
-            tmem_st32(lane_base + L::kTmQl + 32 * piece, lo);
-        }
-        {
-            const int mb = (m + 7) >> 3;
-#pragma unroll 1
-            for (int jb = 0; jb < kPfMP / 8; ++jb) {
-                uint32_t xh[4] = {0u, 0u, 0u, 0u}, xl[4] = {0u, 0u, 0u, 0u};
-                if (jb < mb) {
-                    float acc[8];
-#pragma unroll
-                    for (int k = 0; k < 8; ++k)
-                        acc[k] = 0.f;
-#pragma unroll
-                    for (int i = 0; i < D; ++i) {
-                        const float qi = (i & 1) ? bf16hi(qv[i >> 1]) : bf16lo(qv[i >> 1]);
-                        uint32_t w[4];
-                        ptx::lds128(vk + i * 128 + 16 * jb, w);
-#pragma unroll
-                        for (int k = 0; k < 4; ++k) {
-                            acc[2 * k] = fmaf(qi, bf16lo(w[k]), acc[2 * k]);
-                            acc[2 * k + 1] = fmaf(qi, bf16hi(w[k]), acc[2 * k + 1]);
-                        }
-                    }
-#pragma unroll
-                    for (int k = 0; k < 4; ++k)
-                        wmma16::split_hl(acc[2 * k], acc[2 * k + 1], xh[k], xl[k]);
-                }
-                tmem_st4(lane_base + L::kTmXh + 4 * jb, xh[0], xh[1], xh[2], xh[3]);
-                tmem_st4(lane_base + L::kTmXl + 4 * jb, xl[0], xl[1], xl[2], xl[3]);
-            }
+            tmem_st32(lane_base + L::kTmXh, xh);
+            tmem_st32(lane_base + L::kTmXl, xl);
         }
         tmem_wait_st();
         ptx::tc_fence_before();
         ptx::mbar_arrive(ptx::smem_addr(&b.a_ready));
-        // ---- the previous chunk's value patch, once its last P u' is done
-        if (prev_m >= 0) {
+        // ---- V_v of this chunk, into the buffer the fold two chunks back has finished with
+        if (k >= 2)
+            wmma16::tile_wait(ptx::smem_addr(&b.fold_done), (k - 2) & 1u, &b.abort, p.err, P.wait_ns);
+        if (m > 0) {
+            pf_stage_v<D>(vv + (k & 1) * (D * 128), patch_ptr(ch, 3) + fv, m, r);
+            ptx::fence_proxy_async();
+        }
+        // ---- the previous chunk's sum_j p_j u'_j as hi + lo, for the fold, once its last P u' is done
+        if (k > 0) {
             wmma16::tile_wait(ptx::smem_addr(&b.pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1u, &b.abort, p.err,
                               P.wait_ns);
             ptx::tc_fence_after();
             if (prev_m > 0)
-                pf_fold<D>(lane_base, vv, prev_m);
+                pf_split_w<D>(lane_base);
+            ptx::tc_fence_before();
+            ptx::mbar_arrive(ptx::smem_addr(&b.w_ready));
         }
-        if (m > 0) {   // O_u starts from zero: the value MMAs of the chunk accumulate onto it
-            uint32_t z[32];
-#pragma unroll
-            for (int c = 0; c < 32; ++c)
-                z[c] = 0u;
-            tmem_st32(lane_base + L::kTmOu, z);
-            tmem_st32(lane_base + L::kTmOu + 32, z);
-            tmem_wait_st();
-        }
-        bar_softmax();   // the fold is done with the previous V_v
-        if (m > 0)
-            pf_stage_v<D>(vv, patch_ptr(ch, 3) + fv, m, r);
-        bar_softmax();
         // ---- the tiles
         for (int tl = 0; tl < nt; ++tl, ++n) {
             const int ntok = min(kPfTok, len - tl * kPfTok);
@@ -750,8 +838,11 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
                 const float f = pf_ex2(m_run - m_new);
                 l_run *= f;
                 m_run = m_new;
+                // O_v quiescent: the last P v (and, on a chunk's first tile, the previous fold)
                 wmma16::tile_wait(ptx::smem_addr(&b.pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1u, &b.abort, p.err,
                                   P.wait_ns);
+                if (tl == 0 && k > 0)
+                    wmma16::tile_wait(ptx::smem_addr(&b.fold_done), (k - 1) & 1u, &b.abort, p.err, P.wait_ns);
                 ptx::tc_fence_after();
                 pf_rescale<D>(lane_base, f, m > 0 && tl > 0);
             }
@@ -790,13 +881,18 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
             ptx::mbar_arrive(ptx::smem_addr(&b.p_full[n & 1]));
         }
         prev_m = m;
+        ++k;
     }
     // ---- the end: the last value patch, then out = O_v / l and the log-sum-exp
     if (n > 0) {
         wmma16::tile_wait(ptx::smem_addr(&b.pv_done[(n - 1) & 1]), ((n - 1) >> 1) & 1u, &b.abort, p.err, P.wait_ns);
         ptx::tc_fence_after();
         if (prev_m > 0)
-            pf_fold<D>(lane_base, vv, prev_m);
+            pf_split_w<D>(lane_base);
+        ptx::tc_fence_before();
+        ptx::mbar_arrive(ptx::smem_addr(&b.w_ready));
+        wmma16::tile_wait(ptx::smem_addr(&b.fold_done), (k - 1) & 1u, &b.abort, p.err, P.wait_ns);
+        ptx::tc_fence_after();
     }
     const float inv = n > 0 ? 1.f / l_run : 0.f;
     __nv_bfloat16* og = p.out + qoff;
@@ -853,7 +949,11 @@ __global__ void __launch_bounds__(kPfThreads, 1) prefill_kernel(const __grid_con
             ptx::mbar_init(ptx::smem_addr(&b.p_full[i]), kPfRows);
             ptx::mbar_init(ptx::smem_addr(&b.pv_done[i]), 1);
         }
+        ptx::mbar_init(ptx::smem_addr(&b.vk_ready), kPfRows);
+        ptx::mbar_init(ptx::smem_addr(&b.x_done), 1);
         ptx::mbar_init(ptx::smem_addr(&b.a_ready), kPfRows);
+        ptx::mbar_init(ptx::smem_addr(&b.w_ready), kPfRows);
+        ptx::mbar_init(ptx::smem_addr(&b.fold_done), 1);
         ptx::mbar_init(ptx::smem_addr(&b.drained), 1);
         b.abort = 0;
         ptx::fence_barrier_init();
