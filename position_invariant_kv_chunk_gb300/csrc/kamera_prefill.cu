@@ -142,11 +142,25 @@ __device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32])
         : "memory");
 }
 
+__device__ __forceinline__ void tmem_st1(uint32_t ta, uint32_t v)
+{
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(ta), "r"(v) : "memory");
+}
+
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
 // 16-byte piece c of row r of a 128B-swizzled tile of 128-byte rows (the TMA
 // and MMA layout): piece c ^ (r & 7).
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
+
+// Component i of query row r in the CTA's query tile (K-major, 128B-swizzled
+// atoms of 64 components).
+__device__ __forceinline__ float pf_q_elem(uint32_t qs, int r, int i)
+{
+    uint16_t v;
+    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(qs + (i >> 6) * 16384 + sw128(r, (i >> 3) & 7) + 2 * (i & 7)));
+    return __uint_as_float((uint32_t)v << 16);
+}
 
 __device__ __forceinline__ void bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -677,13 +691,12 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
     const int tok = valid ? row / G : 0, gq = valid ? row - (row / G) * G : 0;
     const int64_t qoff = (((int64_t)seq * p.T + tok) * HQ + (int64_t)h * G + gq) * D;
     const __nv_bfloat16* qg = p.q + qoff;
-    const uint16_t* qg16 = reinterpret_cast<const uint16_t*>(qg);
     const uint32_t lane_base = tm + ((uint32_t)(r & ~31) << 16);   // this warp's 32 TMEM lanes
     const uint32_t qs = sbase + L::kQ, vk = sbase + L::kVk, vv = sbase + L::kVv;
     float2* cs = reinterpret_cast<float2*>(reinterpret_cast<unsigned char*>(&b) - L::kBar + L::kCs);
     const float sl2 = p.scale * 1.4426950408889634f;   // scores in log2 units
     const int ro = rp.rot_offset, rr = rp.rot_dim, half = rr / 2;
-    const bool rot_half = rp.pairing == KAMERA_ROPE_ROTATE_HALF, full_rot = ro == 0 && rr == D;
+    const bool rot_half = rp.pairing == KAMERA_ROPE_ROTATE_HALF;
     float m_run = -INFINITY, l_run = 0.f;
     int c0, c1;
     seq_chunks(p, seq, c0, c1);
@@ -723,62 +736,39 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
         ptx::fence_proxy_async();   // q and V_k, visible to the MMAs
         bar_softmax();
         ptx::mbar_arrive(ptx::smem_addr(&b.vk_ready));
-        // ---- Q' = R(-delta) q, hi + lo, into TMEM (the query row from shared memory)
-        {
-            uint32_t qv[D / 2];
+        // ---- Q' = R(-delta) q, hi + lo, into TMEM: a rolled loop over component
+        // pairs (this code runs once a chunk; unrolled it would not stay in the
+        // instruction cache), each component and its partner read from the query
+        // row in shared memory
+#pragma unroll 1
+        for (int cp = 0; cp < D / 2; ++cp) {
+            float v2[2];
 #pragma unroll
-            for (int i = 0; i < D / 8; ++i) {
-                uint32_t w[4];
-                ptx::lds128(qs + (i >> 3) * 16384 + sw128(r, i & 7), w);
-                qv[4 * i] = w[0];
-                qv[4 * i + 1] = w[1];
-                qv[4 * i + 2] = w[2];
-                qv[4 * i + 3] = w[3];
-            }
-#pragma unroll
-            for (int piece = 0; piece < D / 64; ++piece) {
-                uint32_t hi[32], lo[32];
-#pragma unroll
-                for (int cc = 0; cc < 32; ++cc) {
-                    float v2[2];
-#pragma unroll
-                    for (int e = 0; e < 2; ++e) {
-                        const int i = 64 * piece + 2 * cc + e;
-                        float v = e ? bf16hi(qv[i >> 1]) : bf16lo(qv[i >> 1]);
-                        if (full_rot) {   // the partner is a register: i ^ D/2 (rotate-half) or i ^ 1
-                            const int ph_ = i ^ (D / 2), pi_ = i ^ 1;
-                            const float pvh = (ph_ & 1) ? bf16hi(qv[ph_ >> 1]) : bf16lo(qv[ph_ >> 1]);
-                            const float pvi = (pi_ & 1) ? bf16hi(qv[pi_ >> 1]) : bf16lo(qv[pi_ >> 1]);
-                            const float2 t = rot_half ? cs[i & (D / 2 - 1)] : cs[i >> 1];
-                            const float pv = rot_half ? pvh : pvi;
-                            const bool neg = rot_half ? i < D / 2 : (i & 1) == 0;
-                            v = fmaf(v, t.x, neg ? -(pv * t.y) : pv * t.y);
-                        } else {
-                            const int kk = i - ro;
-                            if (kk >= 0 && kk < rr) {
-                                int f, pi;
-                                bool neg;
-                                if (rot_half) {
-                                    neg = kk < half;
-                                    f = neg ? kk : kk - half;
-                                    pi = neg ? i + half : i - half;
-                                } else {
-                                    neg = (kk & 1) == 0;
-                                    f = kk >> 1;
-                                    pi = neg ? i + 1 : i - 1;
-                                }
-                                const float2 t = cs[f];
-                                const float pv = valid ? __uint_as_float((uint32_t)__ldg(qg16 + pi) << 16) : 0.f;
-                                v = fmaf(v, t.x, neg ? -(pv * t.y) : pv * t.y);
-                            }
-                        }
-                        v2[e] = v;
+            for (int e = 0; e < 2; ++e) {
+                const int i = 2 * cp + e, kk = i - ro;
+                float v = pf_q_elem(qs, r, i);
+                if (kk >= 0 && kk < rr) {
+                    int f, pi;
+                    bool neg;
+                    if (rot_half) {
+                        neg = kk < half;
+                        f = neg ? kk : kk - half;
+                        pi = neg ? i + half : i - half;
+                    } else {
+                        neg = (kk & 1) == 0;
+                        f = kk >> 1;
+                        pi = neg ? i + 1 : i - 1;
                     }
-                    wmma16::split_hl(v2[0], v2[1], hi[cc], lo[cc]);
+                    const float2 t = cs[f];
+                    const float pv = pf_q_elem(qs, r, pi);
+                    v = fmaf(v, t.x, neg ? -(pv * t.y) : pv * t.y);
                 }
-                tmem_st32(lane_base + L::kTmQh + 32 * piece, hi);
-                tmem_st32(lane_base + L::kTmQl + 32 * piece, lo);
+                v2[e] = v;
             }
+            uint32_t hw, lw;
+            wmma16::split_hl(v2[0], v2[1], hw, lw);
+            tmem_st1(lane_base + L::kTmQh + cp, hw);
+            tmem_st1(lane_base + L::kTmQl + cp, lw);
         }
         // ---- X (from the MMA, in the S columns of this chunk's first tile), hi + lo
         {
