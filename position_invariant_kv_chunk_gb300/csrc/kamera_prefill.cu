@@ -158,7 +158,7 @@ __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 
 __device__ __forceinline__ float pf_q_elem(uint32_t qs, int r, int i)
 {
     uint16_t v;
-    asm volatile("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(qs + (i >> 6) * 16384 + sw128(r, (i >> 3) & 7) + 2 * (i & 7)));
+    asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(qs + (i >> 6) * 16384 + sw128(r, (i >> 3) & 7) + 2 * (i & 7)) : "memory");
     return __uint_as_float((uint32_t)v << 16);
 }
 
@@ -740,7 +740,7 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
         // pairs (this code runs once a chunk; unrolled it would not stay in the
         // instruction cache), each component and its partner read from the query
         // row in shared memory
-#pragma unroll 1
+#pragma unroll 2
         for (int cp = 0; cp < D / 2; ++cp) {
             float v2[2];
 #pragma unroll
