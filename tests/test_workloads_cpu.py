@@ -82,3 +82,17 @@ def test_multi_axis_generators():
         elif kind == 3:
             assert not mv[c].any()
     assert (W.axis_moves(8, "tag") == mv).all()   # seeded
+
+
+def test_prefill_flops_and_query_shape():
+    """The prefill flop count against a hand count for a small case (query rows
+    x tokens x 4(d + m), plus 4 d m per query row and patched chunk; every chunk
+    here carries a patch), and the generated query's [S, T, H * G, d] shape."""
+    spec = W.AttendSpec("pf_count", H=2, G=3, d=64, seqs=((10, 20), (5,)), m=8, kind="prefill", T=4)
+    rows = 4 * 2 * 3                               # per sequence
+    want = 4 * (rows * 30 + rows * 5) * (64 + 8) + 4 * (rows * 2 + rows * 1) * 64 * 8
+    assert W.prefill_flops(spec) == want
+    a = W.make_attend(spec, "cpu")
+    assert tuple(a.q.shape) == (2, 4, 6, 64)
+    full = W.qwen_prefill_reused()
+    assert W.prefill_flops(full) == 1843111395328   # the figure the design notes quote
