@@ -142,9 +142,11 @@ __device__ __forceinline__ void tmem_st32(uint32_t ta, const uint32_t (&r)[32])
         : "memory");
 }
 
-__device__ __forceinline__ void tmem_st1(uint32_t ta, uint32_t v)
+__device__ __forceinline__ void tmem_st4(uint32_t ta, const uint32_t (&r)[4])
 {
-    asm volatile("tcgen05.st.sync.aligned.32x32b.x1.b32 [%0], {%1};" ::"r"(ta), "r"(v) : "memory");
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1,%2,%3,%4};" ::"r"(ta), "r"(r[0]), "r"(r[1]),
+                 "r"(r[2]), "r"(r[3])
+                 : "memory");
 }
 
 __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
@@ -152,15 +154,6 @@ __device__ __forceinline__ void tmem_wait_st() { asm volatile("tcgen05.wait::st.
 // 16-byte piece c of row r of a 128B-swizzled tile of 128-byte rows (the TMA
 // and MMA layout): piece c ^ (r & 7).
 __device__ __forceinline__ uint32_t sw128(int r, int c) { return (uint32_t)(r * 128 + ((c ^ (r & 7)) << 4)); }
-
-// Component i of query row r in the CTA's query tile (K-major, 128B-swizzled
-// atoms of 64 components).
-__device__ __forceinline__ float pf_q_elem(uint32_t qs, int r, int i)
-{
-    uint16_t v;
-    asm("ld.shared.u16 %0, [%1];" : "=h"(v) : "r"(qs + (i >> 6) * 16384 + sw128(r, (i >> 3) & 7) + 2 * (i & 7)) : "memory");
-    return __uint_as_float((uint32_t)v << 16);
-}
 
 __device__ __forceinline__ void bar_softmax() { asm volatile("bar.sync 1, 128;" ::: "memory"); }
 
@@ -736,39 +729,58 @@ __device__ void pf_softmax(const PrefillLaunch& P, uint32_t sbase, PfBars& b, ui
         ptx::fence_proxy_async();   // q and V_k, visible to the MMAs
         bar_softmax();
         ptx::mbar_arrive(ptx::smem_addr(&b.vk_ready));
-        // ---- Q' = R(-delta) q, hi + lo, into TMEM: a rolled loop over component
-        // pairs (this code runs once a chunk; unrolled it would not stay in the
-        // instruction cache), each component and its partner read from the query
-        // row in shared memory
-#pragma unroll 2
-        for (int cp = 0; cp < D / 2; ++cp) {
-            float v2[2];
+        // ---- Q' = R(-delta) q, hi + lo, into TMEM: a rolled loop over the row's
+        // 16-byte pieces (this code runs once a chunk; unrolled in full it would not
+        // stay in the instruction cache).  The rotated range starts on a piece and
+        // holds whole pieces (rot_offset a multiple of 8, rot_dim of 16 for
+        // rotate-half and of 8 for interleaved pairs: the C ABI refuses the rest),
+        // so a piece is rotated or not as a whole and its partners are one piece of
+        // the row (rotate-half, half a multiple of 8) or inside it (interleaved).
+        {
+            const float4* cs4 = reinterpret_cast<const float4*>(cs);
+#pragma unroll 1
+            for (int pc = 0; pc < D / 8; ++pc) {
+                float v[8];
+                {
+                    uint32_t w[4];
+                    ptx::lds128(qs + (pc >> 3) * 16384 + sw128(r, pc & 7), w);
 #pragma unroll
-            for (int e = 0; e < 2; ++e) {
-                const int i = 2 * cp + e, kk = i - ro;
-                float v = pf_q_elem(qs, r, i);
-                if (kk >= 0 && kk < rr) {
-                    int f, pi;
-                    bool neg;
-                    if (rot_half) {
-                        neg = kk < half;
-                        f = neg ? kk : kk - half;
-                        pi = neg ? i + half : i - half;
-                    } else {
-                        neg = (kk & 1) == 0;
-                        f = kk >> 1;
-                        pi = neg ? i + 1 : i - 1;
+                    for (int k = 0; k < 4; ++k) {
+                        v[2 * k] = bf16lo(w[k]);
+                        v[2 * k + 1] = bf16hi(w[k]);
                     }
-                    const float2 t = cs[f];
-                    const float pv = pf_q_elem(qs, r, pi);
-                    v = fmaf(v, t.x, neg ? -(pv * t.y) : pv * t.y);
                 }
-                v2[e] = v;
+                const int kk0 = 8 * pc - ro;
+                if (kk0 >= 0 && kk0 < rr) {
+                    if (rot_half) {
+                        const bool neg = kk0 < half;
+                        const int f0 = neg ? kk0 : kk0 - half, ppc = neg ? pc + half / 8 : pc - half / 8;
+                        uint32_t pw[4];
+                        ptx::lds128(qs + (ppc >> 3) * 16384 + sw128(r, ppc & 7), pw);
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {
+                            const float4 t = cs4[(f0 >> 1) + k];   // cos/sin of f0 + 2k and f0 + 2k + 1
+                            const float p0 = bf16lo(pw[k]), p1 = bf16hi(pw[k]);
+                            v[2 * k] = fmaf(v[2 * k], t.x, neg ? -(p0 * t.y) : p0 * t.y);
+                            v[2 * k + 1] = fmaf(v[2 * k + 1], t.z, neg ? -(p1 * t.w) : p1 * t.w);
+                        }
+                    } else {
+#pragma unroll
+                        for (int k = 0; k < 4; ++k) {   // pair (2k, 2k + 1): frequency kk0 / 2 + k
+                            const float2 t = cs[(kk0 >> 1) + k];
+                            const float a = v[2 * k], bb = v[2 * k + 1];
+                            v[2 * k] = fmaf(a, t.x, -(bb * t.y));
+                            v[2 * k + 1] = fmaf(bb, t.x, a * t.y);
+                        }
+                    }
+                }
+                uint32_t hw[4], lw[4];
+#pragma unroll
+                for (int k = 0; k < 4; ++k)
+                    wmma16::split_hl(v[2 * k], v[2 * k + 1], hw[k], lw[k]);
+                tmem_st4(lane_base + L::kTmQh + 4 * pc, hw);
+                tmem_st4(lane_base + L::kTmQl + 4 * pc, lw);
             }
-            uint32_t hw, lw;
-            wmma16::split_hl(v2[0], v2[1], hw, lw);
-            tmem_st1(lane_base + L::kTmQh + cp, hw);
-            tmem_st1(lane_base + L::kTmQl + cp, lw);
         }
         // ---- X (from the MMA, in the S columns of this chunk's first tile), hi + lo
         {

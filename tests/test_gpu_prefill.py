@@ -99,6 +99,12 @@ CASES = {
     "rank0_only": spec("pf_r0", 16, H=1, G=8, d=64, seqs=((129,), (1, 2, 3)), m=0),
     "rank64": spec("pf_m64", 50, H=2, G=3, d=128, seqs=((150,),), m=64),
     "rank12_d64": spec("pf_m12", 40, H=2, G=5, d=64, seqs=((70, 200),), m=12),
+    # partial rotary ranges: rotate-half with a half of three 16-byte pieces, interleaved pairs over
+    # five pieces, both starting past the first piece
+    "rope_half_48_at_8": spec("pf_r48", 30, H=2, G=2, d=64, seqs=((90, 40),), m=8, base=1e4, rot_dim=48,
+                              rot_offset=8),
+    "rope_interleaved_40_at_8": spec("pf_i40", 30, H=1, G=4, d=128, seqs=((100,),), m=16, base=1e4, rot_dim=40,
+                                     rot_offset=8, pairing=K.INTERLEAVED),
     # two 1296-token chunks: 41 tiles, several laps of the tile ring, lazy rescales
     "long_chunks": spec("pf_long", 64, H=1, G=4, d=128, seqs=((1296, 1296),), m=32),
     "one_token": spec("pf_t1", 1, H=2, G=2, d=128, seqs=((100,), (5,)), m=16),
