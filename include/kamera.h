@@ -415,8 +415,9 @@ typedef struct KameraDeficit {
  *   v      bf16 [n_outer*n_inner][cols][m] (written; the Vk/Vv or Vr layout)
  *   sigma  fp32 [n_outer*n_inner][m] singular values (written), or NULL
  * Supported: cols % 8 == 0 and 8 <= cols <= 128 with 1 <= m <= cols (head_dim
- * up to 128, MLA k_rope), or 128 < cols <= 512 with 1 <= m <= 32 (the MLA
- * c_KV block); rows >= 1, n_outer*n_inner < 2^31.  Blocks wider than 128
+ * up to 128, MLA k_rope), or 128 < cols <= 576 with 1 <= m <= 32 (the MLA
+ * c_KV block, or the whole 576-wide latent row c_KV | k_rope as one joint
+ * block); rows >= 1, n_outer*n_inner < 2^31.  Blocks wider than 128
  * columns take subspace iteration on X^T X (three products of a basis of
  * k = min(48, m + 16 rounded up to 16) columns) and a Rayleigh-Ritz step:
  * exact to fp32 rounding when sigma_{k+1} is well below sigma_m (a deficit

@@ -902,8 +902,8 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_kernel(const __grid_
 }
 
 // ------------------------------------------------------------ wide blocks --
-// Blocks wider than one SM can hold G for (128 < cols <= 512: the MLA c_KV
-// block) take subspace iteration with a Rayleigh-Ritz step (Golub & Van Loan,
+// Blocks wider than one SM can hold G for (128 < cols <= 576: the MLA c_KV
+// block, or the whole 576-wide latent row as one joint block) take subspace iteration with a Rayleigh-Ritz step (Golub & Van Loan,
 // section 8.2.4, orthogonal iteration; the Ritz step of section 8.1): a basis
 // Z of k = m + 16 (rounded to 16, at most 48) columns is multiplied by
 // G = X^T X kWideIters times, each product streamed over the rows of X as
@@ -915,7 +915,7 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_kernel(const __grid_
 // the partial Rayleigh-Ritz sums are added over the cluster through
 // distributed shared memory in rank order, so every CTA holds the same basis;
 // rank 0 writes V and sigma, every CTA its rows of U.
-constexpr int kWideMaxCols = 512;
+constexpr int kWideMaxCols = 576;   // rows of Z: one or two per thread
 constexpr int kWideMaxRank = 32;
 constexpr int kWideIters = 3;
 constexpr int kWideT = 32;   // rows of X per staged tile
@@ -941,21 +941,23 @@ __host__ __device__ inline PfWideLayout pf_wide_layout(int c, int m)
     return L;
 }
 
-// Column-wise classical Gram-Schmidt, twice, on Z [c][zs] (one row per thread),
+// Column-wise classical Gram-Schmidt, twice, on Z [c][zs] (one row per thread;
+// rows t and t + 512 when c is above 512),
 // every column normalised; coefficients reduced by shuffles and shared atomics
 // into coef[0 .. k-1], the squared norm into coef[kWideNormSlot].
 constexpr int kWideNormSlot = 63;
-__device__ void wide_cgs2(float* z, int zs, int c, int k, float* coef)
+template <bool TWO>
+__device__ void wide_cgs2_rows(float* z, int zs, int c, int k, float* coef)
 {
-    const int lane = threadIdx.x & 31, t = threadIdx.x;
+    const int lane = threadIdx.x & 31, t = threadIdx.x, t2 = TWO ? t + kPfThreads : c;   // rows t and t + 512
     for (int j = 0; j < k; ++j) {
         for (int pass = 0; pass < 2 && j > 0; ++pass) {
             for (int i = t; i < j; i += kPfThreads)
                 coef[i] = 0.f;
             __syncthreads();
-            const float zj = t < c ? z[t * zs + j] : 0.f;
+            const float zj = t < c ? z[t * zs + j] : 0.f, zj2 = t2 < c ? z[t2 * zs + j] : 0.f;
             for (int i = 0; i < j; ++i) {
-                float part = t < c ? z[t * zs + i] * zj : 0.f;
+                float part = (t < c ? z[t * zs + i] * zj : 0.f) + (t2 < c ? z[t2 * zs + i] * zj2 : 0.f);
                 part = warp_sum(part);
                 if (lane == 0)
                     atomicAdd(&coef[i], part);
@@ -967,22 +969,31 @@ __device__ void wide_cgs2(float* z, int zs, int c, int k, float* coef)
                     acc = fmaf(-coef[i], z[t * zs + i], acc);
                 z[t * zs + j] = acc;
             }
+            if (t2 < c) {
+                float acc = zj2;
+                for (int i = 0; i < j; ++i)
+                    acc = fmaf(-coef[i], z[t2 * zs + i], acc);
+                z[t2 * zs + j] = acc;
+            }
             __syncthreads();
         }
         if (t == 0)
             coef[kWideNormSlot] = 0.f;
         __syncthreads();
-        const float v = t < c ? z[t * zs + j] : 0.f;
-        const float part = warp_sum(v * v);
+        const float v = t < c ? z[t * zs + j] : 0.f, v2 = t2 < c ? z[t2 * zs + j] : 0.f;
+        const float part = warp_sum(v * v + v2 * v2);
         if (lane == 0)
             atomicAdd(&coef[kWideNormSlot], part);
         __syncthreads();
         const float sc = rsqrtf(fmaxf(coef[kWideNormSlot], 1e-30f));
         if (t < c)
             z[t * zs + j] = v * sc;
+        if (t2 < c)
+            z[t2 * zs + j] = v2 * sc;
         __syncthreads();
     }
 }
+
 
 // Stage rows r0 .. r0 + kWideT - 1 of X (the mean of its terms) as fp32
 // [T][c + 4], zero from row r_end on.
@@ -1054,6 +1065,52 @@ __device__ void wide_xb(const float* xt, int c, const float* b, int bs, int ncol
                     out[(t0 + a) * os + j0 + u] = acc[a][u];
 }
 
+// Z <- X^T (X Z) for this CTA's rows of X when Z has more rows than 128 groups
+// of four: three column groups, the thread holds rows 4 ig .. 4 ig + 3 of Z and
+// columns jg kq .. jg kq + kq - 1 (kq <= 16) in registers.
+template <typename TileR0>
+__device__ __noinline__ void wide_product3(const PatchFormParams& p, const __nv_bfloat16* x, float* xt, float* yt,
+                                             float* z, int zs, int c, int k, int kq, int ig, int jg, bool own,
+                                             int n_tiles, int row_hi, const TileR0& tile_r0)
+{
+    constexpr int KQ = 16;
+    float acc[4][KQ] = {};
+    for (int q = 0; q < n_tiles; ++q) {
+        const int r0 = tile_r0(q);
+        wide_stage(p, x, r0, row_hi, xt);
+        __syncthreads();
+        wide_xb(xt, c, z, zs, k, yt, k);
+        __syncthreads();
+        if (own) {
+            for (int tt = 0; tt < kWideT; ++tt) {
+                const float4 xv = *reinterpret_cast<const float4*>(xt + tt * (c + 4) + 4 * ig);
+                const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+                for (int u = 0; u < KQ; ++u) {
+                    if (u < kq && jg * kq + u < k) {
+                        const float yv = yt[tt * k + jg * kq + u];
+#pragma unroll
+                        for (int a = 0; a < 4; ++a)
+                            acc[a][u] = fmaf(xa[a], yv, acc[a][u]);
+                    }
+                }
+            }
+        }
+        __syncthreads();
+    }
+    if (own)
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+            for (int u = 0; u < KQ; ++u)
+                if (u < kq && jg * kq + u < k)
+                    z[(4 * ig + a) * zs + jg * kq + u] = acc[a][u];
+}
+
+// TWO: the block is wider than 512 columns, so Z has more rows than the CTA has
+// threads (two rows a thread in the per-row steps, three column groups in the
+// product).
+template <bool TWO>
 __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __grid_constant__ PatchFormParams p)
 {
     extern __shared__ __align__(16) unsigned char smem[];
@@ -1095,11 +1152,14 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
         z[i * zs + j] = start_entry(i, j);
     }
     __syncthreads();
-    wide_cgs2(z, zs, c, k, s_coef);
+    wide_cgs2_rows<TWO>(z, zs, c, k, s_coef);
 
     // Z <- orth(X^T (X Z)), kWideIters times; the product accumulates in
-    // registers: thread -> rows 4 ig .. 4 ig + 3, columns jg * kq .. + kq
-    const int kq = k / 4, ig = t >> 2, jg = t & 3;
+    // registers: thread -> rows 4 ig .. 4 ig + 3, columns jg * kq .. + kq, with
+    // ncg column groups (4; 3 when the rows of Z outnumber 512 / 4 groups)
+    constexpr int ncg = TWO ? 3 : 4;
+    const int kq = (k + ncg - 1) / ncg, ig = t / ncg, jg = t - (t / ncg) * ncg;
+    const bool own = 4 * ig < c && jg < ncg;
     // The five passes over the rows alternate direction: each pass starts on the
     // rows the one before it read last, which are still in L2 (the 27 blocks of a
     // DeepSeek-V2-Lite chunk stream about as many bytes per pass as L2 holds, so
@@ -1108,60 +1168,68 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
     int pass = 0;
     auto tile_r0 = [&](int q) { return row_lo + ((pass & 1) ? n_tiles - 1 - q : q) * kWideT; };
     for (int it = 0; it < kWideIters; ++it, ++pass) {
-        float acc[4][12] = {};
-        for (int q = 0; q < n_tiles; ++q) {
-            const int r0 = tile_r0(q);
-            wide_stage(p, x, r0, row_hi, xt);
-            __syncthreads();
-            wide_xb(xt, c, z, zs, k, yt, k);
-            __syncthreads();
-            if (4 * ig < c) {
-                for (int tt = 0; tt < kWideT; ++tt) {
-                    const float4 xv = *reinterpret_cast<const float4*>(xt + tt * (c + 4) + 4 * ig);
-                    const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
+        if constexpr (!TWO) {
+            float acc[4][12] = {};
+            for (int q = 0; q < n_tiles; ++q) {
+                const int r0 = tile_r0(q);
+                wide_stage(p, x, r0, row_hi, xt);
+                __syncthreads();
+                wide_xb(xt, c, z, zs, k, yt, k);
+                __syncthreads();
+                if (4 * ig < c) {
+                    for (int tt = 0; tt < kWideT; ++tt) {
+                        const float4 xv = *reinterpret_cast<const float4*>(xt + tt * (c + 4) + 4 * ig);
+                        const float xa[4] = {xv.x, xv.y, xv.z, xv.w};
 #pragma unroll
-                    for (int u = 0; u < 12; ++u) {
-                        if (u < kq) {
-                            const float yv = yt[tt * k + jg * kq + u];
+                        for (int u = 0; u < 12; ++u) {
+                            if (u < kq) {
+                                const float yv = yt[tt * k + jg * kq + u];
 #pragma unroll
-                            for (int a = 0; a < 4; ++a)
-                                acc[a][u] = fmaf(xa[a], yv, acc[a][u]);
+                                for (int a = 0; a < 4; ++a)
+                                    acc[a][u] = fmaf(xa[a], yv, acc[a][u]);
+                            }
                         }
                     }
                 }
+                __syncthreads();
             }
-            __syncthreads();
+            if (4 * ig < c)
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int u = 0; u < 12; ++u)
+                        if (u < kq)
+                            z[(4 * ig + a) * zs + jg * kq + u] = acc[a][u];
+        } else {
+            wide_product3(p, x, xt, yt, z, zs, c, k, kq, ig, jg, own, n_tiles, row_hi, tile_r0);
         }
-        if (4 * ig < c)
-#pragma unroll
-            for (int a = 0; a < 4; ++a)
-#pragma unroll
-                for (int u = 0; u < 12; ++u)
-                    if (u < kq)
-                        z[(4 * ig + a) * zs + jg * kq + u] = acc[a][u];
         if (CL > 1) {   // add the cluster's partial products, in rank order (the same sum in every CTA)
             cluster.sync();
             float sum[48];
+            constexpr int slots = TWO ? 2 : 1;   // rows t, t + 512: the same count in every thread
+            for (int sl = 0; sl < slots; ++sl) {
+                const int row = t + sl * kPfThreads;
 #pragma unroll
-            for (int j = 0; j < 48; ++j)
-                sum[j] = 0.f;
-            if (t < c)
-                for (int q = 0; q < CL; ++q) {
-                    const float* zq = cluster.map_shared_rank(z, q) + t * zs;
+                for (int j = 0; j < 48; ++j)
+                    sum[j] = 0.f;
+                if (row < c)
+                    for (int q = 0; q < CL; ++q) {
+                        const float* zq = cluster.map_shared_rank(z, q) + row * zs;
+#pragma unroll
+                        for (int j = 0; j < 48; ++j)
+                            if (j < k)
+                                sum[j] += zq[j];
+                    }
+                cluster.sync();   // every CTA has read every partial of this row slot
+                if (row < c)
 #pragma unroll
                     for (int j = 0; j < 48; ++j)
                         if (j < k)
-                            sum[j] += zq[j];
-                }
-            cluster.sync();   // every CTA has read every partial
-            if (t < c)
-#pragma unroll
-                for (int j = 0; j < 48; ++j)
-                    if (j < k)
-                        z[t * zs + j] = sum[j];
+                            z[row * zs + j] = sum[j];
+            }
         }
         __syncthreads();
-        wide_cgs2(z, zs, c, k, s_coef);
+        wide_cgs2_rows<TWO>(z, zs, c, k, s_coef);
     }
 
     // Rayleigh-Ritz: C = (X Z)^T (X Z), accumulated per thread over its (a, b) entries
@@ -1245,20 +1313,20 @@ __global__ void __launch_bounds__(kPfThreads, 1) patch_form_wide_kernel(const __
     // V = Z W (row t of Z -> row t of V, in place), bf16 out (every CTA of the
     // cluster forms V for its U rows; rank 0 writes it)
     __nv_bfloat16* vo = p.v + blk * (int64_t)c * m;
-    if (t < c) {
+    for (int row = t; row < c; row += kPfThreads) {
         float zr[48];
 #pragma unroll
         for (int j = 0; j < 48; ++j)
-            zr[j] = j < k ? z[t * zs + j] : 0.f;
+            zr[j] = j < k ? z[row * zs + j] : 0.f;
         for (int r = 0; r < m; ++r) {
             float acc = 0.f;
 #pragma unroll
             for (int j = 0; j < 48; ++j)
                 if (j < k)
                     acc = fmaf(zr[j], s.y[j * ys + r], acc);
-            z[t * zs + r] = acc;
+            z[row * zs + r] = acc;
             if (crank == 0)
-                vo[(int64_t)t * m + r] = __float2bfloat16_rn(acc);
+                vo[(int64_t)row * m + r] = __float2bfloat16_rn(acc);
         }
     }
     __syncthreads();
@@ -1293,8 +1361,8 @@ cudaError_t launch_patch_form(const PatchFormParams& p, int64_t n_blocks, cudaSt
 {
     if (p.cols > kPfMaxCols) {
         const int bytes = pf_wide_layout(p.cols, p.m).end;
-        cudaError_t e = cudaFuncSetAttribute(patch_form_wide_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             bytes);
+        const auto kernel = p.cols > kPfThreads ? patch_form_wide_kernel<true> : patch_form_wide_kernel<false>;
+        cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
         if (e != cudaSuccess)
             return e;
         // Cluster size: the blocks' rows are split over CL CTAs; each size 1..8
@@ -1304,7 +1372,7 @@ cudaError_t launch_patch_form(const PatchFormParams& p, int64_t n_blocks, cudaSt
         q.cluster = 1;
         double best = 1e300;
         for (int cl = 1; cl <= 8; ++cl) {
-            const int fit = cluster_fit(reinterpret_cast<const void*>(patch_form_wide_kernel), kPfThreads, bytes, cl);
+            const int fit = cluster_fit(reinterpret_cast<const void*>(kernel), kPfThreads, bytes, cl);
             if (fit < 1 || (int64_t)n_blocks * cl > 0x7FFFFFFFll)
                 continue;
             const double cost = (double)((n_blocks + fit - 1) / fit) / cl;
@@ -1325,7 +1393,7 @@ cudaError_t launch_patch_form(const PatchFormParams& p, int64_t n_blocks, cudaSt
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        return cudaLaunchKernelEx(&cfg, patch_form_wide_kernel, q);
+        return cudaLaunchKernelEx(&cfg, kernel, q);
     }
     const int bytes = pf_smem_bytes(p.cols, p.m);
     cudaError_t e = cudaFuncSetAttribute(patch_form_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);

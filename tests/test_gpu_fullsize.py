@@ -155,11 +155,13 @@ def test_patch_form_fullsize_every_block():
             check_factors(xh[o, i], uh[o, i], vh[o, i], sh[o, i], spec.m, f"block ({o},{i})")
 
 
-def test_wide_patch_form_fullsize_every_block():
-    """dsv2_patch_form as bench.py times it (27 blocks of 4096 x 512, rank 16: the
+@pytest.mark.parametrize("name", ["dsv2_patch_form", "dsv2_joint_patch_form"])
+def test_wide_patch_form_fullsize_every_block(name):
+    """dsv2_patch_form and dsv2_joint_patch_form as bench.py times them (27
+    blocks of 4096 x 512, or x 576 for the joint latent-row factor, rank 16: the
     wide path, one call): every block against the oracle's truncated SVD."""
     from tests.test_gpu_patchform import check_factors
-    spec = W.dsv2_patch_form()
+    spec = W.FORMATION[name]()
     x = W.make_deficit(spec, DEV)
     xb = x.reshape(spec.kv * spec.L, spec.length, spec.H, spec.d).permute(0, 2, 1, 3)
     sig = torch.empty(spec.kv * spec.L, spec.H, spec.m, dtype=torch.float32, device=DEV)

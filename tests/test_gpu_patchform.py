@@ -179,11 +179,13 @@ def test_factors_feed_relocation():
 
 
 @pytest.mark.parametrize("length,d,m", [(300, 512, 16), (4096, 512, 16), (300, 512, 32), (129, 136, 16),
-                                        (77, 256, 8)])
+                                        (77, 256, 8), (4096, 576, 16), (300, 576, 32), (1000, 520, 8)])
 def test_wide_blocks(length, d, m):
-    """Blocks wider than 128 columns (the 512-wide MLA c_KV block): subspace
-    iteration + Rayleigh-Ritz, held to the same bounds on the planted deficits,
-    whose spectrum falls off past the planted directions."""
+    """Blocks wider than 128 columns (the 512-wide MLA c_KV block, and the
+    whole 576-wide latent row c_KV | k_rope as one joint block, whose basis has
+    more rows than the CTA has threads): subspace iteration + Rayleigh-Ritz,
+    held to the same bounds on the planted deficits, whose spectrum falls off
+    past the planted directions."""
     run_and_check(W.DeficitSpec("pf_wide", L=2, length=length, H=1, d=d, m=m, kv=1))
 
 
@@ -215,6 +217,11 @@ def test_wide_flat_spectrum_is_near_optimal():
                                s_min=0.0, noise=1.0), 16)
 
 
+def test_wide_joint_latent_row_is_near_optimal():
+    near_optimal(W.DeficitSpec("pf_flat576", L=1, length=400, H=1, d=576, m=16, kv=1, planted=1, s_max=0.0,
+                               s_min=0.0, noise=1.0), 16)
+
+
 def test_wide_orbit_patch_is_near_optimal():
     """The mean of three independently planted deficits spreads its energy over
     ~96 directions (no gap after sigma_16): the near-optimality bound."""
@@ -222,7 +229,7 @@ def test_wide_orbit_patch_is_near_optimal():
 
 
 def test_host_errors():
-    x = torch.zeros(1, 1, 16, 520, dtype=torch.bfloat16, device=DEV)
+    x = torch.zeros(1, 1, 16, 584, dtype=torch.bfloat16, device=DEV)   # wider than the 576-wide latent row
     with pytest.raises(K.KameraError) as e:
         K.kamera_form_patch(x, 8)
     assert e.value.status == 3

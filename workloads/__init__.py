@@ -344,7 +344,14 @@ def dsv2_patch_form() -> DeficitSpec:
     return DeficitSpec("dsv2_patch_form", L=27, length=4096, H=1, d=512, m=16, kv=1)
 
 
-FORMATION = {"qwen_patch_form": qwen_patch_form, "dsv2_patch_form": dsv2_patch_form}
+def dsv2_joint_patch_form() -> DeficitSpec:
+    """Rank-16 patch formation for the same chunk with one joint factor over the
+    whole 576-wide latent row (c_KV 512 | k_rope 64): 27 blocks of 4096 x 576."""
+    return DeficitSpec("dsv2_joint_patch_form", L=27, length=4096, H=1, d=576, m=16, kv=1)
+
+
+FORMATION = {"qwen_patch_form": qwen_patch_form, "dsv2_patch_form": dsv2_patch_form,
+             "dsv2_joint_patch_form": dsv2_joint_patch_form}
 
 
 # ------------------------------------------------------ attention inputs --
