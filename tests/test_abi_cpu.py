@@ -160,7 +160,7 @@ def test_form_patch_argument_errors():
             K.kamera_form_patch(x, m, stream=0)
         assert e.value.status == status
     with pytest.raises(K.KameraError) as e:
-        K.kamera_form_patch(torch.zeros(1, 1, 16, 520, dtype=torch.bfloat16), 8, stream=0)   # wider than 512
+        K.kamera_form_patch(torch.zeros(1, 1, 16, 584, dtype=torch.bfloat16), 8, stream=0)   # wider than 576
     assert e.value.status == 3
     with pytest.raises(K.KameraError) as e:
         K.kamera_form_patch(torch.zeros(1, 1, 16, 512, dtype=torch.bfloat16), 33, stream=0)  # wide: rank <= 32
