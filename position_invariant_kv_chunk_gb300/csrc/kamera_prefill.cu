@@ -1001,14 +1001,11 @@ cudaError_t launch_prefill_d(const PrefillParams& p, cudaStream_t stream)
     if (!make_rows_map(&P.map_k, p.k, p.num_rows, width, p.row_stride, 64, kPfTok) ||
         !make_rows_map(&P.map_v, p.v, p.num_rows, width, p.row_stride, 64, kPfTok))
         return cudaErrorInvalidValue;
-    static bool attr_done = false;   // per process: the attribute is per function, not per device
-    if (!attr_done) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
-        if (e != cudaSuccess)
-            return e;
-        attr_done = true;
-    }
+    // set at every launch: the attribute belongs to the current device's context
+    const cudaError_t e =
+        cudaFuncSetAttribute(prefill_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)L::kBytes);
+    if (e != cudaSuccess)
+        return e;
     const int64_t units = (int64_t)p.n_seqs * p.H * p.blocks;
     prefill_kernel<D><<<(unsigned)units, kPfThreads, L::kBytes, stream>>>(P);
     return cudaGetLastError();
