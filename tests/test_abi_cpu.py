@@ -271,6 +271,36 @@ def test_attend_store_row_bound():
     del keep
 
 
+def test_prefill_argument_errors():
+    """Prefill attention's argument checks return before any pointer is used:
+    an unsupported head_dim or rank, a store too tall for 32-bit tile rows, a
+    negative count, an lse that is not 4-byte aligned, out overlapping q."""
+    lib = K.load_library()
+    fake = 1 << 20   # never dereferenced: every call returns first
+    r, keep = K.Rope(1e4, 64)._c(1)
+
+    def call(kv, q, max_rank=8):
+        return lib.kamera_prefill_attend_reused(C.byref(kv), C.byref(q), C.byref(r), C.c_void_p(fake),
+                                                C.c_void_p(fake), 1, 8, max_rank, None, None)
+
+    kv = K._AttnKV(fake, fake + (1 << 24), 1024, 128, 2, 64, 0, 0)
+    q = K._PrefillQuery(fake + (2 << 24), fake + (3 << 24), fake + (4 << 24), 1, 5, 4, 0.125)
+    assert call(kv, q, max_rank=65) == 3                         # ranks up to 64
+    kv96 = K._AttnKV(fake, fake + (1 << 24), 1024, 192, 2, 96, 0, 0)
+    assert call(kv96, q) == 3                                    # head_dim 64 or 128
+    tall = K._AttnKV(fake, fake + (1 << 24), 1 << 31, 128, 2, 64, 0, 0)
+    assert call(tall, q) == 3                                    # rows addressed by 32-bit coordinates
+    neg = K._PrefillQuery(fake + (2 << 24), fake + (3 << 24), 0, 1, -1, 4, 0.125)
+    assert call(kv, neg) == 1
+    odd = K._PrefillQuery(fake + (2 << 24), fake + (3 << 24), fake + (4 << 24) + 2, 1, 5, 4, 0.125)
+    assert call(kv, odd) == 2                                    # lse 4-byte aligned
+    alias = K._PrefillQuery(fake + (2 << 24), fake + (2 << 24), 0, 1, 5, 4, 0.125)
+    assert call(kv, alias) == 1                                  # out overlapping q
+    empty = K._PrefillQuery(fake + (2 << 24), fake + (3 << 24), 0, 1, 0, 4, 0.125)
+    assert call(kv, empty) == 0                                  # no query token: nothing to do
+    del keep
+
+
 def test_compute_calls_take_cuda_tensors_only(monkeypatch):
     """Where CUDA is present, every tensor a compute entry point reads or writes
     must be a CUDA tensor (a host address is not a device address); the binding
@@ -290,6 +320,8 @@ def test_compute_calls_take_cuda_tensors_only(monkeypatch):
         lambda: K.kamera_mla_attend_reused(torch.zeros(8, 576, dtype=torch.bfloat16), 512,
                                            torch.zeros(1, 16, 576, dtype=torch.bfloat16), K.Rope(1e4, 64), ch,
                                            torch.zeros(2, dtype=torch.int32), 1, 8, 0, stream=0),
+        lambda: K.kamera_prefill_attend_reused(sk[0], sk[0].clone(), torch.zeros(1, 3, 2, 64, dtype=torch.bfloat16),
+                                               rope, ch, torch.zeros(2, dtype=torch.int32), 1, 8, 0, stream=0),
     ]
     for call in calls:
         with pytest.raises(ValueError, match="CUDA tensor"):
